@@ -1,0 +1,151 @@
+/*
+ * exl3.h - C ABI of libexl3: fused randomized-Hadamard + bitshift-trellis
+ * decode + GEMV / skinny GEMM for GB300 (sm_103a).
+ *
+ * What is computed (source pages):
+ *   - "Trellis Quantization" (Lecture 1b), Part eight: every 16x16 weight tile
+ *     is one 256-step tail-biting bitshift trellis; the state of step t is the
+ *     16-bit window starting at bit K*t of the tile's circular 256*K-bit stream.
+ *   - same lecture, Part nine: the lookup-free computed codes 3INST and 1MAD
+ *     turn a state into a binary16 weight.
+ *   - "ExLlamaV3 & EXL3 Deep Dive", Section 2: the randomized Hadamard transform
+ *     applied to x on the way in and to the product on the way out, so that
+ *     y = Hb(s_out (.) (scale (.) (W-hat Hb(s_in (.) x)))); Lecture 1b Part
+ *     eleven: Hb is blockwise over 128-element blocks, H_128 Sylvester-ordered
+ *     and normalized by 1/sqrt(128).
+ *   - "EXL3 field guide": per-output-channel binary16 scales.
+ *
+ * Data formats (all little-endian device memory):
+ *   codes   uint32 words; tile (I, J) (rows 16I..16I+15, columns 16J..16J+15)
+ *           occupies words [(I*(n/16) + J) * 8K, +8K).  Stream bit j of a tile
+ *           is bit 31 - (j % 32) of its word j / 32 (MSB first).  Step t of a
+ *           tile is element (16I + t/16, 16J + t%16).
+ *   half    IEEE-754 binary16 bit patterns (exl3_half).
+ *   x       [M][n] row-major halves; y [M][m] row-major halves.
+ *   signs   +-1 halves, length n (s_in) or m (s_out).  NULL = no rotation on
+ *           that side (neither signs nor Hadamard).
+ *   scales  length-m halves.
+ *
+ * Conventions:
+ *   - Ownership: every pointer is caller-owned device memory; the library
+ *     allocates, frees and synchronizes nothing, and keeps no per-call global
+ *     state.  Calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).
+ *   - Validation happens on the host before anything is launched; on any
+ *     error nothing is launched and the outputs are untouched:
+ *       m, n positive multiples of 128 (EXL3_ERR_SHAPE), 1 <= K <= 8
+ *       (EXL3_ERR_K), known codebook (EXL3_ERR_CODEBOOK), batch M within the
+ *       call's range (EXL3_ERR_BATCH), required pointers non-NULL
+ *       (EXL3_ERR_NULL), every device pointer 16-byte aligned (EXL3_ERR_ALIGN),
+ *       workspace large enough (EXL3_ERR_WORKSPACE).
+ *   - A failed launch returns EXL3_ERR_CUDA (the CUDA error is left for
+ *     cudaGetLastError to report as well).
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef EXL3_H_
+#define EXL3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/** A cudaStream_t. */
+typedef struct CUstream_st *exl3_stream_t;
+
+/** IEEE-754 binary16 bit pattern. */
+typedef uint16_t exl3_half;
+
+typedef enum {
+  EXL3_OK = 0,
+  EXL3_ERR_NULL = 1,
+  EXL3_ERR_SHAPE = 2,
+  EXL3_ERR_K = 3,
+  EXL3_ERR_CODEBOOK = 4,
+  EXL3_ERR_BATCH = 5,
+  EXL3_ERR_ALIGN = 6,
+  EXL3_ERR_WORKSPACE = 7,
+  EXL3_ERR_CUDA = 8,
+  EXL3_ERR_DEVICE_CHECK = 9
+} exl3_status;
+
+/** Computed codes of Lecture 1b Part nine.  Ids 2 (MCG) and 3 (mul1) are
+ *  reserved and rejected with EXL3_ERR_CODEBOOK. */
+typedef enum { EXL3_CB_3INST = 0, EXL3_CB_1MAD = 1 } exl3_codebook;
+
+/** Largest batch accepted by exl3_gemm_small. */
+#define EXL3_MAX_BATCH 32
+
+/**
+ * Input-side randomized Hadamard transform (Deep Dive Section 2; Lecture 1b
+ * Part eleven): x_rot[b] = Hb(s_in (.) x[b]) for b < M, rounded once to binary16.
+ *   x      [M][n] halves (read)      s_in  [n] +-1 halves (read, required)
+ *   x_rot  [M][n] halves (written; must not overlap x)
+ *   M >= 1, n a multiple of 128.
+ */
+exl3_status exl3_rht_in(const exl3_half *x, const exl3_half *s_in, exl3_half *x_rot,
+                        int M, int n, exl3_stream_t stream);
+
+/**
+ * Output-side transform (Deep Dive Section 2, the H^T diag(s_left) factor of
+ * the runtime identity; H_128 is symmetric): y[b] = Hb(s_out (.) z[b]).
+ *   z [M][m] halves (read)   s_out [m] (read, required)   y [M][m] (written)
+ */
+exl3_status exl3_rht_out(const exl3_half *z, const exl3_half *s_out, exl3_half *y,
+                         int M, int m, exl3_stream_t stream);
+
+/**
+ * Decode every tile into the unscaled binary16 W-hat (Lecture 1b Parts eight
+ * and nine).  Bit-exact: each weight is one defined binary16 value.
+ *   codes  (m/16)*(n/16)*8K words (read)
+ *   w_out  [m][n] row-major halves (written)
+ */
+exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m, int n,
+                              exl3_half *w_out, exl3_stream_t stream);
+
+/**
+ * Bytes of scratch that exl3_gemv / exl3_gemm_small need for an m x n layer
+ * at batch M (split-K partial sums and per-row-block arrival counters).
+ * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
+ * once after allocation; every call leaves it zero-filled again.  Two calls
+ * that may run concurrently must not share a workspace.
+ */
+size_t exl3_workspace_bytes(int m, int n, int M);
+
+/**
+ * Fused batch-1 layer (the decode-time quantized linear of Deep Dive
+ * Sections 2-3):  y = Hb(s_out (.) (scale (.) (W-hat Hb(s_in (.) x)))),
+ * W-hat decoded on the fly from `codes`, products accumulated in fp32, y
+ * rounded once to binary16.
+ *   x [n] halves, y [m] halves, scales [m] halves (required);
+ *   s_in [n] / s_out [m] or NULL (no rotation on that side);
+ *   workspace: >= exl3_workspace_bytes(m, n, 1) bytes, see there.
+ */
+exl3_status exl3_gemv(const uint32_t *codes, int K, int codebook, int m, int n,
+                      const exl3_half *s_in, const exl3_half *s_out,
+                      const exl3_half *scales, const exl3_half *x, exl3_half *y,
+                      void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
+/**
+ * Same layer for a skinny batch of 1 <= M <= EXL3_MAX_BATCH rows:
+ * x [M][n] -> y [M][m].  workspace >= exl3_workspace_bytes(m, n, M).
+ */
+exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, int n,
+                            const exl3_half *s_in, const exl3_half *s_out,
+                            const exl3_half *scales, int M, const exl3_half *x,
+                            exl3_half *y, void *workspace, size_t workspace_bytes,
+                            exl3_stream_t stream);
+
+/** Static, NUL-terminated description of a status code. */
+const char *exl3_status_string(exl3_status status);
+
+/** Static version string of the library. */
+const char *exl3_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_H_ */

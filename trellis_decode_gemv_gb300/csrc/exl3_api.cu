@@ -1,0 +1,160 @@
+// The C ABI of libexl3 (declared in include/exl3.h): host-side validation,
+// launch planning and dispatch.  Nothing here allocates, frees or
+// synchronizes.
+#include <cuda_runtime.h>
+
+#include "exl3_host.cuh"
+
+namespace exl3 {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+int choose_splits(int m, int n, int mb, int sm_count) {
+  const int rowblocks = m / kRowBlock;
+  const int nblk = n / kRowBlock;
+  const int target = 4 * sm_count;
+  int s = (target + rowblocks - 1) / rowblocks;
+  const int max_blk = static_cast<int>(kXsBudget / (static_cast<size_t>(mb) * kRowBlock * sizeof(float)));
+  const int s_smem = (nblk + max_blk - 1) / max_blk;
+  if (s < s_smem) s = s_smem;
+  if (s > nblk) s = nblk;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : s;
+}
+
+namespace {
+
+exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
+  switch (a.K) {
+    case 1: return launch_layer_k1(a, mb, stream);
+    case 2: return launch_layer_k2(a, mb, stream);
+    case 3: return launch_layer_k3(a, mb, stream);
+    case 4: return launch_layer_k4(a, mb, stream);
+    case 5: return launch_layer_k5(a, mb, stream);
+    case 6: return launch_layer_k6(a, mb, stream);
+    case 7: return launch_layer_k7(a, mb, stream);
+    case 8: return launch_layer_k8(a, mb, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
+// Largest input dimension whose rotated slice fits the shared-memory budget
+// at a batch chunk of 8 and the maximum split count.
+constexpr long long kMaxN = static_cast<long long>(kMaxSplits) *
+                            (kXsBudget / (8 * kRowBlock * sizeof(float))) * kRowBlock;
+
+}  // namespace
+}  // namespace exl3
+
+using namespace exl3;
+
+extern "C" const char* exl3_status_string(exl3_status status) {
+  switch (status) {
+    case EXL3_OK: return "ok";
+    case EXL3_ERR_NULL: return "a required pointer is NULL";
+    case EXL3_ERR_SHAPE: return "m and n must be positive multiples of 128 (and n within the supported maximum)";
+    case EXL3_ERR_K: return "K (bits per weight) must be in 1..8";
+    case EXL3_ERR_CODEBOOK: return "unknown codebook id (0 = 3INST, 1 = 1MAD)";
+    case EXL3_ERR_BATCH: return "batch M out of range";
+    case EXL3_ERR_ALIGN: return "device pointers must be 16-byte aligned";
+    case EXL3_ERR_WORKSPACE: return "workspace missing or smaller than exl3_workspace_bytes()";
+    case EXL3_ERR_CUDA: return "CUDA launch error";
+    case EXL3_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* exl3_version(void) { return "libexl3 0.1.0 sm_103a"; }
+
+extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
+  if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
+  return counters_bytes(m) +
+         sizeof(float) * static_cast<size_t>(max_splits(n)) * static_cast<size_t>(M) * static_cast<size_t>(m);
+}
+
+extern "C" exl3_status exl3_rht_in(const exl3_half* x, const exl3_half* s_in, exl3_half* x_rot,
+                                   int M, int n, exl3_stream_t stream) {
+  if (M < 1) return EXL3_ERR_BATCH;
+  if (n <= 0 || n % kRowBlock) return EXL3_ERR_SHAPE;
+  if (!x || !s_in || !x_rot) return EXL3_ERR_NULL;
+  if (!aligned16(x) || !aligned16(s_in) || !aligned16(x_rot)) return EXL3_ERR_ALIGN;
+  return launch_rht(reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(s_in),
+                    reinterpret_cast<__half*>(x_rot), M, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" exl3_status exl3_rht_out(const exl3_half* z, const exl3_half* s_out, exl3_half* y,
+                                    int M, int m, exl3_stream_t stream) {
+  return exl3_rht_in(z, s_out, y, M, m, stream);
+}
+
+extern "C" exl3_status exl3_decode_tiles(const uint32_t* codes, int K, int codebook, int m, int n,
+                                         exl3_half* w_out, exl3_stream_t stream) {
+  exl3_status st = check_shape(m, n);
+  if (st != EXL3_OK) return st;
+  if ((st = check_k_cb(K, codebook)) != EXL3_OK) return st;
+  if (!codes || !w_out) return EXL3_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(w_out)) return EXL3_ERR_ALIGN;
+  return launch_decode(codes, K, codebook, m, n, reinterpret_cast<__half*>(w_out),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codebook, int m, int n,
+                                       const exl3_half* s_in, const exl3_half* s_out,
+                                       const exl3_half* scales, int M, const exl3_half* x,
+                                       exl3_half* y, void* workspace, size_t workspace_bytes,
+                                       exl3_stream_t stream) {
+  exl3_status st = check_shape(m, n);
+  if (st != EXL3_OK) return st;
+  if (n > kMaxN) return EXL3_ERR_SHAPE;
+  if ((st = check_k_cb(K, codebook)) != EXL3_OK) return st;
+  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+  if (!codes || !scales || !x || !y) return EXL3_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y) ||
+      (s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out)))
+    return EXL3_ERR_ALIGN;
+  const size_t need = exl3_workspace_bytes(m, n, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = device_sm_count();
+  LayerArgs a;
+  a.codes = codes;
+  a.K = K;
+  a.codebook = codebook;
+  a.m = m;
+  a.n = n;
+  a.s_in = reinterpret_cast<const __half*>(s_in);
+  a.s_out = reinterpret_cast<const __half*>(s_out);
+  a.scales = reinterpret_cast<const __half*>(scales);
+  a.counters = static_cast<uint32_t*>(workspace);
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters_bytes(m));
+  for (int done = 0; done < M;) {
+    const int rem = M - done;
+    const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;
+    a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
+    a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
+    a.splits = choose_splits(m, n, mb, sms);
+    if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
+    done += mb;
+  }
+  return EXL3_OK;
+}
+
+extern "C" exl3_status exl3_gemv(const uint32_t* codes, int K, int codebook, int m, int n,
+                                 const exl3_half* s_in, const exl3_half* s_out,
+                                 const exl3_half* scales, const exl3_half* x, exl3_half* y,
+                                 void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  return exl3_gemm_small(codes, K, codebook, m, n, s_in, s_out, scales, 1, x, y, workspace,
+                         workspace_bytes, stream);
+}

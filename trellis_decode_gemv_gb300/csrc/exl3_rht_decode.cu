@@ -1,0 +1,118 @@
+// Standalone randomized Hadamard transform and tile decode kernels.
+//
+// rht:    out[r] = Hb(s (.) in[r]) for each row r, Hb = blockwise 128-point
+//         Walsh-Hadamard / sqrt(128) ("ExLlamaV3 & EXL3 Deep Dive" Section 2;
+//         "Trellis Quantization" Part eleven for the 128-wide blocks).  One
+//         warp per 128-block, 4 elements per lane, shuffle butterflies.
+// decode: W-hat[16I + r][16J + c] = code(state of step 16r + c of tile (I, J))
+//         ("Trellis Quantization" Parts eight and nine).  One thread per row
+//         pair of a tile (32 trellis steps), bit-exact binary16 output.
+#include "exl3_device.cuh"
+#include "exl3_host.cuh"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+    rht_kernel(const __half* __restrict__ in, const __half* __restrict__ signs,
+               __half* __restrict__ out, long long blocks, int d) {
+  const int lane = threadIdx.x & 31;
+  const long long job = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  if (job >= blocks) return;
+  const int per_row = d / kRowBlock;
+  const long long row = job / per_row;
+  const int kb = static_cast<int>(job - row * per_row);
+  const int col = kb * kRowBlock + 4 * lane;
+  const uint2 xr = *reinterpret_cast<const uint2*>(in + row * d + col);
+  const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+  float v[4];
+  {
+    const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+    const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+    v[0] = __low2float(x01) * __low2float(s01);
+    v[1] = __high2float(x01) * __high2float(s01);
+    v[2] = __low2float(x23) * __low2float(s23);
+    v[3] = __high2float(x23) * __high2float(s23);
+  }
+  fwht128_warp(v, lane);
+  const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
+  const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
+  uint2 orr;
+  orr.x = *reinterpret_cast<const uint32_t*>(&o01);
+  orr.y = *reinterpret_cast<const uint32_t*>(&o23);
+  *reinterpret_cast<uint2*>(out + row * d + col) = orr;
+}
+
+template <int K, int CB>
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const uint32_t* __restrict__ codes, int m, int n, __half* __restrict__ w) {
+  const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+  const int tiles_per_row = n / 16;
+  const long long tiles = static_cast<long long>(m / 16) * tiles_per_row;
+  if (gid >= tiles * 8) return;
+  const long long tile = gid >> 3;
+  const int p = static_cast<int>(gid & 7);
+  const long long I = tile / tiles_per_row;
+  const int J = static_cast<int>(tile - I * tiles_per_row);
+  uint32_t wr[RowPair<K>::kPairWords];
+  load_row_pair<K>(codes + tile * RowPair<K>::kTileWords, p, wr);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint32_t packed[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const __half lo = decode_state<CB>(pair_state<K>(wr, 16 * k + c));
+      const __half hi = decode_state<CB>(pair_state<K>(wr, 16 * k + c + 1));
+      packed[c / 2] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+                      (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    }
+    __half* dst = w + (I * 16 + 2 * p + k) * static_cast<long long>(n) + J * 16;
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  }
+}
+
+template <int K>
+exl3_status launch_decode_k(const uint32_t* codes, int codebook, int m, int n, __half* w,
+                            cudaStream_t stream) {
+  const long long threads = static_cast<long long>(m / 16) * (n / 16) * 8;
+  const unsigned grid = static_cast<unsigned>((threads + kThreads - 1) / kThreads);
+  if (codebook == kCb3Inst)
+    decode_kernel<K, kCb3Inst><<<grid, kThreads, 0, stream>>>(codes, m, n, w);
+  else
+    decode_kernel<K, kCb1Mad><<<grid, kThreads, 0, stream>>>(codes, m, n, w);
+  return launch_status();
+}
+
+}  // namespace
+
+exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int rows, int d,
+                       cudaStream_t stream) {
+  const long long blocks = static_cast<long long>(rows) * (d / kRowBlock);
+  const long long per_cta = kThreads / 32;
+  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
+  rht_kernel<<<grid, kThreads, 0, stream>>>(in, signs, out, blocks, d);
+  return launch_status();
+}
+
+exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
+                          cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_decode_k<1>(codes, codebook, m, n, w, stream);
+    case 2: return launch_decode_k<2>(codes, codebook, m, n, w, stream);
+    case 3: return launch_decode_k<3>(codes, codebook, m, n, w, stream);
+    case 4: return launch_decode_k<4>(codes, codebook, m, n, w, stream);
+    case 5: return launch_decode_k<5>(codes, codebook, m, n, w, stream);
+    case 6: return launch_decode_k<6>(codes, codebook, m, n, w, stream);
+    case 7: return launch_decode_k<7>(codes, codebook, m, n, w, stream);
+    case 8: return launch_decode_k<8>(codes, codebook, m, n, w, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
+}  // namespace exl3
