@@ -1,0 +1,89 @@
+"""The C ABI library loads, exports every entry point the header declares, and
+rejects bad arguments on the host before anything reaches a GPU.
+
+These run without a GPU: every call below fails validation, which happens
+before the library touches the CUDA runtime.  The fake pointers are never
+dereferenced.
+"""
+import ctypes
+
+import pytest
+
+from trellis_decode_gemv_gb300 import binding as B
+
+A = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load_library()
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = B.header_entry_points()
+    assert {"exl3_rht_in", "exl3_rht_out", "exl3_decode_tiles", "exl3_gemv",
+            "exl3_gemm_small", "exl3_workspace_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for s in range(10):
+        assert len(B.exl3_status_string(s)) > 0
+    assert "sm_103a" in B.exl3_version()
+
+
+def test_workspace_bytes(lib):
+    assert B.exl3_workspace_bytes(100, 128, 1) == 0
+    assert B.exl3_workspace_bytes(128, 128, 0) == 0
+    assert B.exl3_workspace_bytes(128, 128, 33) == 0
+    w1 = B.exl3_workspace_bytes(4096, 4096, 1)
+    # counters (32 row blocks, padded to 256 B) + 32 splits x 4096 fp32 partials
+    assert w1 == 256 + 4 * 32 * 4096
+    assert B.exl3_workspace_bytes(4096, 4096, 8) == 256 + 4 * 32 * 8 * 4096
+    assert B.exl3_workspace_bytes(1024, 28672, 1) == 256 + 4 * 64 * 1024
+
+
+def _gemm(lib, m=256, n=256, K=2, cb=0, M=1, codes=A, scales=A, x=A, y=A, s_in=A, s_out=A,
+          ws=A, ws_bytes=1 << 30):
+    return lib.exl3_gemm_small(codes, K, cb, m, n, s_in, s_out, scales, M, x, y, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=100), 2), (dict(n=130), 2), (dict(m=0), 2), (dict(n=-128), 2),
+    (dict(K=0), 3), (dict(K=9), 3), (dict(cb=2), 4), (dict(cb=-1), 4),
+    (dict(M=0), 5), (dict(M=33), 5),
+    (dict(codes=None), 1), (dict(scales=None), 1), (dict(x=None), 1), (dict(y=None), 1),
+    (dict(codes=A + 4), 6), (dict(x=A + 2), 6), (dict(y=A + 8), 6), (dict(s_in=A + 2), 6),
+    (dict(s_out=A + 2), 6), (dict(scales=A + 2), 6),
+    (dict(ws=None), 7), (dict(ws_bytes=16), 7), (dict(ws=A + 4), 6),
+])
+def test_gemm_small_validation(lib, kw, status):
+    assert _gemm(lib, **kw) == status
+
+
+def test_gemv_validation(lib):
+    assert lib.exl3_gemv(A, 2, 0, 100, 128, A, A, A, A, A, A, 1 << 20, None) == 2
+    assert lib.exl3_gemv(A, 2, 0, 128, 128, A, A, A, A, A, A, 8, None) == 7
+
+
+def test_decode_and_rht_validation(lib):
+    assert lib.exl3_decode_tiles(A, 2, 0, 128, 96, A, None) == 2
+    assert lib.exl3_decode_tiles(A, 10, 0, 128, 128, A, None) == 3
+    assert lib.exl3_decode_tiles(A, 2, 3, 128, 128, A, None) == 4
+    assert lib.exl3_decode_tiles(None, 2, 0, 128, 128, A, None) == 1
+    assert lib.exl3_decode_tiles(A + 4, 2, 0, 128, 128, A, None) == 6
+    assert lib.exl3_rht_in(A, A, A, 0, 128, None) == 5
+    assert lib.exl3_rht_in(A, A, A, 1, 100, None) == 2
+    assert lib.exl3_rht_in(A, None, A, 1, 128, None) == 1
+    assert lib.exl3_rht_out(A, A, A + 2, 1, 128, None) == 6
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_LIB", None)
+    monkeypatch.setenv("EXL3_LIBRARY", str(tmp_path / "nope.so"))
+    with pytest.raises(B.Exl3Error):
+        B.load_library()
+    monkeypatch.setattr(B, "_LIB", None)
+    monkeypatch.delenv("EXL3_LIBRARY")
+    assert isinstance(B.load_library(), ctypes.CDLL)

@@ -1,0 +1,196 @@
+"""ctypes binding of libexl3 (include/exl3.h).
+
+Each function has the name of the C entry point it calls and only checks and
+marshals torch tensors (device, dtype, contiguity) and passes raw device
+pointers plus the current CUDA stream.  Every step of the computation runs in
+the library's CUDA kernels; there is no other implementation to fall back on,
+and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+CB_3INST = 0
+CB_1MAD = 1
+MAX_BATCH = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+_STATUS_NAMES = {
+    0: "EXL3_OK", 1: "EXL3_ERR_NULL", 2: "EXL3_ERR_SHAPE", 3: "EXL3_ERR_K",
+    4: "EXL3_ERR_CODEBOOK", 5: "EXL3_ERR_BATCH", 6: "EXL3_ERR_ALIGN",
+    7: "EXL3_ERR_WORKSPACE", 8: "EXL3_ERR_CUDA", 9: "EXL3_ERR_DEVICE_CHECK",
+}
+
+
+class Exl3Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("EXL3_LIBRARY", os.path.join(_HERE, "libexl3.so"))
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "exl3_rht_in": ([_P, _P, _P, _I, _I, _P], _I),
+    "exl3_rht_out": ([_P, _P, _P, _I, _I, _P], _I),
+    "exl3_decode_tiles": ([_P, _I, _I, _I, _I, _P, _P], _I),
+    "exl3_workspace_bytes": ([_I, _I, _I], _SZ),
+    "exl3_gemv": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
+    "exl3_gemm_small": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
+    "exl3_status_string": ([_I], ctypes.c_char_p),
+    "exl3_version": ([], ctypes.c_char_p),
+}
+
+
+def header_entry_points() -> list[str]:
+    """Names of the functions declared in include/exl3.h."""
+    hdr = os.path.join(os.path.dirname(_HERE), "include", "exl3.h")
+    text = open(hdr).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(exl3_\w+)\s*\(", text, re.M)))
+
+
+def load_library():
+    """Load libexl3.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise Exl3Error(-1, f"{path} is missing: build it with "
+                            "`python -m trellis_decode_gemv_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load_library().exl3_status_string(status).decode()
+        raise Exl3Error(status, msg)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtypes, device=None) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+_HALF = (torch.float16,)
+_WORDS = (torch.int32, getattr(torch, "uint32", torch.int32))
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def exl3_status_string(status: int) -> str:
+    return load_library().exl3_status_string(status).decode()
+
+
+def exl3_version() -> str:
+    return load_library().exl3_version().decode()
+
+
+def exl3_workspace_bytes(m: int, n: int, M: int = 1) -> int:
+    return int(load_library().exl3_workspace_bytes(m, n, M))
+
+
+def alloc_workspace(m: int, n: int, M: int, device) -> torch.Tensor:
+    """A zero-filled workspace of exl3_workspace_bytes(m, n, M) bytes."""
+    nbytes = exl3_workspace_bytes(m, n, M)
+    if nbytes == 0:
+        raise Exl3Error(2, "invalid shape or batch for a workspace")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def exl3_rht_in(x: torch.Tensor, s_in: torch.Tensor, out: torch.Tensor | None = None):
+    lib = load_library()
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M, n = x2.shape
+    if out is None:
+        out = torch.empty_like(x2)
+    _check(lib.exl3_rht_in(_ptr(x2, "x", _HALF), _ptr(s_in, "s_in", _HALF, x.device),
+                           _ptr(out, "x_rot", _HALF, x.device), M, n, _stream(x.device)))
+    return out.view_as(x)
+
+
+def exl3_rht_out(z: torch.Tensor, s_out: torch.Tensor, out: torch.Tensor | None = None):
+    lib = load_library()
+    z2 = z if z.dim() == 2 else z.view(1, -1)
+    M, m = z2.shape
+    if out is None:
+        out = torch.empty_like(z2)
+    _check(lib.exl3_rht_out(_ptr(z2, "z", _HALF), _ptr(s_out, "s_out", _HALF, z.device),
+                            _ptr(out, "y", _HALF, z.device), M, m, _stream(z.device)))
+    return out.view_as(z)
+
+
+def exl3_decode_tiles(codes: torch.Tensor, K: int, codebook: int, m: int, n: int,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    lib = load_library()
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float16, device=codes.device)
+    _check(lib.exl3_decode_tiles(_ptr(codes, "codes", _WORDS), K, codebook, m, n,
+                                 _ptr(out, "w_out", _HALF, codes.device), _stream(codes.device)))
+    return out
+
+
+def exl3_gemm_small(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspace=None):
+    """y[M, m] = Hb(s_out (.) (scales (.) (W-hat Hb(s_in (.) x[M, n])))).  x is [M, n]."""
+    lib = load_library()
+    dev = codes.device
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, m), dtype=torch.float16, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(m, n, M, dev)
+    _check(lib.exl3_gemm_small(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), M, _ptr(x2, "x", _HALF, dev),
+        _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev),
+        workspace.numel(), _stream(dev)))
+    return y if x.dim() == 2 else y.view(-1)
+
+
+def exl3_gemv(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspace=None):
+    """Batch-1 layer: x [n] (or [1, n]) -> y [m]."""
+    lib = load_library()
+    dev = codes.device
+    if y is None:
+        y = torch.empty(m, dtype=torch.float16, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(m, n, 1, dev)
+    _check(lib.exl3_gemv(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), _ptr(x, "x", _HALF, dev), _ptr(y, "y", _HALF, dev),
+        _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(), _stream(dev)))
+    return y
