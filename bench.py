@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused randomized-Hadamard + bitshift-trellis GEMV.
+
+Metric: fused trellis GEMV weights/s (and effective HBM GB/s, and the
+fraction of the roofline) at batch 1.
+
+Default workload: the Llama-3-8B-shaped decoder layer set -- q/o 4096x4096,
+k/v 1024x4096, gate/up 14336x4096, down 4096x14336, each at K = 2, 3, 4 with
+both computed codes (1MAD, 3INST): 42 GEMVs, 1.309 G weights and 490 MB of
+packed codes per step, all resident in HBM.  A step runs every GEMV once, each
+on its own x.  The step is captured once in a CUDA graph and replayed; the
+490 MB working set is larger than L2, so every weight is re-read from HBM.
+
+Other workloads (--workload): single (4096x4096 K2 1MAD), llama70b (32 layers
+of Llama-3-70B shapes, K2 3INST, 6.85 GB packed), mixed (80-layer 2.9 bpw stack
++ K6 lm_head, 25 GB packed), sweep (14336x4096 and 4096x14336 K3 1MAD at a
+batch given by --batch).
+
+Roofline: per launch T_roof = max(packed+vector bytes / HBM bandwidth,
+decode integer ops / INT32 peak), integer ops per weight 4 (3INST: window
+funnel + mask, LCG multiply-add, mask/XOR) or 5 (1MAD: window funnel + mask,
+LCG, byte sum, int-to-float).  The HBM bandwidth is the measured copy bandwidth
+of this GPU model; the INT32 peak is SMs x 128 integer lanes per clock (4
+schedulers x 32 lanes) x the maximum SM clock.
+
+--impl reference times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+# The oracle's float64 matmuls run single-threaded so the CPU figure states its
+# thread count honestly.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from trellis_decode_gemv_gb300 import synth  # noqa: E402
+
+METRIC = "fused trellis GEMV weights/s & effective HBM GB/s, batch 1, % of roofline"
+L2_BYTES = 129 * 1024 * 1024
+SM_COUNT_NOMINAL = 152
+SM_MAX_MHZ_NOMINAL = 2070.0
+INT_LANES_PER_SM_CLK = 128
+HBM_FALLBACK_GBS = 6800.0
+OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL)), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, SM_MAX_MHZ_NOMINAL, "fallback"
+
+
+def workload(name: str, batch: int):
+    if name == "llama8b":
+        desc = ("Llama-3-8B-shaped layer set at batch 1: q/o 4096x4096, k/v 1024x4096, "
+                "gate/up 14336x4096, down 4096x14336, each at K=2,3,4 x {1MAD,3INST}")
+        return desc, 1, synth.llama8b_layer_set(), 1
+    if name == "single":
+        return "single 4096x4096 layer, K=2, 1MAD, batch 1", 0, synth.SINGLE_4096, 1
+    if name == "llama70b":
+        return ("Llama-3-70B-shaped layers (q/o 8192x8192, k/v 1024x8192, gate/up 28672x8192, "
+                "down 8192x28672) x 32 layers resident, K=2, 3INST, batch 1"), 2, synth.llama70b_stack(), 1
+    if name == "mixed":
+        return ("80-layer mixed-width stack (attn 8192x8192 K4; MLP 28672x8192 / 8192x28672, "
+                "K in {2,3,4}, 2.90 bpw body) + lm_head 128256x8192 K6, 3INST, batch 1"), 4, synth.mixed_stack(), 1
+    if name == "sweep":
+        return (f"14336x4096 and 4096x14336, K=3, 1MAD, batch {batch}"), 3, synth.BATCH_SWEEP_SHAPES, batch
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic(m, n, K, cb, M):
+    weights = m * n
+    nbytes = m * n * K // 8 + 2 * m + 2 * (m + n) + 2 * M * n + 2 * M * m
+    ops = weights * OPS_PER_WEIGHT[cb]
+    return weights, nbytes, ops
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        self.bus_id = bus_id
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50", "-f", self.path]
+            if self.bus_id:
+                cmd[1:1] = ["-i", self.bus_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            out["reasons"] = ["unsampled"]
+            return out
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            out["reasons"] = ["unsampled"]
+            return out
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        out.update(sm_mhz=float(np.median(sm)) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=sorted(reasons), samples=len(rows),
+                   power_w_max=max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+                   if any(r[2].replace(".", "").isdigit() for r in rows) else None)
+        return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_timed(gemvs, M, cfg, sel):
+    """Time only the oracle (input generation excluded)."""
+    from oracle import exl3_oracle as O
+    inputs = []
+    for i in sel:
+        name, m, n, K, cb = gemvs[i]
+        inputs.append((synth.layer_inputs(m, n, K, M, config=cfg, index=i), gemvs[i], i))
+    weights = 0
+    t0 = time.perf_counter()
+    for inp, (name, m, n, K, cb), i in inputs:
+        O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"],
+                                  inp["scales"], inp["x"], [i % (m // 128)])
+        weights += 128 * n * M
+    return weights, time.perf_counter() - t0
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    desc, cfg, gemvs, M = workload(args.workload, args.batch)
+    per_step = min(6, len(gemvs))
+    for s in range(args.warmup):
+        oracle_sample_timed(gemvs, M, cfg, [(s * per_step + i) % len(gemvs) for i in range(per_step)])
+    tw, tt = 0, 0.0
+    for s in range(args.steps):
+        sel = [((args.warmup + s) * per_step + i) % len(gemvs) for i in range(per_step)]
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel)
+        tw += w
+        tt += dt
+    value = tw / tt
+    sample = (f"per step: one 128-row output block of {per_step} of the {len(gemvs)} GEMVs "
+              f"(round-robin), oracle layer forward (decode + float64 product + transforms)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "weights/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tt / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "batch": M},
+        "cpu_baseline": {"value": value, "unit": "weights/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from trellis_decode_gemv_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    B.load_library()
+
+    desc, cfg, gemvs, M = workload(args.workload, args.batch)
+    hbm_gbs, sm_max_mhz, peak_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    p_int = sms * INT_LANES_PER_SM_CLK * sm_max_mhz * 1e6
+
+    # ---- resident inputs ------------------------------------------------
+    total_n = sum(g[2] for g in gemvs) * M
+    total_m = sum(g[1] for g in gemvs) * M
+    X = torch.empty(total_n, dtype=torch.float16, device=dev)
+    Y = torch.empty(total_m, dtype=torch.float16, device=dev)
+    calls = []
+    xo = yo = 0
+    ws_bytes = max(B.exl3_workspace_bytes(m, n, M) for _, m, n, _, _ in gemvs)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    packed = 0
+    for i, (name, m, n, K, cb) in enumerate(gemvs):
+        inp = synth.layer_inputs(m, n, K, M, config=cfg, index=i)
+        codes = torch.from_numpy(inp["codes"].view(np.int32)).to(dev)
+        s_in = torch.from_numpy(inp["s_in"]).to(dev)
+        s_out = torch.from_numpy(inp["s_out"]).to(dev)
+        scales = torch.from_numpy(inp["scales"]).to(dev)
+        X[xo:xo + M * n] = torch.from_numpy(inp["x"].reshape(-1)).to(dev)
+        x = X[xo:xo + M * n].view(M, n)
+        y = Y[yo:yo + M * m].view(M, m)
+        calls.append(dict(name=name, m=m, n=n, K=K, cb=cb, codes=codes, s_in=s_in, s_out=s_out,
+                          scales=scales, x=x, y=y))
+        packed += codes.numel() * 4
+        xo += M * n
+        yo += M * m
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for c in calls:
+            B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
+                              c["scales"], c["x"], y=c["y"], workspace=ws)
+
+    alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M) for c in calls]
+    weights_step = sum(a[0] for a in alg) * M
+    bytes_step = sum(a[1] for a in alg)
+    ops_step = sum(a[2] for a in alg) * M
+    l2_note = (f"inputs larger than L2: {packed / 1e6:.0f} MB of packed codes per step "
+               f"vs {L2_BYTES / 1e6:.0f} MB L2") if packed > L2_BYTES else "L2 NOT exceeded"
+
+    # ---- warm-up + graph capture ----------------------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize(dev)
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        graph = g
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize(dev)
+    except Exception as e:  # capture unsupported: time eager launches
+        print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        graph = None
+
+    def replay():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    # ---- timed region: K steps ------------------------------------------
+    bus = getattr(props, "pci_bus_id", None)
+    clocks = ClockSampler(bus if isinstance(bus, str) else None)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = weights_step * world / (ms_total / 1e3) * args.steps
+
+    # ---- per-launch durations (events around every launch) ---------------
+    nrep = max(3, min(args.steps, 50))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+    dur = np.zeros(len(calls))
+    with torch.cuda.stream(stream):
+        for r in range(nrep + 1):
+            torch.cuda._sleep(int(2e6 + 4e4 * len(calls)))  # keep the queue ahead of the host
+            evs[0].record(stream)
+            for i, c in enumerate(calls):
+                B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
+                                  c["scales"], c["x"], y=c["y"], workspace=ws)
+                evs[i + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            if r > 0:
+                dur += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(len(calls))]) * 1e-3
+    dur /= nrep
+    t_kernel = dur.sum()
+    t_hbm = np.array([a[1] / (hbm_gbs * 1e9) for a in alg])
+    t_int = np.array([a[2] * M / p_int for a in alg])
+    t_roof = np.maximum(t_hbm, t_int)
+    bound = "alu" if t_int.sum() >= t_hbm.sum() else "hbm"
+    if bound == "alu":
+        achieved, peak, unit = ops_step / t_kernel / 1e12, p_int / 1e12, "Tops/s"
+    else:
+        achieved, peak, unit = bytes_step / t_kernel / 1e9, hbm_gbs, "GB/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": (f"INT32: {sms} SMs x {INT_LANES_PER_SM_CLK} lanes/clk x "
+                                f"{sm_max_mhz:.0f} MHz (derived)") if bound == "alu"
+                else f"HBM copy bandwidth ({peak_src})",
+                "kernel": "layer_kernel (fused RHT + trellis decode + GEMV)",
+                "per_launch_us_mean": 1e6 * t_kernel / len(calls)}
+    hbm = {"achieved_gbs": bytes_step / t_kernel / 1e9, "peak_gbs": hbm_gbs, "peak_source": peak_src,
+           "frac": bytes_step / t_kernel / 1e9 / hbm_gbs}
+    roof_pct = 100.0 * t_roof.sum() / t_kernel
+
+    # per-(K, code) summary
+    per = {}
+    for c, d, a, th, ti in zip(calls, dur, alg, t_hbm, t_int):
+        key = f"K{c['K']}.{'1mad' if c['cb'] else '3inst'}"
+        e = per.setdefault(key, [0.0, 0, 0.0])
+        e[0] += d
+        e[1] += a[0] * M
+        e[2] += max(th, ti)
+    per_summary = {k: {"weights_per_s": v[1] / v[0], "roofline_pct": 100 * v[2] / v[0]}
+                   for k, v in sorted(per.items())}
+
+    # ---- e2e: host buffers, copies inside the timed region ---------------
+    Xh = torch.empty(total_n, dtype=torch.float16, pin_memory=True)
+    Xh.copy_(X.cpu())
+    Yh = torch.empty(total_m, dtype=torch.float16, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+            stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    e2e = {"value": weights_step * world * e2e_steps / t_e2e, "unit": "weights/s",
+           "h2d_bytes_per_step": total_n * 2, "d2h_bytes_per_step": total_m * 2,
+           "path": "binding call per GEMV (eager), pinned host x -> device, y -> pinned host"}
+
+    # ---- CPU oracle baseline (rank 0, N=1 only) --------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nsel = len(gemvs) if args.workload == "llama8b" else min(len(gemvs), 8)
+        sel = list(range(nsel)) if nsel == len(gemvs) else list(range(0, len(gemvs), max(1, len(gemvs) // nsel)))[:nsel]
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel)
+        cpu = {"value": w / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
+               "sample": f"one 128-row output block of each of {len(sel)} GEMVs of the workload "
+                         f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "weights/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
+                       "weights_per_step": weights_step, "packed_bytes_per_step": packed,
+                       "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
+                       "cuda_graph": graph is not None},
+            "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
+            "roofline_pct": roof_pct,
+            "roofline": roofline, "hbm": hbm, "per_code": per_summary,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": len(calls) * args.steps * (1 if M <= 8 else (M + 7) // 8),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b",
+                    choices=["llama8b", "single", "llama70b", "mixed", "sweep"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
