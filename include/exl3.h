@@ -68,7 +68,8 @@ typedef enum {
   EXL3_ERR_ALIGN = 6,
   EXL3_ERR_WORKSPACE = 7,
   EXL3_ERR_CUDA = 8,
-  EXL3_ERR_DEVICE_CHECK = 9
+  EXL3_ERR_DEVICE_CHECK = 9,
+  EXL3_ERR_SCRATCH = 10
 } exl3_status;
 
 /** Computed codes of Lecture 1b Part nine.  Ids 2 (MCG) and 3 (mul1) are
@@ -137,6 +138,33 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
                             const exl3_half *scales, int M, const exl3_half *x,
                             exl3_half *y, void *workspace, size_t workspace_bytes,
                             exl3_stream_t stream);
+
+/** Size of the fixed device array that exl3_gemv_noalloc uses as scratch. */
+#define EXL3_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/**
+ * exl3_gemv without a workspace argument, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is unavailable or not allowed
+ * (host callbacks, allocator hooks, plugins whose host framework owns all
+ * device memory, loops that must never allocate).  The source pages have no
+ * counterpart; it computes exactly what exl3_gemv computes, with the same
+ * arguments minus the workspace.
+ *   - Scratch: a file-scope device array of EXL3_NOALLOC_SCRATCH_BYTES bytes,
+ *     present on every GPU that loads the library until the process exits.
+ *     A layer whose split-K scratch (arrival counters + partial sums) would
+ *     not fit is rejected with EXL3_ERR_SCRATCH before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and clears its counters with an
+ *     asynchronous memset on `stream`.  Calls whose work can overlap on the
+ *     GPU (other streams, other host threads) race: serialize them.
+ *   - Allocates and frees nothing; asynchronous on `stream`.
+ */
+exl3_status exl3_gemv_noalloc(const uint32_t *codes, int K, int codebook, int m, int n,
+                              const exl3_half *s_in, const exl3_half *s_out,
+                              const exl3_half *scales, const exl3_half *x, exl3_half *y,
+                              exl3_stream_t stream);
 
 /** Static, NUL-terminated description of a status code. */
 const char *exl3_status_string(exl3_status status);

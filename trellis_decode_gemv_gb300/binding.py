@@ -25,6 +25,7 @@ _STATUS_NAMES = {
     0: "EXL3_OK", 1: "EXL3_ERR_NULL", 2: "EXL3_ERR_SHAPE", 3: "EXL3_ERR_K",
     4: "EXL3_ERR_CODEBOOK", 5: "EXL3_ERR_BATCH", 6: "EXL3_ERR_ALIGN",
     7: "EXL3_ERR_WORKSPACE", 8: "EXL3_ERR_CUDA", 9: "EXL3_ERR_DEVICE_CHECK",
+    10: "EXL3_ERR_SCRATCH",
 }
 
 
@@ -49,6 +50,7 @@ _SIGNATURES = {
     "exl3_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemv": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_small": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
+    "exl3_gemv_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
     "exl3_version": ([], ctypes.c_char_p),
 }
@@ -193,4 +195,20 @@ def exl3_gemv(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspac
         _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
         _ptr(scales, "scales", _HALF, dev), _ptr(x, "x", _HALF, dev), _ptr(y, "y", _HALF, dev),
         _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(), _stream(dev)))
+    return y
+
+
+def exl3_gemv_noalloc(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None):
+    """exl3_gemv for callers that cannot allocate device memory: the library
+    uses its own fixed device scratch array instead of a workspace.  Calls
+    that may overlap on the GPU must be serialized by the caller."""
+    lib = load_library()
+    dev = codes.device
+    if y is None:
+        y = torch.empty(m, dtype=torch.float16, device=dev)
+    _check(lib.exl3_gemv_noalloc(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), _ptr(x, "x", _HALF, dev), _ptr(y, "y", _HALF, dev),
+        _stream(dev)))
     return y

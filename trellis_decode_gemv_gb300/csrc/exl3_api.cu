@@ -70,6 +70,7 @@ extern "C" const char* exl3_status_string(exl3_status status) {
     case EXL3_ERR_WORKSPACE: return "workspace missing or smaller than exl3_workspace_bytes()";
     case EXL3_ERR_CUDA: return "CUDA launch error";
     case EXL3_ERR_DEVICE_CHECK: return "device-side check failed";
+    case EXL3_ERR_SCRATCH: return "layer needs more scratch than exl3_gemv_noalloc's fixed array (EXL3_NOALLOC_SCRATCH_BYTES)";
   }
   return "unknown status";
 }

@@ -1,0 +1,108 @@
+// exl3_gemv_noalloc: the batch-1 fused layer for callers that cannot allocate
+// device memory.
+//
+// exl3_gemv needs a caller-provided workspace (split-K partial sums and
+// per-row-block arrival counters).  Some callers cannot provide one: code that
+// runs where cudaMalloc is unavailable or forbidden (inside a host callback or
+// a custom allocator's own hooks, a plugin whose host framework owns every
+// allocation, a real-time loop that must never allocate).  This entry point
+// takes the same inputs and output but keeps its scratch in a fixed,
+// file-scope device array instead, so it allocates nothing.
+//
+// The array (EXL3_NOALLOC_SCRATCH_BYTES) lives on every GPU that loads the
+// library until the process exits.  All calls share it, so calls whose kernels
+// can overlap on the GPU (different streams, or different host threads on one
+// device) race and must be serialized by the caller.
+#include <cuda_runtime.h>
+
+#include "exl3_host.cuh"
+
+namespace exl3 {
+namespace {
+
+constexpr size_t kScratchBytes = EXL3_NOALLOC_SCRATCH_BYTES;
+
+// The shared scratch.  In host code this name is only a handle for the runtime;
+// the kernels get the device address obtained below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and cached.
+exl3_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EXL3_ERR_CUDA;
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return EXL3_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return EXL3_OK;
+}
+
+exl3_status launch_k(const LayerArgs& a, cudaStream_t stream) {
+  switch (a.K) {
+    case 1: return launch_layer_k1(a, 1, stream);
+    case 2: return launch_layer_k2(a, 1, stream);
+    case 3: return launch_layer_k3(a, 1, stream);
+    case 4: return launch_layer_k4(a, 1, stream);
+    case 5: return launch_layer_k5(a, 1, stream);
+    case 6: return launch_layer_k6(a, 1, stream);
+    case 7: return launch_layer_k7(a, 1, stream);
+    case 8: return launch_layer_k8(a, 1, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
+}  // namespace
+}  // namespace exl3
+
+using namespace exl3;
+
+extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codebook, int m, int n,
+                                         const exl3_half* s_in, const exl3_half* s_out,
+                                         const exl3_half* scales, const exl3_half* x,
+                                         exl3_half* y, exl3_stream_t stream) {
+  exl3_status st = check_shape(m, n);
+  if (st != EXL3_OK) return st;
+  if ((st = check_k_cb(K, codebook)) != EXL3_OK) return st;
+  if (!codes || !scales || !x || !y) return EXL3_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y) ||
+      (s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out)))
+    return EXL3_ERR_ALIGN;
+
+  const int splits = choose_splits(m, n, 1, device_sm_count());
+  const int nblk = n / kRowBlock;
+  const size_t xs_bytes = static_cast<size_t>((nblk + splits - 1) / splits) * kRowBlock * sizeof(float);
+  if (xs_bytes > kXsBudget) return EXL3_ERR_SHAPE;
+  const size_t need = counters_bytes(m) +
+                      (splits > 1 ? sizeof(float) * static_cast<size_t>(splits) * m : 0);
+  if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
+
+  void* scratch = nullptr;
+  if ((st = scratch_address(&scratch)) != EXL3_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // The arrival counters must start at zero; the array keeps whatever the
+  // previous call left, so clear them on the stream first.
+  if (cudaMemsetAsync(scratch, 0, counters_bytes(m), cs) != cudaSuccess) return EXL3_ERR_CUDA;
+
+  LayerArgs a;
+  a.codes = codes;
+  a.K = K;
+  a.codebook = codebook;
+  a.m = m;
+  a.n = n;
+  a.s_in = reinterpret_cast<const __half*>(s_in);
+  a.s_out = reinterpret_cast<const __half*>(s_out);
+  a.scales = reinterpret_cast<const __half*>(scales);
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = reinterpret_cast<__half*>(y);
+  a.counters = static_cast<uint32_t*>(scratch);
+  a.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + counters_bytes(m));
+  a.splits = splits;
+  return launch_k(a, cs);
+}
