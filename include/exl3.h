@@ -111,7 +111,10 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
  * at batch M (split-K partial sums and per-row-block arrival counters).
  * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
  * once after allocation; every call leaves it zero-filled again.  Two calls
- * that may run concurrently must not share a workspace.
+ * that may run concurrently must not share a workspace.  The uint32 at byte
+ * offset 4*(m/128) is a status word: the tensor-core kernel ORs 1 into it if
+ * one of its bounded device-side waits timed out (its outputs are then not
+ * valid); it stays set until the caller clears it.
  */
 size_t exl3_workspace_bytes(int m, int n, int M);
 
@@ -138,6 +141,21 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
                             const exl3_half *scales, int M, const exl3_half *x,
                             exl3_half *y, void *workspace, size_t workspace_bytes,
                             exl3_stream_t stream);
+
+/** Kernel family used by exl3_gemv / exl3_gemm_small. */
+typedef enum {
+  EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 4, tensor-core kernel above */
+  EXL3_PATH_SHUFFLE = 1, /**< decode + fp32 FMA + warp-shuffle reduction, any M */
+  EXL3_PATH_TENSOR = 2   /**< decoded tiles in TMEM feeding tcgen05 MMAs, any M */
+} exl3_path;
+
+/**
+ * Select the kernel family for subsequent exl3_gemv / exl3_gemm_small calls
+ * (a process-wide setting, default EXL3_PATH_AUTO).  Both families compute the
+ * same layer within the documented tolerance.  Returns EXL3_ERR_BATCH for an
+ * unknown value.
+ */
+exl3_status exl3_set_path(int path);
 
 /** Size of the fixed device array that exl3_gemv_noalloc uses as scratch. */
 #define EXL3_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -11,7 +11,7 @@ from __future__ import annotations
 _BINDING_NAMES = (
     "exl3_rht_in", "exl3_rht_out", "exl3_decode_tiles", "exl3_gemv",
     "exl3_gemm_small", "exl3_gemv_noalloc", "exl3_workspace_bytes", "exl3_status_string",
-    "exl3_version", "Exl3Error", "library_path", "load_library",
+    "exl3_version", "exl3_set_path", "workspace_status", "Exl3Error", "library_path", "load_library",
     "CB_3INST", "CB_1MAD",
 )
 

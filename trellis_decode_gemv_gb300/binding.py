@@ -51,6 +51,7 @@ _SIGNATURES = {
     "exl3_gemv": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_small": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemv_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "exl3_set_path": ([_I], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
     "exl3_version": ([], ctypes.c_char_p),
 }
@@ -117,6 +118,21 @@ def exl3_status_string(status: int) -> str:
 
 def exl3_version() -> str:
     return load_library().exl3_version().decode()
+
+
+PATH_AUTO, PATH_SHUFFLE, PATH_TENSOR = 0, 1, 2
+
+
+def exl3_set_path(path: int) -> None:
+    """Select the kernel family of exl3_gemv / exl3_gemm_small (process-wide)."""
+    _check(load_library().exl3_set_path(path))
+
+
+def workspace_status(workspace: torch.Tensor, m: int) -> int:
+    """The workspace's device-side status word (non-zero after a timed-out
+    device wait).  Synchronizes with the current stream."""
+    off = 4 * (m // 128)
+    return int(workspace[off:off + 4].view(torch.int32).item())
 
 
 def exl3_workspace_bytes(m: int, n: int, M: int = 1) -> int:

@@ -3,6 +3,8 @@
 // synchronizes.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "exl3_host.cuh"
 
 namespace exl3 {
@@ -22,7 +24,9 @@ int device_sm_count() {
 int choose_splits(int m, int n, int mb, int sm_count) {
   const int rowblocks = m / kRowBlock;
   const int nblk = n / kRowBlock;
-  const int target = 4 * sm_count;
+  // About one full wave: the batch-1 kernel keeps 6 CTAs of 256 threads
+  // resident per SM (40 registers per thread).
+  const int target = 6 * sm_count;
   int s = (target + rowblocks - 1) / rowblocks;
   const int max_blk = static_cast<int>(kXsBudget / (static_cast<size_t>(mb) * kRowBlock * sizeof(float)));
   const int s_smem = (nblk + max_blk - 1) / max_blk;
@@ -32,7 +36,36 @@ int choose_splits(int m, int n, int mb, int sm_count) {
   return s < 1 ? 1 : s;
 }
 
+int choose_tc_splits(int m, int n, int sm_count) {
+  const int rowblocks = m / kRowBlock;
+  const int nblk = n / kRowBlock;
+  const int target = 2 * sm_count;  // two 288-thread CTAs (256 TMEM columns each) per SM
+  int s = (target + rowblocks - 1) / rowblocks;
+  const int max_blk = kTcMaxSliceCols / kRowBlock;
+  const int s_smem = (nblk + max_blk - 1) / max_blk;
+  if (s < s_smem) s = s_smem;
+  if (s > nblk) s = nblk;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : s;
+}
+
 namespace {
+
+std::atomic<int> g_path{EXL3_PATH_AUTO};
+
+exl3_status launch_tc(const LayerArgs& a, int M, cudaStream_t stream) {
+  switch (a.K) {
+    case 1: return launch_tc_k1(a, M, stream);
+    case 2: return launch_tc_k2(a, M, stream);
+    case 3: return launch_tc_k3(a, M, stream);
+    case 4: return launch_tc_k4(a, M, stream);
+    case 5: return launch_tc_k5(a, M, stream);
+    case 6: return launch_tc_k6(a, M, stream);
+    case 7: return launch_tc_k7(a, M, stream);
+    case 8: return launch_tc_k8(a, M, stream);
+    default: return EXL3_ERR_K;
+  }
+}
 
 exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
   switch (a.K) {
@@ -75,7 +108,14 @@ extern "C" const char* exl3_status_string(exl3_status status) {
   return "unknown status";
 }
 
-extern "C" const char* exl3_version(void) { return "libexl3 0.1.0 sm_103a"; }
+extern "C" const char* exl3_version(void) { return "libexl3 0.2.0 sm_103a"; }
+
+extern "C" exl3_status exl3_set_path(int path) {
+  if (path != EXL3_PATH_AUTO && path != EXL3_PATH_SHUFFLE && path != EXL3_PATH_TENSOR)
+    return EXL3_ERR_BATCH;
+  g_path.store(path, std::memory_order_relaxed);
+  return EXL3_OK;
+}
 
 extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
@@ -129,7 +169,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int sms = device_sm_count();
-  LayerArgs a;
+  LayerArgs a{};
   a.codes = codes;
   a.K = K;
   a.codebook = codebook;
@@ -140,6 +180,15 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.scales = reinterpret_cast<const __half*>(scales);
   a.counters = static_cast<uint32_t*>(workspace);
   a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters_bytes(m));
+  a.status = a.counters + m / kRowBlock;
+  const int path = g_path.load(std::memory_order_relaxed);
+  const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
+  if (tensor) {
+    a.x = reinterpret_cast<const __half*>(x);
+    a.y = reinterpret_cast<__half*>(y);
+    a.splits = choose_tc_splits(m, n, sms);
+    return launch_tc(a, M, cs);
+  }
   for (int done = 0; done < M;) {
     const int rem = M - done;
     const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;

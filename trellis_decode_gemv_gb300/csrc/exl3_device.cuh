@@ -102,6 +102,65 @@ __device__ __forceinline__ uint32_t pair_state(const uint32_t (&w)[RowPair<K>::k
   return v >> 16;
 }
 
+// The 32 bits of the stream starting at bit b (b compile-time), b + 31 within w.
+template <int K>
+__device__ __forceinline__ uint32_t pair_bits32(const uint32_t (&w)[RowPair<K>::kPairWords], int b) {
+  const int q = b >> 5;
+  const int sh = b & 31;
+  return sh == 0 ? w[q] : __funnelshift_l(w[q + 1], w[q], sh);
+}
+
+// All 32 states of a row pair.  When K divides 16, the 32 bits starting at bit
+// K*c hold both the window of step c (top half) and that of step c + 16/K
+// (bottom half), so one funnel shift serves two states.
+template <int K>
+__device__ __forceinline__ void pair_states(const uint32_t (&w)[RowPair<K>::kPairWords],
+                                            uint32_t (&s)[32]) {
+  if constexpr (16 % K == 0) {
+    constexpr int D = 16 / K;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if ((c / D) % 2 == 0) {
+        const uint32_t r = pair_bits32<K>(w, K * c);
+        s[c] = r >> 16;
+        s[c + D] = r & 0xFFFFu;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) s[c] = pair_state<K>(w, c);
+  }
+}
+
+// Weight of a state in fp32, for the fused product.
+//  3INST: the binary16 sum of the two halves (exactly the defined weight),
+//         widened to fp32.
+//  1MAD:  the exact integer S - 510 as fp32, obtained without an int-to-float
+//         conversion: dp4a adds the byte sum to the bit pattern of 1.5 * 2^23
+//         minus 510, whose low mantissa bits then hold 1.5*2^23 + S - 510
+//         exactly, and one subtraction removes the offset.  The 1/sqrt(21845)
+//         factor is applied to x-tilde instead, so this skips the per-weight
+//         binary16 rounding of the defined weight (a relative change of at most
+//         2^-11 per weight, inside the layer tolerance).
+constexpr uint32_t kOneMadMagicBits = 0x4B400000u - static_cast<uint32_t>(kOneMadCentre);
+constexpr float kOneMadMagic = 12582912.0f;  // 1.5 * 2^23
+
+template <int CB>
+__device__ __forceinline__ float decode_f32(uint32_t s) {
+  if constexpr (CB == kCb3Inst) {
+    return __half2float(code_3inst(s));
+  } else {
+    const uint32_t x = lcg(s);
+    return __uint_as_float(__dp4a(x, 0x01010101u, kOneMadMagicBits)) - kOneMadMagic;
+  }
+}
+
+// Factor applied to x-tilde by the fused product for code CB (see decode_f32).
+template <int CB>
+__device__ __forceinline__ float x_factor() {
+  return CB == kCb1Mad ? kOneMadScale : 1.0f;
+}
+
 // ---------------------------------------------------------------------------
 // 128-point fast Walsh-Hadamard transform across one warp, 4 elements per lane
 // (element e = 4*lane + j), unnormalized, Sylvester (natural) order:

@@ -35,10 +35,11 @@ inline exl3_status launch_status() {
 // Number of SMs of the current device (queried once per device).
 int device_sm_count();
 
-// Workspace layout: [counters: one uint32 per 128-row block, padded to 256 B]
+// Workspace layout: [counters: one uint32 per 128-row block, then one status
+// word (non-zero after a device-side wait timed out), padded to 256 B]
 // [partials: fp32 [splits][M][m]].
 inline size_t counters_bytes(int m) {
-  const size_t b = sizeof(uint32_t) * static_cast<size_t>(m / kRowBlock);
+  const size_t b = sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1);
   return (b + 255) & ~static_cast<size_t>(255);
 }
 inline int max_splits(int n) {
@@ -61,6 +62,7 @@ struct LayerArgs {
   __half* y;        // [mb][m]
   float* partials;
   uint32_t* counters;
+  uint32_t* status;  // device-side error bits (tensor-core path), or nullptr
   int splits;
 };
 
@@ -77,5 +79,19 @@ exl3_status launch_layer_k5(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k6(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k7(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k8(const LayerArgs& a, int mb, cudaStream_t stream);
+exl3_status launch_tc_k1(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k2(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k3(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k4(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k5(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k6(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k7(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k8(const LayerArgs& a, int M, cudaStream_t stream);
+
+// Split count for the tensor-core path: about two resident CTAs per SM, and
+// slices of at most kTcMaxSliceCols columns (the duplicated x slice lives in
+// shared memory).
+constexpr int kTcMaxSliceCols = 1024;
+int choose_tc_splits(int m, int n, int sm_count);
 
 }  // namespace exl3

@@ -11,8 +11,10 @@
 // decodes 32 consecutive trellis steps from a word-aligned window.
 //
 // Prologue: the slice of x is rotated (signs, 128-point FWHT across a warp,
-// 1/sqrt(128)) into shared memory as fp32.  Main loop: decode + fp32 FMA into
-// two row accumulators per batch row.  Then a warp-shuffle reduction over the
+// 1/sqrt(128)) into shared memory as fp32, times the code's x factor (see
+// decode_f32).  Main loop: all 32 trellis states of a row pair, decode to fp32,
+// FMA into two row accumulators per batch row, with the next tile's words
+// loaded before the current tile is decoded.  Then a warp-shuffle reduction over the
 // 4 tile groups, and, when the input dimension is split, a last-arriving-CTA
 // combine (fp32 partials in the workspace + one atomic ticket per row block;
 // no CTA ever waits on another).  Epilogue: scale, output signs, 128-point
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kLayerThreads) layer_kernel(LayerArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] *= x_factor<CB>();
     *reinterpret_cast<float4*>(xs + b * ns + kb * kRowBlock + 4 * lane) =
         make_float4(v[0], v[1], v[2], v[3]);
   }
@@ -98,26 +102,35 @@ __global__ void __launch_bounds__(kLayerThreads) layer_kernel(LayerArgs a) {
 
   const int J0 = c0 / 16;
   const int J1 = (c0 + ns) / 16;
-  for (int J = J0 + jt; J < J1; J += 4) {
-    uint32_t w[RowPair<K>::kPairWords];
-    load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);
-    float wt[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) wt[c] = __half2float(decode_state<CB>(pair_state<K>(w, c)));
-    const float* xt = xs + (J * 16 - c0);
+  int J = J0 + jt;
+  uint32_t w[RowPair<K>::kPairWords];
+  if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);
+  while (J < J1) {
+    uint32_t st[32];
+    pair_states<K>(w, st);
+    const int Jc = J;
+    J += 4;
+    if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);  // prefetch
+    const float* xt = xs + (Jc * 16 - c0);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+      float wa[4], wb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wa[j] = decode_f32<CB>(st[4 * q + j]);
+        wb[j] = decode_f32<CB>(st[16 + 4 * q + j]);
+      }
 #pragma unroll
       for (int b = 0; b < MB; ++b) {
         const float4 xv = *reinterpret_cast<const float4*>(xt + b * ns + 4 * q);
-        acc[b][0] = fmaf(wt[4 * q + 0], xv.x, acc[b][0]);
-        acc[b][0] = fmaf(wt[4 * q + 1], xv.y, acc[b][0]);
-        acc[b][0] = fmaf(wt[4 * q + 2], xv.z, acc[b][0]);
-        acc[b][0] = fmaf(wt[4 * q + 3], xv.w, acc[b][0]);
-        acc[b][1] = fmaf(wt[16 + 4 * q + 0], xv.x, acc[b][1]);
-        acc[b][1] = fmaf(wt[16 + 4 * q + 1], xv.y, acc[b][1]);
-        acc[b][1] = fmaf(wt[16 + 4 * q + 2], xv.z, acc[b][1]);
-        acc[b][1] = fmaf(wt[16 + 4 * q + 3], xv.w, acc[b][1]);
+        acc[b][0] = fmaf(wa[0], xv.x, acc[b][0]);
+        acc[b][0] = fmaf(wa[1], xv.y, acc[b][0]);
+        acc[b][0] = fmaf(wa[2], xv.z, acc[b][0]);
+        acc[b][0] = fmaf(wa[3], xv.w, acc[b][0]);
+        acc[b][1] = fmaf(wb[0], xv.x, acc[b][1]);
+        acc[b][1] = fmaf(wb[1], xv.y, acc[b][1]);
+        acc[b][1] = fmaf(wb[2], xv.z, acc[b][1]);
+        acc[b][1] = fmaf(wb[3], xv.w, acc[b][1]);
       }
     }
   }

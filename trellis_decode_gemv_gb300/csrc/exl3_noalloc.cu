@@ -90,7 +90,7 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   // previous call left, so clear them on the stream first.
   if (cudaMemsetAsync(scratch, 0, counters_bytes(m), cs) != cudaSuccess) return EXL3_ERR_CUDA;
 
-  LayerArgs a;
+  LayerArgs a{};
   a.codes = codes;
   a.K = K;
   a.codebook = codebook;

@@ -1,0 +1,3 @@
+// Tensor-core fused layer kernels for K = 4 bits per weight.
+#include "exl3_tc.cuh"
+EXL3_DEFINE_TC_LAUNCHER(4)
