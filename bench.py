@@ -86,6 +86,21 @@ def workload(name: str, batch: int):
     raise SystemExit(f"unknown workload {name}")
 
 
+def kernels_per_call(path: str, M: int) -> int:
+    """Kernel launches of one exl3_gemm_small call: the tensor-core path is one
+    persistent kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2
+    or 1 rows, the x-rotation, layer and epilogue kernels."""
+    tensor = path == "tensor" or (path == "auto" and M > 4)
+    if tensor:
+        return 1
+    chunks, rem = 0, M
+    for c in (8, 4, 2, 1):
+        while rem >= c:
+            rem -= c
+            chunks += 1
+    return 3 * chunks
+
+
 def algorithmic(m, n, K, cb, M):
     weights = m * n
     nbytes = m * n * K // 8 + 2 * m + 2 * (m + n) + 2 * M * n + 2 * M * m
@@ -227,6 +242,7 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     B.load_library()
+    B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[args.path])
 
     desc, cfg, gemvs, M = workload(args.workload, args.batch)
     hbm_gbs, sm_max_mhz, peak_src = measured_peaks()
@@ -418,12 +434,12 @@ def run_ours(args):
             "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
                        "weights_per_step": weights_step, "packed_bytes_per_step": packed,
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
-                       "cuda_graph": graph is not None},
+                       "cuda_graph": graph is not None, "kernel_path": args.path},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
             "roofline_pct": roof_pct,
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(calls) * args.steps * (1 if M <= 8 else (M + 7) // 8),
+            "gpu_launches": len(calls) * args.steps * kernels_per_call(args.path, M),
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -442,6 +458,8 @@ def main():
                     choices=["llama8b", "single", "llama70b", "mixed", "sweep"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto",
+                    help="kernel family of the fused layer (exl3_set_path)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

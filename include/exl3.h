@@ -108,7 +108,8 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
 
 /**
  * Bytes of scratch that exl3_gemv / exl3_gemm_small need for an m x n layer
- * at batch M (split-K partial sums and per-row-block arrival counters).
+ * at batch M (per-row-block arrival counters, fp32 row sums, the rotated x,
+ * and the slice sums of the tensor-core kernel).
  * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
  * once after allocation; every call leaves it zero-filled again.  Two calls
  * that may run concurrently must not share a workspace.  The uint32 at byte
@@ -169,13 +170,14 @@ exl3_status exl3_set_path(int path);
  * arguments minus the workspace.
  *   - Scratch: a file-scope device array of EXL3_NOALLOC_SCRATCH_BYTES bytes,
  *     present on every GPU that loads the library until the process exits.
- *     A layer whose split-K scratch (arrival counters + partial sums) would
- *     not fit is rejected with EXL3_ERR_SCRATCH before anything is launched.
+ *     A layer whose scratch (arrival counters, m fp32 row sums and n words of
+ *     rotated x) would not fit is rejected with EXL3_ERR_SCRATCH before
+ *     anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - Every call shares the one array and clears its counters with an
- *     asynchronous memset on `stream`.  Calls whose work can overlap on the
+ *   - Every call shares the one array and clears its counters and row sums
+ *     with an asynchronous memset on `stream`.  Calls whose work can overlap on the
  *     GPU (other streams, other host threads) race: serialize them.
  *   - Allocates and frees nothing; asynchronous on `stream`.
  */

@@ -33,15 +33,20 @@ def test_status_strings_and_version(lib):
     assert "sm_103a" in B.exl3_version()
 
 
+def _ws(m, n, M):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    counters = a256(4 * (m // 128 + 1))
+    zacc = a256(4 * M * m)
+    xt = a256(4 * M * n)
+    return counters + zacc + xt + 4 * min(n // 128, 64) * M * m
+
+
 def test_workspace_bytes(lib):
     assert B.exl3_workspace_bytes(100, 128, 1) == 0
     assert B.exl3_workspace_bytes(128, 128, 0) == 0
     assert B.exl3_workspace_bytes(128, 128, 33) == 0
-    w1 = B.exl3_workspace_bytes(4096, 4096, 1)
-    # counters (32 row blocks, padded to 256 B) + 32 splits x 4096 fp32 partials
-    assert w1 == 256 + 4 * 32 * 4096
-    assert B.exl3_workspace_bytes(4096, 4096, 8) == 256 + 4 * 32 * 8 * 4096
-    assert B.exl3_workspace_bytes(1024, 28672, 1) == 256 + 4 * 64 * 1024
+    for m, n, M in [(4096, 4096, 1), (4096, 4096, 8), (1024, 28672, 1), (128256, 8192, 32)]:
+        assert B.exl3_workspace_bytes(m, n, M) == _ws(m, n, M)
 
 
 def _gemm(lib, m=256, n=256, K=2, cb=0, M=1, codes=A, scales=A, x=A, y=A, s_in=A, s_out=A,

@@ -91,17 +91,21 @@ def test_gemm_small_batches(M):
 
 
 def test_workspace_reuse_and_special_inputs():
-    """Two calls on one workspace give identical results (the arrival counters
-    are left at zero); x = 0 gives y = 0 exactly; zero scales give 0."""
+    """Two calls on one workspace agree (the arrival counters and the fp32 row
+    sums are left at zero); x = 0 gives y = 0 exactly; zero scales give 0."""
     m, n, K, cb = 1024, 2048, 2, 0
     inp = synth.layer_inputs(m, n, K, 1, config=65, index=0)
     d = upload(inp)
     ws = B.alloc_workspace(m, n, 1, "cuda")
     y1 = _run(d, K, cb, m, n, 1, ws=ws)
     y2 = _run(d, K, cb, m, n, 1, ws=ws)
-    assert torch.equal(y1, y2)
+    # fp32 atomic accumulation order varies: equal up to one binary16 rounding
+    diff = (y1.float() - y2.float()).abs()
+    assert float(diff.max()) <= 2.0 ** -9 * float(y1.float().abs().max())
     cnt = ws[:(m // 128) * 4].view(torch.int32)
     assert int(cnt.abs().sum()) == 0
+    zacc = ws[256:256 + 4 * m].view(torch.float32)
+    assert float(zacc.abs().sum()) == 0.0
     d0 = dict(d, x=torch.zeros_like(d["x"]))
     assert int(_run(d0, K, cb, m, n, 1, ws=ws).float().abs().sum()) == 0
     dz = dict(d, scales=torch.zeros_like(d["scales"]))

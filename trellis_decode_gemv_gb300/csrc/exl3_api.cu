@@ -21,48 +21,46 @@ int device_sm_count() {
   return sms;
 }
 
-int choose_splits(int m, int n, int mb, int sm_count) {
-  const int rowblocks = m / kRowBlock;
-  const int nblk = n / kRowBlock;
-  // About one full wave: the batch-1 kernel keeps 6 CTAs of 256 threads
-  // resident per SM (40 registers per thread).
-  const int target = 6 * sm_count;
-  int s = (target + rowblocks - 1) / rowblocks;
-  const int max_blk = static_cast<int>(kXsBudget / (static_cast<size_t>(mb) * kRowBlock * sizeof(float)));
-  const int s_smem = (nblk + max_blk - 1) / max_blk;
-  if (s < s_smem) s = s_smem;
-  if (s > nblk) s = nblk;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return s < 1 ? 1 : s;
+int choose_layer_ctas(int m, int n, int mb, int sm_count) {
+  const long long units = static_cast<long long>(m / kRowBlock) * (n / 16);
+  long long ctas = (units + 3) / 4;  // at least 4 tile columns per CTA
+  const long long wave = static_cast<long long>(mb == 1 ? 5 : mb == 2 ? 4 : 1) * sm_count;
+  if (ctas > wave) ctas = wave;
+  return ctas < 1 ? 1 : static_cast<int>(ctas);
 }
 
-int choose_tc_splits(int m, int n, int sm_count) {
+int choose_tc_slice(int m, int n, int M, int sm_count) {
   const int rowblocks = m / kRowBlock;
-  const int nblk = n / kRowBlock;
-  const int target = 2 * sm_count;  // two 288-thread CTAs (256 TMEM columns each) per SM
-  int s = (target + rowblocks - 1) / rowblocks;
-  const int max_blk = kTcMaxSliceCols / kRowBlock;
-  const int s_smem = (nblk + max_blk - 1) / max_blk;
-  if (s < s_smem) s = s_smem;
-  if (s > nblk) s = nblk;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return s < 1 ? 1 : s;
+  const int cap = M <= 16 ? 1024 : 512;
+  int best = 0;
+  double best_eff = -1.0;
+  for (int ns = cap; ns >= kRowBlock; ns /= 2) {
+    if (n % ns != 0 || n / ns > kMaxSplits) continue;
+    const long long items = static_cast<long long>(rowblocks) * (n / ns);
+    const long long rounds = (items + sm_count - 1) / sm_count;
+    const double eff = static_cast<double>(items) / static_cast<double>(rounds * sm_count);
+    if (eff > best_eff + 0.05) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
+  return best;  // 0: no admissible slice (n needs more than kMaxSplits slices)
 }
 
 namespace {
 
 std::atomic<int> g_path{EXL3_PATH_AUTO};
 
-exl3_status launch_tc(const LayerArgs& a, int M, cudaStream_t stream) {
+exl3_status launch_tc(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream) {
   switch (a.K) {
-    case 1: return launch_tc_k1(a, M, stream);
-    case 2: return launch_tc_k2(a, M, stream);
-    case 3: return launch_tc_k3(a, M, stream);
-    case 4: return launch_tc_k4(a, M, stream);
-    case 5: return launch_tc_k5(a, M, stream);
-    case 6: return launch_tc_k6(a, M, stream);
-    case 7: return launch_tc_k7(a, M, stream);
-    case 8: return launch_tc_k8(a, M, stream);
+    case 1: return launch_tc_k1(a, M, ns, grid, stream);
+    case 2: return launch_tc_k2(a, M, ns, grid, stream);
+    case 3: return launch_tc_k3(a, M, ns, grid, stream);
+    case 4: return launch_tc_k4(a, M, ns, grid, stream);
+    case 5: return launch_tc_k5(a, M, ns, grid, stream);
+    case 6: return launch_tc_k6(a, M, ns, grid, stream);
+    case 7: return launch_tc_k7(a, M, ns, grid, stream);
+    case 8: return launch_tc_k8(a, M, ns, grid, stream);
     default: return EXL3_ERR_K;
   }
 }
@@ -80,11 +78,6 @@ exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
     default: return EXL3_ERR_K;
   }
 }
-
-// Largest input dimension whose rotated slice fits the shared-memory budget
-// at a batch chunk of 8 and the maximum split count.
-constexpr long long kMaxN = static_cast<long long>(kMaxSplits) *
-                            (kXsBudget / (8 * kRowBlock * sizeof(float))) * kRowBlock;
 
 }  // namespace
 }  // namespace exl3
@@ -119,7 +112,7 @@ extern "C" exl3_status exl3_set_path(int path) {
 
 extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
-  return counters_bytes(m) +
+  return partials_offset(m, n, M) +
          sizeof(float) * static_cast<size_t>(max_splits(n)) * static_cast<size_t>(M) * static_cast<size_t>(m);
 }
 
@@ -156,7 +149,6 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
                                        exl3_stream_t stream) {
   exl3_status st = check_shape(m, n);
   if (st != EXL3_OK) return st;
-  if (n > kMaxN) return EXL3_ERR_SHAPE;
   if ((st = check_k_cb(K, codebook)) != EXL3_OK) return st;
   if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
   if (!codes || !scales || !x || !y) return EXL3_ERR_NULL;
@@ -178,24 +170,33 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.s_in = reinterpret_cast<const __half*>(s_in);
   a.s_out = reinterpret_cast<const __half*>(s_out);
   a.scales = reinterpret_cast<const __half*>(scales);
-  a.counters = static_cast<uint32_t*>(workspace);
-  a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters_bytes(m));
+  char* ws = static_cast<char*>(workspace);
+  a.counters = reinterpret_cast<uint32_t*>(ws);
   a.status = a.counters + m / kRowBlock;
+  a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
+  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, n, M));
+  uint32_t* xt = reinterpret_cast<uint32_t*>(ws + xt_offset(m, M));
   const int path = g_path.load(std::memory_order_relaxed);
   const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
   if (tensor) {
     a.x = reinterpret_cast<const __half*>(x);
     a.y = reinterpret_cast<__half*>(y);
-    a.splits = choose_tc_splits(m, n, sms);
-    return launch_tc(a, M, cs);
+    const int ns = choose_tc_slice(m, n, M, sms);
+    if (ns == 0) return EXL3_ERR_SHAPE;
+    a.splits = n / ns;
+    return launch_tc(a, M, ns, sms, cs);
   }
   for (int done = 0; done < M;) {
     const int rem = M - done;
     const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;
     a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
     a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
-    a.splits = choose_splits(m, n, mb, sms);
+    a.xt = xt;
+    a.ctas = choose_layer_ctas(m, n, mb, sms);
+    if ((st = launch_xt(a.x, a.s_in, xt, mb, n, codebook == EXL3_CB_1MAD ? kOneMadFactor : 1.0f, cs)) != EXL3_OK)
+      return st;
     if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
+    if ((st = launch_epi(a.zacc, a.scales, a.s_out, a.y, mb, m, cs)) != EXL3_OK) return st;
     done += mb;
   }
   return EXL3_OK;

@@ -12,8 +12,10 @@
 namespace exl3 {
 
 constexpr int kRowBlock = 128;      // rows per output block (one output FWHT)
+// 1/sqrt(21845) rounded to binary32: the 1MAD scale, applied to the rotated x
+// by the warp-shuffle path.
+constexpr float kOneMadFactor = 0x1.bb688cp-8f;
 constexpr int kMaxSplits = 64;      // cap on K-dimension slices of one layer
-constexpr size_t kXsBudget = 96 * 1024;  // smem bytes for the rotated x slice
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -35,22 +37,34 @@ inline exl3_status launch_status() {
 // Number of SMs of the current device (queried once per device).
 int device_sm_count();
 
-// Workspace layout: [counters: one uint32 per 128-row block, then one status
-// word (non-zero after a device-side wait timed out), padded to 256 B]
-// [partials: fp32 [splits][M][m]].
+// Workspace layout (all offsets 256-byte aligned):
+//   counters  one uint32 per 128-row block (tiles accumulated so far), then one
+//             status word (non-zero after a device-side wait timed out);
+//   zacc      fp32 [M][m]: row sums accumulated by the warp-shuffle kernel;
+//   xt        uint32 [M][n]: the rotated x as binary16, duplicated in both
+//             halves (written by the x-rotation kernel of each call);
+//   partials  fp32 [slices][M][m]: slice sums of the tensor-core kernel.
+// counters and zacc must be zero before a call and are zero after it.
+inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 inline size_t counters_bytes(int m) {
-  const size_t b = sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1);
-  return (b + 255) & ~static_cast<size_t>(255);
+  return align256(sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1));
+}
+inline size_t zacc_offset(int m) { return counters_bytes(m); }
+inline size_t xt_offset(int m, int M) {
+  return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m);
+}
+inline size_t partials_offset(int m, int n, int M) {
+  return xt_offset(m, M) + align256(sizeof(uint32_t) * static_cast<size_t>(M) * n);
 }
 inline int max_splits(int n) {
   const int nblk = n / kRowBlock;
   return nblk < kMaxSplits ? nblk : kMaxSplits;
 }
 
-// Split count of the K dimension for an m x n layer at batch chunk mb: enough
-// CTAs to cover every SM a few times, each slice a whole number of 128-column
-// blocks, and the rotated x slice within the shared-memory budget.
-int choose_splits(int m, int n, int mb, int sm_count);
+// Number of CTAs of the warp-shuffle kernel at batch chunk mb: one wave (5,
+// 4 or 1 resident 256-thread CTAs per SM for mb = 1, 2, larger), but no
+// fewer than 4 tile columns of work per CTA (one tile per lane group).
+int choose_layer_ctas(int m, int n, int mb, int sm_count);
 
 struct LayerArgs {
   const uint32_t* codes;
@@ -60,10 +74,13 @@ struct LayerArgs {
   const __half* scales;
   const __half* x;  // [mb][n]
   __half* y;        // [mb][m]
-  float* partials;
+  float* partials;    // tensor-core kernel: [splits][M][m]
+  float* zacc;        // warp-shuffle kernel: [mb][m], zero on entry and exit
+  const uint32_t* xt; // warp-shuffle kernel: rotated x, duplicated binary16 [mb][n]
   uint32_t* counters;
-  uint32_t* status;  // device-side error bits (tensor-core path), or nullptr
-  int splits;
+  uint32_t* status;   // device-side error bits (tensor-core path), or nullptr
+  int splits;         // tensor-core kernel: slices of the input dimension
+  int ctas;           // warp-shuffle kernel: grid size
 };
 
 // Internal launchers (one translation unit per K for the layer kernels).
@@ -71,6 +88,14 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
                        cudaStream_t stream);
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
                           cudaStream_t stream);
+// Rotated x for the warp-shuffle kernel: xt[b][c] = binary16(factor * Hb(s_in (.) x[b]))[c]
+// in both halves of a 32-bit word (no rotation when s_in is NULL).
+exl3_status launch_xt(const __half* x, const __half* s_in, uint32_t* xt, int rows, int n, float factor,
+                      cudaStream_t stream);
+// Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
+// per 128-row block (no rotation when s_out is NULL); zeroes zacc.
+exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,
+                       int m, cudaStream_t stream);
 exl3_status launch_layer_k1(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k2(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k3(const LayerArgs& a, int mb, cudaStream_t stream);
@@ -79,19 +104,20 @@ exl3_status launch_layer_k5(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k6(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k7(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k8(const LayerArgs& a, int mb, cudaStream_t stream);
-exl3_status launch_tc_k1(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k2(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k3(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k4(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k5(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k6(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k7(const LayerArgs& a, int M, cudaStream_t stream);
-exl3_status launch_tc_k8(const LayerArgs& a, int M, cudaStream_t stream);
+exl3_status launch_tc_k1(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k2(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k3(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k4(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k5(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k6(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k7(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
+exl3_status launch_tc_k8(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
 
-// Split count for the tensor-core path: about two resident CTAs per SM, and
-// slices of at most kTcMaxSliceCols columns (the duplicated x slice lives in
-// shared memory).
-constexpr int kTcMaxSliceCols = 1024;
-int choose_tc_splits(int m, int n, int sm_count);
+// Work split of the persistent tensor-core kernel: the slice width ns (a
+// divisor of n, a power of two times 128, at most 1024 columns for batches up
+// to 16 and 512 above, at most kMaxSplits slices) that best balances the
+// (m/128) * (n/ns) work items over the resident CTAs (one per SM), preferring
+// wider slices when the balance is within 5%.
+int choose_tc_slice(int m, int n, int M, int sm_count);
 
 }  // namespace exl3

@@ -1,24 +1,44 @@
-// Fused layer kernel, warp-shuffle path:
+// Fused layer kernel, warp-shuffle path (batch 1..8):
 //   y = Hb(s_out (.) (scale (.) (W-hat Hb(s_in (.) x))))
 // ("ExLlamaV3 & EXL3 Deep Dive" Section 2 runtime identity; W-hat decoded on
 // the fly from the bitshift-trellis codes of "Trellis Quantization" Parts
 // eight and nine; blockwise 128-point transforms of Part eleven).
 //
-// One CTA = one 128-row output block x one slice of the input dimension
-// (a whole number of 128-column blocks).  8 warps, warp w owns tile-row
-// 8*blockIdx.x + w.  Inside a warp, lane = 8*jt + p: jt picks every 4th tile
-// of the slice, p the row pair (rows 2p, 2p+1) of the tile, so each thread
-// decodes 32 consecutive trellis steps from a word-aligned window.
+// Each call runs three kernels on the stream, chained by programmatic
+// dependent launch (each starts while its predecessor runs and waits for it,
+// griddepcontrol.wait, before touching memory the predecessor writes):
+//  1. xt_kernel (csrc/exl3_rht_decode.cu) rotates x once: signs, 128-point FWHT
+//     across a warp, 1/sqrt(128), times the code's x factor, rounded to
+//     binary16 and stored duplicated in both halves of a 32-bit word;
+//  2. layer_kernel (below) accumulates W-hat x-tilde into the fp32 row sums
+//     zacc with atomic adds;
+//  3. epi_kernel (csrc/exl3_rht_decode.cu) applies the scale, the output signs
+//     and the 128-point FWHT to each 128-row block of zacc, stores y as
+//     binary16 and zeroes zacc for the next call.
 //
-// Prologue: the slice of x is rotated (signs, 128-point FWHT across a warp,
-// 1/sqrt(128)) into shared memory as fp32, times the code's x factor (see
-// decode_f32).  Main loop: all 32 trellis states of a row pair, decode to fp32,
-// FMA into two row accumulators per batch row, with the next tile's words
-// loaded before the current tile is decoded.  Then a warp-shuffle reduction over the
-// 4 tile groups, and, when the input dimension is split, a last-arriving-CTA
-// combine (fp32 partials in the workspace + one atomic ticket per row block;
-// no CTA ever waits on another).  Epilogue: scale, output signs, 128-point
-// FWHT across a warp, binary16 store.
+// Work split (stream-K style): the (m/128 row blocks) x (n/16 tile columns)
+// work units are cut into gridDim.x equal contiguous ranges, one per CTA; a
+// range is a sequence of segments, each inside one row block.  8 warps per
+// CTA, warp w owns tile-row 8*rb + w of the segment's row block; lane
+// 8*jt + p handles every 4th tile (jt) and the row pair 2p, 2p+1 of the tile,
+// so each thread decodes 32 consecutive trellis steps from a word-aligned
+// window (the next tile's words are loaded before the current tile is
+// decoded).  Per column one packed binary16
+// FMA (HFMA2):
+//   3INST  acc += (lo, hi) * (x, x)   -- the two halves of the mask/XOR step,
+//          so lo*x + hi*x is the weight times x without a separate add;
+//   1MAD   acc += (S_a - 510, S_b - 510) * (x, x) for rows 2p and 2p+1, the
+//          byte sums spliced into binary16 1024 + S by dp4a, paired with one
+//          byte permute and made exact with one packed subtraction of 1534.
+// The packed accumulators are flushed into fp32 after every 16 columns (one
+// tile row), which keeps the binary16 accumulation error near 1e-3 of a
+// tile-row partial sum and about 7e-4 of the result (relative L2).
+//
+// Combine: a warp-shuffle reduction over the 4 tile groups and fp32 atomic adds
+// of each segment's row sums into zacc.  No CTA waits on another; the kernel
+// boundary orders the sums before the epilogue kernel.  The atomic adds make
+// the fp32 summation order, and so the last bit of some outputs, vary from
+// run to run.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -47,174 +67,143 @@ __device__ __forceinline__ void store_half4(__half* p, const float (&v)[4]) {
   *reinterpret_cast<uint2*>(p) = r;
 }
 
-template <int K, int CB, int MB>
-__global__ void __launch_bounds__(kLayerThreads) layer_kernel(LayerArgs a) {
-  extern __shared__ __align__(16) float smem[];
-  __shared__ uint32_t s_ticket;
+// Resident 256-thread CTAs per SM the kernel is compiled for (registers).
+template <int MB>
+__host__ __device__ constexpr int layer_ctas_per_sm() {
+  return MB == 1 ? 5 : MB == 2 ? 4 : 1;
+}
 
+template <int K, int CB, int MB>
+__global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_kernel(LayerArgs a) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int rb = blockIdx.x;
-  const int split = blockIdx.y;
-  const int nblk = a.n / kRowBlock;
-  const int kb0 = static_cast<int>(static_cast<long long>(split) * nblk / a.splits);
-  const int kb1 = static_cast<int>(static_cast<long long>(split + 1) * nblk / a.splits);
-  const int c0 = kb0 * kRowBlock;
-  const int ns = (kb1 - kb0) * kRowBlock;
-  float* xs = smem;            // [MB][ns] rotated x slice
-  float* zs = smem + MB * ns;  // [MB][128] row sums of this block
-
-  // ---- prologue: rotate the x slice into shared memory -------------------
-  const int nkb = ns / kRowBlock;
-  for (int job = warp; job < MB * nkb; job += kLayerThreads / 32) {
-    const int b = job / nkb;
-    const int kb = job - b * nkb;
-    const int col = c0 + kb * kRowBlock + 4 * lane;
-    float v[4];
-    load_half4(a.x + static_cast<size_t>(b) * a.n + col, v);
-    if (a.s_in != nullptr) {
-      float s[4];
-      load_half4(a.s_in + col, s);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] *= s[j];
-      fwht128_warp(v, lane);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] *= x_factor<CB>();
-    *reinterpret_cast<float4*>(xs + b * ns + kb * kRowBlock + 4 * lane) =
-        make_float4(v[0], v[1], v[2], v[3]);
-  }
-  __syncthreads();
-
-  // ---- main loop: decode + fp32 FMA ---------------------------------------
-  constexpr int kTw = RowPair<K>::kTileWords;
-  const int I = rb * (kRowBlock / 16) + warp;
   const int jt = lane >> 3;
   const int p = lane & 7;
-  const int tiles_per_row = a.n / 16;
-  const uint32_t* rowp = a.codes + static_cast<size_t>(I) * tiles_per_row * kTw;
-  float acc[MB][2];
-#pragma unroll
-  for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+  constexpr int kTw = RowPair<K>::kTileWords;
+  const int nt = a.n / 16;
+  const long long units = static_cast<long long>(a.m / kRowBlock) * nt;
+  const long long u_begin = static_cast<long long>(blockIdx.x) * units / gridDim.x;
+  const long long u_end = static_cast<long long>(blockIdx.x + 1) * units / gridDim.x;
+  const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
 
-  const int J0 = c0 / 16;
-  const int J1 = (c0 + ns) / 16;
-  int J = J0 + jt;
-  uint32_t w[RowPair<K>::kPairWords];
-  if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);
-  while (J < J1) {
-    uint32_t st[32];
-    pair_states<K>(w, st);
-    const int Jc = J;
-    J += 4;
-    if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);  // prefetch
-    const float* xt = xs + (Jc * 16 - c0);
+  // The rotated x is written by the preceding kernel on the stream.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  for (long long u = u_begin; u < u_end;) {
+    const int rb = static_cast<int>(u / nt);
+    const int ja = static_cast<int>(u - static_cast<long long>(rb) * nt);
+    const int jb = static_cast<int>(ja + (u_end - u) < nt ? ja + (u_end - u) : nt);
+    const int I = rb * (kRowBlock / 16) + warp;
+    const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
+
+    float acc[MB][2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float wa[4], wb[4];
+    for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+
+    // The rotated x of the current tile is loaded first, the code words of the
+    // next tile before the current one is decoded.
+    int J = ja + jt;
+    uint32_t w[RowPair<K>::kPairWords];
+    if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);
+    while (J < jb) {
+      uint4 xc[MB][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        wa[j] = decode_f32<CB>(st[4 * q + j]);
-        wb[j] = decode_f32<CB>(st[16 + 4 * q + j]);
+      for (int b = 0; b < MB; ++b)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          xc[b][q] = __ldg(reinterpret_cast<const uint4*>(a.xt + static_cast<size_t>(b) * a.n + J * 16 + 4 * q));
+      uint32_t st[32];
+      pair_states<K>(w, st);
+      J += 4;
+      if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);  // prefetch
+      __half2 ha[MB], hb[MB];
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        ha[b] = __float2half2_rn(0.f);
+        hb[b] = __float2half2_rn(0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 xv[MB];
+#pragma unroll
+        for (int b = 0; b < MB; ++b) xv[b] = xc[b][q];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * q + j;
+          const uint32_t xa = lcg(st[c]);
+          const uint32_t xb = lcg(st[16 + c]);
+          if constexpr (CB == kCb3Inst) {
+            const uint32_t pa = (xa & k3InstMask) ^ k3InstMagic;
+            const uint32_t pb = (xb & k3InstMask) ^ k3InstMagic;
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
+              ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
+              hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
+            }
+          } else {
+            const uint32_t ra = __dp4a(xa, 0x01010101u, 0x6400u);
+            const uint32_t rb2 = __dp4a(xb, 0x01010101u, 0x6400u);
+            const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
+            const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
+            }
+          }
+        }
       }
 #pragma unroll
       for (int b = 0; b < MB; ++b) {
-        const float4 xv = *reinterpret_cast<const float4*>(xt + b * ns + 4 * q);
-        acc[b][0] = fmaf(wa[0], xv.x, acc[b][0]);
-        acc[b][0] = fmaf(wa[1], xv.y, acc[b][0]);
-        acc[b][0] = fmaf(wa[2], xv.z, acc[b][0]);
-        acc[b][0] = fmaf(wa[3], xv.w, acc[b][0]);
-        acc[b][1] = fmaf(wb[0], xv.x, acc[b][1]);
-        acc[b][1] = fmaf(wb[1], xv.y, acc[b][1]);
-        acc[b][1] = fmaf(wb[2], xv.z, acc[b][1]);
-        acc[b][1] = fmaf(wb[3], xv.w, acc[b][1]);
+        if constexpr (CB == kCb3Inst) {
+          acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
+          acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
+        } else {
+          acc[b][0] += __low2float(ha[b]);
+          acc[b][1] += __high2float(ha[b]);
+        }
       }
     }
-  }
 
-  // ---- warp-shuffle reduction over the 4 tile groups -----------------------
-#pragma unroll
-  for (int b = 0; b < MB; ++b) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      float v = acc[b][k];
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-      acc[b][k] = v;
-    }
-  }
-  if (jt == 0) {
+    // ---- warp-shuffle reduction over the 4 tile groups, accumulate into zacc --
 #pragma unroll
     for (int b = 0; b < MB; ++b) {
-      zs[b * kRowBlock + warp * 16 + 2 * p] = acc[b][0];
-      zs[b * kRowBlock + warp * 16 + 2 * p + 1] = acc[b][1];
-    }
-  }
-  __syncthreads();
-
-  // ---- split-K combine: the last CTA of this row block sums the partials ---
-  if (a.splits > 1) {
-    float* part = a.partials + static_cast<size_t>(split) * MB * a.m;
-    for (int i = tid; i < MB * kRowBlock; i += kLayerThreads) {
-      const int b = i / kRowBlock;
-      const int r = i - b * kRowBlock;
-      part[static_cast<size_t>(b) * a.m + rb * kRowBlock + r] = zs[i];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_ticket = atomicAdd(a.counters + rb, 1u);
-    __syncthreads();
-    if (s_ticket != static_cast<uint32_t>(a.splits - 1)) return;
-    __threadfence();
-    for (int i = tid; i < MB * kRowBlock; i += kLayerThreads) {
-      const int b = i / kRowBlock;
-      const int r = i - b * kRowBlock;
-      float s = 0.f;
-      for (int sp = 0; sp < a.splits; ++sp)
-        s += __ldcg(a.partials + (static_cast<size_t>(sp) * MB + b) * a.m + rb * kRowBlock + r);
-      zs[i] = s;
-    }
-    if (tid == 0) a.counters[rb] = 0u;  // leave the workspace zeroed for the next call
-    __syncthreads();
-  }
-
-  // ---- epilogue: scale, output signs + FWHT, binary16 ----------------------
-  for (int b = warp; b < MB; b += kLayerThreads / 32) {
-    const int r0 = rb * kRowBlock + 4 * lane;
-    float v[4], sc[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = zs[b * kRowBlock + 4 * lane + j];
-    load_half4(a.scales + r0, sc);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] *= sc[j];
-    if (a.s_out != nullptr) {
-      float s[4];
-      load_half4(a.s_out + r0, s);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] *= s[j];
-      fwht128_warp(v, lane);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
+      for (int k = 0; k < 2; ++k) {
+        float v = acc[b][k];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        acc[b][k] = v;
+      }
     }
-    store_half4(a.y + static_cast<size_t>(b) * a.m + r0, v);
+    if (jt == 0) {
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        float* z = a.zacc + static_cast<size_t>(b) * a.m + rb * kRowBlock + warp * 16 + 2 * p;
+        atomicAdd(z, acc[b][0]);
+        atomicAdd(z + 1, acc[b][1]);
+      }
+    }
+    u += jb - ja;
   }
 }
 
 template <int K, int CB, int MB>
 exl3_status launch_layer_t(const LayerArgs& a, cudaStream_t stream) {
-  const int nblk = a.n / kRowBlock;
-  const int ns_max = ((nblk + a.splits - 1) / a.splits) * kRowBlock;
-  const size_t smem = static_cast<size_t>(MB) * (ns_max + kRowBlock) * sizeof(float);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(layer_kernel<K, CB, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return EXL3_ERR_CUDA;
-  }
-  const dim3 grid(a.m / kRowBlock, a.splits);
-  layer_kernel<K, CB, MB><<<grid, kLayerThreads, smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
+  cfg.blockDim = dim3(kLayerThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, layer_kernel<K, CB, MB>, a) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
 

@@ -1,8 +1,8 @@
 // exl3_gemv_noalloc: the batch-1 fused layer for callers that cannot allocate
 // device memory.
 //
-// exl3_gemv needs a caller-provided workspace (split-K partial sums and
-// per-row-block arrival counters).  Some callers cannot provide one: code that
+// exl3_gemv needs a caller-provided workspace (arrival counters, fp32 row
+// sums and the rotated x).  Some callers cannot provide one: code that
 // runs where cudaMalloc is unavailable or forbidden (inside a host callback or
 // a custom allocator's own hooks, a plugin whose host framework owns every
 // allocation, a real-time loop that must never allocate).  This entry point
@@ -75,21 +75,20 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
       (s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out)))
     return EXL3_ERR_ALIGN;
 
-  const int splits = choose_splits(m, n, 1, device_sm_count());
-  const int nblk = n / kRowBlock;
-  const size_t xs_bytes = static_cast<size_t>((nblk + splits - 1) / splits) * kRowBlock * sizeof(float);
-  if (xs_bytes > kXsBudget) return EXL3_ERR_SHAPE;
-  const size_t need = counters_bytes(m) +
-                      (splits > 1 ? sizeof(float) * static_cast<size_t>(splits) * m : 0);
+  // Scratch layout as in the workspace of exl3_gemv at batch 1: counters
+  // (+ status word), fp32 row sums, rotated x.
+  const size_t need = xt_offset(m, 1) + sizeof(uint32_t) * static_cast<size_t>(n);
   if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
 
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != EXL3_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // The arrival counters must start at zero; the array keeps whatever the
-  // previous call left, so clear them on the stream first.
-  if (cudaMemsetAsync(scratch, 0, counters_bytes(m), cs) != cudaSuccess) return EXL3_ERR_CUDA;
+  // The row sums must start at zero; the array keeps whatever the previous
+  // call left, so clear them (and the counters) on the stream first.
+  if (cudaMemsetAsync(scratch, 0, xt_offset(m, 1), cs) != cudaSuccess) return EXL3_ERR_CUDA;
 
+  char* base = static_cast<char*>(scratch);
+  uint32_t* xt = reinterpret_cast<uint32_t*>(base + xt_offset(m, 1));
   LayerArgs a{};
   a.codes = codes;
   a.K = K;
@@ -101,8 +100,13 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   a.scales = reinterpret_cast<const __half*>(scales);
   a.x = reinterpret_cast<const __half*>(x);
   a.y = reinterpret_cast<__half*>(y);
-  a.counters = static_cast<uint32_t*>(scratch);
-  a.partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + counters_bytes(m));
-  a.splits = splits;
-  return launch_k(a, cs);
+  a.counters = reinterpret_cast<uint32_t*>(base);
+  a.zacc = reinterpret_cast<float*>(base + zacc_offset(m));
+  a.xt = xt;
+  a.ctas = choose_layer_ctas(m, n, 1, device_sm_count());
+  if ((st = launch_xt(a.x, a.s_in, xt, 1, n, codebook == EXL3_CB_1MAD ? kOneMadFactor : 1.0f, cs)) !=
+      EXL3_OK)
+    return st;
+  if ((st = launch_k(a, cs)) != EXL3_OK) return st;
+  return launch_epi(a.zacc, a.scales, a.s_out, a.y, 1, m, cs);
 }
