@@ -32,10 +32,18 @@ constexpr int kCb1Mad = 1;
 
 __device__ __forceinline__ uint32_t lcg(uint32_t s) { return s * kLcgMul + kLcgAdd; }
 
+// (x & k3InstMask) ^ k3InstMagic as one three-input logic instruction
+// (truth table 0x6A = (a & b) ^ c for a = 0xF0, b = 0xCC, c = 0xAA).
+__device__ __forceinline__ uint32_t mask_xor_3inst(uint32_t x) {
+  uint32_t h;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(h) : "r"(x), "r"(k3InstMask), "r"(k3InstMagic));
+  return h;
+}
+
 // 3INST: LCG, mask+XOR into two binary16 halves (one LOP3), one binary16 add
 // rounded to nearest even.
 __device__ __forceinline__ __half code_3inst(uint32_t s) {
-  const uint32_t h = (lcg(s) & k3InstMask) ^ k3InstMagic;
+  const uint32_t h = mask_xor_3inst(lcg(s));
   const __half lo = __ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu));
   const __half hi = __ushort_as_half(static_cast<unsigned short>(h >> 16));
   return __hadd(lo, hi);

@@ -22,8 +22,9 @@
 // CTA, warp w owns tile-row 8*rb + w of the segment's row block; lane
 // 8*jt + p handles every 4th tile (jt) and the row pair 2p, 2p+1 of the tile,
 // so each thread decodes 32 consecutive trellis steps from a word-aligned
-// window (the next tile's words are loaded before the current tile is
-// decoded).  Per column one packed binary16
+// window (code words are loaded two tiles ahead of their decode; the
+// segment's rotated x is staged in shared memory).  Per column one packed
+// binary16
 // FMA (HFMA2):
 //   3INST  acc += (lo, hi) * (x, x)   -- the two halves of the mask/XOR step,
 //          so lo*x + hi*x is the weight times x without a separate add;
@@ -47,6 +48,9 @@
 namespace exl3 {
 
 constexpr int kLayerThreads = 256;
+// Longest segment (tile columns) handled between two shared-memory refills of
+// the rotated x.
+constexpr int kSegTiles = 64;
 
 __device__ __forceinline__ void load_half4(const __half* p, float (&v)[4]) {
   const uint2 r = *reinterpret_cast<const uint2*>(p);
@@ -86,6 +90,7 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
   const long long u_begin = static_cast<long long>(blockIdx.x) * units / gridDim.x;
   const long long u_end = static_cast<long long>(blockIdx.x + 1) * units / gridDim.x;
   const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
+  __shared__ uint4 xs[MB * kSegTiles * 4];  // rotated x of the segment, [MB][tiles][4]
 
   // The rotated x is written by the preceding kernel on the stream.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -93,30 +98,39 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
   for (long long u = u_begin; u < u_end;) {
     const int rb = static_cast<int>(u / nt);
     const int ja = static_cast<int>(u - static_cast<long long>(rb) * nt);
-    const int jb = static_cast<int>(ja + (u_end - u) < nt ? ja + (u_end - u) : nt);
+    const long long left = u_end - u;
+    const int span = left < kSegTiles ? static_cast<int>(left) : kSegTiles;
+    const int jb = ja + span < nt ? ja + span : nt;
     const int I = rb * (kRowBlock / 16) + warp;
     const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
+
+    // Stage the segment's rotated x in shared memory (one barrier per segment).
+    __syncthreads();  // the previous segment's readers are done
+    for (int i = tid; i < MB * (jb - ja) * 4; i += kLayerThreads) {
+      const int b = i / ((jb - ja) * 4);
+      const int e = i - b * (jb - ja) * 4;  // uint4 index within the segment
+      xs[b * kSegTiles * 4 + e] =
+          __ldg(reinterpret_cast<const uint4*>(a.xt + static_cast<size_t>(b) * a.n + ja * 16) + e);
+    }
+    __syncthreads();
 
     float acc[MB][2];
 #pragma unroll
     for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
 
-    // The rotated x of the current tile is loaded first, the code words of the
-    // next tile before the current one is decoded.
+    // Code words are loaded two tiles ahead of their decode.
     int J = ja + jt;
-    uint32_t w[RowPair<K>::kPairWords];
-    if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);
+    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
+    if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
+    if (J + 4 < jb) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
     while (J < jb) {
-      uint4 xc[MB][4];
-#pragma unroll
-      for (int b = 0; b < MB; ++b)
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          xc[b][q] = __ldg(reinterpret_cast<const uint4*>(a.xt + static_cast<size_t>(b) * a.n + J * 16 + 4 * q));
       uint32_t st[32];
-      pair_states<K>(w, st);
+      pair_states<K>(w0, st);
+#pragma unroll
+      for (int i = 0; i < RowPair<K>::kPairWords; ++i) w0[i] = w1[i];
+      if (J + 8 < jb) load_row_pair<K>(rowp + static_cast<size_t>(J + 8) * kTw, p, w1);
+      const uint4* xrow = xs + (J - ja) * 4;
       J += 4;
-      if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w);  // prefetch
       __half2 ha[MB], hb[MB];
 #pragma unroll
       for (int b = 0; b < MB; ++b) {
@@ -127,15 +141,15 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
       for (int q = 0; q < 4; ++q) {
         uint4 xv[MB];
 #pragma unroll
-        for (int b = 0; b < MB; ++b) xv[b] = xc[b][q];
+        for (int b = 0; b < MB; ++b) xv[b] = xrow[b * kSegTiles * 4 + q];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = 4 * q + j;
           const uint32_t xa = lcg(st[c]);
           const uint32_t xb = lcg(st[16 + c]);
           if constexpr (CB == kCb3Inst) {
-            const uint32_t pa = (xa & k3InstMask) ^ k3InstMagic;
-            const uint32_t pb = (xb & k3InstMask) ^ k3InstMagic;
+            const uint32_t pa = mask_xor_3inst(xa);
+            const uint32_t pb = mask_xor_3inst(xb);
 #pragma unroll
             for (int b = 0; b < MB; ++b) {
               const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;

@@ -261,7 +261,7 @@ template <int CB>
 __device__ __forceinline__ uint32_t pair_code(uint32_t s) {
   const uint32_t x = lcg(s);
   if constexpr (CB == kCb3Inst) {
-    return (x & k3InstMask) ^ k3InstMagic;
+    return mask_xor_3inst(x);
   } else {
     return __dp4a(x, 0x01010101u, 0x6400u);  // binary16 bits of 1024 + S, high half +0
   }
