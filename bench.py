@@ -89,7 +89,7 @@ def workload(name: str, batch: int):
 def kernels_per_call(path: str, M: int) -> int:
     """Kernel launches of one exl3_gemm_small call: the tensor-core path is one
     persistent kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2
-    or 1 rows, the x-rotation, layer and epilogue kernels."""
+    or 1 rows, the layer kernel and the epilogue kernel."""
     tensor = path == "tensor" or (path == "auto" and M > 4)
     if tensor:
         return 1
@@ -98,7 +98,7 @@ def kernels_per_call(path: str, M: int) -> int:
         while rem >= c:
             rem -= c
             chunks += 1
-    return 3 * chunks
+    return 2 * chunks
 
 
 def algorithmic(m, n, K, cb, M):

@@ -108,8 +108,8 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
 
 /**
  * Bytes of scratch that exl3_gemv / exl3_gemm_small need for an m x n layer
- * at batch M (per-row-block arrival counters, fp32 row sums, the rotated x,
- * and the slice sums of the tensor-core kernel).
+ * at batch M (fp32 row sums, per-row-block counters and the slice sums of
+ * the tensor-core kernel).
  * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
  * once after allocation; every call leaves it zero-filled again.  Two calls
  * that may run concurrently must not share a workspace.  The uint32 at byte
@@ -170,9 +170,8 @@ exl3_status exl3_set_path(int path);
  * arguments minus the workspace.
  *   - Scratch: a file-scope device array of EXL3_NOALLOC_SCRATCH_BYTES bytes,
  *     present on every GPU that loads the library until the process exits.
- *     A layer whose scratch (arrival counters, m fp32 row sums and n words of
- *     rotated x) would not fit is rejected with EXL3_ERR_SCRATCH before
- *     anything is launched.
+ *     A layer whose scratch (m fp32 row sums and m/128 counters) would not
+ *     fit is rejected with EXL3_ERR_SCRATCH before anything is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

@@ -37,8 +37,7 @@ def _ws(m, n, M):
     a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
     counters = a256(4 * (m // 128 + 1))
     zacc = a256(4 * M * m)
-    xt = a256(4 * M * n)
-    return counters + zacc + xt + 4 * min(n // 128, 64) * M * m
+    return counters + zacc + 4 * min(n // 128, 64) * M * m
 
 
 def test_workspace_bytes(lib):

@@ -112,7 +112,7 @@ extern "C" exl3_status exl3_set_path(int path) {
 
 extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
-  return partials_offset(m, n, M) +
+  return partials_offset(m, M) +
          sizeof(float) * static_cast<size_t>(max_splits(n)) * static_cast<size_t>(M) * static_cast<size_t>(m);
 }
 
@@ -174,8 +174,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.counters = reinterpret_cast<uint32_t*>(ws);
   a.status = a.counters + m / kRowBlock;
   a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, n, M));
-  uint32_t* xt = reinterpret_cast<uint32_t*>(ws + xt_offset(m, M));
+  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, M));
   const int path = g_path.load(std::memory_order_relaxed);
   const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
   if (tensor) {
@@ -191,10 +190,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
     const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;
     a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
     a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
-    a.xt = xt;
     a.ctas = choose_layer_ctas(m, n, mb, sms);
-    if ((st = launch_xt(a.x, a.s_in, xt, mb, n, codebook == EXL3_CB_1MAD ? kOneMadFactor : 1.0f, cs)) != EXL3_OK)
-      return st;
     if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
     if ((st = launch_epi(a.zacc, a.scales, a.s_out, a.y, mb, m, cs)) != EXL3_OK) return st;
     done += mb;

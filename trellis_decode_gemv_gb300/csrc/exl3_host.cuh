@@ -12,9 +12,6 @@
 namespace exl3 {
 
 constexpr int kRowBlock = 128;      // rows per output block (one output FWHT)
-// 1/sqrt(21845) rounded to binary32: the 1MAD scale, applied to the rotated x
-// by the warp-shuffle path.
-constexpr float kOneMadFactor = 0x1.bb688cp-8f;
 constexpr int kMaxSplits = 64;      // cap on K-dimension slices of one layer
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -38,11 +35,9 @@ inline exl3_status launch_status() {
 int device_sm_count();
 
 // Workspace layout (all offsets 256-byte aligned):
-//   counters  one uint32 per 128-row block (tiles accumulated so far), then one
-//             status word (non-zero after a device-side wait timed out);
+//   counters  one uint32 per 128-row block, then one status word (non-zero
+//             after a device-side wait of the tensor-core kernel timed out);
 //   zacc      fp32 [M][m]: row sums accumulated by the warp-shuffle kernel;
-//   xt        uint32 [M][n]: the rotated x as binary16, duplicated in both
-//             halves (written by the x-rotation kernel of each call);
 //   partials  fp32 [slices][M][m]: slice sums of the tensor-core kernel.
 // counters and zacc must be zero before a call and are zero after it.
 inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
@@ -50,11 +45,8 @@ inline size_t counters_bytes(int m) {
   return align256(sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1));
 }
 inline size_t zacc_offset(int m) { return counters_bytes(m); }
-inline size_t xt_offset(int m, int M) {
+inline size_t partials_offset(int m, int M) {
   return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m);
-}
-inline size_t partials_offset(int m, int n, int M) {
-  return xt_offset(m, M) + align256(sizeof(uint32_t) * static_cast<size_t>(M) * n);
 }
 inline int max_splits(int n) {
   const int nblk = n / kRowBlock;
@@ -76,7 +68,6 @@ struct LayerArgs {
   __half* y;        // [mb][m]
   float* partials;    // tensor-core kernel: [splits][M][m]
   float* zacc;        // warp-shuffle kernel: [mb][m], zero on entry and exit
-  const uint32_t* xt; // warp-shuffle kernel: rotated x, duplicated binary16 [mb][n]
   uint32_t* counters;
   uint32_t* status;   // device-side error bits (tensor-core path), or nullptr
   int splits;         // tensor-core kernel: slices of the input dimension
@@ -88,10 +79,6 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
                        cudaStream_t stream);
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
                           cudaStream_t stream);
-// Rotated x for the warp-shuffle kernel: xt[b][c] = binary16(factor * Hb(s_in (.) x[b]))[c]
-// in both halves of a 32-bit word (no rotation when s_in is NULL).
-exl3_status launch_xt(const __half* x, const __half* s_in, uint32_t* xt, int rows, int n, float factor,
-                      cudaStream_t stream);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
 // per 128-row block (no rotation when s_out is NULL); zeroes zacc.
 exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,

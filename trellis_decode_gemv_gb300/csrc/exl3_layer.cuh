@@ -4,15 +4,12 @@
 // the fly from the bitshift-trellis codes of "Trellis Quantization" Parts
 // eight and nine; blockwise 128-point transforms of Part eleven).
 //
-// Each call runs three kernels on the stream, chained by programmatic
-// dependent launch (each starts while its predecessor runs and waits for it,
-// griddepcontrol.wait, before touching memory the predecessor writes):
-//  1. xt_kernel (csrc/exl3_rht_decode.cu) rotates x once: signs, 128-point FWHT
-//     across a warp, 1/sqrt(128), times the code's x factor, rounded to
-//     binary16 and stored duplicated in both halves of a 32-bit word;
-//  2. layer_kernel (below) accumulates W-hat x-tilde into the fp32 row sums
+// Each call runs two kernels on the stream, chained by programmatic dependent
+// launch (the second starts while the first runs and waits for it,
+// griddepcontrol.wait, before reading what it writes):
+//  1. layer_kernel (below) accumulates W-hat x-tilde into the fp32 row sums
 //     zacc with atomic adds;
-//  3. epi_kernel (csrc/exl3_rht_decode.cu) applies the scale, the output signs
+//  2. epi_kernel (csrc/exl3_rht_decode.cu) applies the scale, the output signs
 //     and the 128-point FWHT to each 128-row block of zacc, stores y as
 //     binary16 and zeroes zacc for the next call.
 //
@@ -22,9 +19,11 @@
 // CTA, warp w owns tile-row 8*rb + w of the segment's row block; lane
 // 8*jt + p handles every 4th tile (jt) and the row pair 2p, 2p+1 of the tile,
 // so each thread decodes 32 consecutive trellis steps from a word-aligned
-// window (code words are loaded two tiles ahead of their decode; the
-// segment's rotated x is staged in shared memory).  Per column one packed
-// binary16
+// window (code words are loaded two tiles ahead of their decode).  Each
+// segment starts by rotating the x columns it needs into shared memory (signs,
+// 128-point FWHT across a warp, 1/sqrt(128), times the code's x factor,
+// rounded to binary16, duplicated into both halves of a 32-bit word), one
+// warp per overlapping 128-block.  Per column one packed binary16
 // FMA (HFMA2):
 //   3INST  acc += (lo, hi) * (x, x)   -- the two halves of the mask/XOR step,
 //          so lo*x + hi*x is the weight times x without a separate add;
@@ -92,7 +91,7 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
   const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
   __shared__ uint4 xs[MB * kSegTiles * 4];  // rotated x of the segment, [MB][tiles][4]
 
-  // The rotated x is written by the preceding kernel on the stream.
+  // The previous call's epilogue zeroes zacc: wait for the preceding grid.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (long long u = u_begin; u < u_end;) {
@@ -104,13 +103,38 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
     const int I = rb * (kRowBlock / 16) + warp;
     const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
 
-    // Stage the segment's rotated x in shared memory (one barrier per segment).
+    // Rotate the x columns of the segment into shared memory: every 128-block
+    // that overlaps it, one warp per (batch row, block): signs, 128-point FWHT,
+    // 1/sqrt(128), the code's x factor, binary16, duplicated in both halves.
     __syncthreads();  // the previous segment's readers are done
-    for (int i = tid; i < MB * (jb - ja) * 4; i += kLayerThreads) {
-      const int b = i / ((jb - ja) * 4);
-      const int e = i - b * (jb - ja) * 4;  // uint4 index within the segment
-      xs[b * kSegTiles * 4 + e] =
-          __ldg(reinterpret_cast<const uint4*>(a.xt + static_cast<size_t>(b) * a.n + ja * 16) + e);
+    {
+      const int c_lo = ja * 16;
+      const int c_hi = jb * 16;
+      const int kb0 = c_lo / kRowBlock;
+      const int nkb = (c_hi - 1) / kRowBlock - kb0 + 1;
+      for (int job = warp; job < MB * nkb; job += kLayerThreads / 32) {
+        const int b = job / nkb;
+        const int col = (kb0 + job - b * nkb) * kRowBlock + 4 * lane;
+        float v[4];
+        load_half4(a.x + static_cast<size_t>(b) * a.n + col, v);
+        if (a.s_in != nullptr) {
+          float sg[4];
+          load_half4(a.s_in + col, sg);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] *= sg[j];
+          fwht128_warp(v, lane);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
+        }
+        if (col >= c_lo && col < c_hi) {
+          uint4 pk;
+          pk.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0] * x_factor<CB>()))) * 0x10001u;
+          pk.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1] * x_factor<CB>()))) * 0x10001u;
+          pk.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2] * x_factor<CB>()))) * 0x10001u;
+          pk.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3] * x_factor<CB>()))) * 0x10001u;
+          xs[b * kSegTiles * 4 + (col - c_lo) / 4] = pk;
+        }
+      }
     }
     __syncthreads();
 

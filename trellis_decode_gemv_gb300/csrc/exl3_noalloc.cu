@@ -1,8 +1,7 @@
 // exl3_gemv_noalloc: the batch-1 fused layer for callers that cannot allocate
 // device memory.
 //
-// exl3_gemv needs a caller-provided workspace (arrival counters, fp32 row
-// sums and the rotated x).  Some callers cannot provide one: code that
+// exl3_gemv needs a caller-provided workspace (fp32 row sums and counters).  Some callers cannot provide one: code that
 // runs where cudaMalloc is unavailable or forbidden (inside a host callback or
 // a custom allocator's own hooks, a plugin whose host framework owns every
 // allocation, a real-time loop that must never allocate).  This entry point
@@ -76,8 +75,8 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
     return EXL3_ERR_ALIGN;
 
   // Scratch layout as in the workspace of exl3_gemv at batch 1: counters
-  // (+ status word), fp32 row sums, rotated x.
-  const size_t need = xt_offset(m, 1) + sizeof(uint32_t) * static_cast<size_t>(n);
+  // (+ status word) and the fp32 row sums.
+  const size_t need = partials_offset(m, 1);
   if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
 
   void* scratch = nullptr;
@@ -85,10 +84,9 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The row sums must start at zero; the array keeps whatever the previous
   // call left, so clear them (and the counters) on the stream first.
-  if (cudaMemsetAsync(scratch, 0, xt_offset(m, 1), cs) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, need, cs) != cudaSuccess) return EXL3_ERR_CUDA;
 
   char* base = static_cast<char*>(scratch);
-  uint32_t* xt = reinterpret_cast<uint32_t*>(base + xt_offset(m, 1));
   LayerArgs a{};
   a.codes = codes;
   a.K = K;
@@ -102,11 +100,7 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   a.y = reinterpret_cast<__half*>(y);
   a.counters = reinterpret_cast<uint32_t*>(base);
   a.zacc = reinterpret_cast<float*>(base + zacc_offset(m));
-  a.xt = xt;
   a.ctas = choose_layer_ctas(m, n, 1, device_sm_count());
-  if ((st = launch_xt(a.x, a.s_in, xt, 1, n, codebook == EXL3_CB_1MAD ? kOneMadFactor : 1.0f, cs)) !=
-      EXL3_OK)
-    return st;
   if ((st = launch_k(a, cs)) != EXL3_OK) return st;
   return launch_epi(a.zacc, a.scales, a.s_out, a.y, 1, m, cs);
 }

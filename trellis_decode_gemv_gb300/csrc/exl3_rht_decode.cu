@@ -48,49 +48,6 @@ __global__ void __launch_bounds__(kThreads)
   *reinterpret_cast<uint2*>(out + row * d + col) = orr;
 }
 
-// Rotated x for the warp-shuffle layer kernel: one warp per 128-block,
-// xt = binary16(factor * Hb(s (.) x)) duplicated into both halves of a word.
-// Launched as a programmatic dependent of whatever precedes it on the stream
-// (typically the previous layer kernel, which may still read xt): it lets its
-// own dependent layer kernel launch at once, then waits for the preceding
-// grid before touching memory.  The layer kernel waits for this grid before
-// reading xt.
-__global__ void __launch_bounds__(kThreads)
-    xt_kernel(const __half* __restrict__ in, const __half* __restrict__ signs,
-              uint32_t* __restrict__ out, long long blocks, int d, float factor) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const long long job = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
-  if (job >= blocks) return;
-  const int per_row = d / kRowBlock;
-  const long long row = job / per_row;
-  const int kb = static_cast<int>(job - row * per_row);
-  const int col = kb * kRowBlock + 4 * lane;
-  const uint2 xr = *reinterpret_cast<const uint2*>(in + row * d + col);
-  const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
-  const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
-  float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-  if (signs != nullptr) {
-    const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
-    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-    v[0] *= __low2float(s01);
-    v[1] *= __high2float(s01);
-    v[2] *= __low2float(s23);
-    v[3] *= __high2float(s23);
-    fwht128_warp(v, lane);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
-  }
-  uint4 pk;
-  pk.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0] * factor))) * 0x10001u;
-  pk.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1] * factor))) * 0x10001u;
-  pk.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2] * factor))) * 0x10001u;
-  pk.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3] * factor))) * 0x10001u;
-  *reinterpret_cast<uint4*>(out + row * d + col) = pk;
-}
-
 // Epilogue of the warp-shuffle layer: one warp per (batch row, 128-row block):
 // y = binary16(Hb(s_out (.) (scale (.) zacc))) and zacc := 0.  Launched as a
 // programmatic dependent of the layer kernel; waits for it before reading.
@@ -188,25 +145,6 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
   const long long per_cta = kThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   rht_kernel<<<grid, kThreads, 0, stream>>>(in, signs, out, blocks, d);
-  return launch_status();
-}
-
-exl3_status launch_xt(const __half* x, const __half* s_in, uint32_t* xt, int rows, int n, float factor,
-                      cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(rows) * (n / kRowBlock);
-  const long long per_cta = kThreads / 32;
-  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, xt_kernel, x, s_in, xt, blocks, n, factor) != cudaSuccess)
-    return EXL3_ERR_CUDA;
   return launch_status();
 }
 
