@@ -282,10 +282,12 @@ def run_ours(args):
             B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                               c["scales"], c["x"], y=c["y"], workspace=ws)
 
+    # Decode work (weights, integer ops) does not grow with the batch; the
+    # multiply-accumulates do (macs = weights * M).
     alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M) for c in calls]
-    weights_step = sum(a[0] for a in alg) * M
+    weights_step = sum(a[0] for a in alg)
     bytes_step = sum(a[1] for a in alg)
-    ops_step = sum(a[2] for a in alg) * M
+    ops_step = sum(a[2] for a in alg)
     l2_note = (f"inputs larger than L2: {packed / 1e6:.0f} MB of packed codes per step "
                f"vs {L2_BYTES / 1e6:.0f} MB L2") if packed > L2_BYTES else "L2 NOT exceeded"
 
@@ -358,7 +360,7 @@ def run_ours(args):
     dur /= nrep
     t_kernel = dur.sum()
     t_hbm = np.array([a[1] / (hbm_gbs * 1e9) for a in alg])
-    t_int = np.array([a[2] * M / p_int for a in alg])
+    t_int = np.array([a[2] / p_int for a in alg])
     t_roof = np.maximum(t_hbm, t_int)
     bound = "alu" if t_int.sum() >= t_hbm.sum() else "hbm"
     if bound == "alu":
@@ -382,7 +384,7 @@ def run_ours(args):
         key = f"K{c['K']}.{'1mad' if c['cb'] else '3inst'}"
         e = per.setdefault(key, [0.0, 0, 0.0])
         e[0] += d
-        e[1] += a[0] * M
+        e[1] += a[0]
         e[2] += max(th, ti)
     per_summary = {k: {"weights_per_s": v[1] / v[0], "roofline_pct": 100 * v[2] / v[0]}
                    for k, v in sorted(per.items())}
@@ -436,6 +438,7 @@ def run_ours(args):
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
+            "macs_per_s": value * M,
             "roofline_pct": roof_pct,
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
