@@ -37,7 +37,8 @@ def _ws(m, n, M):
     a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
     counters = a256(4 * (m // 128 + 1))
     zacc = a256(4 * M * m)
-    return counters + zacc + 4 * min(n // 128, 64) * M * m
+    xr = a256(2 * M * n)
+    return counters + zacc + xr + 4 * min(n // 128, 64) * M * m
 
 
 def test_workspace_bytes(lib):

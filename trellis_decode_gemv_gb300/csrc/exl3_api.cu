@@ -112,7 +112,7 @@ extern "C" exl3_status exl3_set_path(int path) {
 
 extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
-  return partials_offset(m, M) +
+  return partials_offset(m, n, M) +
          sizeof(float) * static_cast<size_t>(max_splits(n)) * static_cast<size_t>(M) * static_cast<size_t>(m);
 }
 
@@ -174,7 +174,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.counters = reinterpret_cast<uint32_t*>(ws);
   a.status = a.counters + m / kRowBlock;
   a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, M));
+  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, n, M));
   const int path = g_path.load(std::memory_order_relaxed);
   const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
   if (tensor) {
@@ -183,6 +183,13 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
     const int ns = choose_tc_slice(m, n, M, sms);
     if (ns == 0) return EXL3_ERR_SHAPE;
     a.splits = n / ns;
+    if (a.s_in != nullptr) {
+      // Rotate x once for all work items; the kernel then only lays it out.
+      __half* xr = reinterpret_cast<__half*>(ws + xr_offset(m, M));
+      if ((st = launch_rht(a.x, a.s_in, xr, M, n, cs)) != EXL3_OK) return st;
+      a.x = xr;
+      a.s_in = nullptr;
+    }
     return launch_tc(a, M, ns, sms, cs);
   }
   for (int done = 0; done < M;) {

@@ -38,6 +38,7 @@ int device_sm_count();
 //   counters  one uint32 per 128-row block, then one status word (non-zero
 //             after a device-side wait of the tensor-core kernel timed out);
 //   zacc      fp32 [M][m]: row sums accumulated by the warp-shuffle kernel;
+//   xr        binary16 [M][n]: the rotated x of the tensor-core kernel;
 //   partials  fp32 [slices][M][m]: slice sums of the tensor-core kernel.
 // counters and zacc must be zero before a call and are zero after it.
 inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
@@ -45,8 +46,11 @@ inline size_t counters_bytes(int m) {
   return align256(sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1));
 }
 inline size_t zacc_offset(int m) { return counters_bytes(m); }
-inline size_t partials_offset(int m, int M) {
+inline size_t xr_offset(int m, int M) {
   return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m);
+}
+inline size_t partials_offset(int m, int n, int M) {
+  return xr_offset(m, M) + align256(sizeof(__half) * static_cast<size_t>(M) * n);
 }
 inline int max_splits(int n) {
   const int nblk = n / kRowBlock;

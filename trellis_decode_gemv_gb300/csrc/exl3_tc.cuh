@@ -6,15 +6,17 @@
 //  * Operand A (128 weight rows x K) lives in TMEM.  Each decode thread owns one
 //    weight row of a 128-row block (TMEM lane = row) and, per pipeline stage,
 //    decodes 32 consecutive weights of that row (one row of two adjacent 16x16
-//    tiles), writing one 32-bit TMEM column per weight with tcgen05.st.  The
-//    32-bit column holds a pair of binary16 values whose sum is the weight: for
-//    3INST the two halves straight out of the mask/XOR step ("Trellis
-//    Quantization" Part nine), for 1MAD the half 1024 + S (the dp4a byte sum
-//    spliced into the mantissa of 1024, the int-to-half trick of Part three)
-//    and +0.  So the MMA's K dimension is twice the weight count.
+//    tiles), writing two binary16 weights per 32-bit TMEM column with
+//    tcgen05.st (the lower half holds the even K element).  3INST weights are
+//    the binary16 sums of the two halves of the mask/XOR step ("Trellis
+//    Quantization" Part nine), formed for two columns at once by two byte
+//    permutes and one packed add -- exactly the defined binary16 weights; 1MAD
+//    weights are stored as the half 1024 + S (the dp4a byte sum spliced into
+//    the mantissa of 1024, the int-to-half trick of Part three), paired by one
+//    byte permute.
 //  * Operand B (K x N, N = batch padded to 16 or 32) is the rotated x slice in
-//    shared memory, each value duplicated along K to match the pairs, in the
-//    canonical K-major no-swizzle layout (8x16-byte core matrices).
+//    shared memory, binary16, in the canonical K-major no-swizzle layout
+//    (8x16-byte core matrices).
 //  * D (128 x N fp32) accumulates in TMEM.  For 1MAD, D = sum (1024 + S) x, so
 //    z = C (D - 1534 sum x) with C = 1/sqrt(21845).
 //
@@ -25,8 +27,9 @@
 //               2g, 2g+1 of every 8-tile-column chunk (a warp only reaches its
 //               own 32-lane quarter of TMEM, so the four warps of a warpgroup
 //               cover the 128 rows);
-//   warps 16-19 epilogue: build the duplicated x slice (B) of the next item
-//               (signs, 128-point FWHT across a warp, binary16) and finish the
+//   warps 16-19 epilogue: lay out the x slice (B) of the next item (the
+//               host rotates x once per call with the standalone transform
+//               kernel; these warps wait for it) and finish the
 //               previous item (tcgen05.ld of D, split-K partial sums + an atomic
 //               ticket per row block, and for the last slice the scale, output
 //               signs, FWHT and binary16 store);
@@ -60,10 +63,11 @@ __host__ __device__ constexpr int ring_depth() {
 }
 constexpr int kMaxRing = 8;
 constexpr int kSlots = 8;               // A stages in TMEM
-constexpr int kStageCols = 32;          // weights per row per stage (two tiles)
+constexpr int kStageWeights = 32;       // weights per row per stage (two tiles)
+constexpr int kStageCols = 16;          // TMEM columns per stage (two weights each)
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                // D buffers at columns 0 and 32
-constexpr int kACol = 64;               // A slots at 64 + 32 * slot
+constexpr int kACol = 64;               // A slots at 64 + 16 * slot
 constexpr int kRowPadWords = 16;        // keeps tile-row strips 64 B apart from a bank multiple
 constexpr uint32_t kSpinLimit = 1u << 20;  // about a second of try_wait polling
 constexpr int kEpiBarrier = 1;          // named barrier of the epilogue warps
@@ -155,15 +159,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -255,15 +256,24 @@ __device__ __forceinline__ void row_states(const uint32_t (&raw)[RowWords<K>::kR
   }
 }
 
-// 32-bit TMEM column of one weight: a pair of binary16 values summing to it
-// (the 1MAD value is offset by 1534 and unscaled; the epilogue corrects).
+// One 32-bit TMEM column: the binary16 values of two consecutive weights of a
+// row, the first in the lower half (the 1MAD values are offset by 1534 and
+// unscaled; the epilogue corrects).
 template <int CB>
-__device__ __forceinline__ uint32_t pair_code(uint32_t s) {
-  const uint32_t x = lcg(s);
+__device__ __forceinline__ uint32_t pack_two(uint32_t s0, uint32_t s1) {
+  const uint32_t x0 = lcg(s0);
+  const uint32_t x1 = lcg(s1);
   if constexpr (CB == kCb3Inst) {
-    return mask_xor_3inst(x);
+    const uint32_t h0 = mask_xor_3inst(x0);
+    const uint32_t h1 = mask_xor_3inst(x1);
+    const uint32_t lo = __byte_perm(h0, h1, 0x5410);  // (lo half of w0, lo half of w1)
+    const uint32_t hi = __byte_perm(h0, h1, 0x7632);  // (hi half of w0, hi half of w1)
+    const __half2 w = __hadd2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&hi));
+    return *reinterpret_cast<const uint32_t*>(&w);
   } else {
-    return __dp4a(x, 0x01010101u, 0x6400u);  // binary16 bits of 1024 + S, high half +0
+    const uint32_t d0 = __dp4a(x0, 0x01010101u, 0x6400u);  // binary16 bits of 1024 + S
+    const uint32_t d1 = __dp4a(x1, 0x01010101u, 0x6400u);
+    return __byte_perm(d0, d1, 0x5410);
   }
 }
 
@@ -315,14 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw + ctrl);
   constexpr int kRing = ring_depth<K>();
   unsigned char* bbuf = smem_raw + ctrl + static_cast<size_t>(kRing) * chunk_bytes<K>();
-  const size_t bbytes = static_cast<size_t>(NB) * 2 * p.ns * sizeof(__half);
+  const size_t bbytes = static_cast<size_t>(NB) * p.ns * sizeof(__half);
 
   const LayerArgs& a = p.a;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int tiles_per_row = a.n / 16;
-  const int nst_item = p.ns / kStageCols;
+  const int nst_item = p.ns / kStageWeights;
   const int nchunk_item = p.ns / (kChunkTiles * 16);
   // items of this CTA: blockIdx.x + i * gridDim.x
   const int my_items = p.items > static_cast<int>(blockIdx.x)
@@ -429,11 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         uint32_t st0[16], st1[16];
         row_states<K>(raw0, off, st0);
         row_states<K>(raw1, off, st1);
-        uint32_t v[32];
+        uint32_t v[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          v[c] = pair_code<CB>(st0[c]);
-          v[16 + c] = pair_code<CB>(st1[c]);
+        for (int c = 0; c < 16; c += 2) {
+          v[c / 2] = pack_two<CB>(st0[c], st0[c + 1]);
+          v[8 + c / 2] = pack_two<CB>(st1[c], st1[c + 1]);
         }
         const int gs = 4 * seq + g;  // global stage index of this CTA
         const int aslot = gs % kSlots;
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
           stop = true;
           break;
         }
-        tmem_st32(lane_addr + kACol + aslot * kStageCols, v);
+        tmem_st16(lane_addr + kACol + aslot * kStageCols, v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -481,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
           }
           tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t kk = static_cast<uint32_t>(s) * 64u + 16u * j;  // K offset (halves)
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t kk = static_cast<uint32_t>(s) * kStageWeights + 16u * j;  // K offset
             const uint64_t bd = smem_desc(bbase + (kk / 8) * kLbo, kLbo, kSbo);
             mma_f16_ts(tmem + kDCol + 32 * db, tmem + kACol + aslot * kStageCols + 8 * j, bd, idesc,
                        (s > 0 || j > 0) ? 1u : 0u);
@@ -500,6 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     const int ew = warp - kEpiWarp0;  // 0..3 = TMEM lane quarter
     const int et = tid - kEpiWarp0 * 32;  // 0..127
     const int nkb = p.ns / kRowBlock;
+    // x may be written by the preceding kernel on the stream (the rotation).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int li = 0; li <= my_items; ++li) {
       // Uniform go/stop decision for the four epilogue warps: they share named
       // barriers, so they must leave together.
@@ -550,15 +562,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
             hs += __half2float(h[j]);
           }
           // element (n, k) at ((k/8) * (NB/8) + n/8) * 128 + (n%8) * 16 + (k%8) * 2;
-          // these four values are k = 8 * kc .. 8 * kc + 7 (each twice).
-          const int kc = kb * 32 + lane;
-          const uint32_t o = (static_cast<uint32_t>(kc) * (NB / 8) + n / 8) * 128u + (n % 8) * 16u;
-          uint4 pk;
-          pk.x = static_cast<uint32_t>(__half_as_ushort(h[0])) * 0x10001u;
-          pk.y = static_cast<uint32_t>(__half_as_ushort(h[1])) * 0x10001u;
-          pk.z = static_cast<uint32_t>(__half_as_ushort(h[2])) * 0x10001u;
-          pk.w = static_cast<uint32_t>(__half_as_ushort(h[3])) * 0x10001u;
-          *reinterpret_cast<uint4*>(bsm + o) = pk;
+          // these four values are k = kb*128 + 4*lane .. +3.
+          const int kc = kb * 16 + lane / 2;
+          const uint32_t o = (static_cast<uint32_t>(kc) * (NB / 8) + n / 8) * 128u + (n % 8) * 16u +
+                             (lane % 2) * 8u;
+          uint2 pk;
+          pk.x = static_cast<uint32_t>(__half_as_ushort(h[0])) |
+                 (static_cast<uint32_t>(__half_as_ushort(h[1])) << 16);
+          pk.y = static_cast<uint32_t>(__half_as_ushort(h[2])) |
+                 (static_cast<uint32_t>(__half_as_ushort(h[3])) << 16);
+          *reinterpret_cast<uint2*>(bsm + o) = pk;
           if (CB == kCb1Mad) {
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
@@ -684,12 +697,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   if (tid == 0 && aborted(sh) && a.status != nullptr) atomicOr(a.status, 1u);
 }
 
-// Shared memory: control block + code ring + two B buffers (NB x 2ns halves).
+// Shared memory: control block + code ring + two B buffers (NB x ns halves).
 template <int K>
 inline size_t tc_smem_bytes(int nb, int ns) {
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
   return ctrl + static_cast<size_t>(ring_depth<K>()) * chunk_bytes<K>() +
-         2 * static_cast<size_t>(nb) * 2 * ns * sizeof(__half);
+         2 * static_cast<size_t>(nb) * ns * sizeof(__half);
 }
 
 template <int K, int CB, int NB>
@@ -708,7 +721,17 @@ exl3_status launch_tc_t(const LayerArgs& a, int M, int ns, int grid, cudaStream_
                            static_cast<int>(smem)) != cudaSuccess)
     return EXL3_ERR_CUDA;
   if (grid > p.items) grid = p.items;
-  tc_layer_kernel<K, CB, NB><<<grid, kThreads, smem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tc_layer_kernel<K, CB, NB>, p) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
 
