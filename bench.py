@@ -87,12 +87,13 @@ def workload(name: str, batch: int):
 
 
 def kernels_per_call(path: str, M: int) -> int:
-    """Kernel launches of one exl3_gemm_small call: the tensor-core path is one
-    persistent kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2
-    or 1 rows, the layer kernel and the epilogue kernel."""
+    """Kernel launches of one exl3_gemm_small call: the tensor-core path runs
+    the operand-image kernel, the persistent MMA kernel and the epilogue
+    kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2 or 1 rows,
+    the layer kernel and the epilogue kernel."""
     tensor = path == "tensor" or (path == "auto" and M > 4)
     if tensor:
-        return 1
+        return 3
     chunks, rem = 0, M
     for c in (8, 4, 2, 1):
         while rem >= c:

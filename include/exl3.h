@@ -108,8 +108,9 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
 
 /**
  * Bytes of scratch that exl3_gemv / exl3_gemm_small need for an m x n layer
- * at batch M (fp32 row sums, per-row-block counters and the slice sums of
- * the tensor-core kernel).
+ * at batch M: per-row-block counters and the status word, M*m fp32 row sums,
+ * and for the tensor-core kernel the rotated input laid out as its MMA
+ * operand (16 or 32 rows of n halves) with M*(n/128) fp32 block sums.
  * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
  * once after allocation; every call leaves it zero-filled again.  Two calls
  * that may run concurrently must not share a workspace.  The uint32 at byte

@@ -37,8 +37,10 @@ def _ws(m, n, M):
     a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
     counters = a256(4 * (m // 128 + 1))
     zacc = a256(4 * M * m)
-    xr = a256(2 * M * n)
-    return counters + zacc + xr + 4 * min(n // 128, 64) * M * m
+    nb = 16 if M <= 16 else 32
+    bimg = a256(2 * nb * n)
+    bsum = a256(4 * M * (n // 128))
+    return counters + zacc + bimg + bsum
 
 
 def test_workspace_bytes(lib):

@@ -87,3 +87,27 @@ def test_tc_matches_shuffle_path():
     B.exl3_set_path(B.PATH_SHUFFLE)
     y_sh = _run(inp, K, cb, m, n, 1)
     assert_layer_close(y_tc, y_sh.double().cpu().numpy())
+
+
+def test_tc_workspace_reuse_and_row_sums_cleared():
+    """Two calls in a row on one workspace agree within one binary16 rounding
+    (fp32 reductions land in any order) and leave the row sums at zero; the
+    1024 x 4096 layer has 256 chunks, so the work ranges of the 152-CTA grid
+    straddle row blocks."""
+    m, n, K, cb, M = 1024, 4096, 3, 1, 5
+    inp = synth.layer_inputs(m, n, K, M, config=85, index=0)
+    d = upload(inp)
+    ws = B.alloc_workspace(m, n, M, "cuda")
+    ys = []
+    for _ in range(2):
+        y = torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")
+        B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"],
+                          y=y, workspace=ws)
+        torch.cuda.synchronize()
+        ys.append(y)
+    assert B.workspace_status(ws, m) == 0
+    diff = (ys[0].float() - ys[1].float()).abs()
+    assert float(diff.max()) <= 2.0 ** -9 * float(ys[0].float().abs().max())
+    zacc = ws[256:256 + 4 * M * m].view(torch.float32)
+    assert float(zacc.abs().sum()) == 0.0
+    assert_layer_close(ys[1], _ref(inp, K, cb, m, n), "second call")

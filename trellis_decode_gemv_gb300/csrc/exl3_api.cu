@@ -29,38 +29,21 @@ int choose_layer_ctas(int m, int n, int mb, int sm_count) {
   return ctas < 1 ? 1 : static_cast<int>(ctas);
 }
 
-int choose_tc_slice(int m, int n, int M, int sm_count) {
-  const int rowblocks = m / kRowBlock;
-  const int cap = M <= 16 ? 1024 : 512;
-  int best = 0;
-  double best_eff = -1.0;
-  for (int ns = cap; ns >= kRowBlock; ns /= 2) {
-    if (n % ns != 0 || n / ns > kMaxSplits) continue;
-    const long long items = static_cast<long long>(rowblocks) * (n / ns);
-    const long long rounds = (items + sm_count - 1) / sm_count;
-    const double eff = static_cast<double>(items) / static_cast<double>(rounds * sm_count);
-    if (eff > best_eff + 0.05) {
-      best_eff = eff;
-      best = ns;
-    }
-  }
-  return best;  // 0: no admissible slice (n needs more than kMaxSplits slices)
-}
-
 namespace {
 
 std::atomic<int> g_path{EXL3_PATH_AUTO};
 
-exl3_status launch_tc(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream) {
+exl3_status launch_tc(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                      cudaStream_t stream) {
   switch (a.K) {
-    case 1: return launch_tc_k1(a, M, ns, grid, stream);
-    case 2: return launch_tc_k2(a, M, ns, grid, stream);
-    case 3: return launch_tc_k3(a, M, ns, grid, stream);
-    case 4: return launch_tc_k4(a, M, ns, grid, stream);
-    case 5: return launch_tc_k5(a, M, ns, grid, stream);
-    case 6: return launch_tc_k6(a, M, ns, grid, stream);
-    case 7: return launch_tc_k7(a, M, ns, grid, stream);
-    case 8: return launch_tc_k8(a, M, ns, grid, stream);
+    case 1: return launch_tc_k1(a, bimg, bsum, M, grid, stream);
+    case 2: return launch_tc_k2(a, bimg, bsum, M, grid, stream);
+    case 3: return launch_tc_k3(a, bimg, bsum, M, grid, stream);
+    case 4: return launch_tc_k4(a, bimg, bsum, M, grid, stream);
+    case 5: return launch_tc_k5(a, bimg, bsum, M, grid, stream);
+    case 6: return launch_tc_k6(a, bimg, bsum, M, grid, stream);
+    case 7: return launch_tc_k7(a, bimg, bsum, M, grid, stream);
+    case 8: return launch_tc_k8(a, bimg, bsum, M, grid, stream);
     default: return EXL3_ERR_K;
   }
 }
@@ -112,8 +95,7 @@ extern "C" exl3_status exl3_set_path(int path) {
 
 extern "C" size_t exl3_workspace_bytes(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1 || M > EXL3_MAX_BATCH) return 0;
-  return partials_offset(m, n, M) +
-         sizeof(float) * static_cast<size_t>(max_splits(n)) * static_cast<size_t>(M) * static_cast<size_t>(m);
+  return workspace_total(m, n, M);
 }
 
 extern "C" exl3_status exl3_rht_in(const exl3_half* x, const exl3_half* s_in, exl3_half* x_rot,
@@ -174,23 +156,20 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.counters = reinterpret_cast<uint32_t*>(ws);
   a.status = a.counters + m / kRowBlock;
   a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  a.partials = reinterpret_cast<float*>(ws + partials_offset(m, n, M));
   const int path = g_path.load(std::memory_order_relaxed);
   const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
   if (tensor) {
-    a.x = reinterpret_cast<const __half*>(x);
+    // x-tilde as operand-B images (and, for 1MAD, its block sums), then the
+    // persistent tensor-core kernel into zacc, then the output transform; the
+    // last two are programmatic dependents of the kernel before them.
+    __half* bimg = reinterpret_cast<__half*>(ws + bimg_offset(m, M));
+    float* bsum = codebook == EXL3_CB_1MAD ? reinterpret_cast<float*>(ws + bsum_offset(m, n, M)) : nullptr;
     a.y = reinterpret_cast<__half*>(y);
-    const int ns = choose_tc_slice(m, n, M, sms);
-    if (ns == 0) return EXL3_ERR_SHAPE;
-    a.splits = n / ns;
-    if (a.s_in != nullptr) {
-      // Rotate x once for all work items; the kernel then only lays it out.
-      __half* xr = reinterpret_cast<__half*>(ws + xr_offset(m, M));
-      if ((st = launch_rht(a.x, a.s_in, xr, M, n, cs)) != EXL3_OK) return st;
-      a.x = xr;
-      a.s_in = nullptr;
-    }
-    return launch_tc(a, M, ns, sms, cs);
+    if ((st = launch_bimg(reinterpret_cast<const __half*>(x), a.s_in, bimg, bsum, M, tc_nb(M), n, cs)) !=
+        EXL3_OK)
+      return st;
+    if ((st = launch_tc(a, bimg, bsum, M, sms, cs)) != EXL3_OK) return st;
+    return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, m, cs);
   }
   for (int done = 0; done < M;) {
     const int rem = M - done;

@@ -12,7 +12,6 @@
 namespace exl3 {
 
 constexpr int kRowBlock = 128;      // rows per output block (one output FWHT)
-constexpr int kMaxSplits = 64;      // cap on K-dimension slices of one layer
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -37,24 +36,27 @@ int device_sm_count();
 // Workspace layout (all offsets 256-byte aligned):
 //   counters  one uint32 per 128-row block, then one status word (non-zero
 //             after a device-side wait of the tensor-core kernel timed out);
-//   zacc      fp32 [M][m]: row sums accumulated by the warp-shuffle kernel;
-//   xr        binary16 [M][n]: the rotated x of the tensor-core kernel;
-//   partials  fp32 [slices][M][m]: slice sums of the tensor-core kernel.
+//   zacc      fp32 [M][m]: row sums accumulated by the layer kernels;
+//   bimg      binary16: the rotated x laid out as the tensor-core kernel's
+//             operand B, one (tc_nb(M) x 128) image per 128 input columns;
+//   bsum      fp32 [M][n/128]: sums of the binary16 rotated x per 128 block
+//             (1MAD correction of the tensor-core kernel).
 // counters and zacc must be zero before a call and are zero after it.
 inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+// Batch columns of the tensor-core MMAs (N of the 128 x N x 16 shape).
+inline int tc_nb(int M) { return M <= 16 ? 16 : 32; }
 inline size_t counters_bytes(int m) {
   return align256(sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1));
 }
 inline size_t zacc_offset(int m) { return counters_bytes(m); }
-inline size_t xr_offset(int m, int M) {
+inline size_t bimg_offset(int m, int M) {
   return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m);
 }
-inline size_t partials_offset(int m, int n, int M) {
-  return xr_offset(m, M) + align256(sizeof(__half) * static_cast<size_t>(M) * n);
+inline size_t bsum_offset(int m, int n, int M) {
+  return bimg_offset(m, M) + align256(sizeof(__half) * static_cast<size_t>(tc_nb(M)) * n);
 }
-inline int max_splits(int n) {
-  const int nblk = n / kRowBlock;
-  return nblk < kMaxSplits ? nblk : kMaxSplits;
+inline size_t workspace_total(int m, int n, int M) {
+  return bsum_offset(m, n, M) + align256(sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock));
 }
 
 // Number of CTAs of the warp-shuffle kernel at batch chunk mb: one wave (5,
@@ -70,17 +72,21 @@ struct LayerArgs {
   const __half* scales;
   const __half* x;  // [mb][n]
   __half* y;        // [mb][m]
-  float* partials;    // tensor-core kernel: [splits][M][m]
-  float* zacc;        // warp-shuffle kernel: [mb][m], zero on entry and exit
+  float* zacc;        // [mb][m] fp32 row sums, zero on entry and exit
   uint32_t* counters;
   uint32_t* status;   // device-side error bits (tensor-core path), or nullptr
-  int splits;         // tensor-core kernel: slices of the input dimension
   int ctas;           // warp-shuffle kernel: grid size
 };
 
 // Internal launchers (one translation unit per K for the layer kernels).
 exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int rows, int d,
                        cudaStream_t stream);
+// Operand images of the tensor-core kernel: for every 128-column block kb of
+// x-tilde = Hb(s_in (.) x) (x itself when s_in is NULL), the nb x 128 binary16
+// K-major image at bimg + kb * nb * 128 (rows M..nb-1 zero), and for bsum !=
+// NULL the fp32 sums bsum[b * (n/128) + kb] of the binary16 values.
+exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
+                        int nb, int n, cudaStream_t stream);
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
                           cudaStream_t stream);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
@@ -95,20 +101,21 @@ exl3_status launch_layer_k5(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k6(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k7(const LayerArgs& a, int mb, cudaStream_t stream);
 exl3_status launch_layer_k8(const LayerArgs& a, int mb, cudaStream_t stream);
-exl3_status launch_tc_k1(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k2(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k3(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k4(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k5(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k6(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k7(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-exl3_status launch_tc_k8(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream);
-
-// Work split of the persistent tensor-core kernel: the slice width ns (a
-// divisor of n, a power of two times 128, at most 1024 columns for batches up
-// to 16 and 512 above, at most kMaxSplits slices) that best balances the
-// (m/128) * (n/ns) work items over the resident CTAs (one per SM), preferring
-// wider slices when the balance is within 5%.
-int choose_tc_slice(int m, int n, int M, int sm_count);
+exl3_status launch_tc_k1(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k2(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k3(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k4(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k5(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k6(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k7(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
+exl3_status launch_tc_k8(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                          cudaStream_t stream);
 
 }  // namespace exl3

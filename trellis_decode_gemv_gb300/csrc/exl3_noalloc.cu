@@ -76,7 +76,7 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
 
   // Scratch layout as in the workspace of exl3_gemv at batch 1: counters
   // (+ status word) and the fp32 row sums.
-  const size_t need = xr_offset(m, 1);
+  const size_t need = bimg_offset(m, 1);
   if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
 
   void* scratch = nullptr;

@@ -48,6 +48,59 @@ __global__ void __launch_bounds__(kThreads)
   *reinterpret_cast<uint2*>(out + row * d + col) = orr;
 }
 
+// Operand B images of the tensor-core layer kernel.  One warp per (batch row
+// r < nb, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
+// itself without s_in), rounded to binary16 and stored in the canonical
+// K-major no-swizzle layout of an nb x 128 operand: element (r, k) at half
+// offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + k % 8 of the
+// block's image.  Rows r >= M are zero.  With bsum, also the fp32 sum of the
+// block's binary16 values.  The layer kernel is a programmatic dependent of
+// this one and waits for it before reading the images.
+__global__ void __launch_bounds__(kThreads)
+    bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
+                __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int nkb = n / kRowBlock;
+  const long long job = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  if (job >= static_cast<long long>(nb) * nkb) return;
+  const int r = static_cast<int>(job / nkb);
+  const int kb = static_cast<int>(job - static_cast<long long>(r) * nkb);
+  uint2 o = make_uint2(0u, 0u);
+  if (r < M) {
+    const int col = kb * kRowBlock + 4 * lane;
+    const uint2 xr = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(r) * n + col);
+    if (signs != nullptr) {
+      const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+      const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+      const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+      float v[4] = {__low2float(x01) * __low2float(s01), __high2float(x01) * __high2float(s01),
+                    __low2float(x23) * __low2float(s23), __high2float(x23) * __high2float(s23)};
+      fwht128_warp(v, lane);
+      const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
+      const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
+      o.x = *reinterpret_cast<const uint32_t*>(&o01);
+      o.y = *reinterpret_cast<const uint32_t*>(&o23);
+    } else {
+      o = xr;
+    }
+    if (bsum != nullptr) {
+      const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
+      const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
+      float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
+      if (lane == 0) bsum[static_cast<size_t>(r) * nkb + kb] = hs;
+    }
+  }
+  // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
+  const size_t off = static_cast<size_t>(kb) * nb * kRowBlock +
+                     (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
+  *reinterpret_cast<uint2*>(bimg + off) = o;
+}
+
 // Epilogue of the warp-shuffle layer: one warp per (batch row, 128-row block):
 // y = binary16(Hb(s_out (.) (scale (.) zacc))) and zacc := 0.  Launched as a
 // programmatic dependent of the layer kernel; waits for it before reading.
@@ -145,6 +198,15 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
   const long long per_cta = kThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   rht_kernel<<<grid, kThreads, 0, stream>>>(in, signs, out, blocks, d);
+  return launch_status();
+}
+
+exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
+                        int nb, int n, cudaStream_t stream) {
+  const long long blocks = static_cast<long long>(nb) * (n / kRowBlock);
+  const long long per_cta = kThreads / 32;
+  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
+  bimg_kernel<<<grid, kThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
 }
 

@@ -1,47 +1,53 @@
 // Fused layer kernel, tensor-core path (tcgen05, sm_103a):
-//   y = Hb(s_out (.) (scale (.) (W-hat Hb(s_in (.) x))))   for 1 <= M <= 32.
+//   z = W-hat x-tilde   for 1 <= M <= 32 batch rows,
+// accumulated in fp32 into the workspace row sums; the input transform
+// (x-tilde = Hb(s_in (.) x), laid out as operand B) runs before it and the
+// output transform (y = Hb(s_out (.) (scale (.) z))) after it, both chained by
+// programmatic dependent launch.
 //
 // The decoded 16x16 tiles feed tcgen05 MMAs directly from tensor memory:
 //
-//  * Operand A (128 weight rows x K) lives in TMEM.  Each decode thread owns one
-//    weight row of a 128-row block (TMEM lane = row) and, per pipeline stage,
-//    decodes 32 consecutive weights of that row (one row of two adjacent 16x16
-//    tiles), writing two binary16 weights per 32-bit TMEM column with
-//    tcgen05.st (the lower half holds the even K element).  3INST weights are
-//    the binary16 sums of the two halves of the mask/XOR step ("Trellis
-//    Quantization" Part nine), formed for two columns at once by two byte
-//    permutes and one packed add -- exactly the defined binary16 weights; 1MAD
-//    weights are stored as the half 1024 + S (the dp4a byte sum spliced into
-//    the mantissa of 1024, the int-to-half trick of Part three), paired by one
-//    byte permute.
-//  * Operand B (K x N, N = batch padded to 16 or 32) is the rotated x slice in
-//    shared memory, binary16, in the canonical K-major no-swizzle layout
-//    (8x16-byte core matrices).
-//  * D (128 x N fp32) accumulates in TMEM.  For 1MAD, D = sum (1024 + S) x, so
-//    z = C (D - 1534 sum x) with C = 1/sqrt(21845).
+//  * Operand A (128 weight rows x 128) lives in TMEM.  Each decode thread owns
+//    one weight row of a 128-row block (TMEM lane = row) and, per 128-column
+//    chunk, decodes 32 consecutive weights of that row (one row of two
+//    adjacent 16x16 tiles), writing two binary16 weights per 32-bit TMEM
+//    column with tcgen05.st (the lower half holds the even K element).  3INST
+//    weights are the binary16 sums of the two halves of the mask/XOR step
+//    ("Trellis Quantization" Part nine), formed for two columns at once by two
+//    byte permutes and one packed add -- exactly the defined binary16
+//    weights; 1MAD weights are stored as the half 1024 + S (the dp4a byte sum
+//    spliced into the mantissa of 1024, the int-to-half trick of Part three),
+//    paired by one byte permute.
+//  * Operand B (128 x N, N = batch padded to 16 or 32) is the chunk's slice of
+//    x-tilde, binary16, in the canonical K-major no-swizzle layout (8x16-byte
+//    core matrices), fetched as one contiguous bulk copy per chunk.
+//  * D (128 x N fp32) accumulates in TMEM over a run of chunks of one 128-row
+//    block.  For 1MAD, D = sum (1024 + S) x, so z = C (D - 1534 sum x) with
+//    C = 1/sqrt(21845); the sums of x per 128 block come with operand B.
 //
-// Persistent kernel, one CTA per SM.  Work item = one 128-row output block x
-// one slice of the input dimension (a multiple of 128 columns); CTA b takes
-// items b, b + gridDim.x, ...  Warp roles:
+// Persistent kernel, one CTA per SM, stream-K work split: the (m/128) x
+// (n/128) chunks, row-block major, are cut into gridDim.x contiguous ranges;
+// the chunks of one range that share a row block form a run, whose D the
+// epilogue adds into the row sums with fp32 reductions.  Warp roles:
 //   warps 0-15  decode: four warpgroups; warpgroup g decodes tile columns
-//               2g, 2g+1 of every 8-tile-column chunk (a warp only reaches its
-//               own 32-lane quarter of TMEM, so the four warps of a warpgroup
-//               cover the 128 rows);
-//   warps 16-19 epilogue: lay out the x slice (B) of the next item (the
-//               host rotates x once per call with the standalone transform
-//               kernel; these warps wait for it) and finish the
-//               previous item (tcgen05.ld of D, split-K partial sums + an atomic
-//               ticket per row block, and for the last slice the scale, output
-//               signs, FWHT and binary16 store);
-//   warp 20     MMA issue (one lane) and TMEM allocation;
-//   warp 21     producer: 1-D bulk copies (cp.async.bulk) of each chunk's eight
-//               tile-row strips of packed codes (one lane per strip) into a
-//               4- or 8-deep shared-memory ring.
-// mbarriers: ring full/empty (codes), A full/empty (8 TMEM slots), B full (2
-// buffers), D full/empty (2 TMEM accumulators).  Every wait is bounded: on
-// timeout the thread sets the CTA's abort flag and the workspace status word,
-// every role stops, the producer waits (bounded) for its copies in flight, the
-// MMA lane for its MMAs, TMEM is freed and the CTA exits.
+//               2g, 2g+1 of every chunk (a warp only reaches its own 32-lane
+//               quarter of TMEM, so the four warps of a warpgroup cover the
+//               128 rows);
+//   warps 16-19 epilogue: tcgen05.ld of each run's D, 1MAD correction,
+//               reduction into the row sums;
+//   warp 20     MMA issue (one lane, 8 MMAs of 128 x N x 16 per chunk) and
+//               TMEM allocation;
+//   warp 21     code producer: 1-D bulk copies (cp.async.bulk) of each
+//               chunk's eight tile-row strips of packed codes (one lane per
+//               strip) into a 4- or 8-deep shared-memory ring;
+//   warp 22     operand-B producer: waits for the preceding transform kernel,
+//               then one bulk copy per chunk into a ring slot paired with the
+//               chunk's TMEM slot.
+// mbarriers: code ring full/empty, A full/empty and B full (6 chunk slots),
+// D full/empty (2 TMEM accumulators).  Every wait is bounded: on timeout the
+// thread sets the CTA's abort flag and the workspace status word, every role
+// stops, the producers wait (bounded) for their copies in flight, the MMA lane
+// for its MMAs, TMEM is freed and the CTA exits.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -54,20 +60,21 @@ constexpr int kDecodeWarps = 16;
 constexpr int kEpiWarp0 = 16;
 constexpr int kMmaWarp = 20;
 constexpr int kTmaWarp = 21;
-constexpr int kThreads = 22 * 32;
-constexpr int kChunkTiles = 8;          // tile columns per code chunk (128 columns)
+constexpr int kBWarp = 22;
+constexpr int kThreads = 23 * 32;
+constexpr int kChunkTiles = 8;          // tile columns per chunk (128 columns)
+constexpr int kChunkK = kChunkTiles * 16;
 // Code chunks in flight: 8 for K <= 4, 4 above (shared-memory budget).
 template <int K>
 __host__ __device__ constexpr int ring_depth() {
   return K <= 4 ? 8 : 4;
 }
 constexpr int kMaxRing = 8;
-constexpr int kSlots = 8;               // A stages in TMEM
-constexpr int kStageWeights = 32;       // weights per row per stage (two tiles)
-constexpr int kStageCols = 16;          // TMEM columns per stage (two weights each)
+constexpr int kSlots = 6;               // chunks of A in TMEM (and of B in shared memory)
+constexpr int kChunkCols = 64;          // TMEM columns per chunk (two weights each)
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                // D buffers at columns 0 and 32
-constexpr int kACol = 64;               // A slots at 64 + 16 * slot
+constexpr int kACol = 64;               // A slots at 64 + 64 * slot
 constexpr int kRowPadWords = 16;        // keeps tile-row strips 64 B apart from a bank multiple
 constexpr uint32_t kSpinLimit = 1u << 20;  // about a second of try_wait polling
 constexpr int kEpiBarrier = 1;          // named barrier of the epilogue warps
@@ -279,10 +286,9 @@ __device__ __forceinline__ uint32_t pack_two(uint32_t s0, uint32_t s1) {
 
 struct TcParams {
   LayerArgs a;
+  const __half* bimg;  // operand-B images, one per 128-column block
+  const float* bsum;   // [M][n/128] sums of x-tilde (1MAD), else unused
   int M;
-  int ns;          // slice width (columns), multiple of 128
-  int nslices;     // n / ns
-  int items;       // (m / 128) * nslices
 };
 
 struct TcShared {
@@ -290,16 +296,14 @@ struct TcShared {
   uint64_t ring_empty[kMaxRing];
   uint64_t a_full[kSlots];
   uint64_t a_empty[kSlots];
-  uint64_t b_full[2];
+  uint64_t b_full[kSlots];
   uint64_t d_full[2];
   uint64_t d_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t ticket;
   uint32_t epi_go;
-  float xsum[2][32];
-  float zs[32 * 128];
+  float xsum[32];
 };
 
 template <int K>
@@ -309,6 +313,10 @@ __host__ __device__ constexpr int chunk_row_words() {
 template <int K>
 __host__ __device__ constexpr int chunk_bytes() {
   return 8 * chunk_row_words<K>() * 4;
+}
+template <int NB>
+__host__ __device__ constexpr int bchunk_bytes() {
+  return NB * kChunkK * 2;
 }
 
 __device__ __forceinline__ bool aborted(const TcShared& sh) {
@@ -322,22 +330,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   TcShared& sh = *reinterpret_cast<TcShared*>(smem_raw);
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
-  uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw + ctrl);
+  unsigned char* bring = smem_raw + ctrl;
+  uint32_t* ring = reinterpret_cast<uint32_t*>(bring + static_cast<size_t>(kSlots) * bchunk_bytes<NB>());
   constexpr int kRing = ring_depth<K>();
-  unsigned char* bbuf = smem_raw + ctrl + static_cast<size_t>(kRing) * chunk_bytes<K>();
-  const size_t bbytes = static_cast<size_t>(NB) * p.ns * sizeof(__half);
+
+  // The output kernel may launch now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const LayerArgs& a = p.a;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int tiles_per_row = a.n / 16;
-  const int nst_item = p.ns / kStageWeights;
-  const int nchunk_item = p.ns / (kChunkTiles * 16);
-  // items of this CTA: blockIdx.x + i * gridDim.x
-  const int my_items = p.items > static_cast<int>(blockIdx.x)
-                           ? (p.items - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
+  const int nkb = a.n / kChunkK;
+  const long long total = static_cast<long long>(a.m / kRowBlock) * nkb;
+  const int lo = static_cast<int>(total * blockIdx.x / gridDim.x);
+  const int hi = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
 
   // ---- set-up ---------------------------------------------------------------
   if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -347,11 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       mbar_init(&sh.ring_empty[i], kDecodeWarps);  // one elected arrival per decode warp
     }
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&sh.a_full[i], 4);  // one elected arrival per warp of the warpgroup
+      mbar_init(&sh.a_full[i], kDecodeWarps);
       mbar_init(&sh.a_empty[i], 1);
+      mbar_init(&sh.b_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.b_full[i], 128);
       mbar_init(&sh.d_full[i], 1);
       mbar_init(&sh.d_empty[i], 128);
     }
@@ -359,43 +367,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     sh.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // B rows n >= M stay zero for the whole kernel.
-  for (size_t i = static_cast<size_t>(tid) * 16; i < 2 * bbytes; i += static_cast<size_t>(kThreads) * 16)
-    *reinterpret_cast<uint4*>(bbuf + i) = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == kTmaWarp) {
-    // ---- producer: code chunks into the ring ----------------------------------
+    // ---- code producer: chunks into the ring -------------------------------------
     // Lanes 0-7 each copy one tile-row strip of a chunk; lane 0 posts the
     // expected byte count first.
     int seq = 0;
-    bool stop = false;
-    for (int li = 0; li < my_items && !stop; ++li) {
-      const int item = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
-      const int rb = item / p.nslices;
-      const int sl = item - rb * p.nslices;
-      for (int ch = 0; ch < nchunk_item; ++ch, ++seq) {
-        const int slot = seq % kRing;
-        const int use = seq / kRing;
-        bool ok = true;
-        if (use > 0) ok = mbar_wait(&sh.ring_empty[slot], (use - 1) & 1);
-        if (!ok) set_abort(sh);
-        if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) {
-          stop = true;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * kChunkTiles * 32u * K);
-        __syncwarp();
-        if (lane < 8) {
-          const int J0 = (sl * p.ns) / 16 + ch * kChunkTiles;
-          uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
-          const uint32_t* src =
-              a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + J0) * (8 * K);
-          bulk_g2s(dst + lane * chunk_row_words<K>(), src, kChunkTiles * 32u * K, &sh.ring_full[slot]);
-        }
+    for (int c = lo; c < hi; ++c, ++seq) {
+      const int rb = c / nkb;
+      const int kb = c - rb * nkb;
+      const int slot = seq % kRing;
+      const int use = seq / kRing;
+      bool ok = true;
+      if (use > 0) ok = mbar_wait(&sh.ring_empty[slot], (use - 1) & 1);
+      if (!ok) set_abort(sh);
+      if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
+      if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * kChunkTiles * 32u * K);
+      __syncwarp();
+      if (lane < 8) {
+        uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
+        const uint32_t* src =
+            a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * kChunkTiles) * (8 * K);
+        bulk_g2s(dst + lane * chunk_row_words<K>(), src, kChunkTiles * 32u * K, &sh.ring_full[slot]);
       }
     }
     // Wait (bounded) for every copy issued into the ring to land before exit.
@@ -403,64 +400,75 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       const int s = seq - 1 - i;
       mbar_wait(&sh.ring_full[s % kRing], (s / kRing) & 1);
     }
+  } else if (warp == kBWarp) {
+    // ---- operand-B producer ----------------------------------------------------------
+    if (lane == 0) {
+      // The images are written by the preceding kernel on the stream.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      int seq = 0;
+      for (int c = lo; c < hi; ++c, ++seq) {
+        const int kb = c % nkb;
+        const int slot = seq % kSlots;
+        const int use = seq / kSlots;
+        if (use > 0 && !mbar_wait(&sh.a_empty[slot], (use - 1) & 1)) set_abort(sh);
+        if (aborted(sh)) break;
+        mbar_arrive_expect_tx(&sh.b_full[slot], bchunk_bytes<NB>());
+        bulk_g2s(bring + static_cast<size_t>(slot) * bchunk_bytes<NB>(),
+                 p.bimg + static_cast<size_t>(kb) * NB * kChunkK, bchunk_bytes<NB>(), &sh.b_full[slot]);
+      }
+      for (int i = 0; i < kSlots && i < seq; ++i) {
+        const int s = seq - 1 - i;
+        mbar_wait(&sh.b_full[s % kSlots], (s / kSlots) & 1);
+      }
+    }
   } else if (warp < kDecodeWarps) {
     // ---- decode producers of operand A -------------------------------------------
-    const int g = warp >> 2;              // warpgroup: stage g of every chunk
+    const int g = warp >> 2;              // warpgroup: tiles 2g, 2g+1 of every chunk
     const int quarter = warp & 3;         // TMEM lanes 32 * quarter ..
     const int row = quarter * 32 + lane;  // row within the 128-row block
     const int trow = row >> 4;            // tile row within the block
     const int rr = row & 15;
     const int q0 = (rr * K) >> 1;
     const uint32_t off = static_cast<uint32_t>((rr * K) & 1) * 16u;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol + 16 * g;
     int seq = 0;
-    bool stop = false;
-    for (int li = 0; li < my_items && !stop; ++li) {
-      for (int ch = 0; ch < nchunk_item; ++ch, ++seq) {
-        const int slot = seq % kRing;
-        bool ok = mbar_wait(&sh.ring_full[slot], (seq / kRing) & 1);
-        if (!ok) set_abort(sh);
-        if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) {
-          stop = true;
-          break;
-        }
-        const uint32_t* rw = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4) +
-                             trow * chunk_row_words<K>() + (2 * g) * (8 * K);
-        uint32_t raw0[RowWords<K>::kRaw], raw1[RowWords<K>::kRaw];
+    for (int c = lo; c < hi; ++c, ++seq) {
+      const int slot = seq % kRing;
+      bool ok = mbar_wait(&sh.ring_full[slot], (seq / kRing) & 1);
+      if (!ok) set_abort(sh);
+      if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
+      const uint32_t* rw = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4) +
+                           trow * chunk_row_words<K>() + (2 * g) * (8 * K);
+      uint32_t raw0[RowWords<K>::kRaw], raw1[RowWords<K>::kRaw];
 #pragma unroll
-        for (int i = 0; i < RowWords<K>::kRaw; ++i) {
-          int idx = q0 + i;
-          if (idx >= 8 * K) idx -= 8 * K;
-          raw0[i] = rw[idx];
-          raw1[i] = rw[8 * K + idx];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.ring_empty[slot]);
-        uint32_t st0[16], st1[16];
-        row_states<K>(raw0, off, st0);
-        row_states<K>(raw1, off, st1);
-        uint32_t v[16];
-#pragma unroll
-        for (int c = 0; c < 16; c += 2) {
-          v[c / 2] = pack_two<CB>(st0[c], st0[c + 1]);
-          v[8 + c / 2] = pack_two<CB>(st1[c], st1[c + 1]);
-        }
-        const int gs = 4 * seq + g;  // global stage index of this CTA
-        const int aslot = gs % kSlots;
-        const int use = gs / kSlots;
-        ok = true;
-        if (use > 0) ok = mbar_wait(&sh.a_empty[aslot], (use - 1) & 1);
-        if (!ok) set_abort(sh);
-        if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) {
-          stop = true;
-          break;
-        }
-        tmem_st16(lane_addr + kACol + aslot * kStageCols, v);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.a_full[aslot]);
+      for (int i = 0; i < RowWords<K>::kRaw; ++i) {
+        int idx = q0 + i;
+        if (idx >= 8 * K) idx -= 8 * K;
+        raw0[i] = rw[idx];
+        raw1[i] = rw[8 * K + idx];
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.ring_empty[slot]);
+      uint32_t st0[16], st1[16];
+      row_states<K>(raw0, off, st0);
+      row_states<K>(raw1, off, st1);
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        v[j / 2] = pack_two<CB>(st0[j], st0[j + 1]);
+        v[8 + j / 2] = pack_two<CB>(st1[j], st1[j + 1]);
+      }
+      const int aslot = seq % kSlots;
+      const int use = seq / kSlots;
+      ok = true;
+      if (use > 0) ok = mbar_wait(&sh.a_empty[aslot], (use - 1) & 1);
+      if (!ok) set_abort(sh);
+      if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
+      tmem_st16(lane_addr + aslot * kChunkCols, v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.a_full[aslot]);
     }
   } else if (warp == kMmaWarp) {
     // ---- MMA issue ------------------------------------------------------------------
@@ -468,36 +476,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       constexpr uint32_t idesc = idesc_f16<NB>();
       constexpr uint32_t kLbo = (NB / 8) * 128;  // next 8 K-elements
       constexpr uint32_t kSbo = 128;             // next 8 rows of N
-      int gs = 0;
-      for (int li = 0; li < my_items && !aborted(sh); ++li) {
-        const int db = li & 1;
-        if (!mbar_wait(&sh.b_full[db], (li >> 1) & 1)) {
+      const uint64_t bdesc0 = smem_desc(smem_u32(bring), kLbo, kSbo);
+      int seq = 0;
+      int run = 0;
+      bool bad = false;
+      for (int c = lo; c < hi && !bad; ++run) {
+        const int rb = c / nkb;
+        const int end = min(hi, (rb + 1) * nkb);
+        const int db = run & 1;
+        if (run >= 2 && !mbar_wait(&sh.d_empty[db], ((run >> 1) - 1) & 1)) {
           set_abort(sh);
           break;
         }
-        if (li >= 2 && !mbar_wait(&sh.d_empty[db], ((li >> 1) - 1) & 1)) {
-          set_abort(sh);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t bbase = smem_u32(bbuf + db * bbytes);
-        bool bad = false;
-        for (int s = 0; s < nst_item; ++s, ++gs) {
-          const int aslot = gs % kSlots;
-          if (!mbar_wait(&sh.a_full[aslot], (gs / kSlots) & 1) || aborted(sh)) {
+        for (uint32_t acc = 0; c < end; ++c, ++seq, acc = 1) {
+          const int slot = seq % kSlots;
+          const uint32_t par = (seq / kSlots) & 1;
+          if (!mbar_wait(&sh.a_full[slot], par) || !mbar_wait(&sh.b_full[slot], par) || aborted(sh)) {
             set_abort(sh);
             bad = true;
             break;
           }
           tc_fence_after();
+          // descriptor start address advances by (bytes >> 4) in its low field
+          const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bchunk_bytes<NB>()) >> 4);
+          const uint32_t at = tmem + kACol + slot * kChunkCols;
+          const uint32_t dt = tmem + kDCol + 32 * db;
+          // the first MMA of a run overwrites D
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint32_t kk = static_cast<uint32_t>(s) * kStageWeights + 16u * j;  // K offset
-            const uint64_t bd = smem_desc(bbase + (kk / 8) * kLbo, kLbo, kSbo);
-            mma_f16_ts(tmem + kDCol + 32 * db, tmem + kACol + aslot * kStageCols + 8 * j, bd, idesc,
-                       (s > 0 || j > 0) ? 1u : 0u);
-          }
-          mma_commit(&sh.a_empty[aslot]);
+          for (int j = 0; j < kChunkTiles; ++j)
+            mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, j > 0 ? 1u : acc);
+          mma_commit(&sh.a_empty[slot]);
         }
         if (bad) break;
         mma_commit(&sh.d_full[db]);
@@ -506,184 +514,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       mbar_wait(&sh.mma_done, 0);
     }
   } else {
-    // ---- epilogue warps: B of the next item, finish the previous one ----------------
-    const int ew = warp - kEpiWarp0;  // 0..3 = TMEM lane quarter
+    // ---- epilogue warps: D of each run into the row sums -----------------------------
+    const int ew = warp - kEpiWarp0;      // 0..3 = TMEM lane quarter
     const int et = tid - kEpiWarp0 * 32;  // 0..127
-    const int nkb = p.ns / kRowBlock;
-    // x may be written by the preceding kernel on the stream (the rotation).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int li = 0; li <= my_items; ++li) {
+    int run = 0;
+    for (int c = lo; c < hi; ++run) {
+      const int rb = c / nkb;
+      const int end = min(hi, (rb + 1) * nkb);
+      const int kb0 = c - rb * nkb;
+      const int kb1 = end - rb * nkb;
+      c = end;
       // Uniform go/stop decision for the four epilogue warps: they share named
       // barriers, so they must leave together.
       if (et == 0) sh.epi_go = aborted(sh) ? 0u : 1u;
       epi_sync();
       if (sh.epi_go == 0u) break;
-      if (li < my_items) {
-        // B[li & 1] for item li (free: the MMAs of item li-2 finished before the
-        // epilogue of item li-2 ran in the previous iteration).
-        const int db = li & 1;
-        const int item = static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x);
-        const int sl = item % p.nslices;
-        const int c0 = sl * p.ns;
-        unsigned char* bsm = bbuf + db * bbytes;
-        if (et < 32) sh.xsum[db][et] = 0.f;
-        epi_sync();
-        for (int job = ew; job < p.M * nkb; job += 4) {
-          const int n = job / nkb;
-          const int kb = job - n * nkb;
-          const int col = c0 + kb * kRowBlock + 4 * lane;
-          float v[4];
-          {
-            const uint2 xr = *reinterpret_cast<const uint2*>(a.x + static_cast<size_t>(n) * a.n + col);
-            const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
-            const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
-            v[0] = __low2float(x01);
-            v[1] = __high2float(x01);
-            v[2] = __low2float(x23);
-            v[3] = __high2float(x23);
-          }
-          if (a.s_in != nullptr) {
-            const uint2 sr = *reinterpret_cast<const uint2*>(a.s_in + col);
-            const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-            const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-            v[0] *= __low2float(s01);
-            v[1] *= __high2float(s01);
-            v[2] *= __low2float(s23);
-            v[3] *= __high2float(s23);
-            fwht128_warp(v, lane);
+      if constexpr (CB == kCb1Mad) {
+        // sum of x-tilde over the run's columns, per batch row
+        for (int b = ew; b < p.M; b += 4) {
+          float s = 0.f;
+          for (int kb = kb0 + lane; kb < kb1; kb += 32) s += __ldcg(p.bsum + static_cast<size_t>(b) * nkb + kb);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
-          }
-          __half h[4];
-          float hs = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            h[j] = __float2half_rn(v[j]);
-            hs += __half2float(h[j]);
-          }
-          // element (n, k) at ((k/8) * (NB/8) + n/8) * 128 + (n%8) * 16 + (k%8) * 2;
-          // these four values are k = kb*128 + 4*lane .. +3.
-          const int kc = kb * 16 + lane / 2;
-          const uint32_t o = (static_cast<uint32_t>(kc) * (NB / 8) + n / 8) * 128u + (n % 8) * 16u +
-                             (lane % 2) * 8u;
-          uint2 pk;
-          pk.x = static_cast<uint32_t>(__half_as_ushort(h[0])) |
-                 (static_cast<uint32_t>(__half_as_ushort(h[1])) << 16);
-          pk.y = static_cast<uint32_t>(__half_as_ushort(h[2])) |
-                 (static_cast<uint32_t>(__half_as_ushort(h[3])) << 16);
-          *reinterpret_cast<uint2*>(bsm + o) = pk;
-          if (CB == kCb1Mad) {
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
-            if (lane == 0) atomicAdd(&sh.xsum[db][n], hs);
-          }
+          for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, d);
+          if (lane == 0) sh.xsum[b] = s;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         epi_sync();
-        mbar_arrive(&sh.b_full[db]);
       }
-      if (li >= 1) {
-        // finish item li-1
-        const int pi = li - 1;
-        const int db = pi & 1;
-        const int item = static_cast<int>(blockIdx.x) + pi * static_cast<int>(gridDim.x);
-        const int rb = item / p.nslices;
-        const int sl = item - rb * p.nslices;
-        bool ok = !aborted(sh) && mbar_wait(&sh.d_full[db], (pi >> 1) & 1);
-        if (!ok) set_abort(sh);
-        // tcgen05.ld is a whole-warp instruction: skip it warp-uniformly.
-        if (!__any_sync(0xFFFFFFFFu, !ok)) {
-          tc_fence_after();
-          const int row = ew * 32 + lane;
+      const int db = run & 1;
+      bool ok = !aborted(sh) && mbar_wait(&sh.d_full[db], (run >> 1) & 1);
+      if (!ok) set_abort(sh);
+      // tcgen05.ld is a whole-warp instruction: skip it warp-uniformly.
+      if (!__any_sync(0xFFFFFFFFu, !ok)) {
+        tc_fence_after();
+        const int row = ew * 32 + lane;
+        float* zrow = a.zacc + static_cast<size_t>(rb) * kRowBlock + row;
+#pragma unroll 1
+        for (int h = 0; h < NB / 16; ++h) {
           float d[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + kDCol + 32 * db, d);
+          tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + kDCol + 32 * db + 16 * h, d);
 #pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            if (n < p.M) {
-              float z = d[n];
-              if (CB == kCb1Mad) z = (z - 1534.0f * sh.xsum[db][n]) * kOneMadScale;
-              sh.zs[n * kRowBlock + row] = z;
+          for (int j = 0; j < 16; ++j) {
+            const int b = 16 * h + j;
+            if (b < p.M) {
+              float z = d[j];
+              if constexpr (CB == kCb1Mad) z = (z - 1534.0f * sh.xsum[b]) * kOneMadScale;
+              atomicAdd(zrow + static_cast<size_t>(b) * a.m, z);
             }
-          }
-          if constexpr (NB == 32) {
-            tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + kDCol + 32 * db + 16, d);
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-              if (16 + n < p.M) {
-                float z = d[n];
-                if (CB == kCb1Mad) z = (z - 1534.0f * sh.xsum[db][16 + n]) * kOneMadScale;
-                sh.zs[(16 + n) * kRowBlock + row] = z;
-              }
-            }
-          }
-          tc_fence_before();
-        }
-        mbar_arrive(&sh.d_empty[db]);
-        epi_sync();
-        bool last = true;
-        if (p.nslices > 1) {
-          float* part = a.partials + static_cast<size_t>(sl) * p.M * a.m;
-          for (int i = et; i < p.M * kRowBlock; i += 128) {
-            const int b = i / kRowBlock;
-            const int r = i - b * kRowBlock;
-            part[static_cast<size_t>(b) * a.m + rb * kRowBlock + r] = sh.zs[i];
-          }
-          __threadfence();
-          epi_sync();
-          if (et == 0) sh.ticket = atomicAdd(a.counters + rb, 1u);
-          epi_sync();
-          last = sh.ticket == static_cast<uint32_t>(p.nslices - 1);
-          if (last) {
-            __threadfence();
-            for (int i = et; i < p.M * kRowBlock; i += 128) {
-              const int b = i / kRowBlock;
-              const int r = i - b * kRowBlock;
-              float acc = 0.f;
-              for (int sp = 0; sp < p.nslices; ++sp)
-                acc += __ldcg(a.partials + (static_cast<size_t>(sp) * p.M + b) * a.m + rb * kRowBlock + r);
-              sh.zs[i] = acc;
-            }
-            if (et == 0) a.counters[rb] = 0u;
-            epi_sync();
           }
         }
-        if (last) {
-          for (int b = ew; b < p.M; b += 4) {
-            const int r0 = rb * kRowBlock + 4 * lane;
-            float v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = sh.zs[b * kRowBlock + 4 * lane + j];
-            {
-              const uint2 sr = *reinterpret_cast<const uint2*>(a.scales + r0);
-              const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-              const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-              v[0] *= __low2float(s01);
-              v[1] *= __high2float(s01);
-              v[2] *= __low2float(s23);
-              v[3] *= __high2float(s23);
-            }
-            if (a.s_out != nullptr) {
-              const uint2 sr = *reinterpret_cast<const uint2*>(a.s_out + r0);
-              const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-              const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-              v[0] *= __low2float(s01);
-              v[1] *= __high2float(s01);
-              v[2] *= __low2float(s23);
-              v[3] *= __high2float(s23);
-              fwht128_warp(v, lane);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
-            }
-            const __half2 o01 = __floats2half2_rn(v[0], v[1]);
-            const __half2 o23 = __floats2half2_rn(v[2], v[3]);
-            uint2 o;
-            o.x = *reinterpret_cast<const uint32_t*>(&o01);
-            o.y = *reinterpret_cast<const uint32_t*>(&o23);
-            *reinterpret_cast<uint2*>(a.y + static_cast<size_t>(b) * a.m + r0) = o;
-          }
-        }
-        epi_sync();  // zs is reused by the next item
+        tc_fence_before();
       }
+      mbar_arrive(&sh.d_empty[db]);
     }
   }
 
@@ -697,30 +578,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   if (tid == 0 && aborted(sh) && a.status != nullptr) atomicOr(a.status, 1u);
 }
 
-// Shared memory: control block + code ring + two B buffers (NB x ns halves).
-template <int K>
-inline size_t tc_smem_bytes(int nb, int ns) {
+// Shared memory: control block + B ring + code ring.
+template <int K, int NB>
+inline size_t tc_smem_bytes() {
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
-  return ctrl + static_cast<size_t>(ring_depth<K>()) * chunk_bytes<K>() +
-         2 * static_cast<size_t>(nb) * ns * sizeof(__half);
+  return ctrl + static_cast<size_t>(kSlots) * bchunk_bytes<NB>() +
+         static_cast<size_t>(ring_depth<K>()) * chunk_bytes<K>();
 }
 
 template <int K, int CB, int NB>
-exl3_status launch_tc_t(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream) {
+exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                        cudaStream_t stream) {
   TcParams p;
   p.a = a;
+  p.bimg = bimg;
+  p.bsum = bsum;
   p.M = M;
-  p.ns = ns;
-  p.nslices = a.n / ns;
-  p.items = (a.m / kRowBlock) * p.nslices;
   // At least 116 KB so that a single CTA is resident per SM (it owns all 512
   // TMEM columns; a second CTA would wait in tcgen05.alloc).
-  size_t smem = tc_smem_bytes<K>(NB, ns);
+  size_t smem = tc_smem_bytes<K, NB>();
   if (smem < 116 * 1024) smem = 116 * 1024;
   if (cudaFuncSetAttribute(tc_layer_kernel<K, CB, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return EXL3_ERR_CUDA;
-  if (grid > p.items) grid = p.items;
+  const long long chunks = static_cast<long long>(a.m / kRowBlock) * (a.n / kChunkK);
+  if (grid > chunks) grid = static_cast<int>(chunks);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -736,20 +618,22 @@ exl3_status launch_tc_t(const LayerArgs& a, int M, int ns, int grid, cudaStream_
 }
 
 template <int K>
-exl3_status launch_tc_dispatch(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream) {
+exl3_status launch_tc_dispatch(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                               cudaStream_t stream) {
   if (a.codebook == kCb3Inst)
-    return M <= 16 ? launch_tc_t<K, kCb3Inst, 16>(a, M, ns, grid, stream)
-                   : launch_tc_t<K, kCb3Inst, 32>(a, M, ns, grid, stream);
-  return M <= 16 ? launch_tc_t<K, kCb1Mad, 16>(a, M, ns, grid, stream)
-                 : launch_tc_t<K, kCb1Mad, 32>(a, M, ns, grid, stream);
+    return M <= 16 ? launch_tc_t<K, kCb3Inst, 16>(a, bimg, bsum, M, grid, stream)
+                   : launch_tc_t<K, kCb3Inst, 32>(a, bimg, bsum, M, grid, stream);
+  return M <= 16 ? launch_tc_t<K, kCb1Mad, 16>(a, bimg, bsum, M, grid, stream)
+                 : launch_tc_t<K, kCb1Mad, 32>(a, bimg, bsum, M, grid, stream);
 }
 
 }  // namespace tc
 }  // namespace exl3
 
-#define EXL3_DEFINE_TC_LAUNCHER(KK)                                                           \
-  namespace exl3 {                                                                            \
-  exl3_status launch_tc_k##KK(const LayerArgs& a, int M, int ns, int grid, cudaStream_t stream) { \
-    return tc::launch_tc_dispatch<KK>(a, M, ns, grid, stream);                                \
-  }                                                                                           \
+#define EXL3_DEFINE_TC_LAUNCHER(KK)                                                                  \
+  namespace exl3 {                                                                                   \
+  exl3_status launch_tc_k##KK(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid, \
+                              cudaStream_t stream) {                                                 \
+    return tc::launch_tc_dispatch<KK>(a, bimg, bsum, M, grid, stream);                               \
+  }                                                                                                  \
   }
