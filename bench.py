@@ -74,7 +74,10 @@ def workload(name: str, batch: int):
                 "gate/up 14336x4096, down 4096x14336, each at K=2,3,4 x {1MAD,3INST}")
         return desc, 1, synth.llama8b_layer_set(), 1
     if name == "single":
-        return "single 4096x4096 layer, K=2, 1MAD, batch 1", 0, synth.SINGLE_4096, 1
+        # 32 distinct 4096x4096 layers (128 MB of codes) so that the timed
+        # steps stream from HBM rather than L2
+        return ("4096x4096 layer, K=2, 1MAD, batch 1, 32 distinct instances per step"), 0, \
+            synth.SINGLE_4096 * 32, 1
     if name == "llama70b":
         return ("Llama-3-70B-shaped layers (q/o 8192x8192, k/v 1024x8192, gate/up 28672x8192, "
                 "down 8192x28672) x 32 layers resident, K=2, 3INST, batch 1"), 2, synth.llama70b_stack(), 1
@@ -82,7 +85,9 @@ def workload(name: str, batch: int):
         return ("80-layer mixed-width stack (attn 8192x8192 K4; MLP 28672x8192 / 8192x28672, "
                 "K in {2,3,4}, 2.90 bpw body) + lm_head 128256x8192 K6, 3INST, batch 1"), 4, synth.mixed_stack(), 1
     if name == "sweep":
-        return (f"14336x4096 and 4096x14336, K=3, 1MAD, batch {batch}"), 3, synth.BATCH_SWEEP_SHAPES, batch
+        # four distinct instances of each shape (176 MB of codes, more than L2)
+        return (f"14336x4096 and 4096x14336, K=3, 1MAD, batch {batch}, 4 distinct instances of each"), 3, \
+            synth.BATCH_SWEEP_SHAPES * 4, batch
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -91,7 +96,7 @@ def kernels_per_call(path: str, M: int) -> int:
     the operand-image kernel, the persistent MMA kernel and the epilogue
     kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2 or 1 rows,
     the layer kernel and the epilogue kernel."""
-    tensor = path == "tensor" or (path == "auto" and M > 4)
+    tensor = path == "tensor" or (path == "auto" and M > 2)
     if tensor:
         return 3
     chunks, rem = 0, M

@@ -146,7 +146,7 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
 
 /** Kernel family used by exl3_gemv / exl3_gemm_small. */
 typedef enum {
-  EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 4, tensor-core kernel above */
+  EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, tensor-core kernel above */
   EXL3_PATH_SHUFFLE = 1, /**< decode + fp32 FMA + warp-shuffle reduction, any M */
   EXL3_PATH_TENSOR = 2   /**< decoded tiles in TMEM feeding tcgen05 MMAs, any M */
 } exl3_path;

@@ -90,6 +90,21 @@ def test_gemm_small_batches(M):
     assert_layer_close(y, ref, f"M={M}")
 
 
+@pytest.mark.parametrize("M", [3, 5, 8, 13, 32])
+def test_gemm_small_batches_warp_shuffle(M):
+    """The warp-shuffle kernel (batch chunks of 8, 4, 2, 1) forced for batches
+    that the automatic choice sends to the tensor-core kernel."""
+    m, n, K, cb = 384, 640, 2, 0
+    inp = synth.layer_inputs(m, n, K, M, config=66, index=M)
+    B.exl3_set_path(B.PATH_SHUFFLE)
+    try:
+        y = _run(upload(inp), K, cb, m, n, M)
+    finally:
+        B.exl3_set_path(B.PATH_AUTO)
+    ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    assert_layer_close(y, ref, f"M={M}")
+
+
 def test_workspace_reuse_and_special_inputs():
     """Two calls on one workspace agree (the arrival counters and the fp32 row
     sums are left at zero); x = 0 gives y = 0 exactly; zero scales give 0."""

@@ -157,7 +157,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.status = a.counters + m / kRowBlock;
   a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
   const int path = g_path.load(std::memory_order_relaxed);
-  const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 4);
+  const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2);
   if (tensor) {
     // x-tilde as operand-B images (and, for 1MAD, its block sums), then the
     // persistent tensor-core kernel into zacc, then the output transform; the

@@ -472,47 +472,55 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     }
   } else if (warp == kMmaWarp) {
     // ---- MMA issue ------------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16<NB>();
-      constexpr uint32_t kLbo = (NB / 8) * 128;  // next 8 K-elements
-      constexpr uint32_t kSbo = 128;             // next 8 rows of N
-      const uint64_t bdesc0 = smem_desc(smem_u32(bring), kLbo, kSbo);
-      int seq = 0;
-      int run = 0;
-      bool bad = false;
-      for (int c = lo; c < hi && !bad; ++run) {
-        const int rb = c / nkb;
-        const int end = min(hi, (rb + 1) * nkb);
-        const int db = run & 1;
-        if (run >= 2 && !mbar_wait(&sh.d_empty[db], ((run >> 1) - 1) & 1)) {
+    // The whole warp runs the loop (waits, descriptors: warp-uniform values);
+    // lane 0 issues the MMAs and the commits that track them.
+    constexpr uint32_t idesc = idesc_f16<NB>();
+    constexpr uint32_t kLbo = (NB / 8) * 128;  // next 8 K-elements
+    constexpr uint32_t kSbo = 128;             // next 8 rows of N
+    const uint64_t bdesc0 = smem_desc(smem_u32(bring), kLbo, kSbo);
+    const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    int seq = 0;
+    int run = 0;
+    bool bad = false;
+    for (int c = lo; c < hi && !bad; ++run) {
+      const int rb = c / nkb;
+      const int end = min(hi, (rb + 1) * nkb);
+      const int db = run & 1;
+      const bool okd = run < 2 || mbar_wait(&sh.d_empty[db], ((run >> 1) - 1) & 1);
+      if (__any_sync(0xFFFFFFFFu, !okd)) {
+        set_abort(sh);
+        break;
+      }
+      const uint32_t dt = tm + kDCol + 32 * db;
+      for (uint32_t acc = 0; c < end; ++c, ++seq, acc = 1) {
+        const int slot = seq % kSlots;
+        const uint32_t par = (seq / kSlots) & 1;
+        const bool ok = mbar_wait(&sh.a_full[slot], par) && mbar_wait(&sh.b_full[slot], par) && !aborted(sh);
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
           set_abort(sh);
+          bad = true;
           break;
         }
-        for (uint32_t acc = 0; c < end; ++c, ++seq, acc = 1) {
-          const int slot = seq % kSlots;
-          const uint32_t par = (seq / kSlots) & 1;
-          if (!mbar_wait(&sh.a_full[slot], par) || !mbar_wait(&sh.b_full[slot], par) || aborted(sh)) {
-            set_abort(sh);
-            bad = true;
-            break;
-          }
-          tc_fence_after();
-          // descriptor start address advances by (bytes >> 4) in its low field
-          const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bchunk_bytes<NB>()) >> 4);
-          const uint32_t at = tmem + kACol + slot * kChunkCols;
-          const uint32_t dt = tmem + kDCol + 32 * db;
+        tc_fence_after();
+        // descriptor start address advances by (bytes >> 4) in its low field
+        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bchunk_bytes<NB>()) >> 4);
+        const uint32_t at = tm + kACol + slot * kChunkCols;
+        if (lane == 0) {
           // the first MMA of a run overwrites D
+          mma_f16_ts(dt, at, bd, idesc, acc);
 #pragma unroll
-          for (int j = 0; j < kChunkTiles; ++j)
-            mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, j > 0 ? 1u : acc);
+          for (int j = 1; j < kChunkTiles; ++j) mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, 1u);
           mma_commit(&sh.a_empty[slot]);
         }
-        if (bad) break;
-        mma_commit(&sh.d_full[db]);
+        __syncwarp();
       }
-      mma_commit(&sh.mma_done);
-      mbar_wait(&sh.mma_done, 0);
+      if (bad) break;
+      if (lane == 0) mma_commit(&sh.d_full[db]);
+      __syncwarp();
     }
+    if (lane == 0) mma_commit(&sh.mma_done);
+    __syncwarp();
+    mbar_wait(&sh.mma_done, 0);
   } else {
     // ---- epilogue warps: D of each run into the row sums -----------------------------
     const int ew = warp - kEpiWarp0;      // 0..3 = TMEM lane quarter
