@@ -62,19 +62,19 @@ constexpr int kMmaWarp = 20;
 constexpr int kTmaWarp = 21;
 constexpr int kBWarp = 22;
 constexpr int kThreads = 23 * 32;
-constexpr int kChunkTiles = 8;          // tile columns per chunk (128 columns)
-constexpr int kChunkK = kChunkTiles * 16;
+// A chunk is 16 tile columns (256 input columns) when n allows it, else 8.
+constexpr int kMaxChunkTiles = 16;
 // Code chunks in flight: 8 for K <= 4, 4 above (shared-memory budget).
 template <int K>
 __host__ __device__ constexpr int ring_depth() {
   return K <= 4 ? 8 : 4;
 }
 constexpr int kMaxRing = 8;
-constexpr int kSlots = 6;               // chunks of A in TMEM (and of B in shared memory)
-constexpr int kChunkCols = 64;          // TMEM columns per chunk (two weights each)
+constexpr int kSlots = 3;               // chunks of A in TMEM (and of B in shared memory)
+constexpr int kChunkCols = 128;         // TMEM columns per chunk slot (two weights each)
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                // D buffers at columns 0 and 32
-constexpr int kACol = 64;               // A slots at 64 + 64 * slot
+constexpr int kACol = 64;               // A slots at 64 + 128 * slot
 constexpr int kRowPadWords = 16;        // keeps tile-row strips 64 B apart from a bank multiple
 constexpr uint32_t kSpinLimit = 1u << 20;  // about a second of try_wait polling
 constexpr int kEpiBarrier = 1;          // named barrier of the epilogue warps
@@ -284,11 +284,28 @@ __device__ __forceinline__ uint32_t pack_two(uint32_t s0, uint32_t s1) {
   }
 }
 
+// The 32 TMEM column words of two adjacent tiles of one row (raw words as
+// loaded for that row of each tile).
+template <int K, int CB>
+__device__ __forceinline__ void decode_tile_pair(const uint32_t (&raw0)[RowWords<K>::kRaw],
+                                                 const uint32_t (&raw1)[RowWords<K>::kRaw], uint32_t off,
+                                                 uint32_t (&v)[16]) {
+  uint32_t st0[16], st1[16];
+  row_states<K>(raw0, off, st0);
+  row_states<K>(raw1, off, st1);
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    v[j / 2] = pack_two<CB>(st0[j], st0[j + 1]);
+    v[8 + j / 2] = pack_two<CB>(st1[j], st1[j + 1]);
+  }
+}
+
 struct TcParams {
   LayerArgs a;
   const __half* bimg;  // operand-B images, one per 128-column block
   const float* bsum;   // [M][n/128] sums of x-tilde (1MAD), else unused
   int M;
+  int ct;              // tile columns per chunk: 16, or 8 when n is an odd multiple of 128
 };
 
 struct TcShared {
@@ -308,15 +325,15 @@ struct TcShared {
 
 template <int K>
 __host__ __device__ constexpr int chunk_row_words() {
-  return kChunkTiles * 8 * K + kRowPadWords;
+  return kMaxChunkTiles * 8 * K + kRowPadWords;
 }
 template <int K>
 __host__ __device__ constexpr int chunk_bytes() {
   return 8 * chunk_row_words<K>() * 4;
 }
 template <int NB>
-__host__ __device__ constexpr int bchunk_bytes() {
-  return NB * kChunkK * 2;
+__host__ __device__ constexpr int bslot_bytes() {
+  return NB * kMaxChunkTiles * 16 * 2;
 }
 
 __device__ __forceinline__ bool aborted(const TcShared& sh) {
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   TcShared& sh = *reinterpret_cast<TcShared*>(smem_raw);
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
   unsigned char* bring = smem_raw + ctrl;
-  uint32_t* ring = reinterpret_cast<uint32_t*>(bring + static_cast<size_t>(kSlots) * bchunk_bytes<NB>());
+  uint32_t* ring = reinterpret_cast<uint32_t*>(bring + static_cast<size_t>(kSlots) * bslot_bytes<NB>());
   constexpr int kRing = ring_depth<K>();
 
   // The output kernel may launch now; it waits for this grid to finish.
@@ -342,7 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int tiles_per_row = a.n / 16;
-  const int nkb = a.n / kChunkK;
+  const int ct = p.ct;
+  const int nkb = a.n / (16 * ct);                 // chunks per row block
+  const uint32_t bbytes = static_cast<uint32_t>(NB) * 16u * ct * 2u;  // operand B of one chunk
   const long long total = static_cast<long long>(a.m / kRowBlock) * nkb;
   const int lo = static_cast<int>(total * blockIdx.x / gridDim.x);
   const int hi = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
@@ -386,13 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       if (use > 0) ok = mbar_wait(&sh.ring_empty[slot], (use - 1) & 1);
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * kChunkTiles * 32u * K);
+      if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * ct * 32u * K);
       __syncwarp();
       if (lane < 8) {
         uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
         const uint32_t* src =
-            a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * kChunkTiles) * (8 * K);
-        bulk_g2s(dst + lane * chunk_row_words<K>(), src, kChunkTiles * 32u * K, &sh.ring_full[slot]);
+            a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * ct) * (8 * K);
+        bulk_g2s(dst + lane * chunk_row_words<K>(), src, ct * 32u * K, &sh.ring_full[slot]);
       }
     }
     // Wait (bounded) for every copy issued into the ring to land before exit.
@@ -412,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         const int use = seq / kSlots;
         if (use > 0 && !mbar_wait(&sh.a_empty[slot], (use - 1) & 1)) set_abort(sh);
         if (aborted(sh)) break;
-        mbar_arrive_expect_tx(&sh.b_full[slot], bchunk_bytes<NB>());
-        bulk_g2s(bring + static_cast<size_t>(slot) * bchunk_bytes<NB>(),
-                 p.bimg + static_cast<size_t>(kb) * NB * kChunkK, bchunk_bytes<NB>(), &sh.b_full[slot]);
+        mbar_arrive_expect_tx(&sh.b_full[slot], bbytes);
+        bulk_g2s(bring + static_cast<size_t>(slot) * bslot_bytes<NB>(),
+                 p.bimg + static_cast<size_t>(kb) * NB * 16 * ct, bbytes, &sh.b_full[slot]);
       }
       for (int i = 0; i < kSlots && i < seq; ++i) {
         const int s = seq - 1 - i;
@@ -423,14 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     }
   } else if (warp < kDecodeWarps) {
     // ---- decode producers of operand A -------------------------------------------
-    const int g = warp >> 2;              // warpgroup: tiles 2g, 2g+1 of every chunk
+    // Warpgroup g decodes tile columns g * ct/4 .. g * ct/4 + ct/4 - 1 of every
+    // chunk, two adjacent tiles (one 16-column TMEM group) at a time.
+    const int g = warp >> 2;
     const int quarter = warp & 3;         // TMEM lanes 32 * quarter ..
     const int row = quarter * 32 + lane;  // row within the 128-row block
     const int trow = row >> 4;            // tile row within the block
     const int rr = row & 15;
     const int q0 = (rr * K) >> 1;
     const uint32_t off = static_cast<uint32_t>((rr * K) & 1) * 16u;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol + 16 * g;
+    const int t0 = g * (ct / 4);          // first tile column of this warpgroup
+    const bool two = ct == 16;            // a second tile pair per chunk
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol + 8 * t0;
     int seq = 0;
     for (int c = lo; c < hi; ++c, ++seq) {
       const int slot = seq % kRing;
@@ -438,33 +461,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
       const uint32_t* rw = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4) +
-                           trow * chunk_row_words<K>() + (2 * g) * (8 * K);
-      uint32_t raw0[RowWords<K>::kRaw], raw1[RowWords<K>::kRaw];
+                           trow * chunk_row_words<K>() + t0 * (8 * K);
+      uint32_t raw[4][RowWords<K>::kRaw];
 #pragma unroll
       for (int i = 0; i < RowWords<K>::kRaw; ++i) {
         int idx = q0 + i;
         if (idx >= 8 * K) idx -= 8 * K;
-        raw0[i] = rw[idx];
-        raw1[i] = rw[8 * K + idx];
+        raw[0][i] = rw[idx];
+        raw[1][i] = rw[8 * K + idx];
+        if (two) {
+          raw[2][i] = rw[16 * K + idx];
+          raw[3][i] = rw[24 * K + idx];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.ring_empty[slot]);
-      uint32_t st0[16], st1[16];
-      row_states<K>(raw0, off, st0);
-      row_states<K>(raw1, off, st1);
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        v[j / 2] = pack_two<CB>(st0[j], st0[j + 1]);
-        v[8 + j / 2] = pack_two<CB>(st1[j], st1[j + 1]);
-      }
+      uint32_t v0[16], v1[16];
+      decode_tile_pair<K, CB>(raw[0], raw[1], off, v0);
+      if (two) decode_tile_pair<K, CB>(raw[2], raw[3], off, v1);
       const int aslot = seq % kSlots;
       const int use = seq / kSlots;
       ok = true;
       if (use > 0) ok = mbar_wait(&sh.a_empty[aslot], (use - 1) & 1);
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      tmem_st16(lane_addr + aslot * kChunkCols, v);
+      tmem_st16(lane_addr + aslot * kChunkCols, v0);
+      if (two) tmem_st16(lane_addr + aslot * kChunkCols + 16, v1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -479,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     constexpr uint32_t kSbo = 128;             // next 8 rows of N
     const uint64_t bdesc0 = smem_desc(smem_u32(bring), kLbo, kSbo);
     const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    const bool two_mma = ct == 16;
     int seq = 0;
     int run = 0;
     bool bad = false;
@@ -503,13 +526,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         }
         tc_fence_after();
         // descriptor start address advances by (bytes >> 4) in its low field
-        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bchunk_bytes<NB>()) >> 4);
+        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bslot_bytes<NB>()) >> 4);
         const uint32_t at = tm + kACol + slot * kChunkCols;
         if (lane == 0) {
-          // the first MMA of a run overwrites D
+          // one MMA per tile column (K = 16); the first MMA of a run overwrites D
           mma_f16_ts(dt, at, bd, idesc, acc);
 #pragma unroll
-          for (int j = 1; j < kChunkTiles; ++j) mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, 1u);
+          for (int j = 1; j < 8; ++j) mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, 1u);
+          if (two_mma) {
+#pragma unroll
+            for (int j = 8; j < 16; ++j) mma_f16_ts(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc, 1u);
+          }
           mma_commit(&sh.a_empty[slot]);
         }
         __syncwarp();
@@ -541,7 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         // sum of x-tilde over the run's columns, per batch row
         for (int b = ew; b < p.M; b += 4) {
           float s = 0.f;
-          for (int kb = kb0 + lane; kb < kb1; kb += 32) s += __ldcg(p.bsum + static_cast<size_t>(b) * nkb + kb);
+          const int nblk = a.n / kRowBlock;  // 128-column blocks per row
+          for (int kb = kb0 * (ct / 8) + lane; kb < kb1 * (ct / 8); kb += 32)
+            s += __ldcg(p.bsum + static_cast<size_t>(b) * nblk + kb);
 #pragma unroll
           for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, d);
           if (lane == 0) sh.xsum[b] = s;
@@ -590,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
 template <int K, int NB>
 inline size_t tc_smem_bytes() {
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
-  return ctrl + static_cast<size_t>(kSlots) * bchunk_bytes<NB>() +
+  return ctrl + static_cast<size_t>(kSlots) * bslot_bytes<NB>() +
          static_cast<size_t>(ring_depth<K>()) * chunk_bytes<K>();
 }
 
@@ -602,6 +631,7 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
   p.bimg = bimg;
   p.bsum = bsum;
   p.M = M;
+  p.ct = (a.n % (16 * kMaxChunkTiles)) == 0 ? kMaxChunkTiles : kMaxChunkTiles / 2;
   // At least 116 KB so that a single CTA is resident per SM (it owns all 512
   // TMEM columns; a second CTA would wait in tcgen05.alloc).
   size_t smem = tc_smem_bytes<K, NB>();
@@ -609,7 +639,7 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
   if (cudaFuncSetAttribute(tc_layer_kernel<K, CB, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return EXL3_ERR_CUDA;
-  const long long chunks = static_cast<long long>(a.m / kRowBlock) * (a.n / kChunkK);
+  const long long chunks = static_cast<long long>(a.m / kRowBlock) * (a.n / (16 * p.ct));
   if (grid > chunks) grid = static_cast<int>(chunks);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
