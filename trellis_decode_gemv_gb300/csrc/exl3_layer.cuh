@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
   const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
   __shared__ uint4 xs[MB * kSegTiles * 4];  // rotated x of the segment, [MB][tiles][4]
 
-  // The previous call's epilogue zeroes zacc: wait for the preceding grid.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The output kernel may be scheduled now (it waits for this grid to finish).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  bool waited = false;
   for (long long u = u_begin; u < u_end;) {
     const int rb = static_cast<int>(u / nt);
     const int ja = static_cast<int>(u - static_cast<long long>(rb) * nt);
@@ -102,6 +103,19 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
     const int jb = ja + span < nt ? ja + span : nt;
     const int I = rb * (kRowBlock / 16) + warp;
     const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
+
+    // Code words are loaded two tiles ahead of their decode; the first two are
+    // requested before the segment's x rotation.
+    int J = ja + jt;
+    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
+    if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
+    if (J + 4 < jb) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
+    // x (and the zeroed row sums) come from the preceding grids on the stream;
+    // the codes above do not.
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
 
     // Rotate the x columns of the segment into shared memory: every 128-block
     // that overlaps it, one warp per (batch row, block): signs, 128-point FWHT,
@@ -142,11 +156,6 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
 #pragma unroll
     for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
 
-    // Code words are loaded two tiles ahead of their decode.
-    int J = ja + jt;
-    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
-    if (J < jb) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
-    if (J + 4 < jb) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
     while (J < jb) {
       uint32_t st[32];
       pair_states<K>(w0, st);

@@ -15,6 +15,10 @@ namespace exl3 {
 namespace {
 
 constexpr int kThreads = 256;
+// The two small kernels chained to the layer kernels by programmatic dependent
+// launch: 128 threads and at most 32 registers, so that a CTA fits beside the
+// resident layer kernel and is ready when it finishes.
+constexpr int kSmallThreads = 128;
 
 __global__ void __launch_bounds__(kThreads)
     rht_kernel(const __half* __restrict__ in, const __half* __restrict__ signs,
@@ -56,13 +60,13 @@ __global__ void __launch_bounds__(kThreads)
 // block's image.  Rows r >= M are zero.  With bsum, also the fp32 sum of the
 // block's binary16 values.  The layer kernel is a programmatic dependent of
 // this one and waits for it before reading the images.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kSmallThreads, 16)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
                 __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int nkb = n / kRowBlock;
-  const long long job = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   if (job >= static_cast<long long>(nb) * nkb) return;
   const int r = static_cast<int>(job / nkb);
   const int kb = static_cast<int>(job - static_cast<long long>(r) * nkb);
@@ -104,13 +108,13 @@ __global__ void __launch_bounds__(kThreads)
 // Epilogue of the warp-shuffle layer: one warp per (batch row, 128-row block):
 // y = binary16(Hb(s_out (.) (scale (.) zacc))) and zacc := 0.  Launched as a
 // programmatic dependent of the layer kernel; waits for it before reading.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kSmallThreads, 16)
     epi_kernel(float* __restrict__ zacc, const __half* __restrict__ scales,
                const __half* __restrict__ s_out, __half* __restrict__ y, long long blocks, int m) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const long long job = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   if (job >= blocks) return;
   const int per_row = m / kRowBlock;
   const long long b = job / per_row;
@@ -204,20 +208,20 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(nb) * (n / kRowBlock);
-  const long long per_cta = kThreads / 32;
+  const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  bimg_kernel<<<grid, kThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  bimg_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
 }
 
 exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,
                        int m, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(rows) * (m / kRowBlock);
-  const long long per_cta = kThreads / 32;
+  const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kSmallThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -321,6 +321,7 @@ struct TcShared {
   uint32_t abort;
   uint32_t epi_go;
   float xsum[32];
+  alignas(16) float zt[32 * 128];  // D of a run transposed to [batch][row] for 16-byte reductions
 };
 
 template <int K>
@@ -367,12 +368,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   const int hi = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
 
   // ---- set-up ---------------------------------------------------------------
+  // The code producer initialises its ring and issues the first chunks before
+  // the block-wide barrier, so that their HBM latency overlaps the TMEM
+  // allocation and the initialisation of the other barriers.
+  auto issue_chunk = [&](int seq, int c) {
+    const int rb = c / nkb;
+    const int kb = c - rb * nkb;
+    const int slot = seq % kRing;
+    // Lanes 0-7 each copy one tile-row strip; lane 0 posts the byte count first.
+    if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * ct * 32u * K);
+    __syncwarp();
+    if (lane < 8) {
+      uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
+      const uint32_t* src = a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * ct) * (8 * K);
+      bulk_g2s(dst + lane * chunk_row_words<K>(), src, ct * 32u * K, &sh.ring_full[slot]);
+    }
+  };
+  int pre = 0;
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&sh.ring_full[i], 1);
+        mbar_init(&sh.ring_empty[i], kDecodeWarps);  // one elected arrival per decode warp
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    // Two chunks: issuing more would hold the other warps at the barrier.
+    pre = min(2, hi - lo);
+    for (int s = 0; s < pre; ++s) issue_chunk(s, lo + s);
+  }
   if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(&sh.ring_full[i], 1);
-      mbar_init(&sh.ring_empty[i], kDecodeWarps);  // one elected arrival per decode warp
-    }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sh.a_full[i], kDecodeWarps);
       mbar_init(&sh.a_empty[i], 1);
@@ -392,27 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == kTmaWarp) {
-    // ---- code producer: chunks into the ring -------------------------------------
-    // Lanes 0-7 each copy one tile-row strip of a chunk; lane 0 posts the
-    // expected byte count first.
-    int seq = 0;
-    for (int c = lo; c < hi; ++c, ++seq) {
-      const int rb = c / nkb;
-      const int kb = c - rb * nkb;
+    // ---- code producer: the remaining chunks into the ring ---------------------------
+    int seq = pre;
+    for (int c = lo + pre; c < hi; ++c, ++seq) {
       const int slot = seq % kRing;
       const int use = seq / kRing;
       bool ok = true;
       if (use > 0) ok = mbar_wait(&sh.ring_empty[slot], (use - 1) & 1);
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * ct * 32u * K);
-      __syncwarp();
-      if (lane < 8) {
-        uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
-        const uint32_t* src =
-            a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * ct) * (8 * K);
-        bulk_g2s(dst + lane * chunk_row_words<K>(), src, ct * 32u * K, &sh.ring_full[slot]);
-      }
+      issue_chunk(seq, c);
     }
     // Wait (bounded) for every copy issued into the ring to land before exit.
     for (int i = 0; i < kRing && i < seq; ++i) {
@@ -584,7 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       if (!__any_sync(0xFFFFFFFFu, !ok)) {
         tc_fence_after();
         const int row = ew * 32 + lane;
-        float* zrow = a.zacc + static_cast<size_t>(rb) * kRowBlock + row;
 #pragma unroll 1
         for (int h = 0; h < NB / 16; ++h) {
           float d[16];
@@ -595,13 +610,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
             if (b < p.M) {
               float z = d[j];
               if constexpr (CB == kCb1Mad) z = (z - 1534.0f * sh.xsum[b]) * kOneMadScale;
-              atomicAdd(zrow + static_cast<size_t>(b) * a.m, z);
+              sh.zt[b * kRowBlock + row] = z;
             }
           }
         }
         tc_fence_before();
       }
       mbar_arrive(&sh.d_empty[db]);
+      epi_sync();
+      if (!aborted(sh)) {
+        // four consecutive rows of one batch row per 16-byte reduction
+        float* zblk = a.zacc + static_cast<size_t>(rb) * kRowBlock;
+        for (int i = et; i < p.M * (kRowBlock / 4); i += 128) {
+          const int b = i / (kRowBlock / 4);
+          const int q = i - b * (kRowBlock / 4);
+          const float4 v = *reinterpret_cast<const float4*>(&sh.zt[b * kRowBlock + 4 * q]);
+          atomicAdd(reinterpret_cast<float4*>(zblk + static_cast<size_t>(b) * a.m + 4 * q), v);
+        }
+      }
     }
   }
 
