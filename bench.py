@@ -98,20 +98,22 @@ def workload(name: str, batch: int):
     raise SystemExit(f"unknown workload {name}")
 
 
-def kernels_per_call(path: str, M: int) -> int:
-    """Kernel launches of one exl3_gemm_small call: the tensor-core path runs
-    the operand-image kernel, the persistent MMA kernel and the epilogue
-    kernel; the warp-shuffle path runs, per batch chunk of 8, 4, 2 or 1 rows,
-    the layer kernel and the epilogue kernel."""
+def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
+    """Kernel launches of one exl3_gemm_small call.  Tensor-core path: the
+    operand-image kernel, the persistent MMA kernel and the output kernel.
+    Warp-shuffle path, per batch chunk of 8, 4, 2 or 1 rows: layer kernel and
+    output kernel, plus the x-pair kernel when the chunk runs the sub-unit
+    kernel (chunks above 2 rows, or at least 1024 tiles per SM)."""
     tensor = path == "tensor" or (path == "auto" and M > 2)
     if tensor:
         return 3
-    chunks, rem = 0, M
+    tiles_per_sm = (m // 16) * (n // 16) // sms
+    launches, rem = 0, M
     for c in (8, 4, 2, 1):
         while rem >= c:
             rem -= c
-            chunks += 1
-    return 2 * chunks
+            launches += 3 if (c > 2 or tiles_per_sm >= 1024) else 2
+    return launches
 
 
 def algorithmic(m, n, K, cb, M):
@@ -481,7 +483,7 @@ def run_ours(args):
             "roofline_pct": roof_pct,
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(calls) * args.steps * kernels_per_call(args.path, M),
+            "gpu_launches": args.steps * sum(kernels_per_call(args.path, M, c["m"], c["n"], sms) for c in calls),
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -105,6 +105,18 @@ def test_gemm_small_batches_warp_shuffle(M):
     assert_layer_close(y, ref, f"M={M}")
 
 
+@pytest.mark.parametrize("M,cb", [(1, 0), (1, 1), (2, 1)])
+def test_large_layer_kernel_full(M, cb):
+    """4096 x 10112: at least 1024 tiles per SM, so batch chunks of 1 and 2 run
+    the one-CTA-per-SM sub-unit kernel; n/128 = 79 is odd, so the last
+    sub-unit of every tile row is the ragged 8-tile one.  Checked in full."""
+    m, n, K = 4096, 10112, 2
+    inp = synth.layer_inputs(m, n, K, M, config=67, index=M + 10 * cb)
+    y = _run(upload(inp), K, cb, m, n, M)
+    ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    assert_layer_close(y, ref, f"M={M} cb={cb}")
+
+
 def test_workspace_reuse_and_special_inputs():
     """Two calls on one workspace agree (the arrival counters and the fp32 row
     sums are left at zero); x = 0 gives y = 0 exactly; zero scales give 0."""

@@ -21,12 +21,31 @@ int device_sm_count() {
   return sms;
 }
 
-int choose_layer_ctas(int m, int n, int mb, int sm_count) {
-  const long long units = static_cast<long long>(m / kRowBlock) * (n / 16);
-  long long ctas = (units + 3) / 4;  // at least 4 tile columns per CTA
-  const long long wave = static_cast<long long>(mb == 1 ? 5 : mb == 2 ? 4 : 1) * sm_count;
-  if (ctas > wave) ctas = wave;
-  return ctas < 1 ? 1 : static_cast<int>(ctas);
+LayerPlan plan_layer(int m, int n, int mb, int sm_count) {
+  LayerPlan plan;
+  const long long tiles = static_cast<long long>(m / 16) * (n / 16);
+  const long long per_cta = tiles / sm_count;
+  if (mb <= 2 && per_cta < 1024) {
+    const long long units = static_cast<long long>(m / kRowBlock) * (n / 16);
+    long long ctas = (units + 3) / 4;  // at least 4 tile columns per CTA
+    const long long wave = static_cast<long long>(mb == 1 ? 5 : 4) * sm_count;
+    if (ctas > wave) ctas = wave;
+    plan.ctas = ctas < 1 ? 1 : static_cast<int>(ctas);
+    plan.sub = 0;
+    return plan;
+  }
+  const int warps = mb == 1 ? 32 : mb == 2 ? 24 : mb == 4 ? 16 : 8;
+  int sub = 4;
+  if (per_cta >= 16LL * 2 * warps) {
+    sub = 16;
+  } else if (per_cta >= 8LL * 2 * warps) {
+    sub = 8;
+  }
+  const int nt = n / 16;
+  const long long units = static_cast<long long>(m / 16) * ((nt + sub - 1) / sub);
+  plan.sub = sub;
+  plan.ctas = static_cast<int>(units < sm_count ? units : sm_count);
+  return plan;
 }
 
 namespace {
@@ -171,12 +190,21 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
     if ((st = launch_tc(a, bimg, bsum, M, sms, cs)) != EXL3_OK) return st;
     return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, m, cs);
   }
+  // x pairs of each batch chunk go where the tensor path keeps its operand
+  // images (at least 32 n bytes, enough for 8 rows of n 32-bit pairs).
+  uint32_t* xd = reinterpret_cast<uint32_t*>(ws + bimg_offset(m, M));
   for (int done = 0; done < M;) {
     const int rem = M - done;
     const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;
     a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
     a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
-    a.ctas = choose_layer_ctas(m, n, mb, sms);
+    const LayerPlan plan = plan_layer(m, n, mb, sms);
+    a.ctas = plan.ctas;
+    a.sub = plan.sub;
+    if (plan.sub > 0) {
+      if ((st = launch_xdup(a.x, a.s_in, xd, mb, n, codebook, cs)) != EXL3_OK) return st;
+      a.xdup = xd;
+    }
     if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
     if ((st = launch_epi(a.zacc, a.scales, a.s_out, a.y, mb, m, cs)) != EXL3_OK) return st;
     done += mb;

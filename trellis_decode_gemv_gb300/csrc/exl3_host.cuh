@@ -59,10 +59,17 @@ inline size_t workspace_total(int m, int n, int M) {
   return bsum_offset(m, n, M) + align256(sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock));
 }
 
-// Number of CTAs of the warp-shuffle kernel at batch chunk mb: one wave (5,
-// 4 or 1 resident 256-thread CTAs per SM for mb = 1, 2, larger), but no
-// fewer than 4 tile columns of work per CTA (one tile per lane group).
-int choose_layer_ctas(int m, int n, int mb, int sm_count);
+// Launch plan of the warp-shuffle path.  Layers with at least 1024 tiles per
+// SM (and any batch chunk above 2) use the sub-unit kernel: one CTA per SM
+// (fewer for tiny layers) and sub-units of S in {16, 8, 4} tiles, the largest
+// that still gives every warp about two sub-units.  Smaller layers at batch
+// chunks of 1 or 2 use the segment kernel (sub = 0): one wave of 5 or 4
+// 256-thread CTAs per SM, at least 4 tile columns of work per CTA.
+struct LayerPlan {
+  int ctas;
+  int sub;  // 0: segment kernel
+};
+LayerPlan plan_layer(int m, int n, int mb, int sm_count);
 
 struct LayerArgs {
   const uint32_t* codes;
@@ -75,7 +82,9 @@ struct LayerArgs {
   float* zacc;        // [mb][m] fp32 row sums, zero on entry and exit
   uint32_t* counters;
   uint32_t* status;   // device-side error bits (tensor-core path), or nullptr
+  const uint32_t* xdup;  // warp-shuffle kernel: x pairs [mb][n]
   int ctas;           // warp-shuffle kernel: grid size
+  int sub;            // warp-shuffle kernel: tiles per sub-unit (16, 8 or 4)
 };
 
 // Internal launchers (one translation unit per K for the layer kernels).
@@ -87,6 +96,13 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 // NULL the fp32 sums bsum[b * (n/128) + kb] of the binary16 values.
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream);
+// x pairs of the warp-shuffle kernel: for each of `rows` rows of x, x-tilde =
+// Hb(s_in (.) x) (x without s_in) times the code's x factor (1 for 3INST,
+// 1/sqrt(21845) for 1MAD), rounded to binary16 and duplicated into both halves
+// of a 32-bit word, xd[row][n].  A programmatic dependent of the preceding
+// kernel (waits for it before reading x).
+exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int rows, int n,
+                        int codebook, cudaStream_t stream);
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
                           cudaStream_t stream);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))

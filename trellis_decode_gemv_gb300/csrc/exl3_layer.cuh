@@ -4,27 +4,31 @@
 // the fly from the bitshift-trellis codes of "Trellis Quantization" Parts
 // eight and nine; blockwise 128-point transforms of Part eleven).
 //
-// Each call runs two kernels on the stream, chained by programmatic dependent
-// launch (the second starts while the first runs and waits for it,
-// griddepcontrol.wait, before reading what it writes):
-//  1. layer_kernel (below) accumulates W-hat x-tilde into the fp32 row sums
+// Two kernel designs share the decode and MAC below; the launch plan picks
+// the sub-unit kernel for layers with at least about 1024 tiles per SM and the
+// segment kernel (further down, which rotates x itself) for smaller ones.
+// With the sub-unit kernel a call runs three kernels on the stream, chained by
+// programmatic dependent launch (each starts while its predecessor runs and
+// waits for it, griddepcontrol.wait, before reading what it writes):
+//  1. xdup_kernel (csrc/exl3_rht_decode.cu) writes x-tilde = Hb(s_in (.) x),
+//     times the code's x factor, as binary16 duplicated into both halves of a
+//     32-bit word ("x pairs"), [mb][n];
+//  2. layer_kernel (below) accumulates W-hat x-tilde into the fp32 row sums
 //     zacc with atomic adds;
-//  2. epi_kernel (csrc/exl3_rht_decode.cu) applies the scale, the output signs
+//  3. epi_kernel (csrc/exl3_rht_decode.cu) applies the scale, the output signs
 //     and the 128-point FWHT to each 128-row block of zacc, stores y as
 //     binary16 and zeroes zacc for the next call.
 //
-// Work split (stream-K style): the (m/128 row blocks) x (n/16 tile columns)
-// work units are cut into gridDim.x equal contiguous ranges, one per CTA; a
-// range is a sequence of segments, each inside one row block.  8 warps per
-// CTA, warp w owns tile-row 8*rb + w of the segment's row block; lane
-// 8*jt + p handles every 4th tile (jt) and the row pair 2p, 2p+1 of the tile,
-// so each thread decodes 32 consecutive trellis steps from a word-aligned
-// window (code words are loaded two tiles ahead of their decode).  Each
-// segment starts by rotating the x columns it needs into shared memory (signs,
-// 128-point FWHT across a warp, 1/sqrt(128), times the code's x factor,
-// rounded to binary16, duplicated into both halves of a 32-bit word), one
-// warp per overlapping 128-block.  Per column one packed binary16
-// FMA (HFMA2):
+// Work split: a sub-unit is up to S (16, 8 or 4) consecutive tiles of one tile
+// row; the (m/16) x ceil((n/16)/S) sub-units are cut into gridDim.x equal
+// contiguous ranges, one per CTA (one CTA per SM).  Inside a CTA each warp
+// starts on its own sub-unit and then takes the next free one from a
+// shared-memory counter, so the warps of an SM finish together whatever the
+// scheduler's priorities.  In a sub-unit, lane 8*jt + p handles tiles
+// J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each: 32 consecutive
+// trellis steps from a word-aligned window per tile (code words loaded two
+// tiles ahead of their decode), with the x pairs of the tile's 16 columns read
+// from L1/L2.  Per column one packed binary16 FMA (HFMA2):
 //   3INST  acc += (lo, hi) * (x, x)   -- the two halves of the mask/XOR step,
 //          so lo*x + hi*x is the weight times x without a separate add;
 //   1MAD   acc += (S_a - 510, S_b - 510) * (x, x) for rows 2p and 2p+1, the
@@ -35,10 +39,10 @@
 // tile-row partial sum and about 7e-4 of the result (relative L2).
 //
 // Combine: a warp-shuffle reduction over the 4 tile groups and fp32 atomic adds
-// of each segment's row sums into zacc.  No CTA waits on another; the kernel
-// boundary orders the sums before the epilogue kernel.  The atomic adds make
-// the fp32 summation order, and so the last bit of some outputs, vary from
-// run to run.
+// of each sub-unit's 16 row sums into zacc.  No CTA waits on another; the
+// kernel boundary orders the sums before the epilogue kernel.  The atomic adds
+// make the fp32 summation order, and so the last bit of some outputs, vary
+// from run to run.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -46,7 +50,17 @@
 
 namespace exl3 {
 
-constexpr int kLayerThreads = 256;
+// ---- segment kernel (layers with under about 1024 tiles per SM) ------------
+// Five 256-thread CTAs per SM at batch 1 (four at 2).  The (m/128 row blocks)
+// x (n/16 tile columns) work units are cut into gridDim.x equal contiguous
+// ranges, one per CTA; a range is a sequence of segments inside one row block.
+// Warp w owns tile row w of the segment's row block, lane 8*jt + p tiles
+// ja + jt, ja + jt + 4, ... and row pair 2p, 2p+1.  Each segment starts by
+// rotating the x columns it needs into shared memory (one warp per overlapping
+// 128-block: signs, FWHT, 1/sqrt(128), x factor, binary16 pairs), so no
+// separate x-pair kernel runs; the decode and MAC are those of the sub-unit
+// kernel below.
+constexpr int kSegThreads = 256;
 // Longest segment (tile columns) handled between two shared-memory refills of
 // the rotated x.
 constexpr int kSegTiles = 64;
@@ -72,12 +86,12 @@ __device__ __forceinline__ void store_half4(__half* p, const float (&v)[4]) {
 
 // Resident 256-thread CTAs per SM the kernel is compiled for (registers).
 template <int MB>
-__host__ __device__ constexpr int layer_ctas_per_sm() {
+__host__ __device__ constexpr int seg_ctas_per_sm() {
   return MB == 1 ? 5 : MB == 2 ? 4 : 1;
 }
 
 template <int K, int CB, int MB>
-__global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_kernel(LayerArgs a) {
+__global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_kernel(LayerArgs a) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -126,7 +140,7 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
       const int c_hi = jb * 16;
       const int kb0 = c_lo / kRowBlock;
       const int nkb = (c_hi - 1) / kRowBlock - kb0 + 1;
-      for (int job = warp; job < MB * nkb; job += kLayerThreads / 32) {
+      for (int job = warp; job < MB * nkb; job += kSegThreads / 32) {
         const int b = job / nkb;
         const int col = (kb0 + job - b * nkb) * kRowBlock + 4 * lane;
         float v[4];
@@ -238,11 +252,171 @@ __global__ void __launch_bounds__(kLayerThreads, layer_ctas_per_sm<MB>()) layer_
   }
 }
 
+// ---- sub-unit kernel (larger layers) -------------------------------------------
+
+// Warps of the one CTA per SM: 32 (1024 threads) at batch 1, 24 for chunks of
+// 2, 16 for 4, 8 for 8 (registers).
+template <int MB>
+__host__ __device__ constexpr int layer_warps() {
+  return MB == 1 ? 32 : MB == 2 ? 24 : MB == 4 ? 16 : 8;
+}
+// Registers per thread of the batch-1 kernel.  For K <= 3, 56 x 1024 leaves
+// 8192 of the SM's 65536 registers, room for one 128-thread CTA of the output
+// kernel to be resident, waiting, when the layer kernel finishes (the batch-2
+// kernel, 768 x 80, leaves 4096); wider code words need all 64.
+template <int K>
+__host__ __device__ constexpr int layer_max_regs() {
+  return K <= 3 ? 56 : 64;
+}
+
+template <int K, int CB, int MB>
+__device__ __forceinline__ void layer_body(const LayerArgs& a) {
+  constexpr int kWarps = layer_warps<MB>();
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int jt = lane >> 3;
+  const int p = lane & 7;
+  constexpr int kTw = RowPair<K>::kTileWords;
+  const int nt = a.n / 16;
+  const int S = a.sub;
+  const int per_row = (nt + S - 1) / S;  // sub-units per tile row
+  const long long units = static_cast<long long>(a.m / 16) * per_row;
+  const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
+  const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
+  const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
+  __shared__ int next_unit;
+
+  // The output kernel may be scheduled now (it waits for this grid to finish).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) next_unit = 0;
+  __syncthreads();
+
+  bool waited = false;
+  int u = u_lo + warp;  // first sub-unit: one per warp; then from the counter
+  while (u < u_hi) {
+    const int I = u / per_row;
+    const int J0 = (u - I * per_row) * S;
+    const int J1 = J0 + S < nt ? J0 + S : nt;
+    const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
+
+    // Code words are loaded two tiles ahead of their decode.
+    int J = J0 + jt;
+    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
+    if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
+    if (J + 4 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
+    // The x pairs and the zeroed row sums come from the preceding grids on the
+    // stream; the code words above do not.
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
+    // Take the next sub-unit now; its latency hides under this one.
+    int un = 0;
+    if (lane == 0) un = u_lo + kWarps + atomicAdd(&next_unit, 1);
+    un = __shfl_sync(0xFFFFFFFFu, un, 0);
+
+    float acc[MB][2];
+#pragma unroll
+    for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+
+    while (J < J1) {
+      uint32_t st[32];
+      pair_states<K>(w0, st);
+#pragma unroll
+      for (int i = 0; i < RowPair<K>::kPairWords; ++i) w0[i] = w1[i];
+      if (J + 8 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 8) * kTw, p, w1);
+      const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
+      J += 4;
+      __half2 ha[MB], hb[MB];
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        ha[b] = __float2half2_rn(0.f);
+        hb[b] = __float2half2_rn(0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 xv[MB];
+#pragma unroll
+        for (int b = 0; b < MB; ++b) xv[b] = xrow[static_cast<size_t>(b) * (a.n / 4) + q];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * q + j;
+          const uint32_t xa = lcg(st[c]);
+          const uint32_t xb = lcg(st[16 + c]);
+          if constexpr (CB == kCb3Inst) {
+            const uint32_t pa = mask_xor_3inst(xa);
+            const uint32_t pb = mask_xor_3inst(xb);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
+              ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
+              hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
+            }
+          } else {
+            const uint32_t ra = __dp4a(xa, 0x01010101u, 0x6400u);
+            const uint32_t rb2 = __dp4a(xb, 0x01010101u, 0x6400u);
+            const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
+            const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        if constexpr (CB == kCb3Inst) {
+          acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
+          acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
+        } else {
+          acc[b][0] += __low2float(ha[b]);
+          acc[b][1] += __high2float(ha[b]);
+        }
+      }
+    }
+
+    // ---- warp-shuffle reduction over the 4 tile groups, accumulate into zacc --
+#pragma unroll
+    for (int b = 0; b < MB; ++b) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float v = acc[b][k];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        acc[b][k] = v;
+      }
+    }
+    if (jt == 0) {
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        float* z = a.zacc + static_cast<size_t>(b) * a.m + I * 16 + 2 * p;
+        atomicAdd(z, acc[b][0]);
+        atomicAdd(z + 1, acc[b][1]);
+      }
+    }
+    u = un;
+  }
+}
+
+template <int K, int CB, int MB>
+__global__ void __maxnreg__(layer_max_regs<K>()) layer_kernel(LayerArgs a) {
+  layer_body<K, CB, MB>(a);
+}
+
+template <int K, int CB, int MB>
+__global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) layer_kernel_wide(LayerArgs a) {
+  layer_body<K, CB, MB>(a);
+}
+
 template <int K, int CB, int MB>
 exl3_status launch_layer_t(const LayerArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
-  cfg.blockDim = dim3(kLayerThreads);
+  cfg.blockDim = dim3(32 * layer_warps<MB>());
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -250,28 +424,55 @@ exl3_status launch_layer_t(const LayerArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, layer_kernel<K, CB, MB>, a) != cudaSuccess) return EXL3_ERR_CUDA;
+  cudaError_t e;
+  if constexpr (MB == 1)
+    e = cudaLaunchKernelEx(&cfg, layer_kernel<K, CB, MB>, a);
+  else
+    e = cudaLaunchKernelEx(&cfg, layer_kernel_wide<K, CB, MB>, a);
+  if (e != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
 
-template <int K>
-exl3_status launch_layer_dispatch(const LayerArgs& a, int mb, cudaStream_t stream) {
-  if (a.codebook == kCb3Inst) {
+template <int K, int CB, int MB>
+exl3_status launch_seg_layer_t(const LayerArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
+  cfg.blockDim = dim3(kSegThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, seg_layer_kernel<K, CB, MB>, a) != cudaSuccess) return EXL3_ERR_CUDA;
+  return launch_status();
+}
+
+// a.sub == 0: the segment kernel (batch chunks of 1 or 2); else the sub-unit
+// kernel with a.sub tiles per sub-unit (reads the x pairs at a.xdup).
+template <int K, int CB>
+exl3_status launch_layer_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
+  if (a.sub == 0) {
     switch (mb) {
-      case 1: return launch_layer_t<K, kCb3Inst, 1>(a, stream);
-      case 2: return launch_layer_t<K, kCb3Inst, 2>(a, stream);
-      case 4: return launch_layer_t<K, kCb3Inst, 4>(a, stream);
-      case 8: return launch_layer_t<K, kCb3Inst, 8>(a, stream);
+      case 1: return launch_seg_layer_t<K, CB, 1>(a, stream);
+      case 2: return launch_seg_layer_t<K, CB, 2>(a, stream);
       default: return EXL3_ERR_BATCH;
     }
   }
   switch (mb) {
-    case 1: return launch_layer_t<K, kCb1Mad, 1>(a, stream);
-    case 2: return launch_layer_t<K, kCb1Mad, 2>(a, stream);
-    case 4: return launch_layer_t<K, kCb1Mad, 4>(a, stream);
-    case 8: return launch_layer_t<K, kCb1Mad, 8>(a, stream);
+    case 1: return launch_layer_t<K, CB, 1>(a, stream);
+    case 2: return launch_layer_t<K, CB, 2>(a, stream);
+    case 4: return launch_layer_t<K, CB, 4>(a, stream);
+    case 8: return launch_layer_t<K, CB, 8>(a, stream);
     default: return EXL3_ERR_BATCH;
   }
+}
+
+template <int K>
+exl3_status launch_layer_dispatch(const LayerArgs& a, int mb, cudaStream_t stream) {
+  return a.codebook == kCb3Inst ? launch_layer_cb<K, kCb3Inst>(a, mb, stream)
+                                : launch_layer_cb<K, kCb1Mad>(a, mb, stream);
 }
 
 }  // namespace exl3

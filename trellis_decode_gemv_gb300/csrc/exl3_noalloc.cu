@@ -75,8 +75,9 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
     return EXL3_ERR_ALIGN;
 
   // Scratch layout as in the workspace of exl3_gemv at batch 1: counters
-  // (+ status word) and the fp32 row sums.
-  const size_t need = bimg_offset(m, 1);
+  // (+ status word), the fp32 row sums, then the n x pairs.
+  const size_t zero_bytes = bimg_offset(m, 1);  // counters and row sums
+  const size_t need = zero_bytes + align256(sizeof(uint32_t) * static_cast<size_t>(n));
   if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
 
   void* scratch = nullptr;
@@ -84,7 +85,7 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // The row sums must start at zero; the array keeps whatever the previous
   // call left, so clear them (and the counters) on the stream first.
-  if (cudaMemsetAsync(scratch, 0, need, cs) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, zero_bytes, cs) != cudaSuccess) return EXL3_ERR_CUDA;
 
   char* base = static_cast<char*>(scratch);
   LayerArgs a{};
@@ -100,7 +101,14 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   a.y = reinterpret_cast<__half*>(y);
   a.counters = reinterpret_cast<uint32_t*>(base);
   a.zacc = reinterpret_cast<float*>(base + zacc_offset(m));
-  a.ctas = choose_layer_ctas(m, n, 1, device_sm_count());
+  const LayerPlan plan = plan_layer(m, n, 1, device_sm_count());
+  a.ctas = plan.ctas;
+  a.sub = plan.sub;
+  if (plan.sub > 0) {
+    uint32_t* xd = reinterpret_cast<uint32_t*>(base + zero_bytes);
+    if ((st = launch_xdup(a.x, a.s_in, xd, 1, n, codebook, cs)) != EXL3_OK) return st;
+    a.xdup = xd;
+  }
   if ((st = launch_k(a, cs)) != EXL3_OK) return st;
   return launch_epi(a.zacc, a.scales, a.s_out, a.y, 1, m, cs);
 }

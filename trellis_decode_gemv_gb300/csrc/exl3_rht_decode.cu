@@ -105,6 +105,46 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   *reinterpret_cast<uint2*>(bimg + off) = o;
 }
 
+// x pairs of the warp-shuffle layer kernel.  One warp per (row, 128-block):
+// x-tilde = Hb(s_in (.) x) / sqrt(128) (x itself without s_in), times the
+// code's x factor, rounded once to binary16 and duplicated into both halves of
+// a 32-bit word.
+__global__ void __launch_bounds__(kSmallThreads, 16)
+    xdup_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
+                uint32_t* __restrict__ xd, long long blocks, int n, float factor) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
+  if (job >= blocks) return;
+  const int per_row = n / kRowBlock;
+  const long long row = job / per_row;
+  const int kb = static_cast<int>(job - row * per_row);
+  const size_t off = static_cast<size_t>(row) * n + kb * kRowBlock + 4 * lane;
+  const uint2 xr = *reinterpret_cast<const uint2*>(x + off);
+  const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+  const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+  float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
+  if (signs != nullptr) {
+    const uint2 sr = *reinterpret_cast<const uint2*>(signs + kb * kRowBlock + 4 * lane);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+    v[0] *= __low2float(s01);
+    v[1] *= __high2float(s01);
+    v[2] *= __low2float(s23);
+    v[3] *= __high2float(s23);
+    fwht128_warp(v, lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
+  }
+  uint4 o;
+  o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0] * factor))) * 0x10001u;
+  o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1] * factor))) * 0x10001u;
+  o.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2] * factor))) * 0x10001u;
+  o.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3] * factor))) * 0x10001u;
+  *reinterpret_cast<uint4*>(xd + off) = o;
+}
+
 // Epilogue of the warp-shuffle layer: one warp per (batch row, 128-row block):
 // y = binary16(Hb(s_out (.) (scale (.) zacc))) and zacc := 0.  Launched as a
 // programmatic dependent of the layer kernel; waits for it before reading.
@@ -211,6 +251,26 @@ exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   bimg_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  return launch_status();
+}
+
+exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int rows, int n,
+                        int codebook, cudaStream_t stream) {
+  const long long blocks = static_cast<long long>(rows) * (n / kRowBlock);
+  const long long per_cta = kSmallThreads / 32;
+  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
+  const float factor = codebook == kCb1Mad ? kOneMadScale : 1.0f;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, xdup_kernel, x, s_in, xd, blocks, n, factor) != cudaSuccess)
+    return EXL3_ERR_CUDA;
   return launch_status();
 }
 
