@@ -222,6 +222,35 @@ def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None):
     return weights, dt
 
 
+# ---------------------------------------------------------------------------
+# multi-rank host logic (one replica per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself when
+    no process group runs."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier() -> None:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, steps: int, seconds: float) -> float:
+    """Units per second of the whole job: every rank processes its own
+    units_per_rank_step per step (weak scaling); seconds is the slowest rank's
+    time for `steps` steps."""
+    return units_per_rank_step * world * steps / seconds
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -349,8 +378,7 @@ def run_ours(args):
     bus = getattr(props, "pci_bus_id", None)
     clocks = ClockSampler(bus if isinstance(bus, str) else None)
     clocks.start()
-    if world > 1:
-        dist.barrier()
+    barrier()
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -360,16 +388,11 @@ def run_ours(args):
             replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
+    barrier()
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
     ms_step = ms_total / args.steps
-    value = weights_step * world / (ms_total / 1e3) * args.steps
+    value = whole_job_rate(weights_step, world, args.steps, ms_total / 1e3)
 
     # ---- per-launch durations (events around every launch) ---------------
     nrep = max(3, min(args.steps, 50))
@@ -441,8 +464,7 @@ def run_ours(args):
             step()
             Yh.copy_(Y, non_blocking=True)
         stream.synchronize()
-        if world > 1:
-            dist.barrier()
+        barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             X.copy_(Xh, non_blocking=True)
@@ -450,11 +472,8 @@ def run_ours(args):
             Yh.copy_(Y, non_blocking=True)
             stream.synchronize()
         t_e2e = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e = {"value": weights_step * world * e2e_steps / t_e2e, "unit": "weights/s",
+    t_e2e = max_over_ranks(t_e2e, dev)
+    e2e = {"value": whole_job_rate(weights_step, world, e2e_steps, t_e2e), "unit": "weights/s",
            "h2d_bytes_per_step": total_n * 2, "d2h_bytes_per_step": total_m * 2,
            "path": "binding call per GEMV (eager), pinned host x -> device, y -> pinned host"}
 

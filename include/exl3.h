@@ -159,6 +159,18 @@ typedef enum {
  */
 exl3_status exl3_set_path(int path);
 
+/**
+ * Failure-detection test hook (no counterpart in the pages).  While `on` is
+ * non-zero, the tensor-core kernel's operand-B producer posts nothing, so the
+ * bounded device-side wait for operand B runs out: every role of the kernel
+ * stops, waits (bounded) for its copies in flight, frees its tensor memory,
+ * and the kernel ORs 1 into the workspace status word (see
+ * exl3_workspace_bytes) before it exits.  The call's outputs are then not
+ * valid; later calls with the hook off are unaffected.  No GPU fault, trap or
+ * unbounded wait is involved.  Process-wide, like exl3_set_path.
+ */
+exl3_status exl3_debug_stall_tensor_wait(int on);
+
 /** Size of the fixed device array that exl3_gemv_noalloc uses as scratch. */
 #define EXL3_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -43,6 +43,13 @@ def _ws(m, n, M):
     return counters + zacc + bimg + bsum
 
 
+def test_debug_hook_and_path_setter(lib):
+    assert lib.exl3_debug_stall_tensor_wait(1) == 0
+    assert lib.exl3_debug_stall_tensor_wait(0) == 0
+    assert lib.exl3_set_path(3) == 5  # unknown path: rejected
+    assert lib.exl3_set_path(0) == 0
+
+
 def test_workspace_bytes(lib):
     assert B.exl3_workspace_bytes(100, 128, 1) == 0
     assert B.exl3_workspace_bytes(128, 128, 0) == 0

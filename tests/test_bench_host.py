@@ -1,0 +1,68 @@
+"""Host logic of bench.py that needs no GPU: the multi-rank timing reduction
+(two gloo ranks on CPU), whole-job rates, launch counting, algorithmic bytes
+and the reference arm's rank handling."""
+import io
+import os
+import socket
+import sys
+import contextlib
+
+import pytest
+
+import bench
+from trellis_decode_gemv_gb300 import synth
+
+
+def _free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    import torch.multiprocessing as mp
+
+    from tests import dist_helpers
+
+    world = 2
+    mp.spawn(dist_helpers.max_over_ranks_worker, args=(world, _free_port(), str(tmp_path)),
+             nprocs=world, join=True)
+    vals = [open(tmp_path / f"rank{r}.txt").read().split() for r in range(world)]
+    for t, rate in vals:
+        assert float(t) == 2.5  # the slowest rank's time on every rank
+        assert float(rate) == pytest.approx(1000.0 * 2 * 10 / 2.5)
+
+
+def test_single_process_reduction_is_identity():
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+    bench.barrier()  # no process group: a no-op
+    assert bench.whole_job_rate(5.0, 1, 4, 2.0) == 10.0
+
+
+def test_kernels_per_call():
+    sms = 152
+    assert bench.kernels_per_call("tensor", 1, 4096, 4096, sms) == 3
+    assert bench.kernels_per_call("auto", 3, 4096, 4096, sms) == 3
+    # small layer at batch 1: segment kernel + output kernel
+    assert bench.kernels_per_call("auto", 1, 4096, 4096, sms) == 2
+    # large layer at batch 1: x pairs + sub-unit kernel + output kernel
+    assert bench.kernels_per_call("auto", 1, 14336, 4096, sms) == 3
+    # forced warp-shuffle batch 5 on a small layer: chunk of 4 (3 kernels) + chunk of 1 (2)
+    assert bench.kernels_per_call("shuffle", 5, 1024, 4096, sms) == 5
+
+
+def test_algorithmic_bytes_and_ops():
+    w, b, ops = bench.algorithmic(4096, 4096, 2, synth.CB_1MAD, 1)
+    assert w == 4096 * 4096
+    assert b == 4096 * 4096 * 2 // 8 + 2 * 4096 + 2 * (4096 + 4096) + 2 * 4096 + 2 * 4096
+    assert ops == w * 5
+    assert bench.algorithmic(128, 256, 3, synth.CB_3INST, 2)[2] == 128 * 256 * 4
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    args = bench.argparse.Namespace(workload="single", batch=1, steps=1, warmup=0, gpus=2)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        assert bench.run_reference(args) == 0
+    assert out.getvalue() == ""

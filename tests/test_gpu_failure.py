@@ -1,0 +1,58 @@
+"""Failure detection of the tensor-core kernel, tested without a GPU fault.
+
+The test hook exl3_debug_stall_tensor_wait leaves the kernel's wait for
+operand B unsatisfied (the producer posts nothing).  The bounded wait runs out,
+every role stops, tensor memory is freed, and the kernel sets the workspace
+status word, which the host reads.  The next call, with the hook off, must be
+correct: the context stays usable.
+"""
+import time
+
+import pytest
+import torch
+
+from oracle import exl3_oracle as O
+from trellis_decode_gemv_gb300 import binding as B
+from trellis_decode_gemv_gb300 import synth
+from tests.gpu_helpers import assert_layer_close, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _call(d, K, cb, m, n, M, ws):
+    y = torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")
+    B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"], y=y,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    return y
+
+
+def test_tensor_wait_timeout_sets_status_and_context_survives():
+    m, n, K, cb, M = 384, 1280, 3, 1, 4
+    inp = synth.layer_inputs(m, n, K, M, config=90, index=0)
+    d = upload(inp)
+    ws = B.alloc_workspace(m, n, M, "cuda")
+    B.exl3_set_path(B.PATH_TENSOR)
+    try:
+        B.exl3_debug_stall_tensor_wait(True)
+        try:
+            t0 = time.perf_counter()
+            _call(d, K, cb, m, n, M, ws)
+            elapsed = time.perf_counter() - t0
+        finally:
+            B.exl3_debug_stall_tensor_wait(False)
+        print(f"stalled call returned after {elapsed:.3f} s")
+        assert B.workspace_status(ws, m) == 1
+        assert elapsed < 60.0
+        # the row sums were left at zero by the output kernel
+        zacc = ws[256:256 + 4 * M * m].view(torch.float32)
+        assert float(zacc.abs().sum()) == 0.0
+        # clear the status word; the next call is correct
+        off = 4 * (m // 128)
+        ws[off:off + 4].zero_()
+        y = _call(d, K, cb, m, n, M, ws)
+        assert B.workspace_status(ws, m) == 0
+        ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+        assert_layer_close(y, ref, "after a timed-out call")
+    finally:
+        B.exl3_set_path(B.PATH_AUTO)

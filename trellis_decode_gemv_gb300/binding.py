@@ -52,6 +52,7 @@ _SIGNATURES = {
     "exl3_gemm_small": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemv_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "exl3_set_path": ([_I], _I),
+    "exl3_debug_stall_tensor_wait": ([_I], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
     "exl3_version": ([], ctypes.c_char_p),
 }
@@ -126,6 +127,11 @@ PATH_AUTO, PATH_SHUFFLE, PATH_TENSOR = 0, 1, 2
 def exl3_set_path(path: int) -> None:
     """Select the kernel family of exl3_gemv / exl3_gemm_small (process-wide)."""
     _check(load_library().exl3_set_path(path))
+
+
+def exl3_debug_stall_tensor_wait(on: bool) -> None:
+    """Failure-detection test hook of the tensor-core kernel (see the header)."""
+    _check(load_library().exl3_debug_stall_tensor_wait(1 if on else 0))
 
 
 def workspace_status(workspace: torch.Tensor, m: int) -> int:

@@ -51,6 +51,7 @@ LayerPlan plan_layer(int m, int n, int mb, int sm_count) {
 namespace {
 
 std::atomic<int> g_path{EXL3_PATH_AUTO};
+std::atomic<int> g_debug_stall{0};
 
 exl3_status launch_tc(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                       cudaStream_t stream) {
@@ -109,6 +110,11 @@ extern "C" exl3_status exl3_set_path(int path) {
   if (path != EXL3_PATH_AUTO && path != EXL3_PATH_SHUFFLE && path != EXL3_PATH_TENSOR)
     return EXL3_ERR_BATCH;
   g_path.store(path, std::memory_order_relaxed);
+  return EXL3_OK;
+}
+
+extern "C" exl3_status exl3_debug_stall_tensor_wait(int on) {
+  g_debug_stall.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
   return EXL3_OK;
 }
 
@@ -175,6 +181,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.counters = reinterpret_cast<uint32_t*>(ws);
   a.status = a.counters + m / kRowBlock;
   a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
+  a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
   const int path = g_path.load(std::memory_order_relaxed);
   const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2);
   if (tensor) {

@@ -85,6 +85,7 @@ struct LayerArgs {
   const uint32_t* xdup;  // warp-shuffle kernel: x pairs [mb][n]
   int ctas;           // warp-shuffle kernel: grid size
   int sub;            // warp-shuffle kernel: tiles per sub-unit (16, 8 or 4)
+  int debug_stall;    // tensor-core kernel: test hook, post no operand B
 };
 
 // Internal launchers (one translation unit per K for the layer kernels).

@@ -437,7 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     }
   } else if (warp == kBWarp) {
     // ---- operand-B producer ----------------------------------------------------------
-    if (lane == 0) {
+    // With the failure-detection test hook set this warp posts nothing, so the
+    // MMA lane's bounded wait for operand B runs out.
+    if (lane == 0 && a.debug_stall == 0) {
       // The images are written by the preceding kernel on the stream.
       asm volatile("griddepcontrol.wait;" ::: "memory");
       int seq = 0;
