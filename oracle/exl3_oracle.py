@@ -25,10 +25,10 @@ source pages, named in its docstring:
 Where the pages leave a step open, the reading taken is stated next to the
 constant or function that embodies it.  The codebook constants (LCG multiplier
 and increment, 3INST mask and magic) are readings, not printed by the pages; the
-codebook *structure* is pinned by the tests in ``tests/test_oracle_*.py``, the
-numerical *quality* of these particular constants (the 3INST mean-squared error
-at 2 bits quoted in [TQ] Part nine) needs a trellis encoder and is
-"parity unpinned" here.
+codebook *structure* is pinned by the tests in ``tests/test_oracle_*.py``, and
+the numerical *quality* of these particular constants by the Viterbi encoder in
+``exl3_encoder`` against the mean-squared errors [TQ] Part nine prints for a
+Gaussian source at two bits per weight (``tests/test_oracle_encoder.py``).
 """
 from __future__ import annotations
 
