@@ -116,6 +116,49 @@ def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
     return launches
 
 
+def decoder_groups(gemvs, grouped: bool = True):
+    """Calls of one step: lists of GEMV indices.  A decoder applies q, k and v
+    (and gate and up) to the same step, so consecutive projections of one of
+    those families that share K and the code go into one exl3_gemm_grouped
+    call; everything else is one exl3_gemm_small call."""
+    def base(name):
+        parts = name.split(".")
+        return parts[1] if parts[0].startswith("L") and len(parts) > 1 else parts[0]
+
+    families = ({"q", "k", "v"}, {"gate", "up"})
+    out, i = [], 0
+    while i < len(gemvs):
+        fam = next((f for f in families if base(gemvs[i][0]) in f), None) if grouped else None
+        j = i + 1
+        if fam is not None:
+            seen = {base(gemvs[i][0])}
+            while (j < len(gemvs) and base(gemvs[j][0]) in fam and base(gemvs[j][0]) not in seen
+                   and gemvs[j][3] == gemvs[i][3] and gemvs[j][4] == gemvs[i][4]):
+                seen.add(base(gemvs[j][0]))
+                j += 1
+        out.append(list(range(i, j)))
+        i = j
+    return out
+
+
+def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
+    """Kernel launches of one grouped call over layers of the given (m, n):
+    three per batch chunk on the warp-shuffle path (x pairs, one sub-unit
+    kernel over every layer, output transform); one exl3_gemm_small-like
+    tensor-core chain (three kernels) per layer above batch 2."""
+    if len(shapes) == 1:
+        return kernels_per_call(path, M, shapes[0][0], shapes[0][1], sms)
+    tensor = path == "tensor" or (path == "auto" and M > 2)
+    if tensor:
+        return 3 * len(shapes)
+    chunks, rem = 0, M
+    for c in (8, 4, 2, 1):
+        while rem >= c:
+            rem -= c
+            chunks += 1
+    return 3 * chunks
+
+
 def algorithmic(m, n, K, cb, M):
     weights = m * n
     nbytes = m * n * K // 8 + 2 * m + 2 * (m + n) + 2 * M * n + 2 * M * m
@@ -335,10 +378,25 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.Stream(dev)
 
-    def step():
-        for c in calls:
+    groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
+                            grouped=not args.ungrouped)
+    gws = max([B.exl3_group_workspace_bytes([(calls[i]["m"], calls[i]["n"]) for i in g], M)
+               for g in groups if len(g) > 1] + [0])
+    if gws > ws.numel():
+        ws = torch.zeros(gws, dtype=torch.uint8, device=dev)
+
+    def run_group(g):
+        if len(g) == 1:
+            c = calls[g[0]]
             B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                               c["scales"], c["x"], y=c["y"], workspace=ws)
+        else:
+            c0 = calls[g[0]]
+            B.exl3_gemm_grouped([calls[i] for i in g], c0["K"], c0["cb"], workspace=ws)
+
+    def step():
+        for g in groups:
+            run_group(g)
 
     # Decode work (weights, integer ops) does not grow with the batch; the
     # multiply-accumulates do (macs = weights * M).
@@ -396,19 +454,23 @@ def run_ours(args):
 
     # ---- per-launch durations (events around every launch) ---------------
     nrep = max(3, min(args.steps, 50))
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
-    dur = np.zeros(len(calls))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
+    gdur = np.zeros(len(groups))
     with torch.cuda.stream(stream):
         for r in range(nrep + 1):
-            torch.cuda._sleep(int(2e6 + 4e4 * len(calls)))  # keep the queue ahead of the host
+            torch.cuda._sleep(int(2e6 + 4e4 * len(groups)))  # keep the queue ahead of the host
             evs[0].record(stream)
-            for i, c in enumerate(calls):
-                B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
-                                  c["scales"], c["x"], y=c["y"], workspace=ws)
+            for i, g in enumerate(groups):
+                run_group(g)
                 evs[i + 1].record(stream)
             torch.cuda.synchronize(dev)
             if r > 0:
-                dur += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(len(calls))]) * 1e-3
+                gdur += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(len(groups))]) * 1e-3
+    # a group's time is shared among its GEMVs in proportion to their weights
+    dur = np.zeros(len(calls))
+    for g, d in zip(groups, gdur):
+        w = np.array([calls[i]["m"] * calls[i]["n"] for i in g], dtype=np.float64)
+        dur[g] = d * w / w.sum()
     dur /= nrep
     # The eager per-call durations (events between calls) lose the overlap that
     # programmatic dependent launch gives inside the graph, so they only
@@ -436,8 +498,9 @@ def run_ours(args):
                 else f"HBM copy bandwidth ({peak_src})",
                 "kernel": kname,
                 "timing": "algorithmic ops (bytes) per step / graph-timed step, CUDA events on the launch stream",
-                "per_call_us_mean": 1e6 * t_step / len(calls),
-                "eager_call_us_mean": 1e6 * dur.sum() / len(calls)}
+                "per_call_us_mean": 1e6 * t_step / len(groups),
+                "eager_call_us_mean": 1e6 * dur.sum() / len(groups),
+                "calls_per_step": len(groups)}
     hbm = {"achieved_gbs": bytes_step / t_step / 1e9, "peak_gbs": hbm_gbs, "peak_source": peak_src,
            "frac": bytes_step / t_step / 1e9 / hbm_gbs}
     roof_pct = 100.0 * t_roof.sum() / t_step
@@ -496,13 +559,16 @@ def run_ours(args):
             "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
                        "weights_per_step": weights_step, "packed_bytes_per_step": packed,
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
-                       "cuda_graph": graph is not None, "kernel_path": args.path},
+                       "cuda_graph": graph is not None, "kernel_path": args.path,
+                       "calls": "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
+                       else "one exl3_gemm_small call per GEMV"},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
             "macs_per_s": value * M,
             "roofline_pct": roof_pct,
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * sum(kernels_per_call(args.path, M, c["m"], c["n"], sms) for c in calls),
+            "gpu_launches": args.steps * sum(
+                kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) for g in groups),
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -521,6 +587,8 @@ def main():
                     choices=["llama8b", "single", "llama70b", "mixed", "sweep"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ungrouped", action="store_true",
+                    help="one exl3_gemm_small call per GEMV (no grouped q/k/v and gate/up calls)")
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto",
                     help="kernel family of the fused layer (exl3_set_path)")
     args = ap.parse_args()

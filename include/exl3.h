@@ -144,6 +144,43 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
                             exl3_half *y, void *workspace, size_t workspace_bytes,
                             exl3_stream_t stream);
 
+/** Most layers in one exl3_gemm_grouped call. */
+#define EXL3_MAX_GROUP 8
+
+/** One layer of a grouped call (the arguments of exl3_gemm_small that differ
+ *  between layers; formats as above). */
+typedef struct {
+  const uint32_t *codes;   /* (m/16)*(n/16)*8K words */
+  int m, n;                /* positive multiples of 128 */
+  const exl3_half *s_in;   /* [n] or NULL */
+  const exl3_half *s_out;  /* [m] or NULL */
+  const exl3_half *scales; /* [m] */
+  const exl3_half *x;      /* [M][n] */
+  exl3_half *y;            /* [M][m] */
+} exl3_layer;
+
+/**
+ * Bytes of scratch for exl3_gemm_grouped over `layers` at batch M: a status
+ * word, then for every layer M*m fp32 row sums and M*n 32-bit x pairs (each
+ * 256-byte aligned).  Same zero-fill contract as exl3_workspace_bytes: the
+ * status word is at byte 0.  Returns 0 for an invalid group.
+ */
+size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
+
+/**
+ * `count` (1..EXL3_MAX_GROUP) independent layers that share K, the codebook
+ * and the batch M (1..EXL3_MAX_BATCH): the results equal `count` calls of
+ * exl3_gemm_small, in fewer kernel launches.  The pages have no counterpart;
+ * it serves decoders that apply several projections to the same step (q, k
+ * and v; gate and up).  `layers` is a host array read during the call.  No
+ * layer may read another layer's output (x of one aliasing y of another) in the
+ * same call.  At batch M <= 2 the layers share one chain of three kernels (x
+ * pairs, one decode+GEMV kernel over the tiles of every layer, output
+ * transform); above, each layer runs the tensor-core path in turn.
+ */
+exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
+                              void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
 /** Kernel family used by exl3_gemv / exl3_gemm_small. */
 typedef enum {
   EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, tensor-core kernel above */

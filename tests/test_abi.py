@@ -101,3 +101,43 @@ def test_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_LIB", None)
     monkeypatch.delenv("EXL3_LIBRARY")
     assert isinstance(B.load_library(), ctypes.CDLL)
+
+
+def _group(shapes, codes=A, x=A, y=A, scales=A):
+    arr = (B.Exl3Layer * len(shapes))()
+    for i, (m, n) in enumerate(shapes):
+        arr[i].codes, arr[i].m, arr[i].n = codes, m, n
+        arr[i].s_in = arr[i].s_out = A
+        arr[i].scales, arr[i].x, arr[i].y = scales, x, y
+    return arr
+
+
+def test_group_workspace_bytes(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
+    for M in (1, 2, 5, 32):
+        mb = min(M, 8)
+        shuffle = 256 + sum(a256(4 * mb * m) + a256(4 * mb * n) for m, n in shapes)
+        nb = 16 if M <= 16 else 32
+        tensor = 256 + a256(4 * M * 4096) + a256(2 * nb * 4096) + a256(4 * M * (4096 // 128))
+        assert lib.exl3_group_workspace_bytes(_group(shapes), 3, M) == max(shuffle, tensor)
+    assert lib.exl3_group_workspace_bytes(_group([(100, 128)]), 1, 1) == 0
+    assert lib.exl3_group_workspace_bytes(_group(shapes), 0, 1) == 0
+    assert lib.exl3_group_workspace_bytes(_group(shapes), 9, 1) == 0
+
+
+def test_grouped_validation(lib):
+    g = _group([(256, 256), (128, 384)])
+    ok = dict(K=2, cb=0, M=1, ws=A, wsb=1 << 30)
+
+    def call(arr=g, count=2, K=2, cb=0, M=1, ws=A, wsb=1 << 30):
+        return lib.exl3_gemm_grouped(arr, count, K, cb, M, ws, wsb, None)
+
+    assert call(arr=None) == 1
+    assert call(count=0) == 5 and call(count=9) == 5
+    assert call(K=0) == 3 and call(cb=2) == 4 and call(M=33) == 5
+    assert call(arr=_group([(256, 256), (130, 384)])) == 2
+    assert call(arr=_group([(256, 256)], codes=None), count=1) == 1
+    assert call(arr=_group([(256, 256)], x=A + 2), count=1) == 6
+    assert call(wsb=64) == 7 and call(ws=None) == 7
+    assert ok  # the remaining arguments are valid

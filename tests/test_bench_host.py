@@ -66,3 +66,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(args) == 0
     assert out.getvalue() == ""
+
+
+def test_decoder_groups():
+    g = bench.decoder_groups(synth.llama8b_layer_set())
+    assert len(g) == 24  # per (K, code): [q, k, v], [o], [gate, up], [down]
+    assert g[:4] == [[0, 1, 2], [3], [4, 5], [6]]
+    assert sum(len(x) for x in g) == 42
+    assert all(len(x) == 1 for x in bench.decoder_groups(synth.llama8b_layer_set(), grouped=False))
+    # gate and up of the mixed stack are grouped only when their widths agree
+    gemvs = synth.mixed_stack()
+    for x in bench.decoder_groups(gemvs):
+        assert len({(gemvs[i][3], gemvs[i][4]) for i in x}) == 1
+
+
+def test_kernels_per_group():
+    sms = 152
+    assert bench.kernels_per_group("auto", 1, [(4096, 4096), (1024, 4096), (1024, 4096)], sms) == 3
+    assert bench.kernels_per_group("auto", 5, [(4096, 4096), (1024, 4096)], sms) == 6
+    assert bench.kernels_per_group("shuffle", 5, [(4096, 4096), (1024, 4096)], sms) == 6
+    assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 2

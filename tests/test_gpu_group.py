@@ -1,0 +1,100 @@
+"""GPU parity of exl3_gemm_grouped: several independent layers in one call.
+
+Each layer's output is checked against the oracle's float64 layer (relative L2
+<= 5e-3, |err| <= 1e-2 * max|y_ref|) and against a separate exl3_gemm_small
+call on the same inputs (equal up to one binary16 rounding: the fp32 row sums
+are added in a different order)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import exl3_oracle as O
+from trellis_decode_gemv_gb300 import binding as B
+from trellis_decode_gemv_gb300 import synth
+from tests.gpu_helpers import assert_layer_close, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _layers(shapes, K, cb, M, config, rot=None):
+    out = []
+    for i, (m, n) in enumerate(shapes):
+        inp = synth.layer_inputs(m, n, K, M, config=config, index=i)
+        use_in, use_out = rot[i] if rot else (True, True)
+        if not use_in:
+            inp["s_in"] = None
+        if not use_out:
+            inp["s_out"] = None
+        d = upload({k: v for k, v in inp.items() if v is not None})
+        d.setdefault("s_in", None)
+        d.setdefault("s_out", None)
+        d.update(m=m, n=n, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
+        out.append((inp, d))
+    return out
+
+
+def _check(layers, K, cb, M):
+    for inp, d in layers:
+        m, n = d["m"], d["n"]
+        ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+        assert_layer_close(d["y"], ref, f"{m}x{n}")
+        single = B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+        torch.cuda.synchronize()
+        diff = (single.float() - d["y"].float()).abs().max()
+        assert float(diff) <= 2.0 ** -9 * float(single.float().abs().max()) + 1e-6
+
+
+@pytest.mark.parametrize("M", [1, 2, 5])
+@pytest.mark.parametrize("K,cb", [(3, 1), (2, 0)])
+def test_grouped_mixed_shapes(M, K, cb):
+    shapes = [(256, 384), (384, 1280), (128, 640)]
+    layers = _layers(shapes, K, cb, M, config=70 + M)
+    B.exl3_gemm_grouped([d for _, d in layers], K, cb)
+    torch.cuda.synchronize()
+    _check(layers, K, cb, M)
+
+
+@pytest.mark.parametrize("M", [3, 8])
+def test_grouped_forced_warp_shuffle_chunks(M):
+    shapes = [(256, 512), (512, 256)]
+    layers = _layers(shapes, 4, 1, M, config=75 + M)
+    B.exl3_set_path(B.PATH_SHUFFLE)
+    try:
+        B.exl3_gemm_grouped([d for _, d in layers], 4, 1)
+        torch.cuda.synchronize()
+    finally:
+        B.exl3_set_path(B.PATH_AUTO)
+    _check(layers, 4, 1, M)
+
+
+def test_grouped_rotations_off_and_single_layer():
+    shapes = [(256, 256), (384, 512), (128, 128)]
+    layers = _layers(shapes, 2, 1, 1, config=79, rot=[(False, True), (True, False), (False, False)])
+    B.exl3_gemm_grouped([d for _, d in layers], 2, 1)
+    torch.cuda.synchronize()
+    _check(layers, 2, 1, 1)
+    one = _layers([(640, 384)], 3, 0, 1, config=80)
+    B.exl3_gemm_grouped([d for _, d in one], 3, 0)
+    torch.cuda.synchronize()
+    _check(one, 3, 0, 1)
+
+
+def test_grouped_attention_projections_sampled():
+    """q, k, v of the 8B shapes (4096x4096, 1024x4096, 1024x4096) in one call,
+    K = 2, 1MAD, checked on sampled 128-row blocks of every layer; the group
+    workspace is reused for a second call."""
+    K, cb = 2, 1
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
+    layers = _layers(shapes, K, cb, 1, config=81)
+    ws = B.alloc_group_workspace(shapes, 1, "cuda")
+    for _ in range(2):
+        B.exl3_gemm_grouped([d for _, d in layers], K, cb, workspace=ws)
+        torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    for inp, d in layers:
+        m, n = d["m"], d["n"]
+        rbs = sorted({0, m // 128 - 1, m // 256})
+        ref = O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"],
+                                        inp["scales"], inp["x"], rbs)
+        cols = torch.cat([torch.arange(b * 128, b * 128 + 128) for b in rbs]).cuda()
+        assert_layer_close(d["y"][:, cols], ref, f"{m}x{n}")

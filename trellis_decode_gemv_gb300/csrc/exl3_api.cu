@@ -34,18 +34,20 @@ LayerPlan plan_layer(int m, int n, int mb, int sm_count) {
     plan.sub = 0;
     return plan;
   }
-  const int warps = mb == 1 ? 32 : mb == 2 ? 24 : mb == 4 ? 16 : 8;
-  int sub = 4;
-  if (per_cta >= 16LL * 2 * warps) {
-    sub = 16;
-  } else if (per_cta >= 8LL * 2 * warps) {
-    sub = 8;
-  }
+  const int sub = choose_sub(tiles, mb, sm_count);
   const int nt = n / 16;
   const long long units = static_cast<long long>(m / 16) * ((nt + sub - 1) / sub);
   plan.sub = sub;
   plan.ctas = static_cast<int>(units < sm_count ? units : sm_count);
   return plan;
+}
+
+int choose_sub(long long tiles, int mb, int sm_count) {
+  const int warps = mb == 1 ? 32 : mb == 2 ? 24 : mb == 4 ? 16 : 8;
+  const long long per_cta = tiles / sm_count;
+  if (per_cta >= 16LL * 2 * warps) return 16;
+  if (per_cta >= 8LL * 2 * warps) return 8;
+  return 4;
 }
 
 namespace {
@@ -68,6 +70,20 @@ exl3_status launch_tc(const LayerArgs& a, const __half* bimg, const float* bsum,
   }
 }
 
+exl3_status launch_group(const GroupArgs& a, int K, int codebook, int mb, cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_group_k1(a, codebook, mb, stream);
+    case 2: return launch_group_k2(a, codebook, mb, stream);
+    case 3: return launch_group_k3(a, codebook, mb, stream);
+    case 4: return launch_group_k4(a, codebook, mb, stream);
+    case 5: return launch_group_k5(a, codebook, mb, stream);
+    case 6: return launch_group_k6(a, codebook, mb, stream);
+    case 7: return launch_group_k7(a, codebook, mb, stream);
+    case 8: return launch_group_k8(a, codebook, mb, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
 exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
   switch (a.K) {
     case 1: return launch_layer_k1(a, mb, stream);
@@ -82,7 +98,60 @@ exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
   }
 }
 
+int batch_chunk(int rem) { return rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1; }
+
 }  // namespace
+
+exl3_status run_tensor(LayerArgs a, int M, float* zacc, uint32_t* status, __half* bimg, float* bsum,
+                       cudaStream_t cs) {
+  // x-tilde as operand-B images (and, for 1MAD, its block sums), then the
+  // persistent tensor-core kernel into zacc, then the output transform; the
+  // last two are programmatic dependents of the kernel before them.
+  a.zacc = zacc;
+  a.status = status;
+  if (a.codebook != EXL3_CB_1MAD) bsum = nullptr;
+  exl3_status st = launch_bimg(a.x, a.s_in, bimg, bsum, M, tc_nb(M), a.n, cs);
+  if (st != EXL3_OK) return st;
+  if ((st = launch_tc(a, bimg, bsum, M, device_sm_count(), cs)) != EXL3_OK) return st;
+  return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, a.m, cs);
+}
+
+exl3_status run_shuffle(LayerArgs a, int M, float* zacc, uint32_t* xd, cudaStream_t cs) {
+  const int sms = device_sm_count();
+  a.zacc = zacc;
+  const __half* x = a.x;
+  __half* y = a.y;
+  exl3_status st;
+  for (int done = 0; done < M;) {
+    const int mb = batch_chunk(M - done);
+    a.x = x + static_cast<size_t>(done) * a.n;
+    a.y = y + static_cast<size_t>(done) * a.m;
+    const LayerPlan plan = plan_layer(a.m, a.n, mb, sms);
+    if (plan.sub == 0) {
+      a.ctas = plan.ctas;
+      if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
+    } else {
+      if ((st = launch_xdup(a.x, a.s_in, xd, mb, a.n, a.codebook, cs)) != EXL3_OK) return st;
+      GroupArgs g{};
+      g.count = 1;
+      g.sub = plan.sub;
+      g.l[0].codes = a.codes;
+      g.l[0].xdup = xd;
+      g.l[0].zacc = zacc;
+      g.l[0].m = a.m;
+      g.l[0].n = a.n;
+      g.l[0].u_begin = 0;
+      g.l[0].per_row = (a.n / 16 + plan.sub - 1) / plan.sub;
+      g.units = (a.m / 16) * g.l[0].per_row;
+      g.ctas = plan.ctas;
+      if ((st = launch_group(g, a.K, a.codebook, mb, cs)) != EXL3_OK) return st;
+    }
+    if ((st = launch_epi(zacc, a.scales, a.s_out, a.y, mb, a.m, cs)) != EXL3_OK) return st;
+    done += mb;
+  }
+  return EXL3_OK;
+}
+
 }  // namespace exl3
 
 using namespace exl3;
@@ -167,7 +236,6 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const int sms = device_sm_count();
   LayerArgs a{};
   a.codes = codes;
   a.K = K;
@@ -177,43 +245,159 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   a.s_in = reinterpret_cast<const __half*>(s_in);
   a.s_out = reinterpret_cast<const __half*>(s_out);
   a.scales = reinterpret_cast<const __half*>(scales);
-  char* ws = static_cast<char*>(workspace);
-  a.counters = reinterpret_cast<uint32_t*>(ws);
-  a.status = a.counters + m / kRowBlock;
-  a.zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = reinterpret_cast<__half*>(y);
   a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws) + m / kRowBlock;
+  float* zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
   const int path = g_path.load(std::memory_order_relaxed);
-  const bool tensor = path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2);
-  if (tensor) {
-    // x-tilde as operand-B images (and, for 1MAD, its block sums), then the
-    // persistent tensor-core kernel into zacc, then the output transform; the
-    // last two are programmatic dependents of the kernel before them.
-    __half* bimg = reinterpret_cast<__half*>(ws + bimg_offset(m, M));
-    float* bsum = codebook == EXL3_CB_1MAD ? reinterpret_cast<float*>(ws + bsum_offset(m, n, M)) : nullptr;
-    a.y = reinterpret_cast<__half*>(y);
-    if ((st = launch_bimg(reinterpret_cast<const __half*>(x), a.s_in, bimg, bsum, M, tc_nb(M), n, cs)) !=
-        EXL3_OK)
-      return st;
-    if ((st = launch_tc(a, bimg, bsum, M, sms, cs)) != EXL3_OK) return st;
-    return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, m, cs);
-  }
+  if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2))
+    return run_tensor(a, M, zacc, status, reinterpret_cast<__half*>(ws + bimg_offset(m, M)),
+                      reinterpret_cast<float*>(ws + bsum_offset(m, n, M)), cs);
   // x pairs of each batch chunk go where the tensor path keeps its operand
   // images (at least 32 n bytes, enough for 8 rows of n 32-bit pairs).
-  uint32_t* xd = reinterpret_cast<uint32_t*>(ws + bimg_offset(m, M));
-  for (int done = 0; done < M;) {
-    const int rem = M - done;
-    const int mb = rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1;
-    a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
-    a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
-    const LayerPlan plan = plan_layer(m, n, mb, sms);
-    a.ctas = plan.ctas;
-    a.sub = plan.sub;
-    if (plan.sub > 0) {
-      if ((st = launch_xdup(a.x, a.s_in, xd, mb, n, codebook, cs)) != EXL3_OK) return st;
-      a.xdup = xd;
+  return run_shuffle(a, M, zacc, reinterpret_cast<uint32_t*>(ws + bimg_offset(m, M)), cs);
+}
+
+namespace {
+
+// Workspace of a group: the status word (first 256 bytes), then per layer its
+// fp32 row sums [mb][m] and x pairs [mb][n] (warp-shuffle), or one set of
+// tensor-path regions sized for the largest layer (the layers then run one
+// after another).
+size_t group_shuffle_bytes(const exl3_layer* L, int count, int M) {
+  const size_t mb = static_cast<size_t>(M < 8 ? M : 8);
+  size_t b = 256;
+  for (int i = 0; i < count; ++i)
+    b += align256(sizeof(float) * mb * L[i].m) + align256(sizeof(uint32_t) * mb * L[i].n);
+  return b;
+}
+
+size_t group_tensor_bytes(const exl3_layer* L, int count, int M) {
+  size_t maxm = 0, maxn = 0;
+  for (int i = 0; i < count; ++i) {
+    if (static_cast<size_t>(L[i].m) > maxm) maxm = L[i].m;
+    if (static_cast<size_t>(L[i].n) > maxn) maxn = L[i].n;
+  }
+  return 256 + align256(sizeof(float) * M * maxm) + align256(sizeof(__half) * tc_nb(M) * maxn) +
+         align256(sizeof(float) * M * (maxn / kRowBlock));
+}
+
+}  // namespace
+
+extern "C" size_t exl3_group_workspace_bytes(const exl3_layer* layers, int count, int M) {
+  if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP || M < 1 || M > EXL3_MAX_BATCH) return 0;
+  for (int i = 0; i < count; ++i)
+    if (check_shape(layers[i].m, layers[i].n) != EXL3_OK) return 0;
+  const size_t a = group_shuffle_bytes(layers, count, M);
+  const size_t b = group_tensor_bytes(layers, count, M);
+  return a > b ? a : b;
+}
+
+extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
+                                         void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
+  exl3_status st = check_k_cb(K, codebook);
+  if (st != EXL3_OK) return st;
+  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+  for (int i = 0; i < count; ++i) {
+    const exl3_layer& L = layers[i];
+    if ((st = check_shape(L.m, L.n)) != EXL3_OK) return st;
+    if (!L.codes || !L.scales || !L.x || !L.y) return EXL3_ERR_NULL;
+    if (!aligned16(L.codes) || !aligned16(L.scales) || !aligned16(L.x) || !aligned16(L.y) ||
+        (L.s_in && !aligned16(L.s_in)) || (L.s_out && !aligned16(L.s_out)))
+      return EXL3_ERR_ALIGN;
+  }
+  const size_t need = exl3_group_workspace_bytes(layers, count, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  auto args_of = [&](const exl3_layer& L) {
+    LayerArgs a{};
+    a.codes = L.codes;
+    a.K = K;
+    a.codebook = codebook;
+    a.m = L.m;
+    a.n = L.n;
+    a.s_in = reinterpret_cast<const __half*>(L.s_in);
+    a.s_out = reinterpret_cast<const __half*>(L.s_out);
+    a.scales = reinterpret_cast<const __half*>(L.scales);
+    a.x = reinterpret_cast<const __half*>(L.x);
+    a.y = reinterpret_cast<__half*>(L.y);
+    a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+    return a;
+  };
+  const int path = g_path.load(std::memory_order_relaxed);
+  if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2)) {
+    int maxm = 0, maxn = 0;
+    for (int i = 0; i < count; ++i) {
+      if (layers[i].m > maxm) maxm = layers[i].m;
+      if (layers[i].n > maxn) maxn = layers[i].n;
     }
-    if ((st = launch_layer(a, mb, cs)) != EXL3_OK) return st;
-    if ((st = launch_epi(a.zacc, a.scales, a.s_out, a.y, mb, m, cs)) != EXL3_OK) return st;
+    float* zacc = reinterpret_cast<float*>(ws + 256);
+    __half* bimg = reinterpret_cast<__half*>(ws + 256 + align256(sizeof(float) * M * maxm));
+    float* bsum = reinterpret_cast<float*>(reinterpret_cast<char*>(bimg) +
+                                           align256(sizeof(__half) * tc_nb(M) * maxn));
+    for (int i = 0; i < count; ++i)
+      if ((st = run_tensor(args_of(layers[i]), M, zacc, status, bimg, bsum, cs)) != EXL3_OK) return st;
+    return EXL3_OK;
+  }
+
+  // Warp-shuffle path: per batch chunk, the x pairs of every layer, one
+  // sub-unit kernel over the tiles of every layer, the output transform of
+  // every layer.
+  const int sms = device_sm_count();
+  const size_t mbmax = static_cast<size_t>(M < 8 ? M : 8);
+  float* zacc[kMaxGroup];
+  uint32_t* xd[kMaxGroup];
+  size_t off = 256;
+  long long tiles = 0;
+  for (int i = 0; i < count; ++i) {
+    zacc[i] = reinterpret_cast<float*>(ws + off);
+    off += align256(sizeof(float) * mbmax * layers[i].m);
+    xd[i] = reinterpret_cast<uint32_t*>(ws + off);
+    off += align256(sizeof(uint32_t) * mbmax * layers[i].n);
+    tiles += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
+  }
+  for (int done = 0; done < M;) {
+    const int mb = batch_chunk(M - done);
+    XdupGroup xg{};
+    EpiGroup eg{};
+    GroupArgs g{};
+    xg.count = eg.count = g.count = count;
+    xg.rows = eg.rows = mb;
+    g.sub = choose_sub(tiles, mb, sms);
+    int units = 0;
+    for (int i = 0; i < count; ++i) {
+      const exl3_layer& L = layers[i];
+      xg.e[i].x = reinterpret_cast<const __half*>(L.x) + static_cast<size_t>(done) * L.n;
+      xg.e[i].s_in = reinterpret_cast<const __half*>(L.s_in);
+      xg.e[i].xd = xd[i];
+      xg.e[i].n = L.n;
+      g.l[i].codes = L.codes;
+      g.l[i].xdup = xd[i];
+      g.l[i].zacc = zacc[i];
+      g.l[i].m = L.m;
+      g.l[i].n = L.n;
+      g.l[i].u_begin = units;
+      g.l[i].per_row = (L.n / 16 + g.sub - 1) / g.sub;
+      units += (L.m / 16) * g.l[i].per_row;
+      eg.e[i].zacc = zacc[i];
+      eg.e[i].scales = reinterpret_cast<const __half*>(L.scales);
+      eg.e[i].s_out = reinterpret_cast<const __half*>(L.s_out);
+      eg.e[i].y = reinterpret_cast<__half*>(L.y) + static_cast<size_t>(done) * L.m;
+      eg.e[i].m = L.m;
+    }
+    g.units = units;
+    g.ctas = units < sms ? units : sms;
+    if ((st = launch_xdup_group(xg, codebook, cs)) != EXL3_OK) return st;
+    if ((st = launch_group(g, K, codebook, mb, cs)) != EXL3_OK) return st;
+    if ((st = launch_epi_group(eg, cs)) != EXL3_OK) return st;
     done += mb;
   }
   return EXL3_OK;

@@ -71,6 +71,59 @@ struct LayerPlan {
 };
 LayerPlan plan_layer(int m, int n, int mb, int sm_count);
 
+// ---- groups of independent layers (exl3_gemm_grouped) ---------------------------
+constexpr int kMaxGroup = EXL3_MAX_GROUP;
+
+// One layer of the sub-unit kernel.  Its sub-units are numbered from u_begin
+// in the group's sequence, tile row major.
+struct GroupLayer {
+  const uint32_t* codes;
+  const uint32_t* xdup;  // x pairs [mb][n]
+  float* zacc;           // fp32 row sums [mb][m]
+  int m, n;
+  int u_begin;
+  int per_row;           // sub-units per tile row
+};
+
+struct GroupArgs {
+  GroupLayer l[kMaxGroup];
+  int count;
+  int units;  // sub-units of all layers
+  int sub;    // tiles per sub-unit
+  int ctas;
+};
+
+// x pairs and output transforms of a group: one warp per (layer, batch row,
+// 128-block); the jobs of layer i start at job_begin.
+struct XdupEntry {
+  const __half* x;      // [rows][n]
+  const __half* s_in;   // [n] or nullptr
+  uint32_t* xd;         // [rows][n]
+  int n;
+  long long job_begin;
+};
+struct XdupGroup {
+  XdupEntry e[kMaxGroup];
+  int count;
+  int rows;
+  float factor;         // the code's x factor
+  long long jobs;
+};
+struct EpiEntry {
+  float* zacc;            // [rows][m], zeroed after reading
+  const __half* scales;   // [m]
+  const __half* s_out;    // [m] or nullptr
+  __half* y;              // [rows][m]
+  int m;
+  long long job_begin;
+};
+struct EpiGroup {
+  EpiEntry e[kMaxGroup];
+  int count;
+  int rows;
+  long long jobs;
+};
+
 struct LayerArgs {
   const uint32_t* codes;
   int K, codebook, m, n;
@@ -97,6 +150,32 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 // NULL the fp32 sums bsum[b * (n/128) + kb] of the binary16 values.
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream);
+exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream);
+exl3_status launch_epi_group(EpiGroup g, cudaStream_t stream);
+// The sub-unit kernel over a group (a.sub > 0 tiles per sub-unit, a.ctas CTAs).
+exl3_status launch_group_k1(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k2(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k3(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k4(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k5(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k6(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k7(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_group_k8(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
+// One layer through the tensor-core path (operand images, MMA kernel, output
+// transform) or through the warp-shuffle path (batch chunks of 8/4/2/1; x pairs
+// and the sub-unit kernel, or the segment kernel, then the output transform),
+// with explicit workspace regions: fp32 row sums zacc [M][m] (zero on entry and
+// exit), the status word, operand images bimg and block sums bsum (tensor), x
+// pairs xd [8][n] (warp-shuffle).
+exl3_status run_tensor(LayerArgs a, int M, float* zacc, uint32_t* status, __half* bimg, float* bsum,
+                       cudaStream_t cs);
+exl3_status run_shuffle(LayerArgs a, int M, float* zacc, uint32_t* xd, cudaStream_t cs);
+
+// Sub-unit size S in {16, 8, 4} for `tiles` tiles at batch chunk mb: the
+// largest that still gives every warp of the one CTA per SM about two
+// sub-units.
+int choose_sub(long long tiles, int mb, int sm_count);
+
 // x pairs of the warp-shuffle kernel: for each of `rows` rows of x, x-tilde =
 // Hb(s_in (.) x) (x without s_in) times the code's x factor (1 for 3INST,
 // 1/sqrt(21845) for 1MAD), rounded to binary16 and duplicated into both halves

@@ -270,7 +270,7 @@ __host__ __device__ constexpr int layer_max_regs() {
 }
 
 template <int K, int CB, int MB>
-__device__ __forceinline__ void layer_body(const LayerArgs& a) {
+__device__ __forceinline__ void layer_body(const GroupArgs& g) {
   constexpr int kWarps = layer_warps<MB>();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -278,10 +278,8 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a) {
   const int jt = lane >> 3;
   const int p = lane & 7;
   constexpr int kTw = RowPair<K>::kTileWords;
-  const int nt = a.n / 16;
-  const int S = a.sub;
-  const int per_row = (nt + S - 1) / S;  // sub-units per tile row
-  const long long units = static_cast<long long>(a.m / 16) * per_row;
+  const int S = g.sub;
+  const long long units = g.units;
   const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
   const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
   const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
@@ -295,8 +293,14 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a) {
   bool waited = false;
   int u = u_lo + warp;  // first sub-unit: one per warp; then from the counter
   while (u < u_hi) {
-    const int I = u / per_row;
-    const int J0 = (u - I * per_row) * S;
+    // the layer of sub-unit u, then its tile row and first tile column
+    int li = 0;
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    const GroupLayer& a = g.l[li];
+    const int nt = a.n / 16;
+    const int lu = u - a.u_begin;
+    const int I = lu / a.per_row;
+    const int J0 = (lu - I * a.per_row) * S;
     const int J1 = J0 + S < nt ? J0 + S : nt;
     const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
 
@@ -403,17 +407,17 @@ __device__ __forceinline__ void layer_body(const LayerArgs& a) {
 }
 
 template <int K, int CB, int MB>
-__global__ void __maxnreg__(layer_max_regs<K>()) layer_kernel(LayerArgs a) {
-  layer_body<K, CB, MB>(a);
+__global__ void __maxnreg__(layer_max_regs<K>()) layer_kernel(const GroupArgs g) {
+  layer_body<K, CB, MB>(g);
 }
 
 template <int K, int CB, int MB>
-__global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) layer_kernel_wide(LayerArgs a) {
-  layer_body<K, CB, MB>(a);
+__global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) layer_kernel_wide(const GroupArgs g) {
+  layer_body<K, CB, MB>(g);
 }
 
 template <int K, int CB, int MB>
-exl3_status launch_layer_t(const LayerArgs& a, cudaStream_t stream) {
+exl3_status launch_layer_t(const GroupArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
   cfg.blockDim = dim3(32 * layer_warps<MB>());
@@ -449,17 +453,19 @@ exl3_status launch_seg_layer_t(const LayerArgs& a, cudaStream_t stream) {
   return launch_status();
 }
 
-// a.sub == 0: the segment kernel (batch chunks of 1 or 2); else the sub-unit
-// kernel with a.sub tiles per sub-unit (reads the x pairs at a.xdup).
+// The segment kernel (batch chunks of 1 or 2).
 template <int K, int CB>
-exl3_status launch_layer_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
-  if (a.sub == 0) {
-    switch (mb) {
-      case 1: return launch_seg_layer_t<K, CB, 1>(a, stream);
-      case 2: return launch_seg_layer_t<K, CB, 2>(a, stream);
-      default: return EXL3_ERR_BATCH;
-    }
+exl3_status launch_seg_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
+  switch (mb) {
+    case 1: return launch_seg_layer_t<K, CB, 1>(a, stream);
+    case 2: return launch_seg_layer_t<K, CB, 2>(a, stream);
+    default: return EXL3_ERR_BATCH;
   }
+}
+
+// The sub-unit kernel over a group of layers.
+template <int K, int CB>
+exl3_status launch_group_cb(const GroupArgs& a, int mb, cudaStream_t stream) {
   switch (mb) {
     case 1: return launch_layer_t<K, CB, 1>(a, stream);
     case 2: return launch_layer_t<K, CB, 2>(a, stream);
@@ -471,8 +477,14 @@ exl3_status launch_layer_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
 
 template <int K>
 exl3_status launch_layer_dispatch(const LayerArgs& a, int mb, cudaStream_t stream) {
-  return a.codebook == kCb3Inst ? launch_layer_cb<K, kCb3Inst>(a, mb, stream)
-                                : launch_layer_cb<K, kCb1Mad>(a, mb, stream);
+  return a.codebook == kCb3Inst ? launch_seg_cb<K, kCb3Inst>(a, mb, stream)
+                                : launch_seg_cb<K, kCb1Mad>(a, mb, stream);
+}
+
+template <int K>
+exl3_status launch_group_dispatch(const GroupArgs& a, int codebook, int mb, cudaStream_t stream) {
+  return codebook == kCb3Inst ? launch_group_cb<K, kCb3Inst>(a, mb, stream)
+                              : launch_group_cb<K, kCb1Mad>(a, mb, stream);
 }
 
 }  // namespace exl3
@@ -481,5 +493,8 @@ exl3_status launch_layer_dispatch(const LayerArgs& a, int mb, cudaStream_t strea
   namespace exl3 {                                                                             \
   exl3_status launch_layer_k##KK(const LayerArgs& a, int mb, cudaStream_t stream) {            \
     return launch_layer_dispatch<KK>(a, mb, stream);                                           \
+  }                                                                                            \
+  exl3_status launch_group_k##KK(const GroupArgs& a, int codebook, int mb, cudaStream_t stream) { \
+    return launch_group_dispatch<KK>(a, codebook, mb, stream);                                 \
   }                                                                                            \
   }

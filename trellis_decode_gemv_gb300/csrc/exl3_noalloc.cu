@@ -43,20 +43,6 @@ exl3_status scratch_address(void** out) {
   return EXL3_OK;
 }
 
-exl3_status launch_k(const LayerArgs& a, cudaStream_t stream) {
-  switch (a.K) {
-    case 1: return launch_layer_k1(a, 1, stream);
-    case 2: return launch_layer_k2(a, 1, stream);
-    case 3: return launch_layer_k3(a, 1, stream);
-    case 4: return launch_layer_k4(a, 1, stream);
-    case 5: return launch_layer_k5(a, 1, stream);
-    case 6: return launch_layer_k6(a, 1, stream);
-    case 7: return launch_layer_k7(a, 1, stream);
-    case 8: return launch_layer_k8(a, 1, stream);
-    default: return EXL3_ERR_K;
-  }
-}
-
 }  // namespace
 }  // namespace exl3
 
@@ -99,16 +85,6 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
   a.scales = reinterpret_cast<const __half*>(scales);
   a.x = reinterpret_cast<const __half*>(x);
   a.y = reinterpret_cast<__half*>(y);
-  a.counters = reinterpret_cast<uint32_t*>(base);
-  a.zacc = reinterpret_cast<float*>(base + zacc_offset(m));
-  const LayerPlan plan = plan_layer(m, n, 1, device_sm_count());
-  a.ctas = plan.ctas;
-  a.sub = plan.sub;
-  if (plan.sub > 0) {
-    uint32_t* xd = reinterpret_cast<uint32_t*>(base + zero_bytes);
-    if ((st = launch_xdup(a.x, a.s_in, xd, 1, n, codebook, cs)) != EXL3_OK) return st;
-    a.xdup = xd;
-  }
-  if ((st = launch_k(a, cs)) != EXL3_OK) return st;
-  return launch_epi(a.zacc, a.scales, a.s_out, a.y, 1, m, cs);
+  return run_shuffle(a, 1, reinterpret_cast<float*>(base + zacc_offset(m)),
+                     reinterpret_cast<uint32_t*>(base + zero_bytes), cs);
 }

@@ -105,28 +105,31 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   *reinterpret_cast<uint2*>(bimg + off) = o;
 }
 
-// x pairs of the warp-shuffle layer kernel.  One warp per (row, 128-block):
-// x-tilde = Hb(s_in (.) x) / sqrt(128) (x itself without s_in), times the
-// code's x factor, rounded once to binary16 and duplicated into both halves of
-// a 32-bit word.
-__global__ void __launch_bounds__(kSmallThreads, 16)
-    xdup_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
-                uint32_t* __restrict__ xd, long long blocks, int n, float factor) {
+// x pairs of the warp-shuffle layer kernel, for a group of layers.  One warp
+// per (layer, row, 128-block): x-tilde = Hb(s_in (.) x) / sqrt(128) (x itself
+// without s_in), times the code's x factor, rounded once to binary16 and
+// duplicated into both halves of a 32-bit word.
+__global__ void __launch_bounds__(kSmallThreads, 16) xdup_kernel(const XdupGroup g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
-  if (job >= blocks) return;
+  if (job >= g.jobs) return;
+  int li = 0;
+  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  const XdupEntry& e = g.e[li];
+  const int n = e.n;
   const int per_row = n / kRowBlock;
-  const long long row = job / per_row;
-  const int kb = static_cast<int>(job - row * per_row);
+  const long long local = job - e.job_begin;
+  const long long row = local / per_row;
+  const int kb = static_cast<int>(local - row * per_row);
   const size_t off = static_cast<size_t>(row) * n + kb * kRowBlock + 4 * lane;
-  const uint2 xr = *reinterpret_cast<const uint2*>(x + off);
+  const uint2 xr = *reinterpret_cast<const uint2*>(e.x + off);
   const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
   const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
   float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-  if (signs != nullptr) {
-    const uint2 sr = *reinterpret_cast<const uint2*>(signs + kb * kRowBlock + 4 * lane);
+  if (e.s_in != nullptr) {
+    const uint2 sr = *reinterpret_cast<const uint2*>(e.s_in + kb * kRowBlock + 4 * lane);
     const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
     const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
     v[0] *= __low2float(s01);
@@ -137,35 +140,40 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
   }
+  const float factor = g.factor;
   uint4 o;
   o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0] * factor))) * 0x10001u;
   o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1] * factor))) * 0x10001u;
   o.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2] * factor))) * 0x10001u;
   o.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3] * factor))) * 0x10001u;
-  *reinterpret_cast<uint4*>(xd + off) = o;
+  *reinterpret_cast<uint4*>(e.xd + off) = o;
 }
 
-// Epilogue of the warp-shuffle layer: one warp per (batch row, 128-row block):
-// y = binary16(Hb(s_out (.) (scale (.) zacc))) and zacc := 0.  Launched as a
-// programmatic dependent of the layer kernel; waits for it before reading.
-__global__ void __launch_bounds__(kSmallThreads, 16)
-    epi_kernel(float* __restrict__ zacc, const __half* __restrict__ scales,
-               const __half* __restrict__ s_out, __half* __restrict__ y, long long blocks, int m) {
+// Output transform of the layer kernels, for a group of layers: one warp per
+// (layer, batch row, 128-row block): y = binary16(Hb(s_out (.) (scale (.)
+// zacc))) and zacc := 0.  Launched as a programmatic dependent of the layer
+// kernel; waits for it before reading.
+__global__ void __launch_bounds__(kSmallThreads, 16) epi_kernel(const EpiGroup g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
-  if (job >= blocks) return;
+  if (job >= g.jobs) return;
+  int li = 0;
+  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  const EpiEntry& e = g.e[li];
+  const int m = e.m;
   const int per_row = m / kRowBlock;
-  const long long b = job / per_row;
-  const int rb = static_cast<int>(job - b * per_row);
+  const long long local = job - e.job_begin;
+  const long long b = local / per_row;
+  const int rb = static_cast<int>(local - b * per_row);
   const int r0 = rb * kRowBlock + 4 * lane;
-  float4* zp = reinterpret_cast<float4*>(zacc + b * m + r0);
+  float4* zp = reinterpret_cast<float4*>(e.zacc + b * m + r0);
   const float4 z = __ldcg(zp);
   *zp = make_float4(0.f, 0.f, 0.f, 0.f);
   float v[4] = {z.x, z.y, z.z, z.w};
   {
-    const uint2 sr = *reinterpret_cast<const uint2*>(scales + r0);
+    const uint2 sr = *reinterpret_cast<const uint2*>(e.scales + r0);
     const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
     const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
     v[0] *= __low2float(s01);
@@ -173,8 +181,8 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
     v[2] *= __low2float(s23);
     v[3] *= __high2float(s23);
   }
-  if (s_out != nullptr) {
-    const uint2 sr = *reinterpret_cast<const uint2*>(s_out + r0);
+  if (e.s_out != nullptr) {
+    const uint2 sr = *reinterpret_cast<const uint2*>(e.s_out + r0);
     const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
     const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
     v[0] *= __low2float(s01);
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   uint2 o;
   o.x = *reinterpret_cast<const uint32_t*>(&o01);
   o.y = *reinterpret_cast<const uint32_t*>(&o23);
-  *reinterpret_cast<uint2*>(y + b * m + r0) = o;
+  *reinterpret_cast<uint2*>(e.y + b * m + r0) = o;
 }
 
 template <int K, int CB>
@@ -254,12 +262,13 @@ exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float
   return launch_status();
 }
 
-exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int rows, int n,
-                        int codebook, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(rows) * (n / kRowBlock);
+namespace {
+
+template <typename G, typename Kern>
+exl3_status launch_pdl_small(Kern kernel, const G& g, cudaStream_t stream) {
   const long long per_cta = kSmallThreads / 32;
-  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  const float factor = codebook == kCb1Mad ? kOneMadScale : 1.0f;
+  const unsigned grid = static_cast<unsigned>((g.jobs + per_cta - 1) / per_cta);
+  if (grid == 0) return EXL3_OK;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kSmallThreads);
@@ -269,28 +278,54 @@ exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int r
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, xdup_kernel, x, s_in, xd, blocks, n, factor) != cudaSuccess)
-    return EXL3_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kernel, g) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
+}
+
+}  // namespace
+
+exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream) {
+  g.factor = codebook == kCb1Mad ? kOneMadScale : 1.0f;
+  g.jobs = 0;
+  for (int i = 0; i < g.count; ++i) {
+    g.e[i].job_begin = g.jobs;
+    g.jobs += static_cast<long long>(g.rows) * (g.e[i].n / kRowBlock);
+  }
+  return launch_pdl_small(xdup_kernel, g, stream);
+}
+
+exl3_status launch_epi_group(EpiGroup g, cudaStream_t stream) {
+  g.jobs = 0;
+  for (int i = 0; i < g.count; ++i) {
+    g.e[i].job_begin = g.jobs;
+    g.jobs += static_cast<long long>(g.rows) * (g.e[i].m / kRowBlock);
+  }
+  return launch_pdl_small(epi_kernel, g, stream);
+}
+
+exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int rows, int n,
+                        int codebook, cudaStream_t stream) {
+  XdupGroup g{};
+  g.count = 1;
+  g.rows = rows;
+  g.e[0].x = x;
+  g.e[0].s_in = s_in;
+  g.e[0].xd = xd;
+  g.e[0].n = n;
+  return launch_xdup_group(g, codebook, stream);
 }
 
 exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,
                        int m, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(rows) * (m / kRowBlock);
-  const long long per_cta = kSmallThreads / 32;
-  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kSmallThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, epi_kernel, zacc, scales, s_out, y, blocks, m) != cudaSuccess)
-    return EXL3_ERR_CUDA;
-  return launch_status();
+  EpiGroup g{};
+  g.count = 1;
+  g.rows = rows;
+  g.e[0].zacc = zacc;
+  g.e[0].scales = scales;
+  g.e[0].s_out = s_out;
+  g.e[0].y = y;
+  g.e[0].m = m;
+  return launch_epi_group(g, stream);
 }
 
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
