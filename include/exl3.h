@@ -145,7 +145,7 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
                             exl3_stream_t stream);
 
 /** Most layers in one exl3_gemm_grouped call. */
-#define EXL3_MAX_GROUP 8
+#define EXL3_MAX_GROUP 4
 
 /** One layer of a grouped call (the arguments of exl3_gemm_small that differ
  *  between layers; formats as above). */

@@ -98,3 +98,18 @@ def test_grouped_attention_projections_sampled():
                                         inp["scales"], inp["x"], rbs)
         cols = torch.cat([torch.arange(b * 128, b * 128 + 128) for b in rbs]).cuda()
         assert_layer_close(d["y"][:, cols], ref, f"{m}x{n}")
+
+
+def test_group_object_matches_oracle():
+    """binding.Exl3LinearGroup: bound x/y tensors, called twice with new x."""
+    shapes = [(256, 384), (384, 384)]
+    layers = _layers(shapes, 2, 0, 1, config=82)
+    grp = B.Exl3LinearGroup([d for _, d in layers], 2, 0)
+    grp()
+    for inp, d in layers:  # new inputs written into the bound x
+        x2 = synth.activations(1, d["n"], seed=synth.seed_for(83, d["m"]))
+        d["x"].copy_(torch.from_numpy(x2).cuda())
+        inp["x"] = x2
+    grp()
+    torch.cuda.synchronize()
+    _check(layers, 2, 0, 1)

@@ -184,3 +184,20 @@ def test_batch_sweep_sampled(M, shape):
 ])
 def test_mixed_stack_shapes_sampled(name, m, n, K):
     _sampled(name, m, n, K, 0, 1, config=4, index=K * 1000 + m // 128, blocks=2)
+
+
+def test_layer_object_matches_functional_call():
+    """binding.Exl3Linear (the layer marshalled once) gives the functional
+    call's result, for batch 1 and a smaller batch than it was built for."""
+    m, n, K, cb = 512, 768, 3, 1
+    inp = synth.layer_inputs(m, n, K, 2, config=68, index=0)
+    d = upload(inp)
+    lin = B.Exl3Linear(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], max_batch=2)
+    y2 = lin(d["x"])
+    y1 = lin(d["x"][0])
+    torch.cuda.synchronize()
+    ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    assert_layer_close(y2, ref, "batch 2")
+    assert_layer_close(y1.view(1, -1), ref[:1], "batch 1")
+    with pytest.raises(ValueError):
+        lin(torch.zeros(3, n, dtype=torch.float16, device="cuda"))

@@ -42,7 +42,7 @@ def library_path() -> str:
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
-MAX_GROUP = 8
+MAX_GROUP = 4
 
 
 class Exl3Layer(ctypes.Structure):
@@ -291,3 +291,63 @@ def exl3_gemm_grouped(layers, K, codebook, workspace=None):
                                  _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
                                  _stream(dev)))
     return [L["y"] for L in layers]
+
+
+class Exl3Linear:
+    """One quantized linear layer, marshalled once.
+
+    Holds the layer's device tensors (codes, signs, scales) and a workspace,
+    checked when the object is built; a call then only checks and passes x and
+    y.  Same computation as exl3_gemm_small:
+        y[M, m] = Hb(s_out (.) (scales (.) (W-hat Hb(s_in (.) x[M, n])))).
+    """
+
+    def __init__(self, codes, K, codebook, m, n, s_in, s_out, scales, max_batch=1):
+        lib = load_library()
+        self.device = codes.device
+        self.K, self.codebook, self.m, self.n = K, codebook, m, n
+        self._keep = (codes, s_in, s_out, scales)
+        dev = self.device
+        self._args = (_ptr(codes, "codes", _WORDS, dev), K, codebook, m, n,
+                      _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+                      _ptr(scales, "scales", _HALF, dev))
+        self.workspace = alloc_workspace(m, n, max_batch, dev)
+        self._ws = (self.workspace.data_ptr(), self.workspace.numel())
+        self._max_batch = max_batch
+        self._fn = lib.exl3_gemm_small
+
+    def __call__(self, x, y=None):
+        x2 = x if x.dim() == 2 else x.view(1, -1)
+        M = x2.shape[0]
+        if M > self._max_batch or x2.shape[1] != self.n:
+            raise ValueError(f"x of shape {tuple(x2.shape)} for a layer of n={self.n}, "
+                             f"batch up to {self._max_batch}")
+        if y is None:
+            y = torch.empty((M, self.m), dtype=torch.float16, device=self.device)
+        _check(self._fn(*self._args, M, _ptr(x2, "x", _HALF, self.device), _ptr(y, "y", _HALF, self.device),
+                        *self._ws, torch.cuda.current_stream(self.device).cuda_stream))
+        return y if x.dim() == 2 else y.view(-1)
+
+
+class Exl3LinearGroup:
+    """Independent layers (sharing K, the code and the batch) marshalled once
+    for exl3_gemm_grouped: each layer dict has codes, m, n, s_in, s_out,
+    scales, x [M, n] and y [M, m] -- x and y stay bound to those tensors, whose
+    contents change between calls (decoders write the step's input into x)."""
+
+    def __init__(self, layers, K, codebook):
+        lib = load_library()
+        self.device = layers[0]["codes"].device
+        self.K, self.codebook = K, codebook
+        self.M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+        self._keep = [dict(L) for L in layers]
+        self._arr = _layer_array(layers, self.device, self.M)
+        self.workspace = alloc_group_workspace([(L["m"], L["n"]) for L in layers], self.M, self.device)
+        self._ws = (self.workspace.data_ptr(), self.workspace.numel())
+        self._count = len(layers)
+        self._fn = lib.exl3_gemm_grouped
+
+    def __call__(self):
+        _check(self._fn(self._arr, self._count, self.K, self.codebook, self.M, *self._ws,
+                        torch.cuda.current_stream(self.device).cuda_stream))
+        return [L["y"] for L in self._keep]
