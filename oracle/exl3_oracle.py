@@ -69,6 +69,22 @@ ONE_MAD_SCALE_F32 = np.float32(1.0 / math.sqrt(ONE_MAD_VARIANCE))
 
 CB_3INST = 0
 CB_1MAD = 1
+CB_MCG = 2
+CB_MUL1 = 3
+
+#: mul1 masking, centring and scaling.  [TQ] Part eleven and Part twelve: the
+#: integer generator multiplies the state by a constant, masks each of the four
+#: bytes of the product down to six bits, sums the four bytes (dp4a against a
+#: vector of ones) and subtracts a fixed offset, giving an integer in about
+#: [-126, 126]; EXL3's mul1 moved to the same masked byte sum, and its weight
+#: is an affine function of it.  Reading: the offset is the mean of four
+#: uniform 6-bit values, 4 * 31.5 = 126, and the scale makes the variance one:
+#: 4 * (64**2 - 1) / 12 = 1365.
+MUL1_MASK = 0x3F3F3F3F
+MUL1_CENTRE = 126
+MUL1_VARIANCE = 1365
+#: 1/sqrt(1365) rounded once to binary32.
+MUL1_SCALE_F32 = np.float32(1.0 / math.sqrt(MUL1_VARIANCE))
 
 #: Blockwise Hadamard width.  [TQ] Part eleven: EXL3 rotates 128-blocks along
 #: each axis.
@@ -134,6 +150,44 @@ def lcg(states: np.ndarray) -> np.ndarray:
     return ((np.uint64(LCG_A) * s + np.uint64(LCG_B)) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
 
 
+def mcg(states: np.ndarray) -> np.ndarray:
+    """The multiplicative generator of MCG and mul1: x = A*s mod 2**32, the LCG
+    without its additive constant.  [TQ] Part eleven ("drops the additive
+    constant ... and keeps only the multiply").  Reading: the pages do not print
+    the multiplier they adopt; the one LCG multiplier they print (A) is used."""
+    s = np.asarray(states, dtype=np.uint64)
+    return ((np.uint64(LCG_A) * s) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+
+
+def _mask_xor_add(x: np.ndarray) -> np.ndarray:
+    """Steps two and three of the three-instruction code on a 32-bit x: mask
+    and XOR into two binary16 halves, one correctly rounded binary16 add."""
+    h = (x & np.uint32(MASK_3INST)) ^ np.uint32(MAGIC_3INST)
+    lo = (h & np.uint32(0xFFFF)).astype(np.uint16).view(np.float16)
+    hi = (h >> np.uint32(16)).astype(np.uint16).view(np.float16)
+    return (lo.astype(np.float64) + hi.astype(np.float64)).astype(np.float16)
+
+
+def code_mcg(states: np.ndarray) -> np.ndarray:
+    """MCG: the three-instruction code with the multiplicative generator.
+    [TQ] Part eleven.  Returns float16."""
+    return _mask_xor_add(mcg(states))
+
+
+def code_mul1(states: np.ndarray) -> np.ndarray:
+    """mul1: multiply, mask every byte of the product to six bits, sum the four
+    bytes, subtract 126, scale by 1/sqrt(1365).  [TQ] Parts eleven and twelve.
+
+    Precision reading as for 1MAD: (S - 126) is exact in binary32, multiplied by
+    the binary32 constant with one rounding, then rounded once to binary16.
+    Returns float16."""
+    x = mcg(states) & np.uint32(MUL1_MASK)
+    S = ((x & np.uint32(0xFF)) + ((x >> np.uint32(8)) & np.uint32(0xFF))
+         + ((x >> np.uint32(16)) & np.uint32(0xFF)) + (x >> np.uint32(24)))
+    centred = (S.astype(np.int64) - MUL1_CENTRE).astype(np.float32)
+    return (centred * MUL1_SCALE_F32).astype(np.float32).astype(np.float16)
+
+
 def code_3inst(states: np.ndarray) -> np.ndarray:
     """3INST: LCG, then mask-and-XOR into two binary16 halves, then one binary16
     add of the two halves.  [TQ] Part nine, steps one to three.
@@ -170,6 +224,10 @@ def decode_states(states: np.ndarray, codebook: int) -> np.ndarray:
         return code_3inst(states)
     if codebook == CB_1MAD:
         return code_1mad(states)
+    if codebook == CB_MCG:
+        return code_mcg(states)
+    if codebook == CB_MUL1:
+        return code_mul1(states)
     raise ValueError(f"unknown codebook {codebook}")
 
 

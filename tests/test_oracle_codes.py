@@ -151,9 +151,63 @@ def test_codebook_dispatch():
     st = np.array([0, 1, 0xFFFF], dtype=np.uint32)
     np.testing.assert_array_equal(O.decode_states(st, 0), O.code_3inst(st))
     np.testing.assert_array_equal(O.decode_states(st, 1), O.code_1mad(st))
+    np.testing.assert_array_equal(O.decode_states(st, 2), O.code_mcg(st))
+    np.testing.assert_array_equal(O.decode_states(st, 3), O.code_mul1(st))
     try:
-        O.decode_states(st, 2)
+        O.decode_states(st, 4)
     except ValueError:
         pass
     else:
         raise AssertionError("unknown codebook must raise")
+
+
+def test_mcg_generator_is_the_lcg_without_its_constant():
+    """x_MCG = A*s mod 2**32, so x_LCG - x_MCG = B (mod 2**32) for every state,
+    and the state 0 maps to x = 0, i.e. the two halves 0x3000 = 1/8 each and the
+    weight 1/4."""
+    x_m = O.mcg(ALL).astype(np.uint64)
+    x_l = O.lcg(ALL).astype(np.uint64)
+    assert np.all(((x_l - x_m) & 0xFFFFFFFF) == O.LCG_B)
+    assert float(O.code_mcg(np.array([0], dtype=np.uint32))[0]) == 0.25
+    for s in (1, 2, 12345, 0xFFFF):
+        x = (O.LCG_A * s) & 0xFFFFFFFF
+        h = (x & O.MASK_3INST) ^ O.MAGIC_3INST
+        lo = _half_bits_to_float(h & 0xFFFF)
+        hi = _half_bits_to_float(h >> 16)
+        assert O.code_mcg(np.array([s], dtype=np.uint32)).view(np.uint16)[0] == _round_to_half(lo + hi)
+
+
+def test_mcg_moments_match_3inst():
+    """Same mask/XOR/add as 3INST on another uniform generator: mean about 0,
+    variance about that of 3INST (the closed form of the 3INST test)."""
+    w = O.code_mcg(ALL).astype(np.float64)
+    w3 = O.code_3inst(ALL).astype(np.float64)
+    assert abs(w.mean()) < 0.02
+    assert abs(w.var() - w3.var()) < 0.05 * w3.var()
+
+
+def test_mul1_masked_byte_sum():
+    """w = fp16(fp32(S - 126) * fp32(1/sqrt(1365))) with S the sum of the four
+    bytes of A*s, each masked to six bits (checked with Python integers, exact
+    fractions and CPython's binary16 packing); S spans [0, 252]."""
+    c = Fraction(float(O.MUL1_SCALE_F32))
+    assert O.MUL1_SCALE_F32 == np.float32(1.0 / math.sqrt(1365))
+    w = O.code_mul1(ALL).view(np.uint16)
+    sums = []
+    for s in range(0, 1 << 16, 89):
+        x = (O.LCG_A * s) & 0xFFFFFFFF
+        S = sum((x >> (8 * k)) & 0x3F for k in range(4))
+        sums.append(S)
+        prod = float(np.float32(float((S - 126) * c)))
+        assert w[s] == _round_to_half(prod), s
+    assert min(sums) >= 0 and max(sums) <= 252
+
+
+def test_mul1_closed_form_moments():
+    """Four uniform 6-bit values: mean 126 and variance 4*(64**2-1)/12 = 1365,
+    so the weights have mean about 0 and variance about 1 over all states."""
+    assert 4 * 63 / 2 == O.MUL1_CENTRE and 4 * (64 ** 2 - 1) // 12 == O.MUL1_VARIANCE
+    w = O.code_mul1(ALL).astype(np.float64)
+    assert abs(w.mean()) < 0.02
+    assert abs(w.var() - 1.0) < 0.05
+    assert np.abs(w).max() <= 126 / math.sqrt(1365) * (1 + 2 ** -10)

@@ -93,12 +93,12 @@ def test_3inst_two_bit_mse(gaussian_tiles):
 
 
 def test_computed_codes_match_a_random_table(gaussian_tiles):
-    """Both computed codes do about as well as a truly random Gaussian table
+    """Every computed code does about as well as a truly random Gaussian table
     of the same size on the same samples."""
     rng = np.random.default_rng(99)
     table = rng.normal(size=1 << O.L)
     table /= np.sqrt(np.mean(table ** 2))
     ref = E.trellis_mse(table, gaussian_tiles, 2)
-    for cb in (O.CB_3INST, O.CB_1MAD):
+    for cb in (O.CB_3INST, O.CB_1MAD, O.CB_MCG, O.CB_MUL1):
         mse = E.trellis_mse(E.codebook_values(cb), gaussian_tiles, 2)
         assert abs(mse - ref) < 0.1 * ref, (cb, mse, ref)
