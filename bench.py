@@ -18,8 +18,9 @@ batch given by --batch).
 
 Roofline: per launch T_roof = max(packed+vector bytes / HBM bandwidth,
 decode integer ops / INT32 peak), integer ops per weight 4 (3INST: window
-funnel + mask, LCG multiply-add, mask/XOR) or 5 (1MAD: window funnel + mask,
-LCG, byte sum, int-to-float).  The HBM bandwidth is the measured copy bandwidth
+funnel + mask, LCG multiply-add, mask/XOR; MCG the same with a multiply), 5
+(1MAD: window funnel + mask, LCG, byte sum, int-to-float) or 6 (mul1: as 1MAD
+plus the six-bit byte mask).  The HBM bandwidth is the measured copy bandwidth
 of this GPU model; the INT32 peak is SMs x 128 integer lanes per clock (4
 schedulers x 32 lanes) x the maximum SM clock.
 
@@ -55,7 +56,9 @@ SM_COUNT_NOMINAL = 152
 SM_MAX_MHZ_NOMINAL = 2070.0
 INT_LANES_PER_SM_CLK = 128
 HBM_FALLBACK_GBS = 6800.0
-OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5}
+# MCG: as 3INST (a multiply instead of the multiply-add); mul1: as 1MAD plus
+# the six-bit byte mask
+OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5, synth.CB_MCG: 4, synth.CB_MUL1: 6}
 # DRAM traffic / algorithmic bytes of the dominant kernel, from the ncu
 # captures of those kernels (dram__bytes_read.sum +
 # dram__bytes_write.sum of the captured launches over their algorithmic bytes).
@@ -80,6 +83,10 @@ def workload(name: str, batch: int):
         desc = ("Llama-3-8B-shaped layer set at batch 1: q/o 4096x4096, k/v 1024x4096, "
                 "gate/up 14336x4096, down 4096x14336, each at K=2,3,4 x {1MAD,3INST}")
         return desc, 1, synth.llama8b_layer_set(), 1
+    if name == "llama8b-mcg-mul1":
+        desc = ("Llama-3-8B-shaped layer set at batch 1 with the MCG and mul1 codes: q/o 4096x4096, "
+                "k/v 1024x4096, gate/up 14336x4096, down 4096x14336, each at K=2,3,4")
+        return desc, 5, synth.llama8b_layer_set((synth.CB_MCG, synth.CB_MUL1)), 1
     if name == "single":
         # 32 distinct 4096x4096 layers (128 MB of codes) so that the timed
         # steps stream from HBM rather than L2
@@ -508,7 +515,7 @@ def run_ours(args):
     # per-(K, code) summary
     per = {}
     for c, d, a, th, ti in zip(calls, t_call, alg, t_hbm, t_int):
-        key = f"K{c['K']}.{'1mad' if c['cb'] else '3inst'}"
+        key = f"K{c['K']}.{synth.CODE_NAMES[c['cb']]}"
         e = per.setdefault(key, [0.0, 0, 0.0])
         e[0] += d
         e[1] += a[0]
@@ -603,7 +610,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b",
-                    choices=["llama8b", "single", "llama70b", "mixed", "sweep"])
+                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",

@@ -74,7 +74,12 @@ typedef enum {
 
 /** Computed codes of Lecture 1b Part nine.  Ids 2 (MCG) and 3 (mul1) are
  *  reserved and rejected with EXL3_ERR_CODEBOOK. */
-typedef enum { EXL3_CB_3INST = 0, EXL3_CB_1MAD = 1 } exl3_codebook;
+/** Computed codes ("Trellis Quantization" Parts nine, eleven and twelve):
+ *  3INST and 1MAD on the LCG x = A*s + B; MCG (3INST on the multiplicative
+ *  generator x = A*s) and mul1 (six-bit masked byte sum of A*s, minus 126,
+ *  times 1/sqrt(1365)) as far as the pages fix them; A = 0x9E3779B9,
+ *  B = 0x7F4A7C15. */
+typedef enum { EXL3_CB_3INST = 0, EXL3_CB_1MAD = 1, EXL3_CB_MCG = 2, EXL3_CB_MUL1 = 3 } exl3_codebook;
 
 /** Largest batch accepted by exl3_gemm_small. */
 #define EXL3_MAX_BATCH 32

@@ -65,7 +65,7 @@ def _gemm(lib, m=256, n=256, K=2, cb=0, M=1, codes=A, scales=A, x=A, y=A, s_in=A
 
 @pytest.mark.parametrize("kw,status", [
     (dict(m=100), 2), (dict(n=130), 2), (dict(m=0), 2), (dict(n=-128), 2),
-    (dict(K=0), 3), (dict(K=9), 3), (dict(cb=2), 4), (dict(cb=-1), 4),
+    (dict(K=0), 3), (dict(K=9), 3), (dict(cb=4), 4), (dict(cb=-1), 4),
     (dict(M=0), 5), (dict(M=33), 5),
     (dict(codes=None), 1), (dict(scales=None), 1), (dict(x=None), 1), (dict(y=None), 1),
     (dict(codes=A + 4), 6), (dict(x=A + 2), 6), (dict(y=A + 8), 6), (dict(s_in=A + 2), 6),
@@ -84,7 +84,7 @@ def test_gemv_validation(lib):
 def test_decode_and_rht_validation(lib):
     assert lib.exl3_decode_tiles(A, 2, 0, 128, 96, A, None) == 2
     assert lib.exl3_decode_tiles(A, 10, 0, 128, 128, A, None) == 3
-    assert lib.exl3_decode_tiles(A, 2, 3, 128, 128, A, None) == 4
+    assert lib.exl3_decode_tiles(A, 2, 4, 128, 128, A, None) == 4
     assert lib.exl3_decode_tiles(None, 2, 0, 128, 128, A, None) == 1
     assert lib.exl3_decode_tiles(A + 4, 2, 0, 128, 128, A, None) == 6
     assert lib.exl3_rht_in(A, A, A, 0, 128, None) == 5
@@ -135,7 +135,7 @@ def test_grouped_validation(lib):
 
     assert call(arr=None) == 1
     assert call(count=0) == 5 and call(count=5) == 5
-    assert call(K=0) == 3 and call(cb=2) == 4 and call(M=33) == 5
+    assert call(K=0) == 3 and call(cb=4) == 4 and call(M=33) == 5
     assert call(arr=_group([(256, 256), (130, 384)])) == 2
     assert call(arr=_group([(256, 256)], codes=None), count=1) == 1
     assert call(arr=_group([(256, 256)], x=A + 2), count=1) == 6

@@ -28,10 +28,38 @@ def _decode_gpu(codes, K, cb, m, n):
 
 
 @pytest.mark.parametrize("K", range(1, 9))
-@pytest.mark.parametrize("cb", [0, 1])
+@pytest.mark.parametrize("cb", [0, 1, 2, 3])
 @pytest.mark.parametrize("m,n", [(128, 128), (256, 384)])
 def test_decode_bit_exact_small(K, cb, m, n):
     codes = synth.packed_codes(m, n, K, synth.seed_for(50, 10 * K + cb))
+    w = _decode_gpu(codes, K, cb, m, n).cpu().numpy().view(np.uint16)
+    ref = O.decode_tiles(codes, K, cb, m, n).view(np.uint16)
+    np.testing.assert_array_equal(w, ref)
+
+
+def _every_state_codes():
+    """K = 8 streams whose windows take every 16-bit value: the state of step t
+    is stream bytes t and t+1, so tile j of the first 256 repeats the bytes
+    (j, k) for k = 0..127 and tile j of the next 256 the bytes (j, 128 + k).
+    512 tiles: a 128 x 1024 layer."""
+    K = 8
+    tiles = []
+    for half in (0, 128):
+        for j in range(256):
+            b = np.empty(256, dtype=np.uint8)
+            b[0::2] = j
+            b[1::2] = half + np.arange(128)
+            tiles.append(np.frombuffer(b.tobytes(), dtype=">u4").astype(np.uint32))
+    return np.concatenate(tiles), K, 128, 1024
+
+
+@pytest.mark.parametrize("cb", [0, 1, 2, 3])
+def test_decode_every_state_exhaustive(cb):
+    """Every one of the 2**16 states decoded on the GPU, bit-exact against the
+    oracle."""
+    codes, K, m, n = _every_state_codes()
+    states = O.tile_states(codes.reshape(-1, 8 * K), K)
+    assert len(np.unique(states)) == 1 << 16
     w = _decode_gpu(codes, K, cb, m, n).cpu().numpy().view(np.uint16)
     ref = O.decode_tiles(codes, K, cb, m, n).view(np.uint16)
     np.testing.assert_array_equal(w, ref)
@@ -43,7 +71,7 @@ def test_decode_degenerate_streams():
     for K in (1, 4, 8):
         for fill in (0, 0xFFFFFFFF):
             codes = np.full((m // 16) * (n // 16) * 8 * K, fill, dtype=np.uint32)
-            for cb in (0, 1):
+            for cb in (0, 1, 2, 3):
                 w = _decode_gpu(codes, K, cb, m, n).cpu().numpy().view(np.uint16)
                 np.testing.assert_array_equal(w, O.decode_tiles(codes, K, cb, m, n).view(np.uint16))
 

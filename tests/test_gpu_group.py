@@ -45,7 +45,7 @@ def _check(layers, K, cb, M):
 
 
 @pytest.mark.parametrize("M", [1, 2, 5])
-@pytest.mark.parametrize("K,cb", [(3, 1), (2, 0)])
+@pytest.mark.parametrize("K,cb", [(3, 1), (2, 0), (2, 2), (3, 3)])
 def test_grouped_mixed_shapes(M, K, cb):
     shapes = [(256, 384), (384, 1280), (128, 640)]
     layers = _layers(shapes, K, cb, M, config=70 + M)

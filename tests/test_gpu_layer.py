@@ -35,7 +35,7 @@ def _run(inp_d, K, cb, m, n, M, use_in=True, use_out=True, ws=None, gemv=False):
 
 
 @pytest.mark.parametrize("K", range(1, 9))
-@pytest.mark.parametrize("cb", [0, 1])
+@pytest.mark.parametrize("cb", [0, 1, 2, 3])
 def test_gemv_all_widths(K, cb):
     m, n = 256, 384
     inp = synth.layer_inputs(m, n, K, 1, config=60, index=10 * K + cb)
@@ -105,7 +105,7 @@ def test_gemm_small_batches_warp_shuffle(M):
     assert_layer_close(y, ref, f"M={M}")
 
 
-@pytest.mark.parametrize("M,cb", [(1, 0), (1, 1), (2, 1)])
+@pytest.mark.parametrize("M,cb", [(1, 0), (1, 1), (2, 1), (1, 2), (2, 3)])
 def test_large_layer_kernel_full(M, cb):
     """4096 x 10112: at least 1024 tiles per SM, so batch chunks of 1 and 2 run
     the one-CTA-per-SM sub-unit kernel; n/128 = 79 is odd, so the last

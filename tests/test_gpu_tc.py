@@ -41,7 +41,7 @@ def _ref(inp, K, cb, m, n, use_in=True, use_out=True):
 
 
 @pytest.mark.parametrize("K", range(1, 9))
-@pytest.mark.parametrize("cb", [0, 1])
+@pytest.mark.parametrize("cb", [0, 1, 2, 3])
 def test_tc_all_widths_batch1(K, cb):
     m, n = 256, 384
     inp = synth.layer_inputs(m, n, K, 1, config=80, index=10 * K + cb)
@@ -49,7 +49,7 @@ def test_tc_all_widths_batch1(K, cb):
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 13, 16, 17, 32])
-@pytest.mark.parametrize("cb", [0, 1])
+@pytest.mark.parametrize("cb", [0, 1, 2, 3])
 def test_tc_batches(M, cb):
     m, n, K = 384, 1280, 3
     inp = synth.layer_inputs(m, n, K, M, config=81, index=M + 100 * cb)

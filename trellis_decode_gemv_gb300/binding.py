@@ -16,6 +16,8 @@ import torch
 
 CB_3INST = 0
 CB_1MAD = 1
+CB_MCG = 2
+CB_MUL1 = 3
 MAX_BATCH = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

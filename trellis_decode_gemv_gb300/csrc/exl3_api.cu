@@ -109,7 +109,7 @@ exl3_status run_tensor(LayerArgs a, int M, float* zacc, uint32_t* status, __half
   // last two are programmatic dependents of the kernel before them.
   a.zacc = zacc;
   a.status = status;
-  if (a.codebook != EXL3_CB_1MAD) bsum = nullptr;
+  if (a.codebook != EXL3_CB_1MAD && a.codebook != EXL3_CB_MUL1) bsum = nullptr;
   exl3_status st = launch_bimg(a.x, a.s_in, bimg, bsum, M, tc_nb(M), a.n, cs);
   if (st != EXL3_OK) return st;
   if ((st = launch_tc(a, bimg, bsum, M, device_sm_count(), cs)) != EXL3_OK) return st;

@@ -1,5 +1,5 @@
 // Device-side building blocks shared by every libexl3 kernel: trellis window
-// extraction, the two computed codes, and the 128-point Walsh-Hadamard
+// extraction, the computed codes, and the 128-point Walsh-Hadamard
 // butterfly.  Everything here is the GPU's own statement of the format; nothing
 // is shared with the CPU oracle.
 #pragma once
@@ -58,12 +58,79 @@ __device__ __forceinline__ __half code_1mad(uint32_t s) {
   return __float2half_rn(__fmul_rn(c, kOneMadScale));
 }
 
+// MCG and mul1, EXL3's later codes ("Trellis Quantization", Parts eleven and
+// twelve): the generator keeps only the multiply (the pages do not print the
+// multiplier they adopt; the LCG multiplier above is used).  MCG is 3INST on
+// that generator; mul1 masks every byte of the product to six bits, sums the
+// four bytes (mean 4 * 31.5 = 126, variance 4 * (64^2 - 1) / 12 = 1365),
+// subtracts 126 and scales by 1/sqrt(1365) rounded to binary32 (= 0x3CDDBAC5).
+constexpr int kCbMcg = 2;
+constexpr int kCbMul1 = 3;
+constexpr uint32_t kMul1Mask = 0x3F3F3F3Fu;
+constexpr int kMul1Centre = 126;
+constexpr float kMul1Scale = 0x1.bb758ap-6f;
+
+__device__ __forceinline__ uint32_t mcg(uint32_t s) { return s * kLcgMul; }
+
+// Generator output of code CB for state s.
+template <int CB>
+__device__ __forceinline__ uint32_t generate(uint32_t s) {
+  if constexpr (CB == kCbMcg || CB == kCbMul1) {
+    return mcg(s);
+  } else {
+    return lcg(s);
+  }
+}
+
+// Codes whose weight is an affine function of a byte sum (1MAD, mul1): the
+// word whose bytes are summed, the centre and the scale.
+template <int CB>
+__host__ __device__ constexpr bool byte_sum_code() {
+  return CB == kCb1Mad || CB == kCbMul1;
+}
+template <int CB>
+__device__ __forceinline__ uint32_t summed_bytes(uint32_t x) {
+  if constexpr (CB == kCbMul1) {
+    return x & kMul1Mask;
+  } else {
+    return x;
+  }
+}
+template <int CB>
+__host__ __device__ constexpr int byte_sum_centre() {
+  return CB == kCbMul1 ? kMul1Centre : kOneMadCentre;
+}
+template <int CB>
+__host__ __device__ constexpr float byte_sum_scale() {
+  return CB == kCbMul1 ? kMul1Scale : kOneMadScale;
+}
+
+// MCG: the three-instruction code on the multiplicative generator.
+__device__ __forceinline__ __half code_mcg(uint32_t s) {
+  const uint32_t h = mask_xor_3inst(mcg(s));
+  const __half lo = __ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu));
+  const __half hi = __ushort_as_half(static_cast<unsigned short>(h >> 16));
+  return __hadd(lo, hi);
+}
+
+// mul1: masked byte sum S (one dp4a), (S - 126) exact in binary32, one binary32
+// multiply, one rounding to binary16.
+__device__ __forceinline__ __half code_mul1(uint32_t s) {
+  const int S = static_cast<int>(__dp4a(mcg(s) & kMul1Mask, 0x01010101u, 0u));
+  const float c = static_cast<float>(S - kMul1Centre);
+  return __float2half_rn(__fmul_rn(c, kMul1Scale));
+}
+
 template <int CB>
 __device__ __forceinline__ __half decode_state(uint32_t s) {
   if constexpr (CB == kCb3Inst) {
     return code_3inst(s);
-  } else {
+  } else if constexpr (CB == kCb1Mad) {
     return code_1mad(s);
+  } else if constexpr (CB == kCbMcg) {
+    return code_mcg(s);
+  } else {
+    return code_mul1(s);
   }
 }
 
@@ -140,33 +207,17 @@ __device__ __forceinline__ void pair_states(const uint32_t (&w)[RowPair<K>::kPai
   }
 }
 
-// Weight of a state in fp32, for the fused product.
-//  3INST: the binary16 sum of the two halves (exactly the defined weight),
-//         widened to fp32.
-//  1MAD:  the exact integer S - 510 as fp32, obtained without an int-to-float
-//         conversion: dp4a adds the byte sum to the bit pattern of 1.5 * 2^23
-//         minus 510, whose low mantissa bits then hold 1.5*2^23 + S - 510
-//         exactly, and one subtraction removes the offset.  The 1/sqrt(21845)
-//         factor is applied to x-tilde instead, so this skips the per-weight
-//         binary16 rounding of the defined weight (a relative change of at most
-//         2^-11 per weight, inside the layer tolerance).
-constexpr uint32_t kOneMadMagicBits = 0x4B400000u - static_cast<uint32_t>(kOneMadCentre);
-constexpr float kOneMadMagic = 12582912.0f;  // 1.5 * 2^23
-
+// Factor applied to x-tilde by the fused products: the byte-sum codes
+// multiply x by the exact integer (S - centre) and take their scale from x,
+// which skips the per-weight binary16 rounding of the defined weight (a
+// relative change of at most 2^-11 per weight, inside the layer tolerance).
 template <int CB>
-__device__ __forceinline__ float decode_f32(uint32_t s) {
-  if constexpr (CB == kCb3Inst) {
-    return __half2float(code_3inst(s));
+__host__ __device__ constexpr float x_factor() {
+  if constexpr (byte_sum_code<CB>()) {
+    return byte_sum_scale<CB>();
   } else {
-    const uint32_t x = lcg(s);
-    return __uint_as_float(__dp4a(x, 0x01010101u, kOneMadMagicBits)) - kOneMadMagic;
+    return 1.0f;
   }
-}
-
-// Factor applied to x-tilde by the fused product for code CB (see decode_f32).
-template <int CB>
-__device__ __forceinline__ float x_factor() {
-  return CB == kCb1Mad ? kOneMadScale : 1.0f;
 }
 
 // ---------------------------------------------------------------------------

@@ -22,7 +22,7 @@ inline exl3_status check_shape(int m, int n) {
 
 inline exl3_status check_k_cb(int K, int codebook) {
   if (K < 1 || K > 8) return EXL3_ERR_K;
-  if (codebook != EXL3_CB_3INST && codebook != EXL3_CB_1MAD) return EXL3_ERR_CODEBOOK;
+  if (codebook < EXL3_CB_3INST || codebook > EXL3_CB_MUL1) return EXL3_ERR_CODEBOOK;
   return EXL3_OK;
 }
 

@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_
   const long long units = static_cast<long long>(a.m / kRowBlock) * nt;
   const long long u_begin = static_cast<long long>(blockIdx.x) * units / gridDim.x;
   const long long u_end = static_cast<long long>(blockIdx.x + 1) * units / gridDim.x;
-  const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
+  // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
+  const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
   __shared__ uint4 xs[MB * kSegTiles * 4];  // rotated x of the segment, [MB][tiles][4]
 
   // The output kernel may be scheduled now (it waits for this grid to finish).
@@ -192,9 +193,9 @@ __global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = 4 * q + j;
-          const uint32_t xa = lcg(st[c]);
-          const uint32_t xb = lcg(st[16 + c]);
-          if constexpr (CB == kCb3Inst) {
+          const uint32_t xa = generate<CB>(st[c]);
+          const uint32_t xb = generate<CB>(st[16 + c]);
+          if constexpr (!byte_sum_code<CB>()) {
             const uint32_t pa = mask_xor_3inst(xa);
             const uint32_t pb = mask_xor_3inst(xb);
 #pragma unroll
@@ -205,8 +206,8 @@ __global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_
               hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
             }
           } else {
-            const uint32_t ra = __dp4a(xa, 0x01010101u, 0x6400u);
-            const uint32_t rb2 = __dp4a(xb, 0x01010101u, 0x6400u);
+            const uint32_t ra = __dp4a(summed_bytes<CB>(xa), 0x01010101u, 0x6400u);
+            const uint32_t rb2 = __dp4a(summed_bytes<CB>(xb), 0x01010101u, 0x6400u);
             const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
             const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
 #pragma unroll
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_
       }
 #pragma unroll
       for (int b = 0; b < MB; ++b) {
-        if constexpr (CB == kCb3Inst) {
+        if constexpr (!byte_sum_code<CB>()) {
           acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
           acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
         } else {
@@ -282,7 +283,8 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   const long long units = g.units;
   const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
   const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
-  const __half2 k1534 = __half2half2(__ushort_as_half(0x65FE));  // 1534 = 1024 + 510
+  // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
+  const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
   __shared__ int next_unit;
 
   // The output kernel may be scheduled now (it waits for this grid to finish).
@@ -346,9 +348,9 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = 4 * q + j;
-          const uint32_t xa = lcg(st[c]);
-          const uint32_t xb = lcg(st[16 + c]);
-          if constexpr (CB == kCb3Inst) {
+          const uint32_t xa = generate<CB>(st[c]);
+          const uint32_t xb = generate<CB>(st[16 + c]);
+          if constexpr (!byte_sum_code<CB>()) {
             const uint32_t pa = mask_xor_3inst(xa);
             const uint32_t pb = mask_xor_3inst(xb);
 #pragma unroll
@@ -359,8 +361,8 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
               hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
             }
           } else {
-            const uint32_t ra = __dp4a(xa, 0x01010101u, 0x6400u);
-            const uint32_t rb2 = __dp4a(xb, 0x01010101u, 0x6400u);
+            const uint32_t ra = __dp4a(summed_bytes<CB>(xa), 0x01010101u, 0x6400u);
+            const uint32_t rb2 = __dp4a(summed_bytes<CB>(xb), 0x01010101u, 0x6400u);
             const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
             const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
 #pragma unroll
@@ -373,7 +375,7 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
       }
 #pragma unroll
       for (int b = 0; b < MB; ++b) {
-        if constexpr (CB == kCb3Inst) {
+        if constexpr (!byte_sum_code<CB>()) {
           acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
           acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
         } else {
@@ -477,14 +479,22 @@ exl3_status launch_group_cb(const GroupArgs& a, int mb, cudaStream_t stream) {
 
 template <int K>
 exl3_status launch_layer_dispatch(const LayerArgs& a, int mb, cudaStream_t stream) {
-  return a.codebook == kCb3Inst ? launch_seg_cb<K, kCb3Inst>(a, mb, stream)
-                                : launch_seg_cb<K, kCb1Mad>(a, mb, stream);
+  switch (a.codebook) {
+    case kCb3Inst: return launch_seg_cb<K, kCb3Inst>(a, mb, stream);
+    case kCb1Mad: return launch_seg_cb<K, kCb1Mad>(a, mb, stream);
+    case kCbMcg: return launch_seg_cb<K, kCbMcg>(a, mb, stream);
+    default: return launch_seg_cb<K, kCbMul1>(a, mb, stream);
+  }
 }
 
 template <int K>
 exl3_status launch_group_dispatch(const GroupArgs& a, int codebook, int mb, cudaStream_t stream) {
-  return codebook == kCb3Inst ? launch_group_cb<K, kCb3Inst>(a, mb, stream)
-                              : launch_group_cb<K, kCb1Mad>(a, mb, stream);
+  switch (codebook) {
+    case kCb3Inst: return launch_group_cb<K, kCb3Inst>(a, mb, stream);
+    case kCb1Mad: return launch_group_cb<K, kCb1Mad>(a, mb, stream);
+    case kCbMcg: return launch_group_cb<K, kCbMcg>(a, mb, stream);
+    default: return launch_group_cb<K, kCbMul1>(a, mb, stream);
+  }
 }
 
 }  // namespace exl3

@@ -235,10 +235,12 @@ exl3_status launch_decode_k(const uint32_t* codes, int codebook, int m, int n, _
                             cudaStream_t stream) {
   const long long threads = static_cast<long long>(m / 16) * (n / 16) * 8;
   const unsigned grid = static_cast<unsigned>((threads + kThreads - 1) / kThreads);
-  if (codebook == kCb3Inst)
-    decode_kernel<K, kCb3Inst><<<grid, kThreads, 0, stream>>>(codes, m, n, w);
-  else
-    decode_kernel<K, kCb1Mad><<<grid, kThreads, 0, stream>>>(codes, m, n, w);
+  switch (codebook) {
+    case kCb3Inst: decode_kernel<K, kCb3Inst><<<grid, kThreads, 0, stream>>>(codes, m, n, w); break;
+    case kCb1Mad: decode_kernel<K, kCb1Mad><<<grid, kThreads, 0, stream>>>(codes, m, n, w); break;
+    case kCbMcg: decode_kernel<K, kCbMcg><<<grid, kThreads, 0, stream>>>(codes, m, n, w); break;
+    default: decode_kernel<K, kCbMul1><<<grid, kThreads, 0, stream>>>(codes, m, n, w); break;
+  }
   return launch_status();
 }
 
@@ -285,7 +287,7 @@ exl3_status launch_pdl_small(Kern kernel, const G& g, cudaStream_t stream) {
 }  // namespace
 
 exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream) {
-  g.factor = codebook == kCb1Mad ? kOneMadScale : 1.0f;
+  g.factor = codebook == kCb1Mad ? x_factor<kCb1Mad>() : codebook == kCbMul1 ? x_factor<kCbMul1>() : 1.0f;
   g.jobs = 0;
   for (int i = 0; i < g.count; ++i) {
     g.e[i].job_begin = g.jobs;

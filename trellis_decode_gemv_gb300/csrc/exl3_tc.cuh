@@ -268,9 +268,9 @@ __device__ __forceinline__ void row_states(const uint32_t (&raw)[RowWords<K>::kR
 // unscaled; the epilogue corrects).
 template <int CB>
 __device__ __forceinline__ uint32_t pack_two(uint32_t s0, uint32_t s1) {
-  const uint32_t x0 = lcg(s0);
-  const uint32_t x1 = lcg(s1);
-  if constexpr (CB == kCb3Inst) {
+  const uint32_t x0 = generate<CB>(s0);
+  const uint32_t x1 = generate<CB>(s1);
+  if constexpr (!byte_sum_code<CB>()) {
     const uint32_t h0 = mask_xor_3inst(x0);
     const uint32_t h1 = mask_xor_3inst(x1);
     const uint32_t lo = __byte_perm(h0, h1, 0x5410);  // (lo half of w0, lo half of w1)
@@ -278,8 +278,8 @@ __device__ __forceinline__ uint32_t pack_two(uint32_t s0, uint32_t s1) {
     const __half2 w = __hadd2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&hi));
     return *reinterpret_cast<const uint32_t*>(&w);
   } else {
-    const uint32_t d0 = __dp4a(x0, 0x01010101u, 0x6400u);  // binary16 bits of 1024 + S
-    const uint32_t d1 = __dp4a(x1, 0x01010101u, 0x6400u);
+    const uint32_t d0 = __dp4a(summed_bytes<CB>(x0), 0x01010101u, 0x6400u);  // binary16 bits of 1024 + S
+    const uint32_t d1 = __dp4a(summed_bytes<CB>(x1), 0x01010101u, 0x6400u);
     return __byte_perm(d0, d1, 0x5410);
   }
 }
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       if (et == 0) sh.epi_go = aborted(sh) ? 0u : 1u;
       epi_sync();
       if (sh.epi_go == 0u) break;
-      if constexpr (CB == kCb1Mad) {
+      if constexpr (byte_sum_code<CB>()) {
         // sum of x-tilde over the run's columns, per batch row
         for (int b = ew; b < p.M; b += 4) {
           float s = 0.f;
@@ -611,7 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
             const int b = 16 * h + j;
             if (b < p.M) {
               float z = d[j];
-              if constexpr (CB == kCb1Mad) z = (z - 1534.0f * sh.xsum[b]) * kOneMadScale;
+              if constexpr (byte_sum_code<CB>())
+                z = (z - static_cast<float>(1024 + byte_sum_centre<CB>()) * sh.xsum[b]) * byte_sum_scale<CB>();
               sh.zt[b * kRowBlock + row] = z;
             }
           }
@@ -686,11 +687,20 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
 template <int K>
 exl3_status launch_tc_dispatch(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                                cudaStream_t stream) {
-  if (a.codebook == kCb3Inst)
-    return M <= 16 ? launch_tc_t<K, kCb3Inst, 16>(a, bimg, bsum, M, grid, stream)
-                   : launch_tc_t<K, kCb3Inst, 32>(a, bimg, bsum, M, grid, stream);
-  return M <= 16 ? launch_tc_t<K, kCb1Mad, 16>(a, bimg, bsum, M, grid, stream)
-                 : launch_tc_t<K, kCb1Mad, 32>(a, bimg, bsum, M, grid, stream);
+  switch (a.codebook) {
+    case kCb3Inst:
+      return M <= 16 ? launch_tc_t<K, kCb3Inst, 16>(a, bimg, bsum, M, grid, stream)
+                     : launch_tc_t<K, kCb3Inst, 32>(a, bimg, bsum, M, grid, stream);
+    case kCb1Mad:
+      return M <= 16 ? launch_tc_t<K, kCb1Mad, 16>(a, bimg, bsum, M, grid, stream)
+                     : launch_tc_t<K, kCb1Mad, 32>(a, bimg, bsum, M, grid, stream);
+    case kCbMcg:
+      return M <= 16 ? launch_tc_t<K, kCbMcg, 16>(a, bimg, bsum, M, grid, stream)
+                     : launch_tc_t<K, kCbMcg, 32>(a, bimg, bsum, M, grid, stream);
+    default:
+      return M <= 16 ? launch_tc_t<K, kCbMul1, 16>(a, bimg, bsum, M, grid, stream)
+                     : launch_tc_t<K, kCbMul1, 32>(a, bimg, bsum, M, grid, stream);
+  }
 }
 
 }  // namespace tc

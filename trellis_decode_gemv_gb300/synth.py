@@ -93,14 +93,19 @@ LLAMA70B_SHAPES = [("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192),
                    ("down", 8192, 28672)]
 
 
-def llama8b_layer_set():
+CB_MCG = 2
+CB_MUL1 = 3
+CODE_NAMES = {CB_3INST: "3inst", CB_1MAD: "1mad", CB_MCG: "mcg", CB_MUL1: "mul1"}
+
+
+def llama8b_layer_set(codes=(CB_1MAD, CB_3INST)):
     """Llama-3-8B-shaped decoder layer set: every projection at K = 2, 3, 4 with
-    both codes (42 GEMVs, 1.309 G weights)."""
+    each code (42 GEMVs, 1.309 G weights for two codes)."""
     out = []
-    for cb in (CB_1MAD, CB_3INST):
+    for cb in codes:
         for K in (2, 3, 4):
             for name, m, n in LLAMA8B_SHAPES:
-                out.append((f"{name}.K{K}.{'1mad' if cb else '3inst'}", m, n, K, cb))
+                out.append((f"{name}.K{K}.{CODE_NAMES[cb]}", m, n, K, cb))
     return out
 
 
