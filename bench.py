@@ -56,6 +56,7 @@ SM_COUNT_NOMINAL = 152
 SM_MAX_MHZ_NOMINAL = 2070.0
 INT_LANES_PER_SM_CLK = 128
 HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
 # MCG: as 3INST (a multiply instead of the multiply-add); mul1: as 1MAD plus
 # the six-bit byte mask
 OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5, synth.CB_MCG: 4, synth.CB_MUL1: 6}
@@ -65,17 +66,20 @@ OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5, synth.CB_MCG: 4, synth.CB
 TRAFFIC_RATIO = {
     "shuffle": (29.445 / 29.38, "the ncu capture of layer_kernel on gate/up/down 14336x4096 K4 1MAD"),
     "tensor": (23.12 / 22.15, "the ncu capture of tc_layer_kernel on 14336x4096 K3 1MAD at batch 16"),
+    "dense": (None, None),
 }
 
 
 def measured_peaks():
+    """(HBM GB/s, max SM MHz, dense bf16 TFLOP/s burst, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL)), "measured"
+        return (float(d["hbm_gbs"]), float(d.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL)),
+                float(d.get("bf16_tflops", BF16_FALLBACK_TFLOPS)), "measured")
     except Exception:
-        return HBM_FALLBACK_GBS, SM_MAX_MHZ_NOMINAL, "fallback"
+        return HBM_FALLBACK_GBS, SM_MAX_MHZ_NOMINAL, BF16_FALLBACK_TFLOPS, "fallback"
 
 
 def workload(name: str, batch: int):
@@ -87,6 +91,10 @@ def workload(name: str, batch: int):
         desc = ("Llama-3-8B-shaped layer set at batch 1 with the MCG and mul1 codes: q/o 4096x4096, "
                 "k/v 1024x4096, gate/up 14336x4096, down 4096x14336, each at K=2,3,4")
         return desc, 5, synth.llama8b_layer_set((synth.CB_MCG, synth.CB_MUL1)), 1
+    if name == "prefill":
+        M = batch if batch > 32 else 512
+        return (f"14336x4096 and 4096x14336, K=3, 1MAD, prefill batch {M}, 4 distinct instances of each"), 6, \
+            synth.BATCH_SWEEP_SHAPES * 4, M
     if name == "single":
         # 32 distinct 4096x4096 layers (128 MB of codes) so that the timed
         # steps stream from HBM rather than L2
@@ -112,6 +120,9 @@ def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
     output kernel, plus the x-pair kernel when the chunk runs the sub-unit
     kernel (chunks above 2 rows, or at least 1024 tiles per SM)."""
     tensor = path == "tensor" or (path == "auto" and M > 2)
+    if M > 32:
+        from trellis_decode_gemv_gb300 import binding as B
+        return B.exl3_gemm_launches(m, n, M)
     if tensor:
         return 3
     tiles_per_sm = (m // 16) * (n // 16) // sms
@@ -166,10 +177,14 @@ def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     return 3 * chunks
 
 
-def algorithmic(m, n, K, cb, M):
+def algorithmic(m, n, K, cb, M, path="auto"):
+    """Weights, algorithmic bytes and decode integer ops of one call; above 32
+    batch rows the dense prefill decodes every tile once per call, the
+    tensor-memory passes once per 128-row pass."""
     weights = m * n
     nbytes = m * n * K // 8 + 2 * m + 2 * (m + n) + 2 * M * n + 2 * M * m
-    ops = weights * OPS_PER_WEIGHT[cb]
+    passes = (M + 127) // 128 if (M > 32 and path == "tensor") else 1
+    ops = weights * OPS_PER_WEIGHT[cb] * passes
     return weights, nbytes, ops
 
 
@@ -353,7 +368,7 @@ def run_ours(args):
     B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[args.path])
 
     desc, cfg, gemvs, M = workload(args.workload, args.batch)
-    hbm_gbs, sm_max_mhz, peak_src = measured_peaks()
+    hbm_gbs, sm_max_mhz, bf16_tflops, peak_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     p_int = sms * INT_LANES_PER_SM_CLK * sm_max_mhz * 1e6
@@ -365,7 +380,7 @@ def run_ours(args):
     Y = torch.empty(total_m, dtype=torch.float16, device=dev)
     calls = []
     xo = yo = 0
-    ws_bytes = max(B.exl3_workspace_bytes(m, n, M) for _, m, n, _, _ in gemvs)
+    ws_bytes = max(B.exl3_gemm_workspace_bytes(m, n, M) for _, m, n, _, _ in gemvs)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     packed = 0
     for i, (name, m, n, K, cb) in enumerate(gemvs):
@@ -395,8 +410,9 @@ def run_ours(args):
     def run_group(g):
         if len(g) == 1:
             c = calls[g[0]]
-            B.exl3_gemm_small(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
-                              c["scales"], c["x"], y=c["y"], workspace=ws)
+            fn = B.exl3_gemm if M > 32 else B.exl3_gemm_small
+            fn(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
+               c["scales"], c["x"], y=c["y"], workspace=ws)
         else:
             c0 = calls[g[0]]
             B.exl3_gemm_grouped([calls[i] for i in g], c0["K"], c0["cb"], workspace=ws)
@@ -407,7 +423,7 @@ def run_ours(args):
 
     # Decode work (weights, integer ops) does not grow with the batch; the
     # multiply-accumulates do (macs = weights * M).
-    alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M) for c in calls]
+    alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M, args.path) for c in calls]
     weights_step = sum(a[0] for a in alg)
     bytes_step = sum(a[1] for a in alg)
     ops_step = sum(a[2] for a in alg)
@@ -486,23 +502,38 @@ def run_ours(args):
     t_call = dur * (t_step / dur.sum())
     t_hbm = np.array([a[1] / (hbm_gbs * 1e9) for a in alg])
     t_int = np.array([a[2] / p_int for a in alg])
-    t_roof = np.maximum(t_hbm, t_int)
-    bound = "alu" if t_int.sum() >= t_hbm.sum() else "hbm"
+    # tensor-core term: 2 M m n flops at the measured dense bf16 (= fp16) peak
+    flops_step = 2.0 * M * sum(c["m"] * c["n"] for c in calls) if M > 2 else 0.0
+    p_tensor = bf16_tflops * 1e12
+    t_tc = np.array([2.0 * M * c["m"] * c["n"] / p_tensor if M > 2 else 0.0 for c in calls])
+    t_roof = np.maximum(np.maximum(t_hbm, t_int), t_tc)
+    terms = {"alu": t_int.sum(), "hbm": t_hbm.sum(), "tensor": t_tc.sum()}
+    bound = max(terms, key=terms.get)
     if bound == "alu":
         achieved, peak, unit = ops_step / t_step / 1e12, p_int / 1e12, "Tops/s"
+    elif bound == "tensor":
+        achieved, peak, unit = flops_step / t_step / 1e12, bf16_tflops, "TFLOP/s"
     else:
         achieved, peak, unit = bytes_step / t_step / 1e9, hbm_gbs, "GB/s"
     tensor = args.path == "tensor" or (args.path == "auto" and M > 2)
-    kname = ("tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"
-             if tensor else "layer_kernel (fused input RHT + trellis decode + GEMV) + output kernel")
-    ratio, ratio_src = TRAFFIC_RATIO["tensor" if tensor else "shuffle"]
+    dense = M > 32 and args.path != "tensor"
+    if dense:
+        kname = ("dense_kernel (tcgen05 128x256x16 MMAs, both operands in shared memory) + "
+                 "decode-to-operand-image, operand-B and output kernels")
+    elif tensor:
+        kname = "tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"
+    else:
+        kname = "layer_kernel (fused input RHT + trellis decode + GEMV) + output kernel"
+    ratio, ratio_src = TRAFFIC_RATIO["dense" if dense else "tensor" if tensor else "shuffle"]
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": ratio * bytes_step,
-                "traffic_note": (f"bytes per step: algorithmic bytes x {ratio:.3f}, the DRAM/algorithmic "
+                "frac": achieved / peak, "traffic": None if ratio is None else ratio * bytes_step,
+                "traffic_note": ("no ncu DRAM capture of this kernel yet" if ratio is None else
+                                 f"bytes per step: algorithmic bytes x {ratio:.3f}, the DRAM/algorithmic "
                                  f"ratio of {ratio_src}"),
                 "peak_source": (f"INT32: {sms} SMs x {INT_LANES_PER_SM_CLK} lanes/clk x "
                                 f"{sm_max_mhz:.0f} MHz (derived)") if bound == "alu"
-                else f"HBM copy bandwidth ({peak_src})",
+                else (f"dense bf16 GEMM ({peak_src}; fp16 MMAs run at the same rate)" if bound == "tensor"
+                      else f"HBM copy bandwidth ({peak_src})"),
                 "kernel": kname,
                 "timing": "algorithmic ops (bytes) per step / graph-timed step, CUDA events on the launch stream",
                 "per_call_us_mean": 1e6 * t_step / len(groups),
@@ -610,7 +641,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b",
-                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep"])
+                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",

@@ -121,7 +121,8 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
  * that may run concurrently must not share a workspace.  The uint32 at byte
  * offset 4*(m/128) is a status word: the tensor-core kernel ORs 1 into it if
  * one of its bounded device-side waits timed out (its outputs are then not
- * valid); it stays set until the caller clears it.
+ * valid); it stays set until the caller clears it.  After a call that set it,
+ * zero-fill the whole workspace again before reusing it.
  */
 size_t exl3_workspace_bytes(int m, int n, int M);
 
@@ -148,6 +149,43 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
                             const exl3_half *scales, int M, const exl3_half *x,
                             exl3_half *y, void *workspace, size_t workspace_bytes,
                             exl3_stream_t stream);
+
+/**
+ * Bytes of scratch for exl3_gemm at batch M: exl3_workspace_bytes(m, n, M) for
+ * M <= EXL3_MAX_BATCH; above, enough for either prefill strategy: the
+ * counters and status word, fp32 row sums [M][m], the rotated x as operand
+ * images (M rounded up to 256 rows, times n binary16), the decoded matrix
+ * (m * n binary16) and one uint32 per (128-row block, 256-row batch tile).
+ * Same zero-fill contract and status word as exl3_workspace_bytes.  0 for an
+ * invalid shape or M < 1.
+ */
+size_t exl3_gemm_workspace_bytes(int m, int n, int M);
+
+/**
+ * The layer for any batch M >= 1 (prefill): x [M][n] -> y [M][m].  Up to
+ * EXL3_MAX_BATCH rows this is exl3_gemm_small.  Above, by default, the matrix
+ * is decoded once per call into binary16 in the workspace and a dense
+ * tcgen05 GEMM (128 x 256 x 16 MMAs, both operands in shared memory) runs
+ * over all M rows ("decode a block once and reuse it", Lecture 1b Part
+ * fourteen: at large batch the decode is amortised and the product is a
+ * plain matrix multiplication).  With EXL3_PATH_TENSOR selected, passes of
+ * 128 rows run the tensor-core kernel with 128 batch columns per MMA instead,
+ * decoding each tile once per pass into tensor memory (no decoded copy in
+ * HBM).  Both compute the layer within the documented tolerance.
+ */
+exl3_status exl3_gemm(const uint32_t *codes, int K, int codebook, int m, int n,
+                      const exl3_half *s_in, const exl3_half *s_out,
+                      const exl3_half *scales, int M, const exl3_half *x, exl3_half *y,
+                      void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
+/**
+ * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
+ * call of this shape and batch makes on the current device under the current
+ * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on
+ * the warp-shuffle path; 3 for the dense prefill; 3 per 128-row pass for the
+ * prefill passes.  0 for an invalid shape or M < 1.
+ */
+int exl3_gemm_launches(int m, int n, int M);
 
 /** Most layers in one exl3_gemm_grouped call. */
 #define EXL3_MAX_GROUP 4
@@ -203,8 +241,9 @@ exl3_status exl3_set_path(int path);
 
 /**
  * Failure-detection test hook (no counterpart in the pages).  While `on` is
- * non-zero, the tensor-core kernel's operand-B producer posts nothing, so the
- * bounded device-side wait for operand B runs out: every role of the kernel
+ * non-zero, the operand producers of the tensor-core kernel (operand B) and
+ * of the dense prefill kernel (both operands) post nothing, so the bounded
+ * device-side waits for the operands run out: every role of the kernel
  * stops, waits (bounded) for its copies in flight, frees its tensor memory,
  * and the kernel ORs 1 into the workspace status word (see
  * exl3_workspace_bytes) before it exits.  The call's outputs are then not

@@ -141,3 +141,26 @@ def test_grouped_validation(lib):
     assert call(arr=_group([(256, 256)], x=A + 2), count=1) == 6
     assert call(wsb=64) == 7 and call(ws=None) == 7
     assert ok  # the remaining arguments are valid
+
+
+def test_gemm_prefill_workspace_and_validation(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert B.exl3_gemm_workspace_bytes(4096, 4096, 32) == B.exl3_workspace_bytes(4096, 4096, 32)
+    m, n = 4096, 14336
+    passes = (a256(4 * (m // 128 + 1)) + a256(4 * 128 * m) + a256(2 * 128 * n) + a256(4 * 128 * (n // 128)))
+
+    def dense(M):  # counters | fp32 row sums [M][m] | operand-B tiles of 256 rows | decoded matrix | arrivals
+        tiles = (M + 255) // 256
+        return (a256(4 * (m // 128 + 1)) + a256(4 * M * m) + a256(2 * tiles * 256 * n)
+                + a256(2 * m * n) + a256(4 * (m // 128) * tiles))
+    for M in (33, 256, 257, 5000):
+        assert B.exl3_gemm_workspace_bytes(m, n, M) == max(passes, dense(M))
+    assert B.exl3_gemm_workspace_bytes(m, n, 0) == 0
+    assert lib.exl3_gemm_launches(100, 256, 64) == 0 and lib.exl3_gemm_launches(256, 256, 0) == 0
+    call = lambda **kw: lib.exl3_gemm(kw.get("codes", A), 2, kw.get("cb", 0), kw.get("m", 256), 256, A, A, A,
+                                      kw.get("M", 64), A, A, kw.get("ws", A), kw.get("wsb", 1 << 30), None)  # noqa: E731
+    assert call(M=0) == 5
+    assert call(m=100) == 2
+    assert call(cb=4) == 4
+    assert call(codes=None) == 1
+    assert call(wsb=16) == 7

@@ -1,4 +1,4 @@
-"""Failure detection of the tensor-core kernel, tested without a GPU fault.
+"""Failure detection of the tensor-core kernels, tested without a GPU fault.
 
 The test hook exl3_debug_stall_tensor_wait leaves the kernel's wait for
 operand B unsatisfied (the producer posts nothing).  The bounded wait runs out,
@@ -56,3 +56,39 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
         assert_layer_close(y, ref, "after a timed-out call")
     finally:
         B.exl3_set_path(B.PATH_AUTO)
+
+
+@pytest.mark.parametrize("m,n,M", [(256, 1664, 90), (384, 512, 300)])
+def test_dense_prefill_wait_timeout_sets_status_and_context_survives(m, n, M):
+    """The dense prefill kernel with its producer stalled: with K split (first
+    shape) the row sums stay zero; without (second) nothing is written.  The
+    next call is correct."""
+    K, cb = 2, 0
+    inp = synth.layer_inputs(m, n, K, M, config=98, index=0)
+    d = upload(inp)
+    ws = torch.zeros(B.exl3_gemm_workspace_bytes(m, n, M), dtype=torch.uint8, device="cuda")
+
+    def call():
+        y = torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")
+        B.exl3_gemm(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"], y=y, workspace=ws)
+        torch.cuda.synchronize()
+        return y
+
+    B.exl3_debug_stall_tensor_wait(True)
+    try:
+        t0 = time.perf_counter()
+        call()
+        elapsed = time.perf_counter() - t0
+    finally:
+        B.exl3_debug_stall_tensor_wait(False)
+    print(f"stalled dense call returned after {elapsed:.3f} s")
+    assert B.workspace_status(ws, m) == 1
+    assert elapsed < 60.0
+    zacc = ws[256:256 + 4 * M * m].view(torch.float32)
+    assert float(zacc.abs().sum()) == 0.0
+    off = 4 * (m // 128)
+    ws[off:off + 4].zero_()
+    y = call()
+    assert B.workspace_status(ws, m) == 0
+    ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    assert_layer_close(y, ref, "dense after a timed-out call")

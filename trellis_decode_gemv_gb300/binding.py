@@ -63,6 +63,9 @@ _SIGNATURES = {
     "exl3_gemv_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "exl3_group_workspace_bytes": ([ctypes.POINTER(Exl3Layer), _I, _I], _SZ),
     "exl3_gemm_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "exl3_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
+    "exl3_gemm_launches": ([_I, _I, _I], _I),
+    "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_set_path": ([_I], _I),
     "exl3_debug_stall_tensor_wait": ([_I], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
@@ -300,7 +303,7 @@ class Exl3Linear:
 
     Holds the layer's device tensors (codes, signs, scales) and a workspace,
     checked when the object is built; a call then only checks and passes x and
-    y.  Same computation as exl3_gemm_small:
+    y.  Same computation as exl3_gemm (any batch up to max_batch):
         y[M, m] = Hb(s_out (.) (scales (.) (W-hat Hb(s_in (.) x[M, n])))).
     """
 
@@ -313,10 +316,13 @@ class Exl3Linear:
         self._args = (_ptr(codes, "codes", _WORDS, dev), K, codebook, m, n,
                       _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
                       _ptr(scales, "scales", _HALF, dev))
-        self.workspace = alloc_workspace(m, n, max_batch, dev)
+        nbytes = lib.exl3_gemm_workspace_bytes(m, n, max_batch)
+        if nbytes == 0:
+            raise Exl3Error(2, "invalid shape or batch for a workspace")
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self._ws = (self.workspace.data_ptr(), self.workspace.numel())
         self._max_batch = max_batch
-        self._fn = lib.exl3_gemm_small
+        self._fn = lib.exl3_gemm  # exl3_gemm_small up to 32 rows, 128-row passes above
 
     def __call__(self, x, y=None):
         x2 = x if x.dim() == 2 else x.view(1, -1)
@@ -353,3 +359,35 @@ class Exl3LinearGroup:
         _check(self._fn(self._arr, self._count, self.K, self.codebook, self.M, *self._ws,
                         torch.cuda.current_stream(self.device).cuda_stream))
         return [L["y"] for L in self._keep]
+
+
+def exl3_gemm_workspace_bytes(m: int, n: int, M: int) -> int:
+    return int(load_library().exl3_gemm_workspace_bytes(m, n, M))
+
+
+def exl3_gemm_launches(m: int, n: int, M: int) -> int:
+    """Kernel launches of one exl3_gemm call of this shape and batch on the
+    current device under the current path setting."""
+    return int(load_library().exl3_gemm_launches(m, n, M))
+
+
+def exl3_gemm(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspace=None):
+    """The layer for any batch M (prefill): x [M, n] -> y [M, m]."""
+    lib = load_library()
+    dev = codes.device
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, m), dtype=torch.float16, device=dev)
+    if workspace is None:
+        nbytes = exl3_gemm_workspace_bytes(m, n, M)
+        if nbytes == 0:
+            raise Exl3Error(2, "invalid shape or batch for a workspace")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib.exl3_gemm(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), M, _ptr(x2, "x", _HALF, dev),
+        _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev),
+        workspace.numel(), _stream(dev)))
+    return y if x.dim() == 2 else y.view(-1)

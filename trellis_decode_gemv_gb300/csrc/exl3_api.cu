@@ -403,6 +403,118 @@ extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, in
   return EXL3_OK;
 }
 
+extern "C" size_t exl3_gemm_workspace_bytes(int m, int n, int M) {
+  if (check_shape(m, n) != EXL3_OK || M < 1) return 0;
+  if (M <= EXL3_MAX_BATCH) return exl3_workspace_bytes(m, n, M);
+  // Either prefill strategy may run (exl3_set_path can change between calls).
+  const size_t dense = dense_total(m, n, M);
+  const size_t passes = workspace_total(m, n, kPrefillRows);
+  return dense > passes ? dense : passes;
+}
+
+extern "C" int exl3_gemm_launches(int m, int n, int M) {
+  if (check_shape(m, n) != EXL3_OK || M < 1) return 0;
+  const int path = g_path.load(std::memory_order_relaxed);
+  if (M <= EXL3_MAX_BATCH) {
+    if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2)) return 3;
+    // warp-shuffle path: per batch chunk the layer kernel (plus the x-pair
+    // kernel in front of the sub-unit kernel) and the output kernel
+    const int sms = device_sm_count();
+    int launches = 0;
+    for (int done = 0; done < M;) {
+      const int mb = batch_chunk(M - done);
+      launches += plan_layer(m, n, mb, sms).sub == 0 ? 2 : 3;
+      done += mb;
+    }
+    return launches;
+  }
+  if (path == EXL3_PATH_TENSOR) return 3 * ((M + kPrefillRows - 1) / kPrefillRows);
+  return 3;
+}
+
+namespace {
+
+// Decode once, dense GEMM: W-hat into operand-A images, x-tilde into
+// operand-B images, then the dense kernel.
+exl3_status run_dense(const LayerArgs& a, int M, char* ws, cudaStream_t cs) {
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws) + a.m / kRowBlock;
+  float* zacc = reinterpret_cast<float*>(ws + zacc_offset(a.m));
+  __half* bimg = reinterpret_cast<__half*>(ws + dense_bimg_offset(a.m, M));
+  unsigned char* aimg = reinterpret_cast<unsigned char*>(ws + dense_aimg_offset(a.m, a.n, M));
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + dense_cnt_offset(a.m, a.n, M));
+  exl3_status st = launch_decode_aimg(a.codes, a.K, a.codebook, a.m, a.n, aimg, cs);
+  if (st != EXL3_OK) return st;
+  if ((st = launch_bimg(a.x, a.s_in, bimg, nullptr, M, kDenseNB, a.n, cs)) != EXL3_OK) return st;
+  const int units = (a.m / kRowBlock) * dense_tiles(M);
+  const int split = choose_dense_split(units, a.n / 64, device_sm_count());
+  return launch_dense(aimg, bimg, a.scales, a.s_out, a.y, zacc, cnt, a.m, a.n, M, split, status, a.debug_stall,
+                      cs);
+}
+
+}  // namespace
+
+extern "C" exl3_status exl3_gemm(const uint32_t* codes, int K, int codebook, int m, int n,
+                                 const exl3_half* s_in, const exl3_half* s_out,
+                                 const exl3_half* scales, int M, const exl3_half* x, exl3_half* y,
+                                 void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  if (M < 1) return EXL3_ERR_BATCH;
+  if (M <= EXL3_MAX_BATCH)
+    return exl3_gemm_small(codes, K, codebook, m, n, s_in, s_out, scales, M, x, y, workspace,
+                           workspace_bytes, stream);
+  exl3_status st = check_shape(m, n);
+  if (st != EXL3_OK) return st;
+  if ((st = check_k_cb(K, codebook)) != EXL3_OK) return st;
+  if (!codes || !scales || !x || !y) return EXL3_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y) ||
+      (s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out)))
+    return EXL3_ERR_ALIGN;
+  if (!workspace || workspace_bytes < exl3_gemm_workspace_bytes(m, n, M)) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (g_path.load(std::memory_order_relaxed) != EXL3_PATH_TENSOR) {
+    LayerArgs a{};
+    a.codes = codes;
+    a.K = K;
+    a.codebook = codebook;
+    a.m = m;
+    a.n = n;
+    a.s_in = reinterpret_cast<const __half*>(s_in);
+    a.s_out = reinterpret_cast<const __half*>(s_out);
+    a.scales = reinterpret_cast<const __half*>(scales);
+    a.x = reinterpret_cast<const __half*>(x);
+    a.y = reinterpret_cast<__half*>(y);
+    a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+    return run_dense(a, M, ws, cs);
+  }
+  // EXL3_PATH_TENSOR: passes of up to 128 batch rows through the tensor-core
+  // kernel at N = 128; each pass decodes the tiles once into tensor memory for
+  // all its rows.
+  const int R = kPrefillRows;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws) + m / kRowBlock;
+  float* zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
+  __half* bimg = reinterpret_cast<__half*>(ws + bimg_offset(m, R));
+  float* bsum = reinterpret_cast<float*>(ws + bsum_offset(m, n, R));
+  for (int done = 0; done < M; done += R) {
+    const int rows = M - done < R ? M - done : R;
+    LayerArgs a{};
+    a.codes = codes;
+    a.K = K;
+    a.codebook = codebook;
+    a.m = m;
+    a.n = n;
+    a.s_in = reinterpret_cast<const __half*>(s_in);
+    a.s_out = reinterpret_cast<const __half*>(s_out);
+    a.scales = reinterpret_cast<const __half*>(scales);
+    a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
+    a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
+    a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+    // rows <= 32 use the skinny configuration; its regions fit in this layout
+    if ((st = run_tensor(a, rows, zacc, status, bimg, bsum, cs)) != EXL3_OK) return st;
+  }
+  return EXL3_OK;
+}
+
 extern "C" exl3_status exl3_gemv(const uint32_t* codes, int K, int codebook, int m, int n,
                                  const exl3_half* s_in, const exl3_half* s_out,
                                  const exl3_half* scales, const exl3_half* x, exl3_half* y,

@@ -44,7 +44,9 @@ int device_sm_count();
 // counters and zacc must be zero before a call and are zero after it.
 inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // Batch columns of the tensor-core MMAs (N of the 128 x N x 16 shape).
-inline int tc_nb(int M) { return M <= 16 ? 16 : 32; }
+inline int tc_nb(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 128; }
+// Batch rows per pass of exl3_gemm above EXL3_MAX_BATCH (the N = 128 kernel).
+constexpr int kPrefillRows = 128;
 inline size_t counters_bytes(int m) {
   return align256(sizeof(uint32_t) * (static_cast<size_t>(m / kRowBlock) + 1));
 }
@@ -144,10 +146,11 @@ struct LayerArgs {
 // Internal launchers (one translation unit per K for the layer kernels).
 exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int rows, int d,
                        cudaStream_t stream);
-// Operand images of the tensor-core kernel: for every 128-column block kb of
-// x-tilde = Hb(s_in (.) x) (x itself when s_in is NULL), the nb x 128 binary16
-// K-major image at bimg + kb * nb * 128 (rows M..nb-1 zero), and for bsum !=
-// NULL the fp32 sums bsum[b * (n/128) + kb] of the binary16 values.
+// Operand-B images of the tensor-core kernels: the M rows in tiles of nb; for
+// tile t and every 128-column block kb of x-tilde = Hb(s_in (.) x) (x itself
+// when s_in is NULL), the nb x 128 binary16 K-major image at bimg + t * nb * n
+// + kb * nb * 128 (rows past M zero), and for bsum != NULL the fp32 sums
+// bsum[b * (n/128) + kb] of the binary16 values.
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream);
 exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream);
@@ -185,6 +188,46 @@ exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int r
                         int codebook, cudaStream_t stream);
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,
                           cudaStream_t stream);
+// W-hat decoded into the dense kernel's operand-A images (m * n binary16 in
+// 16 KB images of 128 rows x 64 columns, canonical K-major layout).
+exl3_status launch_decode_aimg(const uint32_t* codes, int K, int codebook, int m, int n,
+                               unsigned char* aimg, cudaStream_t stream);
+// Dense prefill kernel: z = A x-tilde for M batch rows, A from the operand-A
+// images, x-tilde from operand-B images of kDenseNB rows per tile (bimg + tile
+// * kDenseNB * n halves), then y = binary16(Hb(s_out (.) (scale (.) z))).
+// With split == 1 every work unit covers all of K and finishes its block from
+// tensor memory; with split > 1 each unit covers 1/split of K and adds its
+// partial z to zacc [M][m], and the unit that brings the block's counter
+// cnt[block * tiles + tile] to split finishes the block from zacc and zeroes
+// zacc and the counter.  debug_stall: the failure-detection test hook, post no
+// operands.
+exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __half* scales,
+                         const __half* s_out, __half* y, float* zacc, uint32_t* cnt, int m, int n, int M,
+                         int split, uint32_t* status, int debug_stall, cudaStream_t stream);
+
+// Dense prefill path (exl3_gemm above EXL3_MAX_BATCH): batch rows per MMA tile
+// (N of 128 x N x 16) and the workspace layout: counters and status as above,
+// zacc fp32 [M][m], bimg one (kDenseNB x n) operand-B image per tile of
+// kDenseNB batch rows, aimg the decoded matrix as m * n binary16 operand-A
+// images, cnt one uint32 per (128-row block, tile): K-split arrivals.
+constexpr int kDenseNB = 256;
+inline int dense_tiles(int M) { return (M + kDenseNB - 1) / kDenseNB; }
+inline size_t dense_bimg_offset(int m, int M) { return bimg_offset(m, M); }
+inline size_t dense_aimg_offset(int m, int n, int M) {
+  return dense_bimg_offset(m, M) +
+         align256(sizeof(__half) * static_cast<size_t>(dense_tiles(M)) * kDenseNB * n);
+}
+inline size_t dense_cnt_offset(int m, int n, int M) {
+  return dense_aimg_offset(m, n, M) + align256(sizeof(__half) * static_cast<size_t>(m) * n);
+}
+inline size_t dense_total(int m, int n, int M) {
+  return dense_cnt_offset(m, n, M) +
+         align256(sizeof(uint32_t) * static_cast<size_t>(m / kRowBlock) * dense_tiles(M));
+}
+// K splits of the dense kernel: the split s that minimises the per-CTA work
+// ceil(units * s / grid) / s, with a penalty of 5 % per extra split for the
+// partial sums' traffic, and at least 8 stages of 64 columns per split.
+int choose_dense_split(int units, int nstage, int grid);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
 // per 128-row block (no rotation when s_out is NULL); zeroes zacc.
 exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,

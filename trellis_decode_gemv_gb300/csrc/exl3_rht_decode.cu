@@ -52,14 +52,16 @@ __global__ void __launch_bounds__(kThreads)
   *reinterpret_cast<uint2*>(out + row * d + col) = orr;
 }
 
-// Operand B images of the tensor-core layer kernel.  One warp per (batch row
-// r < nb, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
+// Operand B images of the tensor-core kernels.  The M batch rows form tiles of
+// nb rows; tile t's image starts at half offset t * nb * n.  One warp per
+// (batch row, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
 // itself without s_in), rounded to binary16 and stored in the canonical
-// K-major no-swizzle layout of an nb x 128 operand: element (r, k) at half
-// offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + k % 8 of the
-// block's image.  Rows r >= M are zero.  With bsum, also the fp32 sum of the
-// block's binary16 values.  The layer kernel is a programmatic dependent of
-// this one and waits for it before reading the images.
+// K-major no-swizzle layout of an nb x 128 operand: element (r, k), r the row
+// within its tile, at half offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) *
+// 8 + k % 8 of the block's image at kb * nb * 128.  Rows past M are zero.
+// With bsum, also the fp32 sum of the block's binary16 values.  The MMA
+// kernels are programmatic dependents of this one and wait for it before
+// reading the images.
 __global__ void __launch_bounds__(kSmallThreads, 16)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
                 __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
@@ -67,13 +69,16 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   const int lane = threadIdx.x & 31;
   const int nkb = n / kRowBlock;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
-  if (job >= static_cast<long long>(nb) * nkb) return;
-  const int r = static_cast<int>(job / nkb);
-  const int kb = static_cast<int>(job - static_cast<long long>(r) * nkb);
+  const int tiles = (M + nb - 1) / nb;
+  if (job >= static_cast<long long>(tiles) * nb * nkb) return;
+  const int g = static_cast<int>(job / nkb);  // batch row
+  const int kb = static_cast<int>(job - static_cast<long long>(g) * nkb);
+  const int tile = g / nb;
+  const int r = g - tile * nb;  // row within its tile
   uint2 o = make_uint2(0u, 0u);
-  if (r < M) {
+  if (g < M) {
     const int col = kb * kRowBlock + 4 * lane;
-    const uint2 xr = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(r) * n + col);
+    const uint2 xr = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g) * n + col);
     if (signs != nullptr) {
       const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
       const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
@@ -96,11 +101,11 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
       float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
 #pragma unroll
       for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
-      if (lane == 0) bsum[static_cast<size_t>(r) * nkb + kb] = hs;
+      if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
     }
   }
   // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
-  const size_t off = static_cast<size_t>(kb) * nb * kRowBlock +
+  const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
                      (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
   *reinterpret_cast<uint2*>(bimg + off) = o;
 }
@@ -230,6 +235,58 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The same decode, written as the dense tensor-core kernel's operand A: for
+// every 128-row block rb and 64-column stage ks, a 16 KB image at byte
+// (rb * (n / 64) + ks) * 16384 in the canonical K-major no-swizzle layout of a
+// 128 x 64 binary16 operand: element (r, k) at byte
+// ((k / 8) * 16 + r / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
+template <int K, int CB>
+__global__ void __launch_bounds__(kThreads)
+    decode_aimg_kernel(const uint32_t* __restrict__ codes, int m, int n, unsigned char* __restrict__ aimg) {
+  const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
+  const int tiles_per_row = n / 16;
+  const long long tiles = static_cast<long long>(m / 16) * tiles_per_row;
+  if (gid >= tiles * 8) return;
+  const long long tile = gid >> 3;
+  const int p = static_cast<int>(gid & 7);
+  const long long I = tile / tiles_per_row;
+  const int J = static_cast<int>(tile - I * tiles_per_row);
+  uint32_t wr[RowPair<K>::kPairWords];
+  load_row_pair<K>(codes + tile * RowPair<K>::kTileWords, p, wr);
+  const long long rb = I / 8;
+  unsigned char* stage = aimg + (rb * (n / 64) + J / 4) * 16384;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint32_t packed[8];
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const __half lo = decode_state<CB>(pair_state<K>(wr, 16 * k + c));
+      const __half hi = decode_state<CB>(pair_state<K>(wr, 16 * k + c + 1));
+      packed[c / 2] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+                      (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    }
+    const int r = static_cast<int>(I % 8) * 16 + 2 * p + k;  // row within the 128-row block
+    const int kg = 2 * (J % 4);                              // first 8-column group of the tile
+    unsigned char* row0 = stage + ((kg * 16 + r / 8) * 128 + (r % 8) * 16);
+    *reinterpret_cast<uint4*>(row0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    *reinterpret_cast<uint4*>(row0 + 16 * 128) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  }
+}
+
+template <int K>
+exl3_status launch_decode_aimg_k(const uint32_t* codes, int codebook, int m, int n, unsigned char* aimg,
+                                 cudaStream_t stream) {
+  const long long threads = static_cast<long long>(m / 16) * (n / 16) * 8;
+  const unsigned grid = static_cast<unsigned>((threads + kThreads - 1) / kThreads);
+  switch (codebook) {
+    case kCb3Inst: decode_aimg_kernel<K, kCb3Inst><<<grid, kThreads, 0, stream>>>(codes, m, n, aimg); break;
+    case kCb1Mad: decode_aimg_kernel<K, kCb1Mad><<<grid, kThreads, 0, stream>>>(codes, m, n, aimg); break;
+    case kCbMcg: decode_aimg_kernel<K, kCbMcg><<<grid, kThreads, 0, stream>>>(codes, m, n, aimg); break;
+    default: decode_aimg_kernel<K, kCbMul1><<<grid, kThreads, 0, stream>>>(codes, m, n, aimg); break;
+  }
+  return launch_status();
+}
+
 template <int K>
 exl3_status launch_decode_k(const uint32_t* codes, int codebook, int m, int n, __half* w,
                             cudaStream_t stream) {
@@ -257,7 +314,7 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>(nb) * (n / kRowBlock);
+  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * nb * (n / kRowBlock);
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   bimg_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
@@ -328,6 +385,21 @@ exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, _
   g.e[0].y = y;
   g.e[0].m = m;
   return launch_epi_group(g, stream);
+}
+
+exl3_status launch_decode_aimg(const uint32_t* codes, int K, int codebook, int m, int n,
+                               unsigned char* aimg, cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_decode_aimg_k<1>(codes, codebook, m, n, aimg, stream);
+    case 2: return launch_decode_aimg_k<2>(codes, codebook, m, n, aimg, stream);
+    case 3: return launch_decode_aimg_k<3>(codes, codebook, m, n, aimg, stream);
+    case 4: return launch_decode_aimg_k<4>(codes, codebook, m, n, aimg, stream);
+    case 5: return launch_decode_aimg_k<5>(codes, codebook, m, n, aimg, stream);
+    case 6: return launch_decode_aimg_k<6>(codes, codebook, m, n, aimg, stream);
+    case 7: return launch_decode_aimg_k<7>(codes, codebook, m, n, aimg, stream);
+    case 8: return launch_decode_aimg_k<8>(codes, codebook, m, n, aimg, stream);
+    default: return EXL3_ERR_K;
+  }
 }
 
 exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int n, __half* w,

@@ -62,20 +62,40 @@ constexpr int kMmaWarp = 20;
 constexpr int kTmaWarp = 21;
 constexpr int kBWarp = 22;
 constexpr int kThreads = 23 * 32;
-// A chunk is 16 tile columns (256 input columns) when n allows it, else 8.
-constexpr int kMaxChunkTiles = 16;
-// Code chunks in flight: 8 for K <= 4, 4 above (shared-memory budget).
-template <int K>
-__host__ __device__ constexpr int ring_depth() {
-  return K <= 4 ? 8 : 4;
-}
 constexpr int kMaxRing = 8;
-constexpr int kSlots = 3;               // chunks of A in TMEM (and of B in shared memory)
-constexpr int kChunkCols = 128;         // TMEM columns per chunk slot (two weights each)
+constexpr int kMaxSlots = 4;
+constexpr int kMaxNB = 128;
 constexpr int kTmemCols = 512;
-constexpr int kDCol = 0;                // D buffers at columns 0 and 32
-constexpr int kACol = 64;               // A slots at 64 + 128 * slot
+constexpr int kDCol = 0;                // D buffers at columns 0 and Cfg::kDStride
 constexpr int kRowPadWords = 16;        // keeps tile-row strips 64 B apart from a bank multiple
+
+// Layout of the kernel for K-bit codes and N = NB batch columns.
+//  NB <= 32 (skinny batches): chunks of 16 tile columns (256 input columns)
+//    when n allows it, else 8; 3 A slots of 128 TMEM columns after D at
+//    columns 0 and 32; 8 code chunks in flight for K <= 4, 4 above; D is
+//    transposed through shared memory for 16-byte reductions.
+//  NB = 128 (prefill passes of 128 batch rows): chunks of 8 tile columns;
+//    4 A slots of 64 columns after D at columns 0 and 128; 4 code chunks in
+//    flight; 32 KB operand-B slots; D transposed 16 batch columns at a time.
+template <int K, int NB>
+struct TcCfg {
+  static constexpr bool kWide = NB > 32;
+  static constexpr int kMaxTiles = kWide ? 8 : 16;
+  static constexpr int kSlots = kWide ? 4 : 3;
+  static constexpr int kSlotCols = kWide ? 64 : 128;
+  static constexpr int kDStride = kWide ? NB : 32;
+  static constexpr int kACol = 2 * kDStride;
+  static constexpr int kRing = kWide ? 4 : (K <= 4 ? 8 : 4);
+  static constexpr int kRowWords = kMaxTiles * 8 * K + kRowPadWords;
+  static constexpr int kChunkBytes = 8 * kRowWords * 4;
+  static constexpr int kBSlotBytes = NB * kMaxTiles * 16 * 2;
+  // D transposed to [batch][row] for 16-byte reductions: every batch column
+  // (skinny), or 16 at a time (wide)
+  static constexpr int kTransposeCols = kWide ? 16 : 32;
+  static constexpr int kTransposeBytes = kTransposeCols * 128 * 4;
+  static_assert(kACol + kSlots * kSlotCols <= kTmemCols, "TMEM columns");
+  static_assert(kSlots <= kMaxSlots && kRing <= kMaxRing && NB <= kMaxNB, "barrier arrays");
+};
 constexpr uint32_t kSpinLimit = 1u << 20;  // about a second of try_wait polling
 constexpr int kEpiBarrier = 1;          // named barrier of the epilogue warps
 
@@ -311,31 +331,17 @@ struct TcParams {
 struct TcShared {
   uint64_t ring_full[kMaxRing];
   uint64_t ring_empty[kMaxRing];
-  uint64_t a_full[kSlots];
-  uint64_t a_empty[kSlots];
-  uint64_t b_full[kSlots];
+  uint64_t a_full[kMaxSlots];
+  uint64_t a_empty[kMaxSlots];
+  uint64_t b_full[kMaxSlots];
   uint64_t d_full[2];
   uint64_t d_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t epi_go;
-  float xsum[32];
-  alignas(16) float zt[32 * 128];  // D of a run transposed to [batch][row] for 16-byte reductions
+  float xsum[kMaxNB];
 };
-
-template <int K>
-__host__ __device__ constexpr int chunk_row_words() {
-  return kMaxChunkTiles * 8 * K + kRowPadWords;
-}
-template <int K>
-__host__ __device__ constexpr int chunk_bytes() {
-  return 8 * chunk_row_words<K>() * 4;
-}
-template <int NB>
-__host__ __device__ constexpr int bslot_bytes() {
-  return NB * kMaxChunkTiles * 16 * 2;
-}
 
 __device__ __forceinline__ bool aborted(const TcShared& sh) {
   return *reinterpret_cast<const volatile uint32_t*>(&sh.abort) != 0u;
@@ -345,12 +351,16 @@ __device__ __forceinline__ void set_abort(TcShared& sh) { atomicOr(&sh.abort, 1u
 
 template <int K, int CB, int NB>
 __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
+  using Cfg = TcCfg<K, NB>;
+  constexpr int kSlots = Cfg::kSlots;
+  constexpr int kRing = Cfg::kRing;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   TcShared& sh = *reinterpret_cast<TcShared*>(smem_raw);
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
-  unsigned char* bring = smem_raw + ctrl;
-  uint32_t* ring = reinterpret_cast<uint32_t*>(bring + static_cast<size_t>(kSlots) * bslot_bytes<NB>());
-  constexpr int kRing = ring_depth<K>();
+  // D of a run transposed to [batch][row] (skinny batches), 16-byte aligned
+  float* zt = reinterpret_cast<float*>(smem_raw + ctrl);
+  unsigned char* bring = smem_raw + ctrl + Cfg::kTransposeBytes;
+  uint32_t* ring = reinterpret_cast<uint32_t*>(bring + static_cast<size_t>(kSlots) * Cfg::kBSlotBytes);
 
   // The output kernel may launch now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -379,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * ct * 32u * K);
     __syncwarp();
     if (lane < 8) {
-      uint32_t* dst = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4);
+      uint32_t* dst = ring + static_cast<size_t>(slot) * (Cfg::kChunkBytes / 4);
       const uint32_t* src = a.codes + (static_cast<size_t>(rb * 8 + lane) * tiles_per_row + kb * ct) * (8 * K);
-      bulk_g2s(dst + lane * chunk_row_words<K>(), src, ct * 32u * K, &sh.ring_full[slot]);
+      bulk_g2s(dst + lane * Cfg::kRowWords, src, ct * 32u * K, &sh.ring_full[slot]);
     }
   };
   int pre = 0;
@@ -450,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         if (use > 0 && !mbar_wait(&sh.a_empty[slot], (use - 1) & 1)) set_abort(sh);
         if (aborted(sh)) break;
         mbar_arrive_expect_tx(&sh.b_full[slot], bbytes);
-        bulk_g2s(bring + static_cast<size_t>(slot) * bslot_bytes<NB>(),
+        bulk_g2s(bring + static_cast<size_t>(slot) * Cfg::kBSlotBytes,
                  p.bimg + static_cast<size_t>(kb) * NB * 16 * ct, bbytes, &sh.b_full[slot]);
       }
       for (int i = 0; i < kSlots && i < seq; ++i) {
@@ -471,15 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     const uint32_t off = static_cast<uint32_t>((rr * K) & 1) * 16u;
     const int t0 = g * (ct / 4);          // first tile column of this warpgroup
     const bool two = ct == 16;            // a second tile pair per chunk
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol + 8 * t0;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + Cfg::kACol + 8 * t0;
     int seq = 0;
     for (int c = lo; c < hi; ++c, ++seq) {
       const int slot = seq % kRing;
       bool ok = mbar_wait(&sh.ring_full[slot], (seq / kRing) & 1);
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      const uint32_t* rw = ring + static_cast<size_t>(slot) * (chunk_bytes<K>() / 4) +
-                           trow * chunk_row_words<K>() + t0 * (8 * K);
+      const uint32_t* rw = ring + static_cast<size_t>(slot) * (Cfg::kChunkBytes / 4) +
+                           trow * Cfg::kRowWords + t0 * (8 * K);
       uint32_t raw[4][RowWords<K>::kRaw];
 #pragma unroll
       for (int i = 0; i < RowWords<K>::kRaw; ++i) {
@@ -503,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       if (use > 0) ok = mbar_wait(&sh.a_empty[aslot], (use - 1) & 1);
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      tmem_st16(lane_addr + aslot * kChunkCols, v0);
-      if (two) tmem_st16(lane_addr + aslot * kChunkCols + 16, v1);
+      tmem_st16(lane_addr + aslot * Cfg::kSlotCols, v0);
+      if (two) tmem_st16(lane_addr + aslot * Cfg::kSlotCols + 16, v1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         set_abort(sh);
         break;
       }
-      const uint32_t dt = tm + kDCol + 32 * db;
+      const uint32_t dt = tm + kDCol + Cfg::kDStride * db;
       for (uint32_t acc = 0; c < end; ++c, ++seq, acc = 1) {
         const int slot = seq % kSlots;
         const uint32_t par = (seq / kSlots) & 1;
@@ -544,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
         }
         tc_fence_after();
         // descriptor start address advances by (bytes >> 4) in its low field
-        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * bslot_bytes<NB>()) >> 4);
-        const uint32_t at = tm + kACol + slot * kChunkCols;
+        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(slot) * Cfg::kBSlotBytes) >> 4);
+        const uint32_t at = tm + Cfg::kACol + slot * Cfg::kSlotCols;
         if (lane == 0) {
           // one MMA per tile column (K = 16); the first MMA of a run overwrites D
           mma_f16_ts(dt, at, bd, idesc, acc);
@@ -599,38 +609,50 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
       bool ok = !aborted(sh) && mbar_wait(&sh.d_full[db], (run >> 1) & 1);
       if (!ok) set_abort(sh);
       // tcgen05.ld is a whole-warp instruction: skip it warp-uniformly.
-      if (!__any_sync(0xFFFFFFFFu, !ok)) {
-        tc_fence_after();
-        const int row = ew * 32 + lane;
+      const int row = ew * 32 + lane;
+      float* zblk = a.zacc + static_cast<size_t>(rb) * kRowBlock;
+      const bool warp_ok = !__any_sync(0xFFFFFFFFu, !ok);
+      if (warp_ok) tc_fence_after();
+      // D in slices of kTransposeCols batch columns: TMEM -> registers (1MAD
+      // and mul1 corrected) -> shared memory [batch][row] -> 16-byte
+      // reductions of four consecutive rows of one batch row.
+      constexpr int kTc = Cfg::kTransposeCols;
+      const int slices = (p.M + kTc - 1) / kTc;
 #pragma unroll 1
-        for (int h = 0; h < NB / 16; ++h) {
-          float d[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + kDCol + 32 * db + 16 * h, d);
+      for (int sl = 0; sl < slices; ++sl) {
+        if (warp_ok) {
+#pragma unroll 1
+          for (int h = 0; h < kTc / 16; ++h) {
+            const int b0 = sl * kTc + 16 * h;
+            if (b0 >= p.M) break;  // warp-uniform
+            float d[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + kDCol + Cfg::kDStride * db + b0, d);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int b = 16 * h + j;
-            if (b < p.M) {
-              float z = d[j];
-              if constexpr (byte_sum_code<CB>())
-                z = (z - static_cast<float>(1024 + byte_sum_centre<CB>()) * sh.xsum[b]) * byte_sum_scale<CB>();
-              sh.zt[b * kRowBlock + row] = z;
+            for (int j = 0; j < 16; ++j) {
+              const int b = b0 + j;
+              if (b < p.M) {
+                float z = d[j];
+                if constexpr (byte_sum_code<CB>())
+                  z = (z - static_cast<float>(1024 + byte_sum_centre<CB>()) * sh.xsum[b]) * byte_sum_scale<CB>();
+                zt[(16 * h + j) * kRowBlock + row] = z;
+              }
             }
           }
         }
-        tc_fence_before();
-      }
-      mbar_arrive(&sh.d_empty[db]);
-      epi_sync();
-      if (!aborted(sh)) {
-        // four consecutive rows of one batch row per 16-byte reduction
-        float* zblk = a.zacc + static_cast<size_t>(rb) * kRowBlock;
-        for (int i = et; i < p.M * (kRowBlock / 4); i += 128) {
-          const int b = i / (kRowBlock / 4);
-          const int q = i - b * (kRowBlock / 4);
-          const float4 v = *reinterpret_cast<const float4*>(&sh.zt[b * kRowBlock + 4 * q]);
-          atomicAdd(reinterpret_cast<float4*>(zblk + static_cast<size_t>(b) * a.m + 4 * q), v);
+        epi_sync();
+        if (!aborted(sh)) {
+          const int nb = p.M - sl * kTc < kTc ? p.M - sl * kTc : kTc;
+          for (int i = et; i < nb * (kRowBlock / 4); i += 128) {
+            const int bl = i / (kRowBlock / 4);
+            const int q = i - bl * (kRowBlock / 4);
+            const float4 v = *reinterpret_cast<const float4*>(&zt[bl * kRowBlock + 4 * q]);
+            atomicAdd(reinterpret_cast<float4*>(zblk + static_cast<size_t>(sl * kTc + bl) * a.m + 4 * q), v);
+          }
         }
+        epi_sync();  // zt is rewritten by the next slice
       }
+      if (warp_ok) tc_fence_before();
+      mbar_arrive(&sh.d_empty[db]);
     }
   }
 
@@ -644,12 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
   if (tid == 0 && aborted(sh) && a.status != nullptr) atomicOr(a.status, 1u);
 }
 
-// Shared memory: control block + B ring + code ring.
+// Shared memory: control block + transpose buffer + B ring + code ring.
 template <int K, int NB>
 inline size_t tc_smem_bytes() {
+  using Cfg = TcCfg<K, NB>;
   const size_t ctrl = (sizeof(TcShared) + 1023) & ~static_cast<size_t>(1023);
-  return ctrl + static_cast<size_t>(kSlots) * bslot_bytes<NB>() +
-         static_cast<size_t>(ring_depth<K>()) * chunk_bytes<K>();
+  return ctrl + Cfg::kTransposeBytes + static_cast<size_t>(Cfg::kSlots) * Cfg::kBSlotBytes +
+         static_cast<size_t>(Cfg::kRing) * Cfg::kChunkBytes;
 }
 
 template <int K, int CB, int NB>
@@ -660,7 +683,8 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
   p.bimg = bimg;
   p.bsum = bsum;
   p.M = M;
-  p.ct = (a.n % (16 * kMaxChunkTiles)) == 0 ? kMaxChunkTiles : kMaxChunkTiles / 2;
+  using Cfg = TcCfg<K, NB>;
+  p.ct = Cfg::kWide ? 8 : (a.n % 256 == 0 ? 16 : 8);
   // At least 116 KB so that a single CTA is resident per SM (it owns all 512
   // TMEM columns; a second CTA would wait in tcgen05.alloc).
   size_t smem = tc_smem_bytes<K, NB>();
@@ -684,22 +708,23 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
   return launch_status();
 }
 
+template <int K, int CB>
+exl3_status launch_tc_nb(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
+                         cudaStream_t stream) {
+  if (M <= 16) return launch_tc_t<K, CB, 16>(a, bimg, bsum, M, grid, stream);
+  if (M <= 32) return launch_tc_t<K, CB, 32>(a, bimg, bsum, M, grid, stream);
+  return launch_tc_t<K, CB, 128>(a, bimg, bsum, M, grid, stream);
+}
+
+// M <= 128 batch rows; N = 16, 32 or 128 (tc_nb).
 template <int K>
 exl3_status launch_tc_dispatch(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                                cudaStream_t stream) {
   switch (a.codebook) {
-    case kCb3Inst:
-      return M <= 16 ? launch_tc_t<K, kCb3Inst, 16>(a, bimg, bsum, M, grid, stream)
-                     : launch_tc_t<K, kCb3Inst, 32>(a, bimg, bsum, M, grid, stream);
-    case kCb1Mad:
-      return M <= 16 ? launch_tc_t<K, kCb1Mad, 16>(a, bimg, bsum, M, grid, stream)
-                     : launch_tc_t<K, kCb1Mad, 32>(a, bimg, bsum, M, grid, stream);
-    case kCbMcg:
-      return M <= 16 ? launch_tc_t<K, kCbMcg, 16>(a, bimg, bsum, M, grid, stream)
-                     : launch_tc_t<K, kCbMcg, 32>(a, bimg, bsum, M, grid, stream);
-    default:
-      return M <= 16 ? launch_tc_t<K, kCbMul1, 16>(a, bimg, bsum, M, grid, stream)
-                     : launch_tc_t<K, kCbMul1, 32>(a, bimg, bsum, M, grid, stream);
+    case kCb3Inst: return launch_tc_nb<K, kCb3Inst>(a, bimg, bsum, M, grid, stream);
+    case kCb1Mad: return launch_tc_nb<K, kCb1Mad>(a, bimg, bsum, M, grid, stream);
+    case kCbMcg: return launch_tc_nb<K, kCbMcg>(a, bimg, bsum, M, grid, stream);
+    default: return launch_tc_nb<K, kCbMul1>(a, bimg, bsum, M, grid, stream);
   }
 }
 
