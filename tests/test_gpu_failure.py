@@ -58,7 +58,7 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
         B.exl3_set_path(B.PATH_AUTO)
 
 
-@pytest.mark.parametrize("m,n,M", [(256, 1664, 90), (384, 512, 300)])
+@pytest.mark.parametrize("m,n,M", [(256, 3200, 90), (384, 512, 300)])
 def test_dense_prefill_wait_timeout_sets_status_and_context_survives(m, n, M):
     """The dense prefill kernel with its producer stalled: with K split (first
     shape) the row sums stay zero; without (second) nothing is written.  The

@@ -76,9 +76,10 @@ def test_prefill_codes_and_widths(strategy, K, cb):
 
 @pytest.mark.parametrize("K,cb", [(3, 0), (5, 2), (6, 3), (7, 1)])
 def test_prefill_split_k(strategy, K, cb):
-    """Few row blocks and long rows: the dense kernel splits K (26 stages of
-    64 columns in three splits of 8, 9 and 9) and the output kernel finishes."""
-    m, n, M = 256, 1664, 90
+    """Few row blocks and long rows: the dense kernel splits K (50 stages of
+    64 columns in three splits of 16, 17 and 17) and the last split of each
+    block finishes it."""
+    m, n, M = 256, 3200, 90
     inp = synth.layer_inputs(m, n, K, M, config=95, index=K)
     y, ws = _run(inp, K, cb, m, n, M)
     assert_layer_close(y, _ref(inp, K, cb, m, n), f"{strategy} split K={K}")
@@ -155,3 +156,26 @@ def test_small_batches_go_through_gemm_small():
     inp = synth.layer_inputs(m, n, K, M, config=94, index=0)
     y, _ = _run(inp, K, cb, m, n, M)
     assert_layer_close(y, _ref(inp, K, cb, m, n))
+
+
+def test_prefill_passes_repeated_1mad_block_sums():
+    """Back-to-back 128-row passes with the 1MAD correction: each pass's MMA
+    kernel reads the block sums the operand-image kernel before it writes, so
+    every call, repeated, must match on every row."""
+    m, n, K, cb, M = 256, 384, 3, 1, 513
+    inp = synth.layer_inputs(m, n, K, M, config=90, index=M)
+    ref = _ref(inp, K, cb, m, n)
+    B.exl3_set_path(B.PATH_TENSOR)
+    try:
+        d = upload(inp)
+        ws = torch.zeros(B.exl3_gemm_workspace_bytes(m, n, M), dtype=torch.uint8, device="cuda")
+        ys = [torch.empty((M, m), dtype=torch.float16, device="cuda") for _ in range(6)]
+        for y in ys:
+            B.exl3_gemm(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"], y=y, workspace=ws)
+        torch.cuda.synchronize()
+        for i, y in enumerate(ys):
+            got = y.float().cpu().numpy()
+            row_err = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+            assert np.all(row_err <= 5e-3), (i, np.nonzero(row_err > 5e-3)[0][:8])
+    finally:
+        B.exl3_set_path(B.PATH_AUTO)

@@ -13,9 +13,10 @@
 // to the fp32 row sums zacc [M][m], and the unit that completes the block's
 // sums (an arrival counter per block and tile) finishes it from zacc.
 //
-// Warp roles: warps 0-3 epilogue (TMEM lane quarter = warp), warp 4 MMA issue
-// and TMEM allocation (one lane issues), warp 5 producer (one lane: two 1-D
-// bulk copies per stage, 16 KB of A and 32 KB of B, into a 4-deep ring).
+// Warp roles: warps 0-3 and 6-9 epilogue (TMEM lane quarter = warp % 4), warp
+// 4 MMA issue and TMEM allocation (one lane issues), warp 5 producer (one lane:
+// two 1-D bulk copies per stage, 16 KB of A and 32 KB of B, into a 4-deep
+// ring).
 // Stages are 64 input columns: 4 MMAs of 128 x 256 x 16, both operands in
 // shared memory in the canonical K-major no-swizzle layout.  D is
 // double-buffered over all 512 TMEM columns, so a unit's epilogue overlaps the
@@ -48,9 +49,11 @@ constexpr int kStages = 4;
 constexpr int kABytes = 128 * kStageK * 2;   // 16 KB
 constexpr int kBBytes = kNB * kStageK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 6 * 32;
+constexpr int kThreads = 10 * 32;
 constexpr int kMmaWarp = 4;
 constexpr int kProdWarp = 5;
+constexpr int kEpiWarps = 8;  // warps 0-3 and 6-9
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kSlice = 32;          // batch columns per epilogue slice
 constexpr int kTmemCols = 512;
 constexpr int kEpiBarrier = 1;
@@ -105,7 +108,7 @@ __device__ __forceinline__ bool aborted(const DenseShared& sh) {
 }
 __device__ __forceinline__ void set_abort(DenseShared& sh) { atomicOr(&sh.abort, 1u); }
 __device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(128) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
 }
 
 // D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16, cta_group::1.
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.d_full[i], 1);
-      mbar_init(&sh.d_empty[i], 128);
+      mbar_init(&sh.d_empty[i], kEpiThreads);
     }
     mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
@@ -254,7 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
     mbar_wait(&sh.mma_done, 0);
   } else {
     // ---- epilogue: D -> scale, output signs, FWHT -> y ---------------------------------
-    const int row = warp * 32 + lane;  // TMEM lane = row of the 128-row block
+    // Eight warps: warp w reads TMEM lanes 32 * (w % 4) .. + 31 (rows of the
+    // block); the two warps of a lane quarter take 16 batch columns each of a
+    // 32-column slice.  Then every warp finishes whole batch rows.
+    const int quarter = warp & 3;
+    const int half = warp >= 6 ? 1 : 0;
+    const int e = warp < 4 ? warp : warp - 2;  // epilogue warp index 0..7
+    const int row = quarter * 32 + lane;       // TMEM lane = row of the 128-row block
     for (int li = 0; li < my_units; ++li) {
       if (tid == 0) sh.epi_go = aborted(sh) ? 0u : 1u;
       epi_sync();
@@ -292,22 +301,19 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       const int slices = (rows + kSlice - 1) / kSlice;
 #pragma unroll 1
       for (int sl = 0; sl < slices; ++sl) {
-        if (warp_ok) {
-#pragma unroll 1
-          for (int h = 0; h < kSlice / 16; ++h) {
-            const int b0 = sl * kSlice + 16 * h;
-            if (b0 >= rows) break;  // warp-uniform
-            float d[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(kNB * db + b0), d);
+        const int b0 = sl * kSlice + 16 * half;
+        if (warp_ok && b0 < rows) {  // warp-uniform
+          float d[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(kNB * db + b0), d);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sh.zt[(16 * h + j) * kRowBlock + row] = d[j];
-          }
+          for (int j = 0; j < 16; ++j) sh.zt[(16 * half + j) * kRowBlock + row] = d[j];
         }
         epi_sync();
         if (!__any_sync(0xFFFFFFFFu, aborted(sh))) {  // warp-uniform: the FWHT shuffles
           // one batch row per warp at a time: lane holds rows 4*lane .. +3
           const int nb = rows - sl * kSlice < kSlice ? rows - sl * kSlice : kSlice;
-          for (int bl = warp; bl < nb; bl += 4) {
+#pragma unroll 4
+          for (int bl = e; bl < nb; bl += kEpiWarps) {
             const float4 z = *reinterpret_cast<const float4*>(&sh.zt[bl * kRowBlock + 4 * lane]);
             const size_t b = static_cast<size_t>(t) * kNB + sl * kSlice + bl;
             if (finish)
@@ -336,18 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       // kFixRows batch rows per warp in flight: the loads are L2 round trips
       constexpr int kFixRows = 8;
 #pragma unroll 1
-      for (int b0 = warp; b0 < rows; b0 += 4 * kFixRows) {
+      for (int b0 = e; b0 < rows; b0 += kEpiWarps * kFixRows) {
         float4 z[kFixRows];
 #pragma unroll
         for (int i = 0; i < kFixRows; ++i) {
-          const int bl = b0 + 4 * i;
+          const int bl = b0 + kEpiWarps * i;
           z[i] = bl < rows ? __ldcg(reinterpret_cast<const float4*>(
                                  p.zacc + (static_cast<size_t>(t) * kNB + bl) * p.m + r0))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < kFixRows; ++i) {
-          const int bl = b0 + 4 * i;
+          const int bl = b0 + kEpiWarps * i;
           if (bl >= rows) break;  // warp-uniform
           const size_t b = static_cast<size_t>(t) * kNB + bl;
           __stcg(reinterpret_cast<float4*>(p.zacc + b * p.m + r0), make_float4(0.f, 0.f, 0.f, 0.f));
@@ -370,18 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
 }  // namespace dense
 
 int choose_dense_split(int units, int nstage, int grid) {
-  int best = 1;
-  double best_cost = 0.0;
-  for (int s = 1; s <= 16 && nstage / s >= 8; ++s) {
-    const long long frags = static_cast<long long>(units) * s;
-    const long long per_cta = (frags + grid - 1) / grid;
-    const double cost = static_cast<double>(per_cta) / s * (1.0 + 0.05 * (s - 1));
-    if (s == 1 || cost < best_cost - 1e-9) {
-      best = s;
-      best_cost = cost;
-    }
-  }
-  return best;
+  int s = units >= grid ? 1 : grid / units;
+  if (s > nstage / 16) s = nstage / 16;
+  if (s > 16) s = 16;
+  return s < 1 ? 1 : s;
 }
 
 exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __half* scales,

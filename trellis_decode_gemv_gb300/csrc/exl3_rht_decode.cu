@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads)
 
 // Operand B images of the tensor-core kernels.  The M batch rows form tiles of
 // nb rows; tile t's image starts at half offset t * nb * n.  One warp per
-// (batch row, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
+// (four consecutive batch rows, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
 // itself without s_in), rounded to binary16 and stored in the canonical
 // K-major no-swizzle layout of an nb x 128 operand: element (r, k), r the row
 // within its tile, at half offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) *
@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(kThreads)
 // With bsum, also the fp32 sum of the block's binary16 values.  The MMA
 // kernels are programmatic dependents of this one and wait for it before
 // reading the images.
+constexpr int kBimgRows = 4;  // batch rows per warp (independent loads in flight)
+
 __global__ void __launch_bounds__(kSmallThreads, 16)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
                 __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
@@ -70,44 +72,59 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   const int nkb = n / kRowBlock;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   const int tiles = (M + nb - 1) / nb;
-  if (job >= static_cast<long long>(tiles) * nb * nkb) return;
-  const int g = static_cast<int>(job / nkb);  // batch row
-  const int kb = static_cast<int>(job - static_cast<long long>(g) * nkb);
-  const int tile = g / nb;
-  const int r = g - tile * nb;  // row within its tile
-  uint2 o = make_uint2(0u, 0u);
-  if (g < M) {
-    const int col = kb * kRowBlock + 4 * lane;
-    const uint2 xr = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g) * n + col);
-    if (signs != nullptr) {
-      const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
-      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
-      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
-      const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-      const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-      float v[4] = {__low2float(x01) * __low2float(s01), __high2float(x01) * __high2float(s01),
-                    __low2float(x23) * __low2float(s23), __high2float(x23) * __high2float(s23)};
-      fwht128_warp(v, lane);
-      const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
-      const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
-      o.x = *reinterpret_cast<const uint32_t*>(&o01);
-      o.y = *reinterpret_cast<const uint32_t*>(&o23);
-    } else {
-      o = xr;
-    }
-    if (bsum != nullptr) {
-      const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
-      const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
-      float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+  if (job >= static_cast<long long>(tiles) * (nb / kBimgRows) * nkb) return;
+  const int g0 = kBimgRows * static_cast<int>(job / nkb);  // first batch row (nb is a multiple of 4)
+  const int kb = static_cast<int>(job - static_cast<long long>(g0 / kBimgRows) * nkb);
+  const int col = kb * kRowBlock + 4 * lane;
+  uint2 xr[kBimgRows];
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
-      if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
-    }
+  for (int i = 0; i < kBimgRows; ++i)
+    xr[i] = g0 + i < M ? *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g0 + i) * n + col)
+                       : make_uint2(0u, 0u);
+  float s[4] = {1.f, 1.f, 1.f, 1.f};
+  if (signs != nullptr) {
+    const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+    s[0] = __low2float(s01);
+    s[1] = __high2float(s01);
+    s[2] = __low2float(s23);
+    s[3] = __high2float(s23);
   }
-  // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
-  const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
-                     (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
-  *reinterpret_cast<uint2*>(bimg + off) = o;
+#pragma unroll
+  for (int i = 0; i < kBimgRows; ++i) {
+    const int g = g0 + i;  // batch row
+    const int tile = g / nb;
+    const int r = g - tile * nb;  // row within its tile
+    uint2 o = make_uint2(0u, 0u);
+    if (g < M) {  // warp-uniform
+      if (signs != nullptr) {
+        const __half2 x01 = *reinterpret_cast<const __half2*>(&xr[i].x);
+        const __half2 x23 = *reinterpret_cast<const __half2*>(&xr[i].y);
+        float v[4] = {__low2float(x01) * s[0], __high2float(x01) * s[1], __low2float(x23) * s[2],
+                      __high2float(x23) * s[3]};
+        fwht128_warp(v, lane);
+        const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
+        const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
+        o.x = *reinterpret_cast<const uint32_t*>(&o01);
+        o.y = *reinterpret_cast<const uint32_t*>(&o23);
+      } else {
+        o = xr[i];
+      }
+      if (bsum != nullptr) {
+        const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
+        const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
+        float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
+        if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
+      }
+    }
+    // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
+    const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
+                       (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
+    *reinterpret_cast<uint2*>(bimg + off) = o;
+  }
 }
 
 // x pairs of the warp-shuffle layer kernel, for a group of layers.  One warp
@@ -314,7 +331,7 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * nb * (n / kRowBlock);
+  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * (nb / kBimgRows) * (n / kRowBlock);
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   bimg_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);

@@ -578,6 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_layer_kernel(TcParams p) {
     mbar_wait(&sh.mma_done, 0);
   } else {
     // ---- epilogue warps: D of each run into the row sums -----------------------------
+    // The block sums of x-tilde come from the preceding grid on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ew = warp - kEpiWarp0;      // 0..3 = TMEM lane quarter
     const int et = tid - kEpiWarp0 * 32;  // 0..127
     int run = 0;
