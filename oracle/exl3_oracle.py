@@ -18,7 +18,8 @@ source pages, named in its docstring:
         Part three (integer budget, the int-to-half splice), Part six (RHT),
         Part eight (the bitshift trellis: 16-bit window, random access, 16x16
         tiles, tail-biting), Part nine (the 3INST and 1MAD computed codes),
-        Part eleven (EXL3: 128-wide blockwise rotation).
+        Part eleven (EXL3: 128-wide blockwise rotation; QTIP's whole-vector
+        rotation, ``rht_whole``).
   [FG]  "EXL3 field guide" (LLM Cal): per-output-channel scales ("out_scales
         always").
 
@@ -304,6 +305,37 @@ def rht(v: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
     return out.reshape(v.shape)
 
 
+def rht_whole(v: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
+    """QTIP's rotation over the whole last axis, in float64:
+
+        out = H_d (s (.) v) / sqrt(d),  H_d the Sylvester Hadamard matrix of the
+        full (power-of-two) length d.
+
+    [TQ] Part eleven: QTIP rotates whole rows and columns, where EXL3 rotates
+    128-blocks; Part six: the transform is only plus and minus ones, applied as
+    a fast Walsh-Hadamard transform.  The butterflies below are the textbook
+    iterative transform in Sylvester order: at span h, every pair (i, i + h)
+    with bit h of i clear becomes (a + b, a - b).  ``signs is None`` means no
+    rotation on that side.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    if signs is None:
+        return v.copy()
+    d = v.shape[-1]
+    assert d > 0 and d & (d - 1) == 0, "whole-vector rotation needs a power-of-two length"
+    u = (v * np.asarray(signs, dtype=np.float64)).reshape(-1, d).copy()
+    h = 1
+    while h < d:
+        u = u.reshape(-1, d // (2 * h), 2, h)
+        a = u[:, :, 0, :].copy()
+        b = u[:, :, 1, :].copy()
+        u[:, :, 0, :] = a + b
+        u[:, :, 1, :] = a - b
+        u = u.reshape(-1, d)
+        h *= 2
+    return (u / math.sqrt(d)).reshape(v.shape)
+
+
 # ----------------------------------------------------------------------------
 # The layer  ([DD] Section 2, [FG] out_scales)
 # ----------------------------------------------------------------------------
@@ -347,3 +379,15 @@ def layer_forward_rowblocks(codes, K, codebook, m, n, s_in, s_out, scales, x,
         sb = None if s_out is None else s_out[b * 128:(b + 1) * 128]
         outs.append(rht(z, sb))
     return np.concatenate(outs, axis=-1)
+
+
+def layer_forward_whole(codes, K, codebook, m, n, s_in, s_out, scales, x) -> np.ndarray:
+    """The layer with QTIP's whole-vector rotations instead of EXL3's 128-blocks
+    ([TQ] Part eleven): y = H_m (s_out (.) (scale (.) (W-hat H_n (s_in (.) x))))
+    with H_d / sqrt(d) over the full (power-of-two) n and m, in float64.  The
+    same readings as ``layer_forward`` otherwise."""
+    x = np.atleast_2d(np.asarray(x))
+    W = decode_tiles(codes, K, codebook, m, n).astype(np.float64)
+    xt = rht_whole(x.astype(np.float64), s_in)
+    z = (xt @ W.T) * np.asarray(scales, dtype=np.float64)
+    return rht_whole(z, s_out)

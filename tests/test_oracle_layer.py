@@ -7,7 +7,10 @@ Part six (Hadamard entries are only +-1) and Part eleven (128-wide blockwise
 rotation).  Pins: scipy's textbook Sylvester construction, exact integer
 orthogonality, the inverse transform, the y = W x identity on a dense W, and a
 brute-force dense evaluation of the whole layer with a separately written
-sequential trellis walker.
+sequential trellis walker.  The whole-vector variant (QTIP rotates full rows
+and columns, Part eleven) is pinned against scipy's full Sylvester matrices,
+the Kronecker factorization H_{128B} = H_B (x) H_128, orthogonality, and the
+same brute-force layer with full-size matrices.
 """
 import numpy as np
 import pytest
@@ -143,3 +146,66 @@ def test_rowblock_sampling_matches_full():
     part = O.layer_forward_rowblocks(*args, row_blocks=[3, 1])
     np.testing.assert_allclose(part, np.concatenate([full[:, 384:512], full[:, 128:256]], 1),
                                rtol=1e-13, atol=1e-13)
+
+
+# ---- QTIP's whole-vector rotation ("Trellis Quantization" Part eleven) -------
+
+@pytest.mark.parametrize("d", [1, 2, 8, 128, 256, 1024])
+def test_rht_whole_matches_scipy_sylvester(d):
+    """H_d (s (.) v) / sqrt(d) against scipy's Sylvester matrix, row for row."""
+    rng = np.random.default_rng(100 + d)
+    v = rng.standard_normal((3, d))
+    s = np.where(rng.integers(0, 2, d) == 1, 1.0, -1.0)
+    ref = (v * s) @ scipy.linalg.hadamard(d).T / np.sqrt(d)
+    np.testing.assert_allclose(O.rht_whole(v, s), ref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(O.rht_whole(v, None), v)
+
+
+def test_rht_whole_kronecker_and_blockwise():
+    """Sylvester order makes H_{128 B} = H_B (x) H_128, so the whole-vector
+    transform is the blockwise one followed by a transform across the blocks;
+    at d = 128 the two rotations coincide."""
+    for B in (2, 4, 8):
+        np.testing.assert_array_equal(scipy.linalg.hadamard(128 * B),
+                                      np.kron(scipy.linalg.hadamard(B), scipy.linalg.hadamard(128)))
+    rng = np.random.default_rng(7)
+    d = 1024
+    v = rng.standard_normal((2, d))
+    s = np.where(rng.integers(0, 2, d) == 1, 1.0, -1.0)
+    blockwise = O.rht(v, s)  # (I (x) H_128) diag(s) v / sqrt(128)
+    across = blockwise.reshape(2, d // 128, 128).transpose(0, 2, 1) @ scipy.linalg.hadamard(d // 128).T
+    across = across.transpose(0, 2, 1).reshape(2, d) / np.sqrt(d // 128)
+    np.testing.assert_allclose(O.rht_whole(v, s), across, rtol=0, atol=1e-12)
+    v128 = rng.standard_normal((2, 128))
+    s128 = np.where(rng.integers(0, 2, 128) == 1, 1.0, -1.0)
+    np.testing.assert_allclose(O.rht_whole(v128, s128), O.rht(v128, s128), rtol=0, atol=1e-13)
+
+
+def test_rht_whole_is_orthogonal_involution():
+    rng = np.random.default_rng(8)
+    d = 4096
+    v = rng.standard_normal((2, d))
+    s = np.where(rng.integers(0, 2, d) == 1, 1.0, -1.0)
+    out = O.rht_whole(v, s)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=1), np.linalg.norm(v, axis=1), rtol=1e-12)
+    np.testing.assert_allclose(O.rht_whole(out, np.ones(d)) * s, v, rtol=0, atol=1e-11)
+    with pytest.raises(AssertionError):
+        O.rht_whole(np.ones((1, 384)), np.ones(384))
+
+
+def test_layer_whole_brute_force():
+    """The whole-vector layer against a dense evaluation with scipy's full
+    Hadamard matrices and the separately written trellis walker."""
+    m, n, K, cb, M = 256, 512, 2, 1, 3
+    inp = synth.layer_inputs(m, n, K, M, config=93, index=0)
+    W = _walk_decode(inp["codes"], K, cb, m, n)
+    Hm = scipy.linalg.hadamard(m) / np.sqrt(m)
+    Hn = scipy.linalg.hadamard(n) / np.sqrt(n)
+    A = (Hm @ np.diag(inp["s_out"].astype(np.float64)) @ np.diag(inp["scales"].astype(np.float64)) @ W
+         @ Hn @ np.diag(inp["s_in"].astype(np.float64)))
+    y_bf = inp["x"].astype(np.float64) @ A.T
+    y = O.layer_forward_whole(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+    # differs from the blockwise layer (the rotations are not the same map)
+    yb = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+    assert np.abs(y - yb).max() > 0.1 * np.abs(yb).max()
