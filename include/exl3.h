@@ -179,6 +179,44 @@ exl3_status exl3_gemm(const uint32_t *codes, int K, int codebook, int m, int n,
                       void *workspace, size_t workspace_bytes, exl3_stream_t stream);
 
 /**
+ * QTIP's whole-vector randomized Hadamard transform ("Trellis Quantization"
+ * Part eleven: QTIP rotates whole rows and columns where EXL3 rotates
+ * 128-blocks): out[r] = binary16(H_d (signs (.) in[r]) / sqrt(d)) for each of
+ * `rows` rows, H_d the Sylvester Hadamard matrix of order d.
+ *   in, out [rows][d] halves; signs [d] halves of +-1 (required);
+ *   d a power of two, 128 <= d <= 32768, else EXL3_ERR_SHAPE.
+ * fp32 butterflies, one rounding to binary16.  Asynchronous on `stream`.
+ */
+exl3_status exl3_rht_whole(const exl3_half *in, const exl3_half *signs, exl3_half *out,
+                           int rows, int d, exl3_stream_t stream);
+
+/**
+ * Bytes of scratch for exl3_gemm_whole: exl3_gemm_workspace_bytes(m, n, M)
+ * rounded up to 256 bytes (first, so the status word is at byte 4*(m/128) as
+ * for exl3_workspace_bytes), then max(m, n) halves of unit signs, M*n halves
+ * of the input after the cross-block transform and M*m halves of the output
+ * before it (each 256-byte aligned).  Same zero-fill contract.  0 unless m and
+ * n are powers of two in [128, 32768] and M >= 1.
+ */
+size_t exl3_gemm_whole_workspace_bytes(int m, int n, int M);
+
+/**
+ * The layer with QTIP's whole-vector rotations on both sides ("Trellis
+ * Quantization" Part eleven) instead of EXL3's 128-blocks:
+ *   y = binary16(H_m (s_out (.) (scale (.) (W-hat H_n (s_in (.) x)))))
+ * with H_d / sqrt(d) over the full length.  m and n must be powers of two in
+ * [128, 32768] (EXL3_ERR_SHAPE); s_in / s_out NULL = no rotation on that side;
+ * any M >= 1.  Computed as the blockwise layer (exl3_gemm) between two
+ * transforms across the 128-blocks, since H_{128B} = H_B (x) H_128 in
+ * Sylvester order; each of the two adds one binary16 rounding of an
+ * intermediate vector.  Arguments, alignment and errors as exl3_gemm.
+ */
+exl3_status exl3_gemm_whole(const uint32_t *codes, int K, int codebook, int m, int n,
+                            const exl3_half *s_in, const exl3_half *s_out,
+                            const exl3_half *scales, int M, const exl3_half *x, exl3_half *y,
+                            void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
+/**
  * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
  * call of this shape and batch makes on the current device under the current
  * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on

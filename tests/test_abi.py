@@ -164,3 +164,26 @@ def test_gemm_prefill_workspace_and_validation(lib):
     assert call(cb=4) == 4
     assert call(codes=None) == 1
     assert call(wsb=16) == 7
+
+
+def test_whole_vector_workspace_and_validation(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    for m, n, M in ((4096, 1024, 1), (1024, 4096, 40), (128, 32768, 3)):
+        inner = a256(B.exl3_gemm_workspace_bytes(m, n, M))
+        want = inner + a256(2 * max(m, n)) + a256(2 * M * n) + a256(2 * M * m)
+        assert B.exl3_gemm_whole_workspace_bytes(m, n, M) == want
+    for m, n, M in ((384, 1024, 1), (1024, 14336, 1), (65536, 1024, 1), (64, 1024, 1), (1024, 1024, 0)):
+        assert B.exl3_gemm_whole_workspace_bytes(m, n, M) == 0
+    call = lambda **kw: lib.exl3_gemm_whole(kw.get("codes", A), kw.get("K", 2), 0, kw.get("m", 256),  # noqa: E731
+                                            kw.get("n", 512), A, A, A, kw.get("M", 1), A, A, kw.get("ws", A),
+                                            kw.get("wsb", 1 << 30), None)
+    assert call(M=0) == 5
+    assert call(m=384) == 2 and call(n=14336) == 2 and call(n=65536) == 2
+    assert call(K=9) == 3
+    assert call(codes=None) == 1
+    assert call(wsb=16) == 7 and call(ws=None) == 7
+    assert lib.exl3_rht_whole(A, A, A, 0, 1024, None) == 5
+    assert lib.exl3_rht_whole(A, A, A, 2, 1536, None) == 2
+    assert lib.exl3_rht_whole(A, A, A, 2, 65536, None) == 2
+    assert lib.exl3_rht_whole(A, None, A, 2, 1024, None) == 1
+    assert lib.exl3_rht_whole(A + 8, A, A, 2, 1024, None) == 6

@@ -1,0 +1,83 @@
+"""GPU parity of QTIP's whole-vector rotation ("Trellis Quantization" Part
+eleven: QTIP rotates whole rows and columns): the standalone transform
+exl3_rht_whole against the oracle's float64 rht_whole (one binary16 rounding
+of an fp32 computation), and the layer exl3_gemm_whole against the oracle's
+layer_forward_whole (relative L2 <= 5e-3, |err| <= 1e-2 * max|y_ref|) on every
+kernel family: warp-shuffle (M <= 2), tensor-core (3..32) and dense prefill
+(M > 32)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import exl3_oracle as O
+from trellis_decode_gemv_gb300 import binding as B
+from trellis_decode_gemv_gb300 import synth
+from tests.gpu_helpers import assert_layer_close, to_dev, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("rows,d", [(1, 128), (3, 1024), (2, 4096), (5, 16384), (1, 32768)])
+def test_rht_whole_matches_oracle(rows, d):
+    x = synth.activations(rows, d, synth.seed_for(60, d))
+    s = synth.sign_vector(d, synth.seed_for(60, d + 1))
+    ref = O.rht_whole(x.astype(np.float64), s)
+    got = B.exl3_rht_whole(to_dev(x), to_dev(s))
+    torch.cuda.synchronize()
+    g = got.float().cpu().numpy().astype(np.float64)
+    # one rounding to binary16 of an fp32 evaluation
+    assert np.all(np.abs(g - ref) <= np.abs(ref) * 2.0 ** -11 * 1.001 + 1e-5), np.max(np.abs(g - ref))
+
+
+def test_rht_whole_round_trip():
+    """H_d / sqrt(d) is an orthogonal involution: s (.) H(H(s (.) x)) = x up to
+    two binary16 roundings."""
+    d = 8192
+    x = synth.activations(2, d, synth.seed_for(61, 0))
+    s = synth.sign_vector(d, synth.seed_for(61, 1))
+    ones = torch.ones(d, dtype=torch.float16, device="cuda")
+    back = B.exl3_rht_whole(B.exl3_rht_whole(to_dev(x), to_dev(s)), ones) * to_dev(s)
+    torch.cuda.synchronize()
+    err = back.float().cpu().numpy() - x.astype(np.float32)
+    assert np.abs(err).max() < 4 * 2.0 ** -10 * np.abs(x).max()
+
+
+def _layer(inp, K, cb, m, n, s_in=True, s_out=True):
+    d = upload(inp)
+    M = inp["x"].shape[0]
+    y = torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")
+    ws = torch.zeros(B.exl3_gemm_whole_workspace_bytes(m, n, M), dtype=torch.uint8, device="cuda")
+    B.exl3_gemm_whole(d["codes"], K, cb, m, n, d["s_in"] if s_in else None, d["s_out"] if s_out else None,
+                      d["scales"], d["x"], y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.workspace_status(ws, m) == 0
+    ref = O.layer_forward_whole(inp["codes"], K, cb, m, n, inp["s_in"] if s_in else None,
+                                inp["s_out"] if s_out else None, inp["scales"], inp["x"])
+    return y, ref
+
+
+@pytest.mark.parametrize("m,n,M,K,cb", [
+    (128, 128, 1, 2, 0), (256, 512, 1, 3, 1), (1024, 4096, 1, 2, 1), (4096, 1024, 2, 4, 0),
+    (512, 256, 8, 2, 2), (1024, 1024, 17, 3, 3), (256, 1024, 40, 2, 1), (2048, 512, 300, 3, 0),
+])
+def test_gemm_whole_matches_oracle(m, n, M, K, cb):
+    inp = synth.layer_inputs(m, n, K, M, config=62, index=m + n + M)
+    y, ref = _layer(inp, K, cb, m, n)
+    assert_layer_close(y, ref, f"{m}x{n} M={M}")
+
+
+@pytest.mark.parametrize("s_in,s_out", [(False, True), (True, False), (False, False)])
+def test_gemm_whole_one_side(s_in, s_out):
+    m, n, K, cb, M = 512, 2048, 2, 1, 3
+    inp = synth.layer_inputs(m, n, K, M, config=63, index=int(s_in) + 2 * int(s_out))
+    y, ref = _layer(inp, K, cb, m, n, s_in, s_out)
+    assert_layer_close(y, ref, f"s_in={s_in} s_out={s_out}")
+
+
+def test_gemm_whole_4096_square_batch1():
+    """A Llama attention projection shape, every output checked."""
+    m = n = 4096
+    K, cb, M = 2, 1, 1
+    inp = synth.layer_inputs(m, n, K, M, config=64, index=0)
+    y, ref = _layer(inp, K, cb, m, n)
+    assert_layer_close(y, ref, "4096x4096 whole")

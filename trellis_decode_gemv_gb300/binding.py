@@ -65,6 +65,9 @@ _SIGNATURES = {
     "exl3_gemm_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
     "exl3_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_launches": ([_I, _I, _I], _I),
+    "exl3_rht_whole": ([_P, _P, _P, _I, _I, _P], _I),
+    "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
+    "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_set_path": ([_I], _I),
     "exl3_debug_stall_tensor_wait": ([_I], _I),
@@ -363,6 +366,44 @@ class Exl3LinearGroup:
 
 def exl3_gemm_workspace_bytes(m: int, n: int, M: int) -> int:
     return int(load_library().exl3_gemm_workspace_bytes(m, n, M))
+
+
+def exl3_rht_whole(x: torch.Tensor, signs: torch.Tensor, out: torch.Tensor | None = None):
+    """QTIP's whole-vector transform of each row: binary16(H_d (signs (.) x) / sqrt(d))."""
+    lib = load_library()
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    rows, d = x2.shape
+    if out is None:
+        out = torch.empty_like(x2)
+    _check(lib.exl3_rht_whole(_ptr(x2, "x", _HALF), _ptr(signs, "signs", _HALF, x.device),
+                              _ptr(out, "out", _HALF, x.device), rows, d, _stream(x.device)))
+    return out if x.dim() == 2 else out.view(-1)
+
+
+def exl3_gemm_whole_workspace_bytes(m: int, n: int, M: int) -> int:
+    return int(load_library().exl3_gemm_whole_workspace_bytes(m, n, M))
+
+
+def exl3_gemm_whole(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspace=None):
+    """The layer with whole-vector rotations (power-of-two m, n): x [M, n] -> y [M, m]."""
+    lib = load_library()
+    dev = codes.device
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, m), dtype=torch.float16, device=dev)
+    if workspace is None:
+        nbytes = exl3_gemm_whole_workspace_bytes(m, n, M)
+        if nbytes == 0:
+            raise Exl3Error(2, "invalid shape or batch for a whole-vector workspace")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib.exl3_gemm_whole(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), M, _ptr(x2, "x", _HALF, dev),
+        _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev),
+        workspace.numel(), _stream(dev)))
+    return y if x.dim() == 2 else y.view(-1)
 
 
 def exl3_gemm_launches(m: int, n: int, M: int) -> int:

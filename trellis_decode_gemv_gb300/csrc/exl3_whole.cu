@@ -1,0 +1,184 @@
+// QTIP's whole-vector rotation ("Trellis Quantization" Part eleven: QTIP
+// rotates whole rows and columns, EXL3 rotates 128-blocks).
+//
+// With Sylvester ordering H_{128 B} = H_B (x) H_128, so the whole-vector
+// transform of a power-of-two length d = 128 B is the blockwise 128-point
+// transform followed by a B-point transform across the blocks (the two
+// commute).  The layer entry point therefore wraps the blockwise layer:
+//   x' = binary16(H_B-across(s_in (.) x) / sqrt(B)),
+//   u  = blockwise layer on x' with unit input signs (its input transform then
+//        completes H_n) and the real s_out (applied before the output
+//        transform, as the definition wants),
+//   y  = binary16(H_B-across(u) / sqrt(B)) over the m outputs.
+// Each wrapper step adds one binary16 rounding of an intermediate vector.
+//
+// rht_whole_kernel: one CTA per row, the row in shared memory as fp32; an
+// optional blockwise stage (one warp per 128-block, shuffle butterflies), then
+// the butterflies across blocks at spans 128, 256, ..., d / 2.
+#include "exl3_device.cuh"
+#include "exl3_host.cuh"
+
+namespace exl3 {
+
+namespace {
+
+constexpr int kWholeThreads = 1024;
+constexpr int kWholeMax = 32768;  // fp32 row in 128 KB of shared memory
+
+__global__ void __launch_bounds__(kWholeThreads)
+    rht_whole_kernel(const __half* __restrict__ in, const __half* __restrict__ signs,
+                     __half* __restrict__ out, int d, int blockwise, float scale, __half* __restrict__ ones,
+                     int ones_len) {
+  extern __shared__ float u[];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const size_t row = blockIdx.x;
+  const __half* src = in + row * d;
+  if (blockwise) {
+    // one warp per 128-block: signs, 128-point butterflies, into shared memory
+    for (int kb = warp; kb < d / kRowBlock; kb += kWholeThreads / 32) {
+      const int col = kb * kRowBlock + 4 * lane;
+      const uint2 xr = *reinterpret_cast<const uint2*>(src + col);
+      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+      float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
+      if (signs != nullptr) {
+        const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+        const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+        const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+        v[0] *= __low2float(s01);
+        v[1] *= __high2float(s01);
+        v[2] *= __low2float(s23);
+        v[3] *= __high2float(s23);
+      }
+      fwht128_warp(v, lane);
+      *reinterpret_cast<float4*>(&u[col]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  } else {
+    for (int i = 4 * tid; i < d; i += 4 * kWholeThreads) {
+      const uint2 xr = *reinterpret_cast<const uint2*>(src + i);
+      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+      float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
+      if (signs != nullptr) {
+        const uint2 sr = *reinterpret_cast<const uint2*>(signs + i);
+        const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+        const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+        v[0] *= __low2float(s01);
+        v[1] *= __high2float(s01);
+        v[2] *= __low2float(s23);
+        v[3] *= __high2float(s23);
+      }
+      *reinterpret_cast<float4*>(&u[i]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  }
+  __syncthreads();
+  // butterflies across 128-blocks: pair (i, i + h) for every i with bit h clear
+  for (int h = kRowBlock; h < d; h <<= 1) {
+    for (int p = tid; p < d / 2; p += kWholeThreads) {
+      const int i = (p / h) * 2 * h + (p % h);
+      const float a = u[i];
+      const float b = u[i + h];
+      u[i] = a + b;
+      u[i + h] = a - b;
+    }
+    __syncthreads();
+  }
+  for (int i = 4 * tid; i < d; i += 4 * kWholeThreads) {
+    const float4 v = *reinterpret_cast<const float4*>(&u[i]);
+    const __half2 o01 = __floats2half2_rn(v.x * scale, v.y * scale);
+    const __half2 o23 = __floats2half2_rn(v.z * scale, v.w * scale);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&o01);
+    o.y = *reinterpret_cast<const uint32_t*>(&o23);
+    *reinterpret_cast<uint2*>(out + row * d + i) = o;
+  }
+  if (ones != nullptr && blockIdx.x == 0)
+    for (int i = tid; i < ones_len; i += kWholeThreads) ones[i] = __float2half_rn(1.0f);
+}
+
+bool whole_length(int d) { return d >= kRowBlock && d <= kWholeMax && (d & (d - 1)) == 0; }
+
+exl3_status launch_rht_whole(const __half* in, const __half* signs, __half* out, int rows, int d, bool blockwise,
+                             __half* ones, int ones_len, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * static_cast<size_t>(d);
+  if (cudaFuncSetAttribute(rht_whole_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(float) * kWholeMax)) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  // 1/sqrt of the transform length covered here (d, or d / 128 across blocks)
+  const double len = blockwise ? static_cast<double>(d) : static_cast<double>(d / kRowBlock);
+  const float scale = static_cast<float>(1.0 / sqrt(len));
+  rht_whole_kernel<<<rows, kWholeThreads, smem, stream>>>(in, signs, out, d, blockwise ? 1 : 0, scale, ones,
+                                                          ones_len);
+  return launch_status();
+}
+
+inline size_t whole_inner_bytes(int m, int n, int M) { return align256(exl3_gemm_workspace_bytes(m, n, M)); }
+
+}  // namespace
+
+}  // namespace exl3
+
+using namespace exl3;
+
+extern "C" exl3_status exl3_rht_whole(const exl3_half* in, const exl3_half* signs, exl3_half* out, int rows,
+                                      int d, exl3_stream_t stream) {
+  if (rows < 1) return EXL3_ERR_BATCH;
+  if (!whole_length(d)) return EXL3_ERR_SHAPE;
+  if (!in || !signs || !out) return EXL3_ERR_NULL;
+  if (!aligned16(in) || !aligned16(signs) || !aligned16(out)) return EXL3_ERR_ALIGN;
+  return launch_rht_whole(reinterpret_cast<const __half*>(in), reinterpret_cast<const __half*>(signs),
+                          reinterpret_cast<__half*>(out), rows, d, true, nullptr, 0,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exl3_gemm_whole_workspace_bytes(int m, int n, int M) {
+  if (!whole_length(m) || !whole_length(n) || M < 1) return 0;
+  const size_t inner = whole_inner_bytes(m, n, M);
+  if (inner == 0) return 0;
+  const int ones = m > n ? m : n;
+  return inner + align256(sizeof(__half) * static_cast<size_t>(ones)) +
+         align256(sizeof(__half) * static_cast<size_t>(M) * n) + align256(sizeof(__half) * static_cast<size_t>(M) * m);
+}
+
+extern "C" exl3_status exl3_gemm_whole(const uint32_t* codes, int K, int codebook, int m, int n,
+                                       const exl3_half* s_in, const exl3_half* s_out, const exl3_half* scales,
+                                       int M, const exl3_half* x, exl3_half* y, void* workspace,
+                                       size_t workspace_bytes, exl3_stream_t stream) {
+  if (M < 1) return EXL3_ERR_BATCH;
+  if (!whole_length(m) || !whole_length(n)) return EXL3_ERR_SHAPE;
+  exl3_status st = check_k_cb(K, codebook);
+  if (st != EXL3_OK) return st;
+  if (!codes || !scales || !x || !y) return EXL3_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(y) || (s_in && !aligned16(s_in)) ||
+      (s_out && !aligned16(s_out)))
+    return EXL3_ERR_ALIGN;
+  if (!workspace || workspace_bytes < exl3_gemm_whole_workspace_bytes(m, n, M)) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // [inner layer workspace | unit signs | x' | u]; the inner workspace comes
+  // first so the status word sits where exl3_workspace_bytes puts it.
+  char* ws = static_cast<char*>(workspace);
+  const size_t inner = whole_inner_bytes(m, n, M);
+  __half* ones = reinterpret_cast<__half*>(ws + inner);
+  const int ones_len = m > n ? m : n;
+  __half* xp = reinterpret_cast<__half*>(ws + inner + align256(sizeof(__half) * static_cast<size_t>(ones_len)));
+  __half* up = xp + align256(sizeof(__half) * static_cast<size_t>(M) * n) / sizeof(__half);
+  const exl3_half* x_in = x;
+  const exl3_half* signs_in = nullptr;
+  if (s_in != nullptr) {
+    if ((st = launch_rht_whole(reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(s_in), xp, M,
+                               n, false, ones, ones_len, cs)) != EXL3_OK)
+      return st;
+    x_in = reinterpret_cast<const exl3_half*>(xp);
+    signs_in = reinterpret_cast<const exl3_half*>(ones);
+  }
+  exl3_half* y_inner = s_out != nullptr ? reinterpret_cast<exl3_half*>(up) : y;
+  if ((st = exl3_gemm(codes, K, codebook, m, n, signs_in, s_out, scales, M, x_in, y_inner, workspace, inner,
+                      stream)) != EXL3_OK)
+    return st;
+  if (s_out != nullptr)
+    return launch_rht_whole(up, nullptr, reinterpret_cast<__half*>(y), M, m, false, nullptr, 0, cs);
+  return EXL3_OK;
+}
