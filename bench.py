@@ -106,6 +106,12 @@ def workload(name: str, batch: int):
     if name == "mixed":
         return ("80-layer mixed-width stack (attn 8192x8192 K4; MLP 28672x8192 / 8192x28672, "
                 "K in {2,3,4}, 2.90 bpw body) + lm_head 128256x8192 K6, 3INST, batch 1"), 4, synth.mixed_stack(), 1
+    if name == "whole":
+        # QTIP's whole-vector rotations need power-of-two dimensions: the
+        # attention projections of a Llama-3-70B-shaped model, 8 layers
+        # resident (1.21 G weights, 302 MB of codes at K=2, more than L2)
+        return (f"Llama-3-70B attention shapes (q/o 8192x8192, k/v 1024x8192) x 8 layers, K=2, 3INST, "
+                f"whole-vector rotations on both sides, batch {batch}"), 7, synth.whole_attention_stack(), batch
     if name == "sweep":
         # four distinct instances of each shape (176 MB of codes, more than L2)
         return (f"14336x4096 and 4096x14336, K=3, 1MAD, batch {batch}, 4 distinct instances of each"), 3, \
@@ -257,11 +263,12 @@ class ClockSampler:
 # CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None):
+def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None, whole=False):
     """Time only the oracle (input generation excluded) on `blocks` 128-row
     output blocks of each selected GEMV.  With target_s, a one-block pass
     calibrates and a second pass takes as many blocks as fill about target_s
-    seconds; both passes count."""
+    seconds; both passes count.  With whole, the whole-vector layer of each
+    selected GEMV instead (its output transform mixes every row)."""
     from oracle import exl3_oracle as O
     inputs = []
     for i in sel:
@@ -272,6 +279,11 @@ def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None):
         w = 0
         t0 = time.perf_counter()
         for inp, (name, m, n, K, cb), i in inputs:
+            if whole:
+                O.layer_forward_whole(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"],
+                                      inp["x"])
+                w += m * n * M
+                continue
             nb = m // 128
             rbs = sorted({(i + first + 7 * j) % nb for j in range(nblk)})
             O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"],
@@ -280,7 +292,7 @@ def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None):
         return w, time.perf_counter() - t0
 
     weights, dt = one_pass(blocks, 0)
-    if target_s is not None and dt < target_s:
+    if target_s is not None and dt < target_s and not whole:
         more = max(1, int((target_s - dt) / dt))
         w2, dt2 = one_pass(more, 1)
         weights, dt = weights + w2, dt + dt2
@@ -321,18 +333,25 @@ def run_reference(args):
     if rank != 0:
         return 0
     desc, cfg, gemvs, M = workload(args.workload, args.batch)
-    per_step = min(6, len(gemvs))
+    whole = args.workload == "whole"
+    per_step = 1 if whole else min(6, len(gemvs))
+    # the whole-vector oracle runs full layers: take the smallest GEMVs
+    pool = [i for i, g in enumerate(gemvs) if g[1] * g[2] == min(h[1] * h[2] for h in gemvs)] if whole \
+        else list(range(len(gemvs)))
     for s in range(args.warmup):
-        oracle_sample_timed(gemvs, M, cfg, [(s * per_step + i) % len(gemvs) for i in range(per_step)])
+        oracle_sample_timed(gemvs, M, cfg, [pool[(s * per_step + i) % len(pool)] for i in range(per_step)],
+                            whole=whole)
     tw, tt = 0, 0.0
     for s in range(args.steps):
-        sel = [((args.warmup + s) * per_step + i) % len(gemvs) for i in range(per_step)]
-        w, dt = oracle_sample_timed(gemvs, M, cfg, sel)
+        sel = [pool[((args.warmup + s) * per_step + i) % len(pool)] for i in range(per_step)]
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, whole=whole)
         tw += w
         tt += dt
     value = tw / tt
     sample = (f"per step: one 128-row output block of {per_step} of the {len(gemvs)} GEMVs "
-              f"(round-robin), oracle layer forward (decode + float64 product + transforms)")
+              f"(round-robin), oracle layer forward (decode + float64 product + transforms)") if not whole else \
+        (f"per step: one of the smallest GEMVs of the workload in full (round-robin), oracle whole-vector "
+         f"layer forward")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "weights/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -380,7 +399,9 @@ def run_ours(args):
     Y = torch.empty(total_m, dtype=torch.float16, device=dev)
     calls = []
     xo = yo = 0
-    ws_bytes = max(B.exl3_gemm_workspace_bytes(m, n, M) for _, m, n, _, _ in gemvs)
+    whole = args.workload == "whole"
+    ws_of = B.exl3_gemm_whole_workspace_bytes if whole else B.exl3_gemm_workspace_bytes
+    ws_bytes = max(ws_of(m, n, M) for _, m, n, _, _ in gemvs)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     packed = 0
     for i, (name, m, n, K, cb) in enumerate(gemvs):
@@ -401,7 +422,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
 
     groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
-                            grouped=not args.ungrouped)
+                            grouped=not (args.ungrouped or whole))
     gws = max([B.exl3_group_workspace_bytes([(calls[i]["m"], calls[i]["n"]) for i in g], M)
                for g in groups if len(g) > 1] + [0])
     if gws > ws.numel():
@@ -410,7 +431,7 @@ def run_ours(args):
     def run_group(g):
         if len(g) == 1:
             c = calls[g[0]]
-            fn = B.exl3_gemm if M > 32 else B.exl3_gemm_small
+            fn = B.exl3_gemm_whole if whole else B.exl3_gemm if M > 32 else B.exl3_gemm_small
             fn(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                c["scales"], c["x"], y=c["y"], workspace=ws)
         else:
@@ -559,7 +580,12 @@ def run_ours(args):
     # holds its layers), one call per group; x and y are the bound tensors.
     layer_objs = []
     for g in groups:
-        if len(g) == 1:
+        if whole:  # no layer object for the whole-vector variant: the public call itself
+            c = calls[g[0]]
+            layer_objs.append(lambda c=c: B.exl3_gemm_whole(
+                c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
+                y=c["y"], workspace=ws))
+        elif len(g) == 1:
             c = calls[g[0]]
             lin = B.Exl3Linear(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                                c["scales"], max_batch=M)
@@ -602,10 +628,14 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nsel = len(gemvs) if args.workload == "llama8b" else min(len(gemvs), 8)
         sel = list(range(nsel)) if nsel == len(gemvs) else list(range(0, len(gemvs), max(1, len(gemvs) // nsel)))[:nsel]
-        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, target_s=12.0)
+        if whole:  # full layers: the three smallest (k/v) GEMVs
+            sel = sorted(range(len(gemvs)), key=lambda i: gemvs[i][1] * gemvs[i][2])[:3]
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, target_s=12.0, whole=whole)
         cpu = {"value": w / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
-               "sample": f"128-row output blocks of each of {len(sel)} GEMVs of the workload "
-                         f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward"}
+               "sample": (f"{len(sel)} whole GEMVs (the smallest of the workload; {w / 1e6:.1f} M weights, "
+                          f"{dt:.1f} s), oracle whole-vector layer forward") if whole else
+                         (f"128-row output blocks of each of {len(sel)} GEMVs of the workload "
+                          f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward")}
 
     if rank == 0:
         line = {
@@ -617,7 +647,8 @@ def run_ours(args):
                        "weights_per_step": weights_step, "packed_bytes_per_step": packed,
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path,
-                       "calls": "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
+                       "calls": "one exl3_gemm_whole call per GEMV" if whole else
+                       "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
                        else "one exl3_gemm_small call per GEMV"},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
             "macs_per_s": value * M,
@@ -625,6 +656,7 @@ def run_ours(args):
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * sum(
+                (B.exl3_gemm_launches(calls[g[0]]["m"], calls[g[0]]["n"], M) + 2) if whole else
                 kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) for g in groups),
             "clocks": clk,
         }
@@ -641,7 +673,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b",
-                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill"])
+                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill",
+                             "whole"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",

@@ -115,6 +115,13 @@ def llama70b_stack(layers: int = 32):
             for l in range(layers) for name, m, n in LLAMA70B_SHAPES]
 
 
+def whole_attention_stack(layers: int = 8):
+    """Llama-3-70B attention projections (power-of-two shapes, as QTIP's
+    whole-vector rotations need), K = 2, 3INST, all resident."""
+    return [(f"L{l}.{name}", m, n, 2, CB_3INST)
+            for l in range(layers) for name, m, n in LLAMA70B_SHAPES if name in ("q", "k", "v", "o")]
+
+
 BATCH_SWEEP = [1, 2, 4, 8, 16, 32]
 BATCH_SWEEP_SHAPES = [("gate", 14336, 4096, 3, CB_1MAD), ("down", 4096, 14336, 3, CB_1MAD)]
 
