@@ -23,7 +23,11 @@ What it follows:
   onto it.
 
 Everything is numpy and literal; the cost of a path is the sum of squared
-differences between the decoded values and the target sequence.
+differences between the decoded values and the target sequence.  The path
+costs run in float64 by default; a float32 mode takes every argmin decision on
+binary32 costs evaluated in a stated order (``viterbi``), so that another
+binary32 implementation of the same search can be compared with it bit for
+bit (its chosen words and its final cost).
 """
 from __future__ import annotations
 
@@ -33,21 +37,28 @@ from . import exl3_oracle as O
 
 
 def viterbi(values: np.ndarray, target: np.ndarray, K: int, L: int, start: int | None = None,
-            forced: dict | None = None):
+            forced: dict | None = None, dtype=np.float64):
     """Cheapest state path of the L-bit, K-bit-shift trellis for `target`.
 
-    values  float64 [2**L]: the decoded value of every state;
-    target  float64 [T]: the sequence to quantize;
+    values  [2**L]: the decoded value of every state;
+    target  [T]: the sequence to quantize;
     start   None (any first state) or the required first state;
     forced  {t: (mask, bits)}: at step t >= 1 the K appended bits b must
-            satisfy b & mask == bits.
+            satisfy b & mask == bits;
+    dtype   the arithmetic of the path costs: float64, or float32, where every
+            difference, square and sum is one binary32 rounding, in this
+            order: cost_t(s) = best_{t-1}(s >> K) + (v(s) - x_t)^2.  Ties go to
+            the smallest predecessor index h and, at the end, the smallest
+            state.
     Returns (states int64 [T], cost).
     """
+    values = np.asarray(values, dtype=dtype)
+    target = np.asarray(target, dtype=dtype)
     T = len(target)
     nst = 1 << L
     nb = 1 << K
     low = nst >> K
-    inf = np.inf
+    inf = dtype(np.inf)
     cost = (values - target[0]) ** 2
     if start is not None:
         keep = np.zeros(nst, dtype=bool)
@@ -80,10 +91,10 @@ def _stream_bit_of_start(start: int, j: int, L: int) -> int:
     return (start >> (L - 1 - j)) & 1
 
 
-def encode_tile(target: np.ndarray, values: np.ndarray, K: int, L: int = O.L):
+def encode_tile(target: np.ndarray, values: np.ndarray, K: int, L: int = O.L, dtype=np.float64):
     """Tail-biting encoding of one 256-step sequence (one 16x16 tile), by the
-    two-pass approximation of Part eight.  Returns (words uint32 [8K],
-    states int64 [256], mse)."""
+    two-pass approximation of Part eight, with path costs in `dtype` (see
+    ``viterbi``).  Returns (words uint32 [8K], states int64 [256], mse)."""
     T = len(target)
     nbits = T * K
     # Pass 1: the sequence rotated by half its length, free start and end; the
@@ -91,7 +102,7 @@ def encode_tile(target: np.ndarray, values: np.ndarray, K: int, L: int = O.L):
     # wrapping, at the end) of the original sequence.
     half = T // 2
     rotated = np.roll(target, -half)
-    states1, _ = viterbi(values, rotated, K, L)
+    states1, _ = viterbi(values, rotated, K, L, dtype=dtype)
     s_star = int(states1[half])
     # Pass 2: the original sequence, starting with s_star; the bits appended at
     # steps whose new bits lie past the end of the circular stream must repeat
@@ -108,7 +119,7 @@ def encode_tile(target: np.ndarray, values: np.ndarray, K: int, L: int = O.L):
                 bits |= _stream_bit_of_start(s_star, j - nbits, L) << shift
         if mask:
             forced[t] = (mask, bits)
-    states, cost = viterbi(values, target, K, L, start=s_star, forced=forced)
+    states, cost = viterbi(values, target, K, L, start=s_star, forced=forced, dtype=dtype)
     # The stream: the first window, then the K bits appended at each step.
     stream = np.zeros(nbits, dtype=np.uint8)
     for j in range(min(L, nbits)):

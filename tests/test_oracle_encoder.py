@@ -36,22 +36,26 @@ def _brute_force(values, target, K, L, start=None, forced=None):
     return best
 
 
+@pytest.mark.parametrize("dtype,rel", [(np.float64, 1e-12), (np.float32, 1e-5)])
 @pytest.mark.parametrize("K,L,T", [(1, 4, 9), (2, 4, 6), (1, 5, 8)])
-def test_viterbi_matches_brute_force(K, L, T):
+def test_viterbi_matches_brute_force(K, L, T, dtype, rel):
     rng = np.random.default_rng(100 + 10 * K + L)
     values = rng.normal(size=1 << L)
     target = rng.normal(size=T)
-    states, cost = E.viterbi(values, target, K, L)
-    assert cost == pytest.approx(_brute_force(values, target, K, L), rel=1e-12)
+    if dtype == np.float32:  # the brute force sees the same binary32 inputs
+        values = values.astype(np.float32).astype(np.float64)
+        target = target.astype(np.float32).astype(np.float64)
+    states, cost = E.viterbi(values, target, K, L, dtype=dtype)
+    assert cost == pytest.approx(_brute_force(values, target, K, L), rel=rel)
     # the returned path is a legal shift-register path with that cost
     for t in range(1, T):
         assert states[t] >> K == states[t - 1] & ((1 << (L - K)) - 1)
-    assert np.sum((values[states] - target) ** 2) == pytest.approx(cost, rel=1e-12)
+    assert np.sum((values[states] - target) ** 2) == pytest.approx(cost, rel=rel)
     # fixed start and forced appended bits
     forced = {T - 1: ((1 << K) - 1, 1), T - 2: (1, 0)}
-    states, cost = E.viterbi(values, target, K, L, start=3, forced=forced)
+    states, cost = E.viterbi(values, target, K, L, start=3, forced=forced, dtype=dtype)
     assert states[0] == 3
-    assert cost == pytest.approx(_brute_force(values, target, K, L, 3, forced), rel=1e-12)
+    assert cost == pytest.approx(_brute_force(values, target, K, L, 3, forced), rel=rel)
 
 
 @pytest.mark.parametrize("K,cb", [(2, O.CB_3INST), (3, O.CB_1MAD), (1, O.CB_3INST)])
@@ -102,3 +106,37 @@ def test_computed_codes_match_a_random_table(gaussian_tiles):
     for cb in (O.CB_3INST, O.CB_1MAD, O.CB_MCG, O.CB_MUL1):
         mse = E.trellis_mse(E.codebook_values(cb), gaussian_tiles, 2)
         assert abs(mse - ref) < 0.1 * ref, (cb, mse, ref)
+
+
+def test_binary32_costs_follow_the_stated_rounding():
+    """In float32 mode every path cost is the binary32 evaluation, in order, of
+    best + (v - x)^2: recomputed here along the returned path with explicit
+    float32 scalars, it matches bit for bit."""
+    rng = np.random.default_rng(31)
+    K, L, T = 2, 6, 12
+    values = rng.normal(size=1 << L).astype(np.float32)
+    target = rng.normal(size=T).astype(np.float32)
+    states, cost = E.viterbi(values, target, K, L, dtype=np.float32)
+    acc = np.float32(0)
+    for t in range(T):
+        d = np.float32(values[states[t]] - target[t])
+        acc = np.float32(acc + np.float32(d * d)) if t else np.float32(d * d)
+    assert np.float32(cost) == acc
+
+
+@pytest.mark.parametrize("K,cb", [(2, O.CB_3INST), (1, O.CB_1MAD)])
+def test_binary32_encoding_is_a_tail_biting_codeword(K, cb):
+    """The float32 two-pass encoder on raw code values and a target in code
+    units: its words decode to its path, and the path's binary32 cost is the
+    returned one."""
+    rng = np.random.default_rng(41 + K)
+    raw = O.decode_states(np.arange(1 << O.L, dtype=np.uint32), cb).astype(np.float32)
+    sigma = np.sqrt(np.mean(raw.astype(np.float64) ** 2))
+    target = (rng.normal(size=O.STEPS) * sigma).astype(np.float32)
+    words, states, mse = E.encode_tile(target, raw, K, dtype=np.float32)
+    assert np.array_equal(O.tile_states(words, K).astype(np.int64), states)
+    d = raw[states] - target
+    assert np.sum(d.astype(np.float64) ** 2) / O.STEPS == pytest.approx(mse, rel=1e-5)
+    # same quality as the float64 encoder on the normalized problem
+    _, _, mse64 = E.encode_tile(target / sigma, raw / sigma, K)
+    assert mse / sigma ** 2 == pytest.approx(mse64, rel=0.05)
