@@ -217,6 +217,36 @@ exl3_status exl3_gemm_whole(const uint32_t *codes, int K, int codebook, int m, i
                             void *workspace, size_t workspace_bytes, exl3_stream_t stream);
 
 /**
+ * Bytes of workspace for exl3_encode_tiles to encode `ctas` tiles at a time:
+ * 256 * 2^(16-K) bytes per tile in flight (the predecessor chosen for every
+ * group of states at every step).  0 for K outside 1..8 or ctas < 1.
+ */
+size_t exl3_encode_workspace_bytes(int K, int ctas);
+
+/**
+ * Tail-biting Viterbi encoding of `tiles` 256-step sequences ("Trellis
+ * Quantization" Part seven, the Viterbi search; Part eight, the bitshift
+ * trellis with a 16-bit window moving K bits per step and the two-pass
+ * tail-biting approximation).  For each tile: the stream of 256*K bits, as
+ * 8K uint32 words MSB first (the layout exl3_decode_tiles reads), whose
+ * states minimise sum_t (v(state_t) - target_t)^2, v the codebook's binary16
+ * value of a state, and that cost.
+ *   target [tiles][256] float, in code units (to quantize a unit-variance
+ *          source, multiply it by the code's rms value);
+ *   words  [tiles][8K] uint32 (out); cost [tiles] float (out).
+ * Path costs are binary32, each evaluated as best + (v - x)^2 in that order;
+ * the smallest predecessor wins ties, and the smallest state at the end.
+ * The workspace holds one slot of exl3_encode_workspace_bytes(K, 1) bytes per
+ * tile in flight; as many tiles run at once as slots fit, up to one per SM.
+ * Errors: EXL3_ERR_SHAPE (tiles < 1), EXL3_ERR_K, EXL3_ERR_CODEBOOK,
+ * EXL3_ERR_NULL, EXL3_ERR_ALIGN (target or words not 16-byte aligned),
+ * EXL3_ERR_WORKSPACE (smaller than one slot).  Asynchronous on `stream`.
+ */
+exl3_status exl3_encode_tiles(const float *target, int tiles, int K, int codebook,
+                              uint32_t *words, float *cost, void *workspace,
+                              size_t workspace_bytes, exl3_stream_t stream);
+
+/**
  * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
  * call of this shape and batch makes on the current device under the current
  * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on

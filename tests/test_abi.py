@@ -187,3 +187,20 @@ def test_whole_vector_workspace_and_validation(lib):
     assert lib.exl3_rht_whole(A, A, A, 2, 65536, None) == 2
     assert lib.exl3_rht_whole(A, None, A, 2, 1024, None) == 1
     assert lib.exl3_rht_whole(A + 8, A, A, 2, 1024, None) == 6
+
+
+def test_encoder_workspace_and_validation(lib):
+    for K in range(1, 9):
+        assert B.exl3_encode_workspace_bytes(K, 3) == 3 * 256 * (1 << (16 - K))
+    assert B.exl3_encode_workspace_bytes(0, 1) == 0 and B.exl3_encode_workspace_bytes(9, 1) == 0
+    assert B.exl3_encode_workspace_bytes(2, 0) == 0
+    slot = B.exl3_encode_workspace_bytes(2, 1)
+    call = lambda **kw: lib.exl3_encode_tiles(kw.get("t", A), kw.get("tiles", 4), kw.get("K", 2),  # noqa: E731
+                                              kw.get("cb", 0), kw.get("w", A), kw.get("c", A), kw.get("ws", A),
+                                              kw.get("wsb", slot), None)
+    assert call(tiles=0) == 2
+    assert call(K=0) == 3 and call(K=9) == 3
+    assert call(cb=4) == 4
+    assert call(t=None) == 1 and call(w=None) == 1 and call(c=None) == 1
+    assert call(t=A + 4) == 6 and call(w=A + 8) == 6
+    assert call(wsb=slot - 1) == 7 and call(ws=None) == 7

@@ -66,6 +66,8 @@ _SIGNATURES = {
     "exl3_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_launches": ([_I, _I, _I], _I),
     "exl3_rht_whole": ([_P, _P, _P, _I, _I, _P], _I),
+    "exl3_encode_workspace_bytes": ([_I, _I], _SZ),
+    "exl3_encode_tiles": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
@@ -404,6 +406,30 @@ def exl3_gemm_whole(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, wo
         _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev),
         workspace.numel(), _stream(dev)))
     return y if x.dim() == 2 else y.view(-1)
+
+
+def exl3_encode_workspace_bytes(K: int, ctas: int) -> int:
+    return int(load_library().exl3_encode_workspace_bytes(K, ctas))
+
+
+def exl3_encode_tiles(target: torch.Tensor, K: int, codebook: int, words=None, cost=None, workspace=None):
+    """Tail-biting Viterbi encoding of target [tiles, 256] (float32, code units):
+    returns (words [tiles, 8K] int32 storage of uint32, cost [tiles] float32)."""
+    lib = load_library()
+    dev = target.device
+    tiles = target.shape[0]
+    if words is None:
+        words = torch.empty((tiles, 8 * K), dtype=torch.int32, device=dev)
+    if cost is None:
+        cost = torch.empty(tiles, dtype=torch.float32, device=dev)
+    if workspace is None:
+        ctas = min(tiles, torch.cuda.get_device_properties(dev).multi_processor_count)
+        workspace = torch.empty(exl3_encode_workspace_bytes(K, ctas), dtype=torch.uint8, device=dev)
+    _check(lib.exl3_encode_tiles(_ptr(target, "target", (torch.float32,)), tiles, K, codebook,
+                                 _ptr(words, "words", _WORDS, dev), _ptr(cost, "cost", (torch.float32,), dev),
+                                 _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
+                                 _stream(dev)))
+    return words, cost
 
 
 def exl3_gemm_launches(m: int, n: int, M: int) -> int:
