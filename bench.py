@@ -666,6 +666,146 @@ def run_ours(args):
     return 0
 
 
+ENCODE_METRIC = "tail-biting Viterbi encode, weights (trellis steps) encoded per second"
+ENCODE_TILES = 1216  # 8 tiles per SM of a GB300
+
+
+def encode_inputs(K: int, cb: int, tiles: int):
+    """Unit-Gaussian sequences scaled by the code's rms value (code units),
+    binary32 [tiles][256], and that rms value."""
+    from oracle import exl3_oracle as O  # the codebook's rms value only: an input of both sides
+    raw = O.decode_states(np.arange(1 << 16, dtype=np.uint32), cb).astype(np.float64)
+    sigma = float(np.sqrt(np.mean(raw ** 2)))
+    g = synth.activations(tiles, 256, synth.seed_for(8, 0)).astype(np.float64)
+    return (g * sigma).astype(np.float32), sigma
+
+
+def encode_oracle_timed(target, K, cb, target_s):
+    """The oracle's binary32 encoder on whole tiles until about target_s
+    seconds; returns (tiles, seconds)."""
+    from oracle import exl3_encoder as E
+    from oracle import exl3_oracle as O
+    raw = O.decode_states(np.arange(1 << 16, dtype=np.uint32), cb).astype(np.float32)
+    n, t0 = 0, time.perf_counter()
+    while n < len(target):
+        E.encode_tile(target[n], raw, K, dtype=np.float32)
+        n += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    return n, time.perf_counter() - t0
+
+
+def run_encode(args):
+    """The encoder leg: every step encodes ENCODE_TILES tiles of a unit
+    Gaussian source (K = 2, 3INST) with exl3_encode_tiles."""
+    K, cb = 2, 0
+    rank = int(os.environ.get("RANK", "0"))
+    desc = (f"tail-biting two-pass Viterbi encode of {ENCODE_TILES} tiles (256 steps each) of a unit "
+            f"Gaussian source, K={K}, 3INST, binary32 path costs")
+    target, sigma = encode_inputs(K, cb, ENCODE_TILES)
+    weights_step = ENCODE_TILES * 256
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        tw, tt = 0, 0.0
+        steps = max(1, min(args.steps, 20))  # a bounded sample: about a minute in all
+        for _ in range(steps):
+            n, dt = encode_oracle_timed(target, K, cb, target_s=60.0 / steps)
+            tw += n * 256
+            tt += dt
+        value = tw / tt
+        print(json.dumps({
+            "impl": "reference", "metric": ENCODE_METRIC, "value": value, "unit": "weights/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tt / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": {"workload": desc},
+            "cpu_baseline": {"value": value, "unit": "weights/s", "cores": 1, "kind": "oracle",
+                             "sample": "whole tiles of the workload per step, oracle binary32 encoder"},
+            "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return 0
+    import torch
+    from trellis_decode_gemv_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_gbs, sm_max_mhz, _, peak_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    t_dev = torch.from_numpy(target).to(dev)
+    words = torch.empty((ENCODE_TILES, 8 * K), dtype=torch.int32, device=dev)
+    cost = torch.empty(ENCODE_TILES, dtype=torch.float32, device=dev)
+    ws = torch.empty(B.exl3_encode_workspace_bytes(K, sms), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    steps = max(1, min(args.steps, 50))
+
+    def step():
+        B.exl3_encode_tiles(t_dev, K, cb, words=words, cost=cost, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(getattr(props, "pci_bus_id", None) if isinstance(getattr(props, "pci_bus_id", None), str)
+                          else None)
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms_step = ev0.elapsed_time(ev1) / steps
+    value = weights_step / (ms_step / 1e3)
+    mse = float(cost.double().sum()) / weights_step / sigma ** 2
+    # FP32 candidate work: 2 passes x 256 steps x 2^16 states x (sub, mul, add, compare)
+    ops_step = ENCODE_TILES * 2 * 256 * (1 << 16) * 4
+    p_fp32 = sms * 128 * sm_max_mhz * 1e6
+    achieved = ops_step / (ms_step / 1e3)
+    # end to end: pinned host target in, words and costs out, every step
+    th = torch.from_numpy(target).pin_memory()
+    wh = torch.empty_like(words, device="cpu").pin_memory()
+    ch = torch.empty_like(cost, device="cpu").pin_memory()
+    e2e_steps = max(3, min(steps, 20))
+    with torch.cuda.stream(stream):
+        t_dev.copy_(th, non_blocking=True)
+        step()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            t_dev.copy_(th, non_blocking=True)
+            step()
+            wh.copy_(words, non_blocking=True)
+            ch.copy_(cost, non_blocking=True)
+            stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+    cpu = None
+    if not args.no_cpu_baseline:
+        n, dt = encode_oracle_timed(target, K, cb, target_s=12.0)
+        cpu = {"value": n * 256 / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole tiles of the workload ({dt:.1f} s), oracle binary32 encoder"}
+    print(json.dumps({
+        "metric": ENCODE_METRIC, "value": value, "unit": "weights/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "tiles": ENCODE_TILES,
+                   "l2": "each step writes 4 MB of predecessor choices per tile (4.9 GB), far more than L2"},
+        "mse_unit_variance": mse,
+        "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": p_fp32 / 1e12, "unit": "Tops/s",
+                     "frac": achieved / p_fp32, "traffic": None,
+                     "peak_source": f"FP32: {sms} SMs x 128 lanes/clk x {sm_max_mhz:.0f} MHz (derived)",
+                     "kernel": "encode_kernel (one CTA per tile, binary32 path costs)",
+                     "ops_note": "2 passes x 256 steps x 65536 states x 4 ops (sub, mul, add, compare) per tile"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": weights_step * e2e_steps / t_e2e, "unit": "weights/s",
+                "h2d_bytes_per_step": target.nbytes, "d2h_bytes_per_step": words.numel() * 4 + cost.numel() * 4},
+        "clocks": clk, "gpu_launches": steps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -674,7 +814,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill",
-                             "whole"])
+                             "whole", "encode"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",
@@ -684,6 +824,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "encode":
+        return run_encode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

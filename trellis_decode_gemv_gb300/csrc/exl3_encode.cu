@@ -69,6 +69,108 @@ __device__ __forceinline__ float value_of(const __half* vcache, uint32_t s) {
   }
 }
 
+// Minimum over the 2^K predecessors of one group g at one step: the path
+// costs best(h * kQStride + (g >> K)) + (v(s) - x)^2, s = h * kLow + g, with the
+// appended bits of s checked against (fm, fb) when Forced.
+template <int K, int CB, bool First, bool Forced>
+__device__ __forceinline__ float group_min(const float* best, const __half* vcache, int g, float xp, int start,
+                                           uint32_t fm, uint32_t fb, int& bh) {
+  using C = Cfg<K>;
+  const float inf = __int_as_float(0x7f800000);
+  float bc = inf;
+  bh = 0;
+#pragma unroll 4
+  for (int h = 0; h < C::kNb; ++h) {
+    const uint32_t s = static_cast<uint32_t>(h) * C::kLow + g;
+    float base;
+    if constexpr (First)
+      base = (start < 0 || s == static_cast<uint32_t>(start)) ? 0.0f : inf;
+    else
+      base = best[h * C::kQStride + (g >> K)];
+    const float d = __fsub_rn(value_of<K, CB>(vcache, s), xp);
+    float c = __fadd_rn(base, __fmul_rn(d, d));
+    if constexpr (Forced) {
+      if ((s & fm) != fb) c = inf;
+    }
+    if (c < bc) {
+      bc = c;
+      bh = h;
+    }
+  }
+  return bc;
+}
+
+// Small K: one thread takes a whole butterfly q (the 2^K predecessor groups
+// h * kQStride + q feed exactly the 2^K successor groups q * 2^K + b), so each
+// predecessor minimum is read once for 2^K outputs and the values of the 2^K
+// consecutive states h * kLow + q * 2^K + b come in one shared-memory load.
+template <int K>
+struct ByQ {
+  static constexpr bool kOn = K <= 3;
+  static constexpr int kQ = 1 << (16 - 2 * K);  // butterflies
+  static constexpr int kPerThread = kQ >= kThreads ? kQ / kThreads : 1;
+};
+
+template <int K, int CB, bool First, bool Forced>
+__device__ __forceinline__ void butterfly(const float* best, const __half* vcache, int q, float xp, int start,
+                                          uint32_t fm, uint32_t fb, float (&oc)[1 << K], uint64_t& packed_bh) {
+  using C = Cfg<K>;
+  constexpr int NB = C::kNb;
+  const float inf = __int_as_float(0x7f800000);
+  int bh[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    oc[b] = inf;
+    bh[b] = 0;
+  }
+#pragma unroll
+  for (int h = 0; h < NB; ++h) {
+    const uint32_t s0 = static_cast<uint32_t>(h) * C::kLow + static_cast<uint32_t>(q) * NB;
+    float base = First ? 0.0f : best[h * C::kQStride + q];
+    float v[NB];
+    if constexpr (C::kCache && NB == 4) {
+      const uint2 r = *reinterpret_cast<const uint2*>(vcache + s0);
+      const __half2 a = *reinterpret_cast<const __half2*>(&r.x);
+      const __half2 c = *reinterpret_cast<const __half2*>(&r.y);
+      v[0] = __low2float(a);
+      v[1] = __high2float(a);
+      v[2] = __low2float(c);
+      v[3] = __high2float(c);
+    } else if constexpr (C::kCache && NB == 8) {
+      const uint4 r = *reinterpret_cast<const uint4*>(vcache + s0);
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 a = *reinterpret_cast<const __half2*>(&w[i]);
+        v[2 * i] = __low2float(a);
+        v[2 * i + 1] = __high2float(a);
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) v[b] = value_of<K, CB>(vcache, s0 + b);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const uint32_t s = s0 + b;
+      float bs = base;
+      if constexpr (First) bs = (start < 0 || s == static_cast<uint32_t>(start)) ? 0.0f : inf;
+      const float d = __fsub_rn(v[b], xp);
+      float c = __fadd_rn(bs, __fmul_rn(d, d));
+      if constexpr (Forced) {
+        if ((s & fm) != fb) c = inf;
+      }
+      if (c < oc[b]) {
+        oc[b] = c;
+        bh[b] = h;
+      }
+    }
+  }
+  static_assert(NB <= 8, "one byte per choice, at most eight in 64 bits");
+  packed_bh = 0;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) packed_bh |= static_cast<uint64_t>(bh[b]) << (8 * b);
+}
+
 // One Viterbi pass over the tile's 256 steps.  rotated: x_t = target[(t + 128)
 // % 256]; start < 0: any first state; forced: the pass-two constraints in
 // sh.fmask / sh.fbits.  Leaves the cheapest final state and its cost in
@@ -84,30 +186,53 @@ __device__ void viterbi_pass(EncShared& sh, float* best, const __half* vcache, u
     const float xp = sh.x[rotated ? (tp + kSteps / 2) & (kSteps - 1) : tp];
     const uint32_t fm = forced ? sh.fmask[tp] : 0u;
     const uint32_t fb = forced ? sh.fbits[tp] : 0u;
+    if constexpr (ByQ<K>::kOn) {
+      constexpr int NB = C::kNb;
+      float oc[ByQ<K>::kPerThread][NB];
+#pragma unroll
+      for (int j = 0; j < ByQ<K>::kPerThread; ++j) {
+        const int q = tid + j * kThreads;
+        uint64_t pk;
+        if (tp == 0)
+          butterfly<K, CB, true, false>(best, vcache, q, xp, start, fm, fb, oc[j], pk);
+        else if (fm != 0u)
+          butterfly<K, CB, false, true>(best, vcache, q, xp, start, fm, fb, oc[j], pk);
+        else
+          butterfly<K, CB, false, false>(best, vcache, q, xp, start, fm, fb, oc[j], pk);
+        // the 2^K predecessor choices of groups q * 2^K .. + 2^K - 1, one byte each
+        uint8_t* bp = back + static_cast<size_t>(t) * C::kLow + static_cast<size_t>(q) * NB;
+        if constexpr (NB == 2) {
+          *reinterpret_cast<uint16_t*>(bp) = static_cast<uint16_t>(pk);
+        } else if constexpr (NB == 4) {
+          *reinterpret_cast<uint32_t*>(bp) = static_cast<uint32_t>(pk);
+        } else {
+          *reinterpret_cast<uint64_t*>(bp) = pk;
+        }
+      }
+      __syncthreads();  // every read of best for this step is done
+#pragma unroll
+      for (int j = 0; j < ByQ<K>::kPerThread; ++j) {
+        const int q = tid + j * kThreads;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) best[q * NB + b] = oc[j][b];
+      }
+      __syncthreads();
+    } else {
     float out[C::kPer];
 #pragma unroll
     for (int j = 0; j < C::kPer; ++j) {
       const int g = tid + j * kThreads;
       out[j] = inf;
       if (g < C::kLow) {
-        float bc = inf;
-        int bh = 0;
-        for (int h = 0; h < C::kNb; ++h) {
-          const uint32_t s = static_cast<uint32_t>(h) * C::kLow + g;
-          float base;
-          if (tp == 0)
-            base = (start < 0 || s == static_cast<uint32_t>(start)) ? 0.0f : inf;
-          else
-            base = best[h * C::kQStride + (g >> K)];
-          const float d = __fsub_rn(value_of<K, CB>(vcache, s), xp);
-          float c = __fadd_rn(base, __fmul_rn(d, d));
-          if ((s & fm) != fb) c = inf;
-          if (c < bc) {
-            bc = c;
-            bh = h;
-          }
-        }
-        out[j] = bc;
+        int bh;
+        // the first step and the forced steps (the last few of pass two) are
+        // uniform branches; the common step checks nothing
+        if (tp == 0)
+          out[j] = group_min<K, CB, true, false>(best, vcache, g, xp, start, fm, fb, bh);
+        else if (fm != 0u)
+          out[j] = group_min<K, CB, false, true>(best, vcache, g, xp, start, fm, fb, bh);
+        else
+          out[j] = group_min<K, CB, false, false>(best, vcache, g, xp, start, fm, fb, bh);
         back[static_cast<size_t>(t) * C::kLow + g] = static_cast<uint8_t>(bh);
       }
     }
@@ -118,6 +243,7 @@ __device__ void viterbi_pass(EncShared& sh, float* best, const __half* vcache, u
       if (g < C::kLow) best[g] = out[j];
     }
     __syncthreads();
+    }
   }
   // final step: cost of every state, the cheapest (smallest state on ties)
   {
@@ -192,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncParams p) 
     if (tid == 0) {
       uint32_t s = sh.s_last;
       for (int t = kSteps - 1; t > kSteps / 2; --t) {
-        const uint32_t g = s >> K;
-        s = g | (static_cast<uint32_t>(back[static_cast<size_t>(t) * C::kLow + g]) << (16 - K));
+        const uint32_t g = (s >> K) & (C::kLow - 1);
+        s = g | ((static_cast<uint32_t>(back[static_cast<size_t>(t) * C::kLow + g]) & (C::kNb - 1)) << (16 - K));
       }
       sh.s_star = s;
     }
@@ -225,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(const EncParams p) 
       uint32_t s = sh.s_last;
       sh.states[kSteps - 1] = s;
       for (int t = kSteps - 1; t > 0; --t) {
-        const uint32_t g = s >> K;
-        s = g | (static_cast<uint32_t>(back[static_cast<size_t>(t) * C::kLow + g]) << (16 - K));
+        const uint32_t g = (s >> K) & (C::kLow - 1);
+        s = g | ((static_cast<uint32_t>(back[static_cast<size_t>(t) * C::kLow + g]) & (C::kNb - 1)) << (16 - K));
         sh.states[t - 1] = s;
       }
       p.cost[tile] = sh.cost;
