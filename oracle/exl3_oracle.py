@@ -391,3 +391,53 @@ def layer_forward_whole(codes, K, codebook, m, n, s_in, s_out, scales, x) -> np.
     xt = rht_whole(x.astype(np.float64), s_in)
     z = (xt @ W.T) * np.asarray(scales, dtype=np.float64)
     return rht_whole(z, s_out)
+
+
+# ----------------------------------------------------------------------------
+# The int8-activation path ([TQ] Part eleven)
+# ----------------------------------------------------------------------------
+
+#: int8 activations are quantized per 128-column block of each row.
+INT8_BLOCK = 128
+INT8_MAX = 127
+
+
+def quantize_act(xt: np.ndarray):
+    """Activations to int8 for the dp4a path.
+
+    [TQ] Part eleven: with the weight an affine function of a byte sum (mul1)
+    and the activations quantized to eight-bit integers, one dp4a computes
+    code value times activation for four bytes at once.  The pages do not say
+    how the activations are quantized.  Reading: symmetric, per 128-column
+    block of each row of the rotated activations x-tilde (binary16), in
+    binary32: scale = max|x| / 127 (one binary32 division), q = the nearest
+    integer to x / scale (one binary32 division, ties to even); a block of
+    zeros has scale 0 and q 0.  Returns (q int8 [M, n], scale float32
+    [M, n/128]).
+    """
+    xt = np.atleast_2d(np.asarray(xt, dtype=np.float16)).astype(np.float32)
+    M, n = xt.shape
+    assert n % INT8_BLOCK == 0
+    blocks = xt.reshape(M, n // INT8_BLOCK, INT8_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    scale = (amax / np.float32(INT8_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1))
+    q = np.rint(blocks / safe[:, :, None]).astype(np.float32)
+    q = np.where(scale[:, :, None] > 0, q, 0)
+    return q.reshape(M, n).astype(np.int8), scale
+
+
+def layer_forward_int8(codes, K, codebook, m, n, s_out, scales, q, qscale) -> np.ndarray:
+    """The layer on int8 activations: y = Hb(s_out (.) (scale (.) (W-hat x-hat)))
+    with x-hat = q * qscale per 128-column block (already rotated), in float64.
+    Only the byte-sum codes (1MAD, mul1) have the affine form the dp4a path
+    uses ([TQ] Part eleven)."""
+    if codebook not in (CB_1MAD, CB_MUL1):
+        raise ValueError("the int8-activation path needs a byte-sum code (1MAD or mul1)")
+    q = np.atleast_2d(np.asarray(q, dtype=np.float64))
+    M = q.shape[0]
+    xhat = (q.reshape(M, n // INT8_BLOCK, INT8_BLOCK)
+            * np.asarray(qscale, dtype=np.float64).reshape(M, n // INT8_BLOCK, 1)).reshape(M, n)
+    W = decode_tiles(codes, K, codebook, m, n).astype(np.float64)
+    z = (xhat @ W.T) * np.asarray(scales, dtype=np.float64)
+    return rht(z, s_out)
