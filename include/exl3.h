@@ -247,6 +247,57 @@ exl3_status exl3_encode_tiles(const float *target, int tiles, int K, int codeboo
                               size_t workspace_bytes, exl3_stream_t stream);
 
 /**
+ * Activations to int8 for the dp4a path ("Trellis Quantization" Part
+ * eleven).  Per 128-column block of each of M rows of the rotated activations
+ * x_rot (binary16 [M][n]): qscale = max|x| / 127 and q = the nearest integer
+ * to x / qscale, ties to even, both binary32 divisions correctly rounded; a
+ * block of zeros gets qscale 0 and q 0.
+ *   q [M][n] int8 (out), qscale [M][n/128] float (out).
+ * n a multiple of 128 (EXL3_ERR_SHAPE); x_rot and q 16-byte aligned.
+ */
+exl3_status exl3_quantize_act(const exl3_half *x_rot, int M, int n, int8_t *q, float *qscale,
+                              exl3_stream_t stream);
+
+/**
+ * Workspace of exl3_gemm_i8 / exl3_gemm_int8act: counters and status word as
+ * for exl3_workspace_bytes, fp32 row sums [M][m], the activations replicated
+ * into 32-bit words [M][n], per-tile corrections [M][n/16] and per-block
+ * factors [M][n/128] (each 256-byte aligned).  Same zero-fill contract.  0
+ * for an invalid shape or M outside 1..EXL3_MAX_BATCH.
+ */
+size_t exl3_gemm_i8_workspace_bytes(int m, int n, int M);
+
+/**
+ * The layer on int8 activations, for the byte-sum codes only (EXL3_CB_1MAD,
+ * EXL3_CB_MUL1; others EXL3_ERR_CODEBOOK):
+ *   y = binary16(Hb(s_out (.) (scale (.) (W-hat x-hat)))),
+ *   x-hat[b][j] = q[b][j] * qscale[b][j / 128]   (already rotated).
+ * The weight is C * (S - centre) for the byte sum S of a state, so each
+ * product is one dp4a of the four (masked) bytes with q replicated four times
+ * ("Trellis Quantization" Part eleven), accumulated exactly in int32 per
+ * 16-column tile and scaled by C * qscale in binary32.  This uses the exact
+ * affine weight rather than its binary16 rounding (within the layer
+ * tolerance).  q [M][n] int8, qscale [M][n/128] float; 1 <= M <= 32; other
+ * arguments as exl3_gemm_small (no s_in: the activations are given rotated).
+ */
+exl3_status exl3_gemm_i8(const uint32_t *codes, int K, int codebook, int m, int n,
+                         const exl3_half *s_out, const exl3_half *scales, int M, const int8_t *q,
+                         const float *qscale, exl3_half *y, void *workspace,
+                         size_t workspace_bytes, exl3_stream_t stream);
+
+/**
+ * The int8-activation layer from binary16 activations: x-tilde =
+ * binary16(Hb(s_in (.) x)) (x itself without s_in), quantized as by
+ * exl3_quantize_act, then exl3_gemm_i8.  The result differs from exl3_gemm's
+ * by the activation quantization (about 1% relative at batch 1 on Gaussian
+ * activations).  Arguments as exl3_gemm_small, 1MAD or mul1 only.
+ */
+exl3_status exl3_gemm_int8act(const uint32_t *codes, int K, int codebook, int m, int n,
+                              const exl3_half *s_in, const exl3_half *s_out,
+                              const exl3_half *scales, int M, const exl3_half *x, exl3_half *y,
+                              void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
+/**
  * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
  * call of this shape and batch makes on the current device under the current
  * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on

@@ -204,3 +204,28 @@ def test_encoder_workspace_and_validation(lib):
     assert call(t=None) == 1 and call(w=None) == 1 and call(c=None) == 1
     assert call(t=A + 4) == 6 and call(w=A + 8) == 6
     assert call(wsb=slot - 1) == 7 and call(ws=None) == 7
+
+
+def test_int8_path_workspace_and_validation(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    m, n, M = 1024, 4096, 5
+    want = (a256(4 * (m // 128 + 1)) + a256(4 * M * m) + a256(4 * M * n) + a256(4 * M * (n // 16))
+            + a256(4 * M * (n // 128)))
+    assert B.exl3_gemm_i8_workspace_bytes(m, n, M) == want
+    assert B.exl3_gemm_i8_workspace_bytes(m, n, 33) == 0 and B.exl3_gemm_i8_workspace_bytes(100, n, 1) == 0
+    call = lambda **kw: lib.exl3_gemm_i8(kw.get("codes", A), kw.get("K", 2), kw.get("cb", 1), kw.get("m", 256),  # noqa: E731
+                                         256, A, A, kw.get("M", 1), A, kw.get("qs", A), A, kw.get("ws", A),
+                                         kw.get("wsb", 1 << 30), None)
+    assert call(M=0) == 5 and call(M=33) == 5
+    assert call(m=100) == 2
+    assert call(cb=0) == 4 and call(cb=2) == 4 and call(cb=4) == 4
+    assert call(K=9) == 3
+    assert call(codes=None) == 1 and call(qs=None) == 1
+    assert call(wsb=16) == 7
+    f = lambda **kw: lib.exl3_gemm_int8act(A, 2, kw.get("cb", 3), 256, 256, A, A, A, kw.get("M", 1), A,  # noqa: E731
+                                           kw.get("y", A), A, 1 << 30, None)
+    assert f(cb=0) == 4 and f(M=0) == 5 and f(y=None) == 1
+    assert lib.exl3_quantize_act(A, 0, 128, A, A, None) == 5
+    assert lib.exl3_quantize_act(A, 1, 100, A, A, None) == 2
+    assert lib.exl3_quantize_act(A, 1, 128, A, None, None) == 1
+    assert lib.exl3_quantize_act(A + 2, 1, 128, A, A, None) == 6

@@ -1,0 +1,87 @@
+"""GPU parity of the int8-activation path ("Trellis Quantization" Part eleven:
+eight-bit activations, byte-sum codes, one dp4a per four products):
+
+* the quantizer, bit-exact against the oracle's binary32 quantizer on seeded
+  binary16 activations (q and the block scales);
+* exl3_gemm_i8 on given int8 activations against the oracle's float64 layer on
+  the same dequantized activations (relative L2 <= 5e-3, |err| <= 1e-2 *
+  max|y_ref|), for 1MAD and mul1, K = 1..8, batch chunks of 1, 2, 4, 8;
+* exl3_gemm_int8act from binary16 activations against the oracle's
+  quantize-then-layer, and its distance from the unquantized layer."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import exl3_oracle as O
+from trellis_decode_gemv_gb300 import binding as B
+from trellis_decode_gemv_gb300 import synth
+from tests.gpu_helpers import assert_layer_close, layer_error, to_dev, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,n", [(1, 128), (3, 4096), (8, 14336)])
+def test_quantizer_bit_exact(M, n):
+    x = synth.activations(M, n, synth.seed_for(82, n))
+    x[0, :128] = 0  # a zero block
+    q, qs = B.exl3_quantize_act(to_dev(x))
+    torch.cuda.synchronize()
+    q_ref, qs_ref = O.quantize_act(x)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    np.testing.assert_array_equal(qs.cpu().numpy().view(np.uint32), qs_ref.view(np.uint32))
+
+
+def _int8_inputs(m, n, K, M, cfg, idx):
+    inp = synth.layer_inputs(m, n, K, M, config=cfg, index=idx)
+    xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)  # a rotated activation
+    q, qs = O.quantize_act(xt)
+    return inp, q, qs
+
+
+@pytest.mark.parametrize("cb", [1, 3])
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_gemm_i8_codes_and_widths(K, cb):
+    m, n, M = 256, 512, 1
+    inp, q, qs = _int8_inputs(m, n, K, M, 83, 10 * K + cb)
+    d = upload(inp)
+    y = B.exl3_gemm_i8(d["codes"], K, cb, m, n, d["s_out"], d["scales"], to_dev(q), to_dev(qs))
+    torch.cuda.synchronize()
+    ref = O.layer_forward_int8(inp["codes"], K, cb, m, n, inp["s_out"], inp["scales"], q, qs)
+    assert_layer_close(y, ref, f"K={K} cb={cb}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 15, 32])
+def test_gemm_i8_batches(M):
+    m, n, K, cb = 1024, 1024, 3, 3
+    inp, q, qs = _int8_inputs(m, n, K, M, 84, M)
+    d = upload(inp)
+    ws = torch.zeros(B.exl3_gemm_i8_workspace_bytes(m, n, M), dtype=torch.uint8, device="cuda")
+    y = B.exl3_gemm_i8(d["codes"], K, cb, m, n, d["s_out"], d["scales"], to_dev(q), to_dev(qs), workspace=ws)
+    torch.cuda.synchronize()
+    assert B.workspace_status(ws, m) == 0
+    assert float(ws[256:256 + 4 * M * m].view(torch.float32).abs().sum()) == 0.0  # row sums left at zero
+    ref = O.layer_forward_int8(inp["codes"], K, cb, m, n, inp["s_out"], inp["scales"], q, qs)
+    assert_layer_close(y, ref, f"M={M}")
+
+
+@pytest.mark.parametrize("m,n,K,cb", [(14336, 4096, 2, 1), (4096, 14336, 4, 3)])
+def test_gemm_int8act_llama_shapes(m, n, K, cb):
+    """From binary16 activations: against the oracle's quantize-then-layer on
+    sampled row blocks, and about 1% from the unquantized layer."""
+    M = 1
+    inp = synth.layer_inputs(m, n, K, M, config=85, index=K)
+    d = upload(inp)
+    y = B.exl3_gemm_int8act(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+    torch.cuda.synchronize()
+    rbs = [0, 13, m // 128 - 1]
+    xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+    q, qs = O.quantize_act(xt)
+    xhat = (q.astype(np.float64).reshape(M, n // 128, 128) * qs.astype(np.float64)[:, :, None]).reshape(M, n)
+    ref8 = O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, None, inp["s_out"], inp["scales"], xhat, rbs)
+    cols = torch.cat([torch.arange(b * 128, b * 128 + 128) for b in rbs]).cuda()
+    got = y.view(M, m)[:, cols]
+    assert_layer_close(got, ref8, "int8act vs quantized oracle")
+    reff = O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"],
+                                     inp["x"], rbs)
+    rel, _ = layer_error(got, reff)
+    assert 1e-3 < rel < 2.5e-2, rel

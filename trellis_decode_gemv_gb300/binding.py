@@ -67,6 +67,10 @@ _SIGNATURES = {
     "exl3_gemm_launches": ([_I, _I, _I], _I),
     "exl3_rht_whole": ([_P, _P, _P, _I, _I, _P], _I),
     "exl3_encode_workspace_bytes": ([_I, _I], _SZ),
+    "exl3_quantize_act": ([_P, _I, _I, _P, _P, _P], _I),
+    "exl3_gemm_i8_workspace_bytes": ([_I, _I, _I], _SZ),
+    "exl3_gemm_i8": ([_P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _SZ, _P], _I),
+    "exl3_gemm_int8act": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_encode_tiles": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
@@ -430,6 +434,66 @@ def exl3_encode_tiles(target: torch.Tensor, K: int, codebook: int, words=None, c
                                  _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
                                  _stream(dev)))
     return words, cost
+
+
+def exl3_quantize_act(x_rot: torch.Tensor):
+    """int8 activations and per-128-block scales of rotated binary16 activations
+    [M, n]: returns (q int8 [M, n], qscale float32 [M, n/128])."""
+    lib = load_library()
+    x2 = x_rot if x_rot.dim() == 2 else x_rot.view(1, -1)
+    M, n = x2.shape
+    q = torch.empty((M, n), dtype=torch.int8, device=x_rot.device)
+    qs = torch.empty((M, n // 128), dtype=torch.float32, device=x_rot.device)
+    _check(lib.exl3_quantize_act(_ptr(x2, "x_rot", _HALF), M, n, _ptr(q, "q", (torch.int8,), x_rot.device),
+                                 _ptr(qs, "qscale", (torch.float32,), x_rot.device), _stream(x_rot.device)))
+    return q, qs
+
+
+def exl3_gemm_i8_workspace_bytes(m: int, n: int, M: int) -> int:
+    return int(load_library().exl3_gemm_i8_workspace_bytes(m, n, M))
+
+
+def _i8_workspace(m, n, M, dev, workspace):
+    if workspace is not None:
+        return workspace
+    nbytes = exl3_gemm_i8_workspace_bytes(m, n, M)
+    if nbytes == 0:
+        raise Exl3Error(2, "invalid shape or batch for an int8 workspace")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+
+
+def exl3_gemm_i8(codes, K, codebook, m, n, s_out, scales, q, qscale, y=None, workspace=None):
+    """The layer on int8 activations q [M, n] with per-block scales qscale [M, n/128]."""
+    lib = load_library()
+    dev = codes.device
+    q2 = q if q.dim() == 2 else q.view(1, -1)
+    M = q2.shape[0]
+    if y is None:
+        y = torch.empty((M, m), dtype=torch.float16, device=dev)
+    workspace = _i8_workspace(m, n, M, dev, workspace)
+    _check(lib.exl3_gemm_i8(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n, _ptr(s_out, "s_out", _HALF, dev),
+        _ptr(scales, "scales", _HALF, dev), M, _ptr(q2, "q", (torch.int8,), dev),
+        _ptr(qscale, "qscale", (torch.float32,), dev), _ptr(y, "y", _HALF, dev),
+        _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(), _stream(dev)))
+    return y if q.dim() == 2 else y.view(-1)
+
+
+def exl3_gemm_int8act(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, workspace=None):
+    """The int8-activation layer from binary16 activations x [M, n]."""
+    lib = load_library()
+    dev = codes.device
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, m), dtype=torch.float16, device=dev)
+    workspace = _i8_workspace(m, n, M, dev, workspace)
+    _check(lib.exl3_gemm_int8act(
+        _ptr(codes, "codes", _WORDS), K, codebook, m, n, _ptr(s_in, "s_in", _HALF, dev),
+        _ptr(s_out, "s_out", _HALF, dev), _ptr(scales, "scales", _HALF, dev), M, _ptr(x2, "x", _HALF, dev),
+        _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
+        _stream(dev)))
+    return y if x.dim() == 2 else y.view(-1)
 
 
 def exl3_gemm_launches(m: int, n: int, M: int) -> int:

@@ -143,6 +143,28 @@ struct LayerArgs {
   int debug_stall;    // tensor-core kernel: test hook, post no operand B
 };
 
+// The int8-activation layer kernel (one layer, a batch chunk of mb rows).
+struct I8Args {
+  const uint32_t* codes;
+  const int32_t* q4;     // [mb][n]: each int8 activation replicated into the four bytes of a word
+  const int32_t* tcorr;  // [mb][n/16]: centre x (sum of the tile's 16 activations)
+  const float* cs;       // [mb][n/128]: C x the block's activation scale
+  float* zacc;           // [mb][m] fp32 row sums
+  int m, n;
+  int sub;      // tiles per sub-unit
+  int per_row;  // sub-units per tile row
+  int ctas;
+  long long units;
+};
+exl3_status launch_i8_k1(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k2(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k3(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k4(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k5(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k6(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k7(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+exl3_status launch_i8_k8(const I8Args& a, int codebook, int mb, cudaStream_t stream);
+
 // Internal launchers (one translation unit per K for the layer kernels).
 exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int rows, int d,
                        cudaStream_t stream);
