@@ -60,6 +60,9 @@ BF16_FALLBACK_TFLOPS = 1900.0
 # MCG: as 3INST (a multiply instead of the multiply-add); mul1: as 1MAD plus
 # the six-bit byte mask
 OPS_PER_WEIGHT = {synth.CB_3INST: 4, synth.CB_1MAD: 5, synth.CB_MCG: 4, synth.CB_MUL1: 6}
+# the int8-activation path: window, generator, (mul1: six-bit mask), one dp4a
+# that both sums the bytes and multiplies by the activation
+OPS_PER_WEIGHT_INT8 = {synth.CB_1MAD: 3, synth.CB_MUL1: 4}
 # DRAM traffic / algorithmic bytes of the dominant kernel, from the ncu
 # captures of those kernels (dram__bytes_read.sum +
 # dram__bytes_write.sum of the captured launches over their algorithmic bytes).
@@ -67,6 +70,7 @@ TRAFFIC_RATIO = {
     "shuffle": (29.445 / 29.38, "the ncu capture of layer_kernel on gate/up/down 14336x4096 K4 1MAD"),
     "tensor": (23.12 / 22.15, "the ncu capture of tc_layer_kernel on 14336x4096 K3 1MAD at batch 16"),
     "dense": (None, None),
+    "int8": (None, None),
 }
 
 
@@ -106,6 +110,11 @@ def workload(name: str, batch: int):
     if name == "mixed":
         return ("80-layer mixed-width stack (attn 8192x8192 K4; MLP 28672x8192 / 8192x28672, "
                 "K in {2,3,4}, 2.90 bpw body) + lm_head 128256x8192 K6, 3INST, batch 1"), 4, synth.mixed_stack(), 1
+    if name in ("int8", "mad-mul1"):
+        how = ("int8 activations (exl3_gemm_int8act: rotation + per-128-block int8 quantization, "
+               "one dp4a per weight)") if name == "int8" else "binary16 activations (the fused layer)"
+        return (f"Llama-3-8B-shaped layer set with the byte-sum codes 1MAD and mul1 at K=2,3,4, {how}, "
+                f"batch {batch}"), 9, synth.llama8b_layer_set((synth.CB_1MAD, synth.CB_MUL1)), batch
     if name == "whole":
         # QTIP's whole-vector rotations need power-of-two dimensions: the
         # attention projections of a Llama-3-70B-shaped model, 8 layers
@@ -138,6 +147,17 @@ def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
             rem -= c
             launches += 3 if (c > 2 or tiles_per_sm >= 1024) else 2
     return launches
+
+
+def int8_chunks(M: int) -> int:
+    """Layer-kernel launches of one int8-activation call: one per batch chunk
+    of 8, 4, 2 or 1 rows (plus the preparation and output kernels)."""
+    n, rem = 0, M
+    for c in (8, 4, 2, 1):
+        while rem >= c:
+            rem -= c
+            n += 1
+    return n
 
 
 def decoder_groups(gemvs, grouped: bool = True):
@@ -183,14 +203,14 @@ def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     return 3 * chunks
 
 
-def algorithmic(m, n, K, cb, M, path="auto"):
+def algorithmic(m, n, K, cb, M, path="auto", int8=False):
     """Weights, algorithmic bytes and decode integer ops of one call; above 32
     batch rows the dense prefill decodes every tile once per call, the
     tensor-memory passes once per 128-row pass."""
     weights = m * n
     nbytes = m * n * K // 8 + 2 * m + 2 * (m + n) + 2 * M * n + 2 * M * m
     passes = (M + 127) // 128 if (M > 32 and path == "tensor") else 1
-    ops = weights * OPS_PER_WEIGHT[cb] * passes
+    ops = weights * (OPS_PER_WEIGHT_INT8 if int8 else OPS_PER_WEIGHT)[cb] * passes
     return weights, nbytes, ops
 
 
@@ -400,7 +420,9 @@ def run_ours(args):
     calls = []
     xo = yo = 0
     whole = args.workload == "whole"
-    ws_of = B.exl3_gemm_whole_workspace_bytes if whole else B.exl3_gemm_workspace_bytes
+    int8 = args.workload == "int8"
+    ws_of = (B.exl3_gemm_whole_workspace_bytes if whole else B.exl3_gemm_i8_workspace_bytes if int8
+             else B.exl3_gemm_workspace_bytes)
     ws_bytes = max(ws_of(m, n, M) for _, m, n, _, _ in gemvs)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     packed = 0
@@ -422,7 +444,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
 
     groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
-                            grouped=not (args.ungrouped or whole))
+                            grouped=not (args.ungrouped or whole or int8))
     gws = max([B.exl3_group_workspace_bytes([(calls[i]["m"], calls[i]["n"]) for i in g], M)
                for g in groups if len(g) > 1] + [0])
     if gws > ws.numel():
@@ -431,7 +453,8 @@ def run_ours(args):
     def run_group(g):
         if len(g) == 1:
             c = calls[g[0]]
-            fn = B.exl3_gemm_whole if whole else B.exl3_gemm if M > 32 else B.exl3_gemm_small
+            fn = (B.exl3_gemm_whole if whole else B.exl3_gemm_int8act if int8 else B.exl3_gemm if M > 32
+                  else B.exl3_gemm_small)
             fn(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                c["scales"], c["x"], y=c["y"], workspace=ws)
         else:
@@ -444,7 +467,7 @@ def run_ours(args):
 
     # Decode work (weights, integer ops) does not grow with the batch; the
     # multiply-accumulates do (macs = weights * M).
-    alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M, args.path) for c in calls]
+    alg = [algorithmic(c["m"], c["n"], c["K"], c["cb"], M, args.path, int8) for c in calls]
     weights_step = sum(a[0] for a in alg)
     bytes_step = sum(a[1] for a in alg)
     ops_step = sum(a[2] for a in alg)
@@ -524,9 +547,9 @@ def run_ours(args):
     t_hbm = np.array([a[1] / (hbm_gbs * 1e9) for a in alg])
     t_int = np.array([a[2] / p_int for a in alg])
     # tensor-core term: 2 M m n flops at the measured dense bf16 (= fp16) peak
-    flops_step = 2.0 * M * sum(c["m"] * c["n"] for c in calls) if M > 2 else 0.0
+    flops_step = 2.0 * M * sum(c["m"] * c["n"] for c in calls) if (M > 2 and not int8) else 0.0
     p_tensor = bf16_tflops * 1e12
-    t_tc = np.array([2.0 * M * c["m"] * c["n"] / p_tensor if M > 2 else 0.0 for c in calls])
+    t_tc = np.array([2.0 * M * c["m"] * c["n"] / p_tensor if (M > 2 and not int8) else 0.0 for c in calls])
     t_roof = np.maximum(np.maximum(t_hbm, t_int), t_tc)
     terms = {"alu": t_int.sum(), "hbm": t_hbm.sum(), "tensor": t_tc.sum()}
     bound = max(terms, key=terms.get)
@@ -536,16 +559,19 @@ def run_ours(args):
         achieved, peak, unit = flops_step / t_step / 1e12, bf16_tflops, "TFLOP/s"
     else:
         achieved, peak, unit = bytes_step / t_step / 1e9, hbm_gbs, "GB/s"
-    tensor = args.path == "tensor" or (args.path == "auto" and M > 2)
+    tensor = (args.path == "tensor" or (args.path == "auto" and M > 2)) and not int8
     dense = M > 32 and args.path != "tensor"
-    if dense:
+    if int8:
+        kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
+                 "rotation/quantization and output kernels")
+    elif dense:
         kname = ("dense_kernel (tcgen05 128x256x16 MMAs, both operands in shared memory) + "
                  "decode-to-operand-image, operand-B and output kernels")
     elif tensor:
         kname = "tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"
     else:
         kname = "layer_kernel (fused input RHT + trellis decode + GEMV) + output kernel"
-    ratio, ratio_src = TRAFFIC_RATIO["dense" if dense else "tensor" if tensor else "shuffle"]
+    ratio, ratio_src = TRAFFIC_RATIO["int8" if int8 else "dense" if dense else "tensor" if tensor else "shuffle"]
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": None if ratio is None else ratio * bytes_step,
                 "traffic_note": ("no ncu DRAM capture of this kernel yet" if ratio is None else
@@ -580,7 +606,12 @@ def run_ours(args):
     # holds its layers), one call per group; x and y are the bound tensors.
     layer_objs = []
     for g in groups:
-        if whole:  # no layer object for the whole-vector variant: the public call itself
+        if int8:  # the public call itself
+            c = calls[g[0]]
+            layer_objs.append(lambda c=c: B.exl3_gemm_int8act(
+                c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
+                y=c["y"], workspace=ws))
+        elif whole:  # no layer object for the whole-vector variant: the public call itself
             c = calls[g[0]]
             layer_objs.append(lambda c=c: B.exl3_gemm_whole(
                 c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
@@ -648,6 +679,7 @@ def run_ours(args):
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path,
                        "calls": "one exl3_gemm_whole call per GEMV" if whole else
+                       "one exl3_gemm_int8act call per GEMV" if int8 else
                        "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
                        else "one exl3_gemm_small call per GEMV"},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
@@ -657,6 +689,7 @@ def run_ours(args):
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * sum(
                 (B.exl3_gemm_launches(calls[g[0]]["m"], calls[g[0]]["n"], M) + 2) if whole else
+                (2 + int8_chunks(M)) if int8 else
                 kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) for g in groups),
             "clocks": clk,
         }
@@ -814,7 +847,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b",
                     choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill",
-                             "whole", "encode"])
+                             "whole", "encode", "int8", "mad-mul1"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",
