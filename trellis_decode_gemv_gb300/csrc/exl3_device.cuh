@@ -49,13 +49,20 @@ __device__ __forceinline__ __half code_3inst(uint32_t s) {
   return __hadd(lo, hi);
 }
 
+// (S - centre) exactly in binary32 for the byte sum S of x, without an
+// int-to-float conversion: the dp4a adds S onto the bit pattern of 2^23
+// (0x4B000000), which is then the binary32 value 2^23 + S exactly (S < 2^23),
+// and subtracting 2^23 + centre is exact (the magic-number splice of
+// "Trellis Quantization" Part three, in binary32).
+__device__ __forceinline__ float centred_byte_sum(uint32_t x, int centre) {
+  const float biased = __uint_as_float(__dp4a(x, 0x01010101u, 0x4B000000u));
+  return __fsub_rn(biased, 8388608.0f + static_cast<float>(centre));
+}
+
 // 1MAD: LCG, byte sum S (one dp4a against 0x01010101), (S - 510) exact in
 // binary32, one binary32 multiply, one rounding to binary16.
 __device__ __forceinline__ __half code_1mad(uint32_t s) {
-  const uint32_t x = lcg(s);
-  const int S = static_cast<int>(__dp4a(x, 0x01010101u, 0u));
-  const float c = static_cast<float>(S - kOneMadCentre);
-  return __float2half_rn(__fmul_rn(c, kOneMadScale));
+  return __float2half_rn(__fmul_rn(centred_byte_sum(lcg(s), kOneMadCentre), kOneMadScale));
 }
 
 // MCG and mul1, EXL3's later codes ("Trellis Quantization", Parts eleven and
@@ -116,10 +123,14 @@ __device__ __forceinline__ __half code_mcg(uint32_t s) {
 // mul1: masked byte sum S (one dp4a), (S - 126) exact in binary32, one binary32
 // multiply, one rounding to binary16.
 __device__ __forceinline__ __half code_mul1(uint32_t s) {
-  const int S = static_cast<int>(__dp4a(mcg(s) & kMul1Mask, 0x01010101u, 0u));
-  const float c = static_cast<float>(S - kMul1Centre);
-  return __float2half_rn(__fmul_rn(c, kMul1Scale));
+  return __float2half_rn(__fmul_rn(centred_byte_sum(mcg(s) & kMul1Mask, kMul1Centre), kMul1Scale));
 }
+
+// The defined binary16 weights of two states, packed (s0 in the low half):
+// the same roundings as decode_state, two at a time (one paired conversion,
+// or one packed add for the three-instruction codes).
+template <int CB>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t s0, uint32_t s1);
 
 template <int CB>
 __device__ __forceinline__ __half decode_state(uint32_t s) {
@@ -242,6 +253,26 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
       const float o = __shfl_xor_sync(0xFFFFFFFFu, v[j], d);
       v[j] = upper ? (o - v[j]) : (v[j] + o);
     }
+  }
+}
+
+template <int CB>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t s0, uint32_t s1) {
+  if constexpr (CB == kCb1Mad || CB == kCbMul1) {
+    constexpr int centre = CB == kCbMul1 ? kMul1Centre : kOneMadCentre;
+    constexpr float scale = CB == kCbMul1 ? kMul1Scale : kOneMadScale;
+    const uint32_t x0 = CB == kCbMul1 ? (mcg(s0) & kMul1Mask) : lcg(s0);
+    const uint32_t x1 = CB == kCbMul1 ? (mcg(s1) & kMul1Mask) : lcg(s1);
+    const __half2 w = __floats2half2_rn(__fmul_rn(centred_byte_sum(x0, centre), scale),
+                                        __fmul_rn(centred_byte_sum(x1, centre), scale));
+    return *reinterpret_cast<const uint32_t*>(&w);
+  } else {
+    const uint32_t h0 = mask_xor_3inst(CB == kCbMcg ? mcg(s0) : lcg(s0));
+    const uint32_t h1 = mask_xor_3inst(CB == kCbMcg ? mcg(s1) : lcg(s1));
+    const uint32_t lo = __byte_perm(h0, h1, 0x5410);  // (lo0, lo1)
+    const uint32_t hi = __byte_perm(h0, h1, 0x7632);  // (hi0, hi1)
+    const __half2 w = __hadd2(*reinterpret_cast<const __half2*>(&lo), *reinterpret_cast<const __half2*>(&hi));
+    return *reinterpret_cast<const uint32_t*>(&w);
   }
 }
 

@@ -236,16 +236,13 @@ __global__ void __launch_bounds__(kThreads)
   const int J = static_cast<int>(tile - I * tiles_per_row);
   uint32_t wr[RowPair<K>::kPairWords];
   load_row_pair<K>(codes + tile * RowPair<K>::kTileWords, p, wr);
+  uint32_t st[32];
+  pair_states<K>(wr, st);
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     uint32_t packed[8];
 #pragma unroll
-    for (int c = 0; c < 16; c += 2) {
-      const __half lo = decode_state<CB>(pair_state<K>(wr, 16 * k + c));
-      const __half hi = decode_state<CB>(pair_state<K>(wr, 16 * k + c + 1));
-      packed[c / 2] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-                      (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-    }
+    for (int c = 0; c < 16; c += 2) packed[c / 2] = decode_pair<CB>(st[16 * k + c], st[16 * k + c + 1]);
     __half* dst = w + (I * 16 + 2 * p + k) * static_cast<long long>(n) + J * 16;
     reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -257,36 +254,48 @@ __global__ void __launch_bounds__(kThreads)
 // (rb * (n / 64) + ks) * 16384 in the canonical K-major no-swizzle layout of a
 // 128 x 64 binary16 operand: element (r, k) at byte
 // ((k / 8) * 16 + r / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
+// A warp decodes the four tiles of one stage in one tile row (16 rows x 64
+// columns), whose image is eight 256-byte runs (one per 8-column group); the
+// lanes' 16-byte row pieces are regrouped through shared memory so that each
+// store instruction writes two whole runs.
 template <int K, int CB>
 __global__ void __launch_bounds__(kThreads)
     decode_aimg_kernel(const uint32_t* __restrict__ codes, int m, int n, unsigned char* __restrict__ aimg) {
+  __shared__ uint4 runs[kThreads / 32][128];
   const long long gid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   const int tiles_per_row = n / 16;
   const long long tiles = static_cast<long long>(m / 16) * tiles_per_row;
-  if (gid >= tiles * 8) return;
+  if (gid >= tiles * 8) return;  // whole warps: the tile count is a multiple of 8
+  const int lane = threadIdx.x & 31;
+  uint4* run = runs[threadIdx.x >> 5];
   const long long tile = gid >> 3;
   const int p = static_cast<int>(gid & 7);
   const long long I = tile / tiles_per_row;
   const int J = static_cast<int>(tile - I * tiles_per_row);
   uint32_t wr[RowPair<K>::kPairWords];
   load_row_pair<K>(codes + tile * RowPair<K>::kTileWords, p, wr);
-  const long long rb = I / 8;
-  unsigned char* stage = aimg + (rb * (n / 64) + J / 4) * 16384;
+  uint32_t st[32];
+  pair_states<K>(wr, st);
+  const int jt = J % 4;  // this lane's tile within the stage: 8-column groups 2 jt, 2 jt + 1
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     uint32_t packed[8];
 #pragma unroll
-    for (int c = 0; c < 16; c += 2) {
-      const __half lo = decode_state<CB>(pair_state<K>(wr, 16 * k + c));
-      const __half hi = decode_state<CB>(pair_state<K>(wr, 16 * k + c + 1));
-      packed[c / 2] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-                      (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-    }
-    const int r = static_cast<int>(I % 8) * 16 + 2 * p + k;  // row within the 128-row block
-    const int kg = 2 * (J % 4);                              // first 8-column group of the tile
-    unsigned char* row0 = stage + ((kg * 16 + r / 8) * 128 + (r % 8) * 16);
-    *reinterpret_cast<uint4*>(row0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    *reinterpret_cast<uint4*>(row0 + 16 * 128) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    for (int c = 0; c < 16; c += 2) packed[c / 2] = decode_pair<CB>(st[16 * k + c], st[16 * k + c + 1]);
+    const int r = 2 * p + k;  // row within the tile
+    // run kg holds rows r of the tile row at (r / 8) * 8 + r % 8, 16 bytes each
+    run[(2 * jt) * 16 + r] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    run[(2 * jt + 1) * 16 + r] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  }
+  __syncwarp();
+  // run kg goes to ((kg * 16) + 2 * (I % 8)) * 128 of the stage image: core
+  // matrices r / 8 = 0, 1 of the tile row's two 8-row groups, contiguous
+  unsigned char* stage = aimg + ((I / 8) * (n / 64) + J / 4) * 16384 + (I % 8) * 256;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int kg = 2 * i + (lane >> 4);
+    const int off = lane & 15;
+    *reinterpret_cast<uint4*>(stage + kg * 2048 + off * 16) = run[kg * 16 + off];
   }
 }
 
