@@ -444,8 +444,9 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
 
     groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
-                            grouped=not (args.ungrouped or whole or int8))
-    gws = max([B.exl3_group_workspace_bytes([(calls[i]["m"], calls[i]["n"]) for i in g], M)
+                            grouped=not (args.ungrouped or whole))
+    gws_of = B.exl3_group_i8_workspace_bytes if int8 else B.exl3_group_workspace_bytes
+    gws = max([gws_of([(calls[i]["m"], calls[i]["n"]) for i in g], M)
                for g in groups if len(g) > 1] + [0])
     if gws > ws.numel():
         ws = torch.zeros(gws, dtype=torch.uint8, device=dev)
@@ -459,7 +460,8 @@ def run_ours(args):
                c["scales"], c["x"], y=c["y"], workspace=ws)
         else:
             c0 = calls[g[0]]
-            B.exl3_gemm_grouped([calls[i] for i in g], c0["K"], c0["cb"], workspace=ws)
+            gfn = B.exl3_gemm_int8act_grouped if int8 else B.exl3_gemm_grouped
+            gfn([calls[i] for i in g], c0["K"], c0["cb"], workspace=ws)
 
     def step():
         for g in groups:
@@ -606,7 +608,11 @@ def run_ours(args):
     # holds its layers), one call per group; x and y are the bound tensors.
     layer_objs = []
     for g in groups:
-        if int8:  # the public call itself
+        if int8 and len(g) > 1:  # the public calls themselves
+            c0 = calls[g[0]]
+            layer_objs.append(lambda g=g, c0=c0: B.exl3_gemm_int8act_grouped(
+                [calls[i] for i in g], c0["K"], c0["cb"], workspace=ws))
+        elif int8:
             c = calls[g[0]]
             layer_objs.append(lambda c=c: B.exl3_gemm_int8act(
                 c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
@@ -679,7 +685,9 @@ def run_ours(args):
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path,
                        "calls": "one exl3_gemm_whole call per GEMV" if whole else
-                       "one exl3_gemm_int8act call per GEMV" if int8 else
+                       ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
+                        "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
+                       if int8 else
                        "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
                        else "one exl3_gemm_small call per GEMV"},
             "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,

@@ -343,6 +343,25 @@ size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
 exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
                               void *workspace, size_t workspace_bytes, exl3_stream_t stream);
 
+/**
+ * Workspace of exl3_gemm_int8act_grouped: a status word (first 256 bytes),
+ * then per layer the regions of exl3_gemm_i8_workspace_bytes after its
+ * counters (row sums, activation words, tile corrections, block factors).
+ * Same zero-fill contract.  0 for an invalid group.
+ */
+size_t exl3_group_i8_workspace_bytes(const exl3_layer *layers, int count, int M);
+
+/**
+ * `count` (1..EXL3_MAX_GROUP) independent layers on int8 activations, as
+ * `count` calls of exl3_gemm_int8act (same K, byte-sum code and batch
+ * 1..EXL3_MAX_BATCH): one activation kernel for every layer's x, one layer
+ * kernel over the tiles of every layer per batch chunk, one output kernel.
+ * Validation and errors as exl3_gemm_grouped and exl3_gemm_int8act.
+ */
+exl3_status exl3_gemm_int8act_grouped(const exl3_layer *layers, int count, int K, int codebook,
+                                      int M, void *workspace, size_t workspace_bytes,
+                                      exl3_stream_t stream);
+
 /** Kernel family used by exl3_gemv / exl3_gemm_small. */
 typedef enum {
   EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, tensor-core kernel above */

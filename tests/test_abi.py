@@ -229,3 +229,15 @@ def test_int8_path_workspace_and_validation(lib):
     assert lib.exl3_quantize_act(A, 1, 100, A, A, None) == 2
     assert lib.exl3_quantize_act(A, 1, 128, A, None, None) == 1
     assert lib.exl3_quantize_act(A + 2, 1, 128, A, A, None) == 6
+
+
+def test_int8_group_workspace_and_validation(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    shapes, M = [(1024, 4096), (256, 512)], 3
+    want = 256 + sum(a256(4 * M * m) + a256(4 * M * n) + a256(4 * M * (n // 16)) + a256(4 * M * (n // 128))
+                     for m, n in shapes)
+    assert B.exl3_group_i8_workspace_bytes(shapes, M) == want
+    assert B.exl3_group_i8_workspace_bytes([(100, 256)], 1) == 0
+    assert B.exl3_group_i8_workspace_bytes(shapes, 33) == 0
+    assert B.exl3_group_i8_workspace_bytes(shapes * 3, 1) == 0  # more than four layers
+    assert lib.exl3_gemm_int8act_grouped(None, 1, 2, 1, 1, A, 1 << 30, None) == 1

@@ -85,3 +85,31 @@ def test_gemm_int8act_llama_shapes(m, n, K, cb):
                                      inp["x"], rbs)
     rel, _ = layer_error(got, reff)
     assert 1e-3 < rel < 2.5e-2, rel
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_int8act_grouped_matches_the_oracle_per_layer(M):
+    """q/k/v-like layers with different shapes and their own x in one grouped
+    call: each layer within tolerance of the oracle's quantize-then-layer."""
+    K, cb = 2, 3
+    shapes = [(512, 1024), (256, 1024), (256, 1024), (128, 2048)]
+    layers, refs = [], []
+    for i, (m, n) in enumerate(shapes):
+        inp = synth.layer_inputs(m, n, K, M, config=86, index=10 * M + i)
+        d = upload(inp)
+        layers.append(dict(codes=d["codes"], m=m, n=n, s_in=d["s_in"], s_out=d["s_out"], scales=d["scales"],
+                           x=d["x"], y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")))
+        xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+        q, qs = O.quantize_act(xt)
+        refs.append(O.layer_forward_int8(inp["codes"], K, cb, m, n, inp["s_out"], inp["scales"], q, qs))
+    ws = torch.zeros(B.exl3_group_i8_workspace_bytes(shapes, M), dtype=torch.uint8, device="cuda")
+    B.exl3_gemm_int8act_grouped(layers, K, cb, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    for L, ref in zip(layers, refs):
+        assert_layer_close(L["y"], ref, f"grouped {L['m']}x{L['n']} M={M}")
+    # the same layers one call at a time agree within one binary16 rounding
+    for L in layers:
+        y1 = B.exl3_gemm_int8act(L["codes"], K, cb, L["m"], L["n"], L["s_in"], L["s_out"], L["scales"], L["x"])
+        torch.cuda.synchronize()
+        assert float((y1.float() - L["y"].float()).abs().max()) <= 2.0 ** -9 * float(y1.float().abs().max())

@@ -71,6 +71,8 @@ _SIGNATURES = {
     "exl3_gemm_i8_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_i8": ([_P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_int8act": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
+    "exl3_group_i8_workspace_bytes": ([ctypes.POINTER(Exl3Layer), _I, _I], _SZ),
+    "exl3_gemm_int8act_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
     "exl3_encode_tiles": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
@@ -304,6 +306,32 @@ def exl3_gemm_grouped(layers, K, codebook, workspace=None):
     _check(lib.exl3_gemm_grouped(arr, len(layers), K, codebook, M,
                                  _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
                                  _stream(dev)))
+    return [L["y"] for L in layers]
+
+
+def exl3_group_i8_workspace_bytes(shapes, M: int = 1) -> int:
+    """Workspace bytes of a grouped int8-activation call over layers of (m, n)."""
+    arr = (Exl3Layer * len(shapes))()
+    for i, (m, n) in enumerate(shapes):
+        arr[i].m, arr[i].n = m, n
+    return int(load_library().exl3_group_i8_workspace_bytes(arr, len(shapes), M))
+
+
+def exl3_gemm_int8act_grouped(layers, K, codebook, workspace=None):
+    """Independent layers on int8 activations (1MAD or mul1), as dicts like
+    exl3_gemm_grouped's; same results as one exl3_gemm_int8act per layer."""
+    lib = load_library()
+    dev = layers[0]["codes"].device
+    M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+    arr = _layer_array(layers, dev, M)
+    if workspace is None:
+        nbytes = exl3_group_i8_workspace_bytes([(L["m"], L["n"]) for L in layers], M)
+        if nbytes == 0:
+            raise Exl3Error(2, "invalid group for a workspace")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib.exl3_gemm_int8act_grouped(arr, len(layers), K, codebook, M,
+                                         _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
+                                         _stream(dev)))
     return [L["y"] for L in layers]
 
 

@@ -46,6 +46,7 @@ using tc::tmem_ld16;
 constexpr int kNB = kDenseNB;       // batch rows per tile (MMA N)
 constexpr int kStageK = 64;         // input columns per stage
 constexpr int kStages = 4;
+constexpr int kPrefetch = 8;  // stages of operand A requested into L2 ahead of use
 constexpr int kABytes = 128 * kStageK * 2;   // 16 KB
 constexpr int kBBytes = kNB * kStageK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -109,6 +110,11 @@ __device__ __forceinline__ bool aborted(const DenseShared& sh) {
 __device__ __forceinline__ void set_abort(DenseShared& sh) { atomicOr(&sh.abort, 1u); }
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16, cta_group::1.
@@ -202,6 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
           mbar_arrive_expect_tx(&sh.full[slot], kStageBytes);
           bulk_g2s(dst, a_src + static_cast<size_t>(ks) * kABytes, kABytes, &sh.full[slot]);
           bulk_g2s(dst + kABytes, b_src + static_cast<size_t>(ks) * kNB * kStageK, kBBytes, &sh.full[slot]);
+          // operand A streams from DRAM: ask for it kPrefetch stages before
+          // the ring does, so that the ring's copies find it in L2
+          if (ks + kPrefetch < w.ks1)
+            bulk_prefetch_l2(a_src + static_cast<size_t>(ks + kPrefetch) * kABytes, kABytes);
         }
       }
       for (int i = 0; i < kStages && i < seq; ++i) {

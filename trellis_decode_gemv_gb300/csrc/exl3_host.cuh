@@ -143,18 +143,24 @@ struct LayerArgs {
   int debug_stall;    // tensor-core kernel: test hook, post no operand B
 };
 
-// The int8-activation layer kernel (one layer, a batch chunk of mb rows).
-struct I8Args {
+// The int8-activation layer kernel over a group of layers (a batch chunk of
+// mb rows); each sub-unit looks up its layer, as in GroupArgs.
+struct I8Layer {
   const uint32_t* codes;
   const int32_t* q4;     // [mb][n]: each int8 activation replicated into the four bytes of a word
   const int32_t* tcorr;  // [mb][n/16]: centre x (sum of the tile's 16 activations)
   const float* cs;       // [mb][n/128]: C x the block's activation scale
   float* zacc;           // [mb][m] fp32 row sums
   int m, n;
-  int sub;      // tiles per sub-unit
+  int u_begin;  // first sub-unit of this layer
   int per_row;  // sub-units per tile row
+};
+struct I8Args {
+  I8Layer l[kMaxGroup];
+  int count;
+  int sub;  // tiles per sub-unit
   int ctas;
-  long long units;
+  long long units;  // sub-units of all layers
 };
 exl3_status launch_i8_k1(const I8Args& a, int codebook, int mb, cudaStream_t stream);
 exl3_status launch_i8_k2(const I8Args& a, int codebook, int mb, cudaStream_t stream);

@@ -16,8 +16,9 @@
 // Same lane mapping and work split as the warp-shuffle sub-unit kernel: a
 // warp decodes one tile row, lane 8 * jt + p takes rows 2p, 2p + 1 of tiles
 // jt, jt + 4, ... of a sub-unit of consecutive tiles; one CTA per SM, the warps
-// take sub-units from a shared counter; shuffles combine the four tile groups
-// and fp32 reductions add each row's sum into the workspace row sums.
+// take sub-units from a shared counter (the sub-units of up to four layers of
+// a group are numbered one after the other); shuffles combine the four tile
+// groups and fp32 reductions add each row's sum into the workspace row sums.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -43,7 +44,7 @@ __device__ __forceinline__ int byte_dot(uint32_t x, int q4, int acc) {
 }
 
 template <int K, int CB, int MB>
-__device__ __forceinline__ void i8_body(const I8Args& a) {
+__device__ __forceinline__ void i8_body(const I8Args& g) {
   constexpr int kWarps = layer_warps<MB>();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -51,9 +52,8 @@ __device__ __forceinline__ void i8_body(const I8Args& a) {
   const int jt = lane >> 3;
   const int p = lane & 7;
   constexpr int kTw = RowPair<K>::kTileWords;
-  const int S = a.sub;
-  const int nt = a.n / 16;
-  const long long units = a.units;
+  const int S = g.sub;
+  const long long units = g.units;
   const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
   const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
   __shared__ int next_unit;
@@ -65,8 +65,14 @@ __device__ __forceinline__ void i8_body(const I8Args& a) {
   bool waited = false;
   int u = u_lo + warp;
   while (u < u_hi) {
-    const int I = u / a.per_row;
-    const int J0 = (u - I * a.per_row) * S;
+    // the layer of sub-unit u, then its tile row and first tile column
+    int li = 0;
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    const I8Layer& a = g.l[li];
+    const int nt = a.n / 16;
+    const int lu = u - a.u_begin;
+    const int I = lu / a.per_row;
+    const int J0 = (lu - I * a.per_row) * S;
     const int J1 = J0 + S < nt ? J0 + S : nt;
     const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
 

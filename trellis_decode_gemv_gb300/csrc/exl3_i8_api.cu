@@ -23,46 +23,72 @@ namespace {
 
 constexpr int kPrepThreads = 128;
 
-__global__ void __launch_bounds__(kPrepThreads)
-    i8_prep_kernel(const __half* __restrict__ x, const __half* __restrict__ s_in, int rotate,
-                   const int8_t* __restrict__ q_in, const float* __restrict__ qscale_in, int8_t* __restrict__ q_out,
-                   float* __restrict__ qscale_out, int32_t* __restrict__ q4, int32_t* __restrict__ tcorr,
-                   float* __restrict__ cs, int rows, int n, int centre, float C) {
+// One layer's activations for the preparation kernel: binary16 x (rotated
+// here with s_in, or taken as already rotated), or int8 q with its scales;
+// optional outputs q_out / qscale_out (the quantizer) and the layer kernel's
+// operands q4 / tcorr / cs.
+struct PrepEntry {
+  const __half* x;
+  const __half* s_in;
+  const int8_t* q_in;
+  const float* qscale_in;
+  int8_t* q_out;
+  float* qscale_out;
+  int32_t* q4;
+  int32_t* tcorr;
+  float* cs;
+  int n;
+  long long job_begin;
+};
+struct PrepGroup {
+  PrepEntry e[kMaxGroup];
+  int count;
+  int rows;
+  int rotate;
+  int centre;
+  float C;
+  long long jobs;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) i8_prep_kernel(const PrepGroup g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int nkb = n / kRowBlock;
   const long long job = static_cast<long long>(blockIdx.x) * (kPrepThreads / 32) + (threadIdx.x >> 5);
-  if (job >= static_cast<long long>(rows) * nkb) return;
-  const int row = static_cast<int>(job / nkb);
-  const int kb = static_cast<int>(job - static_cast<long long>(row) * nkb);
+  if (job >= g.jobs) return;
+  int li = 0;
+  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  const PrepEntry& e = g.e[li];
+  const int n = e.n;
+  const int nkb = n / kRowBlock;
+  const long long local = job - e.job_begin;
+  const int row = static_cast<int>(local / nkb);
+  const int kb = static_cast<int>(local - static_cast<long long>(row) * nkb);
   const int col = kb * kRowBlock + 4 * lane;
   const size_t at = static_cast<size_t>(row) * n + col;
   int q[4];
   float scale;
-  if (q_in != nullptr) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(q_in + at);
+  if (e.q_in != nullptr) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(e.q_in + at);
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = static_cast<int>(static_cast<int8_t>(w >> (8 * i)));
-    scale = qscale_in[static_cast<size_t>(row) * nkb + kb];
+    scale = e.qscale_in[static_cast<size_t>(row) * nkb + kb];
   } else {
-    const uint2 xr = *reinterpret_cast<const uint2*>(x + at);
+    const uint2 xr = *reinterpret_cast<const uint2*>(e.x + at);
     const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
     const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
     float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-    if (rotate) {
-      if (s_in != nullptr) {
-        const uint2 sr = *reinterpret_cast<const uint2*>(s_in + col);
-        const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-        const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-        v[0] *= __low2float(s01);
-        v[1] *= __high2float(s01);
-        v[2] *= __low2float(s23);
-        v[3] *= __high2float(s23);
-        fwht128_warp(v, lane);
+    if (g.rotate && e.s_in != nullptr) {
+      const uint2 sr = *reinterpret_cast<const uint2*>(e.s_in + col);
+      const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+      const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+      v[0] *= __low2float(s01);
+      v[1] *= __high2float(s01);
+      v[2] *= __low2float(s23);
+      v[3] *= __high2float(s23);
+      fwht128_warp(v, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __half2float(__float2half_rn(v[i] * kInvSqrt128));
-      }
+      for (int i = 0; i < 4; ++i) v[i] = __half2float(__float2half_rn(v[i] * kInvSqrt128));
     }
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
@@ -70,37 +96,40 @@ __global__ void __launch_bounds__(kPrepThreads)
     scale = __fdiv_rn(amax, 127.0f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = amax > 0.0f ? __float2int_rn(__fdiv_rn(v[i], scale)) : 0;
-    if (q_out != nullptr) {
+    if (e.q_out != nullptr) {
       const uint32_t w = (static_cast<uint32_t>(q[0]) & 0xFFu) | ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
                          ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
-      *reinterpret_cast<uint32_t*>(q_out + at) = w;
+      *reinterpret_cast<uint32_t*>(e.q_out + at) = w;
     }
-    if (qscale_out != nullptr && lane == 0) qscale_out[static_cast<size_t>(row) * nkb + kb] = scale;
+    if (e.qscale_out != nullptr && lane == 0) e.qscale_out[static_cast<size_t>(row) * nkb + kb] = scale;
   }
-  if (q4 != nullptr) {
+  if (e.q4 != nullptr) {
     int4 r;
     r.x = static_cast<int>((static_cast<uint32_t>(q[0]) & 0xFFu) * 0x01010101u);
     r.y = static_cast<int>((static_cast<uint32_t>(q[1]) & 0xFFu) * 0x01010101u);
     r.z = static_cast<int>((static_cast<uint32_t>(q[2]) & 0xFFu) * 0x01010101u);
     r.w = static_cast<int>((static_cast<uint32_t>(q[3]) & 0xFFu) * 0x01010101u);
-    *reinterpret_cast<int4*>(q4 + at) = r;
+    *reinterpret_cast<int4*>(e.q4 + at) = r;
     // lanes 4t .. 4t + 3 hold the 16 columns of tile t of the block
     int s = q[0] + q[1] + q[2] + q[3];
     s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
     s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-    if ((lane & 3) == 0) tcorr[static_cast<size_t>(row) * (n / 16) + col / 16] = centre * s;
-    if (lane == 0) cs[static_cast<size_t>(row) * nkb + kb] = __fmul_rn(C, scale);
+    if ((lane & 3) == 0) e.tcorr[static_cast<size_t>(row) * (n / 16) + col / 16] = g.centre * s;
+    if (lane == 0) e.cs[static_cast<size_t>(row) * nkb + kb] = __fmul_rn(g.C, scale);
   }
 }
 
-exl3_status launch_prep(const __half* x, const __half* s_in, bool rotate, const int8_t* q_in,
-                        const float* qscale_in, int8_t* q_out, float* qscale_out, int32_t* q4, int32_t* tcorr,
-                        float* cs, int rows, int n, int codebook, cudaStream_t stream) {
-  const long long jobs = static_cast<long long>(rows) * (n / kRowBlock);
+exl3_status launch_prep(PrepGroup g, int codebook, cudaStream_t stream) {
+  g.centre = codebook == EXL3_CB_MUL1 ? kMul1Centre : kOneMadCentre;
+  g.C = codebook == EXL3_CB_MUL1 ? kMul1Scale : kOneMadScale;
+  long long jobs = 0;
+  for (int i = 0; i < g.count; ++i) {
+    g.e[i].job_begin = jobs;
+    jobs += static_cast<long long>(g.rows) * (g.e[i].n / kRowBlock);
+  }
+  g.jobs = jobs;
   const long long per_cta = kPrepThreads / 32;
   const unsigned grid = static_cast<unsigned>((jobs + per_cta - 1) / per_cta);
-  const int centre = codebook == EXL3_CB_MUL1 ? kMul1Centre : kOneMadCentre;
-  const float C = codebook == EXL3_CB_MUL1 ? kMul1Scale : kOneMadScale;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPrepThreads);
@@ -110,9 +139,7 @@ exl3_status launch_prep(const __half* x, const __half* s_in, bool rotate, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, i8_prep_kernel, x, s_in, rotate ? 1 : 0, q_in, qscale_in, q_out, qscale_out, q4,
-                         tcorr, cs, rows, n, centre, C) != cudaSuccess)
-    return EXL3_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, i8_prep_kernel, g) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
 
@@ -129,21 +156,36 @@ exl3_status launch_i8(const I8Args& a, int K, int codebook, int mb, cudaStream_t
   }
 }
 
-// Workspace: counters and status | fp32 row sums [M][m] | q4 [M][n] int32 |
-// tile corrections [M][n/16] int32 | block factors [M][n/128] fp32.
-size_t i8_q4_offset(int m, int M) { return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m); }
-size_t i8_tcorr_offset(int m, int n, int M) {
-  return i8_q4_offset(m, M) + align256(sizeof(int32_t) * static_cast<size_t>(M) * n);
+// Per-layer operands of the int8 path in a workspace: fp32 row sums [M][m],
+// q4 [M][n] int32, tile corrections [M][n/16] int32, block factors [M][n/128]
+// fp32, each 256-byte aligned, from byte `at`.
+struct I8Region {
+  float* zacc;
+  int32_t* q4;
+  int32_t* tcorr;
+  float* cs;
+};
+size_t i8_layer_bytes(int m, int n, int M) {
+  return align256(sizeof(float) * static_cast<size_t>(M) * m) + align256(sizeof(int32_t) * static_cast<size_t>(M) * n) +
+         align256(sizeof(int32_t) * static_cast<size_t>(M) * (n / 16)) +
+         align256(sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock));
 }
-size_t i8_cs_offset(int m, int n, int M) {
-  return i8_tcorr_offset(m, n, M) + align256(sizeof(int32_t) * static_cast<size_t>(M) * (n / 16));
+I8Region i8_region(char* ws, size_t at, int m, int n, int M) {
+  I8Region r;
+  r.zacc = reinterpret_cast<float*>(ws + at);
+  at += align256(sizeof(float) * static_cast<size_t>(M) * m);
+  r.q4 = reinterpret_cast<int32_t*>(ws + at);
+  at += align256(sizeof(int32_t) * static_cast<size_t>(M) * n);
+  r.tcorr = reinterpret_cast<int32_t*>(ws + at);
+  at += align256(sizeof(int32_t) * static_cast<size_t>(M) * (n / 16));
+  r.cs = reinterpret_cast<float*>(ws + at);
+  return r;
 }
-size_t i8_total(int m, int n, int M) {
-  return i8_cs_offset(m, n, M) + align256(sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock));
-}
+// Single layer: counters and status word, then the layer's region.
+size_t i8_total(int m, int n, int M) { return zacc_offset(m) + i8_layer_bytes(m, n, M); }
 
 exl3_status check_i8(const uint32_t* codes, int K, int codebook, int m, int n, const exl3_half* s_out,
-                     const exl3_half* scales, int M, const void* xin, exl3_half* y, void* ws, size_t ws_bytes) {
+                     const exl3_half* scales, int M, const void* xin, exl3_half* y) {
   if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
   exl3_status st = check_shape(m, n);
   if (st != EXL3_OK) return st;
@@ -152,40 +194,67 @@ exl3_status check_i8(const uint32_t* codes, int K, int codebook, int m, int n, c
   if (!codes || !scales || !xin || !y) return EXL3_ERR_NULL;
   if (!aligned16(codes) || !aligned16(scales) || !aligned16(xin) || !aligned16(y) || (s_out && !aligned16(s_out)))
     return EXL3_ERR_ALIGN;
-  if (!ws || ws_bytes < i8_total(m, n, M)) return EXL3_ERR_WORKSPACE;
-  if (!aligned16(ws)) return EXL3_ERR_ALIGN;
   return EXL3_OK;
 }
 
-// The layer kernel per batch chunk of 8/4/2/1 rows, then the output kernel
-// over all M rows.
-exl3_status run_i8(const uint32_t* codes, int K, int codebook, int m, int n, const __half* s_out,
-                   const __half* scales, int M, __half* y, char* ws, cudaStream_t cs) {
+// The layer kernel over every layer of the group per batch chunk of 8/4/2/1
+// rows, then one output kernel over all layers and rows.
+exl3_status run_i8(const exl3_layer* layers, const I8Region* reg, int count, int K, int codebook, int M,
+                   cudaStream_t cs) {
   const int sms = device_sm_count();
-  float* zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  const int32_t* q4 = reinterpret_cast<const int32_t*>(ws + i8_q4_offset(m, M));
-  const int32_t* tcorr = reinterpret_cast<const int32_t*>(ws + i8_tcorr_offset(m, n, M));
-  const float* csb = reinterpret_cast<const float*>(ws + i8_cs_offset(m, n, M));
-  const long long tiles = static_cast<long long>(m / 16) * (n / 16);
+  long long tiles = 0;
+  for (int i = 0; i < count; ++i) tiles += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
   exl3_status st;
   for (int done = 0; done < M;) {
     const int mb = M - done >= 8 ? 8 : M - done >= 4 ? 4 : M - done >= 2 ? 2 : 1;
     I8Args a{};
-    a.codes = codes;
-    a.q4 = q4 + static_cast<size_t>(done) * n;
-    a.tcorr = tcorr + static_cast<size_t>(done) * (n / 16);
-    a.cs = csb + static_cast<size_t>(done) * (n / kRowBlock);
-    a.zacc = zacc + static_cast<size_t>(done) * m;
-    a.m = m;
-    a.n = n;
+    a.count = count;
     a.sub = choose_sub(tiles, mb, sms);
-    a.per_row = (n / 16 + a.sub - 1) / a.sub;
-    a.units = static_cast<long long>(m / 16) * a.per_row;
-    a.ctas = static_cast<int>(a.units < sms ? a.units : sms);
+    long long units = 0;
+    for (int i = 0; i < count; ++i) {
+      const int m = layers[i].m, n = layers[i].n;
+      I8Layer& l = a.l[i];
+      l.codes = layers[i].codes;
+      l.q4 = reg[i].q4 + static_cast<size_t>(done) * n;
+      l.tcorr = reg[i].tcorr + static_cast<size_t>(done) * (n / 16);
+      l.cs = reg[i].cs + static_cast<size_t>(done) * (n / kRowBlock);
+      l.zacc = reg[i].zacc + static_cast<size_t>(done) * m;
+      l.m = m;
+      l.n = n;
+      l.u_begin = static_cast<int>(units);
+      l.per_row = (n / 16 + a.sub - 1) / a.sub;
+      units += static_cast<long long>(m / 16) * l.per_row;
+    }
+    a.units = units;
+    a.ctas = static_cast<int>(units < sms ? units : sms);
     if ((st = launch_i8(a, K, codebook, mb, cs)) != EXL3_OK) return st;
     done += mb;
   }
-  return launch_epi(zacc, scales, s_out, y, M, m, cs);
+  EpiGroup eg{};
+  eg.count = count;
+  eg.rows = M;
+  for (int i = 0; i < count; ++i) {
+    eg.e[i].zacc = reg[i].zacc;
+    eg.e[i].scales = reinterpret_cast<const __half*>(layers[i].scales);
+    eg.e[i].s_out = reinterpret_cast<const __half*>(layers[i].s_out);
+    eg.e[i].y = reinterpret_cast<__half*>(layers[i].y);
+    eg.e[i].m = layers[i].m;
+  }
+  return launch_epi_group(eg, cs);
+}
+
+exl3_layer layer_of(const uint32_t* codes, int m, int n, const exl3_half* s_in, const exl3_half* s_out,
+                    const exl3_half* scales, const exl3_half* x, exl3_half* y) {
+  exl3_layer L{};
+  L.codes = codes;
+  L.m = m;
+  L.n = n;
+  L.s_in = s_in;
+  L.s_out = s_out;
+  L.scales = scales;
+  L.x = x;
+  L.y = y;
+  return L;
 }
 
 }  // namespace
@@ -200,8 +269,15 @@ extern "C" exl3_status exl3_quantize_act(const exl3_half* x_rot, int M, int n, i
   if (n <= 0 || n % kRowBlock) return EXL3_ERR_SHAPE;
   if (!x_rot || !q || !qscale) return EXL3_ERR_NULL;
   if (!aligned16(x_rot) || !aligned16(q)) return EXL3_ERR_ALIGN;
-  return launch_prep(reinterpret_cast<const __half*>(x_rot), nullptr, false, nullptr, nullptr, q, qscale, nullptr,
-                     nullptr, nullptr, M, n, EXL3_CB_MUL1, reinterpret_cast<cudaStream_t>(stream));
+  PrepGroup g{};
+  g.count = 1;
+  g.rows = M;
+  g.rotate = 0;
+  g.e[0].x = reinterpret_cast<const __half*>(x_rot);
+  g.e[0].q_out = q;
+  g.e[0].qscale_out = qscale;
+  g.e[0].n = n;
+  return launch_prep(g, EXL3_CB_MUL1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exl3_gemm_i8_workspace_bytes(int m, int n, int M) {
@@ -213,34 +289,92 @@ extern "C" exl3_status exl3_gemm_i8(const uint32_t* codes, int K, int codebook, 
                                     const exl3_half* s_out, const exl3_half* scales, int M, const int8_t* q,
                                     const float* qscale, exl3_half* y, void* workspace, size_t workspace_bytes,
                                     exl3_stream_t stream) {
-  exl3_status st = check_i8(codes, K, codebook, m, n, s_out, scales, M, q, y, workspace, workspace_bytes);
+  exl3_status st = check_i8(codes, K, codebook, m, n, s_out, scales, M, q, y);
   if (st != EXL3_OK) return st;
   if (!qscale) return EXL3_ERR_NULL;
+  if (!workspace || workspace_bytes < i8_total(m, n, M)) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  if ((st = launch_prep(nullptr, nullptr, false, q, qscale, nullptr, nullptr,
-                        reinterpret_cast<int32_t*>(ws + i8_q4_offset(m, M)),
-                        reinterpret_cast<int32_t*>(ws + i8_tcorr_offset(m, n, M)),
-                        reinterpret_cast<float*>(ws + i8_cs_offset(m, n, M)), M, n, codebook, cs)) != EXL3_OK)
-    return st;
-  return run_i8(codes, K, codebook, m, n, reinterpret_cast<const __half*>(s_out),
-                reinterpret_cast<const __half*>(scales), M, reinterpret_cast<__half*>(y), ws, cs);
+  const I8Region reg = i8_region(ws, zacc_offset(m), m, n, M);
+  PrepGroup g{};
+  g.count = 1;
+  g.rows = M;
+  g.e[0].q_in = q;
+  g.e[0].qscale_in = qscale;
+  g.e[0].q4 = reg.q4;
+  g.e[0].tcorr = reg.tcorr;
+  g.e[0].cs = reg.cs;
+  g.e[0].n = n;
+  if ((st = launch_prep(g, codebook, cs)) != EXL3_OK) return st;
+  const exl3_layer L = layer_of(codes, m, n, nullptr, s_out, scales, nullptr, y);
+  return run_i8(&L, &reg, 1, K, codebook, M, cs);
+}
+
+// x of every layer rotated and quantized in one preparation kernel, then the
+// layer kernel and the output kernel over the whole group.
+exl3_status run_int8act(const exl3_layer* layers, const I8Region* reg, int count, int K, int codebook, int M,
+                        cudaStream_t cs) {
+  PrepGroup g{};
+  g.count = count;
+  g.rows = M;
+  g.rotate = 1;
+  for (int i = 0; i < count; ++i) {
+    g.e[i].x = reinterpret_cast<const __half*>(layers[i].x);
+    g.e[i].s_in = reinterpret_cast<const __half*>(layers[i].s_in);
+    g.e[i].q4 = reg[i].q4;
+    g.e[i].tcorr = reg[i].tcorr;
+    g.e[i].cs = reg[i].cs;
+    g.e[i].n = layers[i].n;
+  }
+  exl3_status st = launch_prep(g, codebook, cs);
+  if (st != EXL3_OK) return st;
+  return run_i8(layers, reg, count, K, codebook, M, cs);
 }
 
 extern "C" exl3_status exl3_gemm_int8act(const uint32_t* codes, int K, int codebook, int m, int n,
                                          const exl3_half* s_in, const exl3_half* s_out, const exl3_half* scales,
                                          int M, const exl3_half* x, exl3_half* y, void* workspace,
                                          size_t workspace_bytes, exl3_stream_t stream) {
-  exl3_status st = check_i8(codes, K, codebook, m, n, s_out, scales, M, x, y, workspace, workspace_bytes);
+  exl3_status st = check_i8(codes, K, codebook, m, n, s_out, scales, M, x, y);
   if (st != EXL3_OK) return st;
   if (s_in && !aligned16(s_in)) return EXL3_ERR_ALIGN;
-  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!workspace || workspace_bytes < i8_total(m, n, M)) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  const I8Region reg = i8_region(static_cast<char*>(workspace), zacc_offset(m), m, n, M);
+  const exl3_layer L = layer_of(codes, m, n, s_in, s_out, scales, x, y);
+  return run_int8act(&L, &reg, 1, K, codebook, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exl3_group_i8_workspace_bytes(const exl3_layer* layers, int count, int M) {
+  if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP || M < 1 || M > EXL3_MAX_BATCH) return 0;
+  size_t b = 256;  // the status word
+  for (int i = 0; i < count; ++i) {
+    if (check_shape(layers[i].m, layers[i].n) != EXL3_OK) return 0;
+    b += i8_layer_bytes(layers[i].m, layers[i].n, M);
+  }
+  return b;
+}
+
+extern "C" exl3_status exl3_gemm_int8act_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
+                                                 void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
+  exl3_status st;
+  for (int i = 0; i < count; ++i) {
+    const exl3_layer& L = layers[i];
+    if ((st = check_i8(L.codes, K, codebook, L.m, L.n, L.s_out, L.scales, M, L.x, L.y)) != EXL3_OK) return st;
+    if (L.s_in && !aligned16(L.s_in)) return EXL3_ERR_ALIGN;
+  }
+  const size_t need = exl3_group_i8_workspace_bytes(layers, count, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
   char* ws = static_cast<char*>(workspace);
-  if ((st = launch_prep(reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(s_in), true, nullptr,
-                        nullptr, nullptr, nullptr, reinterpret_cast<int32_t*>(ws + i8_q4_offset(m, M)),
-                        reinterpret_cast<int32_t*>(ws + i8_tcorr_offset(m, n, M)),
-                        reinterpret_cast<float*>(ws + i8_cs_offset(m, n, M)), M, n, codebook, cs)) != EXL3_OK)
-    return st;
-  return run_i8(codes, K, codebook, m, n, reinterpret_cast<const __half*>(s_out),
-                reinterpret_cast<const __half*>(scales), M, reinterpret_cast<__half*>(y), ws, cs);
+  I8Region reg[kMaxGroup];
+  size_t at = 256;
+  for (int i = 0; i < count; ++i) {
+    reg[i] = i8_region(ws, at, layers[i].m, layers[i].n, M);
+    at += i8_layer_bytes(layers[i].m, layers[i].n, M);
+  }
+  return run_int8act(layers, reg, count, K, codebook, M, reinterpret_cast<cudaStream_t>(stream));
 }
