@@ -44,6 +44,8 @@ using tc::tmem_dealloc;
 using tc::tmem_ld16;
 
 constexpr int kNB = kDenseNB;       // batch rows per tile (MMA N)
+// (Eight stages of 32 columns, each half an image, ran 1.6x slower: every
+// stage costs a fixed handshake on the MMA side that two MMAs do not cover.)
 constexpr int kStageK = 64;         // input columns per stage
 constexpr int kStages = 4;
 constexpr int kPrefetch = 8;  // stages of operand A requested into L2 ahead of use
