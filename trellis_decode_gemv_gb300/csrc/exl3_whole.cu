@@ -12,9 +12,11 @@
 //   y  = binary16(H_B-across(u) / sqrt(B)) over the m outputs.
 // Each wrapper step adds one binary16 rounding of an intermediate vector.
 //
-// rht_whole_kernel: one CTA per row, the row in shared memory as fp32; an
-// optional blockwise stage (one warp per 128-block, shuffle butterflies), then
-// the butterflies across blocks at spans 128, 256, ..., d / 2.
+// rht_whole_kernel (the standalone transform): one CTA per row, the row in
+// shared memory as fp32; the blockwise stage (one warp per 128-block, shuffle
+// butterflies), then the butterflies across blocks at spans 128, ..., d / 2.
+// rht_cross_kernel (the layer's two wrapper steps): the butterflies across
+// blocks only, eight CTAs per row.
 #include "exl3_device.cuh"
 #include "exl3_host.cuh"
 
@@ -27,51 +29,26 @@ constexpr int kWholeMax = 32768;  // fp32 row in 128 KB of shared memory
 
 __global__ void __launch_bounds__(kWholeThreads)
     rht_whole_kernel(const __half* __restrict__ in, const __half* __restrict__ signs,
-                     __half* __restrict__ out, int d, int blockwise, float scale, __half* __restrict__ ones,
-                     int ones_len) {
+                     __half* __restrict__ out, int d, float scale) {
   extern __shared__ float u[];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const size_t row = blockIdx.x;
   const __half* src = in + row * d;
-  if (blockwise) {
-    // one warp per 128-block: signs, 128-point butterflies, into shared memory
-    for (int kb = warp; kb < d / kRowBlock; kb += kWholeThreads / 32) {
-      const int col = kb * kRowBlock + 4 * lane;
-      const uint2 xr = *reinterpret_cast<const uint2*>(src + col);
-      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
-      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
-      float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-      if (signs != nullptr) {
-        const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
-        const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-        const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-        v[0] *= __low2float(s01);
-        v[1] *= __high2float(s01);
-        v[2] *= __low2float(s23);
-        v[3] *= __high2float(s23);
-      }
-      fwht128_warp(v, lane);
-      *reinterpret_cast<float4*>(&u[col]) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  } else {
-    for (int i = 4 * tid; i < d; i += 4 * kWholeThreads) {
-      const uint2 xr = *reinterpret_cast<const uint2*>(src + i);
-      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
-      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
-      float v[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
-      if (signs != nullptr) {
-        const uint2 sr = *reinterpret_cast<const uint2*>(signs + i);
-        const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-        const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-        v[0] *= __low2float(s01);
-        v[1] *= __high2float(s01);
-        v[2] *= __low2float(s23);
-        v[3] *= __high2float(s23);
-      }
-      *reinterpret_cast<float4*>(&u[i]) = make_float4(v[0], v[1], v[2], v[3]);
-    }
+  // one warp per 128-block: signs, 128-point butterflies, into shared memory
+  for (int kb = warp; kb < d / kRowBlock; kb += kWholeThreads / 32) {
+    const int col = kb * kRowBlock + 4 * lane;
+    const uint2 xr = *reinterpret_cast<const uint2*>(src + col);
+    const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+    const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+    const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+    float v[4] = {__low2float(x01) * __low2float(s01), __high2float(x01) * __high2float(s01),
+                  __low2float(x23) * __low2float(s23), __high2float(x23) * __high2float(s23)};
+    fwht128_warp(v, lane);
+    *reinterpret_cast<float4*>(&u[col]) = make_float4(v[0], v[1], v[2], v[3]);
   }
   __syncthreads();
   // butterflies across 128-blocks: pair (i, i + h) for every i with bit h clear
@@ -94,23 +71,79 @@ __global__ void __launch_bounds__(kWholeThreads)
     o.y = *reinterpret_cast<const uint32_t*>(&o23);
     *reinterpret_cast<uint2*>(out + row * d + i) = o;
   }
+}
+
+// The transform across the 128-blocks alone, spread over CTAs: CTA (row, c)
+// takes within-block columns 16c .. 16c + 15 of every block of the row (the
+// butterflies across blocks never mix columns), so a row of any length uses
+// eight CTAs.  out = binary16(H_B-across(signs (.) in) * scale), B = d / 128.
+constexpr int kCrossCols = 16;
+constexpr int kCrossThreads = 256;
+
+__global__ void __launch_bounds__(kCrossThreads)
+    rht_cross_kernel(const __half* __restrict__ in, const __half* __restrict__ signs, __half* __restrict__ out,
+                     int d, float scale, __half* __restrict__ ones, int ones_len) {
+  __shared__ float u[(kWholeMax / kRowBlock) * kCrossCols];
+  const int nb = d / kRowBlock;
+  const size_t row = blockIdx.x;
+  const int c0 = blockIdx.y * kCrossCols;
+  const int tid = threadIdx.x;
+  // element e of this CTA: block e / 16, column c0 + e % 16
+  for (int e2 = tid; e2 < nb * kCrossCols / 2; e2 += kCrossThreads) {
+    const int e = 2 * e2;
+    const int col = (e / kCrossCols) * kRowBlock + c0 + (e % kCrossCols);
+    const __half2 x = *reinterpret_cast<const __half2*>(in + row * d + col);
+    float a = __low2float(x), b = __high2float(x);
+    if (signs != nullptr) {
+      const __half2 sg = *reinterpret_cast<const __half2*>(signs + col);
+      a *= __low2float(sg);
+      b *= __high2float(sg);
+    }
+    u[e] = a;
+    u[e + 1] = b;
+  }
+  __syncthreads();
+  for (int h = 1; h < nb; h <<= 1) {
+    for (int q = tid; q < nb / 2 * kCrossCols; q += kCrossThreads) {
+      const int pr = q / kCrossCols;  // pair of blocks (b, b + h), bit h of b clear
+      const int j = q % kCrossCols;
+      const int b = (pr / h) * 2 * h + (pr % h);
+      const float x0 = u[b * kCrossCols + j];
+      const float x1 = u[(b + h) * kCrossCols + j];
+      u[b * kCrossCols + j] = x0 + x1;
+      u[(b + h) * kCrossCols + j] = x0 - x1;
+    }
+    __syncthreads();
+  }
+  for (int e2 = tid; e2 < nb * kCrossCols / 2; e2 += kCrossThreads) {
+    const int e = 2 * e2;
+    const int col = (e / kCrossCols) * kRowBlock + c0 + (e % kCrossCols);
+    *reinterpret_cast<__half2*>(out + row * d + col) = __floats2half2_rn(u[e] * scale, u[e + 1] * scale);
+  }
+  // the CTAs of row 0 also write the inner layer's unit signs
   if (ones != nullptr && blockIdx.x == 0)
-    for (int i = tid; i < ones_len; i += kWholeThreads) ones[i] = __float2half_rn(1.0f);
+    for (int i = blockIdx.y * kCrossThreads + tid; i < ones_len; i += gridDim.y * kCrossThreads)
+      ones[i] = __float2half_rn(1.0f);
+}
+
+exl3_status launch_rht_cross(const __half* in, const __half* signs, __half* out, int rows, int d, __half* ones,
+                             int ones_len, cudaStream_t stream) {
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(d / kRowBlock)));
+  rht_cross_kernel<<<dim3(static_cast<unsigned>(rows), kRowBlock / kCrossCols), kCrossThreads, 0, stream>>>(
+      in, signs, out, d, scale, ones, ones_len);
+  return launch_status();
 }
 
 bool whole_length(int d) { return d >= kRowBlock && d <= kWholeMax && (d & (d - 1)) == 0; }
 
-exl3_status launch_rht_whole(const __half* in, const __half* signs, __half* out, int rows, int d, bool blockwise,
-                             __half* ones, int ones_len, cudaStream_t stream) {
+exl3_status launch_rht_whole(const __half* in, const __half* signs, __half* out, int rows, int d,
+                             cudaStream_t stream) {
   const size_t smem = sizeof(float) * static_cast<size_t>(d);
   if (cudaFuncSetAttribute(rht_whole_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(sizeof(float) * kWholeMax)) != cudaSuccess)
     return EXL3_ERR_CUDA;
-  // 1/sqrt of the transform length covered here (d, or d / 128 across blocks)
-  const double len = blockwise ? static_cast<double>(d) : static_cast<double>(d / kRowBlock);
-  const float scale = static_cast<float>(1.0 / sqrt(len));
-  rht_whole_kernel<<<rows, kWholeThreads, smem, stream>>>(in, signs, out, d, blockwise ? 1 : 0, scale, ones,
-                                                          ones_len);
+  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+  rht_whole_kernel<<<rows, kWholeThreads, smem, stream>>>(in, signs, out, d, scale);
   return launch_status();
 }
 
@@ -129,8 +162,7 @@ extern "C" exl3_status exl3_rht_whole(const exl3_half* in, const exl3_half* sign
   if (!in || !signs || !out) return EXL3_ERR_NULL;
   if (!aligned16(in) || !aligned16(signs) || !aligned16(out)) return EXL3_ERR_ALIGN;
   return launch_rht_whole(reinterpret_cast<const __half*>(in), reinterpret_cast<const __half*>(signs),
-                          reinterpret_cast<__half*>(out), rows, d, true, nullptr, 0,
-                          reinterpret_cast<cudaStream_t>(stream));
+                          reinterpret_cast<__half*>(out), rows, d, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exl3_gemm_whole_workspace_bytes(int m, int n, int M) {
@@ -168,8 +200,8 @@ extern "C" exl3_status exl3_gemm_whole(const uint32_t* codes, int K, int codeboo
   const exl3_half* x_in = x;
   const exl3_half* signs_in = nullptr;
   if (s_in != nullptr) {
-    if ((st = launch_rht_whole(reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(s_in), xp, M,
-                               n, false, ones, ones_len, cs)) != EXL3_OK)
+    if ((st = launch_rht_cross(reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(s_in), xp, M, n,
+                               ones, ones_len, cs)) != EXL3_OK)
       return st;
     x_in = reinterpret_cast<const exl3_half*>(xp);
     signs_in = reinterpret_cast<const exl3_half*>(ones);
@@ -178,7 +210,6 @@ extern "C" exl3_status exl3_gemm_whole(const uint32_t* codes, int K, int codeboo
   if ((st = exl3_gemm(codes, K, codebook, m, n, signs_in, s_out, scales, M, x_in, y_inner, workspace, inner,
                       stream)) != EXL3_OK)
     return st;
-  if (s_out != nullptr)
-    return launch_rht_whole(up, nullptr, reinterpret_cast<__half*>(y), M, m, false, nullptr, 0, cs);
+  if (s_out != nullptr) return launch_rht_cross(up, nullptr, reinterpret_cast<__half*>(y), M, m, nullptr, 0, cs);
   return EXL3_OK;
 }
