@@ -179,3 +179,17 @@ def test_prefill_passes_repeated_1mad_block_sums():
             assert np.all(row_err <= 5e-3), (i, np.nonzero(row_err > 5e-3)[0][:8])
     finally:
         B.exl3_set_path(B.PATH_AUTO)
+
+
+def test_prefill_two_rounds_of_units():
+    """228 units (76 row blocks x 3 tiles) over 152 CTAs: two rounds, the
+    second partial; every output checked, scratch left at zero, workspace
+    reused."""
+    m, n, K, cb, M = 9728, 2048, 2, 1, 600
+    inp = synth.layer_inputs(m, n, K, M, config=87, index=0)
+    ref = _ref(inp, K, cb, m, n)
+    y, ws = _run(inp, K, cb, m, n, M)
+    assert_layer_close(y, ref, "tail split")
+    y2, _ = _run(inp, K, cb, m, n, M, ws)
+    assert_layer_close(y2, ref, "tail split, workspace reused")
+    _dense_scratch_left_zero(ws, m, n, M)

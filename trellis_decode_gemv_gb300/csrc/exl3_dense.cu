@@ -3,15 +3,16 @@
 // images ("decode a block once and reuse it", "Trellis Quantization" Part
 // fourteen) and x-tilde in operand-B images of 256 batch rows per tile.
 //
-// Persistent, one CTA per SM.  A work unit is one 128-row output block x one
-// K split (1/split of the input columns) x one tile of 256 batch rows; units
-// are numbered (block, split, tile) with the tile fastest, so CTAs that run
-// at the same time share their operand-A stream in L2, and CTA b takes units
-// b, b + gridDim.x, ...  With split == 1 a unit's D (128 x 256 fp32 in TMEM)
-// is the finished z of its block and the epilogue applies the scale, the
-// output signs and the 128-point FWHT and writes y; with split > 1 it adds D
-// to the fp32 row sums zacc [M][m], and the unit that completes the block's
-// sums (an arrival counter per block and tile) finishes it from zacc.
+// Persistent, one CTA per SM.  A unit is one 128-row output block x one tile
+// of 256 batch rows, numbered with the tile fastest so that CTAs that run at
+// the same time share their operand-A stream in L2; CTA b takes work items b,
+// b + gridDim.x, ...  Whole units come first; the units of the last partial
+// round (all units when there are fewer than SMs) are split in K so that
+// they fill the SMs.  A whole unit's D (128 x 256 fp32 in TMEM) is the
+// finished z of its block: the epilogue applies the scale, the output signs
+// and the 128-point FWHT and writes y.  A split item adds D to the fp32 row
+// sums zacc [M][m], and the item that completes the block's sums (an arrival
+// counter per block and tile) finishes it from zacc.
 //
 // Warp roles: warps 0-3 and 6-9 epilogue (TMEM lane quarter = warp % 4), warp
 // 4 MMA issue and TMEM allocation (one lane issues), warp 5 producer (one lane:
@@ -72,23 +73,39 @@ struct DenseParams {
   uint32_t* status;
   int m, n, M;
   int tiles;        // ceil(M / 256)
-  int split;        // K splits per output block
-  int units;        // (m / 128) * split * tiles
+  int full;         // work items 0 .. full - 1: whole (block, tile) units over all of K
+  int rem;          // the units after those, each split in `split` K ranges
+  int split;
+  int units;        // work items: full + rem * split
   int debug_stall;  // test hook: the producer posts nothing
 };
 
 struct Unit {
   int rb, t, ks0, ks1;  // output block, batch tile, stage range [ks0, ks1)
+  int split;            // K ranges of this (block, tile): 1 = the item finishes it
 };
 
-__device__ __forceinline__ Unit unit_of(const DenseParams& p, int u, int nstage) {
+// Work item i.  Units (block, tile) are numbered tile fastest.  The first
+// `full` items are whole units; the last partial round of units is split in
+// K, split index major, so that the CTAs that run together still share
+// operand-A streams.
+__device__ __forceinline__ Unit unit_of(const DenseParams& p, int i, int nstage) {
   Unit w;
-  w.t = u % p.tiles;
-  const int q = u / p.tiles;
-  const int s = q % p.split;
-  w.rb = q / p.split;
-  w.ks0 = s * nstage / p.split;
-  w.ks1 = (s + 1) * nstage / p.split;
+  int q, s;
+  if (i < p.full) {
+    q = i;
+    s = 0;
+    w.split = 1;
+  } else {
+    const int f = i - p.full;
+    s = f / p.rem;
+    q = p.full + (f - s * p.rem);
+    w.split = p.split;
+  }
+  w.t = q % p.tiles;
+  w.rb = q / p.tiles;
+  w.ks0 = s * nstage / w.split;
+  w.ks1 = (s + 1) * nstage / w.split;
   return w;
 }
 
@@ -284,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       const int rb = w.rb;
       const int t = w.t;
       const int rows = p.M - t * kNB < kNB ? p.M - t * kNB : kNB;  // batch rows of this tile
-      const bool finish = p.split == 1;
+      const bool finish = w.split == 1;
       const int db = li & 1;
       const bool ok = !aborted(sh) && mbar_wait(&sh.d_full[db], (li >> 1) & 1);
       if (!ok) set_abort(sh);
@@ -347,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       __threadfence();
       epi_sync();
       uint32_t* cnt = p.cnt + static_cast<size_t>(rb) * p.tiles + t;
-      if (tid == 0) sh.last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(p.split - 1) ? 1u : 0u;
+      if (tid == 0) sh.last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(w.split - 1) ? 1u : 0u;
       epi_sync();
       if (sh.last == 0u) continue;
       __threadfence();
@@ -388,7 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
 }  // namespace dense
 
 int choose_dense_split(int units, int nstage, int grid) {
-  int s = units >= grid ? 1 : grid / units;
+  // Splitting only the last partial round after whole rounds (224 units on
+  // 152 SMs: 72 units in two K ranges) measured no faster: the partial sums'
+  // reductions and the second pass cost what the idle SMs would have.  So
+  // split only when there are fewer units than SMs.
+  if (units >= grid) return 1;
+  const int rem = units;
+  int s = grid / rem;
   if (s > nstage / 16) s = nstage / 16;
   if (s > 16) s = 16;
   return s < 1 ? 1 : s;
@@ -412,15 +435,19 @@ exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __
   p.n = n;
   p.M = M;
   p.tiles = (M + kNB - 1) / kNB;
+  const int units = (m / kRowBlock) * p.tiles;
+  const int sms = device_sm_count();
   p.split = split;
-  p.units = (m / kRowBlock) * split * p.tiles;
+  p.rem = split > 1 ? units % sms : 0;
+  p.full = units - p.rem;
+  p.units = p.full + p.rem * split;
   p.debug_stall = debug_stall;
   const size_t ctrl = (sizeof(DenseShared) + 1023) & ~static_cast<size_t>(1023);
   const size_t smem = ctrl + static_cast<size_t>(kStages) * kStageBytes;
   if (cudaFuncSetAttribute(dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return EXL3_ERR_CUDA;
-  int grid = device_sm_count();
+  int grid = sms;
   if (grid > p.units) grid = p.units;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -252,11 +252,12 @@ inline size_t dense_total(int m, int n, int M) {
   return dense_cnt_offset(m, n, M) +
          align256(sizeof(uint32_t) * static_cast<size_t>(m / kRowBlock) * dense_tiles(M));
 }
-// K splits of the dense kernel: with fewer work units than CTAs, the largest
-// s with units * s <= grid (every fragment in the first and only round) and at
-// least 16 stages of 64 columns per fragment, at most 16; else 1.  A split
-// costs its partial sums' L2 reductions and a second pass over the block, so
-// it only pays where it fills idle SMs.
+// K splits of the dense kernel: with fewer units than CTAs, the largest s
+// with units * s <= grid, at least 16 stages of 64 columns per split, at most
+// 16; else 1.  A split costs its partial sums' L2 reductions and a second
+// pass over the block, so it is used only where it fills idle SMs.  (The
+// kernel can also split just the last partial round after whole rounds; that
+// measured no faster.)
 int choose_dense_split(int units, int nstage, int grid);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
 // per 128-row block (no rotation when s_out is NULL); zeroes zacc.
