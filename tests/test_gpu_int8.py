@@ -113,3 +113,34 @@ def test_int8act_grouped_matches_the_oracle_per_layer(M):
         y1 = B.exl3_gemm_int8act(L["codes"], K, cb, L["m"], L["n"], L["s_in"], L["s_out"], L["scales"], L["x"])
         torch.cuda.synchronize()
         assert float((y1.float() - L["y"].float()).abs().max()) <= 2.0 ** -9 * float(y1.float().abs().max())
+
+
+def test_int8act_without_rotations():
+    """s_in and s_out absent: x itself is quantized, no output transform."""
+    m, n, K, cb, M = 512, 1024, 3, 1, 2
+    inp = synth.layer_inputs(m, n, K, M, config=88, index=0)
+    d = upload(inp)
+    y = B.exl3_gemm_int8act(d["codes"], K, cb, m, n, None, None, d["scales"], d["x"])
+    torch.cuda.synchronize()
+    q, qs = O.quantize_act(inp["x"])
+    ref = O.layer_forward_int8(inp["codes"], K, cb, m, n, None, inp["scales"], q, qs)
+    assert_layer_close(y, ref, "no rotation")
+
+
+def test_int8act_grouped_batch_32():
+    """32 rows: four batch chunks of eight through the grouped call."""
+    K, cb, M = 2, 1, 32
+    shapes = [(256, 512), (128, 512)]
+    layers, refs = [], []
+    for i, (m, n) in enumerate(shapes):
+        inp = synth.layer_inputs(m, n, K, M, config=89, index=i)
+        d = upload(inp)
+        layers.append(dict(codes=d["codes"], m=m, n=n, s_in=d["s_in"], s_out=d["s_out"], scales=d["scales"],
+                           x=d["x"], y=torch.empty((M, m), dtype=torch.float16, device="cuda")))
+        xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+        q, qs = O.quantize_act(xt)
+        refs.append(O.layer_forward_int8(inp["codes"], K, cb, m, n, inp["s_out"], inp["scales"], q, qs))
+    B.exl3_gemm_int8act_grouped(layers, K, cb)
+    torch.cuda.synchronize()
+    for L, ref in zip(layers, refs):
+        assert_layer_close(L["y"], ref, f"grouped M=32 {L['m']}x{L['n']}")

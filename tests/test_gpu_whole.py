@@ -81,3 +81,12 @@ def test_gemm_whole_4096_square_batch1():
     inp = synth.layer_inputs(m, n, K, M, config=64, index=0)
     y, ref = _layer(inp, K, cb, m, n)
     assert_layer_close(y, ref, "4096x4096 whole")
+
+
+def test_gemm_whole_extreme_lengths():
+    """The longest input (32768: 256 blocks across) into the shortest output
+    (128: nothing across), every output checked."""
+    m, n, K, cb, M = 128, 32768, 2, 0, 2
+    inp = synth.layer_inputs(m, n, K, M, config=65, index=0)
+    y, ref = _layer(inp, K, cb, m, n)
+    assert_layer_close(y, ref, "128 x 32768")
