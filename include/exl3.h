@@ -28,8 +28,8 @@
  *
  * Conventions:
  *   - Ownership: every pointer is caller-owned device memory; the library
- *     allocates, frees and synchronizes nothing, and keeps no per-call global
- *     state.  Calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     allocates, frees and synchronizes nothing (exl3_device_status, which
+ *     waits for the stream, excepted), and keeps no per-call global state.  Calls are asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).
  *   - Validation happens on the host before anything is launched; on any
  *     error nothing is launched and the outputs are untouched:
@@ -72,8 +72,6 @@ typedef enum {
   EXL3_ERR_SCRATCH = 10
 } exl3_status;
 
-/** Computed codes of Lecture 1b Part nine.  Ids 2 (MCG) and 3 (mul1) are
- *  reserved and rejected with EXL3_ERR_CODEBOOK. */
 /** Computed codes ("Trellis Quantization" Parts nine, eleven and twelve):
  *  3INST and 1MAD on the LCG x = A*s + B; MCG (3INST on the multiplicative
  *  generator x = A*s) and mul1 (six-bit masked byte sum of A*s, minus 126,
@@ -389,6 +387,18 @@ exl3_status exl3_set_path(int path);
  * unbounded wait is involved.  Process-wide, like exl3_set_path.
  */
 exl3_status exl3_debug_stall_tensor_wait(int on);
+
+/**
+ * The one call that waits: reads the status word at device address
+ * `status_word` once the work queued on `stream` so far has finished
+ * (byte 4*(m/128) of an exl3_workspace_bytes / exl3_gemm_workspace_bytes /
+ * exl3_gemm_whole_workspace_bytes workspace, byte 0 of a group's).  Returns
+ * EXL3_OK if it is 0, EXL3_ERR_DEVICE_CHECK if a device-side wait of a
+ * preceding call timed out (see exl3_debug_stall_tensor_wait), EXL3_ERR_NULL
+ * for a NULL address, EXL3_ERR_CUDA if the copy or the synchronization
+ * fails.  The word is left as it is.
+ */
+exl3_status exl3_device_status(const void *status_word, exl3_stream_t stream);
 
 /** Size of the fixed device array that exl3_gemv_noalloc uses as scratch. */
 #define EXL3_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -241,3 +241,7 @@ def test_int8_group_workspace_and_validation(lib):
     assert B.exl3_group_i8_workspace_bytes(shapes, 33) == 0
     assert B.exl3_group_i8_workspace_bytes(shapes * 3, 1) == 0  # more than four layers
     assert lib.exl3_gemm_int8act_grouped(None, 1, 2, 1, 1, A, 1 << 30, None) == 1
+
+
+def test_device_status_rejects_null(lib):
+    assert lib.exl3_device_status(None, None) == 1

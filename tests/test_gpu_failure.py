@@ -43,6 +43,7 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
             B.exl3_debug_stall_tensor_wait(False)
         print(f"stalled call returned after {elapsed:.3f} s")
         assert B.workspace_status(ws, m) == 1
+        assert B.exl3_device_status(ws, 4 * (m // 128)) == 9  # EXL3_ERR_DEVICE_CHECK
         assert elapsed < 60.0
         # the row sums were left at zero by the output kernel
         zacc = ws[256:256 + 4 * M * m].view(torch.float32)
@@ -52,6 +53,7 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
         ws[off:off + 4].zero_()
         y = _call(d, K, cb, m, n, M, ws)
         assert B.workspace_status(ws, m) == 0
+        assert B.exl3_device_status(ws, 4 * (m // 128)) == 0
         ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
         assert_layer_close(y, ref, "after a timed-out call")
     finally:

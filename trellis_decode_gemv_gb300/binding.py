@@ -79,6 +79,7 @@ _SIGNATURES = {
     "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_set_path": ([_I], _I),
     "exl3_debug_stall_tensor_wait": ([_I], _I),
+    "exl3_device_status": ([_P, _P], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
     "exl3_version": ([], ctypes.c_char_p),
 }
@@ -158,6 +159,17 @@ def exl3_set_path(path: int) -> None:
 def exl3_debug_stall_tensor_wait(on: bool) -> None:
     """Failure-detection test hook of the tensor-core kernel (see the header)."""
     _check(load_library().exl3_debug_stall_tensor_wait(1 if on else 0))
+
+
+def exl3_device_status(workspace: torch.Tensor, offset: int) -> int:
+    """The library's check of the status word at byte `offset` of a workspace:
+    0 (EXL3_OK) or 9 (EXL3_ERR_DEVICE_CHECK).  Waits for the current stream."""
+    lib = load_library()
+    dev = workspace.device
+    st = lib.exl3_device_status(_ptr(workspace, "workspace", (torch.uint8,), dev) + offset, _stream(dev))
+    if st not in (0, 9):
+        _check(st)
+    return st
 
 
 def workspace_status(workspace: torch.Tensor, m: int) -> int:

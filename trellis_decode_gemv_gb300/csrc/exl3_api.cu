@@ -182,6 +182,16 @@ extern "C" exl3_status exl3_set_path(int path) {
   return EXL3_OK;
 }
 
+extern "C" exl3_status exl3_device_status(const void* status_word, exl3_stream_t stream) {
+  if (status_word == nullptr) return EXL3_ERR_NULL;
+  uint32_t word = 0;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, status_word, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return EXL3_ERR_CUDA;
+  return word == 0u ? EXL3_OK : EXL3_ERR_DEVICE_CHECK;
+}
+
 extern "C" exl3_status exl3_debug_stall_tensor_wait(int on) {
   g_debug_stall.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
   return EXL3_OK;
