@@ -54,17 +54,19 @@ __global__ void __launch_bounds__(kThreads)
 
 // Operand B images of the tensor-core kernels.  The M batch rows form tiles of
 // nb rows; tile t's image starts at half offset t * nb * n.  One warp per
-// (four consecutive batch rows, 128-column block kb): x-tilde = Hb(s_in (.) x) of that block (x
-// itself without s_in), rounded to binary16 and stored in the canonical
+// (R consecutive batch rows, 128-column block kb): x-tilde = Hb(s_in (.) x) of
+// that block (x itself without s_in), rounded to binary16 and stored in the canonical
 // K-major no-swizzle layout of an nb x 128 operand: element (r, k), r the row
 // within its tile, at half offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) *
 // 8 + k % 8 of the block's image at kb * nb * 128.  Rows past M are zero.
 // With bsum, also the fp32 sum of the block's binary16 values.  The MMA
 // kernels are programmatic dependents of this one and wait for it before
 // reading the images.
-constexpr int kBimgRows = 4;  // batch rows per warp (independent loads in flight)
-
-__global__ void __launch_bounds__(kSmallThreads, 16)
+// R batch rows per warp: 4 for the dense kernel's 256-row tiles (independent
+// loads in flight), 1 for the small tiles of the skinny tensor-core kernel
+// (more warps, shortest latency to the MMA kernel waiting for it).
+template <int R>
+__global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
                 __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -72,13 +74,13 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
   const int nkb = n / kRowBlock;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   const int tiles = (M + nb - 1) / nb;
-  if (job >= static_cast<long long>(tiles) * (nb / kBimgRows) * nkb) return;
-  const int g0 = kBimgRows * static_cast<int>(job / nkb);  // first batch row (nb is a multiple of 4)
-  const int kb = static_cast<int>(job - static_cast<long long>(g0 / kBimgRows) * nkb);
+  if (job >= static_cast<long long>(tiles) * (nb / R) * nkb) return;
+  const int g0 = R * static_cast<int>(job / nkb);  // first batch row (nb is a multiple of R)
+  const int kb = static_cast<int>(job - static_cast<long long>(g0 / R) * nkb);
   const int col = kb * kRowBlock + 4 * lane;
-  uint2 xr[kBimgRows];
+  uint2 xr[R];
 #pragma unroll
-  for (int i = 0; i < kBimgRows; ++i)
+  for (int i = 0; i < R; ++i)
     xr[i] = g0 + i < M ? *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g0 + i) * n + col)
                        : make_uint2(0u, 0u);
   float s[4] = {1.f, 1.f, 1.f, 1.f};
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(kSmallThreads, 16)
     s[3] = __high2float(s23);
   }
 #pragma unroll
-  for (int i = 0; i < kBimgRows; ++i) {
+  for (int i = 0; i < R; ++i) {
     const int g = g0 + i;  // batch row
     const int tile = g / nb;
     const int r = g - tile * nb;  // row within its tile
@@ -340,10 +342,14 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * (nb / kBimgRows) * (n / kRowBlock);
+  const int R = nb >= 128 ? 4 : 1;
+  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * (nb / R) * (n / kRowBlock);
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  bimg_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  if (R == 4)
+    bimg_kernel<4><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  else
+    bimg_kernel<1><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
 }
 
