@@ -766,8 +766,14 @@ def run_encode(args):
             flush=True)
         return 0
     import torch
+    import torch.distributed as dist
     from trellis_decode_gemv_gb300 import binding as B
-    dev = torch.device("cuda", 0)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:  # one replica per GPU; the ranks meet only at the barriers
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
     hbm_gbs, sm_max_mhz, _, peak_src = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -789,6 +795,7 @@ def run_encode(args):
     clocks = ClockSampler(getattr(props, "pci_bus_id", None) if isinstance(getattr(props, "pci_bus_id", None), str)
                           else None)
     clocks.start()
+    barrier()
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -798,9 +805,11 @@ def run_encode(args):
             step()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
+    barrier()
     clk = clocks.stop()
-    ms_step = ev0.elapsed_time(ev1) / steps
-    value = weights_step / (ms_step / 1e3)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    ms_step = ms_total / steps
+    value = whole_job_rate(weights_step, world, steps, ms_total / 1e3)
     mse = float(cost.double().sum()) / weights_step / sigma ** 2
     # FP32 candidate work: 2 passes x 256 steps x 2^16 states x (sub, mul, add, compare)
     ops_step = ENCODE_TILES * 2 * 256 * (1 << 16) * 4
@@ -823,13 +832,16 @@ def run_encode(args):
             ch.copy_(cost, non_blocking=True)
             stream.synchronize()
         t_e2e = time.perf_counter() - t0
+    t_e2e = max_over_ranks(t_e2e, dev)
     cpu = None
-    if not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, dt = encode_oracle_timed(target, K, cb, target_s=12.0)
         cpu = {"value": n * 256 / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} whole tiles of the workload ({dt:.1f} s), oracle binary32 encoder"}
+    if rank != 0:
+        return 0
     print(json.dumps({
-        "metric": ENCODE_METRIC, "value": value, "unit": "weights/s", "n_gpus": 1, "steps": steps,
+        "metric": ENCODE_METRIC, "value": value, "unit": "weights/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "tiles": ENCODE_TILES,
@@ -841,7 +853,7 @@ def run_encode(args):
                      "kernel": "encode_kernel (one CTA per tile, binary32 path costs)",
                      "ops_note": "2 passes x 256 steps x 65536 states x 4 ops (sub, mul, add, compare) per tile"},
         "cpu_baseline": cpu,
-        "e2e": {"value": weights_step * e2e_steps / t_e2e, "unit": "weights/s",
+        "e2e": {"value": whole_job_rate(weights_step, world, e2e_steps, t_e2e), "unit": "weights/s",
                 "h2d_bytes_per_step": target.nbytes, "d2h_bytes_per_step": words.numel() * 4 + cost.numel() * 4},
         "clocks": clk, "gpu_launches": steps}), flush=True)
     return 0
