@@ -62,9 +62,9 @@ __global__ void __launch_bounds__(kThreads)
 // With bsum, also the fp32 sum of the block's binary16 values.  The MMA
 // kernels are programmatic dependents of this one and wait for it before
 // reading the images.
-// R batch rows per warp: 4 for the dense kernel's 256-row tiles (independent
-// loads in flight), 1 for the small tiles of the skinny tensor-core kernel
-// (more warps, shortest latency to the MMA kernel waiting for it).
+// R batch rows per warp (the launcher uses R = 1, for the small tiles of the
+// skinny tensor-core kernel: many warps, the shortest latency to the MMA
+// kernel waiting for it; tiles of 128 rows and more use bimg8_kernel below).
 template <int R>
 __global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
@@ -126,6 +126,85 @@ __global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
     const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
                        (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
     *reinterpret_cast<uint2*>(bimg + off) = o;
+  }
+}
+
+// The same images for tiles of at least 128 rows, eight rows per warp: the
+// eight rows of one 8-row group give, per 8-column group, one whole 128-byte
+// run of the image, so the warp regroups its rows through shared memory and
+// each store instruction writes four whole runs (per-row stores would write
+// every 32-byte sector in two halves).
+__global__ void __launch_bounds__(kSmallThreads, 8)
+    bimg8_kernel(const __half* __restrict__ x, const __half* __restrict__ signs, __half* __restrict__ bimg,
+                 float* __restrict__ bsum, int M, int nb, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ uint2 runs[kSmallThreads / 32][16 * 8 * 2];  // [8-column group][row][half of the group]
+  const int lane = threadIdx.x & 31;
+  uint2* run = runs[threadIdx.x >> 5];
+  const int nkb = n / kRowBlock;
+  const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
+  const int tiles = (M + nb - 1) / nb;
+  if (job >= static_cast<long long>(tiles) * (nb / 8) * nkb) return;
+  const int g0 = 8 * static_cast<int>(job / nkb);  // first of eight batch rows, one 8-row group
+  const int kb = static_cast<int>(job - static_cast<long long>(g0 / 8) * nkb);
+  const int col = kb * kRowBlock + 4 * lane;
+  uint2 xr[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    xr[i] = g0 + i < M ? *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g0 + i) * n + col)
+                       : make_uint2(0u, 0u);
+  float s[4] = {1.f, 1.f, 1.f, 1.f};
+  if (signs != nullptr) {
+    const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+    s[0] = __low2float(s01);
+    s[1] = __high2float(s01);
+    s[2] = __low2float(s23);
+    s[3] = __high2float(s23);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int g = g0 + i;
+    uint2 o = make_uint2(0u, 0u);
+    if (g < M) {  // warp-uniform
+      if (signs != nullptr) {
+        const __half2 x01 = *reinterpret_cast<const __half2*>(&xr[i].x);
+        const __half2 x23 = *reinterpret_cast<const __half2*>(&xr[i].y);
+        float v[4] = {__low2float(x01) * s[0], __high2float(x01) * s[1], __low2float(x23) * s[2],
+                      __high2float(x23) * s[3]};
+        fwht128_warp(v, lane);
+        const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
+        const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
+        o.x = *reinterpret_cast<const uint32_t*>(&o01);
+        o.y = *reinterpret_cast<const uint32_t*>(&o23);
+      } else {
+        o = xr[i];
+      }
+      if (bsum != nullptr) {
+        const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
+        const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
+        float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
+        if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
+      }
+    }
+    // this lane's columns 4 * lane .. + 3 are half (lane % 2) of 8-column group lane / 2
+    run[((lane / 2) * 8 + i) * 2 + (lane % 2)] = o;
+  }
+  __syncwarp();
+  // run kg (rows 0..7 of the group, 16 bytes each) lies at half offset
+  // (kg * (nb / 8) + r / 8) * 64 of the block image, r the group's first row
+  const int tile = g0 / nb;
+  const int r = g0 - tile * nb;
+  __half* img = bimg + static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock;
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int c = 32 * st + lane;  // 16-byte piece: run c / 8, row c % 8
+    const int kg = c / 8;
+    const uint4 v = *reinterpret_cast<const uint4*>(&run[2 * c]);
+    *reinterpret_cast<uint4*>(img + (static_cast<size_t>(kg) * (nb / 8) + r / 8) * 64 + (c % 8) * 8) = v;
   }
 }
 
@@ -342,12 +421,12 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
-  const int R = nb >= 128 ? 4 : 1;
+  const int R = nb >= 128 ? 8 : 1;
   const long long blocks = static_cast<long long>((M + nb - 1) / nb) * (nb / R) * (n / kRowBlock);
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  if (R == 4)
-    bimg_kernel<4><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  if (R == 8)
+    bimg8_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   else
     bimg_kernel<1><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
