@@ -567,7 +567,7 @@ def run_ours(args):
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
     elif dense:
-        kname = ("dense_kernel (tcgen05 128x256x16 MMAs, both operands in shared memory) + "
+        kname = ("dense_kernel (tcgen05 128xNx16 MMAs, N = 64/128/256 by batch, both operands in shared memory) + "
                  "decode-to-operand-image, operand-B and output kernels")
     elif tensor:
         kname = "tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"

@@ -153,7 +153,8 @@ exl3_status exl3_gemm_small(const uint32_t *codes, int K, int codebook, int m, i
  * M <= EXL3_MAX_BATCH; above, enough for either prefill strategy: the
  * counters and status word, fp32 row sums [M][m], the rotated x as operand
  * images (M rounded up to 256 rows, times n binary16), the decoded matrix
- * (m * n binary16) and one uint32 per (128-row block, 256-row batch tile).
+ * (m * n binary16) and one uint32 per (128-row block, 256-row batch tile);
+ * batches of up to 128 rows run as one narrower tile inside these regions.
  * Same zero-fill contract and status word as exl3_workspace_bytes.  0 for an
  * invalid shape or M < 1.
  */
@@ -163,8 +164,9 @@ size_t exl3_gemm_workspace_bytes(int m, int n, int M);
  * The layer for any batch M >= 1 (prefill): x [M][n] -> y [M][m].  Up to
  * EXL3_MAX_BATCH rows this is exl3_gemm_small.  Above, by default, the matrix
  * is decoded once per call into binary16 in the workspace and a dense
- * tcgen05 GEMM (128 x 256 x 16 MMAs, both operands in shared memory) runs
- * over all M rows ("decode a block once and reuse it", Lecture 1b Part
+ * tcgen05 GEMM (128 x N x 16 MMAs, both operands in shared memory; N = 64
+ * up to 64 rows, 128 up to 128, else tiles of 256) runs over all M rows
+ * ("decode a block once and reuse it", Lecture 1b Part
  * fourteen: at large batch the decode is amortised and the product is a
  * plain matrix multiplication).  With EXL3_PATH_TENSOR selected, passes of
  * 128 rows run the tensor-core kernel with 128 batch columns per MMA instead,

@@ -3,7 +3,8 @@ float64 layer (relative L2 <= 5e-3, |err| <= 1e-2 * max|y_ref|), for both
 prefill strategies:
 
 * dense (the default): the matrix decoded once into binary16 operand images,
-  then the dense tcgen05 kernel over tiles of 256 batch rows, finishing the
+  then the dense tcgen05 kernel over batch tiles (one tile of 64 rows up to
+  M = 64, one of 128 up to M = 128, tiles of 256 above), finishing the
   layer from tensor memory when every unit covers all of K (n < 1024 here) or
   adding partial sums of K splits, the last split finishing the block
   (n >= 1024 with few row blocks);
@@ -57,7 +58,7 @@ def _ref(inp, K, cb, m, n):
     return O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
 
 
-@pytest.mark.parametrize("M", [33, 100, 128, 129, 160, 256, 300, 513])
+@pytest.mark.parametrize("M", [33, 64, 65, 100, 128, 129, 160, 256, 300, 513])
 def test_prefill_batches(strategy, M):
     m, n, K, cb = 256, 384, 3, 1
     inp = synth.layer_inputs(m, n, K, M, config=90, index=M)
@@ -193,3 +194,17 @@ def test_prefill_two_rounds_of_units():
     y2, _ = _run(inp, K, cb, m, n, M, ws)
     assert_layer_close(y2, ref, "tail split, workspace reused")
     _dense_scratch_left_zero(ws, m, n, M)
+
+
+@pytest.mark.parametrize("M", [40, 120])
+def test_prefill_narrow_tiles_two_rounds_and_split(M):
+    """The 64- and 128-row tiles: 160 row blocks over 152 CTAs (a second,
+    partial round), then a layer of two row blocks split in K; every output
+    checked, scratch left at zero."""
+    for m, n, cfg in [(20480, 256, 0), (256, 3200, 1)]:
+        K, cb = 2, 1
+        inp = synth.layer_inputs(m, n, K, M, config=86, index=2 * M + cfg)
+        ref = _ref(inp, K, cb, m, n)
+        y, ws = _run(inp, K, cb, m, n, M)
+        assert_layer_close(y, ref, f"{m}x{n} M={M}")
+        _dense_scratch_left_zero(ws, m, n, M)

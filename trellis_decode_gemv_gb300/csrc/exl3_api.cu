@@ -454,11 +454,12 @@ exl3_status run_dense(const LayerArgs& a, int M, char* ws, cudaStream_t cs) {
   uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + dense_cnt_offset(a.m, a.n, M));
   exl3_status st = launch_decode_aimg(a.codes, a.K, a.codebook, a.m, a.n, aimg, cs);
   if (st != EXL3_OK) return st;
-  if ((st = launch_bimg(a.x, a.s_in, bimg, nullptr, M, kDenseNB, a.n, cs)) != EXL3_OK) return st;
-  const int units = (a.m / kRowBlock) * dense_tiles(M);
+  const int nb = dense_nb(M);
+  if ((st = launch_bimg(a.x, a.s_in, bimg, nullptr, M, nb, a.n, cs)) != EXL3_OK) return st;
+  const int units = (a.m / kRowBlock) * ((M + nb - 1) / nb);
   const int split = choose_dense_split(units, a.n / 64, device_sm_count());
-  return launch_dense(aimg, bimg, a.scales, a.s_out, a.y, zacc, cnt, a.m, a.n, M, split, status, a.debug_stall,
-                      cs);
+  return launch_dense(aimg, bimg, a.scales, a.s_out, a.y, zacc, cnt, a.m, a.n, M, nb, split, status,
+                      a.debug_stall, cs);
 }
 
 }  // namespace

@@ -44,22 +44,32 @@ using tc::tmem_alloc;
 using tc::tmem_dealloc;
 using tc::tmem_ld16;
 
-constexpr int kNB = kDenseNB;       // batch rows per tile (MMA N)
 // (Eight stages of 32 columns, each half an image, ran 1.6x slower: every
 // stage costs a fixed handshake on the MMA side that two MMAs do not cover.)
 constexpr int kStageK = 64;         // input columns per stage
-constexpr int kStages = 4;
 constexpr int kPrefetch = 8;  // stages of operand A requested into L2 ahead of use
 constexpr int kABytes = 128 * kStageK * 2;   // 16 KB
-constexpr int kBBytes = kNB * kStageK * 2;   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRingBytes = 192 * 1024;
+constexpr int kMaxStages = 8;
+
+// Batch rows per tile NB (the MMA's N: 64, 128 or 256): operand-B bytes per
+// stage, the ring depth that fills 192 KB (4, 6 or 8 stages) and the TMEM
+// columns of the double-buffered D.
+template <int NB>
+struct Shape {
+  static_assert(NB == 64 || NB == 128 || NB == 256, "tile width");
+  static constexpr int kBBytes = NB * kStageK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+  static constexpr int kTmemCols = 2 * NB;
+  static_assert(kStages <= kMaxStages, "ring depth");
+};
 constexpr int kThreads = 10 * 32;
 constexpr int kMmaWarp = 4;
 constexpr int kProdWarp = 5;
 constexpr int kEpiWarps = 8;  // warps 0-3 and 6-9
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kSlice = 32;          // batch columns per epilogue slice
-constexpr int kTmemCols = 512;
 constexpr int kEpiBarrier = 1;
 
 struct DenseParams {
@@ -72,7 +82,7 @@ struct DenseParams {
   uint32_t* cnt;
   uint32_t* status;
   int m, n, M;
-  int tiles;        // ceil(M / 256)
+  int tiles;        // ceil(M / NB)
   int full;         // work items 0 .. full - 1: whole (block, tile) units over all of K
   int rem;          // the units after those, each split in `split` K ranges
   int split;
@@ -110,8 +120,8 @@ __device__ __forceinline__ Unit unit_of(const DenseParams& p, int i, int nstage)
 }
 
 struct DenseShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t d_full[2];
   uint64_t d_empty[2];
   uint64_t mma_done;
@@ -167,7 +177,12 @@ __device__ __forceinline__ void finish_rows(const DenseParams& p, float4 z, cons
   *reinterpret_cast<uint2*>(p.y + b * p.m + r0) = o;
 }
 
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p) {
+  using S = Shape<NB>;
+  constexpr int kStages = S::kStages;
+  constexpr int kStageBytes = S::kStageBytes;
+  constexpr int kBBytes = S::kBBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DenseShared& sh = *reinterpret_cast<DenseShared*>(smem_raw);
   const size_t ctrl = (sizeof(DenseShared) + 1023) & ~static_cast<size_t>(1023);
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
                            ? (p.units - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                            : 0;
 
-  if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, S::kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh.full[i], 1);
@@ -214,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       for (int li = 0; li < my_units && !stop; ++li) {
         const Unit w = unit_of(p, static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x), nstage);
         const unsigned char* a_src = p.aimg + static_cast<size_t>(w.rb) * nstage * kABytes;
-        const __half* b_src = p.bimg + static_cast<size_t>(w.t) * kNB * p.n;
+        const __half* b_src = p.bimg + static_cast<size_t>(w.t) * NB * p.n;
         for (int ks = w.ks0; ks < w.ks1; ++ks, ++seq) {
           const int slot = seq % kStages;
           const int use = seq / kStages;
@@ -226,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
           unsigned char* dst = ring + static_cast<size_t>(slot) * kStageBytes;
           mbar_arrive_expect_tx(&sh.full[slot], kStageBytes);
           bulk_g2s(dst, a_src + static_cast<size_t>(ks) * kABytes, kABytes, &sh.full[slot]);
-          bulk_g2s(dst + kABytes, b_src + static_cast<size_t>(ks) * kNB * kStageK, kBBytes, &sh.full[slot]);
+          bulk_g2s(dst + kABytes, b_src + static_cast<size_t>(ks) * NB * kStageK, kBBytes, &sh.full[slot]);
           // operand A streams from DRAM: ask for it kPrefetch stages before
           // the ring does, so that the ring's copies find it in L2
           if (ks + kPrefetch < w.ks1)
@@ -240,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
     }
   } else if (warp == kMmaWarp) {
     // ---- MMA issue: the warp runs the loop, lane 0 issues ------------------------------
-    constexpr uint32_t idesc = tc::idesc_f16<kNB>();
+    constexpr uint32_t idesc = tc::idesc_f16<NB>();
     constexpr uint32_t kALbo = 16 * 128;         // next 8 K-elements of A (16 groups of 8 rows)
-    constexpr uint32_t kBLbo = (kNB / 8) * 128;  // next 8 K-elements of B
+    constexpr uint32_t kBLbo = (NB / 8) * 128;  // next 8 K-elements of B
     const uint64_t adesc0 = smem_desc(smem_u32(ring), kALbo, 128);
     const uint64_t bdesc0 = smem_desc(smem_u32(ring + kABytes), kBLbo, 128);
     const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
@@ -256,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
         break;
       }
       tc_fence_after();
-      const uint32_t dt = tm + static_cast<uint32_t>(kNB * db);
+      const uint32_t dt = tm + static_cast<uint32_t>(NB * db);
       const Unit w = unit_of(p, static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x), nstage);
       for (int ks = w.ks0; ks < w.ks1; ++ks, ++seq) {
         const int slot = seq % kStages;
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
       const Unit w = unit_of(p, static_cast<int>(blockIdx.x) + li * static_cast<int>(gridDim.x), nstage);
       const int rb = w.rb;
       const int t = w.t;
-      const int rows = p.M - t * kNB < kNB ? p.M - t * kNB : kNB;  // batch rows of this tile
+      const int rows = p.M - t * NB < NB ? p.M - t * NB : NB;  // batch rows of this tile
       const bool finish = w.split == 1;
       const int db = li & 1;
       const bool ok = !aborted(sh) && mbar_wait(&sh.d_full[db], (li >> 1) & 1);
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
         const int b0 = sl * kSlice + 16 * half;
         if (warp_ok && b0 < rows) {  // warp-uniform
           float d[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(kNB * db + b0), d);
+          tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(NB * db + b0), d);
 #pragma unroll
           for (int j = 0; j < 16; ++j) sh.zt[(16 * half + j) * kRowBlock + row] = d[j];
         }
@@ -344,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
 #pragma unroll 4
           for (int bl = e; bl < nb; bl += kEpiWarps) {
             const float4 z = *reinterpret_cast<const float4*>(&sh.zt[bl * kRowBlock + 4 * lane]);
-            const size_t b = static_cast<size_t>(t) * kNB + sl * kSlice + bl;
+            const size_t b = static_cast<size_t>(t) * NB + sl * kSlice + bl;
             if (finish)
               finish_rows(p, z, sc, so, lane, b, r0);
             else
@@ -377,14 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
         for (int i = 0; i < kFixRows; ++i) {
           const int bl = b0 + kEpiWarps * i;
           z[i] = bl < rows ? __ldcg(reinterpret_cast<const float4*>(
-                                 p.zacc + (static_cast<size_t>(t) * kNB + bl) * p.m + r0))
+                                 p.zacc + (static_cast<size_t>(t) * NB + bl) * p.m + r0))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < kFixRows; ++i) {
           const int bl = b0 + kEpiWarps * i;
           if (bl >= rows) break;  // warp-uniform
-          const size_t b = static_cast<size_t>(t) * kNB + bl;
+          const size_t b = static_cast<size_t>(t) * NB + bl;
           __stcg(reinterpret_cast<float4*>(p.zacc + b * p.m + r0), make_float4(0.f, 0.f, 0.f, 0.f));
           finish_rows(p, z[i], sc, so, lane, b, r0);
         }
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_kernel(const DenseParams p)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, S::kTmemCols);
   }
   if (tid == 0 && aborted(sh) && p.status != nullptr) atomicOr(p.status, 1u);
 }
@@ -417,9 +432,45 @@ int choose_dense_split(int units, int nstage, int grid) {
   return s < 1 ? 1 : s;
 }
 
+namespace {
+
+template <int NB>
+exl3_status launch_dense_nb(dense::DenseParams p, int split, cudaStream_t stream) {
+  using namespace dense;
+  using S = Shape<NB>;
+  p.tiles = (p.M + NB - 1) / NB;
+  const int units = (p.m / kRowBlock) * p.tiles;
+  const int sms = device_sm_count();
+  p.split = split;
+  p.rem = split > 1 ? units % sms : 0;
+  p.full = units - p.rem;
+  p.units = p.full + p.rem * split;
+  const size_t ctrl = (sizeof(DenseShared) + 1023) & ~static_cast<size_t>(1023);
+  const size_t smem = ctrl + static_cast<size_t>(S::kStages) * S::kStageBytes;
+  if (cudaFuncSetAttribute(dense_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return EXL3_ERR_CUDA;
+  int grid = sms;
+  if (grid > p.units) grid = p.units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, dense_kernel<NB>, p) != cudaSuccess) return EXL3_ERR_CUDA;
+  return launch_status();
+}
+
+}  // namespace
+
 exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __half* scales,
                          const __half* s_out, __half* y, float* zacc, uint32_t* cnt, int m, int n, int M,
-                         int split, uint32_t* status, int debug_stall, cudaStream_t stream) {
+                         int nb, int split, uint32_t* status, int debug_stall, cudaStream_t stream) {
   using namespace dense;
   if (split < 1 || split > n / kStageK) return EXL3_ERR_SHAPE;
   DenseParams p;
@@ -434,33 +485,17 @@ exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __
   p.m = m;
   p.n = n;
   p.M = M;
-  p.tiles = (M + kNB - 1) / kNB;
-  const int units = (m / kRowBlock) * p.tiles;
-  const int sms = device_sm_count();
-  p.split = split;
-  p.rem = split > 1 ? units % sms : 0;
-  p.full = units - p.rem;
-  p.units = p.full + p.rem * split;
   p.debug_stall = debug_stall;
-  const size_t ctrl = (sizeof(DenseShared) + 1023) & ~static_cast<size_t>(1023);
-  const size_t smem = ctrl + static_cast<size_t>(kStages) * kStageBytes;
-  if (cudaFuncSetAttribute(dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return EXL3_ERR_CUDA;
-  int grid = sms;
-  if (grid > p.units) grid = p.units;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, dense_kernel, p) != cudaSuccess) return EXL3_ERR_CUDA;
-  return launch_status();
+  switch (nb) {
+    case 64:
+      return launch_dense_nb<64>(p, split, stream);
+    case 128:
+      return launch_dense_nb<128>(p, split, stream);
+    case 256:
+      return launch_dense_nb<256>(p, split, stream);
+    default:
+      return EXL3_ERR_SHAPE;
+  }
 }
 
 }  // namespace exl3

@@ -221,8 +221,9 @@ exl3_status launch_decode(const uint32_t* codes, int K, int codebook, int m, int
 exl3_status launch_decode_aimg(const uint32_t* codes, int K, int codebook, int m, int n,
                                unsigned char* aimg, cudaStream_t stream);
 // Dense prefill kernel: z = A x-tilde for M batch rows, A from the operand-A
-// images, x-tilde from operand-B images of kDenseNB rows per tile (bimg + tile
-// * kDenseNB * n halves), then y = binary16(Hb(s_out (.) (scale (.) z))).
+// images, x-tilde from operand-B images of nb rows per tile (nb = 64, 128 or
+// 256; bimg + tile * nb * n halves), then y = binary16(Hb(s_out (.) (scale (.)
+// z))).
 // With split == 1 every work unit covers all of K and finishes its block from
 // tensor memory; with split > 1 each unit covers 1/split of K and adds its
 // partial z to zacc [M][m], and the unit that brings the block's counter
@@ -231,14 +232,17 @@ exl3_status launch_decode_aimg(const uint32_t* codes, int K, int codebook, int m
 // operands.
 exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __half* scales,
                          const __half* s_out, __half* y, float* zacc, uint32_t* cnt, int m, int n, int M,
-                         int split, uint32_t* status, int debug_stall, cudaStream_t stream);
+                         int nb, int split, uint32_t* status, int debug_stall, cudaStream_t stream);
 
 // Dense prefill path (exl3_gemm above EXL3_MAX_BATCH): batch rows per MMA tile
 // (N of 128 x N x 16) and the workspace layout: counters and status as above,
-// zacc fp32 [M][m], bimg one (kDenseNB x n) operand-B image per tile of
-// kDenseNB batch rows, aimg the decoded matrix as m * n binary16 operand-A
-// images, cnt one uint32 per (128-row block, tile): K-split arrivals.
+// zacc fp32 [M][m], bimg one (nb x n) operand-B image per tile of nb batch
+// rows, aimg the decoded matrix as m * n binary16 operand-A images, cnt one
+// uint32 per (128-row block, tile): K-split arrivals.  The regions are sized
+// for tiles of kDenseNB rows; a batch of M <= 128 rows runs as one tile of
+// dense_nb(M) <= M rounded up, which fits in them.
 constexpr int kDenseNB = 256;
+inline int dense_nb(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : kDenseNB; }
 inline int dense_tiles(int M) { return (M + kDenseNB - 1) / kDenseNB; }
 inline size_t dense_bimg_offset(int m, int M) { return bimg_offset(m, M); }
 inline size_t dense_aimg_offset(int m, int n, int M) {
