@@ -405,6 +405,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     B.load_library()
     B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[args.path])
+    B.exl3_set_prefill({"auto": B.PREFILL_AUTO, "fused": B.PREFILL_FUSED,
+                        "decode_once": B.PREFILL_DECODE_ONCE}[args.prefill])
 
     desc, cfg, gemvs, M = workload(args.workload, args.batch)
     hbm_gbs, sm_max_mhz, bf16_tflops, peak_src = measured_peaks()
@@ -566,6 +568,9 @@ def run_ours(args):
     if int8:
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
+    elif dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256)):
+        kname = ("dense_kernel, fused (eight warps decode each stage's codes into the operand-A image in shared "
+                 "memory; tcgen05 128xNx16 MMAs, N = 128/256 by batch) + operand-B kernel")
     elif dense:
         kname = ("dense_kernel (tcgen05 128xNx16 MMAs, N = 64/128/256 by batch, both operands in shared memory) + "
                  "decode-to-operand-image, operand-B and output kernels")
@@ -684,6 +689,7 @@ def run_ours(args):
                        "weights_per_step": weights_step, "packed_bytes_per_step": packed,
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path,
+                       "prefill": args.prefill,
                        "calls": "one exl3_gemm_whole call per GEMV" if whole else
                        ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
                         "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
@@ -874,6 +880,8 @@ def main():
                     help="one exl3_gemm_small call per GEMV (no grouped q/k/v and gate/up calls)")
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto",
                     help="kernel family of the fused layer (exl3_set_path)")
+    ap.add_argument("--prefill", choices=["auto", "fused", "decode_once"], default="auto",
+                    help="prefill strategy above 32 batch rows (exl3_set_prefill)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

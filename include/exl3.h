@@ -162,16 +162,21 @@ size_t exl3_gemm_workspace_bytes(int m, int n, int M);
 
 /**
  * The layer for any batch M >= 1 (prefill): x [M][n] -> y [M][m].  Up to
- * EXL3_MAX_BATCH rows this is exl3_gemm_small.  Above, by default, the matrix
- * is decoded once per call into binary16 in the workspace and a dense
- * tcgen05 GEMM (128 x N x 16 MMAs, both operands in shared memory; N = 64
- * up to 64 rows, 128 up to 128, else tiles of 256) runs over all M rows
- * ("decode a block once and reuse it", Lecture 1b Part
- * fourteen: at large batch the decode is amortised and the product is a
- * plain matrix multiplication).  With EXL3_PATH_TENSOR selected, passes of
- * 128 rows run the tensor-core kernel with 128 batch columns per MMA instead,
- * decoding each tile once per pass into tensor memory (no decoded copy in
- * HBM).  Both compute the layer within the documented tolerance.
+ * EXL3_MAX_BATCH rows this is exl3_gemm_small.  Above, a tcgen05 GEMM (128 x
+ * N x 16 MMAs, both operands in shared memory) runs over all M rows, with the
+ * weights in one of two ways (exl3_set_prefill):
+ *   - fused (default up to 256 rows): each CTA decodes the codes of every
+ *     64-column stage into a binary16 operand image in shared memory, once
+ *     per batch tile (N = 128 up to 128 rows, else tiles of 256);
+ *   - decode-once (default above 256 rows): the matrix is decoded once per
+ *     call into binary16 in the workspace and streamed from there (N = 64
+ *     up to 64 rows, 128 up to 128, else tiles of 256): "decode a block once
+ *     and reuse it", Lecture 1b Part fourteen -- at large batch the decode is
+ *     amortised and the product is a plain matrix multiplication.
+ * With EXL3_PATH_TENSOR selected, passes of 128 rows run the tensor-core
+ * kernel with 128 batch columns per MMA instead, decoding each tile once per
+ * pass into tensor memory.  All compute the layer within the documented
+ * tolerance.
  */
 exl3_status exl3_gemm(const uint32_t *codes, int K, int codebook, int m, int n,
                       const exl3_half *s_in, const exl3_half *s_out,
@@ -301,8 +306,9 @@ exl3_status exl3_gemm_int8act(const uint32_t *codes, int K, int codebook, int m,
  * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
  * call of this shape and batch makes on the current device under the current
  * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on
- * the warp-shuffle path; 3 for the dense prefill; 3 per 128-row pass for the
- * prefill passes.  0 for an invalid shape or M < 1.
+ * the warp-shuffle path; 2 for the fused prefill, 3 for the decode-once
+ * prefill (exl3_set_prefill); 3 per 128-row pass for the prefill passes.  0
+ * for an invalid shape or M < 1.
  */
 int exl3_gemm_launches(int m, int n, int M);
 
@@ -368,6 +374,23 @@ typedef enum {
   EXL3_PATH_SHUFFLE = 1, /**< decode + fp32 FMA + warp-shuffle reduction, any M */
   EXL3_PATH_TENSOR = 2   /**< decoded tiles in TMEM feeding tcgen05 MMAs, any M */
 } exl3_path;
+
+/** Prefill strategy of exl3_gemm above EXL3_MAX_BATCH rows. */
+typedef enum {
+  EXL3_PREFILL_AUTO = 0,        /**< fused up to 256 rows, decode-once above */
+  EXL3_PREFILL_FUSED = 1,       /**< codes decoded into shared memory inside the GEMM, per batch tile */
+  EXL3_PREFILL_DECODE_ONCE = 2  /**< the matrix decoded once per call into HBM, then a dense GEMM */
+} exl3_prefill;
+
+/**
+ * Select the prefill strategy of subsequent exl3_gemm calls with M >
+ * EXL3_MAX_BATCH (a process-wide setting, default EXL3_PREFILL_AUTO; ignored
+ * while exl3_set_path(EXL3_PATH_TENSOR) selects 128-row passes).  Every
+ * strategy computes the layer within the documented tolerance and uses the
+ * workspace of exl3_gemm_workspace_bytes.  Returns EXL3_ERR_BATCH for an
+ * unknown value.
+ */
+exl3_status exl3_set_prefill(int strategy);
 
 /**
  * Select the kernel family for subsequent exl3_gemv / exl3_gemm_small calls

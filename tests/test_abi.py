@@ -48,6 +48,10 @@ def test_debug_hook_and_path_setter(lib):
     assert lib.exl3_debug_stall_tensor_wait(0) == 0
     assert lib.exl3_set_path(3) == 5  # unknown path: rejected
     assert lib.exl3_set_path(0) == 0
+    assert lib.exl3_set_prefill(3) == 5  # unknown prefill strategy: rejected
+    assert lib.exl3_set_prefill(-1) == 5
+    for s in (1, 2, 0):
+        assert lib.exl3_set_prefill(s) == 0
 
 
 def test_workspace_bytes(lib):

@@ -60,12 +60,21 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
         B.exl3_set_path(B.PATH_AUTO)
 
 
+@pytest.mark.parametrize("prefill", ["fused", "decode_once"])
 @pytest.mark.parametrize("m,n,M", [(256, 3200, 90), (384, 512, 300)])
-def test_dense_prefill_wait_timeout_sets_status_and_context_survives(m, n, M):
-    """The dense prefill kernel with its producer stalled: with K split (first
-    shape) the row sums stay zero; without (second) nothing is written.  The
-    next call is correct."""
+def test_dense_prefill_wait_timeout_sets_status_and_context_survives(m, n, M, prefill):
+    """The dense prefill kernel (fused, or from decoded images) with its
+    producer stalled: with K split (first shape) the row sums stay zero;
+    without (second) nothing is written.  The next call is correct."""
     K, cb = 2, 0
+    B.exl3_set_prefill(B.PREFILL_FUSED if prefill == "fused" else B.PREFILL_DECODE_ONCE)
+    try:
+        _dense_stall(m, n, M, K, cb)
+    finally:
+        B.exl3_set_prefill(B.PREFILL_AUTO)
+
+
+def _dense_stall(m, n, M, K, cb):
     inp = synth.layer_inputs(m, n, K, M, config=98, index=0)
     d = upload(inp)
     ws = torch.zeros(B.exl3_gemm_workspace_bytes(m, n, M), dtype=torch.uint8, device="cuda")

@@ -2,9 +2,13 @@
 float64 layer (relative L2 <= 5e-3, |err| <= 1e-2 * max|y_ref|), for both
 prefill strategies:
 
-* dense (the default): the matrix decoded once into binary16 operand images,
-  then the dense tcgen05 kernel over batch tiles (one tile of 64 rows up to
-  M = 64, one of 128 up to M = 128, tiles of 256 above), finishing the
+* fused (the default up to 256 rows): the dense tcgen05 kernel with eight
+  decode warps that turn each stage's codes into the binary16 operand-A image
+  in shared memory, over batch tiles of 128 rows (M <= 128) or 256;
+* decode-once (the default above 256 rows): the matrix decoded once into
+  binary16 operand images, then the dense tcgen05 kernel over batch tiles
+  (one tile of 64 rows up to M = 64, one of 128 up to M = 128, tiles of 256
+  above).  Both dense variants finish the
   layer from tensor memory when every unit covers all of K (n < 1024 here) or
   adding partial sums of K splits, the last split finishing the block
   (n >= 1024 with few row blocks);
@@ -25,11 +29,31 @@ from tests.gpu_helpers import assert_layer_close, upload
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["dense", "passes"])
-def strategy(request):
-    B.exl3_set_path(B.PATH_AUTO if request.param == "dense" else B.PATH_TENSOR)
-    yield request.param
+_PREFILL = {"fused": B.PREFILL_FUSED, "decode_once": B.PREFILL_DECODE_ONCE}
+
+
+def _select(strategy):
+    B.exl3_set_path(B.PATH_TENSOR if strategy == "passes" else B.PATH_AUTO)
+    B.exl3_set_prefill(_PREFILL.get(strategy, B.PREFILL_AUTO))
+
+
+def _reset():
     B.exl3_set_path(B.PATH_AUTO)
+    B.exl3_set_prefill(B.PREFILL_AUTO)
+
+
+@pytest.fixture(params=["fused", "decode_once", "passes"])
+def strategy(request):
+    _select(request.param)
+    yield request.param
+    _reset()
+
+
+@pytest.fixture(params=["fused", "decode_once"])
+def dense_strategy(request):
+    _select(request.param)
+    yield request.param
+    _reset()
 
 
 def _run(inp, K, cb, m, n, M, ws=None):
@@ -78,17 +102,17 @@ def test_prefill_codes_and_widths(strategy, K, cb):
 @pytest.mark.parametrize("K,cb", [(3, 0), (5, 2), (6, 3), (7, 1)])
 def test_prefill_split_k(strategy, K, cb):
     """Few row blocks and long rows: the dense kernel splits K (50 stages of
-    64 columns in three splits of 16, 17 and 17) and the last split of each
-    block finishes it."""
+    64 columns: three splits of 16, 17 and 17 from decoded images, ten of five
+    fused) and the last split of each block finishes it."""
     m, n, M = 256, 3200, 90
     inp = synth.layer_inputs(m, n, K, M, config=95, index=K)
     y, ws = _run(inp, K, cb, m, n, M)
     assert_layer_close(y, _ref(inp, K, cb, m, n), f"{strategy} split K={K}")
-    if strategy == "dense":
+    if strategy != "passes":
         _dense_scratch_left_zero(ws, m, n, M)
 
 
-def test_prefill_split_k_several_tiles():
+def test_prefill_split_k_several_tiles(dense_strategy):
     """K split with three batch tiles (the last ragged) and repeated calls on
     one workspace: every (block, tile) counter is reset for the next call."""
     m, n, K, cb, M = 384, 2048, 2, 1, 600
@@ -121,7 +145,7 @@ def test_prefill_ragged_chunks_and_workspace_reuse(strategy):
     y1, ws = _run(inp, K, cb, m, n, M)
     y2, _ = _run(inp, K, cb, m, n, M, ws)
     assert float((y1.float() - y2.float()).abs().max()) <= 2.0 ** -9 * float(y1.float().abs().max())
-    if strategy == "dense":
+    if strategy != "passes":
         _dense_scratch_left_zero(ws, m, n, M)
     else:  # fp32 row sums [128][m] after the counters
         assert float(ws[256:256 + 4 * 128 * m].view(torch.float32).abs().sum()) == 0.0
@@ -143,7 +167,7 @@ def test_prefill_large_sampled(strategy):
     assert_layer_close(y[rows][:, cols], ref, f"{strategy} 4096x4096 M=512")
 
 
-def test_prefill_full_width_single_pass_dense():
+def test_prefill_full_width_single_pass_dense(dense_strategy):
     """Enough row blocks for one unit per CTA without a K split: 9728 x 512,
     300 rows (152 units of 128 rows x 256 batch rows), every output checked."""
     m, n, K, cb, M = 9728, 512, 2, 3, 300
@@ -182,7 +206,7 @@ def test_prefill_passes_repeated_1mad_block_sums():
         B.exl3_set_path(B.PATH_AUTO)
 
 
-def test_prefill_two_rounds_of_units():
+def test_prefill_two_rounds_of_units(dense_strategy):
     """228 units (76 row blocks x 3 tiles) over 152 CTAs: two rounds, the
     second partial; every output checked, scratch left at zero, workspace
     reused."""
@@ -197,7 +221,7 @@ def test_prefill_two_rounds_of_units():
 
 
 @pytest.mark.parametrize("M", [40, 120])
-def test_prefill_narrow_tiles_two_rounds_and_split(M):
+def test_prefill_narrow_tiles_two_rounds_and_split(dense_strategy, M):
     """The 64- and 128-row tiles: 160 row blocks over 152 CTAs (a second,
     partial round), then a layer of two row blocks split in K; every output
     checked, scratch left at zero."""

@@ -78,6 +78,7 @@ _SIGNATURES = {
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_set_path": ([_I], _I),
+    "exl3_set_prefill": ([_I], _I),
     "exl3_debug_stall_tensor_wait": ([_I], _I),
     "exl3_device_status": ([_P, _P], _I),
     "exl3_status_string": ([_I], ctypes.c_char_p),
@@ -154,6 +155,14 @@ PATH_AUTO, PATH_SHUFFLE, PATH_TENSOR = 0, 1, 2
 def exl3_set_path(path: int) -> None:
     """Select the kernel family of exl3_gemv / exl3_gemm_small (process-wide)."""
     _check(load_library().exl3_set_path(path))
+
+
+PREFILL_AUTO, PREFILL_FUSED, PREFILL_DECODE_ONCE = 0, 1, 2
+
+
+def exl3_set_prefill(strategy: int) -> None:
+    """Select the prefill strategy of exl3_gemm above 32 rows (process-wide)."""
+    _check(load_library().exl3_set_prefill(strategy))
 
 
 def exl3_debug_stall_tensor_wait(on: bool) -> None:

@@ -53,6 +53,7 @@ int choose_sub(long long tiles, int mb, int sm_count) {
 namespace {
 
 std::atomic<int> g_path{EXL3_PATH_AUTO};
+std::atomic<int> g_prefill{EXL3_PREFILL_AUTO};
 std::atomic<int> g_debug_stall{0};
 
 exl3_status launch_tc(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
@@ -99,6 +100,17 @@ exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
 }
 
 int batch_chunk(int rem) { return rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1; }
+
+// Prefill strategy above EXL3_MAX_BATCH rows (outside EXL3_PATH_TENSOR): the
+// fused kernel decodes every tile once per batch tile, the decode-once path
+// once per call plus a round trip of the decoded matrix through HBM.
+constexpr int kFusedMaxRows = 256;
+bool prefill_fused(int M) {
+  const int s = g_prefill.load(std::memory_order_relaxed);
+  return s == EXL3_PREFILL_FUSED || (s == EXL3_PREFILL_AUTO && M <= kFusedMaxRows);
+}
+// Batch tile of the fused kernel: one tile of 128 rows up to 128, else 256.
+int fused_nb(int M) { return M <= 128 ? 128 : 256; }
 
 }  // namespace
 
@@ -174,6 +186,13 @@ extern "C" const char* exl3_status_string(exl3_status status) {
 }
 
 extern "C" const char* exl3_version(void) { return "libexl3 0.2.0 sm_103a"; }
+
+extern "C" exl3_status exl3_set_prefill(int strategy) {
+  if (strategy != EXL3_PREFILL_AUTO && strategy != EXL3_PREFILL_FUSED && strategy != EXL3_PREFILL_DECODE_ONCE)
+    return EXL3_ERR_BATCH;
+  g_prefill.store(strategy, std::memory_order_relaxed);
+  return EXL3_OK;
+}
 
 extern "C" exl3_status exl3_set_path(int path) {
   if (path != EXL3_PATH_AUTO && path != EXL3_PATH_SHUFFLE && path != EXL3_PATH_TENSOR)
@@ -439,10 +458,26 @@ extern "C" int exl3_gemm_launches(int m, int n, int M) {
     return launches;
   }
   if (path == EXL3_PATH_TENSOR) return 3 * ((M + kPrefillRows - 1) / kPrefillRows);
-  return 3;
+  return prefill_fused(M) ? 2 : 3;
 }
 
 namespace {
+
+// Fused prefill: x-tilde into operand-B images, then the dense kernel that
+// decodes its operand A from the codes in shared memory.
+exl3_status run_fused(const LayerArgs& a, int M, char* ws, cudaStream_t cs) {
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws) + a.m / kRowBlock;
+  float* zacc = reinterpret_cast<float*>(ws + zacc_offset(a.m));
+  __half* bimg = reinterpret_cast<__half*>(ws + dense_bimg_offset(a.m, M));
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(ws + dense_cnt_offset(a.m, a.n, M));
+  const int nb = fused_nb(M);
+  exl3_status st = launch_bimg(a.x, a.s_in, bimg, nullptr, M, nb, a.n, cs);
+  if (st != EXL3_OK) return st;
+  const int units = (a.m / kRowBlock) * ((M + nb - 1) / nb);
+  const int split = choose_fused_split(units, a.n / 64, device_sm_count(), M < nb ? M : nb);
+  return launch_fused(a.codes, a.K, a.codebook, bimg, a.scales, a.s_out, a.y, zacc, cnt, a.m, a.n, M, nb, split,
+                      status, a.debug_stall, cs);
+}
 
 // Decode once, dense GEMM: W-hat into operand-A images, x-tilde into
 // operand-B images, then the dense kernel.
@@ -496,7 +531,7 @@ extern "C" exl3_status exl3_gemm(const uint32_t* codes, int K, int codebook, int
     a.x = reinterpret_cast<const __half*>(x);
     a.y = reinterpret_cast<__half*>(y);
     a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
-    return run_dense(a, M, ws, cs);
+    return prefill_fused(M) ? run_fused(a, M, ws, cs) : run_dense(a, M, ws, cs);
   }
   // EXL3_PATH_TENSOR: passes of up to 128 batch rows through the tensor-core
   // kernel at N = 128; each pass decodes the tiles once into tensor memory for

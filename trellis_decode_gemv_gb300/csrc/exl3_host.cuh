@@ -234,6 +234,13 @@ exl3_status launch_dense(const unsigned char* aimg, const __half* bimg, const __
                          const __half* s_out, __half* y, float* zacc, uint32_t* cnt, int m, int n, int M,
                          int nb, int split, uint32_t* status, int debug_stall, cudaStream_t stream);
 
+// Fused prefill kernel: as launch_dense, but each CTA decodes operand A from
+// the packed codes (K bits, codebook) into shared memory stage by stage; nb =
+// 128 or 256.  No operand-A images.
+exl3_status launch_fused(const uint32_t* codes, int K, int codebook, const __half* bimg, const __half* scales,
+                         const __half* s_out, __half* y, float* zacc, uint32_t* cnt, int m, int n, int M,
+                         int nb, int split, uint32_t* status, int debug_stall, cudaStream_t stream);
+
 // Dense prefill path (exl3_gemm above EXL3_MAX_BATCH): batch rows per MMA tile
 // (N of 128 x N x 16) and the workspace layout: counters and status as above,
 // zacc fp32 [M][m], bimg one (nb x n) operand-B image per tile of nb batch
@@ -263,6 +270,10 @@ inline size_t dense_total(int m, int n, int M) {
 // kernel can also split just the last partial round after whole rounds; that
 // measured no faster.)
 int choose_dense_split(int units, int nstage, int grid);
+// K splits of the fused kernel: with fewer units than CTAs, the s (up to 16,
+// at least 4 stages per split) that minimises rounds x stages per item plus
+// a charge per round for the partial sums of `rows` batch rows; else 1.
+int choose_fused_split(int units, int nstage, int grid, int rows);
 // Epilogue of the warp-shuffle path: y = binary16(Hb(s_out (.) (scale (.) zacc)))
 // per 128-row block (no rotation when s_out is NULL); zeroes zacc.
 exl3_status launch_epi(float* zacc, const __half* scales, const __half* s_out, __half* y, int rows,
