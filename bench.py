@@ -569,8 +569,8 @@ def run_ours(args):
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
     elif dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256)):
-        kname = ("dense_kernel, fused (eight warps decode each stage's codes into the operand-A image in shared "
-                 "memory; tcgen05 128xNx16 MMAs, N = 128/256 by batch) + operand-B kernel")
+        kname = ("dense_kernel, fused (sixteen warps decode each stage's codes into the operand-A image in shared "
+                 "memory; tcgen05 128xNx16 MMAs, N = 64/128/256 by batch) + operand-B kernel")
     elif dense:
         kname = ("dense_kernel (tcgen05 128xNx16 MMAs, N = 64/128/256 by batch, both operands in shared memory) + "
                  "decode-to-operand-image, operand-B and output kernels")

@@ -167,7 +167,7 @@ size_t exl3_gemm_workspace_bytes(int m, int n, int M);
  * weights in one of two ways (exl3_set_prefill):
  *   - fused (default up to 256 rows): each CTA decodes the codes of every
  *     64-column stage into a binary16 operand image in shared memory, once
- *     per batch tile (N = 128 up to 128 rows, else tiles of 256);
+ *     per batch tile (N = 64 up to 64 rows, 128 up to 128, else tiles of 256);
  *   - decode-once (default above 256 rows): the matrix is decoded once per
  *     call into binary16 in the workspace and streamed from there (N = 64
  *     up to 64 rows, 128 up to 128, else tiles of 256): "decode a block once

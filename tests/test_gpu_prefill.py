@@ -4,7 +4,8 @@ prefill strategies:
 
 * fused (the default up to 256 rows): the dense tcgen05 kernel with eight
   decode warps that turn each stage's codes into the binary16 operand-A image
-  in shared memory, over batch tiles of 128 rows (M <= 128) or 256;
+  in shared memory, over batch tiles of 64 rows (M <= 64), 128 (M <= 128) or
+  256;
 * decode-once (the default above 256 rows): the matrix decoded once into
   binary16 operand images, then the dense tcgen05 kernel over batch tiles
   (one tile of 64 rows up to M = 64, one of 128 up to M = 128, tiles of 256

@@ -109,8 +109,9 @@ bool prefill_fused(int M) {
   const int s = g_prefill.load(std::memory_order_relaxed);
   return s == EXL3_PREFILL_FUSED || (s == EXL3_PREFILL_AUTO && M <= kFusedMaxRows);
 }
-// Batch tile of the fused kernel: one tile of 128 rows up to 128, else 256.
-int fused_nb(int M) { return M <= 128 ? 128 : 256; }
+// Batch tile of the fused kernel: one tile of 64 rows up to 64, of 128 up to
+// 128, else tiles of 256.
+int fused_nb(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
 }  // namespace
 

@@ -630,9 +630,17 @@ exl3_status launch_dense_kernel(DenseParams p, int split, cudaStream_t stream) {
   return launch_status();
 }
 
-// The fused kernel for K-bit codes: NB in {128, 256}, any codebook.
+// The fused kernel for K-bit codes: NB in {64, 128, 256}, any codebook.
 template <int K>
 exl3_status launch_fused_dispatch(const DenseParams& p, int codebook, int nb, int split, cudaStream_t stream) {
+  if (nb == 64) {
+    switch (codebook) {
+      case kCb3Inst: return launch_dense_kernel<64, K, kCb3Inst>(p, split, stream);
+      case kCb1Mad: return launch_dense_kernel<64, K, kCb1Mad>(p, split, stream);
+      case kCbMcg: return launch_dense_kernel<64, K, kCbMcg>(p, split, stream);
+      default: return launch_dense_kernel<64, K, kCbMul1>(p, split, stream);
+    }
+  }
   if (nb == 128) {
     switch (codebook) {
       case kCb3Inst: return launch_dense_kernel<128, K, kCb3Inst>(p, split, stream);
