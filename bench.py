@@ -445,9 +445,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.Stream(dev)
 
+    # grouped calls take at most 32 batch rows
     groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
-                            grouped=not (args.ungrouped or whole))
-    gws_of = B.exl3_group_i8_workspace_bytes if int8 else B.exl3_group_workspace_bytes
+                            grouped=not (args.ungrouped or (whole and M > 32)))
+    gws_of = (B.exl3_group_i8_workspace_bytes if int8 else B.exl3_gemm_whole_grouped_workspace_bytes if whole
+              else B.exl3_group_workspace_bytes)
     gws = max([gws_of([(calls[i]["m"], calls[i]["n"]) for i in g], M)
                for g in groups if len(g) > 1] + [0])
     if gws > ws.numel():
@@ -462,7 +464,8 @@ def run_ours(args):
                c["scales"], c["x"], y=c["y"], workspace=ws)
         else:
             c0 = calls[g[0]]
-            gfn = B.exl3_gemm_int8act_grouped if int8 else B.exl3_gemm_grouped
+            gfn = (B.exl3_gemm_int8act_grouped if int8 else B.exl3_gemm_whole_grouped if whole
+                   else B.exl3_gemm_grouped)
             gfn([calls[i] for i in g], c0["K"], c0["cb"], workspace=ws)
 
     def step():
@@ -622,7 +625,11 @@ def run_ours(args):
             layer_objs.append(lambda c=c: B.exl3_gemm_int8act(
                 c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
                 y=c["y"], workspace=ws))
-        elif whole:  # no layer object for the whole-vector variant: the public call itself
+        elif whole and len(g) > 1:  # no layer object for the whole-vector variant: the public calls
+            c0 = calls[g[0]]
+            layer_objs.append(lambda g=g, c0=c0: B.exl3_gemm_whole_grouped(
+                [calls[i] for i in g], c0["K"], c0["cb"], workspace=ws))
+        elif whole:
             c = calls[g[0]]
             layer_objs.append(lambda c=c: B.exl3_gemm_whole(
                 c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
@@ -690,7 +697,9 @@ def run_ours(args):
                        "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                        "cuda_graph": graph is not None, "kernel_path": args.path,
                        "prefill": args.prefill,
-                       "calls": "one exl3_gemm_whole call per GEMV" if whole else
+                       "calls": ("q/k/v grouped per exl3_gemm_whole_grouped call, o one exl3_gemm_whole call"
+                                 if whole and not args.ungrouped and M <= 32 else "one exl3_gemm_whole call per GEMV")
+                       if whole else
                        ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
                         "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
                        if int8 else
@@ -702,7 +711,8 @@ def run_ours(args):
             "roofline": roofline, "hbm": hbm, "per_code": per_summary,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * sum(
-                (B.exl3_gemm_launches(calls[g[0]]["m"], calls[g[0]]["n"], M) + 2) if whole else
+                (B.exl3_gemm_launches(calls[g[0]]["m"], calls[g[0]]["n"], M) + 2) if whole and len(g) == 1 else
+                (kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) + 2) if whole else
                 (2 + int8_chunks(M)) if int8 else
                 kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) for g in groups),
             "clocks": clk,

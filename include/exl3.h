@@ -350,6 +350,31 @@ exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int co
                               void *workspace, size_t workspace_bytes, exl3_stream_t stream);
 
 /**
+ * Bytes of scratch for exl3_gemm_whole_grouped: exl3_group_workspace_bytes of
+ * the same layers rounded up to 256 bytes (first, so the status word is at
+ * byte 0), then max over the layers of max(m, n) halves of unit signs, then
+ * per layer M*n halves of its transformed input and M*m halves of its output
+ * before the last transform (each 256-byte aligned).  Same zero-fill
+ * contract.  0 for an invalid group (count outside 1..EXL3_MAX_GROUP, M
+ * outside 1..EXL3_MAX_BATCH, an m or n not a power of two in [128, 32768]).
+ */
+size_t exl3_gemm_whole_grouped_workspace_bytes(const exl3_layer *layers, int count, int M);
+
+/**
+ * `count` (1..EXL3_MAX_GROUP) independent layers with QTIP's whole-vector
+ * rotations ("Trellis Quantization" Part eleven), sharing K, the codebook and
+ * the batch M (1..EXL3_MAX_BATCH): the results equal `count` calls of
+ * exl3_gemm_whole, in one chain -- one transform kernel across the
+ * 128-blocks for every layer's input, exl3_gemm_grouped on the transformed
+ * inputs, one transform kernel for every layer's output.  Layers as for
+ * exl3_gemm_grouped (s_in / s_out NULL = no rotation on that side); m and n
+ * powers of two in [128, 32768] (EXL3_ERR_SHAPE).  Other errors as
+ * exl3_gemm_grouped.
+ */
+exl3_status exl3_gemm_whole_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
+                                    void *workspace, size_t workspace_bytes, exl3_stream_t stream);
+
+/**
  * Workspace of exl3_gemm_int8act_grouped: a status word (first 256 bytes),
  * then per layer the regions of exl3_gemm_i8_workspace_bytes after its
  * counters (row sums, activation words, tile corrections, block factors).

@@ -193,6 +193,34 @@ def test_whole_vector_workspace_and_validation(lib):
     assert lib.exl3_rht_whole(A + 8, A, A, 2, 1024, None) == 6
 
 
+def test_whole_grouped_workspace_and_validation(lib):
+    a256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
+    for M in (1, 3, 32):
+        inner = a256(lib.exl3_group_workspace_bytes(_group(shapes), 3, M))
+        want = inner + a256(2 * 4096) + sum(a256(2 * M * n) + a256(2 * M * m) for m, n in shapes)
+        assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 3, M) == want
+        assert B.exl3_gemm_whole_grouped_workspace_bytes(shapes, M) == want
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group([(384, 1024)]), 1, 1) == 0
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 3, 33) == 0
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 0, 1) == 0
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 5, 1) == 0
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(None, 1, 1) == 0
+    g = _group([(256, 512), (1024, 512)])
+
+    def call(arr=g, count=2, K=2, cb=0, M=1, ws=A, wsb=1 << 30):
+        return lib.exl3_gemm_whole_grouped(arr, count, K, cb, M, ws, wsb, None)
+
+    assert call(arr=None) == 1
+    assert call(count=0) == 2 and call(count=5) == 2
+    assert call(M=0) == 5 and call(M=33) == 5
+    assert call(arr=_group([(256, 512), (384, 512)])) == 2
+    assert call(K=9) == 3 and call(cb=4) == 4
+    assert call(arr=_group([(256, 512)], scales=None), count=1) == 1
+    assert call(arr=_group([(256, 512)], y=A + 2), count=1) == 6
+    assert call(wsb=64) == 7 and call(ws=None) == 7 and call(ws=A + 8) == 6
+
+
 def test_encoder_workspace_and_validation(lib):
     for K in range(1, 9):
         assert B.exl3_encode_workspace_bytes(K, 3) == 3 * 256 * (1 << (16 - K))

@@ -90,3 +90,57 @@ def test_gemm_whole_extreme_lengths():
     inp = synth.layer_inputs(m, n, K, M, config=65, index=0)
     y, ref = _layer(inp, K, cb, m, n)
     assert_layer_close(y, ref, "128 x 32768")
+
+
+def _whole_group(shapes, K, M, config, rot=None):
+    out = []
+    for i, (m, n) in enumerate(shapes):
+        inp = synth.layer_inputs(m, n, K, M, config=config, index=i)
+        use_in, use_out = rot[i] if rot else (True, True)
+        if not use_in:
+            inp["s_in"] = None
+        if not use_out:
+            inp["s_out"] = None
+        d = upload({k: v for k, v in inp.items() if v is not None})
+        d.setdefault("s_in", None)
+        d.setdefault("s_out", None)
+        d.update(m=m, n=n, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
+        out.append((inp, d))
+    return out
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 32])
+@pytest.mark.parametrize("K,cb", [(2, 0), (3, 1)])
+def test_gemm_whole_grouped_matches_oracle(M, K, cb):
+    """q/k/v-like group (one wide, two narrow outputs) and lengths that differ
+    per layer: one chain of launches, every layer against the oracle's
+    whole-vector layer, the status word (byte 0) left at zero."""
+    shapes = [(1024, 1024), (256, 1024), (256, 1024)] if M != 5 else [(512, 2048), (2048, 512), (128, 128)]
+    layers = _whole_group(shapes, K, M, config=66 + M)
+    ws = torch.zeros(B.exl3_gemm_whole_grouped_workspace_bytes(shapes, M), dtype=torch.uint8, device="cuda")
+    B.exl3_gemm_whole_grouped([d for _, d in layers], K, cb, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32)[0]) == 0
+    for inp, d in layers:
+        ref = O.layer_forward_whole(inp["codes"], K, cb, d["m"], d["n"], inp["s_in"], inp["s_out"], inp["scales"],
+                                    inp["x"])
+        assert_layer_close(d["y"], ref, f"grouped {d['m']}x{d['n']} M={M}")
+
+
+def test_gemm_whole_grouped_one_sided_and_reuse():
+    """Layers without an input or an output rotation in the same group, and
+    a second call on the same workspace."""
+    shapes = [(512, 1024), (1024, 512), (256, 256), (128, 2048)]
+    rot = [(False, True), (True, False), (False, False), (True, True)]
+    K, cb, M = 2, 1, 3
+    layers = _whole_group(shapes, K, M, config=69, rot=rot)
+    ws = torch.zeros(B.exl3_gemm_whole_grouped_workspace_bytes(shapes, M), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        for _, d in layers:
+            d["y"].fill_(float("nan"))
+        B.exl3_gemm_whole_grouped([d for _, d in layers], K, cb, workspace=ws)
+        torch.cuda.synchronize()
+        for inp, d in layers:
+            ref = O.layer_forward_whole(inp["codes"], K, cb, d["m"], d["n"], inp["s_in"], inp["s_out"],
+                                        inp["scales"], inp["x"])
+            assert_layer_close(d["y"], ref, f"one-sided {d['m']}x{d['n']}")

@@ -76,6 +76,8 @@ _SIGNATURES = {
     "exl3_encode_tiles": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
+    "exl3_gemm_whole_grouped_workspace_bytes": ([ctypes.POINTER(Exl3Layer), _I, _I], _SZ),
+    "exl3_gemm_whole_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
     "exl3_gemm": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_set_path": ([_I], _I),
     "exl3_set_prefill": ([_I], _I),
@@ -459,6 +461,33 @@ def exl3_gemm_whole(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, wo
         _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev),
         workspace.numel(), _stream(dev)))
     return y if x.dim() == 2 else y.view(-1)
+
+
+def exl3_gemm_whole_grouped_workspace_bytes(shapes, M: int = 1) -> int:
+    """Workspace bytes of a grouped whole-vector call over layers of (m, n)."""
+    arr = (Exl3Layer * len(shapes))()
+    for i, (m, n) in enumerate(shapes):
+        arr[i].m, arr[i].n = m, n
+    return int(load_library().exl3_gemm_whole_grouped_workspace_bytes(arr, len(shapes), M))
+
+
+def exl3_gemm_whole_grouped(layers, K, codebook, workspace=None):
+    """Independent whole-vector layers sharing K, the codebook and the batch
+    (dicts as for exl3_gemm_grouped, power-of-two m and n): same results as
+    one exl3_gemm_whole per layer, in one chain of launches."""
+    lib = load_library()
+    dev = layers[0]["codes"].device
+    M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+    arr = _layer_array(layers, dev, M)
+    if workspace is None:
+        nbytes = exl3_gemm_whole_grouped_workspace_bytes([(L["m"], L["n"]) for L in layers], M)
+        if nbytes == 0:
+            raise Exl3Error(2, "invalid group for a whole-vector workspace")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib.exl3_gemm_whole_grouped(arr, len(layers), K, codebook, M,
+                                       _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
+                                       _stream(dev)))
+    return [L["y"] for L in layers]
 
 
 def exl3_encode_workspace_bytes(K: int, ctas: int) -> int:

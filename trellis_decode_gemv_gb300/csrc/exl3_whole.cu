@@ -76,16 +76,34 @@ __global__ void __launch_bounds__(kWholeThreads)
 // The transform across the 128-blocks alone, spread over CTAs: CTA (row, c)
 // takes within-block columns 16c .. 16c + 15 of every block of the row (the
 // butterflies across blocks never mix columns), so a row of any length uses
-// eight CTAs.  out = binary16(H_B-across(signs (.) in) * scale), B = d / 128.
+// eight CTAs.  out = binary16(H_B-across(signs (.) in) * scale), B = d / 128,
+// for up to EXL3_MAX_GROUP vectors of their own lengths (CTA row index =
+// vector * rows + row).
 constexpr int kCrossCols = 16;
 constexpr int kCrossThreads = 256;
 
-__global__ void __launch_bounds__(kCrossThreads)
-    rht_cross_kernel(const __half* __restrict__ in, const __half* __restrict__ signs, __half* __restrict__ out,
-                     int d, float scale, __half* __restrict__ ones, int ones_len) {
+struct CrossGroup {
+  const __half* in[EXL3_MAX_GROUP];
+  const __half* signs[EXL3_MAX_GROUP];  // NULL: no signs
+  __half* out[EXL3_MAX_GROUP];
+  int d[EXL3_MAX_GROUP];
+  float scale[EXL3_MAX_GROUP];
+  int count;
+  int rows;
+  __half* ones;  // when not NULL, the CTAs of the first row write ones_len unit signs here
+  int ones_len;
+};
+
+__global__ void __launch_bounds__(kCrossThreads) rht_cross_kernel(const CrossGroup g) {
   __shared__ float u[(kWholeMax / kRowBlock) * kCrossCols];
+  const int l = static_cast<int>(blockIdx.x) / g.rows;
+  const size_t row = static_cast<size_t>(blockIdx.x) - static_cast<size_t>(l) * g.rows;
+  const int d = g.d[l];
+  const __half* __restrict__ in = g.in[l];
+  const __half* __restrict__ signs = g.signs[l];
+  __half* __restrict__ out = g.out[l];
+  const float scale = g.scale[l];
   const int nb = d / kRowBlock;
-  const size_t row = blockIdx.x;
   const int c0 = blockIdx.y * kCrossCols;
   const int tid = threadIdx.x;
   // element e of this CTA: block e / 16, column c0 + e % 16
@@ -120,18 +138,37 @@ __global__ void __launch_bounds__(kCrossThreads)
     const int col = (e / kCrossCols) * kRowBlock + c0 + (e % kCrossCols);
     *reinterpret_cast<__half2*>(out + row * d + col) = __floats2half2_rn(u[e] * scale, u[e + 1] * scale);
   }
-  // the CTAs of row 0 also write the inner layer's unit signs
-  if (ones != nullptr && blockIdx.x == 0)
-    for (int i = blockIdx.y * kCrossThreads + tid; i < ones_len; i += gridDim.y * kCrossThreads)
-      ones[i] = __float2half_rn(1.0f);
+  // the CTAs of the first row also write the inner layers' unit signs
+  if (g.ones != nullptr && blockIdx.x == 0)
+    for (int i = blockIdx.y * kCrossThreads + tid; i < g.ones_len; i += gridDim.y * kCrossThreads)
+      g.ones[i] = __float2half_rn(1.0f);
+}
+
+// Adds vector l of a cross-block transform group (scale 1/sqrt(d/128)).
+void cross_add(CrossGroup& g, const __half* in, const __half* signs, __half* out, int d) {
+  g.in[g.count] = in;
+  g.signs[g.count] = signs;
+  g.out[g.count] = out;
+  g.d[g.count] = d;
+  g.scale[g.count] = static_cast<float>(1.0 / sqrt(static_cast<double>(d / kRowBlock)));
+  ++g.count;
+}
+
+exl3_status launch_cross_group(const CrossGroup& g, cudaStream_t stream) {
+  if (g.count == 0) return EXL3_OK;
+  rht_cross_kernel<<<dim3(static_cast<unsigned>(g.rows * g.count), kRowBlock / kCrossCols), kCrossThreads, 0,
+                     stream>>>(g);
+  return launch_status();
 }
 
 exl3_status launch_rht_cross(const __half* in, const __half* signs, __half* out, int rows, int d, __half* ones,
                              int ones_len, cudaStream_t stream) {
-  const float scale = static_cast<float>(1.0 / sqrt(static_cast<double>(d / kRowBlock)));
-  rht_cross_kernel<<<dim3(static_cast<unsigned>(rows), kRowBlock / kCrossCols), kCrossThreads, 0, stream>>>(
-      in, signs, out, d, scale, ones, ones_len);
-  return launch_status();
+  CrossGroup g{};
+  g.rows = rows;
+  g.ones = ones;
+  g.ones_len = ones_len;
+  cross_add(g, in, signs, out, d);
+  return launch_cross_group(g, stream);
 }
 
 bool whole_length(int d) { return d >= kRowBlock && d <= kWholeMax && (d & (d - 1)) == 0; }
@@ -212,4 +249,77 @@ extern "C" exl3_status exl3_gemm_whole(const uint32_t* codes, int K, int codeboo
     return st;
   if (s_out != nullptr) return launch_rht_cross(up, nullptr, reinterpret_cast<__half*>(y), M, m, nullptr, 0, cs);
   return EXL3_OK;
+}
+
+extern "C" size_t exl3_gemm_whole_grouped_workspace_bytes(const exl3_layer* layers, int count, int M) {
+  if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP || M < 1 || M > EXL3_MAX_BATCH) return 0;
+  int ones = 0;
+  size_t vecs = 0;
+  for (int i = 0; i < count; ++i) {
+    const int m = layers[i].m, n = layers[i].n;
+    if (!whole_length(m) || !whole_length(n)) return 0;
+    ones = m > ones ? m : ones;
+    ones = n > ones ? n : ones;
+    vecs += align256(sizeof(__half) * static_cast<size_t>(M) * n) + align256(sizeof(__half) * static_cast<size_t>(M) * m);
+  }
+  const size_t inner = exl3_group_workspace_bytes(layers, count, M);
+  if (inner == 0) return 0;
+  return align256(inner) + align256(sizeof(__half) * static_cast<size_t>(ones)) + vecs;
+}
+
+extern "C" exl3_status exl3_gemm_whole_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
+                                               void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_SHAPE;
+  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+  for (int i = 0; i < count; ++i)
+    if (!whole_length(layers[i].m) || !whole_length(layers[i].n)) return EXL3_ERR_SHAPE;
+  exl3_status st = check_k_cb(K, codebook);
+  if (st != EXL3_OK) return st;
+  for (int i = 0; i < count; ++i) {
+    const exl3_layer& L = layers[i];
+    if (!L.codes || !L.scales || !L.x || !L.y) return EXL3_ERR_NULL;
+    if (!aligned16(L.codes) || !aligned16(L.scales) || !aligned16(L.x) || !aligned16(L.y) ||
+        (L.s_in && !aligned16(L.s_in)) || (L.s_out && !aligned16(L.s_out)))
+      return EXL3_ERR_ALIGN;
+  }
+  if (!workspace || workspace_bytes < exl3_gemm_whole_grouped_workspace_bytes(layers, count, M))
+    return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // [inner group workspace | unit signs | x' of every layer | u of every layer]
+  char* ws = static_cast<char*>(workspace);
+  const size_t inner = align256(exl3_group_workspace_bytes(layers, count, M));
+  int ones_len = 0;
+  for (int i = 0; i < count; ++i) {
+    ones_len = layers[i].m > ones_len ? layers[i].m : ones_len;
+    ones_len = layers[i].n > ones_len ? layers[i].n : ones_len;
+  }
+  __half* ones = reinterpret_cast<__half*>(ws + inner);
+  char* cur = ws + inner + align256(sizeof(__half) * static_cast<size_t>(ones_len));
+  exl3_layer in_layers[EXL3_MAX_GROUP];
+  CrossGroup gin{}, gout{};
+  gin.rows = gout.rows = M;
+  gin.ones = ones;
+  gin.ones_len = ones_len;
+  for (int i = 0; i < count; ++i) {
+    const exl3_layer& L = layers[i];
+    __half* xp = reinterpret_cast<__half*>(cur);
+    cur += align256(sizeof(__half) * static_cast<size_t>(M) * L.n);
+    __half* up = reinterpret_cast<__half*>(cur);
+    cur += align256(sizeof(__half) * static_cast<size_t>(M) * L.m);
+    in_layers[i] = L;
+    if (L.s_in != nullptr) {
+      cross_add(gin, reinterpret_cast<const __half*>(L.x), reinterpret_cast<const __half*>(L.s_in), xp, L.n);
+      in_layers[i].x = reinterpret_cast<const exl3_half*>(xp);
+      in_layers[i].s_in = reinterpret_cast<const exl3_half*>(ones);
+    }
+    if (L.s_out != nullptr) {
+      cross_add(gout, up, nullptr, reinterpret_cast<__half*>(L.y), L.m);
+      in_layers[i].y = reinterpret_cast<exl3_half*>(up);
+    }
+  }
+  if ((st = launch_cross_group(gin, cs)) != EXL3_OK) return st;
+  if ((st = exl3_gemm_grouped(in_layers, count, K, codebook, M, workspace, inner, stream)) != EXL3_OK) return st;
+  return launch_cross_group(gout, cs);
 }
