@@ -233,3 +233,20 @@ def test_prefill_narrow_tiles_two_rounds_and_split(dense_strategy, M):
         y, ws = _run(inp, K, cb, m, n, M)
         assert_layer_close(y, ref, f"{m}x{n} M={M}")
         _dense_scratch_left_zero(ws, m, n, M)
+
+
+@pytest.mark.parametrize("M", [100, 200])
+@pytest.mark.parametrize("K,cb", [(2, 0), (3, 2), (4, 3), (5, 1)])
+def test_prefill_fused_codes_on_wide_tiles(K, cb, M):
+    """The fused kernel's 128- and 256-row tiles with every code: the
+    three-instruction codes as defined binary16 weights, the byte-sum codes as
+    exact centred sums with the scale applied to z."""
+    _select("fused")
+    try:
+        m, n = 384, 640
+        inp = synth.layer_inputs(m, n, K, M, config=85, index=10 * K + cb + M)
+        y, ws = _run(inp, K, cb, m, n, M)
+        assert_layer_close(y, _ref(inp, K, cb, m, n), f"fused K={K} cb={cb} M={M}")
+        _dense_scratch_left_zero(ws, m, n, M)
+    finally:
+        _reset()
