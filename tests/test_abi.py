@@ -54,6 +54,21 @@ def test_debug_hook_and_path_setter(lib):
         assert lib.exl3_set_prefill(s) == 0
 
 
+def test_prefill_strategy_launch_counts(lib):
+    """exl3_gemm above 32 rows: two launches fused (operand B, fused GEMM),
+    three decode-once (decode to images, operand B, GEMM); AUTO takes the
+    fused kernel up to 256 rows."""
+    try:
+        assert lib.exl3_set_prefill(1) == 0
+        assert lib.exl3_gemm_launches(256, 512, 64) == 2 and lib.exl3_gemm_launches(256, 512, 1000) == 2
+        assert lib.exl3_set_prefill(2) == 0
+        assert lib.exl3_gemm_launches(256, 512, 64) == 3
+        assert lib.exl3_set_prefill(0) == 0
+        assert lib.exl3_gemm_launches(256, 512, 256) == 2 and lib.exl3_gemm_launches(256, 512, 257) == 3
+    finally:
+        lib.exl3_set_prefill(0)
+
+
 def test_workspace_bytes(lib):
     assert B.exl3_workspace_bytes(100, 128, 1) == 0
     assert B.exl3_workspace_bytes(128, 128, 0) == 0

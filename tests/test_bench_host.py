@@ -86,3 +86,14 @@ def test_kernels_per_group():
     assert bench.kernels_per_group("auto", 5, [(4096, 4096), (1024, 4096)], sms) == 6
     assert bench.kernels_per_group("shuffle", 5, [(4096, 4096), (1024, 4096)], sms) == 6
     assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 2
+
+
+def test_decoder_groups_whole_vector_stack():
+    """The whole-vector workload groups q, k and v of each layer (one
+    exl3_gemm_whole_grouped call) and runs o alone."""
+    gemvs = synth.whole_attention_stack()
+    g = bench.decoder_groups(gemvs)
+    assert len(g) == 16
+    for x in g:
+        names = [gemvs[i][0].split(".")[1] for i in x]
+        assert names in (["q", "k", "v"], ["o"])
