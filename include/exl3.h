@@ -369,7 +369,7 @@ size_t exl3_gemm_whole_grouped_workspace_bytes(const exl3_layer *layers, int cou
  * inputs, one transform kernel for every layer's output.  Layers as for
  * exl3_gemm_grouped (s_in / s_out NULL = no rotation on that side); m and n
  * powers of two in [128, 32768] (EXL3_ERR_SHAPE).  Other errors as
- * exl3_gemm_grouped.
+ * exl3_gemm_grouped (EXL3_ERR_BATCH for count or M out of range).
  */
 exl3_status exl3_gemm_whole_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
                                     void *workspace, size_t workspace_bytes, exl3_stream_t stream);

@@ -270,7 +270,7 @@ extern "C" size_t exl3_gemm_whole_grouped_workspace_bytes(const exl3_layer* laye
 extern "C" exl3_status exl3_gemm_whole_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
                                                void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
   if (layers == nullptr) return EXL3_ERR_NULL;
-  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_SHAPE;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;  // as exl3_gemm_grouped
   if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
   for (int i = 0; i < count; ++i)
     if (!whole_length(layers[i].m) || !whole_length(layers[i].n)) return EXL3_ERR_SHAPE;
