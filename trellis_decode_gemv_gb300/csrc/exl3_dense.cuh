@@ -81,10 +81,10 @@ constexpr int kEpiWarps = 8;  // warps 0-3 and 6-9
 constexpr int kEpiThreads = 32 * kEpiWarps;
 template <int K>
 struct Roles {
-  // fused: kLanes groups of eight decode warps (one per tile row of a stage),
-  // group g decoding the stages seq with seq % kLanes == g
-  static constexpr int kLanes = 2;
-  static constexpr int kDecodeWarps = K == 0 ? 0 : 8 * kLanes;
+  // fused: kGroups groups of eight decode warps (one per tile row of a
+  // stage), group g decoding the stages seq with seq % kGroups == g
+  static constexpr int kGroups = 2;
+  static constexpr int kDecodeWarps = K == 0 ? 0 : 8 * kGroups;
   static constexpr int kThreads = (kDecWarp0 + kDecodeWarps) * 32;
 };
 constexpr int kSlice = 32;          // batch columns per epilogue slice
@@ -209,11 +209,12 @@ __device__ __forceinline__ void finish_rows(const DenseParams& p, float4 z, cons
   *reinterpret_cast<uint2*>(p.y + b * p.m + r0) = o;
 }
 
-// Decode warp (d, g) of the fused kernel: tile row d of every kLanes-th
-// stage's 128-row block (stages g, g + kLanes, ...), 4 tiles of 16 columns.  Lane (jt, pp) = (lane / 8, lane % 8) decodes
-// rows 2pp and 2pp + 1 of tile jt (32 consecutive steps of the tile's
-// stream) into the stage's operand-A image: 16 bytes of a row per store, row
-// r of the block at (column group) * 2048 + r * 16.  Lanes with pp >= 4 store
+// Decode warp (d, g) of the fused kernel: tile row d of the 128-row block of
+// every kGroups-th stage (stages g, g + kGroups, ...), 4 tiles of 16 columns.
+// Lane (jt, pp) = (lane / 8, lane % 8) decodes rows 2pp and 2pp + 1 of tile
+// jt (32 consecutive steps of the tile's stream) into the stage's operand-A
+// image: 16 bytes of a row per store, row r of the block at (column group) *
+// 2048 + r * 16.  Lanes with pp >= 4 store
 // their second row first, so the eight lanes of each store phase cover all 32
 // banks.  The code words of the next kAhead stages are in flight (registers)
 // while a stage decodes: one stage's decode is shorter than an L2 round trip.
@@ -250,7 +251,7 @@ template <int NB, int K, int CB>
 __device__ __forceinline__ void decode_role(const DenseParams& p, DenseShared& sh, unsigned char* ring,
                                             int d, int g, int lane, int my_units, int nstage) {
   using S = Shape<NB>;
-  constexpr int kLanes = Roles<K>::kLanes;
+  constexpr int kGroups = Roles<K>::kGroups;
   constexpr int kStages = S::kStages;
   constexpr int kWords = RowPair<K>::kPairWords;
   const int jt = lane >> 3;
@@ -285,14 +286,14 @@ __device__ __forceinline__ void decode_role(const DenseParams& p, DenseShared& s
       const uint32_t* t =
           p.codes + (static_cast<size_t>(c.w.rb * 8 + d) * tpr + static_cast<size_t>(c.ks) * 4 + jt) * (8 * K);
       load_row_pair<K>(t, pp, dst);
-      requested += kLanes;
-      for (int i = 0; i < kLanes; ++i) advance();
+      requested += kGroups;
+      for (int i = 0; i < kGroups; ++i) advance();
     }
   };
   uint32_t q[kAhead + 1][kWords];  // q[i]: the words of this warp's i-th next stage
 #pragma unroll
   for (int i = 0; i < kAhead; ++i) request(q[i]);
-  for (int seq = g; seq < total; seq += kLanes) {
+  for (int seq = g; seq < total; seq += kGroups) {
     request(q[kAhead]);
     uint32_t st[32];
     pair_states<K>(q[0], st);
