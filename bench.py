@@ -70,6 +70,10 @@ TRAFFIC_RATIO = {
     "shuffle": (29.445 / 29.38, "the ncu capture of layer_kernel on gate/up/down 14336x4096 K4 1MAD"),
     "tensor": (23.12 / 22.15, "the ncu capture of tc_layer_kernel on 14336x4096 K3 1MAD at batch 16"),
     "dense": (None, None),
+    # DRAM reads 26.0 + 26.6 MB against 2 x 23.86 MB of algorithmic bytes
+    "fused64": ((26.0 + 26.6) / (2 * 23.86),
+                "the ncu capture of the fused dense_kernel (64-row tiles) on 14336x4096 and 4096x14336 K3 1MAD "
+                "at batch 48"),
     "int8": (None, None),
 }
 
@@ -568,10 +572,11 @@ def run_ours(args):
         achieved, peak, unit = bytes_step / t_step / 1e9, hbm_gbs, "GB/s"
     tensor = (args.path == "tensor" or (args.path == "auto" and M > 2)) and not int8
     dense = M > 32 and args.path != "tensor"
+    fused = dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256))
     if int8:
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
-    elif dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256)):
+    elif fused:
         kname = ("dense_kernel, fused (sixteen warps decode each stage's codes into the operand-A image in shared "
                  "memory; tcgen05 128xNx16 MMAs, N = 64/128/256 by batch) + operand-B kernel")
     elif dense:
@@ -581,7 +586,8 @@ def run_ours(args):
         kname = "tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"
     else:
         kname = "layer_kernel (fused input RHT + trellis decode + GEMV) + output kernel"
-    ratio, ratio_src = TRAFFIC_RATIO["int8" if int8 else "dense" if dense else "tensor" if tensor else "shuffle"]
+    ratio, ratio_src = TRAFFIC_RATIO["int8" if int8 else ("fused64" if fused and M <= 64 else "dense") if dense
+                                     else "tensor" if tensor else "shuffle"]
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": None if ratio is None else ratio * bytes_step,
                 "traffic_note": ("no ncu DRAM capture of this kernel yet" if ratio is None else
