@@ -72,6 +72,7 @@ TRAFFIC_RATIO = {
     "dense": (None, None),
     # DRAM reads 26.0 + 26.6 MB against 2 x 23.86 MB of algorithmic bytes; the
     # packed codes are most of both, so the ratio holds for tiles up to 128 rows
+    "mv": (None, None),
     "fused": ((26.0 + 26.6) / (2 * 23.86),
               "the ncu capture of the fused dense_kernel (128-row tiles) on 14336x4096 and 4096x14336 K3 1MAD "
               "at batch 48"),
@@ -134,17 +135,17 @@ def workload(name: str, batch: int):
 
 
 def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
-    """Kernel launches of one exl3_gemm_small call.  Tensor-core path: the
-    operand-image kernel, the persistent MMA kernel and the output kernel.
-    Warp-shuffle path, per batch chunk of 8, 4, 2 or 1 rows: layer kernel and
-    output kernel, plus the x-pair kernel when the chunk runs the sub-unit
-    kernel (chunks above 2 rows, or at least 1024 tiles per SM)."""
-    tensor = path == "tensor" or (path == "auto" and M > 2)
+    """Kernel launches of one exl3_gemm_small call.  Decode-MMA kernel (every
+    path but the warp-shuffle one): one launch at M <= 2, plus the
+    operand-image kernel above.  Warp-shuffle path, per batch chunk of 8, 4, 2
+    or 1 rows: layer kernel and output kernel, plus the x-pair kernel when the
+    chunk runs the sub-unit kernel (chunks above 2 rows, or at least 1024
+    tiles per SM)."""
     if M > 32:
         from trellis_decode_gemv_gb300 import binding as B
         return B.exl3_gemm_launches(m, n, M)
-    if tensor:
-        return 3
+    if path != "shuffle":
+        return 1 if M <= 2 else 2
     tiles_per_sm = (m // 16) * (n // 16) // sms
     launches, rem = 0, M
     for c in (8, 4, 2, 1):
@@ -192,14 +193,13 @@ def decoder_groups(gemvs, grouped: bool = True):
 
 def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     """Kernel launches of one grouped call over layers of the given (m, n):
-    three per batch chunk on the warp-shuffle path (x pairs, one sub-unit
-    kernel over every layer, output transform); one exl3_gemm_small-like
-    tensor-core chain (three kernels) per layer above batch 2."""
+    one decode-MMA launch over every layer (plus one operand-image kernel per
+    layer above batch 2); on the warp-shuffle path three per batch chunk (x
+    pairs, one sub-unit kernel over every layer, output transform)."""
     if len(shapes) == 1:
         return kernels_per_call(path, M, shapes[0][0], shapes[0][1], sms)
-    tensor = path == "tensor" or (path == "auto" and M > 2)
-    if tensor:
-        return 3 * len(shapes)
+    if path != "shuffle":
+        return 1 if M <= 2 else 1 + len(shapes)
     chunks, rem = 0, M
     for c in (8, 4, 2, 1):
         while rem >= c:
@@ -224,6 +224,9 @@ def algorithmic(m, n, K, cb, M, path="auto", int8=False):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi sampling of the SM clock, power and throttle reasons every
+    50 ms while the benchmark runs; statistics over the samples taken since
+    the last mark (one timed region) or over the whole run."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -232,6 +235,7 @@ class ClockSampler:
         self.proc = None
         self.bus_id = bus_id
         self.path = None
+        self._mark = 0
 
     def start(self):
         try:
@@ -246,31 +250,27 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
-        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        if self.proc is None:
-            out["reasons"] = ["unsampled"]
-            return out
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(5)
-        except Exception:
-            self.proc.kill()
+    def _rows(self):
         rows = []
         try:
             for line in open(self.path):
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 8:
                     rows.append(parts)
-            os.unlink(self.path)
         except Exception:
             pass
+        return rows
+
+    @staticmethod
+    def _stats(rows):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": len(rows)}
         if not rows:
             out["reasons"] = ["unsampled"]
             return out
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        num = lambda v: v.replace(".", "").isdigit()  # noqa: E731
+        sm = [float(r[0]) for r in rows if num(r[0])]
+        mx = [float(r[1]) for r in rows if num(r[1])]
+        pw = [float(r[2]) for r in rows if num(r[2])]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -278,10 +278,34 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         out.update(sm_mhz=float(np.median(sm)) if sm else None, sm_max_mhz=max(mx) if mx else None,
-                   reasons=sorted(reasons), samples=len(rows),
-                   power_w_max=max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
-                   if any(r[2].replace(".", "").isdigit() for r in rows) else None)
+                   reasons=sorted(reasons), power_w_max=max(pw) if pw else None)
         return out
+
+    def mark(self):
+        if self.proc is not None:
+            self._mark = len(self._rows())
+
+    def since_mark(self):
+        if self.proc is None:
+            return self._stats([])
+        time.sleep(0.12)  # the sample covering the region's end
+        return self._stats(self._rows()[self._mark:])
+
+    def stop(self):
+        if self.proc is None:
+            return self._stats([])
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        rows = self._rows()
+        try:
+            os.unlink(self.path)
+        except Exception:
+            pass
+        return self._stats(rows)
 
 
 # ---------------------------------------------------------------------------
@@ -357,8 +381,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    desc, cfg, gemvs, M = workload(args.workload, args.batch)
-    whole = args.workload == "whole"
+    # the default run's headline is the Llama-3-8B layer set
+    wl = "llama8b" if args.workload == "all" else args.workload
+    desc, cfg, gemvs, M = workload(wl, args.batch)
+    whole = wl == "whole"
     per_step = 1 if whole else min(6, len(gemvs))
     # the whole-vector oracle runs full layers: take the smallest GEMVs
     pool = [i for i, g in enumerate(gemvs) if g[1] * g[2] == min(h[1] * h[2] for h in gemvs)] if whole \
@@ -395,51 +421,82 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
-    from trellis_decode_gemv_gb300 import binding as B
+def int_peak_probe(B, torch, dev, stream, sms, clocks_mhz):
+    """The integer-throughput probe (exl3_probe_int): ops per clock per SM of
+    each instruction kind and of the two mixes, timed with CUDA events on the
+    stream; the measured INT32 peak is the best mix in ops/s."""
+    blocks, iters = 8 * sms, 256
+    out = torch.empty(blocks * 256, dtype=torch.int32, device=dev)
+    res = {}
+    with torch.cuda.stream(stream):
+        for kind in sorted(B.PROBE_KINDS):
+            B.exl3_probe_int(kind, out, blocks, iters)  # warm-up
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 5
+            e0.record(stream)
+            for _ in range(reps):
+                ops = B.exl3_probe_int(kind, out, blocks, iters)
+            e1.record(stream)
+            stream.synchronize()
+            sec = e0.elapsed_time(e1) * 1e-3
+            rate = ops * reps / sec
+            res[B.PROBE_KINDS[kind]] = {"ops_per_s": rate, "ops_per_clk_sm": rate / (sms * clocks_mhz * 1e6)}
+    best = max(("IMAD+LOP3", "IMAD+IDP4A+LOP3+SHF"), key=lambda k: res[k]["ops_per_s"])
+    return {"kinds": res, "peak_ops_per_s": res[best]["ops_per_s"], "peak_kind": best,
+            "clock_mhz_assumed": clocks_mhz,
+            "how": (f"exl3_probe_int: {blocks} CTAs x 256 threads x 8 independent chains x {4 * iters} "
+                    "instructions, 5 launches per kind, CUDA events; ops/clk/SM at the stated clock")}
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
-    B.load_library()
-    B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[args.path])
-    B.exl3_set_prefill({"auto": B.PREFILL_AUTO, "fused": B.PREFILL_FUSED,
-                        "decode_once": B.PREFILL_DECODE_ONCE}[args.prefill])
 
-    desc, cfg, gemvs, M = workload(args.workload, args.batch)
-    hbm_gbs, sm_max_mhz, bf16_tflops, peak_src = measured_peaks()
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    p_int = sms * INT_LANES_PER_SM_CLK * sm_max_mhz * 1e6
+def launches_of_group(B, path, M, shapes, sms, whole, int8):
+    """Kernel launches of one call of the step (a single layer or a group)."""
+    if whole:
+        if len(shapes) == 1:
+            return B.exl3_gemm_launches(shapes[0][0], shapes[0][1], M) + 2
+        return kernels_per_group(path, M, shapes, sms) + 2
+    if int8:
+        return 2 + int8_chunks(M)
+    return kernels_per_group(path, M, shapes, sms)
+
+
+def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cpu=False):
+    """One workload: resident inputs, warm-up, graph capture, `steps` timed
+    graph replays (CUDA events on the launch stream), per-call apportioning,
+    roofline terms, the end-to-end leg and (optionally) the oracle baseline."""
+    torch, B, dev, stream = ctx["torch"], ctx["B"], ctx["dev"], ctx["stream"]
+    sms, world, rank = ctx["sms"], ctx["world"], ctx["rank"]
+    hbm_gbs, bf16_tflops, peak_src, p_int = ctx["hbm_gbs"], ctx["bf16_tflops"], ctx["peak_src"], ctx["p_int"]
+    desc, cfg, gemvs, M = workload(wl, batch)
 
     # ---- resident inputs ------------------------------------------------
+    # Codes are uniform random words drawn on the device (torch's Philox
+    # generator, seeded per tensor from the same seed table as the host
+    # generator): tens of GB for the largest stacks.  Signs, scales and x come
+    # from the host generator.
     total_n = sum(g[2] for g in gemvs) * M
     total_m = sum(g[1] for g in gemvs) * M
     X = torch.empty(total_n, dtype=torch.float16, device=dev)
     Y = torch.empty(total_m, dtype=torch.float16, device=dev)
     calls = []
     xo = yo = 0
-    whole = args.workload == "whole"
-    int8 = args.workload == "int8"
+    whole = wl == "whole"
+    int8 = wl == "int8"
     ws_of = (B.exl3_gemm_whole_workspace_bytes if whole else B.exl3_gemm_i8_workspace_bytes if int8
              else B.exl3_gemm_workspace_bytes)
     ws_bytes = max(ws_of(m, n, M) for _, m, n, _, _ in gemvs)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     packed = 0
+    gen = torch.Generator(device=dev)
     for i, (name, m, n, K, cb) in enumerate(gemvs):
-        inp = synth.layer_inputs(m, n, K, M, config=cfg, index=i)
-        codes = torch.from_numpy(inp["codes"].view(np.int32)).to(dev)
-        s_in = torch.from_numpy(inp["s_in"]).to(dev)
-        s_out = torch.from_numpy(inp["s_out"]).to(dev)
-        scales = torch.from_numpy(inp["scales"]).to(dev)
-        X[xo:xo + M * n] = torch.from_numpy(inp["x"].reshape(-1)).to(dev)
+        words = (m // 16) * (n // 16) * 8 * K
+        gen.manual_seed(synth.seed_for(cfg, 10 * i) & ((1 << 63) - 1))
+        codes = torch.randint(-(1 << 31), 1 << 31, (words,), generator=gen, device=dev, dtype=torch.int64).to(
+            torch.int32)
+        b = 10 * i
+        s_in = torch.from_numpy(synth.sign_vector(n, synth.seed_for(cfg, b + 1))).to(dev)
+        s_out = torch.from_numpy(synth.sign_vector(m, synth.seed_for(cfg, b + 2))).to(dev)
+        scales = torch.from_numpy(synth.channel_scales(m, synth.seed_for(cfg, b + 3))).to(dev)
+        X[xo:xo + M * n] = torch.from_numpy(synth.activations(M, n, synth.seed_for(cfg, b + 4)).reshape(-1)).to(dev)
         x = X[xo:xo + M * n].view(M, n)
         y = Y[yo:yo + M * m].view(M, m)
         calls.append(dict(name=name, m=m, n=n, K=K, cb=cb, codes=codes, s_in=s_in, s_out=s_out,
@@ -448,7 +505,6 @@ def run_ours(args):
         xo += M * n
         yo += M * m
     torch.cuda.synchronize(dev)
-    stream = torch.cuda.Stream(dev)
 
     # grouped calls take at most 32 batch rows
     groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
@@ -488,7 +544,7 @@ def run_ours(args):
 
     # ---- warm-up + graph capture ----------------------------------------
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(max(warmup, 3)):
             step()
     torch.cuda.synchronize(dev)
     graph = None
@@ -511,28 +567,26 @@ def run_ours(args):
         else:
             step()
 
-    # ---- timed region: K steps ------------------------------------------
-    bus = getattr(props, "pci_bus_id", None)
-    clocks = ClockSampler(bus if isinstance(bus, str) else None)
-    clocks.start()
+    # ---- timed region: `steps` steps ----------------------------------------
+    ctx["clocks"].mark()
     barrier()
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    clk = clocks.stop()
+    clk = ctx["clocks"].since_mark()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
-    ms_step = ms_total / args.steps
-    value = whole_job_rate(weights_step, world, args.steps, ms_total / 1e3)
+    ms_step = ms_total / steps
+    value = whole_job_rate(weights_step, world, steps, ms_total / 1e3)
 
     # ---- per-launch durations (events around every launch) ---------------
-    nrep = max(3, min(args.steps, 50))
+    nrep = max(3, min(steps, 20))
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(groups) + 1)]
     gdur = np.zeros(len(groups))
     with torch.cuda.stream(stream):
@@ -559,9 +613,10 @@ def run_ours(args):
     t_hbm = np.array([a[1] / (hbm_gbs * 1e9) for a in alg])
     t_int = np.array([a[2] / p_int for a in alg])
     # tensor-core term: 2 M m n flops at the measured dense bf16 (= fp16) peak
-    flops_step = 2.0 * M * sum(c["m"] * c["n"] for c in calls) if (M > 2 and not int8) else 0.0
+    # (above 32 rows only: below, the MMAs' flops are far under the peak)
+    flops_step = 2.0 * M * sum(c["m"] * c["n"] for c in calls) if (M > 32 and not int8) else 0.0
     p_tensor = bf16_tflops * 1e12
-    t_tc = np.array([2.0 * M * c["m"] * c["n"] / p_tensor if (M > 2 and not int8) else 0.0 for c in calls])
+    t_tc = np.array([2.0 * M * c["m"] * c["n"] / p_tensor if (M > 32 and not int8) else 0.0 for c in calls])
     t_roof = np.maximum(np.maximum(t_hbm, t_int), t_tc)
     terms = {"alu": t_int.sum(), "hbm": t_hbm.sum(), "tensor": t_tc.sum()}
     bound = max(terms, key=terms.get)
@@ -571,31 +626,40 @@ def run_ours(args):
         achieved, peak, unit = flops_step / t_step / 1e12, bf16_tflops, "TFLOP/s"
     else:
         achieved, peak, unit = bytes_step / t_step / 1e9, hbm_gbs, "GB/s"
-    tensor = (args.path == "tensor" or (args.path == "auto" and M > 2)) and not int8
+    shuffle = args.path == "shuffle" and M <= 32
     dense = M > 32 and args.path != "tensor"
+    passes = M > 32 and args.path == "tensor"
     fused = dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256))
     if int8:
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
+        tkey = "int8"
     elif fused:
         kname = ("dense_kernel, fused (sixteen warps decode each stage's codes into the operand-A image in shared "
                  "memory; tcgen05 128xNx16 MMAs, N = 64/128/256 by batch) + operand-B kernel")
+        tkey = "fused" if M <= 128 else "dense"
     elif dense:
         kname = ("dense_kernel (tcgen05 128xNx16 MMAs, N = 64/128/256 by batch, both operands in shared memory) + "
                  "decode-to-operand-image, operand-B and output kernels")
-    elif tensor:
-        kname = "tc_layer_kernel (decoded tiles in TMEM -> tcgen05 MMAs) + operand-image and output kernels"
+        tkey = "dense"
+    elif passes:
+        kname = "tc_layer_kernel (128-row passes: decoded tiles in TMEM -> tcgen05 MMAs) + operand and output kernels"
+        tkey = "tensor"
+    elif shuffle:
+        kname = "layer_kernel / seg_layer_kernel (trellis decode + HFMA2 + warp shuffles) + x-pair and output kernels"
+        tkey = "shuffle"
     else:
-        kname = "layer_kernel (fused input RHT + trellis decode + GEMV) + output kernel"
-    ratio, ratio_src = TRAFFIC_RATIO["int8" if int8 else ("fused" if fused and M <= 128 else "dense") if dense
-                                     else "tensor" if tensor else "shuffle"]
+        kname = ("mv_kernel (decode into TMEM, tcgen05 128xNx16 MMAs; input RHT by in-kernel x warps at M <= 2, "
+                 "output RHT by the CTA completing each 128-row block)" + (" + operand-image kernel" if M > 2 else ""))
+        tkey = "mv"
+    ratio, ratio_src = TRAFFIC_RATIO[tkey]
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": None if ratio is None else ratio * bytes_step,
                 "traffic_note": ("no ncu DRAM capture of this kernel yet" if ratio is None else
                                  f"bytes per step: algorithmic bytes x {ratio:.3f}, the DRAM/algorithmic "
                                  f"ratio of {ratio_src}"),
                 "peak_source": (f"INT32: {sms} SMs x {INT_LANES_PER_SM_CLK} lanes/clk x "
-                                f"{sm_max_mhz:.0f} MHz (derived)") if bound == "alu"
+                                f"{ctx['sm_max_mhz']:.0f} MHz (derived)") if bound == "alu"
                 else (f"dense bf16 GEMM ({peak_src}; fp16 MMAs run at the same rate)" if bound == "tensor"
                       else f"HBM copy bandwidth ({peak_src})"),
                 "kernel": kname,
@@ -603,6 +667,10 @@ def run_ours(args):
                 "per_call_us_mean": 1e6 * t_step / len(groups),
                 "eager_call_us_mean": 1e6 * dur.sum() / len(groups),
                 "calls_per_step": len(groups)}
+    if bound == "alu" and ctx.get("probe"):
+        pm = ctx["probe"]["peak_ops_per_s"] / 1e12
+        roofline.update(peak_measured=pm, frac_measured=achieved / pm,
+                        peak_measured_source=f"exl3_probe_int, {ctx['probe']['peak_kind']} chains (measured)")
     hbm = {"achieved_gbs": bytes_step / t_step / 1e9, "peak_gbs": hbm_gbs, "peak_source": peak_src,
            "frac": bytes_step / t_step / 1e9 / hbm_gbs}
     roof_pct = 100.0 * t_roof.sum() / t_step
@@ -619,8 +687,59 @@ def run_ours(args):
                    for k, v in sorted(per.items())}
 
     # ---- e2e: host buffers, copies inside the timed region ---------------
-    # The public per-layer objects of the binding (marshalled once, as a model
-    # holds its layers), one call per group; x and y are the bound tensors.
+    e2e = None
+    if want_e2e:
+        e2e = measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps)
+
+    # ---- CPU oracle baseline (rank 0, N=1 only) --------------------------
+    cpu = None
+    if want_cpu and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nsel = len(gemvs) if wl == "llama8b" else min(len(gemvs), 8)
+        sel = list(range(nsel)) if nsel == len(gemvs) else list(range(0, len(gemvs), max(1, len(gemvs) // nsel)))[:nsel]
+        if whole:  # full layers: the three smallest (k/v) GEMVs
+            sel = sorted(range(len(gemvs)), key=lambda i: gemvs[i][1] * gemvs[i][2])[:3]
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, target_s=12.0, whole=whole)
+        cpu = {"value": w / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
+               "sample": (f"{len(sel)} whole GEMVs (the smallest of the workload; {w / 1e6:.1f} M weights, "
+                          f"{dt:.1f} s), oracle whole-vector layer forward") if whole else
+                         (f"128-row output blocks of each of {len(sel)} GEMVs of the workload "
+                          f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward")}
+
+    launches_step = sum(launches_of_group(B, args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms,
+                                          whole, int8) for g in groups)
+    res = {
+        "value": value, "unit": "weights/s", "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
+        "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
+                   "weights_per_step": weights_step, "packed_bytes_per_step": packed,
+                   "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
+                   "cuda_graph": graph is not None, "kernel_path": args.path, "prefill": args.prefill,
+                   "calls": ("q/k/v grouped per exl3_gemm_whole_grouped call, o one exl3_gemm_whole call"
+                             if whole and not args.ungrouped and M <= 32 else "one exl3_gemm_whole call per GEMV")
+                   if whole else
+                   ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
+                    "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
+                   if int8 else
+                   "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
+                   else "one exl3_gemm_small call per GEMV"},
+        "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
+        "macs_per_s": value * M,
+        "roofline_pct": roof_pct,
+        "roofline": roofline, "hbm": hbm, "per_code": per_summary,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": steps * launches_step, "launches_per_step": launches_step,
+        "clocks": clk,
+    }
+    del calls, X, Y, ws, graph
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps):
+    """The same workload through the binding's public per-layer objects,
+    eager, with the step's x copied in from pinned host memory and y copied
+    back inside the timed region."""
+    torch, B, dev, stream, world = ctx["torch"], ctx["B"], ctx["dev"], ctx["stream"], ctx["world"]
     layer_objs = []
     for g in groups:
         if int8 and len(g) > 1:  # the public calls themselves
@@ -658,7 +777,7 @@ def run_ours(args):
     Xh = torch.empty(total_n, dtype=torch.float16, pin_memory=True)
     Xh.copy_(X.cpu())
     Yh = torch.empty(total_m, dtype=torch.float16, pin_memory=True)
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = max(3, min(steps, 200))
     with torch.cuda.stream(stream):
         for _ in range(2):
             X.copy_(Xh, non_blocking=True)
@@ -674,56 +793,104 @@ def run_ours(args):
             stream.synchronize()
         t_e2e = time.perf_counter() - t0
     t_e2e = max_over_ranks(t_e2e, dev)
-    e2e = {"value": whole_job_rate(weights_step, world, e2e_steps, t_e2e), "unit": "weights/s",
-           "h2d_bytes_per_step": total_n * 2, "d2h_bytes_per_step": total_m * 2,
-           "path": ("binding layer objects (Exl3Linear / Exl3LinearGroup), eager calls; pinned host x -> "
-                    "device, y -> pinned host, inside the timed region")}
+    return {"value": whole_job_rate(weights_step, world, e2e_steps, t_e2e), "unit": "weights/s",
+            "steps": e2e_steps, "h2d_bytes_per_step": total_n * 2, "d2h_bytes_per_step": total_m * 2,
+            "path": ("binding layer objects (Exl3Linear / Exl3LinearGroup), eager calls; pinned host x -> "
+                     "device, y -> pinned host, inside the timed region")}
 
-    # ---- CPU oracle baseline (rank 0, N=1 only) --------------------------
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nsel = len(gemvs) if args.workload == "llama8b" else min(len(gemvs), 8)
-        sel = list(range(nsel)) if nsel == len(gemvs) else list(range(0, len(gemvs), max(1, len(gemvs) // nsel)))[:nsel]
-        if whole:  # full layers: the three smallest (k/v) GEMVs
-            sel = sorted(range(len(gemvs)), key=lambda i: gemvs[i][1] * gemvs[i][2])[:3]
-        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, target_s=12.0, whole=whole)
-        cpu = {"value": w / dt, "unit": "weights/s", "cores": 1, "kind": "oracle",
-               "sample": (f"{len(sel)} whole GEMVs (the smallest of the workload; {w / 1e6:.1f} M weights, "
-                          f"{dt:.1f} s), oracle whole-vector layer forward") if whole else
-                         (f"128-row output blocks of each of {len(sel)} GEMVs of the workload "
-                          f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward")}
 
+# The configurations of the default run: the headline (the Llama-3-8B layer
+# set at batch 1) first, then the other four, each timed with the same steps
+# and warm-up.  C3 is the batch sweep on the two MLP shapes.
+ALL_CONFIGS = [("C1", "llama8b", 1), ("C0", "single", 1), ("C2", "llama70b", 1)] + \
+    [(f"C3.M{M}", "sweep", M) for M in synth.BATCH_SWEEP] + [("C4", "mixed", 1)]
+
+
+def _summary(r):
+    """The per-config record of the default run."""
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "effective_gbs", "macs_per_s", "roofline_pct",
+            "gpu_launches", "launches_per_step")
+    out = {k: r[k] for k in keep}
+    out["workload"] = r["config"]["workload"]
+    out["batch"] = r["config"]["batch"]
+    out["weights_per_step"] = r["config"]["weights_per_step"]
+    out["l2"] = r["config"]["l2"]
+    ro = r["roofline"]
+    out["roofline"] = {k: ro[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic") if k in ro}
+    for k in ("peak_measured", "frac_measured"):
+        if k in ro:
+            out["roofline"][k] = ro[k]
+    out["hbm_frac"] = r["hbm"]["frac"]
+    out["e2e"] = None if r["e2e"] is None else {"value": r["e2e"]["value"], "unit": r["e2e"]["unit"]}
+    out["per_code"] = r["per_code"]
+    out["clocks"] = r["clocks"]
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from trellis_decode_gemv_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    B.load_library()
+    B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[args.path])
+    B.exl3_set_prefill({"auto": B.PREFILL_AUTO, "fused": B.PREFILL_FUSED,
+                        "decode_once": B.PREFILL_DECODE_ONCE}[args.prefill])
+    hbm_gbs, sm_max_mhz, bf16_tflops, peak_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    bus = getattr(props, "pci_bus_id", None)
+    clocks = ClockSampler(bus if isinstance(bus, str) else None)
+    clocks.start()
+    stream = torch.cuda.Stream(dev)
+    ctx = dict(torch=torch, B=B, dev=dev, stream=stream, sms=sms, world=world, rank=rank, hbm_gbs=hbm_gbs,
+               bf16_tflops=bf16_tflops, peak_src=peak_src, sm_max_mhz=sm_max_mhz,
+               p_int=sms * INT_LANES_PER_SM_CLK * sm_max_mhz * 1e6, clocks=clocks)
+    ctx["probe"] = int_peak_probe(B, torch, dev, stream, sms, sm_max_mhz)
+
+    if args.workload == "all":
+        runs = {}
+        for key, wl, M in ALL_CONFIGS:
+            runs[key] = measure_workload(ctx, args, wl, M, args.steps, args.warmup,
+                                         want_e2e=True, want_cpu=(key == "C1"))
+        head = runs["C1"]
+    else:
+        head = measure_workload(ctx, args, args.workload, args.batch, args.steps, args.warmup,
+                                want_e2e=True, want_cpu=True)
+        runs = None
+    clk_all = clocks.stop()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "weights/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "metric": METRIC, "value": head["value"], "unit": "weights/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
-            "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
-                       "weights_per_step": weights_step, "packed_bytes_per_step": packed,
-                       "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
-                       "cuda_graph": graph is not None, "kernel_path": args.path,
-                       "prefill": args.prefill,
-                       "calls": ("q/k/v grouped per exl3_gemm_whole_grouped call, o one exl3_gemm_whole call"
-                                 if whole and not args.ungrouped and M <= 32 else "one exl3_gemm_whole call per GEMV")
-                       if whole else
-                       ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
-                        "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
-                       if int8 else
-                       "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
-                       else "one exl3_gemm_small call per GEMV"},
-            "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
-            "macs_per_s": value * M,
-            "roofline_pct": roof_pct,
-            "roofline": roofline, "hbm": hbm, "per_code": per_summary,
-            "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * sum(
-                (B.exl3_gemm_launches(calls[g[0]]["m"], calls[g[0]]["n"], M) + 2) if whole and len(g) == 1 else
-                (kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) + 2) if whole else
-                (2 + int8_chunks(M)) if int8 else
-                kernels_per_group(args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms) for g in groups),
-            "clocks": clk,
+            "dtype": "f16" if args.path != "shuffle" else "f16-partials",
+            "arith": ("binary16 weights x binary16 x-tilde on tcgen05 MMAs, fp32 accumulation in TMEM and fp32 "
+                      "split-K reductions; y rounded once to binary16") if args.path != "shuffle" else
+                     ("binary16 products, 16-column binary16 partial sums, fp32 beyond"),
+            "data": "synthetic",
+            "config": head["config"],
+            "effective_gbs": head["effective_gbs"], "macs_per_s": head["macs_per_s"],
+            "roofline_pct": head["roofline_pct"], "roofline": head["roofline"], "hbm": head["hbm"],
+            "per_code": head["per_code"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "int_peak_probe": ctx["probe"],
+            "clocks": clk_all,
         }
+        if runs is not None:
+            line["configs"] = {k: _summary(v) for k, v in runs.items()}
+            line["configs_note"] = ("every config timed in this run with the same --steps/--warmup: C1 the "
+                                    "headline (top-level fields), C0 single 4096x4096, C2 Llama-3-70B stack, "
+                                    "C3 batch sweep M=1..32, C4 mixed 2.9 bpw stack + lm_head")
+            line["gpu_launches_all_configs"] = sum(v["gpu_launches"] for v in runs.values())
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -734,12 +901,23 @@ ENCODE_METRIC = "tail-biting Viterbi encode, weights (trellis steps) encoded per
 ENCODE_TILES = 1216  # 8 tiles per SM of a GB300
 
 
+def code_rms(cb: int) -> float:
+    """Closed-form rms value of a code's weights over uniform states.  The
+    byte-sum codes are centred and scaled to unit variance by definition.  A
+    three-instruction weight is the sum of two independent binary16 halves of
+    random sign, biased exponent uniform in 12..15 and a uniform 10-bit
+    mantissa: E[w^2] = 2 * (1/4) * sum_e 4^(e-15) * mean_k (1 + k/1024)^2."""
+    if cb in (synth.CB_1MAD, synth.CB_MUL1):
+        return 1.0
+    k = np.arange(1024, dtype=np.float64)
+    m2 = float(np.mean((1.0 + k / 1024.0) ** 2))
+    return float(np.sqrt(2.0 * 0.25 * sum(4.0 ** (e - 15) for e in range(12, 16)) * m2))
+
+
 def encode_inputs(K: int, cb: int, tiles: int):
     """Unit-Gaussian sequences scaled by the code's rms value (code units),
     binary32 [tiles][256], and that rms value."""
-    from oracle import exl3_oracle as O  # the codebook's rms value only: an input of both sides
-    raw = O.decode_states(np.arange(1 << 16, dtype=np.uint32), cb).astype(np.float64)
-    sigma = float(np.sqrt(np.mean(raw ** 2)))
+    sigma = code_rms(cb)
     g = synth.activations(tiles, 256, synth.seed_for(8, 0)).astype(np.float64)
     return (g * sigma).astype(np.float32), sigma
 
@@ -888,9 +1066,10 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b",
-                    choices=["llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill",
-                             "whole", "encode", "int8", "mad-mul1"])
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "llama8b", "llama8b-mcg-mul1", "single", "llama70b", "mixed", "sweep", "prefill",
+                             "whole", "encode", "int8", "mad-mul1"],
+                    help="all (default): every config, the Llama-3-8B layer set at batch 1 as the headline")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ungrouped", action="store_true",

@@ -462,11 +462,15 @@ exl3_status exl3_device_status(const void *status_word, exl3_stream_t stream);
  * arguments minus the workspace.
  *   - Scratch: a file-scope device array of EXL3_NOALLOC_SCRATCH_BYTES bytes,
  *     present on every GPU that loads the library until the process exits.
- *     A layer whose scratch (m fp32 row sums and m/128 counters) would not
- *     fit is rejected with EXL3_ERR_SCRATCH before anything is launched.
+ *     A layer fits if a256(4*(m/128 + 1)) + a256(4*m) + a256(4*n) <=
+ *     EXL3_NOALLOC_SCRATCH_BYTES, a256 rounding up to a multiple of 256 (the
+ *     block counters and status word, m fp32 row sums, n 32-bit x pairs);
+ *     a larger layer is rejected with EXL3_ERR_SCRATCH before anything is
+ *     launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  `stream` must belong to the current device
+ *     (EXL3_ERR_CUDA otherwise: the address is per device).
  *   - Every call shares the one array and clears its counters and row sums
  *     with an asynchronous memset on `stream`.  Calls whose work can overlap on the
  *     GPU (other streams, other host threads) race: serialize them.
@@ -476,6 +480,21 @@ exl3_status exl3_gemv_noalloc(const uint32_t *codes, int K, int codebook, int m,
                               const exl3_half *s_in, const exl3_half *s_out,
                               const exl3_half *scales, const exl3_half *x, exl3_half *y,
                               exl3_stream_t stream);
+
+/**
+ * Integer-throughput probe (a measurement aid; the pages have no counterpart):
+ * launches `blocks` CTAs of 256 threads, each thread running 8 independent
+ * dependency chains of 4*iters instructions of one kind -- 0 IMAD
+ * (mad.lo.u32), 1 LOP3, 2 SHF (funnel shift), 3 IDP4A, 4 PRMT -- or an even
+ * mix over the chains: 5 IMAD + LOP3, 6 IMAD + IDP4A + LOP3 + SHF.  The
+ * caller times it on `stream`; it executes blocks * 8192 * iters
+ * instructions.  The INT32 term of the layer roofline ("Trellis Quantization"
+ * Part three counts the decode in integer instructions per weight) is checked
+ * against it.  out: device array of blocks * 256 uint32 (the chains' results),
+ * 16-byte aligned.  Errors: EXL3_ERR_BATCH (unknown kind), EXL3_ERR_SHAPE
+ * (blocks or iters < 1), EXL3_ERR_NULL, EXL3_ERR_ALIGN, EXL3_ERR_CUDA.
+ */
+exl3_status exl3_probe_int(int kind, uint32_t *out, int blocks, int iters, exl3_stream_t stream);
 
 /** Static, NUL-terminated description of a status code. */
 const char *exl3_status_string(exl3_status status);

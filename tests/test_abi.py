@@ -38,7 +38,7 @@ def _ws(m, n, M):
     counters = a256(4 * (m // 128 + 1))
     zacc = a256(4 * M * m)
     nb = 16 if M <= 16 else 32
-    bimg = a256(2 * nb * n)
+    bimg = a256(2 * 2 * nb * n)  # operand images; the three-instruction codes store each value twice
     bsum = a256(4 * M * (n // 128))
     return counters + zacc + bimg + bsum
 
@@ -136,10 +136,13 @@ def test_group_workspace_bytes(lib):
     shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
     for M in (1, 2, 5, 32):
         mb = min(M, 8)
-        shuffle = 256 + sum(a256(4 * mb * m) + a256(4 * mb * n) for m, n in shapes)
         nb = 16 if M <= 16 else 32
-        tensor = 256 + a256(4 * M * 4096) + a256(2 * nb * 4096) + a256(4 * M * (4096 // 128))
-        assert lib.exl3_group_workspace_bytes(_group(shapes), 3, M) == max(shuffle, tensor)
+        # status word; per layer block counters and row sums; per layer the x
+        # pairs or (M > 2) the decode-MMA kernel's operand images
+        fixed = 256 + sum(a256(4 * (m // 128)) + a256(4 * M * m) for m, n in shapes)
+        scratch = sum(a256(max(4 * mb * n, a256(2 * 2 * nb * n) + 4 * M * (n // 128) if M > 2 else 0))
+                      for m, n in shapes)
+        assert lib.exl3_group_workspace_bytes(_group(shapes), 3, M) == fixed + scratch
     assert lib.exl3_group_workspace_bytes(_group([(100, 128)]), 1, 1) == 0
     assert lib.exl3_group_workspace_bytes(_group(shapes), 0, 1) == 0
     assert lib.exl3_group_workspace_bytes(_group(shapes), 5, 1) == 0

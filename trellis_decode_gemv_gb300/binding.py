@@ -65,6 +65,7 @@ _SIGNATURES = {
     "exl3_gemm_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
     "exl3_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_launches": ([_I, _I, _I], _I),
+    "exl3_probe_int": ([_I, _P, _I, _I, _P], _I),
     "exl3_rht_whole": ([_P, _P, _P, _I, _I, _P], _I),
     "exl3_encode_workspace_bytes": ([_I, _I], _SZ),
     "exl3_quantize_act": ([_P, _I, _I, _P, _P, _P], _I),
@@ -277,11 +278,13 @@ def exl3_gemv_noalloc(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None):
     dev = codes.device
     if y is None:
         y = torch.empty(m, dtype=torch.float16, device=dev)
-    _check(lib.exl3_gemv_noalloc(
-        _ptr(codes, "codes", _WORDS), K, codebook, m, n,
-        _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
-        _ptr(scales, "scales", _HALF, dev), _ptr(x, "x", _HALF, dev), _ptr(y, "y", _HALF, dev),
-        _stream(dev)))
+    # the scratch array's address is per device: make the tensors' device current
+    with torch.cuda.device(dev):
+        _check(lib.exl3_gemv_noalloc(
+            _ptr(codes, "codes", _WORDS), K, codebook, m, n,
+            _ptr(s_in, "s_in", _HALF, dev), _ptr(s_out, "s_out", _HALF, dev),
+            _ptr(scales, "scales", _HALF, dev), _ptr(x, "x", _HALF, dev), _ptr(y, "y", _HALF, dev),
+            _stream(dev)))
     return y
 
 
@@ -572,6 +575,21 @@ def exl3_gemm_int8act(codes, K, codebook, m, n, s_in, s_out, scales, x, y=None, 
         _ptr(y, "y", _HALF, dev), _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
         _stream(dev)))
     return y if x.dim() == 2 else y.view(-1)
+
+
+PROBE_KINDS = {0: "IMAD", 1: "LOP3", 2: "SHF", 3: "IDP4A", 4: "PRMT", 5: "IMAD+LOP3", 6: "IMAD+IDP4A+LOP3+SHF"}
+
+
+def exl3_probe_int(kind: int, out: torch.Tensor, blocks: int, iters: int) -> int:
+    """Launch the integer-throughput probe on the current stream of out's
+    device; returns the number of instructions it executes (blocks * 8192 *
+    iters).  out: int32 tensor of at least blocks * 256 elements."""
+    lib = load_library()
+    dev = out.device
+    if out.numel() < blocks * 256:
+        raise ValueError("out holds fewer than blocks * 256 words")
+    _check(lib.exl3_probe_int(kind, _ptr(out, "out", _WORDS, dev), blocks, iters, _stream(dev)))
+    return blocks * 8192 * iters
 
 
 def exl3_gemm_launches(m: int, n: int, M: int) -> int:

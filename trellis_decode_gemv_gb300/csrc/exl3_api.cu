@@ -99,7 +99,25 @@ exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
   }
 }
 
+exl3_status launch_mv(const MvParams& p, int K, int codebook, int grid, bool ct16, cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_mv_k1(p, codebook, grid, ct16, stream);
+    case 2: return launch_mv_k2(p, codebook, grid, ct16, stream);
+    case 3: return launch_mv_k3(p, codebook, grid, ct16, stream);
+    case 4: return launch_mv_k4(p, codebook, grid, ct16, stream);
+    case 5: return launch_mv_k5(p, codebook, grid, ct16, stream);
+    case 6: return launch_mv_k6(p, codebook, grid, ct16, stream);
+    case 7: return launch_mv_k7(p, codebook, grid, ct16, stream);
+    case 8: return launch_mv_k8(p, codebook, grid, ct16, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
 int batch_chunk(int rem) { return rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1; }
+
+// The warp-shuffle kernels run only when exl3_set_path selects them; every
+// other setting takes the decode-MMA kernel up to EXL3_MAX_BATCH rows.
+bool use_shuffle() { return g_path.load(std::memory_order_relaxed) == EXL3_PATH_SHUFFLE; }
 
 // Prefill strategy above EXL3_MAX_BATCH rows (outside EXL3_PATH_TENSOR): the
 // fused kernel decodes every tile once per batch tile, the decode-once path
@@ -123,10 +141,35 @@ exl3_status run_tensor(LayerArgs a, int M, float* zacc, uint32_t* status, __half
   a.zacc = zacc;
   a.status = status;
   if (a.codebook != EXL3_CB_1MAD && a.codebook != EXL3_CB_MUL1) bsum = nullptr;
-  exl3_status st = launch_bimg(a.x, a.s_in, bimg, bsum, M, tc_nb(M), a.n, cs);
+  exl3_status st = launch_bimg(a.x, a.s_in, bimg, bsum, M, kPrefillRows, a.n, cs);
   if (st != EXL3_OK) return st;
   if ((st = launch_tc(a, bimg, bsum, M, device_sm_count(), cs)) != EXL3_OK) return st;
   return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, a.m, cs);
+}
+
+exl3_status run_mv(MvParams p, int K, int codebook, cudaStream_t cs) {
+  bool all256 = true;
+  for (int i = 0; i < p.count; ++i)
+    if (p.l[i].n % 256 != 0) all256 = false;
+  const int ct = mv_ct(codebook, all256);
+  int units = 0;
+  for (int i = 0; i < p.count; ++i) {
+    p.l[i].nkb = p.l[i].n / (16 * ct);
+    p.l[i].u_begin = units;
+    units += (p.l[i].m / kRowBlock) * p.l[i].nkb;
+  }
+  p.units = units;
+  const int sms = device_sm_count();
+  const int grid = units < sms ? units : sms;
+  exl3_status st;
+  if (p.M > 2) {
+    for (int i = 0; i < p.count; ++i)
+      if ((st = launch_bimg_mv(p.l[i].x, p.l[i].s_in, const_cast<__half*>(p.l[i].bimg),
+                               mv_paired(codebook) ? const_cast<float*>(p.l[i].bsum) : nullptr, p.M, mv_nb(p.M),
+                               p.l[i].n, !mv_paired(codebook), cs)) != EXL3_OK)
+        return st;
+  }
+  return launch_mv(p, K, codebook, grid, ct == 16, cs);
 }
 
 exl3_status run_shuffle(LayerArgs a, int M, float* zacc, uint32_t* xd, cudaStream_t cs) {
@@ -281,10 +324,27 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws) + m / kRowBlock;
   float* zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  const int path = g_path.load(std::memory_order_relaxed);
-  if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2))
-    return run_tensor(a, M, zacc, status, reinterpret_cast<__half*>(ws + bimg_offset(m, M)),
-                      reinterpret_cast<float*>(ws + bsum_offset(m, n, M)), cs);
+  if (!use_shuffle()) {
+    MvParams p{};
+    p.count = 1;
+    p.M = M;
+    p.status = status;
+    p.debug_stall = a.debug_stall;
+    MvLayer& L = p.l[0];
+    L.codes = codes;
+    L.x = a.x;
+    L.s_in = a.s_in;
+    L.bimg = reinterpret_cast<const __half*>(ws + bimg_offset(m, M));
+    L.bsum = reinterpret_cast<const float*>(ws + bsum_offset(m, n, M));
+    L.scales = a.scales;
+    L.s_out = a.s_out;
+    L.y = a.y;
+    L.zacc = zacc;
+    L.cnt = reinterpret_cast<uint32_t*>(ws);
+    L.m = m;
+    L.n = n;
+    return run_mv(p, K, codebook, cs);
+  }
   // x pairs of each batch chunk go where the tensor path keeps its operand
   // images (at least 32 n bytes, enough for 8 rows of n 32-bit pairs).
   return run_shuffle(a, M, zacc, reinterpret_cast<uint32_t*>(ws + bimg_offset(m, M)), cs);
@@ -293,25 +353,32 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
 namespace {
 
 // Workspace of a group: the status word (first 256 bytes), then per layer its
-// fp32 row sums [mb][m] and x pairs [mb][n] (warp-shuffle), or one set of
-// tensor-path regions sized for the largest layer (the layers then run one
-// after another).
-size_t group_shuffle_bytes(const exl3_layer* L, int count, int M) {
-  const size_t mb = static_cast<size_t>(M < 8 ? M : 8);
-  size_t b = 256;
-  for (int i = 0; i < count; ++i)
-    b += align256(sizeof(float) * mb * L[i].m) + align256(sizeof(uint32_t) * mb * L[i].n);
-  return b;
-}
+// block counters (m/128 words) and fp32 row sums [M][m], both zero on entry
+// and exit, then per layer one scratch region: the x pairs of the warp-shuffle
+// path ([min(M, 8)][n] words) or the decode-MMA kernel's operand images.
+struct GroupLayout {
+  size_t cnt[kMaxGroup], zacc[kMaxGroup], scratch[kMaxGroup];
+  size_t total;
+};
 
-size_t group_tensor_bytes(const exl3_layer* L, int count, int M) {
-  size_t maxm = 0, maxn = 0;
+GroupLayout group_layout(const exl3_layer* L, int count, int M) {
+  GroupLayout g{};
+  const size_t mb = static_cast<size_t>(M < 8 ? M : 8);
+  size_t off = 256;
   for (int i = 0; i < count; ++i) {
-    if (static_cast<size_t>(L[i].m) > maxm) maxm = L[i].m;
-    if (static_cast<size_t>(L[i].n) > maxn) maxn = L[i].n;
+    g.cnt[i] = off;
+    off += align256(sizeof(uint32_t) * (L[i].m / kRowBlock));
+    g.zacc[i] = off;
+    off += align256(sizeof(float) * static_cast<size_t>(M) * L[i].m);
   }
-  return 256 + align256(sizeof(float) * M * maxm) + align256(sizeof(__half) * tc_nb(M) * maxn) +
-         align256(sizeof(float) * M * (maxn / kRowBlock));
+  for (int i = 0; i < count; ++i) {
+    g.scratch[i] = off;
+    const size_t xd = sizeof(uint32_t) * mb * L[i].n;
+    const size_t img = M > 2 ? align256(mv_bimg_bytes(L[i].n, M)) + mv_bsum_bytes(L[i].n, M) : 0;
+    off += align256(xd > img ? xd : img);
+  }
+  g.total = off;
+  return g;
 }
 
 }  // namespace
@@ -320,9 +387,7 @@ extern "C" size_t exl3_group_workspace_bytes(const exl3_layer* layers, int count
   if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP || M < 1 || M > EXL3_MAX_BATCH) return 0;
   for (int i = 0; i < count; ++i)
     if (check_shape(layers[i].m, layers[i].n) != EXL3_OK) return 0;
-  const size_t a = group_shuffle_bytes(layers, count, M);
-  const size_t b = group_tensor_bytes(layers, count, M);
-  return a > b ? a : b;
+  return group_layout(layers, count, M).total;
 }
 
 extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
@@ -347,51 +412,42 @@ extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, in
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  auto args_of = [&](const exl3_layer& L) {
-    LayerArgs a{};
-    a.codes = L.codes;
-    a.K = K;
-    a.codebook = codebook;
-    a.m = L.m;
-    a.n = L.n;
-    a.s_in = reinterpret_cast<const __half*>(L.s_in);
-    a.s_out = reinterpret_cast<const __half*>(L.s_out);
-    a.scales = reinterpret_cast<const __half*>(L.scales);
-    a.x = reinterpret_cast<const __half*>(L.x);
-    a.y = reinterpret_cast<__half*>(L.y);
-    a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
-    return a;
-  };
-  const int path = g_path.load(std::memory_order_relaxed);
-  if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2)) {
-    int maxm = 0, maxn = 0;
+  const GroupLayout gl = group_layout(layers, count, M);
+  if (!use_shuffle()) {
+    MvParams p{};
+    p.count = count;
+    p.M = M;
+    p.status = status;
+    p.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
     for (int i = 0; i < count; ++i) {
-      if (layers[i].m > maxm) maxm = layers[i].m;
-      if (layers[i].n > maxn) maxn = layers[i].n;
+      const exl3_layer& L = layers[i];
+      MvLayer& d = p.l[i];
+      d.codes = L.codes;
+      d.x = reinterpret_cast<const __half*>(L.x);
+      d.s_in = reinterpret_cast<const __half*>(L.s_in);
+      d.bimg = reinterpret_cast<const __half*>(ws + gl.scratch[i]);
+      d.bsum = reinterpret_cast<const float*>(ws + gl.scratch[i] + align256(mv_bimg_bytes(L.n, M)));
+      d.scales = reinterpret_cast<const __half*>(L.scales);
+      d.s_out = reinterpret_cast<const __half*>(L.s_out);
+      d.y = reinterpret_cast<__half*>(L.y);
+      d.zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
+      d.cnt = reinterpret_cast<uint32_t*>(ws + gl.cnt[i]);
+      d.m = L.m;
+      d.n = L.n;
     }
-    float* zacc = reinterpret_cast<float*>(ws + 256);
-    __half* bimg = reinterpret_cast<__half*>(ws + 256 + align256(sizeof(float) * M * maxm));
-    float* bsum = reinterpret_cast<float*>(reinterpret_cast<char*>(bimg) +
-                                           align256(sizeof(__half) * tc_nb(M) * maxn));
-    for (int i = 0; i < count; ++i)
-      if ((st = run_tensor(args_of(layers[i]), M, zacc, status, bimg, bsum, cs)) != EXL3_OK) return st;
-    return EXL3_OK;
+    return run_mv(p, K, codebook, cs);
   }
 
   // Warp-shuffle path: per batch chunk, the x pairs of every layer, one
   // sub-unit kernel over the tiles of every layer, the output transform of
   // every layer.
   const int sms = device_sm_count();
-  const size_t mbmax = static_cast<size_t>(M < 8 ? M : 8);
   float* zacc[kMaxGroup];
   uint32_t* xd[kMaxGroup];
-  size_t off = 256;
   long long tiles = 0;
   for (int i = 0; i < count; ++i) {
-    zacc[i] = reinterpret_cast<float*>(ws + off);
-    off += align256(sizeof(float) * mbmax * layers[i].m);
-    xd[i] = reinterpret_cast<uint32_t*>(ws + off);
-    off += align256(sizeof(uint32_t) * mbmax * layers[i].n);
+    zacc[i] = reinterpret_cast<float*>(ws + gl.zacc[i]);
+    xd[i] = reinterpret_cast<uint32_t*>(ws + gl.scratch[i]);
     tiles += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
   }
   for (int done = 0; done < M;) {
@@ -446,7 +502,7 @@ extern "C" int exl3_gemm_launches(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1) return 0;
   const int path = g_path.load(std::memory_order_relaxed);
   if (M <= EXL3_MAX_BATCH) {
-    if (path == EXL3_PATH_TENSOR || (path == EXL3_PATH_AUTO && M > 2)) return 3;
+    if (path != EXL3_PATH_SHUFFLE) return mv_launches(1, M);
     // warp-shuffle path: per batch chunk the layer kernel (plus the x-pair
     // kernel in front of the sub-unit kernel) and the output kernel
     const int sms = device_sm_count();
@@ -556,7 +612,7 @@ extern "C" exl3_status exl3_gemm(const uint32_t* codes, int K, int codebook, int
     a.x = reinterpret_cast<const __half*>(x) + static_cast<size_t>(done) * n;
     a.y = reinterpret_cast<__half*>(y) + static_cast<size_t>(done) * m;
     a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
-    // rows <= 32 use the skinny configuration; its regions fit in this layout
+    // a last pass of fewer rows runs the same N = 128 kernel (rows past it zero)
     if ((st = run_tensor(a, rows, zacc, status, bimg, bsum, cs)) != EXL3_OK) return st;
   }
   return EXL3_OK;

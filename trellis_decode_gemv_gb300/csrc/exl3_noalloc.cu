@@ -14,6 +14,8 @@
 // device) race and must be serialized by the caller.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "exl3_host.cuh"
 
 namespace exl3 {
@@ -26,20 +28,22 @@ constexpr size_t kScratchBytes = EXL3_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// Per device, the array's device address once looked up.  Host threads may
+// make their first calls on a device at the same time: each may look the
+// address up (the runtime returns the same value) and the stores and loads are
+// atomic, so no thread reads a half-written pointer.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
-exl3_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EXL3_ERR_CUDA;
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return EXL3_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+// Device address of the scratch on device `dev` (which must be current),
+// looked up once and cached.
+exl3_status scratch_address(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return EXL3_ERR_CUDA;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return EXL3_ERR_CUDA;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return EXL3_OK;
 }
 
@@ -60,15 +64,21 @@ extern "C" exl3_status exl3_gemv_noalloc(const uint32_t* codes, int K, int codeb
       (s_in && !aligned16(s_in)) || (s_out && !aligned16(s_out)))
     return EXL3_ERR_ALIGN;
 
-  // Scratch layout as in the workspace of exl3_gemv at batch 1: counters
-  // (+ status word), the fp32 row sums, then the n x pairs.
-  const size_t zero_bytes = bimg_offset(m, 1);  // counters and row sums
+  // Scratch layout as in the workspace of exl3_gemv at batch 1: the block
+  // counters and the status word, the m fp32 row sums, then the n 32-bit x
+  // pairs of the warp-shuffle kernel.
+  const size_t zero_bytes = bimg_offset(m, 1);  // counters, status word and row sums
   const size_t need = zero_bytes + align256(sizeof(uint32_t) * static_cast<size_t>(n));
   if (need > kScratchBytes) return EXL3_ERR_SCRATCH;
 
-  void* scratch = nullptr;
-  if ((st = scratch_address(&scratch)) != EXL3_OK) return st;
+  // The array's address is per device: it must be the address on the device
+  // that runs `stream`, which must be the current device.
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, sdev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(cs, &sdev) != cudaSuccess || sdev != dev)
+    return EXL3_ERR_CUDA;
+  void* scratch = nullptr;
+  if ((st = scratch_address(dev, &scratch)) != EXL3_OK) return st;
   // The row sums must start at zero; the array keeps whatever the previous
   // call left, so clear them (and the counters) on the stream first.
   if (cudaMemsetAsync(scratch, 0, zero_bytes, cs) != cudaSuccess) return EXL3_ERR_CUDA;

@@ -710,15 +710,16 @@ exl3_status launch_tc_t(const LayerArgs& a, const __half* bimg, const float* bsu
   return launch_status();
 }
 
+// Passes of up to 128 batch rows (exl3_gemm above EXL3_MAX_BATCH rows with
+// the tensor path selected): N = 128.  Skinny batches run the decode-MMA
+// kernel (csrc/exl3_mv.cuh) instead.
 template <int K, int CB>
 exl3_status launch_tc_nb(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                          cudaStream_t stream) {
-  if (M <= 16) return launch_tc_t<K, CB, 16>(a, bimg, bsum, M, grid, stream);
-  if (M <= 32) return launch_tc_t<K, CB, 32>(a, bimg, bsum, M, grid, stream);
-  return launch_tc_t<K, CB, 128>(a, bimg, bsum, M, grid, stream);
+  return launch_tc_t<K, CB, kMaxNB>(a, bimg, bsum, M, grid, stream);
 }
 
-// M <= 128 batch rows; N = 16, 32 or 128 (tc_nb).
+// M <= 128 batch rows; N = 128.
 template <int K>
 exl3_status launch_tc_dispatch(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                                cudaStream_t stream) {

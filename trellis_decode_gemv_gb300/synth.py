@@ -63,6 +63,18 @@ def activations(M: int, n: int, seed: int) -> np.ndarray:
     return _rng(seed).standard_normal(size=(M, n)).astype(np.float16)
 
 
+def outlier_activations(M: int, n: int, seed: int, channels: int = 4, magnitude: float = 1000.0) -> np.ndarray:
+    """Heavy-tailed activations: fp16(N(0, 1)) with `channels` channels (the
+    same columns in every row) set to +-magnitude with random signs -- the
+    outlier features that the input rotation exists to spread out."""
+    rng = _rng(seed)
+    x = rng.standard_normal(size=(M, n))
+    cols = rng.choice(n, size=channels, replace=False)
+    signs = np.where(rng.integers(0, 2, size=(M, channels)) == 1, 1.0, -1.0)
+    x[:, cols] = magnitude * signs
+    return x.astype(np.float16)
+
+
 def layer_inputs(m: int, n: int, K: int, M: int, config: int, index: int) -> dict:
     """All inputs of one layer with the standard seeds (tensor ids 10*index+0..4)."""
     b = 10 * index
