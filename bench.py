@@ -134,6 +134,12 @@ def workload(name: str, batch: int):
     raise SystemExit(f"unknown workload {name}")
 
 
+def uses_shuffle(path: str, M: int) -> bool:
+    """The kernel family of a call of M <= 32 rows (exl3_set_path): the
+    warp-shuffle kernels at M <= 2 under AUTO, the decode-MMA kernel above."""
+    return path == "shuffle" or (path == "auto" and M <= 2)
+
+
 def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
     """Kernel launches of one exl3_gemm_small call.  Decode-MMA kernel (every
     path but the warp-shuffle one): one launch at M <= 2, plus the
@@ -144,7 +150,7 @@ def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
     if M > 32:
         from trellis_decode_gemv_gb300 import binding as B
         return B.exl3_gemm_launches(m, n, M)
-    if path != "shuffle":
+    if not uses_shuffle(path, M):
         return 1 if M <= 2 else 2
     tiles_per_sm = (m // 16) * (n // 16) // sms
     launches, rem = 0, M
@@ -198,7 +204,7 @@ def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     pairs, one sub-unit kernel over every layer, output transform)."""
     if len(shapes) == 1:
         return kernels_per_call(path, M, shapes[0][0], shapes[0][1], sms)
-    if path != "shuffle":
+    if not uses_shuffle(path, M):
         return 1 if M <= 2 else 1 + len(shapes)
     chunks, rem = 0, M
     for c in (8, 4, 2, 1):
@@ -282,8 +288,10 @@ class ClockSampler:
         return out
 
     def mark(self):
+        # the last sample before the region counts too: regions shorter than
+        # the 50 ms sampling interval still get the samples around them
         if self.proc is not None:
-            self._mark = len(self._rows())
+            self._mark = max(0, len(self._rows()) - 1)
 
     def since_mark(self):
         if self.proc is None:
@@ -626,7 +634,7 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
         achieved, peak, unit = flops_step / t_step / 1e12, bf16_tflops, "TFLOP/s"
     else:
         achieved, peak, unit = bytes_step / t_step / 1e9, hbm_gbs, "GB/s"
-    shuffle = args.path == "shuffle" and M <= 32
+    shuffle = uses_shuffle(args.path, M) and M <= 32
     dense = M > 32 and args.path != "tensor"
     passes = M > 32 and args.path == "tensor"
     fused = dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256))
@@ -872,10 +880,12 @@ def run_ours(args):
             "metric": METRIC, "value": head["value"], "unit": "weights/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16" if args.path != "shuffle" else "f16-partials",
-            "arith": ("binary16 weights x binary16 x-tilde on tcgen05 MMAs, fp32 accumulation in TMEM and fp32 "
-                      "split-K reductions; y rounded once to binary16") if args.path != "shuffle" else
-                     ("binary16 products, 16-column binary16 partial sums, fp32 beyond"),
+            "dtype": "f16",
+            "arith": ("binary16 products of the weights and x-tilde, accumulated in binary16 over each tile row "
+                      "(16 columns, HFMA2), fp32 beyond (warp-shuffle kernels, batch <= 2)")
+                     if uses_shuffle(args.path, head["config"]["batch"]) else
+                     ("binary16 weights x binary16 x-tilde on tcgen05 MMAs, fp32 accumulation in TMEM and fp32 "
+                      "split-K reductions; y rounded once to binary16"),
             "data": "synthetic",
             "config": head["config"],
             "effective_gbs": head["effective_gbs"], "macs_per_s": head["macs_per_s"],

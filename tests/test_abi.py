@@ -38,7 +38,7 @@ def _ws(m, n, M):
     counters = a256(4 * (m // 128 + 1))
     zacc = a256(4 * M * m)
     nb = 16 if M <= 16 else 32
-    bimg = a256(2 * 2 * nb * n)  # operand images; the three-instruction codes store each value twice
+    bimg = a256(2 * nb * n)
     bsum = a256(4 * M * (n // 128))
     return counters + zacc + bimg + bsum
 
@@ -140,7 +140,7 @@ def test_group_workspace_bytes(lib):
         # status word; per layer block counters and row sums; per layer the x
         # pairs or (M > 2) the decode-MMA kernel's operand images
         fixed = 256 + sum(a256(4 * (m // 128)) + a256(4 * M * m) for m, n in shapes)
-        scratch = sum(a256(max(4 * mb * n, a256(2 * 2 * nb * n) + 4 * M * (n // 128) if M > 2 else 0))
+        scratch = sum(a256(max(4 * mb * n, a256(2 * nb * n) + 4 * M * (n // 128) if M > 2 else 0))
                       for m, n in shapes)
         assert lib.exl3_group_workspace_bytes(_group(shapes), 3, M) == fixed + scratch
     assert lib.exl3_group_workspace_bytes(_group([(100, 128)]), 1, 1) == 0

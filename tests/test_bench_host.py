@@ -41,15 +41,16 @@ def test_single_process_reduction_is_identity():
 
 def test_kernels_per_call():
     sms = 152
-    # decode-MMA kernel: one launch at batch 1 and 2, plus the operand-image kernel above
-    assert bench.kernels_per_call("auto", 1, 4096, 4096, sms) == 1
+    # decode-MMA kernel (M > 2, or forced): one launch at batch 1 and 2, plus the operand-image kernel above
+    assert bench.kernels_per_call("tensor", 1, 4096, 4096, sms) == 1
     assert bench.kernels_per_call("tensor", 2, 14336, 4096, sms) == 1
     assert bench.kernels_per_call("auto", 3, 4096, 4096, sms) == 2
     assert bench.kernels_per_call("auto", 32, 4096, 4096, sms) == 2
-    # warp-shuffle, small layer at batch 1: segment kernel + output kernel
+    # warp-shuffle (AUTO at batch <= 2), small layer at batch 1: segment kernel + output kernel
+    assert bench.kernels_per_call("auto", 1, 4096, 4096, sms) == 2
     assert bench.kernels_per_call("shuffle", 1, 4096, 4096, sms) == 2
     # large layer at batch 1: x pairs + sub-unit kernel + output kernel
-    assert bench.kernels_per_call("shuffle", 1, 14336, 4096, sms) == 3
+    assert bench.kernels_per_call("auto", 1, 14336, 4096, sms) == 3
     # forced warp-shuffle batch 5 on a small layer: chunk of 4 (3 kernels) + chunk of 1 (2)
     assert bench.kernels_per_call("shuffle", 5, 1024, 4096, sms) == 5
 
@@ -85,12 +86,13 @@ def test_decoder_groups():
 
 def test_kernels_per_group():
     sms = 152
-    # one decode-MMA launch over every layer; above batch 2 one image kernel per layer first
-    assert bench.kernels_per_group("auto", 1, [(4096, 4096), (1024, 4096), (1024, 4096)], sms) == 1
+    # warp-shuffle at batch <= 2: x pairs, one sub-unit kernel over every layer, output transform
+    assert bench.kernels_per_group("auto", 1, [(4096, 4096), (1024, 4096), (1024, 4096)], sms) == 3
+    # decode-MMA above: one image kernel per layer, one launch over every layer
     assert bench.kernels_per_group("auto", 5, [(4096, 4096), (1024, 4096)], sms) == 3
+    assert bench.kernels_per_group("tensor", 1, [(4096, 4096), (1024, 4096)], sms) == 1
     assert bench.kernels_per_group("shuffle", 5, [(4096, 4096), (1024, 4096)], sms) == 6
-    assert bench.kernels_per_group("shuffle", 1, [(4096, 4096), (1024, 4096)], sms) == 3
-    assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 1
+    assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 2
 
 
 def test_decoder_groups_whole_vector_stack():

@@ -27,8 +27,11 @@ def _call(d, K, cb, m, n, M, ws):
     return y
 
 
-def test_tensor_wait_timeout_sets_status_and_context_survives():
-    m, n, K, cb, M = 384, 1280, 3, 1, 4
+@pytest.mark.parametrize("M", [1, 4])
+def test_tensor_wait_timeout_sets_status_and_context_survives(M):
+    """The decode-MMA kernel with its MMAs never issued (the hook): at M = 1
+    the kernel rotates x itself, at M = 4 an image kernel runs first."""
+    m, n, K, cb = 384, 1280, 3, 1
     inp = synth.layer_inputs(m, n, K, M, config=90, index=0)
     d = upload(inp)
     ws = B.alloc_workspace(m, n, M, "cuda")
@@ -45,9 +48,10 @@ def test_tensor_wait_timeout_sets_status_and_context_survives():
         assert B.workspace_status(ws, m) == 1
         assert B.exl3_device_status(ws, 4 * (m // 128)) == 9  # EXL3_ERR_DEVICE_CHECK
         assert elapsed < 60.0
-        # the row sums were left at zero by the output kernel
+        # no partial sum reached the row sums, no block counter moved
         zacc = ws[256:256 + 4 * M * m].view(torch.float32)
         assert float(zacc.abs().sum()) == 0.0
+        assert int(ws[:4 * (m // 128)].view(torch.int32).abs().sum()) == 0
         # clear the status word; the next call is correct
         off = 4 * (m // 128)
         ws[off:off + 4].zero_()

@@ -99,25 +99,32 @@ exl3_status launch_layer(const LayerArgs& a, int mb, cudaStream_t stream) {
   }
 }
 
-exl3_status launch_mv(const MvParams& p, int K, int codebook, int grid, bool ct16, cudaStream_t stream) {
+exl3_status launch_mv(const MvParams& p, int K, int codebook, int grid, cudaStream_t stream) {
   switch (K) {
-    case 1: return launch_mv_k1(p, codebook, grid, ct16, stream);
-    case 2: return launch_mv_k2(p, codebook, grid, ct16, stream);
-    case 3: return launch_mv_k3(p, codebook, grid, ct16, stream);
-    case 4: return launch_mv_k4(p, codebook, grid, ct16, stream);
-    case 5: return launch_mv_k5(p, codebook, grid, ct16, stream);
-    case 6: return launch_mv_k6(p, codebook, grid, ct16, stream);
-    case 7: return launch_mv_k7(p, codebook, grid, ct16, stream);
-    case 8: return launch_mv_k8(p, codebook, grid, ct16, stream);
+    case 1: return launch_mv_k1(p, codebook, grid, stream);
+    case 2: return launch_mv_k2(p, codebook, grid, stream);
+    case 3: return launch_mv_k3(p, codebook, grid, stream);
+    case 4: return launch_mv_k4(p, codebook, grid, stream);
+    case 5: return launch_mv_k5(p, codebook, grid, stream);
+    case 6: return launch_mv_k6(p, codebook, grid, stream);
+    case 7: return launch_mv_k7(p, codebook, grid, stream);
+    case 8: return launch_mv_k8(p, codebook, grid, stream);
     default: return EXL3_ERR_K;
   }
 }
 
 int batch_chunk(int rem) { return rem >= 8 ? 8 : rem >= 4 ? 4 : rem >= 2 ? 2 : 1; }
 
-// The warp-shuffle kernels run only when exl3_set_path selects them; every
-// other setting takes the decode-MMA kernel up to EXL3_MAX_BATCH rows.
-bool use_shuffle() { return g_path.load(std::memory_order_relaxed) == EXL3_PATH_SHUFFLE; }
+// Kernel family of a call of M <= EXL3_MAX_BATCH rows: the warp-shuffle
+// kernels at M <= 2 (and whenever exl3_set_path selects them), the
+// decode-MMA kernel above (and whenever EXL3_PATH_TENSOR selects it).  At
+// batch 1 the warp-shuffle kernels decode and multiply in the same 32 warps
+// per SM; the decode-MMA kernel's decoders, issuers and epilogue warps spend
+// too much of each chunk on their hand-offs to beat them there (measured).
+bool use_shuffle(int M) {
+  const int path = g_path.load(std::memory_order_relaxed);
+  return path == EXL3_PATH_SHUFFLE || (path == EXL3_PATH_AUTO && M <= 2);
+}
 
 // Prefill strategy above EXL3_MAX_BATCH rows (outside EXL3_PATH_TENSOR): the
 // fused kernel decodes every tile once per batch tile, the decode-once path
@@ -147,29 +154,62 @@ exl3_status run_tensor(LayerArgs a, int M, float* zacc, uint32_t* status, __half
   return launch_epi(a.zacc, a.scales, a.s_out, a.y, M, a.m, cs);
 }
 
+// The decode-MMA kernel loads the codes of a chunk (eight tile-row strips of
+// 8 tiles) with one 2-D tensor copy: the codes as (m/16) rows of (n/16) * 4K
+// 64-bit elements, a box of 32K x 8.
+// The driver's tensor-map encoder, looked up through the runtime (so that the
+// library loads, for its host-side checks, where no driver is installed).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+      return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
+}
+
+exl3_status mv_codes_map(CUtensorMap* map, const uint32_t* codes, int K, int m, int n) {
+  const EncodeTiledFn encode = encode_tiled();
+  if (encode == nullptr) return EXL3_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(n / 16) * 4 * K, static_cast<cuuint64_t>(m / 16)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(n / 16) * 8 * K * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * K), 8u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(codes), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? EXL3_OK : EXL3_ERR_CUDA;
+}
+
 exl3_status run_mv(MvParams p, int K, int codebook, cudaStream_t cs) {
-  bool all256 = true;
-  for (int i = 0; i < p.count; ++i)
-    if (p.l[i].n % 256 != 0) all256 = false;
-  const int ct = mv_ct(codebook, all256);
   int units = 0;
+  exl3_status st;
   for (int i = 0; i < p.count; ++i) {
-    p.l[i].nkb = p.l[i].n / (16 * ct);
+    if ((st = mv_codes_map(&p.l[i].codes_map, p.l[i].codes, K, p.l[i].m, p.l[i].n)) != EXL3_OK) return st;
+    p.l[i].nkb = p.l[i].n / kMvChunkCols;
     p.l[i].u_begin = units;
     units += (p.l[i].m / kRowBlock) * p.l[i].nkb;
   }
   p.units = units;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
-  exl3_status st;
   if (p.M > 2) {
     for (int i = 0; i < p.count; ++i)
-      if ((st = launch_bimg_mv(p.l[i].x, p.l[i].s_in, const_cast<__half*>(p.l[i].bimg),
-                               mv_paired(codebook) ? const_cast<float*>(p.l[i].bsum) : nullptr, p.M, mv_nb(p.M),
-                               p.l[i].n, !mv_paired(codebook), cs)) != EXL3_OK)
+      if ((st = launch_bimg(p.l[i].x, p.l[i].s_in, const_cast<__half*>(p.l[i].bimg),
+                            mv_centred(codebook) ? const_cast<float*>(p.l[i].bsum) : nullptr, p.M, mv_nb(p.M),
+                            p.l[i].n, cs)) != EXL3_OK)
         return st;
   }
-  return launch_mv(p, K, codebook, grid, ct == 16, cs);
+  return launch_mv(p, K, codebook, grid, cs);
 }
 
 exl3_status run_shuffle(LayerArgs a, int M, float* zacc, uint32_t* xd, cudaStream_t cs) {
@@ -324,7 +364,7 @@ extern "C" exl3_status exl3_gemm_small(const uint32_t* codes, int K, int codeboo
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws) + m / kRowBlock;
   float* zacc = reinterpret_cast<float*>(ws + zacc_offset(m));
-  if (!use_shuffle()) {
+  if (!use_shuffle(M)) {
     MvParams p{};
     p.count = 1;
     p.M = M;
@@ -413,7 +453,7 @@ extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, in
   char* ws = static_cast<char*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   const GroupLayout gl = group_layout(layers, count, M);
-  if (!use_shuffle()) {
+  if (!use_shuffle(M)) {
     MvParams p{};
     p.count = count;
     p.M = M;
@@ -502,7 +542,7 @@ extern "C" int exl3_gemm_launches(int m, int n, int M) {
   if (check_shape(m, n) != EXL3_OK || M < 1) return 0;
   const int path = g_path.load(std::memory_order_relaxed);
   if (M <= EXL3_MAX_BATCH) {
-    if (path != EXL3_PATH_SHUFFLE) return mv_launches(1, M);
+    if (!use_shuffle(M)) return mv_launches(1, M);
     // warp-shuffle path: per batch chunk the layer kernel (plus the x-pair
     // kernel in front of the sub-unit kernel) and the output kernel
     const int sms = device_sm_count();

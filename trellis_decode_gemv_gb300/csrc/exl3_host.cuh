@@ -2,6 +2,7 @@
 // internal launcher declarations shared by the translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -54,12 +55,8 @@ inline size_t zacc_offset(int m) { return counters_bytes(m); }
 inline size_t bimg_offset(int m, int M) {
   return zacc_offset(m) + align256(sizeof(float) * static_cast<size_t>(M) * m);
 }
-// The image region holds either the tensor-core kernel's images (tc_nb(M) x n)
-// or, up to 32 rows, the decode-MMA kernel's (twice that: the
-// three-instruction codes duplicate every value).
 inline size_t bsum_offset(int m, int n, int M) {
-  const size_t img = static_cast<size_t>(tc_nb(M)) * n * (M <= 32 ? 2 : 1);
-  return bimg_offset(m, M) + align256(sizeof(__half) * img);
+  return bimg_offset(m, M) + align256(sizeof(__half) * static_cast<size_t>(tc_nb(M)) * n);
 }
 inline size_t workspace_total(int m, int n, int M) {
   return bsum_offset(m, n, M) + align256(sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock));
@@ -150,6 +147,9 @@ struct LayerArgs {
 // ---- decode-MMA kernel (csrc/exl3_mv.cuh), 1 <= M <= 32 -------------------------
 // One layer of a call.  Units of layer i are u_begin .. u_begin + (m/128)*nkb.
 struct MvLayer {
+  // the codes as a 2-D tensor of 64-bit elements: (m/16) tile rows of
+  // (n/16) * 4K elements; one box is the 8 tile-row strips of one chunk
+  CUtensorMap codes_map;
   const uint32_t* codes;
   const __half* x;       // [M][n] (x warps compute x-tilde; M <= 2)
   const __half* s_in;    // [n] or nullptr
@@ -174,29 +174,26 @@ struct MvParams {
   int debug_stall;       // test hook: operand B is never posted
 };
 
-// Tiles per chunk of the decode-MMA kernel: 16 for the byte-sum codes (two
-// weights per TMEM column) when every n is a multiple of 256, else 8.
-inline bool mv_paired(int codebook) { return codebook == EXL3_CB_1MAD || codebook == EXL3_CB_MUL1; }
-inline int mv_ct(int codebook, bool all_n256) { return mv_paired(codebook) && all_n256 ? 16 : 8; }
+// The decode-MMA kernel works in chunks of 128 input columns; the byte-sum
+// codes (1MAD, mul1) are centred through the sums of operand B.
+inline bool mv_centred(int codebook) { return codebook == EXL3_CB_1MAD || codebook == EXL3_CB_MUL1; }
+constexpr int kMvChunkCols = 128;
 // Batch columns N of its MMAs.
 inline int mv_nb(int M) { return M <= 16 ? 16 : 32; }
 // Operand-B images of the decode-MMA kernel for M > 2 (x-tilde computed in
-// the kernel below that): per 128-column block kb an (NB x 128 d) binary16
-// K-major image at kb * NB * 128 * d halves, d = 2 for the three-instruction
-// codes (each x-tilde value twice, k = 2c and 2c + 1), else 1.
-inline size_t mv_bimg_bytes(int n, int M) { return sizeof(__half) * 2 * static_cast<size_t>(mv_nb(M)) * n; }
+// the kernel below that): launch_bimg's layout, one (NB x 128) binary16
+// K-major image per 128-column block.
+inline size_t mv_bimg_bytes(int n, int M) { return sizeof(__half) * static_cast<size_t>(mv_nb(M)) * n; }
 // ... and their block sums, fp32 [M][n/128].
 inline size_t mv_bsum_bytes(int n, int M) { return sizeof(float) * static_cast<size_t>(M) * (n / kRowBlock); }
-exl3_status launch_bimg_mv(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M, int nb, int n,
-                           bool dup, cudaStream_t stream);
-exl3_status launch_mv_k1(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k2(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k3(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k4(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k5(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k6(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k7(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
-exl3_status launch_mv_k8(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream);
+exl3_status launch_mv_k1(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k2(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k3(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k4(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k5(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k6(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k7(const MvParams& p, int codebook, int grid, cudaStream_t stream);
+exl3_status launch_mv_k8(const MvParams& p, int codebook, int grid, cudaStream_t stream);
 // A call of the decode-MMA kernel over p.count layers of K bits and the given
 // code at batch p.M: fills the plan fields (units, chunks, grid), writes the
 // operand images first for M > 2 (p.l[i].bimg must point at

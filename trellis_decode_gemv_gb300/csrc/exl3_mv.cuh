@@ -12,60 +12,68 @@
 //    tensor memory (TMEM) as operand A of tcgen05 MMAs of 128 x N x 16 (N =
 //    16 or 32 batch columns, rows past M zero), x-tilde is operand B in
 //    shared memory and the fp32 accumulator D lives in TMEM;
-//  * the decoders store only what the code produces:
-//      byte-sum codes (1MAD, mul1): the binary16 value 1024 + S spliced by
-//        dp4a, two weights paired by one byte permute; the centring,
-//        -(1024 + centre) * sum(x-tilde), is one more MMA per chunk whose
-//        operand A is a constant column of -(1024 + centre) in TMEM and whose
-//        operand B holds the chunk's sums of x-tilde split into two binary16
-//        parts (hi + lo);
-//      three-instruction codes (3INST, MCG): the 32-bit mask/XOR result as
-//        it is -- its two binary16 halves lo and hi are two K elements of
-//        operand A, and x-tilde is duplicated in operand B, so the MMA forms
-//        lo*x + hi*x without an add per weight (K doubled);
-//  * the input transform is computed in the kernel by four x warps (M <= 2),
-//    each taking every fourth chunk: x and the signs are loaded and rotated
-//    before the warp waits for the chunk's slot, and x-tilde goes straight
+//  * the decoders store one binary16 value per weight, two per TMEM column:
+//      byte-sum codes (1MAD, mul1): 1024 + S, the dp4a byte sum spliced into
+//        the mantissa of 1024; the centring, -(1024 + centre) * sum(x-tilde),
+//        is one more MMA per chunk whose operand A is a constant column of
+//        -(1024 + centre) in TMEM and whose operand B holds the chunk's sums
+//        of x-tilde split into two binary16 parts (hi + lo);
+//      three-instruction codes (3INST, MCG): the defined weight, the binary16
+//        sum lo + hi of the two halves of the mask/XOR word (one packed add on
+//        the word's halves per weight, one byte permute per pair).  Storing lo
+//        and hi as two K elements would save those instructions but double
+//        the MMAs, and at 128 x N x 16 the tensor core takes about 50 cycles
+//        per MMA whatever N <= 64 is;
+//  * the input transform is computed in the kernel (M <= 2): x and the signs
+//    are loaded and rotated before the slot is free, and x-tilde goes straight
 //    into the operand-B slot; above M = 2 one small kernel writes the operand
 //    images (and, for the byte-sum codes, their 128-column sums) once per
-//    call and the x warps bulk-copy them into the slots;
+//    call and they are bulk-copied into the slots;
 //  * split-K partial sums are added into fp32 row sums in L2 (one reduction
 //    per row and batch row per run), and the CTA whose arrival completes a
 //    128-row block reads the row sums back, applies scale, output signs and
 //    the 128-point FWHT, stores y and clears the row sums and the block's
 //    counter: the output transform needs no kernel of its own.
 //
-// Work split: a unit is one 128-row block x one chunk of CT tile columns of
-// one layer (CT = 16 for the byte-sum codes when every n is a multiple of
-// 256, else 8); the units of all layers of the call, layer, block and chunk
-// major, are cut into gridDim.x contiguous ranges (stream-K), one persistent
-// CTA per SM.  The units of a range that share a layer and block form a run,
-// accumulated in one TMEM D.
+// MMA issue.  A tcgen05.mma is issued by one thread, and that thread's warp
+// competes for its scheduler with the decoders of the same SM sub-partition
+// (a TMEM lane quarter belongs to one sub-partition, so every sub-partition
+// decodes): measured, a lone issuer beside busy warps of its own
+// sub-partition stalls for hundreds of cycles per MMA, against about 50 for
+// the tensor core.  So six issuers, spread over the sub-partitions, share the
+// MMAs: issuer i takes the chunks seq = i (mod 6) and owns A slot i and B
+// slot i (six slots also keep each decoder team two chunks ahead of the MMAs
+// it waits for).
+// D is zeroed by the epilogue when it takes a run's sums out, so every MMA
+// accumulates and the order in which the issuers' MMAs reach the tensor core
+// does not matter.
 //
-// Warp roles (18 warps):
-//   0-7   decoders.  Warp w reaches TMEM lanes 32*(w%4) ..; thread = weight
-//         row of the block (its TMEM lane), w/4 picks the half of the chunk's
-//         tiles it decodes.  Per chunk: the row's code words from the
+// Work split: a unit is one 128-row block x one chunk of 8 tile columns (128
+// input columns) of one layer; the units of all layers of the call, layer,
+// block and chunk major, are cut into gridDim.x contiguous ranges (stream-K),
+// one persistent CTA per SM.  The units of a range that share a layer and
+// block form a run, accumulated in one TMEM D.
+//
+// Warp roles (19 warps):
+//   0-7   decoders, two teams of four: warp w reaches TMEM lanes 32*(w%4) ..
+//         (thread = weight row of the block), team w/4 takes the chunks of
+//         its parity.  Per chunk: the row's code words of 8 tiles from the
 //         shared-memory ring, 16 generator outputs per tile (funnel shifts
-//         give two windows each; for the three-instruction codes the second
-//         window's generator output comes from the 32-bit funnel word by two
-//         multiply-adds, which moves work from the ALU to the FMA pipe),
-//         code, tcgen05.st of 32 or 64 columns, one arrival.
-//   8     MMA issue (one lane) and TMEM allocation.
-//   9     code producer: eight bulk copies (one per tile-row strip) per chunk
-//         into a 2..8-deep ring.
-//   10-13 x warps: operand B of each chunk (see above).
-//   14-17 epilogue: D of each run out of TMEM into the row sums, the block
-//         ticket and, for the completing CTA, the output transform.
-// mbarriers: ring full/empty, A full/empty (3 TMEM slots), B full/empty (one
-// operand-B slot per x warp), D full/empty (2 accumulators).  Every parity
-// wait is on a barrier whose previous phase the waiting thread itself has
-// seen complete (the decoders and the MMA lane take the chunks in order, each
-// x warp owns its slot), so no wait can mistake a phase two behind for the
-// one it needs.
-// Every wait is bounded: on timeout the thread sets the CTA's abort flag and
-// the call's status word, every role stops, the producers wait (bounded) for
-// their copies in flight, the MMA lane for its MMAs, and TMEM is freed.
+//         give two windows each; for every code but 1MAD the second window's
+//         generator output comes from the 32-bit funnel word by two
+//         multiply-adds, which moves work from the ALU to the FMA pipe), the
+//         code, two tcgen05.st of 32 columns, one arrival.
+//   9-14  issuers: operand B of their chunks, then the chunks' MMAs.
+//   15-18 epilogue: D of each run out of TMEM (then zeroed) into the row sums,
+//         the block ticket and, for the completing CTA, the output transform.
+//         Warp 15 allocates TMEM.
+// mbarriers: ring full/empty, A full/empty (6 TMEM slots), B full (bulk
+// copies), D full/empty (2 accumulators).  Every parity wait is on a barrier
+// whose previous phase the waiting thread itself has seen complete, so no
+// wait can mistake a phase two behind for the one it needs.  Every wait is
+// bounded: on timeout the thread sets the CTA's abort flag and the call's
+// status word, every role stops, the issuers wait (bounded) for their MMAs,
+// and TMEM is freed.
 #pragma once
 
 #include "exl3_tc.cuh"
@@ -81,9 +89,7 @@ using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
 using tc::mma_commit;
-using tc::mma_f16_ts;
 using tc::RowWords;
-using tc::row_states;
 using tc::smem_desc;
 using tc::smem_u32;
 using tc::tc_fence_after;
@@ -92,74 +98,56 @@ using tc::tmem_alloc;
 using tc::tmem_dealloc;
 using tc::tmem_st_wait;
 
-constexpr int kDecWarps = 8;
-constexpr int kDQ = kDecWarps / 4;  // decode warps per TMEM lane quarter
-constexpr int kMmaWarp = 8;
-constexpr int kCodeWarp = 9;
-constexpr int kXWarp0 = 10;
-constexpr int kXWarps = 4;
-constexpr int kEpiWarp0 = 14;
-constexpr int kWarps = 18;
+constexpr int kCT = 8;             // tile columns per chunk (128 input columns)
+constexpr int kTeams = 3;          // decoder teams
+constexpr int kDecWarps = 4 * kTeams;
+constexpr int kIss0 = kDecWarps;       // first issuer warp
+constexpr int kIssuers = 6;            // over all four SM sub-partitions
+constexpr int kEpiWarp0 = kIss0 + kIssuers;  // four warps, one per TMEM lane quarter
+constexpr int kWarps = kEpiWarp0 + 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kSlots = 3;        // A slots in TMEM
-constexpr int kSlotCols = 128;   // TMEM columns of one A slot
-constexpr int kACol = 64;        // A slots after the two D accumulators (<= 32 columns each)
-constexpr int kConstCol = kACol + 3 * 128;  // 8 columns: the centring column of the byte-sum codes
-constexpr int kExtK = 16;        // operand-B K elements of the centring MMA
+constexpr int kSlotCols = 64;      // TMEM columns of one A slot (8 tiles x 16 weights / 2)
+constexpr int kACol = 64;          // A slots after the two D accumulators (<= 32 columns each)
+constexpr int kConstCol = kACol + kIssuers * kSlotCols;  // 8 columns: the centring column
 constexpr int kTmemCols = 512;
-constexpr int kMaxRing = 8;
-constexpr int kRowPad = 16;      // words after each tile-row strip: lanes 16-31 read 16 banks away
+constexpr int kExtK = 16;          // operand-B K elements of the centring MMA
+constexpr int kKext = kCT * 16;    // operand-B K elements of a chunk
+constexpr int kMmas = kKext / 16;  // MMAs (K = 16) per chunk
+constexpr int kMaxRing = 12;
 constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory of one CTA
-constexpr int kEpiBarrier = 2;   // named barriers (0 is __syncthreads)
-constexpr int kXBarrier = 3;
+constexpr int kEpiBarrier = 2;     // named barriers (0 is __syncthreads)
 constexpr int kMaxM = 32;
+static_assert(kConstCol + 8 <= kTmemCols, "TMEM columns");
+static_assert(kIssuers % kTeams == 0, "each A slot belongs to one decoder team");
 
-// Codes whose weight is an affine function of a byte sum store one binary16
-// per weight (two per TMEM column); the three-instruction codes store the
-// two halves of the mask/XOR word (one weight per column, K doubled).
-template <int CB>
-__host__ __device__ constexpr bool paired_code() {
-  return byte_sum_code<CB>();
-}
-
-template <int K, int CB, int CT, int NB>
+template <int K, int CB, int NB>
 struct MvCfg {
-  static constexpr bool kPaired = paired_code<CB>();
-  static constexpr int kColsPerTile = kPaired ? 8 : 16;   // TMEM columns per tile row
-  static constexpr int kTpt = CT / kDQ;                    // tiles per decode thread per chunk
-  static constexpr int kThreadCols = kTpt * kColsPerTile;  // 64, or 32 (byte-sum codes, CT = 8)
-  static constexpr int kStoreTiles = 32 / kColsPerTile;    // tiles per 32-column store
-  static constexpr int kStores = kTpt / kStoreTiles;
-  static constexpr int kMmas = CT * kColsPerTile / 8;      // MMAs (K = 16) per chunk
-  static constexpr int kKext = 16 * kMmas;                 // operand-B K elements per chunk
-  static constexpr int kBSlotBytes = (256 + kExtK) * NB * 2;  // the largest chunk + the centring block
+  // the byte-sum codes store 1024 + S and are centred by one more MMA
+  static constexpr bool kCentred = byte_sum_code<CB>();
+  static constexpr int kBSlotBytes = (kKext + kExtK) * NB * 2;  // a chunk + the centring block
   static constexpr int kChunkBytesB = kKext * NB * 2;
-  static constexpr int kStripWords = CT * 8 * K;
-  static constexpr int kRowWords = kStripWords + kRowPad;
+  static constexpr int kStripWords = kCT * 8 * K;  // one tile row of the chunk, dense as the tensor copy lands
+  static constexpr int kRowWords = kStripWords;
   static constexpr int kChunkBytes = 8 * kRowWords * 4;
   // the code ring takes what the control block, the operand-B slots and the
-  // output transpose buffer leave (1 KB kept spare)
+  // output transpose buffer leave (1 KB kept spare); a multiple of the
+  // number of teams, so that each slot belongs to one decoder team
   static constexpr int kRingRaw =
-      (kSmemLimit - 1024 - kXWarps * kBSlotBytes - kMaxM * 128 * 4 - 1024) / kChunkBytes;
-  static constexpr int kRing = kRingRaw > kMaxRing ? kMaxRing : (kRingRaw < 2 ? 2 : kRingRaw);
-  static constexpr int kBlocksPerChunk = kPaired ? CT / 8 : 1;  // 128-column blocks of x per chunk
-  static_assert(kTpt % kStoreTiles == 0, "store grouping");
-  static_assert(kDQ * kThreadCols <= kSlotCols, "TMEM slot");
-  static_assert(kACol + kSlots * kSlotCols == kConstCol && kConstCol + 8 <= kTmemCols && 2 * NB <= kACol,
-                "TMEM columns");
-  static_assert(kKext <= 256, "operand-B slot");
+      (kSmemLimit - 1024 - kIssuers * kBSlotBytes - kMaxM * 128 * 4 - 1024) / kChunkBytes;
+  static constexpr int kRingClamped = kRingRaw > kMaxRing ? kMaxRing : (kRingRaw < kTeams ? kTeams : kRingRaw);
+  static constexpr int kRing = kRingClamped - kRingClamped % kTeams;
+  static_assert(2 * NB <= kACol, "D accumulators");
 };
 
 struct MvShared {
   uint64_t ring_full[kMaxRing];
   uint64_t ring_empty[kMaxRing];
-  uint64_t a_full[kSlots];
-  uint64_t a_empty[kSlots];
-  uint64_t b_full[kXWarps];
-  uint64_t b_empty[kXWarps];
+  uint64_t a_full[kIssuers];
+  uint64_t a_empty[kIssuers];
+  uint64_t b_full[kIssuers];
   uint64_t d_full[2];
   uint64_t d_empty[2];
-  uint64_t mma_done;
+  uint64_t mma_done[kIssuers];
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t last;
@@ -183,7 +171,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
-// D[tmem] += A[tmem] x B[smem desc] (accumulating; no predicate set-up per MMA).
+// D[tmem] += A[tmem] x B[smem desc] (always accumulating: D starts zeroed).
 __device__ __forceinline__ void mma_f16_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -203,6 +191,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t v0) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+
+// Tensor copy of one box of a 2-D map into shared memory, completion counted
+// on an mbarrier (coordinates in elements: x innermost).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -225,6 +223,13 @@ __device__ __forceinline__ void locate(const MvParams& p, int u, int& li, int& r
 // CTA whose stream-K range holds unit u (ranges [c*U/G, (c+1)*U/G), G <= U).
 __device__ __forceinline__ int owner(long long u, long long units, long long grid) {
   return static_cast<int>(((u + 1) * grid - 1) / units);
+}
+
+__device__ __forceinline__ void tmem_st16_zero(uint32_t taddr) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(taddr), "r"(0u)
+      : "memory");
 }
 
 // Generator outputs of the 16 steps of one tile row: the windows start at
@@ -270,27 +275,42 @@ __device__ __forceinline__ void row_generate(const uint32_t (&raw)[RowWords<K>::
   }
 }
 
-// One TMEM column of a byte-sum code: the binary16 values 1024 + S of two
-// consecutive weights (the dp4a byte sum spliced into the mantissa of 1024),
-// the first in the lower half.
+// One TMEM column: two consecutive weights of a row as binary16, the first
+// in the lower half, from their generator outputs.
+//   byte-sum codes: 1024 + S (the dp4a byte sum spliced into the mantissa of
+//   1024), centred later by the centring MMA;
+//   three-instruction codes: the defined weight lo + hi, rounded to nearest
+//   even -- one packed add of the word's two halves (broadcast) per weight.
 template <int CB>
-__device__ __forceinline__ uint32_t paired_col(uint32_t g0, uint32_t g1) {
-  const uint32_t d0 = __dp4a(summed_bytes<CB>(g0), 0x01010101u, 0x6400u);
-  const uint32_t d1 = __dp4a(summed_bytes<CB>(g1), 0x01010101u, 0x6400u);
-  return __byte_perm(d0, d1, 0x5410);
+__device__ __forceinline__ uint32_t pack_col(uint32_t g0, uint32_t g1) {
+  if constexpr (byte_sum_code<CB>()) {
+    const uint32_t d0 = __dp4a(summed_bytes<CB>(g0), 0x01010101u, 0x6400u);
+    const uint32_t d1 = __dp4a(summed_bytes<CB>(g1), 0x01010101u, 0x6400u);
+    return __byte_perm(d0, d1, 0x5410);
+  } else {
+    const uint32_t h0 = mask_xor_3inst(g0);
+    const uint32_t h1 = mask_xor_3inst(g1);
+    const __half2 a = *reinterpret_cast<const __half2*>(&h0);
+    const __half2 b = *reinterpret_cast<const __half2*>(&h1);
+    const __half2 w0 = __hadd2(__low2half2(a), __high2half2(a));  // (w0, w0)
+    const __half2 w1 = __hadd2(__low2half2(b), __high2half2(b));  // (w1, w1)
+    return __byte_perm(*reinterpret_cast<const uint32_t*>(&w0), *reinterpret_cast<const uint32_t*>(&w1), 0x5410);
+  }
 }
 
-template <int K, int CB, int CT, int NB, bool FUSE>
-__global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
-  using Cfg = MvCfg<K, CB, CT, NB>;
+template <int K, int CB, int NB, bool FUSE>
+__global__ void __launch_bounds__(kThreads, 1) mv_kernel(const __grid_constant__ MvParams p) {
+  using Cfg = MvCfg<K, CB, NB>;
   constexpr int kRing = Cfg::kRing;
   constexpr int kTw = 8 * K;  // words per tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   MvShared& sh = *reinterpret_cast<MvShared*>(smem_raw);
   const size_t ctrl = (sizeof(MvShared) + 1023) & ~static_cast<size_t>(1023);
-  unsigned char* bslots = smem_raw + ctrl;  // kXWarps x kBSlotBytes, 1024-aligned
-  float* zt = reinterpret_cast<float*>(bslots + kXWarps * Cfg::kBSlotBytes);  // [M][128]
-  uint32_t* ring = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(zt) + kMaxM * 128 * 4);
+  // the code ring first (1024-aligned for the tensor copies), then the
+  // operand-B slots and the output transpose buffer
+  uint32_t* ring = reinterpret_cast<uint32_t*>(smem_raw + ctrl);
+  unsigned char* bslots = smem_raw + ctrl + static_cast<size_t>(kRing) * Cfg::kChunkBytes;  // kIssuers slots
+  float* zt = reinterpret_cast<float*>(bslots + kIssuers * Cfg::kBSlotBytes);  // [M][128]
 
   // The next kernel on the stream may be scheduled now: it waits for this
   // grid to complete before it reads anything this grid writes.
@@ -305,48 +325,30 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
   const int hi = static_cast<int>(U * (blockIdx.x + 1) / G);
 
   // ---- set-up: barriers, TMEM; the code producer issues its first chunks first
-  auto issue_chunk = [&](int seq, int u) {
+  auto issue_chunk = [&](int seq, int u) {  // by lane 0
     int li, rb, kc;
     locate(p, u, li, rb, kc);
-    const MvLayer& L = p.l[li];
     const int slot = seq % kRing;
-    if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[slot], 8u * Cfg::kStripWords * 4u);
-    __syncwarp();
-    if (lane < 8) {
-      uint32_t* dst = ring + static_cast<size_t>(slot) * (Cfg::kChunkBytes / 4) + lane * Cfg::kRowWords;
-      const uint32_t* src =
-          L.codes + (static_cast<size_t>(rb * 8 + lane) * (L.n / 16) + static_cast<size_t>(kc) * CT) * kTw;
-      bulk_g2s(dst, src, Cfg::kStripWords * 4u, &sh.ring_full[slot]);
-    }
+    mbar_arrive_expect_tx(&sh.ring_full[slot], Cfg::kChunkBytes);
+    tma_load_2d(ring + static_cast<size_t>(slot) * (Cfg::kChunkBytes / 4), &p.l[li].codes_map, kc * 32 * K, rb * 8,
+                &sh.ring_full[slot]);
   };
-  int pre = 0;
-  if (warp == kCodeWarp) {
-    if (lane == 0) {
-      for (int i = 0; i < kRing; ++i) {
-        mbar_init(&sh.ring_full[i], 1);
-        mbar_init(&sh.ring_empty[i], kDecWarps);
-      }
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    pre = min(2, hi - lo);
-    for (int s = 0; s < pre; ++s) issue_chunk(s, lo + s);
-  }
-  if (warp == kMmaWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
+  if (warp == kEpiWarp0) tmem_alloc(&sh.tmem_base, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&sh.a_full[i], kDecWarps);
-      mbar_init(&sh.a_empty[i], 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&sh.ring_full[i], 1);
+      mbar_init(&sh.ring_empty[i], 4);  // one elected arrival per warp of the consuming team
     }
-    for (int i = 0; i < kXWarps; ++i) {
+    for (int i = 0; i < kIssuers; ++i) {
+      mbar_init(&sh.a_full[i], 4);  // the four warps of the decoding team
+      mbar_init(&sh.a_empty[i], 1);
       mbar_init(&sh.b_full[i], 1);
-      mbar_init(&sh.b_empty[i], 1);
+      mbar_init(&sh.mma_done[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.d_full[i], 1);
+      mbar_init(&sh.d_full[i], kIssuers);
       mbar_init(&sh.d_empty[i], 4);
     }
-    mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -354,71 +356,96 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  // Both accumulators start at zero (the MMAs always accumulate), and the
+  // centring column of the byte-sum codes holds A = -(1024 + centre) at K
+  // elements 0 and 1, zero elsewhere.
+  if (warp >= kEpiWarp0) {
+    const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    tmem_st16_zero(tmem + lanes + 0);
+    if constexpr (NB > 16) tmem_st16_zero(tmem + lanes + 16);
+    tmem_st16_zero(tmem + lanes + NB);
+    if constexpr (NB > 16) tmem_st16_zero(tmem + lanes + NB + 16);
+    if constexpr (Cfg::kCentred) {
+      const uint32_t c2 =
+          static_cast<uint32_t>(__half_as_ushort(__int2half_rn(-(1024 + byte_sum_centre<CB>())))) * 0x10001u;
+      tmem_st8(tmem + lanes + kConstCol, c2);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp < kDecWarps) {
     // ---- decoders ----------------------------------------------------------------
     const int quarter = warp & 3;
-    const int half = warp >> 2;
+    const int team = warp >> 2;  // 0 .. kTeams-1
+    // The team's lead lane (warp 4*team, lane 0) loads the team's codes: its
+    // first kRing/kTeams chunks now, then at the start of each chunk s the
+    // chunk s - kTeams + kRing, into the slot of chunk s - kTeams (which the
+    // team has finished reading).  A separate producer warp beside the
+    // decoders measured one copy per ~1300 cycles: it starved for issue.
+    const bool lead = quarter == 0 && lane == 0;
+    const int count = hi - lo;
+    int fetched = team;  // the team's next chunk to load
+    if (lead)
+      for (; fetched < count && fetched < kRing; fetched += kTeams) issue_chunk(fetched, lo + fetched);
+    int consumed = team;  // the team's next chunk to wait for
     const int row = quarter * 32 + lane;  // row within the 128-row block (TMEM lane)
     const int trow = row >> 4;
     const int rr = row & 15;
     const int q0 = (rr * K) >> 1;  // first word of the row's window, and its bit offset
     const uint32_t off = static_cast<uint32_t>((rr * K) & 1) * 16u;
-    const uint32_t lane_addr =
-        tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kACol + half * Cfg::kThreadCols;
-    if constexpr (Cfg::kPaired) {
-      // The centring column: A = -(1024 + centre) at K elements 0 and 1, zero
-      // elsewhere (stored once; the first a_full arrival publishes it).
-      if (half == 0) {
-        const uint32_t c2 =
-            static_cast<uint32_t>(__half_as_ushort(__int2half_rn(-(1024 + byte_sum_centre<CB>())))) * 0x10001u;
-        tmem_st8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kConstCol, c2);
-      }
-    }
+    const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
     // the second window of a funnel word through the FMA pipe where the
     // code's other steps load the ALU more (every code but 1MAD)
     constexpr bool kLoByImad = CB != kCb1Mad;
-    int seq = 0;
-    for (int u = lo; u < hi; ++u, ++seq) {
+    for (int u = lo + team, seq = team; u < hi; u += kTeams, seq += kTeams) {
       const int rslot = seq % kRing;
+      if (lead && fetched < count && seq >= kTeams) {
+        // the slot of chunk fetched - kRing = seq - kTeams has been read by all four warps
+        const int prev = fetched - kRing;
+        if (mbar_wait(&sh.ring_empty[prev % kRing], (prev / kRing) & 1)) {
+          issue_chunk(fetched, lo + fetched);
+          fetched += kTeams;
+        } else {
+          set_abort(sh);
+        }
+      }
       bool ok = mbar_wait(&sh.ring_full[rslot], (seq / kRing) & 1);
+      if (ok) consumed = seq + kTeams;
       if (!ok) set_abort(sh);
       if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      const uint32_t* rw = ring + static_cast<size_t>(rslot) * (Cfg::kChunkBytes / 4) + trow * Cfg::kRowWords +
-                           half * Cfg::kTpt * kTw;
-      const int aslot = seq % kSlots;
-      const int ause = seq / kSlots;
+      const uint32_t* rw = ring + static_cast<size_t>(rslot) * (Cfg::kChunkBytes / 4) + trow * Cfg::kRowWords;
+      const int aslot = seq % kIssuers;
+      const int ause = seq / kIssuers;
       bool stop = false;
 #pragma unroll
-      for (int g = 0; g < Cfg::kStores; ++g) {
-        uint32_t raw[Cfg::kStoreTiles][RowWords<K>::kRaw];
+      for (int g = 0; g < 2; ++g) {  // two groups of four tiles, 32 TMEM columns each
+        uint32_t raw[4][RowWords<K>::kRaw];
 #pragma unroll
-        for (int t = 0; t < Cfg::kStoreTiles; ++t) {
+        for (int t = 0; t < 4; ++t) {
 #pragma unroll
           for (int i = 0; i < RowWords<K>::kRaw; ++i) {
             int idx = q0 + i;
             if (idx >= kTw) idx -= kTw;
-            raw[t][i] = rw[(g * Cfg::kStoreTiles + t) * kTw + idx];
+            raw[t][i] = rw[(g * 4 + t) * kTw + idx];
           }
         }
-        if (g == Cfg::kStores - 1) {
+        if (g == 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.ring_empty[rslot]);
         }
         uint32_t v[32];
 #pragma unroll
-        for (int t = 0; t < Cfg::kStoreTiles; ++t) {
+        for (int t = 0; t < 4; ++t) {
           uint32_t gen[16];
           row_generate<K, CB, kLoByImad>(raw[t], off, gen);
-          if constexpr (Cfg::kPaired) {
 #pragma unroll
-            for (int c = 0; c < 16; c += 2) v[t * 8 + c / 2] = paired_col<CB>(gen[c], gen[c + 1]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[t * 16 + c] = mask_xor_3inst(gen[c]);
-          }
+          for (int c = 0; c < 16; c += 2) v[t * 8 + c / 2] = pack_col<CB>(gen[c], gen[c + 1]);
         }
         if (g == 0 && ause > 0) {
+          // the MMAs of the slot's previous chunk (this team's, four back) are done
           ok = mbar_wait(&sh.a_empty[aslot], (ause - 1) & 1);
           if (!ok) set_abort(sh);
           if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) {
@@ -426,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
             break;
           }
         }
-        tmem_st32(lane_addr + aslot * kSlotCols + g * 32, v);
+        tmem_st32(tmem + lanes + kACol + aslot * kSlotCols + g * 32, v);
       }
       if (stop) break;
       tmem_st_wait();
@@ -435,228 +462,176 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
       if (lane == 0) mbar_arrive(&sh.a_full[aslot]);
     }
     tmem_st_wait();
-  } else if (warp == kMmaWarp) {
-    // ---- MMA issue --------------------------------------------------------------------
-    constexpr uint32_t idesc = idesc_f16<NB>();
-    constexpr uint32_t kLbo = (NB / 8) * 128;  // next 8 K elements
-    constexpr uint32_t kSbo = 128;             // next 8 rows of N
-    const uint64_t bdesc0 = smem_desc(smem_u32(bslots), kLbo, kSbo);
-    int seq = 0;
-    int run = 0;
-    bool bad = false;
-    for (int u = lo; u < hi && !bad; ++run) {
-      int li, rb, kc;
-      locate(p, u, li, rb, kc);
-      const int end = min(hi, u + (p.l[li].nkb - kc));
-      const int db = run & 1;
-      const bool okd = run < 2 || mbar_wait(&sh.d_empty[db], ((run >> 1) - 1) & 1);
-      if (__any_sync(0xFFFFFFFFu, !okd)) {
-        set_abort(sh);
-        break;
-      }
-      const uint32_t dt = tmem + static_cast<uint32_t>(db * NB);
-      for (uint32_t acc = 0; u < end; ++u, ++seq, acc = 1) {
-        const int slot = seq % kSlots;
-        const int bslot = seq % kXWarps;
-        const bool ok = mbar_wait(&sh.a_full[slot], (seq / kSlots) & 1) &&
-                        mbar_wait(&sh.b_full[bslot], (seq / kXWarps) & 1) && !aborted(sh);
-        if (__any_sync(0xFFFFFFFFu, !ok)) {
-          set_abort(sh);
-          bad = true;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t bd = bdesc0 + ((static_cast<uint32_t>(bslot) * Cfg::kBSlotBytes) >> 4);
-        const uint32_t at = tmem + kACol + slot * kSlotCols;
-        if (lane == 0) {
-          mma_f16_ts(dt, at, bd, idesc, acc);
-#pragma unroll
-          for (int j = 1; j < Cfg::kMmas; ++j) mma_f16_ts_acc(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc);
-          if constexpr (Cfg::kPaired)  // the centring MMA
-            mma_f16_ts_acc(dt, tmem + kConstCol, bd + ((static_cast<uint32_t>(Cfg::kKext / 8) * kLbo) >> 4), idesc);
-          mma_commit(&sh.a_empty[slot]);
-          mma_commit(&sh.b_empty[bslot]);
-        }
-        __syncwarp();
-      }
-      if (bad) break;
-      if (lane == 0) mma_commit(&sh.d_full[db]);
-      __syncwarp();
-    }
-    if (lane == 0) mma_commit(&sh.mma_done);
-    __syncwarp();
-    mbar_wait(&sh.mma_done, 0);
-  } else if (warp == kCodeWarp) {
-    // ---- code producer ------------------------------------------------------------------
-    int seq = pre;
-    for (int u = lo + pre; u < hi; ++u, ++seq) {
-      const int slot = seq % kRing;
-      const int use = seq / kRing;
-      bool ok = true;
-      if (use > 0) ok = mbar_wait(&sh.ring_empty[slot], (use - 1) & 1);
-      if (!ok) set_abort(sh);
-      if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      issue_chunk(seq, u);
-    }
-    // Every copy issued into the ring must land before the CTA exits.
-    for (int i = 0; i < kRing && i < seq; ++i) {
-      const int s = seq - 1 - i;
-      mbar_wait(&sh.ring_full[s % kRing], (s / kRing) & 1);
-    }
-  } else if (warp < kXWarp0 + kXWarps) {
-    // ---- operand B ----------------------------------------------------------------------
-    // x warp xw produces the chunks seq = xw, xw + kXWarps, ...  The slots
-    // start zeroed (rows M.., the unused K elements of the centring block);
-    // afterwards only rows < M are written.
-    const int xw = warp - kXWarp0;
-    const int xt = tid - kXWarp0 * 32;
+    // Copies the team loaded but never read (an aborted call) must land
+    // before the CTA exits; each slot's phases move only with this team.
+    if (lead)
+      for (int c = consumed; c < fetched; c += kTeams) mbar_wait(&sh.ring_full[c % kRing], (c / kRing) & 1);
+  } else if (warp < kIss0 + kIssuers) {
+    // ---- issuers: operand B, then the MMAs of chunks seq = i (mod 4) --------------------
+    const int is = warp - kIss0;
+    unsigned char* bs = bslots + static_cast<size_t>(is) * Cfg::kBSlotBytes;  // this issuer's slot
     {
-      uint4* bz = reinterpret_cast<uint4*>(bslots);
-      for (int i = xt; i < kXWarps * Cfg::kBSlotBytes / 16; i += 32 * kXWarps) bz[i] = make_uint4(0u, 0u, 0u, 0u);
+      // rows M.. and the centring block's unused K elements stay zero
+      uint4* bz = reinterpret_cast<uint4*>(bs);
+      for (int i = lane; i < Cfg::kBSlotBytes / 16; i += 32) bz[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
-    named_sync(kXBarrier, 32 * kXWarps);
+    __syncwarp();
     // x, the signs and the operand images may be written by the preceding
     // grid on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int M = p.M;
-    unsigned char* bs = bslots + static_cast<size_t>(xw) * Cfg::kBSlotBytes;  // this warp's slot
-    int last = -1;  // the last chunk this warp posted
-    for (int u = lo + xw, seq = xw; u < hi; u += kXWarps, seq += kXWarps) {
-      const int use = seq / kXWarps;
-      int li, rb, kc;
-      locate(p, u, li, rb, kc);
+    const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+    constexpr uint32_t idesc = idesc_f16<NB>();
+    constexpr uint32_t kLbo = (NB / 8) * 128;  // next 8 K elements
+    constexpr uint32_t kSbo = 128;             // next 8 rows of N
+    const uint64_t bd = smem_desc(smem_u32(bs), kLbo, kSbo);
+    const uint32_t at = tm + kACol + is * kSlotCols;
+    bool bad = p.debug_stall != 0;  // test hook: no MMA is ever issued, so the waits on them run out
+    int issued = 0;
+    int run = 0;
+    for (int u0 = lo; u0 < hi && !bad; ++run) {
+      int li, rb, kc0;
+      locate(p, u0, li, rb, kc0);
       const MvLayer& L = p.l[li];
-      // centring sums of this chunk, per batch row (byte-sum codes)
-      float csum[2] = {0.f, 0.f};
-      uint2 hv[Cfg::kBlocksPerChunk * 2];
-      if constexpr (FUSE) {
-        // Load and rotate before waiting for the slot: the L2 latency of x
-        // overlaps the MMAs still reading the slot.
-        uint2 xr[Cfg::kBlocksPerChunk * 2];
-        uint2 sr[Cfg::kBlocksPerChunk];
-#pragma unroll
-        for (int blk = 0; blk < Cfg::kBlocksPerChunk; ++blk) {
-          const int col = kc * CT * 16 + blk * kRowBlock + 4 * lane;
-          sr[blk] = L.s_in != nullptr ? *reinterpret_cast<const uint2*>(L.s_in + col) : make_uint2(0u, 0u);
+      const int u1 = min(hi, u0 + (L.nkb - kc0));  // this run: units u0 .. u1-1
+      const int db = run & 1;
+      const uint32_t dt = tm + static_cast<uint32_t>(db * NB);
+      // the epilogue has taken the run two back out of this accumulator (and zeroed it)
+      if (run >= 2) {
+        const bool okd = mbar_wait(&sh.d_empty[db], ((run >> 1) - 1) & 1);
+        if (!okd) set_abort(sh);
+        if (__any_sync(0xFFFFFFFFu, !okd || aborted(sh))) break;
+      }
+      // this issuer's chunks of the run: seq = u - lo = is (mod kIssuers)
+      const int s0 = u0 - lo, s1 = u1 - lo;
+      int seq = s0 + ((is - s0) % kIssuers + kIssuers) % kIssuers;
+      bool mine = false;
+      for (; seq < s1; seq += kIssuers) {
+        const int kc = kc0 + (seq - s0);
+        const int use = seq / kIssuers;
+        float csum[2] = {0.f, 0.f};  // centring sums of this chunk, per batch row
+        uint2 hv[2];
+        if constexpr (FUSE) {
+          // Load and rotate before waiting for the slot: the L2 latency of x
+          // overlaps the MMAs still reading it.
+          const int col = kc * kCT * 16 + 4 * lane;
+          const uint2 sr = L.s_in != nullptr ? *reinterpret_cast<const uint2*>(L.s_in + col) : make_uint2(0u, 0u);
+          uint2 xr[2];
 #pragma unroll
           for (int b = 0; b < 2; ++b)
-            xr[blk * 2 + b] = b < M ? *reinterpret_cast<const uint2*>(L.x + static_cast<size_t>(b) * L.n + col)
-                                    : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int blk = 0; blk < Cfg::kBlocksPerChunk; ++blk) {
+            xr[b] = b < M ? *reinterpret_cast<const uint2*>(L.x + static_cast<size_t>(b) * L.n + col)
+                          : make_uint2(0u, 0u);
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             if (b < M) {  // warp-uniform
-              const uint2 x2 = xr[blk * 2 + b];
-              float v[4] = {__low2float(*reinterpret_cast<const __half2*>(&x2.x)),
-                            __high2float(*reinterpret_cast<const __half2*>(&x2.x)),
-                            __low2float(*reinterpret_cast<const __half2*>(&x2.y)),
-                            __high2float(*reinterpret_cast<const __half2*>(&x2.y))};
+              float v[4] = {__low2float(*reinterpret_cast<const __half2*>(&xr[b].x)),
+                            __high2float(*reinterpret_cast<const __half2*>(&xr[b].x)),
+                            __low2float(*reinterpret_cast<const __half2*>(&xr[b].y)),
+                            __high2float(*reinterpret_cast<const __half2*>(&xr[b].y))};
               if (L.s_in != nullptr) {
-                v[0] *= __low2float(*reinterpret_cast<const __half2*>(&sr[blk].x));
-                v[1] *= __high2float(*reinterpret_cast<const __half2*>(&sr[blk].x));
-                v[2] *= __low2float(*reinterpret_cast<const __half2*>(&sr[blk].y));
-                v[3] *= __high2float(*reinterpret_cast<const __half2*>(&sr[blk].y));
+                v[0] *= __low2float(*reinterpret_cast<const __half2*>(&sr.x));
+                v[1] *= __high2float(*reinterpret_cast<const __half2*>(&sr.x));
+                v[2] *= __low2float(*reinterpret_cast<const __half2*>(&sr.y));
+                v[3] *= __high2float(*reinterpret_cast<const __half2*>(&sr.y));
                 fwht128_warp(v, lane);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
               }
               const __half2 o01 = __floats2half2_rn(v[0], v[1]);
               const __half2 o23 = __floats2half2_rn(v[2], v[3]);
-              hv[blk * 2 + b].x = *reinterpret_cast<const uint32_t*>(&o01);
-              hv[blk * 2 + b].y = *reinterpret_cast<const uint32_t*>(&o23);
-              if constexpr (Cfg::kPaired)
-                csum[b] += (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+              hv[b].x = *reinterpret_cast<const uint32_t*>(&o01);
+              hv[b].y = *reinterpret_cast<const uint32_t*>(&o23);
+              if constexpr (Cfg::kCentred)
+                csum[b] = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
             }
           }
+        } else if constexpr (Cfg::kCentred) {
+          // the chunk's sum of the binary16 operand values, from the image kernel
+          if (lane < M) csum[0] = __ldcg(L.bsum + static_cast<size_t>(lane) * (L.n / kRowBlock) + kc);
         }
-      } else if constexpr (Cfg::kPaired) {
-        // the chunk's sums of the binary16 operand values, from the image kernel
-        const int nblk = L.n / kRowBlock;
-#pragma unroll
-        for (int blk = 0; blk < Cfg::kBlocksPerChunk; ++blk) {
-          const int b = lane;
-          if (b < M) csum[0] += __ldcg(L.bsum + static_cast<size_t>(b) * nblk + kc * Cfg::kBlocksPerChunk + blk);
+        // wait until this issuer's MMAs of its previous chunk are done with the slots
+        bool ok = true;
+        if (use > 0) ok = mbar_wait(&sh.a_empty[is], (use - 1) & 1);
+        if (!ok) set_abort(sh);
+        if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) {
+          bad = true;
+          break;
         }
-      }
-      // wait until the MMAs of the slot's previous chunk are done with it
-      bool ok = true;
-      if (use > 0) ok = mbar_wait(&sh.b_empty[xw], (use - 1) & 1);
-      if (!ok) set_abort(sh);
-      if (__any_sync(0xFFFFFFFFu, !ok || aborted(sh))) break;
-      if constexpr (!FUSE) {
-        if (lane == 0 && p.debug_stall == 0) {
-          mbar_expect_tx(&sh.b_full[xw], Cfg::kChunkBytesB);
-          bulk_g2s(bs, L.bimg + static_cast<size_t>(kc) * Cfg::kKext * NB, Cfg::kChunkBytesB, &sh.b_full[xw]);
-        }
-      } else {
-#pragma unroll
-        for (int blk = 0; blk < Cfg::kBlocksPerChunk; ++blk) {
+        if constexpr (!FUSE) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sh.b_full[is], Cfg::kChunkBytesB);
+            bulk_g2s(bs, L.bimg + static_cast<size_t>(kc) * kKext * NB, Cfg::kChunkBytesB, &sh.b_full[is]);
+          }
+        } else {
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             if (b < M) {
-              if constexpr (Cfg::kPaired) {
-                // K elements k = blk*128 + 4*lane .. +3: half a 16-byte core row
-                const int k = blk * kRowBlock + 4 * lane;
-                *reinterpret_cast<uint2*>(bs + ((k >> 3) * (NB / 8) + (b >> 3)) * 128 + (b & 7) * 16 + (k & 7) * 2) =
-                    hv[blk * 2 + b];
-              } else {
-                // K elements 8*lane .. 8*lane+7: columns 4*lane .. 4*lane+3, each twice
-                const uint2 h = hv[blk * 2 + b];
-                uint4 o;
-                o.x = (h.x & 0xFFFFu) * 0x10001u;
-                o.y = (h.x >> 16) * 0x10001u;
-                o.z = (h.y & 0xFFFFu) * 0x10001u;
-                o.w = (h.y >> 16) * 0x10001u;
-                *reinterpret_cast<uint4*>(bs + (lane * (NB / 8) + (b >> 3)) * 128 + (b & 7) * 16) = o;
-              }
+              // K elements k = 4*lane .. +3: half a 16-byte core row
+              const int k = 4 * lane;
+              *reinterpret_cast<uint2*>(bs + ((k >> 3) * (NB / 8) + (b >> 3)) * 128 + (b & 7) * 16 + (k & 7) * 2) =
+                  hv[b];
             }
           }
         }
-      }
-      if constexpr (Cfg::kPaired) {
-        // Sum of the chunk's operand values per batch row, as hi + lo in
-        // binary16 at K elements kKext and kKext + 1 of the centring block.
-        float sums[2] = {csum[0], csum[1]};
-        if constexpr (FUSE) {
+        if constexpr (Cfg::kCentred) {
+          // Sum of the chunk's operand values per batch row, as hi + lo in
+          // binary16 at K elements kKext and kKext + 1 of the centring block.
+          float sums[2] = {csum[0], csum[1]};
+          if constexpr (FUSE) {
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < 2; ++b)
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) sums[b] += __shfl_xor_sync(0xFFFFFFFFu, sums[b], d);
-        }
-        constexpr int ke = Cfg::kKext;
-        if constexpr (FUSE) {
+              for (int d = 16; d > 0; d >>= 1) sums[b] += __shfl_xor_sync(0xFFFFFFFFu, sums[b], d);
+          }
           if (lane < M) {
-            const float sv = lane == 0 ? sums[0] : sums[1];
+            const float sv = FUSE ? (lane == 0 ? sums[0] : sums[1]) : sums[0];
             const __half h = __float2half_rn(sv);
             const __half l = __float2half_rn(sv - __half2float(h));
-            *reinterpret_cast<__half2*>(bs + ((ke >> 3) * (NB / 8) + (lane >> 3)) * 128 + (lane & 7) * 16) =
-                __halves2half2(h, l);
-          }
-        } else {
-          if (lane < M) {
-            const __half h = __float2half_rn(sums[0]);
-            const __half l = __float2half_rn(sums[0] - __half2float(h));
-            *reinterpret_cast<__half2*>(bs + ((ke >> 3) * (NB / 8) + (lane >> 3)) * 128 + (lane & 7) * 16) =
+            *reinterpret_cast<__half2*>(bs + ((kKext >> 3) * (NB / 8) + (lane >> 3)) * 128 + (lane & 7) * 16) =
                 __halves2half2(h, l);
           }
         }
+        // generic-proxy stores, read by the tensor core (async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if constexpr (!FUSE) ok = mbar_wait(&sh.b_full[is], use & 1);  // the bulk copy has landed
+        // the decoders' A of this chunk
+        ok = ok && mbar_wait(&sh.a_full[is], use & 1) && !aborted(sh);
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
+          set_abort(sh);
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < kMmas; ++j) mma_f16_ts_acc(dt, at + 8 * j, bd + ((2u * j * kLbo) >> 4), idesc);
+          if constexpr (Cfg::kCentred)  // the centring MMA
+            mma_f16_ts_acc(dt, tm + kConstCol, bd + ((static_cast<uint32_t>(kKext / 8) * kLbo) >> 4), idesc);
+          mma_commit(&sh.a_empty[is]);
+        }
+        __syncwarp();
+        mine = true;
+        ++issued;
       }
-      // generic-proxy stores, read by the tensor core (async proxy)
-      fence_proxy_async_smem();
+      if (bad) break;
+      // this issuer is done with the run: its commit arrives once its MMAs
+      // are complete (a plain arrival if it had no chunk in the run)
+      if (lane == 0) {
+        if (mine)
+          mma_commit(&sh.d_full[db]);
+        else
+          mbar_arrive(&sh.d_full[db]);
+      }
       __syncwarp();
-      // With the failure-detection test hook set operand B is never posted,
-      // so the MMA lane's bounded wait runs out.
-      if (lane == 0 && p.debug_stall == 0) mbar_arrive(&sh.b_full[xw]);
-      last = seq;
+      u0 = u1;
     }
-    if constexpr (!FUSE) {
-      // The bulk copy of the last chunk posted must land before the CTA
-      // exits (every earlier one was consumed before this warp waited for
-      // its slot again); only this warp moves its slot's b_full phases.
-      if (lane == 0 && p.debug_stall == 0 && last >= 0) mbar_wait(&sh.b_full[xw], (last / kXWarps) & 1);
+    // every MMA this issuer started has completed before TMEM is freed
+    if (issued > 0) {
+      if (lane == 0) mma_commit(&sh.mma_done[is]);
+      __syncwarp();
+      mbar_wait(&sh.mma_done[is], 0);
     }
   } else {
     // ---- epilogue ---------------------------------------------------------------------
@@ -665,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
     const int ew = warp & 3;  // TMEM lane quarter
     const int et = tid - kEpiWarp0 * 32;
     const int row = ew * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(ew * 32) << 16;
     const int M = p.M;
     const float factor = x_factor<CB>();
     int run = 0;
@@ -688,15 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
       float d[NB];
       {
         float d16[16];
-        tc::tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + db * NB, d16);
+        tc::tmem_ld16(tmem + lanes + db * NB, d16);
 #pragma unroll
         for (int j = 0; j < 16; ++j) d[j] = d16[j];
         if constexpr (NB > 16) {
-          tc::tmem_ld16(tmem + (static_cast<uint32_t>(ew * 32) << 16) + db * NB + 16, d16);
+          tc::tmem_ld16(tmem + lanes + db * NB + 16, d16);
 #pragma unroll
           for (int j = 0; j < 16; ++j) d[16 + j] = d16[j];
         }
       }
+      // zero the accumulator for the run after next, then hand it back
+      tmem_st16_zero(tmem + lanes + db * NB);
+      if constexpr (NB > 16) tmem_st16_zero(tmem + lanes + db * NB + 16);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.d_empty[db]);
@@ -749,28 +729,28 @@ __global__ void __launch_bounds__(kThreads, 1) mv_kernel(const MvParams p) {
   // ---- teardown ---------------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kEpiWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
   if (tid == 0 && aborted(sh) && p.status != nullptr) atomicOr(p.status, 1u);
 }
 
-template <int K, int CB, int CT, int NB>
+template <int K, int CB, int NB>
 inline size_t mv_smem_bytes() {
-  using Cfg = MvCfg<K, CB, CT, NB>;
+  using Cfg = MvCfg<K, CB, NB>;
   const size_t ctrl = (sizeof(MvShared) + 1023) & ~static_cast<size_t>(1023);
-  return ctrl + static_cast<size_t>(kXWarps) * Cfg::kBSlotBytes + static_cast<size_t>(kMaxM) * 128 * 4 +
-         static_cast<size_t>(Cfg::kRing) * Cfg::kChunkBytes;
+  return ctrl + static_cast<size_t>(Cfg::kRing) * Cfg::kChunkBytes + static_cast<size_t>(kIssuers) * Cfg::kBSlotBytes +
+         static_cast<size_t>(kMaxM) * 128 * 4;
 }
 
-template <int K, int CB, int CT, int NB, bool FUSE>
+template <int K, int CB, int NB, bool FUSE>
 exl3_status launch_mv_t(const MvParams& p, int grid, cudaStream_t stream) {
-  size_t smem = mv_smem_bytes<K, CB, CT, NB>();
+  size_t smem = mv_smem_bytes<K, CB, NB>();
   // At least 116 KB so that a single CTA is resident per SM (it owns all 512
   // TMEM columns; a second CTA would wait in tcgen05.alloc).
   if (smem < 116 * 1024) smem = 116 * 1024;
-  if (cudaFuncSetAttribute(mv_kernel<K, CB, CT, NB, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(mv_kernel<K, CB, NB, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return EXL3_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -783,35 +763,25 @@ exl3_status launch_mv_t(const MvParams& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mv_kernel<K, CB, CT, NB, FUSE>, p) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, mv_kernel<K, CB, NB, FUSE>, p) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
 
-// Tiles per chunk: 16 for the byte-sum codes when ct16 (every n a multiple
-// of 256), else 8; N = 16 up to 16 batch rows, else 32; the x warps compute
-// x-tilde for M <= 2.
+// N = 16 up to 16 batch rows, else 32; x-tilde computed in the kernel for M <= 2.
 template <int K, int CB>
-exl3_status launch_mv_cb(const MvParams& p, int grid, bool ct16, cudaStream_t stream) {
-  const bool fuse = p.M <= 2;
-  if constexpr (paired_code<CB>()) {
-    if (ct16) {
-      if (fuse) return launch_mv_t<K, CB, 16, 16, true>(p, grid, stream);
-      if (p.M <= 16) return launch_mv_t<K, CB, 16, 16, false>(p, grid, stream);
-      return launch_mv_t<K, CB, 16, 32, false>(p, grid, stream);
-    }
-  }
-  if (fuse) return launch_mv_t<K, CB, 8, 16, true>(p, grid, stream);
-  if (p.M <= 16) return launch_mv_t<K, CB, 8, 16, false>(p, grid, stream);
-  return launch_mv_t<K, CB, 8, 32, false>(p, grid, stream);
+exl3_status launch_mv_cb(const MvParams& p, int grid, cudaStream_t stream) {
+  if (p.M <= 2) return launch_mv_t<K, CB, 16, true>(p, grid, stream);
+  if (p.M <= 16) return launch_mv_t<K, CB, 16, false>(p, grid, stream);
+  return launch_mv_t<K, CB, 32, false>(p, grid, stream);
 }
 
 template <int K>
-exl3_status launch_mv_dispatch(const MvParams& p, int codebook, int grid, bool ct16, cudaStream_t stream) {
+exl3_status launch_mv_dispatch(const MvParams& p, int codebook, int grid, cudaStream_t stream) {
   switch (codebook) {
-    case kCb3Inst: return launch_mv_cb<K, kCb3Inst>(p, grid, ct16, stream);
-    case kCb1Mad: return launch_mv_cb<K, kCb1Mad>(p, grid, ct16, stream);
-    case kCbMcg: return launch_mv_cb<K, kCbMcg>(p, grid, ct16, stream);
-    default: return launch_mv_cb<K, kCbMul1>(p, grid, ct16, stream);
+    case kCb3Inst: return launch_mv_cb<K, kCb3Inst>(p, grid, stream);
+    case kCb1Mad: return launch_mv_cb<K, kCb1Mad>(p, grid, stream);
+    case kCbMcg: return launch_mv_cb<K, kCbMcg>(p, grid, stream);
+    default: return launch_mv_cb<K, kCbMul1>(p, grid, stream);
   }
 }
 
@@ -820,8 +790,7 @@ exl3_status launch_mv_dispatch(const MvParams& p, int codebook, int grid, bool c
 
 #define EXL3_DEFINE_MV_LAUNCHER(KK)                                                                  \
   namespace exl3 {                                                                                   \
-  exl3_status launch_mv_k##KK(const MvParams& p, int codebook, int grid, bool ct16,                  \
-                              cudaStream_t stream) {                                                 \
-    return mv::launch_mv_dispatch<KK>(p, codebook, grid, ct16, stream);                              \
+  exl3_status launch_mv_k##KK(const MvParams& p, int codebook, int grid, cudaStream_t stream) {      \
+    return mv::launch_mv_dispatch<KK>(p, codebook, grid, stream);                                    \
   }                                                                                                  \
   }

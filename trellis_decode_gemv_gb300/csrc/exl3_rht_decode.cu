@@ -65,10 +65,7 @@ __global__ void __launch_bounds__(kThreads)
 // R batch rows per warp (the launcher uses R = 1, for the small tiles of the
 // skinny tensor-core kernel: many warps, the shortest latency to the MMA
 // kernel waiting for it; tiles of 128 rows and more use bimg8_kernel below).
-// With DUP (the decode-MMA kernel's three-instruction codes, whose operand A
-// holds the two halves of each weight as two K elements) every value is
-// stored twice, at k = 2c and 2c + 1 of a (nb x 256) image per 128 columns.
-template <int R, bool DUP = false>
+template <int R>
 __global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
     bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
                 __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
@@ -125,22 +122,10 @@ __global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
         if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
       }
     }
-    if constexpr (DUP) {
-      // k = 8 * lane .. 8 * lane + 7: one whole 16-byte core-matrix row
-      const size_t off = static_cast<size_t>(tile) * nb * 2 * n + static_cast<size_t>(kb) * nb * 2 * kRowBlock +
-                         (static_cast<size_t>(lane) * (nb / 8) + r / 8) * 64 + (r % 8) * 8;
-      uint4 d;
-      d.x = (o.x & 0xFFFFu) * 0x10001u;
-      d.y = (o.x >> 16) * 0x10001u;
-      d.z = (o.y & 0xFFFFu) * 0x10001u;
-      d.w = (o.y >> 16) * 0x10001u;
-      *reinterpret_cast<uint4*>(bimg + off) = d;
-    } else {
-      // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
-      const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
-                         (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
-      *reinterpret_cast<uint2*>(bimg + off) = o;
-    }
+    // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
+    const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
+                       (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
+    *reinterpret_cast<uint2*>(bimg + off) = o;
   }
 }
 
@@ -431,18 +416,6 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
   const long long per_cta = kThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
   rht_kernel<<<grid, kThreads, 0, stream>>>(in, signs, out, blocks, d);
-  return launch_status();
-}
-
-exl3_status launch_bimg_mv(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M, int nb, int n,
-                           bool dup, cudaStream_t stream) {
-  const long long blocks = static_cast<long long>((M + nb - 1) / nb) * nb * (n / kRowBlock);
-  const long long per_cta = kSmallThreads / 32;
-  const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  if (dup)
-    bimg_kernel<1, true><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
-  else
-    bimg_kernel<1, false><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
 }
 
