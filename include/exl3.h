@@ -112,8 +112,9 @@ exl3_status exl3_decode_tiles(const uint32_t *codes, int K, int codebook, int m,
 /**
  * Bytes of scratch that exl3_gemv / exl3_gemm_small need for an m x n layer
  * at batch M: per-row-block counters and the status word, M*m fp32 row sums,
- * and for the tensor-core kernel the rotated input laid out as its MMA
- * operand (16 or 32 rows of n halves) with M*(n/128) fp32 block sums.
+ * and then either the warp-shuffle kernel's x pairs (M*n 32-bit words) or the
+ * decode-MMA kernel's rotated input laid out as its MMA operand (16 or 32
+ * rows of n halves) with M*(n/128) fp32 block sums.
  * Returns 0 for an invalid shape or batch.  The workspace must be zero-filled
  * once after allocation; every call leaves it zero-filled again.  Two calls
  * that may run concurrently must not share a workspace.  The uint32 at byte
@@ -127,8 +128,13 @@ size_t exl3_workspace_bytes(int m, int n, int M);
 /**
  * Fused batch-1 layer (the decode-time quantized linear of Deep Dive
  * Sections 2-3):  y = Hb(s_out (.) (scale (.) (W-hat Hb(s_in (.) x)))),
- * W-hat decoded on the fly from `codes`, products accumulated in fp32, y
- * rounded once to binary16.
+ * W-hat decoded on the fly from `codes`, y rounded once to binary16.
+ * Arithmetic: on the warp-shuffle kernel (batch 1 and 2 by default) each
+ * weight-activation product is formed and summed in binary16 over the 16
+ * columns of one tile, and the tile sums are accumulated in fp32; on the
+ * decode-MMA kernel (batch 3 to 32 by default) binary16 weights and
+ * binary16 rotated activations meet in tcgen05 MMAs that accumulate in fp32.
+ * Both stay within the documented tolerance of the exact layer.
  *   x [n] halves, y [m] halves, scales [m] halves (required);
  *   s_in [n] / s_out [m] or NULL (no rotation on that side);
  *   workspace: >= exl3_workspace_bytes(m, n, 1) bytes, see there.
@@ -305,8 +311,11 @@ exl3_status exl3_gemm_int8act(const uint32_t *codes, int K, int codebook, int m,
 /**
  * Kernel launches one exl3_gemm (or exl3_gemm_small / exl3_gemv, M <= 32)
  * call of this shape and batch makes on the current device under the current
- * exl3_set_path setting: 3 on the tensor-core path; 2 or 3 per batch chunk on
- * the warp-shuffle path; 2 for the fused prefill, 3 for the decode-once
+ * exl3_set_path setting.  Up to 32 rows: on the decode-MMA kernel 1 at M <= 2
+ * (input transform, layer and output transform in one launch) and 2 above
+ * (operand image, layer kernel); on the warp-shuffle kernel 2 or 3 per batch
+ * chunk (x pairs when the layer is split into sub-units, layer, output
+ * transform).  Above 32 rows: 2 for the fused prefill, 3 for the decode-once
  * prefill (exl3_set_prefill); 3 per 128-row pass for the prefill passes.  0
  * for an invalid shape or M < 1.
  */
@@ -329,9 +338,12 @@ typedef struct {
 
 /**
  * Bytes of scratch for exl3_gemm_grouped over `layers` at batch M: a status
- * word, then for every layer M*m fp32 row sums and M*n 32-bit x pairs (each
- * 256-byte aligned).  Same zero-fill contract as exl3_workspace_bytes: the
- * status word is at byte 0.  Returns 0 for an invalid group.
+ * word (first 256 bytes), then for every layer its per-row-block counters
+ * and M*m fp32 row sums, then for every layer the larger of
+ * min(M, 8)*n 32-bit x pairs and, for M > 2, the decode-MMA operand image
+ * with its block sums (as for exl3_workspace_bytes); each region 256-byte
+ * aligned.  Same zero-fill contract as exl3_workspace_bytes: the status word
+ * is at byte 0.  Returns 0 for an invalid group.
  */
 size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
 
@@ -342,9 +354,12 @@ size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
  * it serves decoders that apply several projections to the same step (q, k
  * and v; gate and up).  `layers` is a host array read during the call.  No
  * layer may read another layer's output (x of one aliasing y of another) in the
- * same call.  At batch M <= 2 the layers share one chain of three kernels (x
- * pairs, one decode+GEMV kernel over the tiles of every layer, output
- * transform); above, each layer runs the tensor-core path in turn.
+ * same call.  On the warp-shuffle kernel the layers share one chain per batch
+ * chunk (x pairs of every layer, one decode+GEMV kernel over the tiles of
+ * every layer, one output kernel for every layer); on the decode-MMA kernel
+ * one operand image per layer, then one layer kernel over the tiles of every
+ * layer (at M <= 2, that one launch alone).  The workspace's per-layer
+ * scratch is sized for either.
  */
 exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
                               void *workspace, size_t workspace_bytes, exl3_stream_t stream);
@@ -395,9 +410,9 @@ exl3_status exl3_gemm_int8act_grouped(const exl3_layer *layers, int count, int K
 
 /** Kernel family used by exl3_gemv / exl3_gemm_small. */
 typedef enum {
-  EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, tensor-core kernel above */
-  EXL3_PATH_SHUFFLE = 1, /**< decode + fp32 FMA + warp-shuffle reduction, any M */
-  EXL3_PATH_TENSOR = 2   /**< decoded tiles in TMEM feeding tcgen05 MMAs, any M */
+  EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, decode-MMA kernel above */
+  EXL3_PATH_SHUFFLE = 1, /**< decode + binary16 FMA per tile, fp32 across tiles, warp-shuffle reduction; any M */
+  EXL3_PATH_TENSOR = 2   /**< decode-MMA: decoded tiles in TMEM feeding tcgen05 MMAs (fp32 accumulation); any M */
 } exl3_path;
 
 /** Prefill strategy of exl3_gemm above EXL3_MAX_BATCH rows. */

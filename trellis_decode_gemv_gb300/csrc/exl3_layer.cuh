@@ -20,11 +20,9 @@
 //     binary16 and zeroes zacc for the next call.
 //
 // Work split: a sub-unit is up to S (16, 8 or 4) consecutive tiles of one tile
-// row; the (m/16) x ceil((n/16)/S) sub-units are cut into gridDim.x equal
-// contiguous ranges, one per CTA (one CTA per SM).  Inside a CTA each warp
-// starts on its own sub-unit and then takes the next free one from a
-// shared-memory counter, so the warps of an SM finish together whatever the
-// scheduler's priorities.  In a sub-unit, lane 8*jt + p handles tiles
+// row; one CTA per SM.  Each warp starts on its own sub-unit and then takes
+// the next free one from a device-wide counter, so the warps of all SMs
+// finish together whatever the scheduler's priorities.  In a sub-unit, lane 8*jt + p handles tiles
 // J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each: 32 consecutive
 // trellis steps from a word-aligned window per tile (code words loaded two
 // tiles ahead of their decode), with the x pairs of the tile's 16 columns read
@@ -270,7 +268,35 @@ __host__ __device__ constexpr int layer_max_regs() {
   return K <= 3 ? 56 : 64;
 }
 
-template <int K, int CB, int MB>
+// Generator outputs of the 32 steps of a row pair (rows 2p, 2p+1 of a tile):
+// the windows at bits K*c of the pair's words w.  When K divides 16 one
+// 32-bit funnel word r holds the windows of steps c (top half) and c + 16/K
+// (bottom half): one funnel shift, a shift and a mask for two windows.
+template <int K, int CB>
+__device__ __forceinline__ void pair_generate(const uint32_t (&w)[RowPair<K>::kPairWords], uint32_t (&g)[32]) {
+  constexpr uint32_t kAdd = (CB == kCbMcg || CB == kCbMul1) ? 0u : kLcgAdd;
+  if constexpr (16 % K == 0) {
+    constexpr int D = 16 / K;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if ((c / D) % 2 == 0) {
+        const uint32_t r = pair_bits32<K>(w, K * c);
+        g[c] = (r >> 16) * kLcgMul + kAdd;
+        g[c + D] = (r & 0xFFFFu) * kLcgMul + kAdd;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) g[c] = pair_state<K>(w, c) * kLcgMul + kAdd;
+  }
+}
+
+// One sub-unit kernel pass: sub-units of 4*TPL tiles of one tile row, lane
+// 8*jt + p taking tiles J0 + jt + 4t (t < TPL) and rows 2p, 2p+1 of each.
+// Work: warp w of CTA b takes sub-units b * warps + w + i * (grid * warps).
+// (A device-wide atomic counter balanced the SMs better but cost more than
+// it saved: one L2 address taking an atomic from every warp per sub-unit.)
+template <int K, int CB, int MB, int TPL>
 __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   constexpr int kWarps = layer_warps<MB>();
   const int tid = threadIdx.x;
@@ -279,22 +305,17 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   const int jt = lane >> 3;
   const int p = lane & 7;
   constexpr int kTw = RowPair<K>::kTileWords;
-  const int S = g.sub;
-  const long long units = g.units;
-  const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
-  const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
+  const int units = g.units;
+  const int stride = static_cast<int>(gridDim.x) * kWarps;
   // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
   const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
-  __shared__ int next_unit;
 
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (tid == 0) next_unit = 0;
-  __syncthreads();
 
   bool waited = false;
-  int u = u_lo + warp;  // first sub-unit: one per warp; then from the counter
-  while (u < u_hi) {
+  int u = static_cast<int>(blockIdx.x) * kWarps + warp;
+  while (u < units) {
     // the layer of sub-unit u, then its tile row and first tile column
     int li = 0;
     while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
@@ -302,85 +323,78 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
     const int nt = a.n / 16;
     const int lu = u - a.u_begin;
     const int I = lu / a.per_row;
-    const int J0 = (lu - I * a.per_row) * S;
-    const int J1 = J0 + S < nt ? J0 + S : nt;
-    const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
+    const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
+    const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
 
-    // Code words are loaded two tiles ahead of their decode.
-    int J = J0 + jt;
-    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
-    if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
-    if (J + 4 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
-    // The x pairs and the zeroed row sums come from the preceding grids on the
-    // stream; the code words above do not.
+    // Code words two tiles ahead of their decode.
+    uint32_t w[2][RowPair<K>::kPairWords];
+    if (J0 < nt) load_row_pair<K>(tp, p, w[0]);
+    if (TPL > 1 && J0 + 4 < nt) load_row_pair<K>(tp + 4 * kTw, p, w[1]);
+    // The x pairs and the zeroed row sums come from the preceding grids on
+    // the stream; the code words above do not.
     if (!waited) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       waited = true;
     }
-    // Take the next sub-unit now; its latency hides under this one.
-    int un = 0;
-    if (lane == 0) un = u_lo + kWarps + atomicAdd(&next_unit, 1);
-    un = __shfl_sync(0xFFFFFFFFu, un, 0);
 
     float acc[MB][2];
 #pragma unroll
     for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
 
-    while (J < J1) {
-      uint32_t st[32];
-      pair_states<K>(w0, st);
 #pragma unroll
-      for (int i = 0; i < RowPair<K>::kPairWords; ++i) w0[i] = w1[i];
-      if (J + 8 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 8) * kTw, p, w1);
-      const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
-      J += 4;
-      __half2 ha[MB], hb[MB];
+    for (int t = 0; t < TPL; ++t) {
+      const int J = J0 + 4 * t;
+      if (J < nt) {  // all lanes but on a row's ragged last sub-unit
+        uint32_t gen[32];
+        pair_generate<K, CB>(w[t & 1], gen);
+        if (t + 2 < TPL && J + 8 < nt) load_row_pair<K>(tp + (4 * t + 8) * kTw, p, w[t & 1]);
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
+        __half2 ha[MB], hb[MB];
 #pragma unroll
-      for (int b = 0; b < MB; ++b) {
-        ha[b] = __float2half2_rn(0.f);
-        hb[b] = __float2half2_rn(0.f);
-      }
+        for (int b = 0; b < MB; ++b) {
+          ha[b] = __float2half2_rn(0.f);
+          hb[b] = __float2half2_rn(0.f);
+        }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 xv[MB];
+        for (int q = 0; q < 4; ++q) {
+          uint4 xv[MB];
 #pragma unroll
-        for (int b = 0; b < MB; ++b) xv[b] = xrow[static_cast<size_t>(b) * (a.n / 4) + q];
+          for (int b = 0; b < MB; ++b) xv[b] = xrow[static_cast<size_t>(b) * (a.n / 4) + q];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = 4 * q + j;
-          const uint32_t xa = generate<CB>(st[c]);
-          const uint32_t xb = generate<CB>(st[16 + c]);
-          if constexpr (!byte_sum_code<CB>()) {
-            const uint32_t pa = mask_xor_3inst(xa);
-            const uint32_t pb = mask_xor_3inst(xb);
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * q + j;
+            if constexpr (!byte_sum_code<CB>()) {
+              const uint32_t pa = mask_xor_3inst(gen[c]);
+              const uint32_t pb = mask_xor_3inst(gen[16 + c]);
 #pragma unroll
-            for (int b = 0; b < MB; ++b) {
-              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
-              const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
-              ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
-              hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
-            }
-          } else {
-            const uint32_t ra = __dp4a(summed_bytes<CB>(xa), 0x01010101u, 0x6400u);
-            const uint32_t rb2 = __dp4a(summed_bytes<CB>(xb), 0x01010101u, 0x6400u);
-            const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
-            const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
+              for (int b = 0; b < MB; ++b) {
+                const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+                const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
+                ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
+                hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
+              }
+            } else {
+              const uint32_t ra = __dp4a(summed_bytes<CB>(gen[c]), 0x01010101u, 0x6400u);
+              const uint32_t rb2 = __dp4a(summed_bytes<CB>(gen[16 + c]), 0x01010101u, 0x6400u);
+              const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
+              const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
 #pragma unroll
-            for (int b = 0; b < MB; ++b) {
-              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
-              ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
+              for (int b = 0; b < MB; ++b) {
+                const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+                ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
+              }
             }
           }
         }
-      }
 #pragma unroll
-      for (int b = 0; b < MB; ++b) {
-        if constexpr (!byte_sum_code<CB>()) {
-          acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
-          acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
-        } else {
-          acc[b][0] += __low2float(ha[b]);
-          acc[b][1] += __high2float(ha[b]);
+        for (int b = 0; b < MB; ++b) {
+          if constexpr (!byte_sum_code<CB>()) {
+            acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
+            acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
+          } else {
+            acc[b][0] += __low2float(ha[b]);
+            acc[b][1] += __high2float(ha[b]);
+          }
         }
       }
     }
@@ -404,21 +418,21 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
         atomicAdd(z + 1, acc[b][1]);
       }
     }
-    u = un;
+    u += stride;
   }
 }
 
-template <int K, int CB, int MB>
+template <int K, int CB, int MB, int TPL>
 __global__ void __maxnreg__(layer_max_regs<K>()) layer_kernel(const GroupArgs g) {
-  layer_body<K, CB, MB>(g);
+  layer_body<K, CB, MB, TPL>(g);
 }
 
-template <int K, int CB, int MB>
+template <int K, int CB, int MB, int TPL>
 __global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) layer_kernel_wide(const GroupArgs g) {
-  layer_body<K, CB, MB>(g);
+  layer_body<K, CB, MB, TPL>(g);
 }
 
-template <int K, int CB, int MB>
+template <int K, int CB, int MB, int TPL>
 exl3_status launch_layer_t(const GroupArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
@@ -432,9 +446,9 @@ exl3_status launch_layer_t(const GroupArgs& a, cudaStream_t stream) {
   cfg.numAttrs = 1;
   cudaError_t e;
   if constexpr (MB == 1)
-    e = cudaLaunchKernelEx(&cfg, layer_kernel<K, CB, MB>, a);
+    e = cudaLaunchKernelEx(&cfg, layer_kernel<K, CB, MB, TPL>, a);
   else
-    e = cudaLaunchKernelEx(&cfg, layer_kernel_wide<K, CB, MB>, a);
+    e = cudaLaunchKernelEx(&cfg, layer_kernel_wide<K, CB, MB, TPL>, a);
   if (e != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
 }
@@ -465,14 +479,24 @@ exl3_status launch_seg_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
   }
 }
 
-// The sub-unit kernel over a group of layers.
+// The sub-unit kernel over a group of layers (sub-units of a.sub = 16, 8 or 4
+// tiles: 4, 2 or 1 tiles per lane).
+template <int K, int CB, int MB>
+exl3_status launch_group_mb(const GroupArgs& a, cudaStream_t stream) {
+  switch (a.sub) {
+    case 16: return launch_layer_t<K, CB, MB, 4>(a, stream);
+    case 8: return launch_layer_t<K, CB, MB, 2>(a, stream);
+    default: return launch_layer_t<K, CB, MB, 1>(a, stream);
+  }
+}
+
 template <int K, int CB>
 exl3_status launch_group_cb(const GroupArgs& a, int mb, cudaStream_t stream) {
   switch (mb) {
-    case 1: return launch_layer_t<K, CB, 1>(a, stream);
-    case 2: return launch_layer_t<K, CB, 2>(a, stream);
-    case 4: return launch_layer_t<K, CB, 4>(a, stream);
-    case 8: return launch_layer_t<K, CB, 8>(a, stream);
+    case 1: return launch_group_mb<K, CB, 1>(a, stream);
+    case 2: return launch_group_mb<K, CB, 2>(a, stream);
+    case 4: return launch_group_mb<K, CB, 4>(a, stream);
+    case 8: return launch_group_mb<K, CB, 8>(a, stream);
     default: return EXL3_ERR_BATCH;
   }
 }
