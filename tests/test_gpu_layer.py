@@ -186,6 +186,13 @@ def test_mixed_stack_shapes_sampled(name, m, n, K):
     _sampled(name, m, n, K, 0, 1, config=4, index=K * 1000 + m // 128, blocks=2)
 
 
+@pytest.mark.parametrize("M", [1, 2])
+def test_ragged_units_sampled(M):
+    """A long layer with n/16 = 72 tile columns: the batch-1/2 kernel cuts tile
+    rows into 16-tile units, so every row ends in a partial unit of 8 tiles."""
+    _sampled(f"34688x1152 M={M}", 34688, 1152, 2, 1, M, config=69, index=M, blocks=3)
+
+
 def test_layer_object_matches_functional_call():
     """binding.Exl3Linear (the layer marshalled once) gives the functional
     call's result, for batch 1 and a smaller batch than it was built for."""
