@@ -197,6 +197,33 @@ def decoder_groups(gemvs, grouped: bool = True):
     return out
 
 
+def class_groups(gemvs, max_group: int):
+    """Calls of one step when every GEMV of the step that shares K and the code
+    goes into one exl3_gemm_grouped call (at most max_group layers each): the
+    GEMVs of a step are independent, each on its own x, so one kernel chain
+    serves a whole class."""
+    order, by = [], {}
+    for i, g in enumerate(gemvs):
+        key = (g[3], g[4])
+        if key not in by:
+            by[key] = []
+            order.append(key)
+        by[key].append(i)
+    out = []
+    for key in order:
+        idx = by[key]
+        out += [idx[s:s + max_group] for s in range(0, len(idx), max_group)]
+    return out
+
+
+GROUPING_CALLS = {
+    "class": "every GEMV of the step that shares K and the code in one grouped call",
+    "decoder": "q/k/v and gate/up grouped per call (the projections a decoder applies to one step), "
+               "the rest one call each",
+    "none": "one call per GEMV",
+}
+
+
 def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     """Kernel launches of one grouped call over layers of the given (m, n):
     one decode-MMA launch over every layer (plus one operand-image kernel per
@@ -467,7 +494,7 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8):
     return kernels_per_group(path, M, shapes, sms)
 
 
-def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cpu=False):
+def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cpu=False, grouping=None):
     """One workload: resident inputs, warm-up, graph capture, `steps` timed
     graph replays (CUDA events on the launch stream), per-call apportioning,
     roofline terms, the end-to-end leg and (optionally) the oracle baseline."""
@@ -515,8 +542,14 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     torch.cuda.synchronize(dev)
 
     # grouped calls take at most 32 batch rows
-    groups = decoder_groups([(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls],
-                            grouped=not (args.ungrouped or (whole and M > 32)))
+    grouping = grouping or args.grouping
+    if M > 32:
+        grouping = "none"
+    shapes_kc = [(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls]
+    if grouping == "class":
+        groups = class_groups(shapes_kc, B.MAX_GROUP)
+    else:
+        groups = decoder_groups(shapes_kc, grouped=grouping == "decoder")
     gws_of = (B.exl3_group_i8_workspace_bytes if int8 else B.exl3_gemm_whole_grouped_workspace_bytes if whole
               else B.exl3_group_workspace_bytes)
     gws = max([gws_of([(calls[i]["m"], calls[i]["n"]) for i in g], M)
@@ -721,14 +754,11 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
                    "weights_per_step": weights_step, "packed_bytes_per_step": packed,
                    "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
                    "cuda_graph": graph is not None, "kernel_path": args.path, "prefill": args.prefill,
-                   "calls": ("q/k/v grouped per exl3_gemm_whole_grouped call, o one exl3_gemm_whole call"
-                             if whole and not args.ungrouped and M <= 32 else "one exl3_gemm_whole call per GEMV")
-                   if whole else
-                   ("q/k/v and gate/up grouped per exl3_gemm_int8act_grouped call, the rest one "
-                    "exl3_gemm_int8act call each" if not args.ungrouped else "one exl3_gemm_int8act call per GEMV")
-                   if int8 else
-                   "q/k/v and gate/up grouped per exl3_gemm_grouped call" if not args.ungrouped
-                   else "one exl3_gemm_small call per GEMV"},
+                   "grouping": grouping,
+                   "calls": GROUPING_CALLS[grouping] + (
+                       " (exl3_gemm_whole_grouped / exl3_gemm_whole)" if whole else
+                       " (exl3_gemm_int8act_grouped / exl3_gemm_int8act)" if int8 else
+                       " (exl3_gemm_grouped / exl3_gemm_small)") + f"; {len(groups)} calls per step"},
         "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
         "macs_per_s": value * M,
         "roofline_pct": roof_pct,
@@ -832,6 +862,9 @@ def _summary(r):
     out["e2e"] = None if r["e2e"] is None else {"value": r["e2e"]["value"], "unit": r["e2e"]["unit"]}
     out["per_code"] = r["per_code"]
     out["clocks"] = r["clocks"]
+    out["grouping"] = r["config"]["grouping"]
+    if "decoder_grouping" in r:
+        out["decoder_grouping"] = r["decoder_grouping"]
     return out
 
 
@@ -864,15 +897,28 @@ def run_ours(args):
                p_int=sms * INT_LANES_PER_SM_CLK * sm_max_mhz * 1e6, clocks=clocks)
     ctx["probe"] = int_peak_probe(B, torch, dev, stream, sms, sm_max_mhz)
 
+    def with_decoder_grouping(res, wl, M):
+        # the same workload with only the decoder's own groups (q/k/v,
+        # gate/up): every other GEMV of the step waits for its predecessor
+        if args.grouping != "class" or M > 32 or wl in ("encode",):
+            return res
+        d = measure_workload(ctx, args, wl, M, min(args.steps, 300), args.warmup, want_e2e=False,
+                             want_cpu=False, grouping="decoder")
+        res["decoder_grouping"] = {"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+                                   "roofline_frac": d["roofline"]["frac"], "calls": d["config"]["calls"],
+                                   "steps": d["steps"]}
+        return res
+
     if args.workload == "all":
         runs = {}
         for key, wl, M in ALL_CONFIGS:
-            runs[key] = measure_workload(ctx, args, wl, M, args.steps, args.warmup,
-                                         want_e2e=True, want_cpu=(key == "C1"))
+            runs[key] = with_decoder_grouping(measure_workload(ctx, args, wl, M, args.steps, args.warmup,
+                                                               want_e2e=True, want_cpu=(key == "C1")), wl, M)
         head = runs["C1"]
     else:
-        head = measure_workload(ctx, args, args.workload, args.batch, args.steps, args.warmup,
-                                want_e2e=True, want_cpu=True)
+        head = with_decoder_grouping(measure_workload(ctx, args, args.workload, args.batch, args.steps,
+                                                      args.warmup, want_e2e=True, want_cpu=True),
+                                     args.workload, args.batch)
         runs = None
     clk_all = clocks.stop()
     if rank == 0:
@@ -892,6 +938,7 @@ def run_ours(args):
             "roofline_pct": head["roofline_pct"], "roofline": head["roofline"], "hbm": head["hbm"],
             "per_code": head["per_code"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
             "gpu_launches": head["gpu_launches"],
+            "decoder_grouping": head.get("decoder_grouping"),
             "int_peak_probe": ctx["probe"],
             "clocks": clk_all,
         }
@@ -1082,13 +1129,17 @@ def main():
                     help="all (default): every config, the Llama-3-8B layer set at batch 1 as the headline")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ungrouped", action="store_true",
-                    help="one exl3_gemm_small call per GEMV (no grouped q/k/v and gate/up calls)")
+    ap.add_argument("--grouping", choices=["class", "decoder", "none"], default="class",
+                    help="class: every GEMV of a step sharing K and the code in one grouped call; decoder: "
+                         "q/k/v and gate/up grouped; none: one call per GEMV")
+    ap.add_argument("--ungrouped", action="store_true", help="same as --grouping none")
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto",
                     help="kernel family of the fused layer (exl3_set_path)")
     ap.add_argument("--prefill", choices=["auto", "fused", "decode_once"], default="auto",
                     help="prefill strategy above 32 batch rows (exl3_set_prefill)")
     args = ap.parse_args()
+    if args.ungrouped:
+        args.grouping = "none"
     if args.warmup < 3:
         args.warmup = 3
     if args.workload == "encode":

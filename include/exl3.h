@@ -321,8 +321,8 @@ exl3_status exl3_gemm_int8act(const uint32_t *codes, int K, int codebook, int m,
  */
 int exl3_gemm_launches(int m, int n, int M);
 
-/** Most layers in one exl3_gemm_grouped call. */
-#define EXL3_MAX_GROUP 4
+/** Most layers in one grouped call (exl3_gemm_grouped and its variants). */
+#define EXL3_MAX_GROUP 64
 
 /** One layer of a grouped call (the arguments of exl3_gemm_small that differ
  *  between layers; formats as above). */
@@ -352,7 +352,10 @@ size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
  * and the batch M (1..EXL3_MAX_BATCH): the results equal `count` calls of
  * exl3_gemm_small, in fewer kernel launches.  The pages have no counterpart;
  * it serves decoders that apply several projections to the same step (q, k
- * and v; gate and up).  `layers` is a host array read during the call.  No
+ * and v; gate and up), and any set of independent layers of one K and code
+ * (the experts of a mixture-of-experts layer, or the layers of several
+ * sequences' steps), whose kernel chain it runs once for all of them.
+ * `layers` is a host array read during the call.  No
  * layer may read another layer's output (x of one aliasing y of another) in the
  * same call.  On the warp-shuffle kernel the layers share one chain per batch
  * chunk (x pairs of every layer, one decode+GEMV kernel over the tiles of

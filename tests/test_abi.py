@@ -145,7 +145,7 @@ def test_group_workspace_bytes(lib):
         assert lib.exl3_group_workspace_bytes(_group(shapes), 3, M) == fixed + scratch
     assert lib.exl3_group_workspace_bytes(_group([(100, 128)]), 1, 1) == 0
     assert lib.exl3_group_workspace_bytes(_group(shapes), 0, 1) == 0
-    assert lib.exl3_group_workspace_bytes(_group(shapes), 5, 1) == 0
+    assert lib.exl3_group_workspace_bytes(_group(shapes), B.MAX_GROUP + 1, 1) == 0
 
 
 def test_grouped_validation(lib):
@@ -156,7 +156,7 @@ def test_grouped_validation(lib):
         return lib.exl3_gemm_grouped(arr, count, K, cb, M, ws, wsb, None)
 
     assert call(arr=None) == 1
-    assert call(count=0) == 5 and call(count=5) == 5
+    assert call(count=0) == 5 and call(count=B.MAX_GROUP + 1) == 5
     assert call(K=0) == 3 and call(cb=4) == 4 and call(M=33) == 5
     assert call(arr=_group([(256, 256), (130, 384)])) == 2
     assert call(arr=_group([(256, 256)], codes=None), count=1) == 1
@@ -222,7 +222,7 @@ def test_whole_grouped_workspace_and_validation(lib):
     assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group([(384, 1024)]), 1, 1) == 0
     assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 3, 33) == 0
     assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 0, 1) == 0
-    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), 5, 1) == 0
+    assert lib.exl3_gemm_whole_grouped_workspace_bytes(_group(shapes), B.MAX_GROUP + 1, 1) == 0
     assert lib.exl3_gemm_whole_grouped_workspace_bytes(None, 1, 1) == 0
     g = _group([(256, 512), (1024, 512)])
 
@@ -230,7 +230,7 @@ def test_whole_grouped_workspace_and_validation(lib):
         return lib.exl3_gemm_whole_grouped(arr, count, K, cb, M, ws, wsb, None)
 
     assert call(arr=None) == 1
-    assert call(count=0) == 5 and call(count=5) == 5  # as exl3_gemm_grouped
+    assert call(count=0) == 5 and call(count=B.MAX_GROUP + 1) == 5  # as exl3_gemm_grouped
     assert call(M=0) == 5 and call(M=33) == 5
     assert call(arr=_group([(256, 512), (384, 512)])) == 2
     assert call(K=9) == 3 and call(cb=4) == 4
@@ -289,7 +289,7 @@ def test_int8_group_workspace_and_validation(lib):
     assert B.exl3_group_i8_workspace_bytes(shapes, M) == want
     assert B.exl3_group_i8_workspace_bytes([(100, 256)], 1) == 0
     assert B.exl3_group_i8_workspace_bytes(shapes, 33) == 0
-    assert B.exl3_group_i8_workspace_bytes(shapes * 3, 1) == 0  # more than four layers
+    assert B.exl3_group_i8_workspace_bytes(shapes * 33, 1) == 0  # more than EXL3_MAX_GROUP layers
     assert lib.exl3_gemm_int8act_grouped(None, 1, 2, 1, 1, A, 1 << 30, None) == 1
 
 

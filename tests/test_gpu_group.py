@@ -113,3 +113,25 @@ def test_group_object_matches_oracle():
     grp()
     torch.cuda.synchronize()
     _check(layers, 2, 0, 1)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_grouped_many_layers(M):
+    """A full group of EXL3_MAX_GROUP layers of mixed shapes (the layers are
+    found by binary search over their first units), each checked against a
+    separate call; a sample against the oracle."""
+    rng = np.random.default_rng(90 + M)
+    dims = [128, 256, 384, 640]
+    shapes = [(int(rng.choice(dims)), int(rng.choice(dims))) for _ in range(B.MAX_GROUP)]
+    layers = _layers(shapes, 2, 1, M, config=90 + M)
+    B.exl3_gemm_grouped([d for _, d in layers], 2, 1)
+    torch.cuda.synchronize()
+    for i, (inp, d) in enumerate(layers):
+        m, n = d["m"], d["n"]
+        single = B.exl3_gemm_small(d["codes"], 2, 1, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+        torch.cuda.synchronize()
+        diff = (single.float() - d["y"].float()).abs().max()
+        assert float(diff) <= 2.0 ** -9 * float(single.float().abs().max()) + 1e-6, f"layer {i} {m}x{n}"
+    _check([layers[0], layers[len(layers) // 2], layers[-1]], 2, 1, M)
+    with pytest.raises((ValueError, B.Exl3Error)):
+        B.exl3_gemm_grouped([d for _, d in layers] + [layers[0][1]], 2, 1)

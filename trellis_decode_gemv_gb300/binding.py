@@ -44,7 +44,7 @@ def library_path() -> str:
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
-MAX_GROUP = 4
+MAX_GROUP = 64
 
 
 class Exl3Layer(ctypes.Structure):

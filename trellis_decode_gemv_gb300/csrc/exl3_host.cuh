@@ -362,4 +362,10 @@ exl3_status launch_tc_k7(const LayerArgs& a, const __half* bimg, const float* bs
 exl3_status launch_tc_k8(const LayerArgs& a, const __half* bimg, const float* bsum, int M, int grid,
                           cudaStream_t stream);
 
+// Kernel parameter blocks of a grouped call stay within the 32764 bytes a
+// launch may pass.
+static_assert(sizeof(GroupArgs) <= 32764 && sizeof(MvParams) <= 32764 && sizeof(XdupGroup) <= 32764 &&
+                  sizeof(EpiGroup) <= 32764,
+              "kernel parameters");
+
 }  // namespace exl3

@@ -67,7 +67,13 @@ __device__ __forceinline__ void i8_body(const I8Args& g) {
   while (u < u_hi) {
     // the layer of sub-unit u, then its tile row and first tile column
     int li = 0;
-    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    {
+      int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
+      while (li < hi) {
+        const int mid = (li + hi + 1) >> 1;
+        if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
+      }
+    }
     const I8Layer& a = g.l[li];
     const int nt = a.n / 16;
     const int lu = u - a.u_begin;

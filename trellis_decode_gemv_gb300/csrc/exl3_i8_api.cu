@@ -57,7 +57,13 @@ __global__ void __launch_bounds__(kPrepThreads) i8_prep_kernel(const PrepGroup g
   const long long job = static_cast<long long>(blockIdx.x) * (kPrepThreads / 32) + (threadIdx.x >> 5);
   if (job >= g.jobs) return;
   int li = 0;
-  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  {
+    int hi = g.count - 1;  // the last layer whose first job is <= job
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (job >= g.e[mid].job_begin) li = mid; else hi = mid - 1;
+    }
+  }
   const PrepEntry& e = g.e[li];
   const int n = e.n;
   const int nkb = n / kRowBlock;

@@ -20,9 +20,8 @@
 //     binary16 and zeroes zacc for the next call.
 //
 // Work split: a sub-unit is up to S (16, 8 or 4) consecutive tiles of one tile
-// row; one CTA per SM.  Each warp starts on its own sub-unit and then takes
-// the next free one from a device-wide counter, so the warps of all SMs
-// finish together whatever the scheduler's priorities.  In a sub-unit, lane 8*jt + p handles tiles
+// row; one CTA per SM; warp w of CTA b takes the sub-units b * warps + w +
+// i * (grid * warps).  In a sub-unit, lane 8*jt + p handles tiles
 // J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each: 32 consecutive
 // trellis steps from a word-aligned window per tile (code words loaded two
 // tiles ahead of their decode), with the x pairs of the tile's 16 columns read
@@ -318,7 +317,13 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   while (u < units) {
     // the layer of sub-unit u, then its tile row and first tile column
     int li = 0;
-    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    {
+      int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
+      while (li < hi) {
+        const int mid = (li + hi + 1) >> 1;
+        if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
+      }
+    }
     const GroupLayer& a = g.l[li];
     const int nt = a.n / 16;
     const int lu = u - a.u_begin;

@@ -54,19 +54,22 @@
 // one persistent CTA per SM.  The units of a range that share a layer and
 // block form a run, accumulated in one TMEM D.
 //
-// Warp roles (19 warps):
-//   0-7   decoders, two teams of four: warp w reaches TMEM lanes 32*(w%4) ..
-//         (thread = weight row of the block), team w/4 takes the chunks of
-//         its parity.  Per chunk: the row's code words of 8 tiles from the
-//         shared-memory ring, 16 generator outputs per tile (funnel shifts
-//         give two windows each; for every code but 1MAD the second window's
-//         generator output comes from the 32-bit funnel word by two
-//         multiply-adds, which moves work from the ALU to the FMA pipe), the
-//         code, two tcgen05.st of 32 columns, one arrival.
-//   9-14  issuers: operand B of their chunks, then the chunks' MMAs.
-//   15-18 epilogue: D of each run out of TMEM (then zeroed) into the row sums,
+// Warp roles (22 warps):
+//   0-11  decoders, three teams of four: warp w reaches TMEM lanes 32*(w%4) ..
+//         (thread = weight row of the block), team w/4 takes the chunks seq
+//         = w/4 (mod 3).  The team's lead lane loads each of its chunks' codes
+//         with one 2-D tensor copy (the 8 tile-row strips of the chunk, the
+//         codes viewed as (m/16) rows of (n/16)*8K words) into the shared-
+//         memory ring.  Per chunk a thread: the row's code words of 8 tiles,
+//         16 generator outputs per tile (funnel shifts give two windows each;
+//         for every code but 1MAD the second window's generator output comes
+//         from the 32-bit funnel word by two multiply-adds, which moves work
+//         from the ALU to the FMA pipe), the code, two tcgen05.st of 32
+//         columns, one arrival.
+//   12-17 issuers: operand B of their chunks, then the chunks' MMAs.
+//   18-21 epilogue: D of each run out of TMEM (then zeroed) into the row sums,
 //         the block ticket and, for the completing CTA, the output transform.
-//         Warp 15 allocates TMEM.
+//         Warp 18 allocates TMEM.
 // mbarriers: ring full/empty, A full/empty (6 TMEM slots), B full (bulk
 // copies), D full/empty (2 accumulators).  Every parity wait is on a barrier
 // whose previous phase the waiting thread itself has seen complete, so no
@@ -214,7 +217,13 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 // Layer, 128-row block and chunk of unit u.
 __device__ __forceinline__ void locate(const MvParams& p, int u, int& li, int& rb, int& kc) {
   li = 0;
-  while (li + 1 < p.count && u >= p.l[li + 1].u_begin) ++li;
+  {
+    int hi = p.count - 1;  // the last layer whose first unit is <= u
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (u >= p.l[mid].u_begin) li = mid; else hi = mid - 1;
+    }
+  }
   const int lu = u - p.l[li].u_begin;
   rb = lu / p.l[li].nkb;
   kc = lu - rb * p.l[li].nkb;

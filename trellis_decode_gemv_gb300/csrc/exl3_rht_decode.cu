@@ -219,7 +219,13 @@ __global__ void __launch_bounds__(kSmallThreads, 16) xdup_kernel(const XdupGroup
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   if (job >= g.jobs) return;
   int li = 0;
-  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  {
+    int hi = g.count - 1;  // the last layer whose first job is <= job
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (job >= g.e[mid].job_begin) li = mid; else hi = mid - 1;
+    }
+  }
   const XdupEntry& e = g.e[li];
   const int n = e.n;
   const int per_row = n / kRowBlock;
@@ -263,7 +269,13 @@ __global__ void __launch_bounds__(kSmallThreads, 16) epi_kernel(const EpiGroup g
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
   if (job >= g.jobs) return;
   int li = 0;
-  while (li + 1 < g.count && job >= g.e[li + 1].job_begin) ++li;
+  {
+    int hi = g.count - 1;  // the last layer whose first job is <= job
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (job >= g.e[mid].job_begin) li = mid; else hi = mid - 1;
+    }
+  }
   const EpiEntry& e = g.e[li];
   const int m = e.m;
   const int per_row = m / kRowBlock;
