@@ -67,12 +67,16 @@ OPS_PER_WEIGHT_INT8 = {synth.CB_1MAD: 3, synth.CB_MUL1: 4}
 # captures of those kernels (dram__bytes_read.sum +
 # dram__bytes_write.sum of the captured launches over their algorithmic bytes).
 TRAFFIC_RATIO = {
-    "shuffle": (29.445 / 29.38, "the ncu capture of layer_kernel on gate/up/down 14336x4096 K4 1MAD"),
+    # DRAM reads against the algorithmic bytes of one grouped launch over the 7
+    # Llama-3-8B projections (218 M weights): 54.87 / 54.94 MB at K2 3INST,
+    # 109.40 / 109.47 MB at K4 1MAD (x and the signs come from L2)
+    "shuffle": (54.870 / 54.940, "the ncu capture of layer_kernel on one grouped call over the 7 Llama-3-8B "
+                                 "projections, K2 3INST"),
     "tensor": (23.12 / 22.15, "the ncu capture of tc_layer_kernel on 14336x4096 K3 1MAD at batch 16"),
     "dense": (None, None),
     # DRAM reads 26.0 + 26.6 MB against 2 x 23.86 MB of algorithmic bytes; the
     # packed codes are most of both, so the ratio holds for tiles up to 128 rows
-    "mv": (None, None),
+    "mv": (22.830 / 22.655, "the ncu capture of mv_kernel on 4096x14336 K3 1MAD at batch 16"),
     "fused": ((26.0 + 26.6) / (2 * 23.86),
               "the ncu capture of the fused dense_kernel (128-row tiles) on 14336x4096 and 4096x14336 K3 1MAD "
               "at batch 48"),
@@ -216,7 +220,16 @@ def class_groups(gemvs, max_group: int):
     return out
 
 
+def step_groups(gemvs, max_group: int):
+    """Calls of one step when every GEMV of the step goes into exl3_gemm_multi
+    calls of at most max_group layers (mixed K and code)."""
+    idx = list(range(len(gemvs)))
+    return [idx[s:s + max_group] for s in range(0, len(idx), max_group)]
+
+
 GROUPING_CALLS = {
+    "step": "every GEMV of the step in exl3_gemm_multi calls (mixed K and code: one x-pair kernel, a layer "
+            "kernel per (K, code) class, one output kernel)",
     "class": "every GEMV of the step that shares K and the code in one grouped call",
     "decoder": "q/k/v and gate/up grouped per call (the projections a decoder applies to one step), "
                "the rest one call each",
@@ -279,7 +292,11 @@ class ClockSampler:
             if self.bus_id:
                 cmd[1:1] = ["-i", self.bus_id]
             self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            # nvidia-smi takes a moment to start: wait (at most 10 s) for its
+            # first samples, so that the first timed region is covered
+            t0 = time.time()
+            while len(self._rows()) < 2 and time.time() - t0 < 10.0 and self.proc.poll() is None:
+                time.sleep(0.05)
         except Exception:
             self.proc = None
 
@@ -483,7 +500,7 @@ def int_peak_probe(B, torch, dev, stream, sms, clocks_mhz):
                     "instructions, 5 launches per kind, CUDA events; ops/clk/SM at the stated clock")}
 
 
-def launches_of_group(B, path, M, shapes, sms, whole, int8):
+def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
     """Kernel launches of one call of the step (a single layer or a group)."""
     if whole:
         if len(shapes) == 1:
@@ -491,6 +508,13 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8):
         return kernels_per_group(path, M, shapes, sms) + 2
     if int8:
         return 2 + int8_chunks(M)
+    if kcs is not None and len(shapes) > 1:  # exl3_gemm_multi: one chain, a layer kernel per (K, code) class
+        classes = {}
+        for sh, kc in zip(shapes, kcs):
+            classes.setdefault(kc, []).append(sh)
+        if uses_shuffle(path, M):
+            return int8_chunks(M) * (2 + len(classes))
+        return sum(1 if M <= 2 else 1 + len(shs) for shs in classes.values())
     return kernels_per_group(path, M, shapes, sms)
 
 
@@ -546,7 +570,11 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     if M > 32:
         grouping = "none"
     shapes_kc = [(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls]
-    if grouping == "class":
+    if grouping == "step" and (whole or int8):
+        grouping = "class"
+    if grouping == "step":
+        groups = step_groups(shapes_kc, B.MAX_GROUP)
+    elif grouping == "class":
         groups = class_groups(shapes_kc, B.MAX_GROUP)
     else:
         groups = decoder_groups(shapes_kc, grouped=grouping == "decoder")
@@ -564,6 +592,8 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
                   else B.exl3_gemm_small)
             fn(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                c["scales"], c["x"], y=c["y"], workspace=ws)
+        elif grouping == "step":
+            B.exl3_gemm_multi([calls[i] for i in g], workspace=ws)
         else:
             c0 = calls[g[0]]
             gfn = (B.exl3_gemm_int8act_grouped if int8 else B.exl3_gemm_whole_grouped if whole
@@ -730,7 +760,8 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     # ---- e2e: host buffers, copies inside the timed region ---------------
     e2e = None
     if want_e2e:
-        e2e = measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps)
+        e2e = measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps,
+                          grouping)
 
     # ---- CPU oracle baseline (rank 0, N=1 only) --------------------------
     cpu = None
@@ -747,7 +778,9 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
                           f"({w / 1e6:.1f} M weights, {dt:.1f} s), oracle layer forward")}
 
     launches_step = sum(launches_of_group(B, args.path, M, [(calls[i]["m"], calls[i]["n"]) for i in g], sms,
-                                          whole, int8) for g in groups)
+                                          whole, int8,
+                                          [(calls[i]["K"], calls[i]["cb"]) for i in g] if grouping == "step"
+                                          else None) for g in groups)
     res = {
         "value": value, "unit": "weights/s", "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
         "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
@@ -773,7 +806,8 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     return res
 
 
-def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps):
+def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, weights_step, steps,
+                grouping="class"):
     """The same workload through the binding's public per-layer objects,
     eager, with the step's x copied in from pinned host memory and y copied
     back inside the timed region."""
@@ -798,6 +832,8 @@ def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, 
             layer_objs.append(lambda c=c: B.exl3_gemm_whole(
                 c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"], c["scales"], c["x"],
                 y=c["y"], workspace=ws))
+        elif grouping == "step" and len(g) > 1:  # the mixed-code layer object
+            layer_objs.append(B.Exl3LinearMulti([calls[i] for i in g]))
         elif len(g) == 1:
             c = calls[g[0]]
             lin = B.Exl3Linear(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
@@ -833,7 +869,8 @@ def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, 
     t_e2e = max_over_ranks(t_e2e, dev)
     return {"value": whole_job_rate(weights_step, world, e2e_steps, t_e2e), "unit": "weights/s",
             "steps": e2e_steps, "h2d_bytes_per_step": total_n * 2, "d2h_bytes_per_step": total_m * 2,
-            "path": ("binding layer objects (Exl3Linear / Exl3LinearGroup), eager calls; pinned host x -> "
+            "path": ("binding layer objects (Exl3Linear / Exl3LinearGroup / Exl3LinearMulti), eager calls; "
+                     "pinned host x -> "
                      "device, y -> pinned host, inside the timed region")}
 
 
@@ -900,7 +937,7 @@ def run_ours(args):
     def with_decoder_grouping(res, wl, M):
         # the same workload with only the decoder's own groups (q/k/v,
         # gate/up): every other GEMV of the step waits for its predecessor
-        if args.grouping != "class" or M > 32 or wl in ("encode",):
+        if args.grouping not in ("step", "class") or M > 32 or wl in ("encode",):
             return res
         d = measure_workload(ctx, args, wl, M, min(args.steps, 300), args.warmup, want_e2e=False,
                              want_cpu=False, grouping="decoder")
@@ -1129,9 +1166,10 @@ def main():
                     help="all (default): every config, the Llama-3-8B layer set at batch 1 as the headline")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--grouping", choices=["class", "decoder", "none"], default="class",
-                    help="class: every GEMV of a step sharing K and the code in one grouped call; decoder: "
-                         "q/k/v and gate/up grouped; none: one call per GEMV")
+    ap.add_argument("--grouping", choices=["step", "class", "decoder", "none"], default="step",
+                    help="step: every GEMV of a step in exl3_gemm_multi calls (mixed K and code); class: every "
+                         "GEMV of a step sharing K and the code in one grouped call; decoder: q/k/v and gate/up "
+                         "grouped; none: one call per GEMV")
     ap.add_argument("--ungrouped", action="store_true", help="same as --grouping none")
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto",
                     help="kernel family of the fused layer (exl3_set_path)")

@@ -367,6 +367,36 @@ size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
 exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,
                               void *workspace, size_t workspace_bytes, exl3_stream_t stream);
 
+/** One layer of a multi-code grouped call: a layer with its own K and code. */
+typedef struct {
+  exl3_layer layer;
+  int K;        /* 1..8 */
+  int codebook; /* EXL3_CB_* */
+} exl3_layer_kc;
+
+/**
+ * Bytes of scratch for exl3_gemm_multi: exl3_group_workspace_bytes of the
+ * same layers (the plain layers' shapes and M).  0 for an invalid group.
+ */
+size_t exl3_multi_workspace_bytes(const exl3_layer_kc *layers, int count, int M);
+
+/**
+ * `count` (1..EXL3_MAX_GROUP) independent layers of their own K and code at one
+ * batch M (1..EXL3_MAX_BATCH): the results equal `count` calls of
+ * exl3_gemm_small.  The pages have no counterpart; EXL3 models give each
+ * tensor its own bit width ("EXL3 field guide"), so a decoder step's layers
+ * differ in K.  On the warp-shuffle kernels (M <= 2 by default) the layers
+ * share one kernel chain per batch chunk: one x-pair kernel over every layer,
+ * one sub-unit kernel per (K, code) class over that class's layers (in order
+ * of first appearance, each a programmatic dependent of the one before), one
+ * output kernel over every layer.  On the decode-MMA kernel each class runs
+ * as exl3_gemm_grouped would run it.
+ * Validation and errors as exl3_gemm_grouped, K and the code checked per
+ * layer; workspace >= exl3_multi_workspace_bytes, same zero-fill contract.
+ */
+exl3_status exl3_gemm_multi(const exl3_layer_kc *layers, int count, int M, void *workspace,
+                            size_t workspace_bytes, exl3_stream_t stream);
+
 /**
  * Bytes of scratch for exl3_gemm_whole_grouped: exl3_group_workspace_bytes of
  * the same layers rounded up to 256 bytes (first, so the status word is at
@@ -486,9 +516,10 @@ exl3_status exl3_device_status(const void *status_word, exl3_stream_t stream);
  *     a larger layer is rejected with EXL3_ERR_SCRATCH before anything is
  *     launched.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.  `stream` must belong to the current device
- *     (EXL3_ERR_CUDA otherwise: the address is per device).
+ *     (cudaGetSymbolAddress) with that device current.  `stream` must belong
+ *     to the current device (EXL3_ERR_CUDA otherwise: the address is per
+ *     device).  The call is not supported inside a stream capture (there it
+ *     returns EXL3_ERR_CUDA).
  *   - Every call shares the one array and clears its counters and row sums
  *     with an asynchronous memset on `stream`.  Calls whose work can overlap on the
  *     GPU (other streams, other host threads) race: serialize them.

@@ -135,3 +135,41 @@ def test_grouped_many_layers(M):
     _check([layers[0], layers[len(layers) // 2], layers[-1]], 2, 1, M)
     with pytest.raises((ValueError, B.Exl3Error)):
         B.exl3_gemm_grouped([d for _, d in layers] + [layers[0][1]], 2, 1)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_multi_code_group(M):
+    """Layers of different K and code (every code, K = 1..8) in one
+    exl3_gemm_multi call: one chain with a layer kernel per (K, code) class
+    at M <= 2, the decode-MMA path per class above; each layer equals a
+    separate call, a sample equals the oracle."""
+    kcs = [(2, 0), (3, 1), (4, 0), (5, 0), (6, 0), (2, 1), (4, 1), (3, 0), (1, 0), (8, 1), (2, 2), (3, 3)]
+    shapes = [(256, 384), (384, 256), (128, 640), (256, 256), (128, 384), (384, 512), (256, 128), (512, 256),
+              (128, 256), (256, 256), (384, 128), (128, 512)]
+    layers = []
+    for i, ((m, n), (K, cb)) in enumerate(zip(shapes, kcs)):
+        inp = synth.layer_inputs(m, n, K, M, config=95 + M, index=i)
+        d = upload(inp)
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
+        layers.append((inp, d))
+    B.exl3_gemm_multi([d for _, d in layers])
+    torch.cuda.synchronize()
+    for i, (inp, d) in enumerate(layers):
+        m, n, K, cb = d["m"], d["n"], d["K"], d["cb"]
+        single = B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+        torch.cuda.synchronize()
+        diff = (single.float() - d["y"].float()).abs().max()
+        assert float(diff) <= 2.0 ** -9 * float(single.float().abs().max()) + 1e-6, f"layer {i} K{K} cb{cb}"
+        if i % 4 == 0:
+            ref = O.layer_forward(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"], inp["x"])
+            assert_layer_close(d["y"], ref, f"layer {i} K{K} cb{cb}")
+    # the marshalled-once object: same outputs, written into the bound y
+    first = [d["y"].clone() for _, d in layers]
+    for _, d in layers:
+        d["y"].fill_(float("nan"))
+    obj = B.Exl3LinearMulti([d for _, d in layers])
+    obj()
+    torch.cuda.synchronize()
+    for (_, d), y0 in zip(layers, first):
+        diff = (y0.float() - d["y"].float()).abs().max()
+        assert float(diff) <= 2.0 ** -9 * float(y0.float().abs().max()) + 1e-6

@@ -53,6 +53,11 @@ class Exl3Layer(ctypes.Structure):
                 ("scales", _P), ("x", _P), ("y", _P)]
 
 
+class Exl3LayerKC(ctypes.Structure):
+    """exl3_layer_kc of the header: a layer with its own K and code."""
+    _fields_ = [("layer", Exl3Layer), ("K", _I), ("codebook", _I)]
+
+
 _SIGNATURES = {
     "exl3_rht_in": ([_P, _P, _P, _I, _I, _P], _I),
     "exl3_rht_out": ([_P, _P, _P, _I, _I, _P], _I),
@@ -63,6 +68,8 @@ _SIGNATURES = {
     "exl3_gemv_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "exl3_group_workspace_bytes": ([ctypes.POINTER(Exl3Layer), _I, _I], _SZ),
     "exl3_gemm_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "exl3_multi_workspace_bytes": ([ctypes.POINTER(Exl3LayerKC), _I, _I], _SZ),
+    "exl3_gemm_multi": ([ctypes.POINTER(Exl3LayerKC), _I, _I, _P, _SZ, _P], _I),
     "exl3_gemm_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_launches": ([_I, _I, _I], _I),
     "exl3_probe_int": ([_I, _P, _I, _I, _P], _I),
@@ -304,6 +311,36 @@ def _layer_array(layers, dev, M):
     return arr
 
 
+def exl3_gemm_multi(layers, workspace=None):
+    """Independent layers of their own K and code at one batch: each dict as
+    for exl3_gemm_grouped plus K and cb.  Same results as one exl3_gemm_small
+    per layer; at batch 1 and 2 the layers of the multi-code kernel's (K, code)
+    pairs share one kernel chain."""
+    lib = load_library()
+    dev = layers[0]["codes"].device
+    M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+    plain = _layer_array(layers, dev, M)
+    arr = (Exl3LayerKC * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i].layer = plain[i]
+        arr[i].K = int(L["K"])
+        arr[i].codebook = int(L["cb"])
+    if workspace is None:
+        workspace = alloc_group_workspace([(L["m"], L["n"]) for L in layers], M, dev)
+    _check(lib.exl3_gemm_multi(arr, len(layers), M, _ptr(workspace, "workspace", (torch.uint8,), dev),
+                               workspace.numel(), _stream(dev)))
+    return [L["y"] for L in layers]
+
+
+def exl3_multi_workspace_bytes(shapes, M: int = 1) -> int:
+    """Workspace bytes of a multi-code grouped call over layers of (m, n)."""
+    arr = (Exl3LayerKC * len(shapes))()
+    for i, (m, n) in enumerate(shapes):
+        arr[i].layer.m, arr[i].layer.n = m, n
+        arr[i].K, arr[i].codebook = 2, 0
+    return int(load_library().exl3_multi_workspace_bytes(arr, len(shapes), M))
+
+
 def exl3_group_workspace_bytes(shapes, M: int = 1) -> int:
     """Workspace bytes of a grouped call over layers of the given (m, n)."""
     arr = (Exl3Layer * len(shapes))()
@@ -420,6 +457,33 @@ class Exl3LinearGroup:
 
     def __call__(self):
         _check(self._fn(self._arr, self._count, self.K, self.codebook, self.M, *self._ws,
+                        torch.cuda.current_stream(self.device).cuda_stream))
+        return [L["y"] for L in self._keep]
+
+
+class Exl3LinearMulti:
+    """Independent layers of their own K and code (one batch) marshalled once
+    for exl3_gemm_multi: each layer dict as for Exl3LinearGroup plus K and cb;
+    x and y stay bound to those tensors."""
+
+    def __init__(self, layers):
+        lib = load_library()
+        self.device = layers[0]["codes"].device
+        self.M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+        self._keep = [dict(L) for L in layers]
+        plain = _layer_array(layers, self.device, self.M)
+        self._arr = (Exl3LayerKC * len(layers))()
+        for i, L in enumerate(layers):
+            self._arr[i].layer = plain[i]
+            self._arr[i].K = int(L["K"])
+            self._arr[i].codebook = int(L["cb"])
+        self.workspace = alloc_group_workspace([(L["m"], L["n"]) for L in layers], self.M, self.device)
+        self._ws = (self.workspace.data_ptr(), self.workspace.numel())
+        self._count = len(layers)
+        self._fn = lib.exl3_gemm_multi
+
+    def __call__(self):
+        _check(self._fn(self._arr, self._count, self.M, *self._ws,
                         torch.cuda.current_stream(self.device).cuda_stream))
         return [L["y"] for L in self._keep]
 

@@ -430,13 +430,10 @@ extern "C" size_t exl3_group_workspace_bytes(const exl3_layer* layers, int count
   return group_layout(layers, count, M).total;
 }
 
-extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
-                                         void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
-  if (layers == nullptr) return EXL3_ERR_NULL;
-  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
-  exl3_status st = check_k_cb(K, codebook);
-  if (st != EXL3_OK) return st;
-  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+namespace {
+
+exl3_status check_group_layers(const exl3_layer* layers, int count) {
+  exl3_status st;
   for (int i = 0; i < count; ++i) {
     const exl3_layer& L = layers[i];
     if ((st = check_shape(L.m, L.n)) != EXL3_OK) return st;
@@ -445,88 +442,184 @@ extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, in
         (L.s_in && !aligned16(L.s_in)) || (L.s_out && !aligned16(L.s_out)))
       return EXL3_ERR_ALIGN;
   }
-  const size_t need = exl3_group_workspace_bytes(layers, count, M);
-  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  return EXL3_OK;
+}
 
-  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace);
+// The layers idx[0 .. count) of `layers`, each of its own K (ks[j]) and code
+// (codes[j]), with the per-layer workspace regions of gl.  Warp-shuffle path:
+// per batch chunk one kernel chain -- the x pairs of every layer, then one
+// sub-unit kernel per (K, code) class over the tiles of that class's layers
+// (the classes in order of first appearance, each a programmatic dependent of
+// the one before), then the output transform of every layer.  Decode-MMA
+// path: one call of it per class.
+exl3_status group_chain(const exl3_layer* layers, const int* idx, int count, const int* ks, const int* codes, int M,
+                        const GroupLayout& gl, char* ws, cudaStream_t cs) {
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  const GroupLayout gl = group_layout(layers, count, M);
-  if (!use_shuffle(M)) {
-    MvParams p{};
-    p.count = count;
-    p.M = M;
-    p.status = status;
-    p.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
-    for (int i = 0; i < count; ++i) {
-      const exl3_layer& L = layers[i];
-      MvLayer& d = p.l[i];
-      d.codes = L.codes;
-      d.x = reinterpret_cast<const __half*>(L.x);
-      d.s_in = reinterpret_cast<const __half*>(L.s_in);
-      d.bimg = reinterpret_cast<const __half*>(ws + gl.scratch[i]);
-      d.bsum = reinterpret_cast<const float*>(ws + gl.scratch[i] + align256(mv_bimg_bytes(L.n, M)));
-      d.scales = reinterpret_cast<const __half*>(L.scales);
-      d.s_out = reinterpret_cast<const __half*>(L.s_out);
-      d.y = reinterpret_cast<__half*>(L.y);
-      d.zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
-      d.cnt = reinterpret_cast<uint32_t*>(ws + gl.cnt[i]);
-      d.m = L.m;
-      d.n = L.n;
+  exl3_status st;
+  // the classes: cls[j] = index of layer j's (K, code) among the distinct pairs
+  int cls[kMaxGroup], ncls = 0, cls_k[kMaxGroup], cls_cb[kMaxGroup];
+  for (int j = 0; j < count; ++j) {
+    int c = 0;
+    while (c < ncls && !(cls_k[c] == ks[j] && cls_cb[c] == codes[j])) ++c;
+    if (c == ncls) {
+      cls_k[c] = ks[j];
+      cls_cb[c] = codes[j];
+      ++ncls;
     }
-    return run_mv(p, K, codebook, cs);
+    cls[j] = c;
+  }
+  if (!use_shuffle(M)) {
+    for (int c = 0; c < ncls; ++c) {
+      const int K = cls_k[c], codebook = cls_cb[c];
+      MvParams p{};
+      p.M = M;
+      p.status = status;
+      p.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+      for (int j = 0; j < count; ++j) {
+        if (cls[j] != c) continue;
+        const int i = idx[j];
+        const exl3_layer& L = layers[i];
+        MvLayer& d = p.l[p.count++];
+        d.codes = L.codes;
+        d.x = reinterpret_cast<const __half*>(L.x);
+        d.s_in = reinterpret_cast<const __half*>(L.s_in);
+        d.bimg = reinterpret_cast<const __half*>(ws + gl.scratch[i]);
+        d.bsum = reinterpret_cast<const float*>(ws + gl.scratch[i] + align256(mv_bimg_bytes(L.n, M)));
+        d.scales = reinterpret_cast<const __half*>(L.scales);
+        d.s_out = reinterpret_cast<const __half*>(L.s_out);
+        d.y = reinterpret_cast<__half*>(L.y);
+        d.zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
+        d.cnt = reinterpret_cast<uint32_t*>(ws + gl.cnt[i]);
+        d.m = L.m;
+        d.n = L.n;
+      }
+      if ((st = run_mv(p, K, codebook, cs)) != EXL3_OK) return st;
+    }
+    return EXL3_OK;
   }
 
-  // Warp-shuffle path: per batch chunk, the x pairs of every layer, one
-  // sub-unit kernel over the tiles of every layer, the output transform of
-  // every layer.
+  // Warp-shuffle path.
   const int sms = device_sm_count();
-  float* zacc[kMaxGroup];
-  uint32_t* xd[kMaxGroup];
-  long long tiles = 0;
-  for (int i = 0; i < count; ++i) {
-    zacc[i] = reinterpret_cast<float*>(ws + gl.zacc[i]);
-    xd[i] = reinterpret_cast<uint32_t*>(ws + gl.scratch[i]);
-    tiles += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
-  }
+  long long tiles[kMaxGroup] = {};  // per class
+  for (int j = 0; j < count; ++j)
+    tiles[cls[j]] += static_cast<long long>(layers[idx[j]].m / 16) * (layers[idx[j]].n / 16);
   for (int done = 0; done < M;) {
     const int mb = batch_chunk(M - done);
     XdupGroup xg{};
     EpiGroup eg{};
-    GroupArgs g{};
-    xg.count = eg.count = g.count = count;
+    xg.count = eg.count = count;
     xg.rows = eg.rows = mb;
-    g.sub = choose_sub(tiles, mb, sms);
-    int units = 0;
-    for (int i = 0; i < count; ++i) {
+    for (int j = 0; j < count; ++j) {
+      const int i = idx[j];
       const exl3_layer& L = layers[i];
-      xg.e[i].x = reinterpret_cast<const __half*>(L.x) + static_cast<size_t>(done) * L.n;
-      xg.e[i].s_in = reinterpret_cast<const __half*>(L.s_in);
-      xg.e[i].xd = xd[i];
-      xg.e[i].n = L.n;
-      g.l[i].codes = L.codes;
-      g.l[i].xdup = xd[i];
-      g.l[i].zacc = zacc[i];
-      g.l[i].m = L.m;
-      g.l[i].n = L.n;
-      g.l[i].u_begin = units;
-      g.l[i].per_row = (L.n / 16 + g.sub - 1) / g.sub;
-      units += (L.m / 16) * g.l[i].per_row;
-      eg.e[i].zacc = zacc[i];
-      eg.e[i].scales = reinterpret_cast<const __half*>(L.scales);
-      eg.e[i].s_out = reinterpret_cast<const __half*>(L.s_out);
-      eg.e[i].y = reinterpret_cast<__half*>(L.y) + static_cast<size_t>(done) * L.m;
-      eg.e[i].m = L.m;
+      float* zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
+      uint32_t* xd = reinterpret_cast<uint32_t*>(ws + gl.scratch[i]);
+      xg.e[j].x = reinterpret_cast<const __half*>(L.x) + static_cast<size_t>(done) * L.n;
+      xg.e[j].s_in = reinterpret_cast<const __half*>(L.s_in);
+      xg.e[j].xd = xd;
+      xg.e[j].n = L.n;
+      xg.e[j].factor = code_x_factor(codes[j]);
+      eg.e[j].zacc = zacc;
+      eg.e[j].scales = reinterpret_cast<const __half*>(L.scales);
+      eg.e[j].s_out = reinterpret_cast<const __half*>(L.s_out);
+      eg.e[j].y = reinterpret_cast<__half*>(L.y) + static_cast<size_t>(done) * L.m;
+      eg.e[j].m = L.m;
     }
-    g.units = units;
-    g.ctas = units < sms ? units : sms;
-    if ((st = launch_xdup_group(xg, codebook, cs)) != EXL3_OK) return st;
-    if ((st = launch_group(g, K, codebook, mb, cs)) != EXL3_OK) return st;
+    if ((st = launch_xdup_group(xg, -1, cs)) != EXL3_OK) return st;
+    for (int c = 0; c < ncls; ++c) {
+      GroupArgs g{};
+      const int sub = choose_sub(tiles[c], mb, sms);
+      g.sub = sub;
+      int units = 0;
+      for (int j = 0; j < count; ++j) {
+        if (cls[j] != c) continue;
+        const int i = idx[j];
+        const exl3_layer& L = layers[i];
+        GroupLayer& d = g.l[g.count++];
+        d.codes = L.codes;
+        d.xdup = reinterpret_cast<uint32_t*>(ws + gl.scratch[i]);
+        d.zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
+        d.m = L.m;
+        d.n = L.n;
+        d.u_begin = units;
+        d.per_row = (L.n / 16 + sub - 1) / sub;
+        units += (L.m / 16) * d.per_row;
+      }
+      g.units = units;
+      g.ctas = units < sms ? units : sms;
+      if ((st = launch_group(g, cls_k[c], cls_cb[c], mb, cs)) != EXL3_OK) return st;
+    }
     if ((st = launch_epi_group(eg, cs)) != EXL3_OK) return st;
     done += mb;
   }
   return EXL3_OK;
+}
+
+}  // namespace
+
+extern "C" exl3_status exl3_gemm_grouped(const exl3_layer* layers, int count, int K, int codebook, int M,
+                                         void* workspace, size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
+  exl3_status st = check_k_cb(K, codebook);
+  if (st != EXL3_OK) return st;
+  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+  if ((st = check_group_layers(layers, count)) != EXL3_OK) return st;
+  const size_t need = exl3_group_workspace_bytes(layers, count, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+
+  const GroupLayout gl = group_layout(layers, count, M);
+  int idx[kMaxGroup], ks[kMaxGroup], codes[kMaxGroup];
+  for (int i = 0; i < count; ++i) {
+    idx[i] = i;
+    ks[i] = K;
+    codes[i] = codebook;
+  }
+  return group_chain(layers, idx, count, ks, codes, M, gl, static_cast<char*>(workspace),
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// The plain layers of a multi-code group (their shapes set the workspace).
+void plain_layers(const exl3_layer_kc* layers, int count, exl3_layer* out) {
+  for (int i = 0; i < count; ++i) out[i] = layers[i].layer;
+}
+
+}  // namespace
+
+extern "C" size_t exl3_multi_workspace_bytes(const exl3_layer_kc* layers, int count, int M) {
+  if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP) return 0;
+  exl3_layer plain[kMaxGroup];
+  plain_layers(layers, count, plain);
+  return exl3_group_workspace_bytes(plain, count, M);
+}
+
+extern "C" exl3_status exl3_gemm_multi(const exl3_layer_kc* layers, int count, int M, void* workspace,
+                                       size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
+  if (M < 1 || M > EXL3_MAX_BATCH) return EXL3_ERR_BATCH;
+  exl3_status st;
+  for (int i = 0; i < count; ++i)
+    if ((st = check_k_cb(layers[i].K, layers[i].codebook)) != EXL3_OK) return st;
+  exl3_layer plain[kMaxGroup];
+  plain_layers(layers, count, plain);
+  if ((st = check_group_layers(plain, count)) != EXL3_OK) return st;
+  const size_t need = exl3_group_workspace_bytes(plain, count, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+
+  const GroupLayout gl = group_layout(plain, count, M);
+  int idx[kMaxGroup], ks[kMaxGroup], codes[kMaxGroup];
+  for (int i = 0; i < count; ++i) {
+    idx[i] = i;
+    ks[i] = layers[i].K;
+    codes[i] = layers[i].codebook;
+  }
+  return group_chain(plain, idx, count, ks, codes, M, gl, static_cast<char*>(workspace),
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exl3_gemm_workspace_bytes(int m, int n, int M) {

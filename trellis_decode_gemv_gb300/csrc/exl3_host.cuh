@@ -103,13 +103,13 @@ struct XdupEntry {
   const __half* s_in;   // [n] or nullptr
   uint32_t* xd;         // [rows][n]
   int n;
+  float factor;         // the layer's code's x factor
   long long job_begin;
 };
 struct XdupGroup {
   XdupEntry e[kMaxGroup];
   int count;
   int rows;
-  float factor;         // the code's x factor
   long long jobs;
 };
 struct EpiEntry {
@@ -240,7 +240,12 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 // bsum[b * (n/128) + kb] of the binary16 values.
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream);
+// x pairs of a group; codebook >= 0 sets every entry's x factor from it, -1
+// keeps the factors the entries carry (layers of different codes).
 exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream);
+// The factor the x pairs carry for a code (the byte-sum codes' scale).
+float code_x_factor(int codebook);
+
 exl3_status launch_epi_group(EpiGroup g, cudaStream_t stream);
 // The sub-unit kernel over a group (a.sub > 0 tiles per sub-unit, a.ctas CTAs).
 exl3_status launch_group_k1(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);

@@ -290,140 +290,144 @@ __device__ __forceinline__ void pair_generate(const uint32_t (&w)[RowPair<K>::kP
   }
 }
 
-// One sub-unit kernel pass: sub-units of 4*TPL tiles of one tile row, lane
-// 8*jt + p taking tiles J0 + jt + 4t (t < TPL) and rows 2p, 2p+1 of each.
-// Work: warp w of CTA b takes sub-units b * warps + w + i * (grid * warps).
+// Sub-units are 4*TPL tiles of one tile row, lane 8*jt + p taking tiles
+// J0 + jt + 4t (t < TPL) and rows 2p, 2p+1 of each.
+
+// The layer of sub-unit u of a group: the last whose first sub-unit is <= u.
+__device__ __forceinline__ int group_layer_of(const GroupArgs& g, int u) {
+  int li = 0, hi = g.count - 1;
+  while (li < hi) {
+    const int mid = (li + hi + 1) >> 1;
+    if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
+  }
+  return li;
+}
+
+// Sub-unit lu of layer a (lane 8*jt + p): decode + MAC of its 4*TPL tiles,
+// warp-shuffle reduction, fp32 atomic adds of its 16 row sums.  The first
+// call of a warp waits for the preceding grids (x pairs, zeroed row sums)
+// after requesting its code words.
+template <int K, int CB, int MB, int TPL>
+__device__ __forceinline__ void layer_unit(const GroupLayer& a, int lu, int lane, bool& waited) {
+  const int jt = lane >> 3;
+  const int p = lane & 7;
+  constexpr int kTw = RowPair<K>::kTileWords;
+  // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
+  const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
+  const int nt = a.n / 16;
+  const int I = lu / a.per_row;
+  const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
+  const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
+
+  // Code words two tiles ahead of their decode.
+  uint32_t w[2][RowPair<K>::kPairWords];
+  if (J0 < nt) load_row_pair<K>(tp, p, w[0]);
+  if (TPL > 1 && J0 + 4 < nt) load_row_pair<K>(tp + 4 * kTw, p, w[1]);
+  // The x pairs and the zeroed row sums come from the preceding grids on
+  // the stream; the code words above do not.
+  if (!waited) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+  }
+
+  float acc[MB][2];
+#pragma unroll
+  for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+
+#pragma unroll
+  for (int t = 0; t < TPL; ++t) {
+    const int J = J0 + 4 * t;
+    if (J < nt) {  // all lanes but on a row's ragged last sub-unit
+      uint32_t gen[32];
+      pair_generate<K, CB>(w[t & 1], gen);
+      if (t + 2 < TPL && J + 8 < nt) load_row_pair<K>(tp + (4 * t + 8) * kTw, p, w[t & 1]);
+      const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
+      __half2 ha[MB], hb[MB];
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        ha[b] = __float2half2_rn(0.f);
+        hb[b] = __float2half2_rn(0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 xv[MB];
+#pragma unroll
+        for (int b = 0; b < MB; ++b) xv[b] = xrow[static_cast<size_t>(b) * (a.n / 4) + q];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * q + j;
+          if constexpr (!byte_sum_code<CB>()) {
+            const uint32_t pa = mask_xor_3inst(gen[c]);
+            const uint32_t pb = mask_xor_3inst(gen[16 + c]);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
+              ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
+              hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
+            }
+          } else {
+            const uint32_t ra = __dp4a(summed_bytes<CB>(gen[c]), 0x01010101u, 0x6400u);
+            const uint32_t rb2 = __dp4a(summed_bytes<CB>(gen[16 + c]), 0x01010101u, 0x6400u);
+            const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
+            const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) {
+              const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
+              ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < MB; ++b) {
+        if constexpr (!byte_sum_code<CB>()) {
+          acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
+          acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
+        } else {
+          acc[b][0] += __low2float(ha[b]);
+          acc[b][1] += __high2float(ha[b]);
+        }
+      }
+    }
+  }
+
+  // ---- warp-shuffle reduction over the 4 tile groups, accumulate into zacc --
+#pragma unroll
+  for (int b = 0; b < MB; ++b) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float v = acc[b][k];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+      acc[b][k] = v;
+    }
+  }
+  if (jt == 0) {
+#pragma unroll
+    for (int b = 0; b < MB; ++b) {
+      float* z = a.zacc + static_cast<size_t>(b) * a.m + I * 16 + 2 * p;
+      atomicAdd(z, acc[b][0]);
+      atomicAdd(z + 1, acc[b][1]);
+    }
+  }
+}
+
+// Warp w of CTA b takes the sub-units b * warps + w + i * (grid * warps).
 // (A device-wide atomic counter balanced the SMs better but cost more than
 // it saved: one L2 address taking an atomic from every warp per sub-unit.)
 template <int K, int CB, int MB, int TPL>
 __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   constexpr int kWarps = layer_warps<MB>();
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int jt = lane >> 3;
-  const int p = lane & 7;
-  constexpr int kTw = RowPair<K>::kTileWords;
-  const int units = g.units;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int stride = static_cast<int>(gridDim.x) * kWarps;
-  // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
-  const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
-
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   bool waited = false;
-  int u = static_cast<int>(blockIdx.x) * kWarps + warp;
-  while (u < units) {
-    // the layer of sub-unit u, then its tile row and first tile column
-    int li = 0;
-    {
-      int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
-      while (li < hi) {
-        const int mid = (li + hi + 1) >> 1;
-        if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
-      }
-    }
-    const GroupLayer& a = g.l[li];
-    const int nt = a.n / 16;
-    const int lu = u - a.u_begin;
-    const int I = lu / a.per_row;
-    const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
-    const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
-
-    // Code words two tiles ahead of their decode.
-    uint32_t w[2][RowPair<K>::kPairWords];
-    if (J0 < nt) load_row_pair<K>(tp, p, w[0]);
-    if (TPL > 1 && J0 + 4 < nt) load_row_pair<K>(tp + 4 * kTw, p, w[1]);
-    // The x pairs and the zeroed row sums come from the preceding grids on
-    // the stream; the code words above do not.
-    if (!waited) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      waited = true;
-    }
-
-    float acc[MB][2];
-#pragma unroll
-    for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
-
-#pragma unroll
-    for (int t = 0; t < TPL; ++t) {
-      const int J = J0 + 4 * t;
-      if (J < nt) {  // all lanes but on a row's ragged last sub-unit
-        uint32_t gen[32];
-        pair_generate<K, CB>(w[t & 1], gen);
-        if (t + 2 < TPL && J + 8 < nt) load_row_pair<K>(tp + (4 * t + 8) * kTw, p, w[t & 1]);
-        const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
-        __half2 ha[MB], hb[MB];
-#pragma unroll
-        for (int b = 0; b < MB; ++b) {
-          ha[b] = __float2half2_rn(0.f);
-          hb[b] = __float2half2_rn(0.f);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 xv[MB];
-#pragma unroll
-          for (int b = 0; b < MB; ++b) xv[b] = xrow[static_cast<size_t>(b) * (a.n / 4) + q];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = 4 * q + j;
-            if constexpr (!byte_sum_code<CB>()) {
-              const uint32_t pa = mask_xor_3inst(gen[c]);
-              const uint32_t pb = mask_xor_3inst(gen[16 + c]);
-#pragma unroll
-              for (int b = 0; b < MB; ++b) {
-                const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
-                const __half2 x2 = *reinterpret_cast<const __half2*>(&xw);
-                ha[b] = __hfma2(*reinterpret_cast<const __half2*>(&pa), x2, ha[b]);
-                hb[b] = __hfma2(*reinterpret_cast<const __half2*>(&pb), x2, hb[b]);
-              }
-            } else {
-              const uint32_t ra = __dp4a(summed_bytes<CB>(gen[c]), 0x01010101u, 0x6400u);
-              const uint32_t rb2 = __dp4a(summed_bytes<CB>(gen[16 + c]), 0x01010101u, 0x6400u);
-              const uint32_t pr = __byte_perm(ra, rb2, 0x5410);  // (1024 + S_a, 1024 + S_b)
-              const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&pr), k1534);
-#pragma unroll
-              for (int b = 0; b < MB; ++b) {
-                const uint32_t xw = j == 0 ? xv[b].x : j == 1 ? xv[b].y : j == 2 ? xv[b].z : xv[b].w;
-                ha[b] = __hfma2(v, *reinterpret_cast<const __half2*>(&xw), ha[b]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < MB; ++b) {
-          if constexpr (!byte_sum_code<CB>()) {
-            acc[b][0] += __low2float(ha[b]) + __high2float(ha[b]);
-            acc[b][1] += __low2float(hb[b]) + __high2float(hb[b]);
-          } else {
-            acc[b][0] += __low2float(ha[b]);
-            acc[b][1] += __high2float(ha[b]);
-          }
-        }
-      }
-    }
-
-    // ---- warp-shuffle reduction over the 4 tile groups, accumulate into zacc --
-#pragma unroll
-    for (int b = 0; b < MB; ++b) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        float v = acc[b][k];
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-        acc[b][k] = v;
-      }
-    }
-    if (jt == 0) {
-#pragma unroll
-      for (int b = 0; b < MB; ++b) {
-        float* z = a.zacc + static_cast<size_t>(b) * a.m + I * 16 + 2 * p;
-        atomicAdd(z, acc[b][0]);
-        atomicAdd(z + 1, acc[b][1]);
-      }
-    }
-    u += stride;
+  for (int u = static_cast<int>(blockIdx.x) * kWarps + warp; u < g.units; u += stride) {
+    const GroupLayer& a = g.l[group_layer_of(g, u)];
+    layer_unit<K, CB, MB, TPL>(a, u - a.u_begin, lane, waited);
   }
 }
 

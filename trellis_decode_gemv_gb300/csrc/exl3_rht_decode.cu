@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kSmallThreads, 16) xdup_kernel(const XdupGroup
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] *= kInvSqrt128;
   }
-  const float factor = g.factor;
+  const float factor = e.factor;
   uint4 o;
   o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0] * factor))) * 0x10001u;
   o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1] * factor))) * 0x10001u;
@@ -466,8 +466,13 @@ exl3_status launch_pdl_small(Kern kernel, const G& g, cudaStream_t stream) {
 
 }  // namespace
 
+float code_x_factor(int codebook) {
+  return codebook == kCb1Mad ? x_factor<kCb1Mad>() : codebook == kCbMul1 ? x_factor<kCbMul1>() : 1.0f;
+}
+
 exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream) {
-  g.factor = codebook == kCb1Mad ? x_factor<kCb1Mad>() : codebook == kCbMul1 ? x_factor<kCbMul1>() : 1.0f;
+  if (codebook >= 0)
+    for (int i = 0; i < g.count; ++i) g.e[i].factor = code_x_factor(codebook);
   g.jobs = 0;
   for (int i = 0; i < g.count; ++i) {
     g.e[i].job_begin = g.jobs;
