@@ -318,11 +318,20 @@ __device__ __forceinline__ void layer_unit(const GroupLayer& a, int lu, int lane
   const int I = lu / a.per_row;
   const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
   const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
+  // this lane's words: from word pK of each tile; the last row pair's words
+  // past the tile's end wrap to its start (p = 7, words K ..)
+  const uint32_t* lp = tp + p * K;
+  const uint32_t* lw = lp - (p == 7 ? kTw : 0);
+  constexpr int kPw = RowPair<K>::kPairWords;
+  auto load_pair = [&](int toff, uint32_t (&wd)[kPw]) {
+#pragma unroll
+    for (int i = 0; i < kPw; ++i) wd[i] = __ldg((i < K ? lp : lw) + toff + i);
+  };
 
   // Code words two tiles ahead of their decode.
-  uint32_t w[2][RowPair<K>::kPairWords];
-  if (J0 < nt) load_row_pair<K>(tp, p, w[0]);
-  if (TPL > 1 && J0 + 4 < nt) load_row_pair<K>(tp + 4 * kTw, p, w[1]);
+  uint32_t w[2][kPw];
+  if (J0 < nt) load_pair(0, w[0]);
+  if (TPL > 1 && J0 + 4 < nt) load_pair(4 * kTw, w[1]);
   // The x pairs and the zeroed row sums come from the preceding grids on
   // the stream; the code words above do not.
   if (!waited) {
@@ -340,7 +349,7 @@ __device__ __forceinline__ void layer_unit(const GroupLayer& a, int lu, int lane
     if (J < nt) {  // all lanes but on a row's ragged last sub-unit
       uint32_t gen[32];
       pair_generate<K, CB>(w[t & 1], gen);
-      if (t + 2 < TPL && J + 8 < nt) load_row_pair<K>(tp + (4 * t + 8) * kTw, p, w[t & 1]);
+      if (t + 2 < TPL && J + 8 < nt) load_pair((4 * t + 8) * kTw, w[t & 1]);
       const uint4* xrow = reinterpret_cast<const uint4*>(a.xdup + static_cast<size_t>(J) * 16);
       __half2 ha[MB], hb[MB];
 #pragma unroll
