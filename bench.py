@@ -239,13 +239,13 @@ GROUPING_CALLS = {
 
 def kernels_per_group(path: str, M: int, shapes, sms: int) -> int:
     """Kernel launches of one grouped call over layers of the given (m, n):
-    one decode-MMA launch over every layer (plus one operand-image kernel per
-    layer above batch 2); on the warp-shuffle path three per batch chunk (x
-    pairs, one sub-unit kernel over every layer, output transform)."""
+    one decode-MMA launch over every layer (after one operand-image launch for
+    every layer above batch 2); on the warp-shuffle path three per batch chunk
+    (x pairs, one sub-unit kernel over every layer, output transform)."""
     if len(shapes) == 1:
         return kernels_per_call(path, M, shapes[0][0], shapes[0][1], sms)
     if not uses_shuffle(path, M):
-        return 1 if M <= 2 else 1 + len(shapes)
+        return 1 if M <= 2 else 2  # one operand-image launch for every layer, one decode-MMA launch
     chunks, rem = 0, M
     for c in (8, 4, 2, 1):
         while rem >= c:
@@ -514,7 +514,7 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
             classes.setdefault(kc, []).append(sh)
         if uses_shuffle(path, M):
             return int8_chunks(M) * (2 + len(classes))
-        return sum(1 if M <= 2 else 1 + len(shs) for shs in classes.values())
+        return sum(1 if M <= 2 else 2 for shs in classes.values())
     return kernels_per_group(path, M, shapes, sms)
 
 

@@ -360,8 +360,8 @@ size_t exl3_group_workspace_bytes(const exl3_layer *layers, int count, int M);
  * same call.  On the warp-shuffle kernel the layers share one chain per batch
  * chunk (x pairs of every layer, one decode+GEMV kernel over the tiles of
  * every layer, one output kernel for every layer); on the decode-MMA kernel
- * one operand image per layer, then one layer kernel over the tiles of every
- * layer (at M <= 2, that one launch alone).  The workspace's per-layer
+ * one operand-image launch for every layer, then one layer kernel over the
+ * tiles of every layer (at M <= 2, that one launch alone).  The workspace's per-layer
  * scratch is sized for either.
  */
 exl3_status exl3_gemm_grouped(const exl3_layer *layers, int count, int K, int codebook, int M,

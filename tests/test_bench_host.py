@@ -88,8 +88,8 @@ def test_kernels_per_group():
     sms = 152
     # warp-shuffle at batch <= 2: x pairs, one sub-unit kernel over every layer, output transform
     assert bench.kernels_per_group("auto", 1, [(4096, 4096), (1024, 4096), (1024, 4096)], sms) == 3
-    # decode-MMA above: one image kernel per layer, one launch over every layer
-    assert bench.kernels_per_group("auto", 5, [(4096, 4096), (1024, 4096)], sms) == 3
+    # decode-MMA above: one image launch for every layer, one launch over every layer
+    assert bench.kernels_per_group("auto", 5, [(4096, 4096), (1024, 4096)], sms) == 2
     assert bench.kernels_per_group("tensor", 1, [(4096, 4096), (1024, 4096)], sms) == 1
     assert bench.kernels_per_group("shuffle", 5, [(4096, 4096), (1024, 4096)], sms) == 6
     assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 2

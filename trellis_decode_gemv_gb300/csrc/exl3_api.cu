@@ -43,7 +43,7 @@ LayerPlan plan_layer(int m, int n, int mb, int sm_count) {
 }
 
 int choose_sub(long long tiles, int mb, int sm_count) {
-  const int warps = mb == 1 ? 32 : mb == 2 ? 24 : mb == 4 ? 16 : 8;
+  const int warps = mb <= 2 ? 32 : mb == 4 ? 16 : 8;
   const long long per_cta = tiles / sm_count;
   if (per_cta >= 16LL * 2 * warps) return 16;
   if (per_cta >= 8LL * 2 * warps) return 8;
@@ -203,11 +203,13 @@ exl3_status run_mv(MvParams p, int K, int codebook, cudaStream_t cs) {
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
   if (p.M > 2) {
+    // one operand-image launch for every layer of the call
+    BimgGroup bg{};
+    bg.count = p.count;
     for (int i = 0; i < p.count; ++i)
-      if ((st = launch_bimg(p.l[i].x, p.l[i].s_in, const_cast<__half*>(p.l[i].bimg),
-                            mv_centred(codebook) ? const_cast<float*>(p.l[i].bsum) : nullptr, p.M, mv_nb(p.M),
-                            p.l[i].n, cs)) != EXL3_OK)
-        return st;
+      bg.e[i] = BimgEntry{p.l[i].x, p.l[i].s_in, const_cast<__half*>(p.l[i].bimg),
+                          mv_centred(codebook) ? const_cast<float*>(p.l[i].bsum) : nullptr, p.l[i].n, 0};
+    if ((st = launch_bimg_group(bg, p.M, mv_nb(p.M), cs)) != EXL3_OK) return st;
   }
   return launch_mv(p, K, codebook, grid, cs);
 }

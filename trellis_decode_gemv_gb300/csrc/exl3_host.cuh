@@ -112,6 +112,23 @@ struct XdupGroup {
   int rows;
   long long jobs;
 };
+// Operand-B images of the decode-MMA kernel for a group of layers: one warp
+// per (layer, batch row, 128-block); the jobs of layer i start at job_begin.
+struct BimgEntry {
+  const __half* x;      // [M][n]
+  const __half* s_in;   // [n] or nullptr
+  __half* bimg;         // the images (mv_bimg_bytes(n, M))
+  float* bsum;          // [M][n/128] block sums, or nullptr
+  int n;
+  long long job_begin;
+};
+struct BimgGroup {
+  BimgEntry e[kMaxGroup];
+  int count;
+  int M;
+  int nb;               // rows per image tile (16 or 32)
+  long long jobs;
+};
 struct EpiEntry {
   float* zacc;            // [rows][m], zeroed after reading
   const __half* scales;   // [m]
@@ -200,7 +217,7 @@ exl3_status launch_mv_k8(const MvParams& p, int codebook, int grid, cudaStream_t
 // mv_bimg_bytes(n, M) of workspace each), then one launch.
 exl3_status run_mv(MvParams p, int K, int codebook, cudaStream_t stream);
 // Kernel launches of run_mv.
-inline int mv_launches(int count, int M) { return M <= 2 ? 1 : count + 1; }
+inline int mv_launches(int count, int M) { return M <= 2 || count < 1 ? 1 : 2; }
 
 // The int8-activation layer kernel over a group of layers (a batch chunk of
 // mb rows); each sub-unit looks up its layer, as in GroupArgs.
@@ -243,6 +260,8 @@ exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float
 // x pairs of a group; codebook >= 0 sets every entry's x factor from it, -1
 // keeps the factors the entries carry (layers of different codes).
 exl3_status launch_xdup_group(XdupGroup g, int codebook, cudaStream_t stream);
+// One launch of the operand-image kernel for every entry of g (nb < 128).
+exl3_status launch_bimg_group(BimgGroup g, int M, int nb, cudaStream_t stream);
 // The factor the x pairs carry for a code (the byte-sum codes' scale).
 float code_x_factor(int codebook);
 
@@ -370,7 +389,7 @@ exl3_status launch_tc_k8(const LayerArgs& a, const __half* bimg, const float* bs
 // Kernel parameter blocks of a grouped call stay within the 32764 bytes a
 // launch may pass.
 static_assert(sizeof(GroupArgs) <= 32764 && sizeof(MvParams) <= 32764 && sizeof(XdupGroup) <= 32764 &&
-                  sizeof(EpiGroup) <= 32764,
+                  sizeof(EpiGroup) <= 32764 && sizeof(BimgGroup) <= 32764,
               "kernel parameters");
 
 }  // namespace exl3

@@ -252,11 +252,12 @@ __global__ void __launch_bounds__(kSegThreads, seg_ctas_per_sm<MB>()) seg_layer_
 
 // ---- sub-unit kernel (larger layers) -------------------------------------------
 
-// Warps of the one CTA per SM: 32 (1024 threads) at batch 1, 24 for chunks of
-// 2, 16 for 4, 8 for 8 (registers).
+// Warps of the one CTA per SM: 32 (1024 threads) at batch 1 and 2 (64
+// registers: 24 warps with more registers measured 3-5% slower at batch 2),
+// 16 for chunks of 4, 8 for 8 (registers).
 template <int MB>
 __host__ __device__ constexpr int layer_warps() {
-  return MB == 1 ? 32 : MB == 2 ? 24 : MB == 4 ? 16 : 8;
+  return MB <= 2 ? 32 : MB == 4 ? 16 : 8;
 }
 // Registers per thread of the batch-1 kernel.  For K <= 3, 56 x 1024 leaves
 // 8192 of the SM's 65536 registers, room for one 128-thread CTA of the output

@@ -52,81 +52,75 @@ __global__ void __launch_bounds__(kThreads)
   *reinterpret_cast<uint2*>(out + row * d + col) = orr;
 }
 
-// Operand B images of the tensor-core kernels.  The M batch rows form tiles of
-// nb rows; tile t's image starts at half offset t * nb * n.  One warp per
-// (R consecutive batch rows, 128-column block kb): x-tilde = Hb(s_in (.) x) of
-// that block (x itself without s_in), rounded to binary16 and stored in the canonical
-// K-major no-swizzle layout of an nb x 128 operand: element (r, k), r the row
-// within its tile, at half offset ((k / 8) * (nb / 8) + r / 8) * 64 + (r % 8) *
-// 8 + k % 8 of the block's image at kb * nb * 128.  Rows past M are zero.
-// With bsum, also the fp32 sum of the block's binary16 values.  The MMA
-// kernels are programmatic dependents of this one and wait for it before
-// reading the images.
-// R batch rows per warp (the launcher uses R = 1, for the small tiles of the
-// skinny tensor-core kernel: many warps, the shortest latency to the MMA
-// kernel waiting for it; tiles of 128 rows and more use bimg8_kernel below).
-template <int R>
-__global__ void __launch_bounds__(kSmallThreads, R == 1 ? 16 : 8)
-    bimg_kernel(const __half* __restrict__ x, const __half* __restrict__ signs,
-                __half* __restrict__ bimg, float* __restrict__ bsum, int M, int nb, int n) {
+// Operand B images of the tensor-core kernels, for a group of layers.  The M
+// batch rows form tiles of nb rows; tile t's image starts at half offset t *
+// nb * n.  One warp per (layer, batch row, 128-column block kb): x-tilde =
+// Hb(s_in (.) x) of that block (x itself without s_in), rounded to binary16 and
+// stored in the canonical K-major no-swizzle layout of an nb x 128 operand:
+// element (r, k), r the row within its tile, at half offset ((k / 8) * (nb /
+// 8) + r / 8) * 64 + (r % 8) * 8 + k % 8 of the block's image at kb * nb * 128.
+// Rows past M are zero.  With bsum, also the fp32 sum of the block's binary16
+// values.  Launched as a programmatic dependent (it waits for the preceding
+// grid before reading x); the MMA kernels are programmatic dependents of this
+// one and wait for it before reading the images.  One launch serves every
+// layer of a call (tiles of 128 rows and more use bimg8_kernel below).
+__global__ void __launch_bounds__(kSmallThreads, 16) bimg_kernel(const BimgGroup g) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // x may be written by the preceding grid on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int nkb = n / kRowBlock;
   const long long job = static_cast<long long>(blockIdx.x) * (kSmallThreads / 32) + (threadIdx.x >> 5);
-  const int tiles = (M + nb - 1) / nb;
-  if (job >= static_cast<long long>(tiles) * (nb / R) * nkb) return;
-  const int g0 = R * static_cast<int>(job / nkb);  // first batch row (nb is a multiple of R)
-  const int kb = static_cast<int>(job - static_cast<long long>(g0 / R) * nkb);
-  const int col = kb * kRowBlock + 4 * lane;
-  uint2 xr[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i)
-    xr[i] = g0 + i < M ? *reinterpret_cast<const uint2*>(x + static_cast<size_t>(g0 + i) * n + col)
-                       : make_uint2(0u, 0u);
-  float s[4] = {1.f, 1.f, 1.f, 1.f};
-  if (signs != nullptr) {
-    const uint2 sr = *reinterpret_cast<const uint2*>(signs + col);
-    const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
-    const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
-    s[0] = __low2float(s01);
-    s[1] = __high2float(s01);
-    s[2] = __low2float(s23);
-    s[3] = __high2float(s23);
-  }
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int g = g0 + i;  // batch row
-    const int tile = g / nb;
-    const int r = g - tile * nb;  // row within its tile
-    uint2 o = make_uint2(0u, 0u);
-    if (g < M) {  // warp-uniform
-      if (signs != nullptr) {
-        const __half2 x01 = *reinterpret_cast<const __half2*>(&xr[i].x);
-        const __half2 x23 = *reinterpret_cast<const __half2*>(&xr[i].y);
-        float v[4] = {__low2float(x01) * s[0], __high2float(x01) * s[1], __low2float(x23) * s[2],
-                      __high2float(x23) * s[3]};
-        fwht128_warp(v, lane);
-        const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
-        const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
-        o.x = *reinterpret_cast<const uint32_t*>(&o01);
-        o.y = *reinterpret_cast<const uint32_t*>(&o23);
-      } else {
-        o = xr[i];
-      }
-      if (bsum != nullptr) {
-        const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
-        const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
-        float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
-        if (lane == 0) bsum[static_cast<size_t>(g) * nkb + kb] = hs;
-      }
+  if (job >= g.jobs) return;
+  int li = 0;
+  {
+    int hi = g.count - 1;  // the last layer whose first job is <= job
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (job >= g.e[mid].job_begin) li = mid; else hi = mid - 1;
     }
-    // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
-    const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
-                       (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
-    *reinterpret_cast<uint2*>(bimg + off) = o;
   }
+  const BimgEntry& e = g.e[li];
+  const int n = e.n, nb = g.nb, M = g.M;
+  const int nkb = n / kRowBlock;
+  const long long lj = job - e.job_begin;
+  const int gr = static_cast<int>(lj / nkb);  // batch row
+  const int kb = static_cast<int>(lj - static_cast<long long>(gr) * nkb);
+  const int col = kb * kRowBlock + 4 * lane;
+  const uint2 xr = gr < M ? *reinterpret_cast<const uint2*>(e.x + static_cast<size_t>(gr) * n + col)
+                          : make_uint2(0u, 0u);
+  const int tile = gr / nb;
+  const int r = gr - tile * nb;  // row within its tile
+  uint2 o = make_uint2(0u, 0u);
+  if (gr < M) {  // warp-uniform
+    if (e.s_in != nullptr) {
+      const uint2 sr = *reinterpret_cast<const uint2*>(e.s_in + col);
+      const __half2 s01 = *reinterpret_cast<const __half2*>(&sr.x);
+      const __half2 s23 = *reinterpret_cast<const __half2*>(&sr.y);
+      const __half2 x01 = *reinterpret_cast<const __half2*>(&xr.x);
+      const __half2 x23 = *reinterpret_cast<const __half2*>(&xr.y);
+      float v[4] = {__low2float(x01) * __low2float(s01), __high2float(x01) * __high2float(s01),
+                    __low2float(x23) * __low2float(s23), __high2float(x23) * __high2float(s23)};
+      fwht128_warp(v, lane);
+      const __half2 o01 = __floats2half2_rn(v[0] * kInvSqrt128, v[1] * kInvSqrt128);
+      const __half2 o23 = __floats2half2_rn(v[2] * kInvSqrt128, v[3] * kInvSqrt128);
+      o.x = *reinterpret_cast<const uint32_t*>(&o01);
+      o.y = *reinterpret_cast<const uint32_t*>(&o23);
+    } else {
+      o = xr;
+    }
+    if (e.bsum != nullptr) {
+      const __half2 o01 = *reinterpret_cast<const __half2*>(&o.x);
+      const __half2 o23 = *reinterpret_cast<const __half2*>(&o.y);
+      float hs = (__low2float(o01) + __high2float(o01)) + (__low2float(o23) + __high2float(o23));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, d);
+      if (lane == 0) e.bsum[static_cast<size_t>(gr) * nkb + kb] = hs;
+    }
+  }
+  // This lane's four values are k = 4 * lane .. 4 * lane + 3 of the block.
+  const size_t off = static_cast<size_t>(tile) * nb * n + static_cast<size_t>(kb) * nb * kRowBlock +
+                     (static_cast<size_t>(lane / 2) * (nb / 8) + r / 8) * 64 + (r % 8) * 8 + (lane % 2) * 4;
+  *reinterpret_cast<uint2*>(e.bimg + off) = o;
 }
 
 // The same images for tiles of at least 128 rows, eight rows per warp: the
@@ -433,14 +427,17 @@ exl3_status launch_rht(const __half* in, const __half* signs, __half* out, int r
 
 exl3_status launch_bimg(const __half* x, const __half* s_in, __half* bimg, float* bsum, int M,
                         int nb, int n, cudaStream_t stream) {
-  const int R = nb >= 128 ? 8 : 1;
+  if (nb < 128) {
+    BimgGroup g{};
+    g.count = 1;
+    g.e[0] = BimgEntry{x, s_in, bimg, bsum, n, 0};
+    return launch_bimg_group(g, M, nb, stream);
+  }
+  constexpr int R = 8;
   const long long blocks = static_cast<long long>((M + nb - 1) / nb) * (nb / R) * (n / kRowBlock);
   const long long per_cta = kSmallThreads / 32;
   const unsigned grid = static_cast<unsigned>((blocks + per_cta - 1) / per_cta);
-  if (R == 8)
-    bimg8_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
-  else
-    bimg_kernel<1><<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
+  bimg8_kernel<<<grid, kSmallThreads, 0, stream>>>(x, s_in, bimg, bsum, M, nb, n);
   return launch_status();
 }
 
@@ -488,6 +485,19 @@ exl3_status launch_epi_group(EpiGroup g, cudaStream_t stream) {
     g.jobs += static_cast<long long>(g.rows) * (g.e[i].m / kRowBlock);
   }
   return launch_pdl_small(epi_kernel, g, stream);
+}
+
+exl3_status launch_bimg_group(BimgGroup g, int M, int nb, cudaStream_t stream) {
+  if (nb >= 128) return EXL3_ERR_BATCH;  // wide tiles: launch_bimg
+  g.M = M;
+  g.nb = nb;
+  g.jobs = 0;
+  const long long rows = static_cast<long long>((M + nb - 1) / nb) * nb;
+  for (int i = 0; i < g.count; ++i) {
+    g.e[i].job_begin = g.jobs;
+    g.jobs += rows * (g.e[i].n / kRowBlock);
+  }
+  return launch_pdl_small(bimg_kernel, g, stream);
 }
 
 exl3_status launch_xdup(const __half* x, const __half* s_in, uint32_t* xd, int rows, int n,
