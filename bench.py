@@ -228,8 +228,8 @@ def step_groups(gemvs, max_group: int):
 
 
 GROUPING_CALLS = {
-    "step": "every GEMV of the step in exl3_gemm_multi calls (mixed K and code: one x-pair kernel, a layer "
-            "kernel per (K, code) class, one output kernel)",
+    "step": "every GEMV of the step in multi-code calls of up to 64 layers (mixed K and code: one input "
+            "kernel, a layer kernel per (K, code) class, one output kernel)",
     "class": "every GEMV of the step that shares K and the code in one grouped call",
     "decoder": "q/k/v and gate/up grouped per call (the projections a decoder applies to one step), "
                "the rest one call each",
@@ -506,8 +506,8 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
         if len(shapes) == 1:
             return B.exl3_gemm_launches(shapes[0][0], shapes[0][1], M) + 2
         return kernels_per_group(path, M, shapes, sms) + 2
-    if int8:
-        return 2 + int8_chunks(M)
+    if int8:  # one activation kernel, a layer kernel per chunk and (K, code) class, one output kernel
+        return 2 + int8_chunks(M) * (len(set(kcs)) if kcs is not None else 1)
     if kcs is not None and len(shapes) > 1:  # exl3_gemm_multi: one chain, a layer kernel per (K, code) class
         classes = {}
         for sh, kc in zip(shapes, kcs):
@@ -570,7 +570,7 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     if M > 32:
         grouping = "none"
     shapes_kc = [(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls]
-    if grouping == "step" and (whole or int8):
+    if grouping == "step" and whole:
         grouping = "class"
     if grouping == "step":
         groups = step_groups(shapes_kc, B.MAX_GROUP)
@@ -593,7 +593,7 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
             fn(c["codes"], c["K"], c["cb"], c["m"], c["n"], c["s_in"], c["s_out"],
                c["scales"], c["x"], y=c["y"], workspace=ws)
         elif grouping == "step":
-            B.exl3_gemm_multi([calls[i] for i in g], workspace=ws)
+            (B.exl3_gemm_int8act_multi if int8 else B.exl3_gemm_multi)([calls[i] for i in g], workspace=ws)
         else:
             c0 = calls[g[0]]
             gfn = (B.exl3_gemm_int8act_grouped if int8 else B.exl3_gemm_whole_grouped if whole
@@ -790,6 +790,7 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
                    "grouping": grouping,
                    "calls": GROUPING_CALLS[grouping] + (
                        " (exl3_gemm_whole_grouped / exl3_gemm_whole)" if whole else
+                       " (exl3_gemm_int8act_multi / exl3_gemm_int8act)" if int8 and grouping == "step" else
                        " (exl3_gemm_int8act_grouped / exl3_gemm_int8act)" if int8 else
                        " (exl3_gemm_grouped / exl3_gemm_small)") + f"; {len(groups)} calls per step"},
         "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
@@ -814,7 +815,9 @@ def measure_e2e(ctx, calls, groups, M, ws, whole, int8, total_n, total_m, X, Y, 
     torch, B, dev, stream, world = ctx["torch"], ctx["B"], ctx["dev"], ctx["stream"], ctx["world"]
     layer_objs = []
     for g in groups:
-        if int8 and len(g) > 1:  # the public calls themselves
+        if int8 and grouping == "step" and len(g) > 1:  # the mixed-code layer object
+            layer_objs.append(B.Exl3LinearMulti([calls[i] for i in g], int8=True))
+        elif int8 and len(g) > 1:  # the public calls themselves
             c0 = calls[g[0]]
             layer_objs.append(lambda g=g, c0=c0: B.exl3_gemm_int8act_grouped(
                 [calls[i] for i in g], c0["K"], c0["cb"], workspace=ws))

@@ -441,6 +441,26 @@ exl3_status exl3_gemm_int8act_grouped(const exl3_layer *layers, int count, int K
                                       int M, void *workspace, size_t workspace_bytes,
                                       exl3_stream_t stream);
 
+/**
+ * Bytes of scratch for exl3_gemm_int8act_multi: exl3_group_i8_workspace_bytes
+ * of the same layers.  0 for an invalid group.
+ */
+size_t exl3_multi_i8_workspace_bytes(const exl3_layer_kc *layers, int count, int M);
+
+/**
+ * `count` (1..EXL3_MAX_GROUP) independent layers on int8 activations, each
+ * with its own K and byte-sum code (1MAD or mul1), at one batch M
+ * (1..EXL3_MAX_BATCH): the results equal `count` calls of exl3_gemm_int8act.
+ * One activation kernel for every layer's x (each layer's tile corrections
+ * and block factors with its own code's centre and scale), per batch chunk one
+ * int8 layer kernel per (K, code) class (in order of first appearance), one
+ * output kernel.  Validation and errors as exl3_gemm_int8act_grouped, K and the
+ * code checked per layer; workspace >= exl3_multi_i8_workspace_bytes, same
+ * zero-fill contract.
+ */
+exl3_status exl3_gemm_int8act_multi(const exl3_layer_kc *layers, int count, int M, void *workspace,
+                                    size_t workspace_bytes, exl3_stream_t stream);
+
 /** Kernel family used by exl3_gemv / exl3_gemm_small. */
 typedef enum {
   EXL3_PATH_AUTO = 0,    /**< warp-shuffle kernel for M <= 2, decode-MMA kernel above */

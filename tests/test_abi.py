@@ -324,3 +324,34 @@ def test_multi_workspace_and_validation(lib):
     assert call() == 6
     arr[1].layer.x = A
     assert call(wsb=64) == 7 and call(ws=None) == 7
+
+
+def test_int8_multi_workspace_and_validation(lib):
+    shapes = [(256, 384), (1024, 4096), (128, 128)]
+    for M in (1, 2, 7):
+        assert B.exl3_multi_i8_workspace_bytes(shapes, M) == B.exl3_group_i8_workspace_bytes(shapes, M)
+    arr = (B.Exl3LayerKC * 2)()
+    for i, (m, n) in enumerate([(256, 256), (128, 384)]):
+        arr[i].layer.codes, arr[i].layer.m, arr[i].layer.n = A, m, n
+        arr[i].layer.scales, arr[i].layer.x, arr[i].layer.y = A, A, A
+        arr[i].K, arr[i].codebook = 2 + i, 1 + 2 * i  # 1MAD, mul1
+
+    def call(count=2, M=1, ws=A, wsb=1 << 30):
+        return lib.exl3_gemm_int8act_multi(arr, count, M, ws, wsb, None)
+
+    assert lib.exl3_gemm_int8act_multi(None, 1, 1, A, 1 << 30, None) == 1
+    assert call(count=0) == 5 and call(count=B.MAX_GROUP + 1) == 5 and call(M=33) == 5
+    arr[1].K = 9
+    assert call() == 3
+    arr[1].K = 3
+    for bad in (0, 2, 4):  # 3INST and MCG have no byte sum; 4 is no code
+        arr[1].codebook = bad
+        assert call() == 4
+    arr[1].codebook = 3
+    arr[1].layer.m = 130
+    assert call() == 2
+    arr[1].layer.m = 128
+    arr[1].layer.x = A + 2
+    assert call() == 6
+    arr[1].layer.x = A
+    assert call(wsb=64) == 7 and call(ws=None) == 7

@@ -95,6 +95,17 @@ def test_kernels_per_group():
     assert bench.kernels_per_group("auto", 1, [(1024, 4096)], sms) == 2
 
 
+def test_launches_of_multi_code_groups():
+    """A multi-code call: one input and one output kernel around a layer
+    kernel per (K, code) class and batch chunk (int8: chunks of 8/4/2/1 rows)."""
+    sms, shapes = 152, [(4096, 4096), (1024, 4096), (1024, 4096)]
+    kcs = [(2, 1), (3, 3), (2, 1)]
+    assert bench.launches_of_group(None, "auto", 1, shapes, sms, False, True, kcs) == 4
+    assert bench.launches_of_group(None, "auto", 3, shapes, sms, False, True, kcs) == 6
+    assert bench.launches_of_group(None, "auto", 1, shapes, sms, False, True) == 3
+    assert bench.launches_of_group(None, "auto", 2, shapes, sms, False, False, kcs) == 4
+
+
 def test_decoder_groups_whole_vector_stack():
     """The whole-vector workload groups q, k and v of each layer (one
     exl3_gemm_whole_grouped call) and runs o alone."""

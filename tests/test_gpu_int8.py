@@ -7,7 +7,9 @@ eight-bit activations, byte-sum codes, one dp4a per four products):
   the same dequantized activations (relative L2 <= 5e-3, |err| <= 1e-2 *
   max|y_ref|), for 1MAD and mul1, K = 1..8, batch chunks of 1, 2, 4, 8;
 * exl3_gemm_int8act from binary16 activations against the oracle's
-  quantize-then-layer, and its distance from the unquantized layer."""
+  quantize-then-layer, and its distance from the unquantized layer;
+* the grouped calls (one K and code; and layers of their own K and code in one
+  chain) against the same per layer."""
 import numpy as np
 import pytest
 import torch
@@ -144,3 +146,44 @@ def test_int8act_grouped_batch_32():
     torch.cuda.synchronize()
     for L, ref in zip(layers, refs):
         assert_layer_close(L["y"], ref, f"grouped M=32 {L['m']}x{L['n']}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_int8act_multi_code_group(M):
+    """Layers of every K and both byte-sum codes, classes interleaved, in one
+    exl3_gemm_int8act_multi call: each layer within tolerance of the oracle's
+    quantize-then-layer, and within one binary16 rounding of its own
+    exl3_gemm_int8act call; the marshalled-once object gives the same."""
+    kcs = [(2, 1), (3, 3), (2, 1), (1, 3), (4, 1), (5, 3), (6, 1), (7, 3), (8, 1), (3, 3), (2, 3)]
+    shapes = [(256, 512), (128, 1024), (384, 256), (128, 128), (256, 384), (128, 256), (128, 512),
+              (256, 128), (128, 256), (512, 256), (128, 640)]
+    layers, refs = [], []
+    for i, ((K, cb), (m, n)) in enumerate(zip(kcs, shapes)):
+        inp = synth.layer_inputs(m, n, K, M, config=91, index=100 * M + i)
+        d = upload(inp)
+        layers.append(dict(codes=d["codes"], m=m, n=n, K=K, cb=cb, s_in=d["s_in"], s_out=d["s_out"],
+                           scales=d["scales"], x=d["x"],
+                           y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda")))
+        xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+        q, qs = O.quantize_act(xt)
+        refs.append(O.layer_forward_int8(inp["codes"], K, cb, m, n, inp["s_out"], inp["scales"], q, qs))
+    ws = torch.zeros(B.exl3_multi_i8_workspace_bytes(shapes, M), dtype=torch.uint8, device="cuda")
+    B.exl3_gemm_int8act_multi(layers, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    for L, ref in zip(layers, refs):
+        assert_layer_close(L["y"], ref, f"multi K{L['K']} cb{L['cb']} {L['m']}x{L['n']} M={M}")
+    for L in layers:
+        y1 = B.exl3_gemm_int8act(L["codes"], L["K"], L["cb"], L["m"], L["n"], L["s_in"], L["s_out"], L["scales"],
+                                 L["x"])
+        torch.cuda.synchronize()
+        assert float((y1.float() - L["y"].float()).abs().max()) <= 2.0 ** -9 * float(y1.float().abs().max())
+    first = [L["y"].clone() for L in layers]
+    obj = B.Exl3LinearMulti(layers, int8=True)
+    for L in layers:
+        L["y"].fill_(float("nan"))
+    obj()
+    obj()  # the workspace is left clean for the next call
+    torch.cuda.synchronize()
+    for L, y0 in zip(layers, first):
+        assert float((y0.float() - L["y"].float()).abs().max()) <= 2.0 ** -9 * float(y0.float().abs().max())

@@ -81,6 +81,8 @@ _SIGNATURES = {
     "exl3_gemm_int8act": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_group_i8_workspace_bytes": ([ctypes.POINTER(Exl3Layer), _I, _I], _SZ),
     "exl3_gemm_int8act_grouped": ([ctypes.POINTER(Exl3Layer), _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "exl3_multi_i8_workspace_bytes": ([ctypes.POINTER(Exl3LayerKC), _I, _I], _SZ),
+    "exl3_gemm_int8act_multi": ([ctypes.POINTER(Exl3LayerKC), _I, _I, _P, _SZ, _P], _I),
     "exl3_encode_tiles": ([_P, _I, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "exl3_gemm_whole_workspace_bytes": ([_I, _I, _I], _SZ),
     "exl3_gemm_whole": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P], _I),
@@ -311,6 +313,16 @@ def _layer_array(layers, dev, M):
     return arr
 
 
+def _kc_array(layers, dev, M):
+    plain = _layer_array(layers, dev, M)
+    arr = (Exl3LayerKC * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i].layer = plain[i]
+        arr[i].K = int(L["K"])
+        arr[i].codebook = int(L["cb"])
+    return arr
+
+
 def exl3_gemm_multi(layers, workspace=None):
     """Independent layers of their own K and code at one batch: each dict as
     for exl3_gemm_grouped plus K and cb.  Same results as one exl3_gemm_small
@@ -319,12 +331,7 @@ def exl3_gemm_multi(layers, workspace=None):
     lib = load_library()
     dev = layers[0]["codes"].device
     M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
-    plain = _layer_array(layers, dev, M)
-    arr = (Exl3LayerKC * len(layers))()
-    for i, L in enumerate(layers):
-        arr[i].layer = plain[i]
-        arr[i].K = int(L["K"])
-        arr[i].codebook = int(L["cb"])
+    arr = _kc_array(layers, dev, M)
     if workspace is None:
         workspace = alloc_group_workspace([(L["m"], L["n"]) for L in layers], M, dev)
     _check(lib.exl3_gemm_multi(arr, len(layers), M, _ptr(workspace, "workspace", (torch.uint8,), dev),
@@ -380,6 +387,37 @@ def exl3_group_i8_workspace_bytes(shapes, M: int = 1) -> int:
     return int(load_library().exl3_group_i8_workspace_bytes(arr, len(shapes), M))
 
 
+def exl3_multi_i8_workspace_bytes(shapes, M: int = 1) -> int:
+    """Workspace bytes of a multi-code int8-activation call over layers of (m, n)."""
+    arr = (Exl3LayerKC * len(shapes))()
+    for i, (m, n) in enumerate(shapes):
+        arr[i].layer.m, arr[i].layer.n = m, n
+        arr[i].K, arr[i].codebook = 2, 1
+    return int(load_library().exl3_multi_i8_workspace_bytes(arr, len(shapes), M))
+
+
+def _i8_group_workspace(shapes, M, dev):
+    nbytes = exl3_group_i8_workspace_bytes(shapes, M)
+    if nbytes == 0:
+        raise Exl3Error(2, "invalid group for a workspace")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+
+
+def exl3_gemm_int8act_multi(layers, workspace=None):
+    """Independent layers on int8 activations, each of its own K and byte-sum
+    code (dicts as for exl3_gemm_multi, cb 1MAD or mul1); same results as one
+    exl3_gemm_int8act per layer, in one kernel chain."""
+    lib = load_library()
+    dev = layers[0]["codes"].device
+    M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
+    arr = _kc_array(layers, dev, M)
+    if workspace is None:
+        workspace = _i8_group_workspace([(L["m"], L["n"]) for L in layers], M, dev)
+    _check(lib.exl3_gemm_int8act_multi(arr, len(layers), M, _ptr(workspace, "workspace", (torch.uint8,), dev),
+                                       workspace.numel(), _stream(dev)))
+    return [L["y"] for L in layers]
+
+
 def exl3_gemm_int8act_grouped(layers, K, codebook, workspace=None):
     """Independent layers on int8 activations (1MAD or mul1), as dicts like
     exl3_gemm_grouped's; same results as one exl3_gemm_int8act per layer."""
@@ -388,10 +426,7 @@ def exl3_gemm_int8act_grouped(layers, K, codebook, workspace=None):
     M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
     arr = _layer_array(layers, dev, M)
     if workspace is None:
-        nbytes = exl3_group_i8_workspace_bytes([(L["m"], L["n"]) for L in layers], M)
-        if nbytes == 0:
-            raise Exl3Error(2, "invalid group for a workspace")
-        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        workspace = _i8_group_workspace([(L["m"], L["n"]) for L in layers], M, dev)
     _check(lib.exl3_gemm_int8act_grouped(arr, len(layers), K, codebook, M,
                                          _ptr(workspace, "workspace", (torch.uint8,), dev), workspace.numel(),
                                          _stream(dev)))
@@ -463,24 +498,22 @@ class Exl3LinearGroup:
 
 class Exl3LinearMulti:
     """Independent layers of their own K and code (one batch) marshalled once
-    for exl3_gemm_multi: each layer dict as for Exl3LinearGroup plus K and cb;
-    x and y stay bound to those tensors."""
+    for exl3_gemm_multi (or, with int8=True, exl3_gemm_int8act_multi): each
+    layer dict as for Exl3LinearGroup plus K and cb; x and y stay bound to
+    those tensors."""
 
-    def __init__(self, layers):
+    def __init__(self, layers, int8=False):
         lib = load_library()
         self.device = layers[0]["codes"].device
         self.M = layers[0]["x"].shape[0] if layers[0]["x"].dim() == 2 else 1
         self._keep = [dict(L) for L in layers]
-        plain = _layer_array(layers, self.device, self.M)
-        self._arr = (Exl3LayerKC * len(layers))()
-        for i, L in enumerate(layers):
-            self._arr[i].layer = plain[i]
-            self._arr[i].K = int(L["K"])
-            self._arr[i].codebook = int(L["cb"])
-        self.workspace = alloc_group_workspace([(L["m"], L["n"]) for L in layers], self.M, self.device)
+        self._arr = _kc_array(layers, self.device, self.M)
+        shapes = [(L["m"], L["n"]) for L in layers]
+        self.workspace = (_i8_group_workspace(shapes, self.M, self.device) if int8
+                          else alloc_group_workspace(shapes, self.M, self.device))
         self._ws = (self.workspace.data_ptr(), self.workspace.numel())
         self._count = len(layers)
-        self._fn = lib.exl3_gemm_multi
+        self._fn = lib.exl3_gemm_int8act_multi if int8 else lib.exl3_gemm_multi
 
     def __call__(self):
         _check(self._fn(self._arr, self._count, self.M, *self._ws,

@@ -15,10 +15,11 @@
 //
 // Same lane mapping and work split as the warp-shuffle sub-unit kernel: a
 // warp decodes one tile row, lane 8 * jt + p takes rows 2p, 2p + 1 of tiles
-// jt, jt + 4, ... of a sub-unit of consecutive tiles; one CTA per SM, the warps
-// take sub-units from a shared counter (the sub-units of up to four layers of
-// a group are numbered one after the other); shuffles combine the four tile
-// groups and fp32 reductions add each row's sum into the workspace row sums.
+// jt, jt + 4, ... of a sub-unit of 4 * TPL consecutive tiles (unrolled); one
+// CTA per SM, sub-units interleaved over the warps of all CTAs (the sub-units
+// of the layers of a group are numbered one after the other); shuffles combine
+// the four tile groups and fp32 reductions add each row's sum into the
+// workspace row sums.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -43,69 +44,47 @@ __device__ __forceinline__ int byte_dot(uint32_t x, int q4, int acc) {
   }
 }
 
-template <int K, int CB, int MB>
-__device__ __forceinline__ void i8_body(const I8Args& g) {
-  constexpr int kWarps = layer_warps<MB>();
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
+// Sub-unit lu of layer a (lane 8*jt + p): tiles J0 + jt + 4t (t < TPL), rows
+// 2p, 2p+1 of each; code words two tiles ahead, addressed from one per-lane
+// pointer (and one for the last row pair's wrapped words), as in the binary16
+// sub-unit kernel.
+template <int K, int CB, int MB, int TPL>
+__device__ __forceinline__ void i8_unit(const I8Layer& a, int lu, int lane, bool& waited) {
   const int jt = lane >> 3;
   const int p = lane & 7;
   constexpr int kTw = RowPair<K>::kTileWords;
-  const int S = g.sub;
-  const long long units = g.units;
-  const int u_lo = static_cast<int>(units * blockIdx.x / gridDim.x);
-  const int u_hi = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
-  __shared__ int next_unit;
-
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (tid == 0) next_unit = 0;
-  __syncthreads();
-
-  bool waited = false;
-  int u = u_lo + warp;
-  while (u < u_hi) {
-    // the layer of sub-unit u, then its tile row and first tile column
-    int li = 0;
-    {
-      int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
-      while (li < hi) {
-        const int mid = (li + hi + 1) >> 1;
-        if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
-      }
-    }
-    const I8Layer& a = g.l[li];
-    const int nt = a.n / 16;
-    const int lu = u - a.u_begin;
-    const int I = lu / a.per_row;
-    const int J0 = (lu - I * a.per_row) * S;
-    const int J1 = J0 + S < nt ? J0 + S : nt;
-    const uint32_t* rowp = a.codes + static_cast<size_t>(I) * nt * kTw;
-
-    int J = J0 + jt;
-    uint32_t w0[RowPair<K>::kPairWords], w1[RowPair<K>::kPairWords];
-    if (J < J1) load_row_pair<K>(rowp + static_cast<size_t>(J) * kTw, p, w0);
-    if (J + 4 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 4) * kTw, p, w1);
-    // The activation words, tile corrections and block factors come from the
-    // preceding grid on the stream; the code words above do not.
-    if (!waited) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      waited = true;
-    }
-    int un = 0;
-    if (lane == 0) un = u_lo + kWarps + atomicAdd(&next_unit, 1);
-    un = __shfl_sync(0xFFFFFFFFu, un, 0);
-
-    float acc[MB][2];
+  constexpr int kPw = RowPair<K>::kPairWords;
+  const int nt = a.n / 16;
+  const int I = lu / a.per_row;
+  const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
+  const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
+  const uint32_t* lp = tp + p * K;
+  const uint32_t* lw = lp - (p == 7 ? kTw : 0);
+  auto load_pair = [&](int toff, uint32_t (&wd)[kPw]) {
 #pragma unroll
-    for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+    for (int i = 0; i < kPw; ++i) wd[i] = __ldg((i < K ? lp : lw) + toff + i);
+  };
+  uint32_t w[2][kPw];
+  if (J0 < nt) load_pair(0, w[0]);
+  if (TPL > 1 && J0 + 4 < nt) load_pair(4 * kTw, w[1]);
+  // The activation words, tile corrections and block factors come from the
+  // preceding grid on the stream; the code words above do not.
+  if (!waited) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+  }
 
-    while (J < J1) {
-      uint32_t st[32];
-      pair_states<K>(w0, st);
+  float acc[MB][2];
 #pragma unroll
-      for (int i = 0; i < RowPair<K>::kPairWords; ++i) w0[i] = w1[i];
-      if (J + 8 < J1) load_row_pair<K>(rowp + static_cast<size_t>(J + 8) * kTw, p, w1);
+  for (int b = 0; b < MB; ++b) acc[b][0] = acc[b][1] = 0.f;
+
+#pragma unroll
+  for (int t = 0; t < TPL; ++t) {
+    const int J = J0 + 4 * t;
+    if (J < nt) {  // all lanes but on a row's ragged last sub-unit
+      uint32_t gen[32];
+      pair_generate<K, CB>(w[t & 1], gen);
+      if (t + 2 < TPL && J + 8 < nt) load_pair((4 * t + 8) * kTw, w[t & 1]);
       const int4* qrow = reinterpret_cast<const int4*>(a.q4 + static_cast<size_t>(J) * 16);
       int ia[MB], ib[MB];
 #pragma unroll
@@ -118,13 +97,11 @@ __device__ __forceinline__ void i8_body(const I8Args& g) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = 4 * q + j;
-          const uint32_t xa = generate<CB>(st[c]);
-          const uint32_t xb = generate<CB>(st[16 + c]);
 #pragma unroll
           for (int b = 0; b < MB; ++b) {
             const int qw = j == 0 ? qv[b].x : j == 1 ? qv[b].y : j == 2 ? qv[b].z : qv[b].w;
-            ia[b] = byte_dot<CB>(xa, qw, ia[b]);
-            ib[b] = byte_dot<CB>(xb, qw, ib[b]);
+            ia[b] = byte_dot<CB>(gen[c], qw, ia[b]);
+            ib[b] = byte_dot<CB>(gen[16 + c], qw, ib[b]);
           }
         }
       }
@@ -135,58 +112,86 @@ __device__ __forceinline__ void i8_body(const I8Args& g) {
         acc[b][0] = fmaf(f, static_cast<float>(ia[b] - corr), acc[b][0]);
         acc[b][1] = fmaf(f, static_cast<float>(ib[b] - corr), acc[b][1]);
       }
-      J += 4;
     }
+  }
 
 #pragma unroll
+  for (int b = 0; b < MB; ++b) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float v = acc[b][k];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+      acc[b][k] = v;
+    }
+  }
+  if (jt == 0) {
+#pragma unroll
     for (int b = 0; b < MB; ++b) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        float v = acc[b][k];
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-        acc[b][k] = v;
-      }
+      float* z = a.zacc + static_cast<size_t>(b) * a.m + I * 16 + 2 * p;
+      atomicAdd(z, acc[b][0]);
+      atomicAdd(z + 1, acc[b][1]);
     }
-    if (jt == 0) {
-#pragma unroll
-      for (int b = 0; b < MB; ++b) {
-        float* z = a.zacc + static_cast<size_t>(b) * a.m + I * 16 + 2 * p;
-        atomicAdd(z, acc[b][0]);
-        atomicAdd(z + 1, acc[b][1]);
-      }
-    }
-    u = un;
   }
 }
 
-template <int K, int CB, int MB>
-__global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) i8_kernel(const I8Args a) {
-  i8_body<K, CB, MB>(a);
+// Warps per CTA: 32 at batch 1; batch 2 keeps 16 (its byte-dot sums and
+// activation words do not fit 64 registers at four tiles a lane).
+template <int MB>
+constexpr int i8_warps() { return MB == 1 ? 32 : MB <= 4 ? 16 : 8; }
+
+// Warp w of CTA b takes the sub-units b * warps + w + i * (grid * warps).
+template <int K, int CB, int MB, int TPL>
+__global__ void __launch_bounds__(32 * i8_warps<MB>(), 1) i8_kernel(const I8Args g) {
+  constexpr int kWarps = i8_warps<MB>();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const long long stride = static_cast<long long>(gridDim.x) * kWarps;
+  // The output kernel may be scheduled now (it waits for this grid to finish).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  bool waited = false;
+  for (long long u = static_cast<long long>(blockIdx.x) * kWarps + warp; u < g.units; u += stride) {
+    int li = 0, hi = g.count - 1;  // the last layer whose first sub-unit is <= u
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
+    }
+    const I8Layer& a = g.l[li];
+    i8_unit<K, CB, MB, TPL>(a, static_cast<int>(u - a.u_begin), lane, waited);
+  }
 }
 
-template <int K, int CB, int MB>
+template <int K, int CB, int MB, int TPL>
 exl3_status launch_i8_t(const I8Args& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
-  cfg.blockDim = dim3(32 * layer_warps<MB>());
+  cfg.blockDim = dim3(32 * i8_warps<MB>());
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, i8_kernel<K, CB, MB>, a) != cudaSuccess) return EXL3_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, i8_kernel<K, CB, MB, TPL>, a) != cudaSuccess) return EXL3_ERR_CUDA;
   return launch_status();
+}
+
+template <int K, int CB, int MB>
+exl3_status launch_i8_mb(const I8Args& a, cudaStream_t stream) {
+  switch (a.sub) {
+    case 16: return launch_i8_t<K, CB, MB, 4>(a, stream);
+    case 8: return launch_i8_t<K, CB, MB, 2>(a, stream);
+    default: return launch_i8_t<K, CB, MB, 1>(a, stream);
+  }
 }
 
 template <int K, int CB>
 exl3_status launch_i8_cb(const I8Args& a, int mb, cudaStream_t stream) {
   switch (mb) {
-    case 1: return launch_i8_t<K, CB, 1>(a, stream);
-    case 2: return launch_i8_t<K, CB, 2>(a, stream);
-    case 4: return launch_i8_t<K, CB, 4>(a, stream);
-    case 8: return launch_i8_t<K, CB, 8>(a, stream);
+    case 1: return launch_i8_mb<K, CB, 1>(a, stream);
+    case 2: return launch_i8_mb<K, CB, 2>(a, stream);
+    case 4: return launch_i8_mb<K, CB, 4>(a, stream);
+    case 8: return launch_i8_mb<K, CB, 8>(a, stream);
     default: return EXL3_ERR_BATCH;
   }
 }

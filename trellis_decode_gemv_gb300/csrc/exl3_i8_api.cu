@@ -26,7 +26,7 @@ constexpr int kPrepThreads = 128;
 // One layer's activations for the preparation kernel: binary16 x (rotated
 // here with s_in, or taken as already rotated), or int8 q with its scales;
 // optional outputs q_out / qscale_out (the quantizer) and the layer kernel's
-// operands q4 / tcorr / cs.
+// operands q4 / tcorr / cs, with the code's centre and scale C.
 struct PrepEntry {
   const __half* x;
   const __half* s_in;
@@ -38,6 +38,8 @@ struct PrepEntry {
   int32_t* tcorr;
   float* cs;
   int n;
+  int centre;
+  float C;
   long long job_begin;
 };
 struct PrepGroup {
@@ -45,8 +47,6 @@ struct PrepGroup {
   int count;
   int rows;
   int rotate;
-  int centre;
-  float C;
   long long jobs;
 };
 
@@ -120,14 +120,18 @@ __global__ void __launch_bounds__(kPrepThreads) i8_prep_kernel(const PrepGroup g
     int s = q[0] + q[1] + q[2] + q[3];
     s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
     s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-    if ((lane & 3) == 0) e.tcorr[static_cast<size_t>(row) * (n / 16) + col / 16] = g.centre * s;
-    if (lane == 0) e.cs[static_cast<size_t>(row) * nkb + kb] = __fmul_rn(g.C, scale);
+    if ((lane & 3) == 0) e.tcorr[static_cast<size_t>(row) * (n / 16) + col / 16] = e.centre * s;
+    if (lane == 0) e.cs[static_cast<size_t>(row) * nkb + kb] = __fmul_rn(e.C, scale);
   }
 }
 
-exl3_status launch_prep(PrepGroup g, int codebook, cudaStream_t stream) {
-  g.centre = codebook == EXL3_CB_MUL1 ? kMul1Centre : kOneMadCentre;
-  g.C = codebook == EXL3_CB_MUL1 ? kMul1Scale : kOneMadScale;
+void set_code(PrepEntry& e, int codebook) {
+  e.centre = codebook == EXL3_CB_MUL1 ? kMul1Centre : kOneMadCentre;
+  e.C = codebook == EXL3_CB_MUL1 ? kMul1Scale : kOneMadScale;
+}
+
+// Entries carry their code's centre and scale (set_code).
+exl3_status launch_prep(PrepGroup g, cudaStream_t stream) {
   long long jobs = 0;
   for (int i = 0; i < g.count; ++i) {
     g.e[i].job_begin = jobs;
@@ -203,37 +207,48 @@ exl3_status check_i8(const uint32_t* codes, int K, int codebook, int m, int n, c
   return EXL3_OK;
 }
 
-// The layer kernel over every layer of the group per batch chunk of 8/4/2/1
-// rows, then one output kernel over all layers and rows.
-exl3_status run_i8(const exl3_layer* layers, const I8Region* reg, int count, int K, int codebook, int M,
+// Per batch chunk of 8/4/2/1 rows, one layer kernel per (K, code) class over
+// that class's layers (classes in order of first appearance; ks / cbs give
+// each layer's K and code), then one output kernel over all layers and rows.
+exl3_status run_i8(const exl3_layer* layers, const I8Region* reg, int count, const int* ks, const int* cbs, int M,
                    cudaStream_t cs) {
   const int sms = device_sm_count();
-  long long tiles = 0;
-  for (int i = 0; i < count; ++i) tiles += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
+  int cls[kMaxGroup], nclass = 0;  // the first layer of each class
+  int of[kMaxGroup];               // each layer's class
+  long long tiles[kMaxGroup] = {};
+  for (int i = 0; i < count; ++i) {
+    int c = 0;
+    while (c < nclass && (ks[cls[c]] != ks[i] || cbs[cls[c]] != cbs[i])) ++c;
+    if (c == nclass) cls[nclass++] = i;
+    of[i] = c;
+    tiles[c] += static_cast<long long>(layers[i].m / 16) * (layers[i].n / 16);
+  }
   exl3_status st;
   for (int done = 0; done < M;) {
     const int mb = M - done >= 8 ? 8 : M - done >= 4 ? 4 : M - done >= 2 ? 2 : 1;
-    I8Args a{};
-    a.count = count;
-    a.sub = choose_sub(tiles, mb, sms);
-    long long units = 0;
-    for (int i = 0; i < count; ++i) {
-      const int m = layers[i].m, n = layers[i].n;
-      I8Layer& l = a.l[i];
-      l.codes = layers[i].codes;
-      l.q4 = reg[i].q4 + static_cast<size_t>(done) * n;
-      l.tcorr = reg[i].tcorr + static_cast<size_t>(done) * (n / 16);
-      l.cs = reg[i].cs + static_cast<size_t>(done) * (n / kRowBlock);
-      l.zacc = reg[i].zacc + static_cast<size_t>(done) * m;
-      l.m = m;
-      l.n = n;
-      l.u_begin = static_cast<int>(units);
-      l.per_row = (n / 16 + a.sub - 1) / a.sub;
-      units += static_cast<long long>(m / 16) * l.per_row;
+    for (int c = 0; c < nclass; ++c) {
+      I8Args a{};
+      a.sub = choose_sub(tiles[c], mb, sms);
+      long long units = 0;
+      for (int i = 0; i < count; ++i) {
+        if (of[i] != c) continue;
+        const int m = layers[i].m, n = layers[i].n;
+        I8Layer& l = a.l[a.count++];
+        l.codes = layers[i].codes;
+        l.q4 = reg[i].q4 + static_cast<size_t>(done) * n;
+        l.tcorr = reg[i].tcorr + static_cast<size_t>(done) * (n / 16);
+        l.cs = reg[i].cs + static_cast<size_t>(done) * (n / kRowBlock);
+        l.zacc = reg[i].zacc + static_cast<size_t>(done) * m;
+        l.m = m;
+        l.n = n;
+        l.u_begin = static_cast<int>(units);
+        l.per_row = (n / 16 + a.sub - 1) / a.sub;
+        units += static_cast<long long>(m / 16) * l.per_row;
+      }
+      a.units = units;
+      a.ctas = static_cast<int>(units < sms ? units : sms);
+      if ((st = launch_i8(a, ks[cls[c]], cbs[cls[c]], mb, cs)) != EXL3_OK) return st;
     }
-    a.units = units;
-    a.ctas = static_cast<int>(units < sms ? units : sms);
-    if ((st = launch_i8(a, K, codebook, mb, cs)) != EXL3_OK) return st;
     done += mb;
   }
   EpiGroup eg{};
@@ -283,7 +298,7 @@ extern "C" exl3_status exl3_quantize_act(const exl3_half* x_rot, int M, int n, i
   g.e[0].q_out = q;
   g.e[0].qscale_out = qscale;
   g.e[0].n = n;
-  return launch_prep(g, EXL3_CB_MUL1, reinterpret_cast<cudaStream_t>(stream));
+  return launch_prep(g, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exl3_gemm_i8_workspace_bytes(int m, int n, int M) {
@@ -312,15 +327,16 @@ extern "C" exl3_status exl3_gemm_i8(const uint32_t* codes, int K, int codebook, 
   g.e[0].tcorr = reg.tcorr;
   g.e[0].cs = reg.cs;
   g.e[0].n = n;
-  if ((st = launch_prep(g, codebook, cs)) != EXL3_OK) return st;
+  set_code(g.e[0], codebook);
+  if ((st = launch_prep(g, cs)) != EXL3_OK) return st;
   const exl3_layer L = layer_of(codes, m, n, nullptr, s_out, scales, nullptr, y);
-  return run_i8(&L, &reg, 1, K, codebook, M, cs);
+  return run_i8(&L, &reg, 1, &K, &codebook, M, cs);
 }
 
 // x of every layer rotated and quantized in one preparation kernel, then the
-// layer kernel and the output kernel over the whole group.
-exl3_status run_int8act(const exl3_layer* layers, const I8Region* reg, int count, int K, int codebook, int M,
-                        cudaStream_t cs) {
+// layer kernels and the output kernel over the whole group.
+exl3_status run_int8act(const exl3_layer* layers, const I8Region* reg, int count, const int* ks, const int* cbs,
+                        int M, cudaStream_t cs) {
   PrepGroup g{};
   g.count = count;
   g.rows = M;
@@ -332,10 +348,11 @@ exl3_status run_int8act(const exl3_layer* layers, const I8Region* reg, int count
     g.e[i].tcorr = reg[i].tcorr;
     g.e[i].cs = reg[i].cs;
     g.e[i].n = layers[i].n;
+    set_code(g.e[i], cbs[i]);
   }
-  exl3_status st = launch_prep(g, codebook, cs);
+  exl3_status st = launch_prep(g, cs);
   if (st != EXL3_OK) return st;
-  return run_i8(layers, reg, count, K, codebook, M, cs);
+  return run_i8(layers, reg, count, ks, cbs, M, cs);
 }
 
 extern "C" exl3_status exl3_gemm_int8act(const uint32_t* codes, int K, int codebook, int m, int n,
@@ -349,7 +366,7 @@ extern "C" exl3_status exl3_gemm_int8act(const uint32_t* codes, int K, int codeb
   if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
   const I8Region reg = i8_region(static_cast<char*>(workspace), zacc_offset(m), m, n, M);
   const exl3_layer L = layer_of(codes, m, n, s_in, s_out, scales, x, y);
-  return run_int8act(&L, &reg, 1, K, codebook, M, reinterpret_cast<cudaStream_t>(stream));
+  return run_int8act(&L, &reg, 1, &K, &codebook, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exl3_group_i8_workspace_bytes(const exl3_layer* layers, int count, int M) {
@@ -377,10 +394,50 @@ extern "C" exl3_status exl3_gemm_int8act_grouped(const exl3_layer* layers, int c
   if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
   char* ws = static_cast<char*>(workspace);
   I8Region reg[kMaxGroup];
+  int ks[kMaxGroup], cbs[kMaxGroup];
   size_t at = 256;
   for (int i = 0; i < count; ++i) {
     reg[i] = i8_region(ws, at, layers[i].m, layers[i].n, M);
     at += i8_layer_bytes(layers[i].m, layers[i].n, M);
+    ks[i] = K;
+    cbs[i] = codebook;
   }
-  return run_int8act(layers, reg, count, K, codebook, M, reinterpret_cast<cudaStream_t>(stream));
+  return run_int8act(layers, reg, count, ks, cbs, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exl3_multi_i8_workspace_bytes(const exl3_layer_kc* layers, int count, int M) {
+  if (layers == nullptr || count < 1 || count > EXL3_MAX_GROUP) return 0;
+  exl3_layer plain[kMaxGroup];
+  for (int i = 0; i < count; ++i) plain[i] = layers[i].layer;
+  return exl3_group_i8_workspace_bytes(plain, count, M);
+}
+
+extern "C" exl3_status exl3_gemm_int8act_multi(const exl3_layer_kc* layers, int count, int M, void* workspace,
+                                               size_t workspace_bytes, exl3_stream_t stream) {
+  if (layers == nullptr) return EXL3_ERR_NULL;
+  if (count < 1 || count > EXL3_MAX_GROUP) return EXL3_ERR_BATCH;
+  exl3_layer plain[kMaxGroup];
+  int ks[kMaxGroup], cbs[kMaxGroup];
+  exl3_status st;
+  for (int i = 0; i < count; ++i) {
+    const exl3_layer& L = layers[i].layer;
+    if ((st = check_i8(L.codes, layers[i].K, layers[i].codebook, L.m, L.n, L.s_out, L.scales, M, L.x, L.y)) !=
+        EXL3_OK)
+      return st;
+    if (L.s_in && !aligned16(L.s_in)) return EXL3_ERR_ALIGN;
+    plain[i] = L;
+    ks[i] = layers[i].K;
+    cbs[i] = layers[i].codebook;
+  }
+  const size_t need = exl3_group_i8_workspace_bytes(plain, count, M);
+  if (!workspace || workspace_bytes < need) return EXL3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EXL3_ERR_ALIGN;
+  char* ws = static_cast<char*>(workspace);
+  I8Region reg[kMaxGroup];
+  size_t at = 256;
+  for (int i = 0; i < count; ++i) {
+    reg[i] = i8_region(ws, at, plain[i].m, plain[i].n, M);
+    at += i8_layer_bytes(plain[i].m, plain[i].n, M);
+  }
+  return run_int8act(plain, reg, count, ks, cbs, M, reinterpret_cast<cudaStream_t>(stream));
 }

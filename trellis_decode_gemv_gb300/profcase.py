@@ -3,12 +3,13 @@ ncu captures of one kernel (the summaries under profiles/ name the command).
 
     python -m trellis_decode_gemv_gb300.profcase layer --shape 14336x4096 --K 2 --cb 0 --M 1
     python -m trellis_decode_gemv_gb300.profcase group --K 2 --cb 0 --M 1
+    python -m trellis_decode_gemv_gb300.profcase group --K 2 --cb 1 --int8
 
 `layer`: `--inst` distinct instances of one m x n layer (uniform random code
 words, the input recipe's signs, scales and activations), `--calls` calls of
 exl3_gemm_small in turn.  `group`: the Llama-3-8B layer set of one (K, code)
-class (q, k, v, o, gate, up, down) as one exl3_gemm_grouped call, `--calls`
-times.  Nothing is checked here: the parity tests do that.
+class (q, k, v, o, gate, up, down) as one exl3_gemm_grouped call (with
+`--int8`, one exl3_gemm_int8act_grouped call), `--calls` times.  Nothing is checked here: the parity tests do that.
 """
 import argparse
 
@@ -44,6 +45,7 @@ def main(argv=None):
     ap.add_argument("--inst", type=int, default=8)
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto")
+    ap.add_argument("--int8", action="store_true", help="group case on int8 activations (1MAD or mul1)")
     a = ap.parse_args(argv)
     B.load_library()
     B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[a.path])
@@ -60,13 +62,19 @@ def main(argv=None):
         weights = m * n
     else:
         layers = [_layer(m, n, a.K, a.M, 2000 + 10 * i, dev) for i, (m, n) in enumerate(LLAMA8B_CLASS)]
-        ws = B.alloc_group_workspace(LLAMA8B_CLASS, a.M, dev)
+        if a.int8:
+            ws = torch.zeros(B.exl3_group_i8_workspace_bytes(LLAMA8B_CLASS, a.M), dtype=torch.uint8, device=dev)
+            call = B.exl3_gemm_int8act_grouped
+        else:
+            ws = B.alloc_group_workspace(LLAMA8B_CLASS, a.M, dev)
+            call = B.exl3_gemm_grouped
         torch.cuda.synchronize()
         for _ in range(a.calls):
-            B.exl3_gemm_grouped(layers, a.K, a.cb, workspace=ws)
+            call(layers, a.K, a.cb, workspace=ws)
         weights = sum(m * n for m, n in LLAMA8B_CLASS)
     torch.cuda.synchronize()
-    print(f"{a.case}: {a.calls} calls, {weights / 1e6:.1f} M weights each, K={a.K} code={a.cb} M={a.M}")
+    print(f"{a.case}: {a.calls} calls, {weights / 1e6:.1f} M weights each, K={a.K} code={a.cb} M={a.M}"
+          f"{' int8' if a.int8 else ''}")
     return 0
 
 
