@@ -241,6 +241,7 @@ exl3_status run_shuffle(LayerArgs a, int M, float* zacc, uint32_t* xd, cudaStrea
       g.l[0].u_begin = 0;
       g.l[0].per_row = (a.n / 16 + plan.sub - 1) / plan.sub;
       g.units = (a.m / 16) * g.l[0].per_row;
+      g.l[0].row_magic = div_magic(g.l[0].per_row, g.units);
       g.ctas = plan.ctas;
       if ((st = launch_group(g, a.K, a.codebook, mb, cs)) != EXL3_OK) return st;
     }
@@ -545,6 +546,7 @@ exl3_status group_chain(const exl3_layer* layers, const int* idx, int count, con
         d.n = L.n;
         d.u_begin = units;
         d.per_row = (L.n / 16 + sub - 1) / sub;
+        d.row_magic = div_magic(d.per_row, static_cast<long long>(L.m / 16) * d.per_row);
         units += (L.m / 16) * d.per_row;
       }
       g.units = units;

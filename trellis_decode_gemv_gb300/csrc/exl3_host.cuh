@@ -21,6 +21,18 @@ inline exl3_status check_shape(int m, int n) {
   return EXL3_OK;
 }
 
+// floor(u / d) for 0 <= u < n_end as the high word of u * magic, with magic =
+// ceil(2^32 / d): u * magic / 2^32 = u / d + u * e / (d * 2^32), e = magic * d
+// - 2^32 < d, so the floor is exact while u * e < 2^32.  0 when that does not
+// hold for every u < n_end (or d < 2): the caller divides.
+inline uint32_t div_magic(long long d, long long n_end) {
+  if (d < 2 || d >= (1LL << 32)) return 0;
+  const unsigned long long m = ((1ULL << 32) + static_cast<unsigned long long>(d) - 1) / static_cast<unsigned long long>(d);
+  const unsigned long long e = m * static_cast<unsigned long long>(d) - (1ULL << 32);
+  if (n_end < 0 || n_end >= (1LL << 32)) return 0;
+  return static_cast<unsigned long long>(n_end) * e < (1ULL << 32) ? static_cast<uint32_t>(m) : 0u;
+}
+
 inline exl3_status check_k_cb(int K, int codebook) {
   if (K < 1 || K > 8) return EXL3_ERR_K;
   if (codebook < EXL3_CB_3INST || codebook > EXL3_CB_MUL1) return EXL3_ERR_CODEBOOK;
@@ -86,6 +98,7 @@ struct GroupLayer {
   int m, n;
   int u_begin;
   int per_row;           // sub-units per tile row
+  uint32_t row_magic;    // div_magic(per_row, the layer's sub-units), 0: divide
 };
 
 struct GroupArgs {
@@ -230,6 +243,7 @@ struct I8Layer {
   int m, n;
   int u_begin;  // first sub-unit of this layer
   int per_row;  // sub-units per tile row
+  uint32_t row_magic;  // div_magic(per_row, the layer's sub-units), 0: divide
 };
 struct I8Args {
   I8Layer l[kMaxGroup];

@@ -55,7 +55,7 @@ __device__ __forceinline__ void i8_unit(const I8Layer& a, int lu, int lane, bool
   constexpr int kTw = RowPair<K>::kTileWords;
   constexpr int kPw = RowPair<K>::kPairWords;
   const int nt = a.n / 16;
-  const int I = lu / a.per_row;
+  const int I = a.row_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(lu), a.row_magic)) : lu / a.per_row;
   const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
   const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
   const uint32_t* lp = tp + p * K;
@@ -150,12 +150,19 @@ __global__ void __launch_bounds__(32 * i8_warps<MB>(), 1) i8_kernel(const I8Args
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   bool waited = false;
-  for (long long u = static_cast<long long>(blockIdx.x) * kWarps + warp; u < g.units; u += stride) {
-    int li = 0, hi = g.count - 1;  // the last layer whose first sub-unit is <= u
+  long long u = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  if (u >= g.units) return;
+  int li = 0;
+  {
+    int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
     while (li < hi) {
       const int mid = (li + hi + 1) >> 1;
       if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
     }
+  }
+  for (; u < g.units; u += stride) {
+    // a warp's sub-units increase, so its layer index only moves forward
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
     const I8Layer& a = g.l[li];
     i8_unit<K, CB, MB, TPL>(a, static_cast<int>(u - a.u_begin), lane, waited);
   }

@@ -243,6 +243,7 @@ exl3_status run_i8(const exl3_layer* layers, const I8Region* reg, int count, con
         l.n = n;
         l.u_begin = static_cast<int>(units);
         l.per_row = (n / 16 + a.sub - 1) / a.sub;
+        l.row_magic = div_magic(l.per_row, static_cast<long long>(m / 16) * l.per_row);
         units += static_cast<long long>(m / 16) * l.per_row;
       }
       a.units = units;

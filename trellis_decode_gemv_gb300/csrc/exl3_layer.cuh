@@ -316,7 +316,7 @@ __device__ __forceinline__ void layer_unit(const GroupLayer& a, int lu, int lane
   // binary16 of 1024 + the byte-sum centre (1534 for 1MAD, 1150 for mul1)
   const __half2 k1534 = __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6400 + byte_sum_centre<CB>())));
   const int nt = a.n / 16;
-  const int I = lu / a.per_row;
+  const int I = a.row_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(lu), a.row_magic)) : lu / a.per_row;
   const int J0 = (lu - I * a.per_row) * (4 * TPL) + jt;  // this lane's first tile
   const uint32_t* tp = a.codes + (static_cast<size_t>(I) * nt + J0) * kTw;
   // this lane's words: from word pK of each tile; the last row pair's words
@@ -435,8 +435,13 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   bool waited = false;
-  for (int u = static_cast<int>(blockIdx.x) * kWarps + warp; u < g.units; u += stride) {
-    const GroupLayer& a = g.l[group_layer_of(g, u)];
+  int u = static_cast<int>(blockIdx.x) * kWarps + warp;
+  if (u >= g.units) return;
+  int li = group_layer_of(g, u);
+  for (; u < g.units; u += stride) {
+    // a warp's sub-units increase, so its layer index only moves forward
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    const GroupLayer& a = g.l[li];
     layer_unit<K, CB, MB, TPL>(a, u - a.u_begin, lane, waited);
   }
 }
