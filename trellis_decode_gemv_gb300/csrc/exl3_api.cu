@@ -45,6 +45,9 @@ LayerPlan plan_layer(int m, int n, int mb, int sm_count) {
 int choose_sub(long long tiles, int mb, int sm_count) {
   const int warps = mb <= 2 ? 32 : mb == 4 ? 16 : 8;
   const long long per_cta = tiles / sm_count;
+  // (per-sub-unit work -- the layer lookup, the row index, the reduction --
+  // is a few per cent of a 16-tile sub-unit's instructions at batch 1)
+  if (mb == 1 && per_cta >= 32LL * 2 * warps) return 32;
   if (per_cta >= 16LL * 2 * warps) return 16;
   if (per_cta >= 8LL * 2 * warps) return 8;
   return 4;

@@ -170,7 +170,7 @@ struct LayerArgs {
   uint32_t* status;   // device-side error bits (tensor-core path), or nullptr
   const uint32_t* xdup;  // warp-shuffle kernel: x pairs [mb][n]
   int ctas;           // warp-shuffle kernel: grid size
-  int sub;            // warp-shuffle kernel: tiles per sub-unit (16, 8 or 4)
+  int sub;            // warp-shuffle kernel: tiles per sub-unit (32, 16, 8 or 4)
   int debug_stall;    // tensor-core kernel: test hook, post no operand B
 };
 

@@ -140,7 +140,7 @@ __device__ __forceinline__ void i8_unit(const I8Layer& a, int lu, int lane, bool
 template <int MB>
 constexpr int i8_warps() { return MB == 1 ? 32 : MB <= 4 ? 16 : 8; }
 
-// Warp w of CTA b takes the sub-units b * warps + w + i * (grid * warps).
+// Warp w of CTA b takes the sub-units w * grid + b + i * (grid * warps).
 template <int K, int CB, int MB, int TPL>
 __global__ void __launch_bounds__(32 * i8_warps<MB>(), 1) i8_kernel(const I8Args g) {
   constexpr int kWarps = i8_warps<MB>();
@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(32 * i8_warps<MB>(), 1) i8_kernel(const I8Args
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   bool waited = false;
-  long long u = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  // CTA-fastest numbering: the last partial round falls on every SM alike
+  long long u = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
   if (u >= g.units) return;
   int li = 0;
   {
@@ -186,6 +187,9 @@ exl3_status launch_i8_t(const I8Args& a, cudaStream_t stream) {
 template <int K, int CB, int MB>
 exl3_status launch_i8_mb(const I8Args& a, cudaStream_t stream) {
   switch (a.sub) {
+    case 32:
+      if constexpr (MB == 1) return launch_i8_t<K, CB, MB, 8>(a, stream);
+      return EXL3_ERR_BATCH;
     case 16: return launch_i8_t<K, CB, MB, 4>(a, stream);
     case 8: return launch_i8_t<K, CB, MB, 2>(a, stream);
     default: return launch_i8_t<K, CB, MB, 1>(a, stream);

@@ -19,9 +19,11 @@
 //     and the 128-point FWHT to each 128-row block of zacc, stores y as
 //     binary16 and zeroes zacc for the next call.
 //
-// Work split: a sub-unit is up to S (16, 8 or 4) consecutive tiles of one tile
-// row; one CTA per SM; warp w of CTA b takes the sub-units b * warps + w +
-// i * (grid * warps).  In a sub-unit, lane 8*jt + p handles tiles
+// Work split: a sub-unit is up to S (32, 16, 8 or 4; 32 at batch 1 only)
+// consecutive tiles of one tile row; one CTA per SM; warp w of CTA b takes the
+// sub-units w * grid + b + i * (grid * warps), each warp's tile row found by
+// a multiply-high with a per-layer magic number and its layer by stepping
+// forward from the one of its previous sub-unit.  In a sub-unit, lane 8*jt + p handles tiles
 // J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each: 32 consecutive
 // trellis steps from a word-aligned window per tile (code words loaded two
 // tiles ahead of their decode), with the x pairs of the tile's 16 columns read
@@ -423,9 +425,9 @@ __device__ __forceinline__ void layer_unit(const GroupLayer& a, int lu, int lane
   }
 }
 
-// Warp w of CTA b takes the sub-units b * warps + w + i * (grid * warps).
-// (A device-wide atomic counter balanced the SMs better but cost more than
-// it saved: one L2 address taking an atomic from every warp per sub-unit.)
+// Warp w of CTA b takes the sub-units w * grid + b + i * (grid * warps).
+// (A device-wide atomic counter cost more than it saved: one L2 address taking
+// an atomic from every warp per sub-unit.)
 template <int K, int CB, int MB, int TPL>
 __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   constexpr int kWarps = layer_warps<MB>();
@@ -435,7 +437,9 @@ __device__ __forceinline__ void layer_body(const GroupArgs& g) {
   // The output kernel may be scheduled now (it waits for this grid to finish).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   bool waited = false;
-  int u = static_cast<int>(blockIdx.x) * kWarps + warp;
+  // CTA-fastest numbering: the sub-units of the last partial round (one more
+  // for some warps) fall on every SM alike, not on the first CTAs only.
+  int u = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
   if (u >= g.units) return;
   int li = group_layer_of(g, u);
   for (; u < g.units; u += stride) {
@@ -503,11 +507,14 @@ exl3_status launch_seg_cb(const LayerArgs& a, int mb, cudaStream_t stream) {
   }
 }
 
-// The sub-unit kernel over a group of layers (sub-units of a.sub = 16, 8 or 4
-// tiles: 4, 2 or 1 tiles per lane).
+// The sub-unit kernel over a group of layers (sub-units of a.sub = 32, 16, 8
+// or 4 tiles: 8, 4, 2 or 1 tiles per lane; 32 at batch 1 only).
 template <int K, int CB, int MB>
 exl3_status launch_group_mb(const GroupArgs& a, cudaStream_t stream) {
   switch (a.sub) {
+    case 32:
+      if constexpr (MB == 1) return launch_layer_t<K, CB, MB, 8>(a, stream);
+      return EXL3_ERR_BATCH;
     case 16: return launch_layer_t<K, CB, MB, 4>(a, stream);
     case 8: return launch_layer_t<K, CB, MB, 2>(a, stream);
     default: return launch_layer_t<K, CB, MB, 1>(a, stream);
