@@ -173,3 +173,33 @@ def test_multi_code_group(M):
     for (_, d), y0 in zip(layers, first):
         diff = (y0.float() - d["y"].float()).abs().max()
         assert float(diff) <= 2.0 ** -9 * float(y0.float().abs().max()) + 1e-6
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_multi_repeated_calls_see_new_x(M):
+    """One marshalled multi-code object called twice with new activations
+    written into the same x tensors (the same workspace, so the same x-pair
+    scratch): the second call's outputs follow the new x.  The sub-unit
+    kernels after a chain's first one do not wait for it before they read x
+    pairs, so this checks that they never read the previous call's."""
+    kcs = [(2, 0), (3, 1), (2, 1), (4, 0), (2, 0)]
+    shapes = [(1024, 2048), (512, 1024), (768, 1024), (256, 512), (1024, 1024)]
+    layers, inps = [], []
+    for i, ((m, n), (K, cb)) in enumerate(zip(shapes, kcs)):
+        inp = synth.layer_inputs(m, n, K, M, config=131 + M, index=i)
+        d = upload(inp)
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
+        layers.append(d)
+        inps.append(inp)
+    obj = B.Exl3LinearMulti(layers)
+    for call in range(2):
+        if call:
+            for i, (d, inp) in enumerate(zip(layers, inps)):
+                inp["x"] = synth.activations(M, d["n"], synth.seed_for(141 + M, i))
+                d["x"].copy_(torch.from_numpy(inp["x"]).to("cuda"))
+        obj()
+        torch.cuda.synchronize()
+        for i, (d, inp) in enumerate(zip(layers, inps)):
+            ref = O.layer_forward(inp["codes"], d["K"], d["cb"], d["m"], d["n"], inp["s_in"], inp["s_out"],
+                                  inp["scales"], inp["x"])
+            assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")

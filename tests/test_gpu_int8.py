@@ -187,3 +187,32 @@ def test_int8act_multi_code_group(M):
     torch.cuda.synchronize()
     for L, y0 in zip(layers, first):
         assert float((y0.float() - L["y"].float()).abs().max()) <= 2.0 ** -9 * float(y0.float().abs().max())
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_int8act_multi_repeated_calls_see_new_x(M):
+    """As the binary16 multi-code test: a second call of the same object after
+    new activations are written into the same x tensors follows the new x."""
+    kcs = [(2, 1), (3, 3), (2, 3), (4, 1)]
+    shapes = [(1024, 2048), (512, 1024), (768, 1024), (256, 512)]
+    layers, inps = [], []
+    for i, ((m, n), (K, cb)) in enumerate(zip(shapes, kcs)):
+        inp = synth.layer_inputs(m, n, K, M, config=151 + M, index=i)
+        d = upload(inp)
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
+        layers.append(d)
+        inps.append(inp)
+    obj = B.Exl3LinearMulti(layers, int8=True)
+    for call in range(2):
+        if call:
+            for i, (d, inp) in enumerate(zip(layers, inps)):
+                inp["x"] = synth.activations(M, d["n"], synth.seed_for(161 + M, i))
+                d["x"].copy_(torch.from_numpy(inp["x"]).to("cuda"))
+        obj()
+        torch.cuda.synchronize()
+        for i, (d, inp) in enumerate(zip(layers, inps)):
+            xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+            q, qs = O.quantize_act(xt)
+            ref = O.layer_forward_int8(inp["codes"], d["K"], d["cb"], d["m"], d["n"], inp["s_out"], inp["scales"],
+                                       q, qs)
+            assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")
