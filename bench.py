@@ -67,11 +67,12 @@ OPS_PER_WEIGHT_INT8 = {synth.CB_1MAD: 3, synth.CB_MUL1: 4}
 # captures of those kernels (dram__bytes_read.sum +
 # dram__bytes_write.sum of the captured launches over their algorithmic bytes).
 TRAFFIC_RATIO = {
-    # DRAM reads against the algorithmic bytes of one grouped launch over the 7
-    # Llama-3-8B projections (218 M weights): 54.87 / 54.94 MB at K2 3INST,
-    # 109.40 / 109.47 MB at K4 1MAD (x and the signs come from L2)
-    "shuffle": (54.870 / 54.940, "the ncu capture of layer_kernel on one grouped call over the 7 Llama-3-8B "
-                                 "projections, K2 3INST"),
+    # DRAM reads + writes against the algorithmic bytes of one grouped launch
+    # over the 7 Llama-3-8B projections (218 M weights): (54.881 + 0.029) /
+    # 54.940 MB at K2 3INST, (109.415 + 3.208) / 109.466 MB at K4 1MAD (x and
+    # the signs come from L2; the writes are the fp32 row-sum atomics)
+    "shuffle": ((54.881 + 0.029) / 54.940, "the ncu capture of layer_kernel (32-tile sub-units) on one grouped "
+                                           "call over the 7 Llama-3-8B projections, K2 3INST"),
     "tensor": (23.12 / 22.15, "the ncu capture of tc_layer_kernel on 14336x4096 K3 1MAD at batch 16"),
     "dense": (None, None),
     # DRAM reads 26.0 + 26.6 MB against 2 x 23.86 MB of algorithmic bytes; the
@@ -80,7 +81,10 @@ TRAFFIC_RATIO = {
     "fused": ((26.0 + 26.6) / (2 * 23.86),
               "the ncu capture of the fused dense_kernel (128-row tiles) on 14336x4096 and 4096x14336 K3 1MAD "
               "at batch 48"),
-    "int8": (None, None),
+    # the int8-activation layer kernel on the same call at K2 1MAD:
+    # (54.889 + 0.029) / 54.940 MB
+    "int8": ((54.889 + 0.029) / 54.940, "the ncu capture of i8_kernel (32-tile sub-units) on one grouped "
+                                        "int8-activation call over the 7 Llama-3-8B projections, K2 1MAD"),
 }
 
 
