@@ -169,6 +169,22 @@ def kernels_per_call(path: str, M: int, m: int, n: int, sms: int) -> int:
     return launches
 
 
+def multi_layer_launches(mb: int, classes: dict, sms: int) -> int:
+    """Sub-unit kernel launches of one batch chunk of an exl3_gemm_multi call:
+    one per (K, code) class, except at chunks of one row, where the classes of
+    one K whose tiles give every SM at least 2048 (32-tile sub-units) share
+    one launch."""
+    if mb != 1:
+        return len(classes)
+    by_k = {}
+    for (K, _cb), shs in classes.items():
+        by_k.setdefault(K, []).append(sum((m // 16) * (n // 16) for m, n in shs))
+    n = 0
+    for tiles in by_k.values():
+        n += 1 if (len(tiles) > 1 and sum(tiles) // sms >= 2048) else len(tiles)
+    return n
+
+
 def int8_chunks(M: int) -> int:
     """Layer-kernel launches of one int8-activation call: one per batch chunk
     of 8, 4, 2 or 1 rows (plus the preparation and output kernels)."""
@@ -512,12 +528,17 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
         return kernels_per_group(path, M, shapes, sms) + 2
     if int8:  # one activation kernel, a layer kernel per chunk and (K, code) class, one output kernel
         return 2 + int8_chunks(M) * (len(set(kcs)) if kcs is not None else 1)
-    if kcs is not None and len(shapes) > 1:  # exl3_gemm_multi: one chain, a layer kernel per (K, code) class
+    if kcs is not None and len(shapes) > 1:  # exl3_gemm_multi: one chain per batch chunk
         classes = {}
         for sh, kc in zip(shapes, kcs):
             classes.setdefault(kc, []).append(sh)
         if uses_shuffle(path, M):
-            return int8_chunks(M) * (2 + len(classes))
+            total, rem = 0, M
+            for c in (8, 4, 2, 1):
+                while rem >= c:
+                    rem -= c
+                    total += 2 + multi_layer_launches(c, classes, sms)
+            return total
         return sum(1 if M <= 2 else 2 for shs in classes.values())
     return kernels_per_group(path, M, shapes, sms)
 

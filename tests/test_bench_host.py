@@ -104,6 +104,19 @@ def test_launches_of_multi_code_groups():
     assert bench.launches_of_group(None, "auto", 3, shapes, sms, False, True, kcs) == 6
     assert bench.launches_of_group(None, "auto", 1, shapes, sms, False, True) == 3
     assert bench.launches_of_group(None, "auto", 2, shapes, sms, False, False, kcs) == 4
+    # batch 1, the llama8b step: K = 2, 3, 4 each with 3INST and 1MAD, 218 M
+    # weights per class: one launch per K between the x-pair and output kernels
+    step = [(m, n) for m, n in [(4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (14336, 4096),
+                                (14336, 4096), (4096, 14336)]]
+    shs, kc6 = [], []
+    for K in (2, 3, 4):
+        for cb in (0, 1):
+            shs += step
+            kc6 += [(K, cb)] * len(step)
+    assert bench.launches_of_group(None, "auto", 1, shs, sms, False, False, kc6) == 5
+    assert bench.launches_of_group(None, "auto", 2, shs, sms, False, False, kc6) == 8
+    assert bench.launches_of_group(None, "shuffle", 3, shs, sms, False, False, kc6) == 8 + 5
+    assert bench.launches_of_group(None, "auto", 3, shs, sms, False, False, kc6) == 12  # decode-MMA: 2 per class
 
 
 def test_decoder_groups_whole_vector_stack():

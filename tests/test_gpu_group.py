@@ -203,3 +203,34 @@ def test_multi_repeated_calls_see_new_x(M):
             ref = O.layer_forward(inp["codes"], d["K"], d["cb"], d["m"], d["n"], inp["s_in"], inp["s_out"],
                                   inp["scales"], inp["x"])
             assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")
+
+
+def test_multi_one_k_launch_sampled():
+    """Batch 1, a step whose K = 2 layers of all four codes are large enough
+    for 32-tile sub-units: they run in one launch (one loop per code), the
+    K = 3 layer on its own kernel.  Layers interleave codes and include a
+    ragged row (72 tile columns); sampled 128-row blocks of each output
+    against the oracle, and every output against separate calls."""
+    spec = [(14336, 4096, 2, 0), (1024, 4096, 2, 3), (4096, 4096, 2, 1), (1024, 4096, 3, 1),
+            (4096, 4096, 2, 2), (1024, 1152, 2, 0), (1024, 4096, 2, 1)]
+    layers = []
+    for i, (m, n, K, cb) in enumerate(spec):
+        inp = synth.layer_inputs(m, n, K, 1, config=171, index=i)
+        d = upload(inp)
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((1, m), float("nan"), dtype=torch.float16, device="cuda"))
+        layers.append((inp, d))
+    B.exl3_gemm_multi([d for _, d in layers])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(171)
+    for i, (inp, d) in enumerate(layers):
+        m, n, K, cb = d["m"], d["n"], d["K"], d["cb"]
+        single = B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+        torch.cuda.synchronize()
+        diff = (single.float() - d["y"].float()).abs().max()
+        assert float(diff) <= 2.0 ** -9 * float(single.float().abs().max()) + 1e-6, f"layer {i} K{K} cb{cb}"
+        nb = m // 128
+        rbs = sorted(set([0, nb - 1] + list(rng.integers(0, nb, 2))))
+        ref = O.layer_forward_rowblocks(inp["codes"], K, cb, m, n, inp["s_in"], inp["s_out"], inp["scales"],
+                                        inp["x"], rbs)
+        cols = torch.cat([torch.arange(b * 128, b * 128 + 128) for b in rbs]).cuda()
+        assert_layer_close(d["y"][:, cols], ref, f"layer {i} K{K} cb{cb}")

@@ -74,6 +74,20 @@ exl3_status launch_tc(const LayerArgs& a, const __half* bimg, const float* bsum,
   }
 }
 
+exl3_status launch_group_kset(const GroupArgs& a, int K, cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_group_kset_k1(a, stream);
+    case 2: return launch_group_kset_k2(a, stream);
+    case 3: return launch_group_kset_k3(a, stream);
+    case 4: return launch_group_kset_k4(a, stream);
+    case 5: return launch_group_kset_k5(a, stream);
+    case 6: return launch_group_kset_k6(a, stream);
+    case 7: return launch_group_kset_k7(a, stream);
+    case 8: return launch_group_kset_k8(a, stream);
+    default: return EXL3_ERR_K;
+  }
+}
+
 exl3_status launch_group(const GroupArgs& a, int K, int codebook, int mb, cudaStream_t stream) {
   switch (K) {
     case 1: return launch_group_k1(a, codebook, mb, stream);
@@ -532,7 +546,49 @@ exl3_status group_chain(const exl3_layer* layers, const int* idx, int count, con
       eg.e[j].m = L.m;
     }
     if ((st = launch_xdup_group(xg, -1, cs)) != EXL3_OK) return st;
+    bool launched[kMaxGroup] = {};
     for (int c = 0; c < ncls; ++c) {
+      if (launched[c]) continue;
+      if (mb == 1) {
+        // the classes of this K: at 32-tile sub-units, one launch for all of them
+        const int K = cls_k[c];
+        long long ktiles = 0;
+        int nk = 0;
+        for (int c2 = c; c2 < ncls; ++c2)
+          if (cls_k[c2] == K) {
+            ktiles += tiles[c2];
+            ++nk;
+          }
+        if (nk > 1 && choose_sub(ktiles, 1, sms) == 32) {
+          GroupArgs g{};
+          g.sub = 32;
+          int units = 0;
+          for (int code = 0; code < 4; ++code) {
+            for (int j = 0; j < count; ++j) {
+              if (ks[j] != K || codes[j] != code) continue;
+              const int i = idx[j];
+              const exl3_layer& L = layers[i];
+              GroupLayer& d = g.l[g.count++];
+              d.codes = L.codes;
+              d.xdup = reinterpret_cast<uint32_t*>(ws + gl.scratch[i]);
+              d.zacc = reinterpret_cast<float*>(ws + gl.zacc[i]);
+              d.m = L.m;
+              d.n = L.n;
+              d.u_begin = units;
+              d.per_row = (L.n / 16 + 31) / 32;
+              d.row_magic = div_magic(d.per_row, static_cast<long long>(L.m / 16) * d.per_row);
+              units += (L.m / 16) * d.per_row;
+            }
+            g.code_end[code] = units;
+          }
+          g.units = units;
+          g.ctas = units < sms ? units : sms;
+          if ((st = launch_group_kset(g, K, cs)) != EXL3_OK) return st;
+          for (int c2 = c; c2 < ncls; ++c2)
+            if (cls_k[c2] == K) launched[c2] = true;
+          continue;
+        }
+      }
       GroupArgs g{};
       const int sub = choose_sub(tiles[c], mb, sms);
       g.sub = sub;

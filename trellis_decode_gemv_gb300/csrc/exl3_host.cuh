@@ -107,6 +107,9 @@ struct GroupArgs {
   int units;  // sub-units of all layers
   int sub;    // tiles per sub-unit
   int ctas;
+  // the one-K kernel (launch_group_kset_k*): layers ordered by code, the
+  // sub-units of code c end at code_end[c]
+  int code_end[4];
 };
 
 // x pairs and output transforms of a group: one warp per (layer, batch row,
@@ -281,6 +284,16 @@ float code_x_factor(int codebook);
 
 exl3_status launch_epi_group(EpiGroup g, cudaStream_t stream);
 // The sub-unit kernel over a group (a.sub > 0 tiles per sub-unit, a.ctas CTAs).
+// Batch 1, 32-tile sub-units: the layers of every code of one K in one
+// kernel, one loop per code over that code's sub-units (GroupArgs::code_end).
+exl3_status launch_group_kset_k1(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k2(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k3(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k4(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k5(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k6(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k7(const GroupArgs& a, cudaStream_t stream);
+exl3_status launch_group_kset_k8(const GroupArgs& a, cudaStream_t stream);
 exl3_status launch_group_k1(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
 exl3_status launch_group_k2(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);
 exl3_status launch_group_k3(const GroupArgs& a, int codebook, int mb, cudaStream_t stream);

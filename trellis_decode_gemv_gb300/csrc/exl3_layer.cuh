@@ -460,6 +460,56 @@ __global__ void __launch_bounds__(32 * layer_warps<MB>(), 1) layer_kernel_wide(c
   layer_body<K, CB, MB, TPL>(g);
 }
 
+// The sub-units of code CB (up to `end`) of a one-K kernel, continuing the
+// warp's sequence u; returns where it stopped.
+template <int K, int CB>
+__device__ __forceinline__ int kset_loop(const GroupArgs& g, int u, int stride, int end, int& li, int lane,
+                                         bool& waited) {
+  for (; u < end; u += stride) {
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    const GroupLayer& a = g.l[li];
+    layer_unit<K, CB, 1, 8>(a, u - a.u_begin, lane, waited);
+  }
+  return u;
+}
+
+// Batch 1, 32-tile sub-units: the layers of all four codes of one K, ordered
+// by code, in one launch.  A warp's sub-units (numbered and interleaved as in
+// layer_body) run through four loops in turn, one per code, each with its own
+// decode inlined, so that the step's layers of one K share one launch ramp
+// and one tail.
+template <int K>
+__global__ void __maxnreg__(layer_max_regs<K>()) layer_kernel_kset(const GroupArgs g) {
+  constexpr int kWarps = layer_warps<1>();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int stride = static_cast<int>(gridDim.x) * kWarps;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  bool waited = false;
+  int u = warp * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+  if (u >= g.units) return;
+  int li = group_layer_of(g, u);
+  u = kset_loop<K, kCb3Inst>(g, u, stride, g.code_end[0], li, lane, waited);
+  u = kset_loop<K, kCb1Mad>(g, u, stride, g.code_end[1], li, lane, waited);
+  u = kset_loop<K, kCbMcg>(g, u, stride, g.code_end[2], li, lane, waited);
+  kset_loop<K, kCbMul1>(g, u, stride, g.code_end[3], li, lane, waited);
+}
+
+template <int K>
+exl3_status launch_kset_t(const GroupArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
+  cfg.blockDim = dim3(32 * layer_warps<1>());
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, layer_kernel_kset<K>, a) != cudaSuccess) return EXL3_ERR_CUDA;
+  return launch_status();
+}
+
 template <int K, int CB, int MB, int TPL>
 exl3_status launch_layer_t(const GroupArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -561,5 +611,8 @@ exl3_status launch_group_dispatch(const GroupArgs& a, int codebook, int mb, cuda
   }                                                                                            \
   exl3_status launch_group_k##KK(const GroupArgs& a, int codebook, int mb, cudaStream_t stream) { \
     return launch_group_dispatch<KK>(a, codebook, mb, stream);                                 \
+  }                                                                                            \
+  exl3_status launch_group_kset_k##KK(const GroupArgs& a, cudaStream_t stream) {               \
+    return launch_kset_t<KK>(a, stream);                                                       \
   }                                                                                            \
   }
