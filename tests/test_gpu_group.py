@@ -205,17 +205,22 @@ def test_multi_repeated_calls_see_new_x(M):
             assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")
 
 
-def test_multi_one_k_launch_sampled():
-    """Batch 1, a step whose K = 2 layers of all four codes are large enough
-    for 32-tile sub-units: they run in one launch (one loop per code), the
-    K = 3 layer on its own kernel.  Layers interleave codes and include a
-    ragged row (72 tile columns); sampled 128-row blocks of each output
-    against the oracle, and every output against separate calls."""
-    spec = [(14336, 4096, 2, 0), (1024, 4096, 2, 3), (4096, 4096, 2, 1), (1024, 4096, 3, 1),
-            (4096, 4096, 2, 2), (1024, 1152, 2, 0), (1024, 4096, 2, 1)]
+@pytest.mark.parametrize("case", ["K2 codes in one launch", "K6 codes in one launch"])
+def test_multi_class_launches_sampled(case):
+    """Batch 1: the classes of one K whose tiles are enough for 32-tile
+    sub-units share one launch (one loop per code), the other classes run
+    one launch each.  Layers interleave K and codes and include a ragged row
+    (72 tile columns); sampled 128-row blocks of each output against the
+    oracle, and every output against separate calls."""
+    if case.startswith("K2"):
+        spec = [(14336, 4096, 2, 0), (1024, 4096, 2, 3), (4096, 4096, 4, 1), (1024, 4096, 3, 1),
+                (4096, 4096, 2, 2), (1024, 1152, 3, 0), (1024, 4096, 2, 1), (4096, 4096, 6, 0)]
+    else:
+        spec = [(14336, 4096, 6, 0), (4096, 4096, 6, 1), (1024, 4096, 6, 0), (1024, 1152, 6, 3),
+                (1024, 4096, 2, 1)]
     layers = []
     for i, (m, n, K, cb) in enumerate(spec):
-        inp = synth.layer_inputs(m, n, K, 1, config=171, index=i)
+        inp = synth.layer_inputs(m, n, K, 1, config=171 + len(spec), index=i)
         d = upload(inp)
         d.update(m=m, n=n, K=K, cb=cb, y=torch.full((1, m), float("nan"), dtype=torch.float16, device="cuda"))
         layers.append((inp, d))
