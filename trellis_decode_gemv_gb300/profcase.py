@@ -4,12 +4,14 @@ ncu captures of one kernel (the summaries under profiles/ name the command).
     python -m trellis_decode_gemv_gb300.profcase layer --shape 14336x4096 --K 2 --cb 0 --M 1
     python -m trellis_decode_gemv_gb300.profcase group --K 2 --cb 0 --M 1
     python -m trellis_decode_gemv_gb300.profcase group --K 2 --cb 1 --int8
+    python -m trellis_decode_gemv_gb300.profcase group --K 2 --cb 0,1
 
 `layer`: `--inst` distinct instances of one m x n layer (uniform random code
 words, the input recipe's signs, scales and activations), `--calls` calls of
 exl3_gemm_small in turn.  `group`: the Llama-3-8B layer set of one (K, code)
 class (q, k, v, o, gate, up, down) as one exl3_gemm_grouped call (with
-`--int8`, one exl3_gemm_int8act_grouped call), `--calls` times.  Nothing is checked here: the parity tests do that.
+`--int8`, one exl3_gemm_int8act_grouped call; with several codes, the set once
+per code in one exl3_gemm_multi call), `--calls` times.  Nothing is checked here: the parity tests do that.
 """
 import argparse
 
@@ -40,13 +42,15 @@ def main(argv=None):
     ap.add_argument("case", choices=["layer", "group"])
     ap.add_argument("--shape", default="14336x4096")
     ap.add_argument("--K", type=int, default=2)
-    ap.add_argument("--cb", type=int, default=0)
+    ap.add_argument("--cb", default="0", help="code, or a comma-separated list (group case: one multi-code call)")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--inst", type=int, default=8)
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--path", choices=["auto", "shuffle", "tensor"], default="auto")
     ap.add_argument("--int8", action="store_true", help="group case on int8 activations (1MAD or mul1)")
     a = ap.parse_args(argv)
+    cbs = [int(c) for c in a.cb.split(",")]
+    a.cb = cbs[0]
     B.load_library()
     B.exl3_set_path({"auto": B.PATH_AUTO, "shuffle": B.PATH_SHUFFLE, "tensor": B.PATH_TENSOR}[a.path])
     dev = torch.device("cuda")
@@ -61,19 +65,27 @@ def main(argv=None):
                               workspace=ws)
         weights = m * n
     else:
-        layers = [_layer(m, n, a.K, a.M, 2000 + 10 * i, dev) for i, (m, n) in enumerate(LLAMA8B_CLASS)]
-        if a.int8:
-            ws = torch.zeros(B.exl3_group_i8_workspace_bytes(LLAMA8B_CLASS, a.M), dtype=torch.uint8, device=dev)
-            call = B.exl3_gemm_int8act_grouped
+        if len(cbs) > 1:
+            layers = [dict(_layer(m, n, a.K, a.M, 3000 + 10 * i + 100 * c, dev), K=a.K, cb=c)
+                      for c in cbs for i, (m, n) in enumerate(LLAMA8B_CLASS)]
+            ws = B.alloc_group_workspace([(L["m"], L["n"]) for L in layers], a.M, dev)
+
+            def call(ls, K, cb, workspace):
+                B.exl3_gemm_multi(ls, workspace=workspace)
         else:
-            ws = B.alloc_group_workspace(LLAMA8B_CLASS, a.M, dev)
-            call = B.exl3_gemm_grouped
+            layers = [_layer(m, n, a.K, a.M, 2000 + 10 * i, dev) for i, (m, n) in enumerate(LLAMA8B_CLASS)]
+            if a.int8:
+                ws = torch.zeros(B.exl3_group_i8_workspace_bytes(LLAMA8B_CLASS, a.M), dtype=torch.uint8, device=dev)
+                call = B.exl3_gemm_int8act_grouped
+            else:
+                ws = B.alloc_group_workspace(LLAMA8B_CLASS, a.M, dev)
+                call = B.exl3_gemm_grouped
         torch.cuda.synchronize()
         for _ in range(a.calls):
             call(layers, a.K, a.cb, workspace=ws)
-        weights = sum(m * n for m, n in LLAMA8B_CLASS)
+        weights = sum(m * n for m, n in LLAMA8B_CLASS) * len(cbs)
     torch.cuda.synchronize()
-    print(f"{a.case}: {a.calls} calls, {weights / 1e6:.1f} M weights each, K={a.K} code={a.cb} M={a.M}"
+    print(f"{a.case}: {a.calls} calls, {weights / 1e6:.1f} M weights each, K={a.K} code={','.join(map(str, cbs))} M={a.M}"
           f"{' int8' if a.int8 else ''}")
     return 0
 
