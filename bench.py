@@ -526,8 +526,18 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
         if len(shapes) == 1:
             return B.exl3_gemm_launches(shapes[0][0], shapes[0][1], M) + 2
         return kernels_per_group(path, M, shapes, sms) + 2
-    if int8:  # one activation kernel, a layer kernel per chunk and (K, code) class, one output kernel
-        return 2 + int8_chunks(M) * (len(set(kcs)) if kcs is not None else 1)
+    if int8:  # one activation kernel, the layer kernels of each batch chunk, one output kernel
+        if kcs is None:
+            return 2 + int8_chunks(M)
+        classes = {}
+        for sh, kc in zip(shapes, kcs):
+            classes.setdefault(kc, []).append(sh)
+        total, rem = 2, M
+        for c in (8, 4, 2, 1):
+            while rem >= c:
+                rem -= c
+                total += multi_layer_launches(c, classes, sms)
+        return total
     if kcs is not None and len(shapes) > 1:  # exl3_gemm_multi: one chain per batch chunk
         classes = {}
         for sh, kc in zip(shapes, kcs):

@@ -114,6 +114,10 @@ def test_launches_of_multi_code_groups():
             shs += step
             kc6 += [(K, cb)] * len(step)
     assert bench.launches_of_group(None, "auto", 1, shs, sms, False, False, kc6) == 5
+    # the int8 path the same way (1MAD and mul1 of one K share a launch)
+    kc6b = [(K, 1 if cb == 0 else 3) for K, cb in kc6]
+    assert bench.launches_of_group(None, "auto", 1, shs, sms, False, True, kc6b) == 5
+    assert bench.launches_of_group(None, "auto", 3, shs, sms, False, True, kc6b) == 2 + 6 + 3
     assert bench.launches_of_group(None, "auto", 2, shs, sms, False, False, kc6) == 8
     assert bench.launches_of_group(None, "shuffle", 3, shs, sms, False, False, kc6) == 8 + 5
     assert bench.launches_of_group(None, "auto", 3, shs, sms, False, False, kc6) == 12  # decode-MMA: 2 per class

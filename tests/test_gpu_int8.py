@@ -216,3 +216,33 @@ def test_int8act_multi_repeated_calls_see_new_x(M):
             ref = O.layer_forward_int8(inp["codes"], d["K"], d["cb"], d["m"], d["n"], inp["s_out"], inp["scales"],
                                        q, qs)
             assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")
+
+
+def test_int8act_multi_one_k_launch():
+    """Batch 1, the 1MAD and mul1 layers of K = 2 large enough for 32-tile
+    sub-units share one launch (one loop per code), with a ragged row (72 tile
+    columns) and a K = 3 layer on its own kernel: every output within one
+    binary16 rounding of its own exl3_gemm_int8act call (parity-tested against
+    the oracle above), the small layers also against the oracle."""
+    spec = [(14336, 4096, 2, 1), (4096, 4096, 2, 3), (1024, 1152, 2, 3), (1024, 4096, 3, 1),
+            (1024, 4096, 2, 1)]
+    layers, inps = [], []
+    for i, (m, n, K, cb) in enumerate(spec):
+        inp = synth.layer_inputs(m, n, K, 1, config=181, index=i)
+        d = upload(inp)
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((1, m), float("nan"), dtype=torch.float16, device="cuda"))
+        layers.append(d)
+        inps.append(inp)
+    B.exl3_gemm_int8act_multi(layers)
+    torch.cuda.synchronize()
+    for i, (d, inp) in enumerate(zip(layers, inps)):
+        y1 = B.exl3_gemm_int8act(d["codes"], d["K"], d["cb"], d["m"], d["n"], d["s_in"], d["s_out"], d["scales"],
+                                 d["x"])
+        torch.cuda.synchronize()
+        assert float((y1.float() - d["y"].float()).abs().max()) <= 2.0 ** -9 * float(y1.float().abs().max())
+        if d["m"] * d["n"] <= 1024 * 4096:
+            xt = O.rht(inp["x"].astype(np.float64), inp["s_in"]).astype(np.float16)
+            q, qs = O.quantize_act(xt)
+            ref = O.layer_forward_int8(inp["codes"], d["K"], d["cb"], d["m"], d["n"], inp["s_out"], inp["scales"],
+                                       q, qs)
+            assert_layer_close(d["y"], ref, f"layer {i} K{d['K']} cb{d['cb']}")

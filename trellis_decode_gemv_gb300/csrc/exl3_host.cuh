@@ -254,7 +254,20 @@ struct I8Args {
   int sub;  // tiles per sub-unit
   int ctas;
   long long units;  // sub-units of all layers
+  // the one-K kernel (launch_i8_kset_k*): layers ordered by code, the
+  // sub-units of 1MAD end at class_end[0], of mul1 at class_end[1]
+  long long class_end[2];
 };
+// Batch 1, 32-tile sub-units: the 1MAD and mul1 layers of one K in one
+// kernel, one loop per code (I8Args::class_end).
+exl3_status launch_i8_kset_k1(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k2(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k3(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k4(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k5(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k6(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k7(const I8Args& a, cudaStream_t stream);
+exl3_status launch_i8_kset_k8(const I8Args& a, cudaStream_t stream);
 exl3_status launch_i8_k1(const I8Args& a, int codebook, int mb, cudaStream_t stream);
 exl3_status launch_i8_k2(const I8Args& a, int codebook, int mb, cudaStream_t stream);
 exl3_status launch_i8_k3(const I8Args& a, int codebook, int mb, cudaStream_t stream);

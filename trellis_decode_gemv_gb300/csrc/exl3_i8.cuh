@@ -169,6 +169,58 @@ __global__ void __launch_bounds__(32 * i8_warps<MB>(), 1) i8_kernel(const I8Args
   }
 }
 
+// The sub-units of code CB (up to `end`) of a one-K kernel, continuing the
+// warp's sequence u; returns where it stopped.
+template <int K, int CB>
+__device__ __forceinline__ long long i8_kset_loop(const I8Args& g, long long u, long long stride, long long end,
+                                                  int& li, int lane, bool& waited) {
+  for (; u < end; u += stride) {
+    while (li + 1 < g.count && u >= g.l[li + 1].u_begin) ++li;
+    const I8Layer& a = g.l[li];
+    i8_unit<K, CB, 1, 8>(a, static_cast<int>(u - a.u_begin), lane, waited);
+  }
+  return u;
+}
+
+// Batch 1, 32-tile sub-units: the 1MAD and mul1 layers of one K, ordered by
+// code, in one launch, as the binary16 one-K kernel.
+template <int K>
+__global__ void __launch_bounds__(32 * i8_warps<1>(), 1) i8_kernel_kset(const I8Args g) {
+  constexpr int kWarps = i8_warps<1>();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const long long stride = static_cast<long long>(gridDim.x) * kWarps;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  bool waited = false;
+  long long u = static_cast<long long>(warp) * gridDim.x + blockIdx.x;
+  if (u >= g.units) return;
+  int li = 0;
+  {
+    int hi = g.count - 1;  // the last layer whose first sub-unit is <= u
+    while (li < hi) {
+      const int mid = (li + hi + 1) >> 1;
+      if (u >= g.l[mid].u_begin) li = mid; else hi = mid - 1;
+    }
+  }
+  u = i8_kset_loop<K, kCb1Mad>(g, u, stride, g.class_end[0], li, lane, waited);
+  i8_kset_loop<K, kCbMul1>(g, u, stride, g.class_end[1], li, lane, waited);
+}
+
+template <int K>
+exl3_status launch_i8_kset_t(const I8Args& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.ctas));
+  cfg.blockDim = dim3(32 * i8_warps<1>());
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, i8_kernel_kset<K>, a) != cudaSuccess) return EXL3_ERR_CUDA;
+  return launch_status();
+}
+
 template <int K, int CB, int MB, int TPL>
 exl3_status launch_i8_t(const I8Args& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -222,5 +274,8 @@ exl3_status launch_i8_dispatch(const I8Args& a, int codebook, int mb, cudaStream
   namespace exl3 {                                                                      \
   exl3_status launch_i8_k##KK(const I8Args& a, int codebook, int mb, cudaStream_t stream) { \
     return launch_i8_dispatch<KK>(a, codebook, mb, stream);                             \
+  }                                                                                     \
+  exl3_status launch_i8_kset_k##KK(const I8Args& a, cudaStream_t stream) {              \
+    return launch_i8_kset_t<KK>(a, stream);                                             \
   }                                                                                     \
   }

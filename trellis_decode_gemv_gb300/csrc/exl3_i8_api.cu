@@ -153,6 +153,19 @@ exl3_status launch_prep(PrepGroup g, cudaStream_t stream) {
   return launch_status();
 }
 
+exl3_status launch_i8_kset(const I8Args& a, int K, cudaStream_t stream) {
+  switch (K) {
+    case 1: return launch_i8_kset_k1(a, stream);
+    case 2: return launch_i8_kset_k2(a, stream);
+    case 3: return launch_i8_kset_k3(a, stream);
+    case 4: return launch_i8_kset_k4(a, stream);
+    case 5: return launch_i8_kset_k5(a, stream);
+    case 6: return launch_i8_kset_k6(a, stream);
+    case 7: return launch_i8_kset_k7(a, stream);
+    default: return launch_i8_kset_k8(a, stream);
+  }
+}
+
 exl3_status launch_i8(const I8Args& a, int K, int codebook, int mb, cudaStream_t stream) {
   switch (K) {
     case 1: return launch_i8_k1(a, codebook, mb, stream);
@@ -226,29 +239,61 @@ exl3_status run_i8(const exl3_layer* layers, const I8Region* reg, int count, con
   exl3_status st;
   for (int done = 0; done < M;) {
     const int mb = M - done >= 8 ? 8 : M - done >= 4 ? 4 : M - done >= 2 ? 2 : 1;
+    // layer i's entry of a launch of `sub`-tile sub-units; units counts on
+    auto add_layer = [&](I8Args& a, int i, int sub, long long& units) {
+      const int m = layers[i].m, n = layers[i].n;
+      I8Layer& l = a.l[a.count++];
+      l.codes = layers[i].codes;
+      l.q4 = reg[i].q4 + static_cast<size_t>(done) * n;
+      l.tcorr = reg[i].tcorr + static_cast<size_t>(done) * (n / 16);
+      l.cs = reg[i].cs + static_cast<size_t>(done) * (n / kRowBlock);
+      l.zacc = reg[i].zacc + static_cast<size_t>(done) * m;
+      l.m = m;
+      l.n = n;
+      l.u_begin = static_cast<int>(units);
+      l.per_row = (n / 16 + sub - 1) / sub;
+      l.row_magic = div_magic(l.per_row, static_cast<long long>(m / 16) * l.per_row);
+      units += static_cast<long long>(m / 16) * l.per_row;
+    };
+    bool launched[kMaxGroup] = {};
     for (int c = 0; c < nclass; ++c) {
+      if (launched[c]) continue;
+      const int K = ks[cls[c]];
+      if (mb == 1) {
+        // both codes of this K: at 32-tile sub-units, one launch
+        long long ktiles = 0;
+        int nk = 0;
+        for (int c2 = c; c2 < nclass; ++c2)
+          if (ks[cls[c2]] == K) {
+            ktiles += tiles[c2];
+            ++nk;
+          }
+        if (nk > 1 && choose_sub(ktiles, 1, sms) == 32) {
+          I8Args a{};
+          a.sub = 32;
+          long long units = 0;
+          const int order[2] = {EXL3_CB_1MAD, EXL3_CB_MUL1};
+          for (int k = 0; k < 2; ++k) {
+            for (int i = 0; i < count; ++i)
+              if (ks[i] == K && cbs[i] == order[k]) add_layer(a, i, 32, units);
+            a.class_end[k] = units;
+          }
+          a.units = units;
+          a.ctas = static_cast<int>(units < sms ? units : sms);
+          if ((st = launch_i8_kset(a, K, cs)) != EXL3_OK) return st;
+          for (int c2 = c; c2 < nclass; ++c2)
+            if (ks[cls[c2]] == K) launched[c2] = true;
+          continue;
+        }
+      }
       I8Args a{};
       a.sub = choose_sub(tiles[c], mb, sms);
       long long units = 0;
-      for (int i = 0; i < count; ++i) {
-        if (of[i] != c) continue;
-        const int m = layers[i].m, n = layers[i].n;
-        I8Layer& l = a.l[a.count++];
-        l.codes = layers[i].codes;
-        l.q4 = reg[i].q4 + static_cast<size_t>(done) * n;
-        l.tcorr = reg[i].tcorr + static_cast<size_t>(done) * (n / 16);
-        l.cs = reg[i].cs + static_cast<size_t>(done) * (n / kRowBlock);
-        l.zacc = reg[i].zacc + static_cast<size_t>(done) * m;
-        l.m = m;
-        l.n = n;
-        l.u_begin = static_cast<int>(units);
-        l.per_row = (n / 16 + a.sub - 1) / a.sub;
-        l.row_magic = div_magic(l.per_row, static_cast<long long>(m / 16) * l.per_row);
-        units += static_cast<long long>(m / 16) * l.per_row;
-      }
+      for (int i = 0; i < count; ++i)
+        if (of[i] == c) add_layer(a, i, a.sub, units);
       a.units = units;
       a.ctas = static_cast<int>(units < sms ? units : sms);
-      if ((st = launch_i8(a, ks[cls[c]], cbs[cls[c]], mb, cs)) != EXL3_OK) return st;
+      if ((st = launch_i8(a, K, cbs[cls[c]], mb, cs)) != EXL3_OK) return st;
     }
     done += mb;
   }
