@@ -384,17 +384,24 @@ class ClockSampler:
 # CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None, whole=False):
+def oracle_sample_timed(gemvs, M, cfg, sel, blocks=1, target_s=None, whole=False, cache=None):
     """Time only the oracle (input generation excluded) on `blocks` 128-row
     output blocks of each selected GEMV.  With target_s, a one-block pass
     calibrates and a second pass takes as many blocks as fill about target_s
     seconds; both passes count.  With whole, the whole-vector layer of each
-    selected GEMV instead (its output transform mixes every row)."""
+    selected GEMV instead (its output transform mixes every row).  `cache`
+    (a dict) keeps the generated inputs of each GEMV for later calls."""
     from oracle import exl3_oracle as O
     inputs = []
     for i in sel:
         name, m, n, K, cb = gemvs[i]
-        inputs.append((synth.layer_inputs(m, n, K, M, config=cfg, index=i), gemvs[i], i))
+        if cache is not None and i in cache:
+            inp = cache[i]
+        else:
+            inp = synth.layer_inputs(m, n, K, M, config=cfg, index=i)
+            if cache is not None:
+                cache[i] = inp
+        inputs.append((inp, gemvs[i], i))
 
     def one_pass(nblk, first):
         w = 0
@@ -461,13 +468,22 @@ def run_reference(args):
     # the whole-vector oracle runs full layers: take the smallest GEMVs
     pool = [i for i, g in enumerate(gemvs) if g[1] * g[2] == min(h[1] * h[2] for h in gemvs)] if whole \
         else list(range(len(gemvs)))
+    # every GEMV's inputs are generated once (outside the timed oracle calls)
+    cache = {}
+    if not whole:
+        # 128-row blocks per step: up to 6, fewer when the run has many steps,
+        # so that the oracle's time stays near a minute and a half on this host
+        # (one untimed step of 6 blocks gives the time of a block)
+        _w, dt = oracle_sample_timed(gemvs, M, cfg, pool[:per_step], whole=False, cache=cache)
+        per_block = max(dt / per_step, 1e-4)
+        per_step = max(1, min(per_step, int(90.0 / (max(args.steps + args.warmup, 1) * per_block))))
     for s in range(args.warmup):
         oracle_sample_timed(gemvs, M, cfg, [pool[(s * per_step + i) % len(pool)] for i in range(per_step)],
-                            whole=whole)
+                            whole=whole, cache=cache)
     tw, tt = 0, 0.0
     for s in range(args.steps):
         sel = [pool[((args.warmup + s) * per_step + i) % len(pool)] for i in range(per_step)]
-        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, whole=whole)
+        w, dt = oracle_sample_timed(gemvs, M, cfg, sel, whole=whole, cache=cache)
         tw += w
         tt += dt
     value = tw / tt
