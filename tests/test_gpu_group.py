@@ -205,13 +205,17 @@ def test_multi_repeated_calls_see_new_x(M):
             assert_layer_close(d["y"], ref, f"call {call} layer {i} K{d['K']} cb{d['cb']}")
 
 
-@pytest.mark.parametrize("case", ["K2 codes in one launch", "K6 codes in one launch"])
+@pytest.mark.parametrize("case", ["K2 codes in one launch", "K6 codes in one launch",
+                                  "K2 codes, 3 rows on the warp-shuffle path"])
 def test_multi_class_launches_sampled(case):
     """Batch 1: the classes of one K whose tiles are enough for 32-tile
     sub-units share one launch (one loop per code), the other classes run
     one launch each.  Layers interleave K and codes and include a ragged row
     (72 tile columns); sampled 128-row blocks of each output against the
-    oracle, and every output against separate calls."""
+    oracle, and every output against separate calls.  With 3 rows on the
+    warp-shuffle kernels the one-row chunk after the two-row one takes the
+    shared launch."""
+    M = 3 if "3 rows" in case else 1
     if case.startswith("K2"):
         spec = [(14336, 4096, 2, 0), (1024, 4096, 2, 3), (4096, 4096, 4, 1), (1024, 4096, 3, 1),
                 (4096, 4096, 2, 2), (1024, 1152, 3, 0), (1024, 4096, 2, 1), (4096, 4096, 6, 0)]
@@ -220,17 +224,22 @@ def test_multi_class_launches_sampled(case):
                 (1024, 4096, 2, 1)]
     layers = []
     for i, (m, n, K, cb) in enumerate(spec):
-        inp = synth.layer_inputs(m, n, K, 1, config=171 + len(spec), index=i)
+        inp = synth.layer_inputs(m, n, K, M, config=171 + len(spec) + M, index=i)
         d = upload(inp)
-        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((1, m), float("nan"), dtype=torch.float16, device="cuda"))
+        d.update(m=m, n=n, K=K, cb=cb, y=torch.full((M, m), float("nan"), dtype=torch.float16, device="cuda"))
         layers.append((inp, d))
-    B.exl3_gemm_multi([d for _, d in layers])
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(171)
-    for i, (inp, d) in enumerate(layers):
-        m, n, K, cb = d["m"], d["n"], d["K"], d["cb"]
-        single = B.exl3_gemm_small(d["codes"], K, cb, m, n, d["s_in"], d["s_out"], d["scales"], d["x"])
+    if M > 2:
+        B.exl3_set_path(B.PATH_SHUFFLE)
+    try:
+        B.exl3_gemm_multi([d for _, d in layers])
+        singles = [B.exl3_gemm_small(d["codes"], d["K"], d["cb"], d["m"], d["n"], d["s_in"], d["s_out"],
+                                     d["scales"], d["x"]) for _, d in layers]
         torch.cuda.synchronize()
+    finally:
+        B.exl3_set_path(B.PATH_AUTO)
+    rng = np.random.default_rng(171)
+    for i, ((inp, d), single) in enumerate(zip(layers, singles)):
+        m, n, K, cb = d["m"], d["n"], d["K"], d["cb"]
         diff = (single.float() - d["y"].float()).abs().max()
         assert float(diff) <= 2.0 ** -9 * float(single.float().abs().max()) + 1e-6, f"layer {i} K{K} cb{cb}"
         nb = m // 128
