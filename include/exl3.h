@@ -388,8 +388,9 @@ size_t exl3_multi_workspace_bytes(const exl3_layer_kc *layers, int count, int M)
  * differ in K.  On the warp-shuffle kernels (M <= 2 by default) the layers
  * share one kernel chain per batch chunk: one x-pair kernel over every layer,
  * one sub-unit kernel per (K, code) class over that class's layers (in order
- * of first appearance, each a programmatic dependent of the one before), one
- * output kernel over every layer.  On the decode-MMA kernel each class runs
+ * of first appearance, each a programmatic dependent of the one before; in a
+ * chunk of one row, one kernel for all the classes of one K when their tiles
+ * give every SM at least 2048), one output kernel over every layer.  On the decode-MMA kernel each class runs
  * as exl3_gemm_grouped would run it.
  * Validation and errors as exl3_gemm_grouped, K and the code checked per
  * layer; workspace >= exl3_multi_workspace_bytes, same zero-fill contract.
@@ -453,8 +454,9 @@ size_t exl3_multi_i8_workspace_bytes(const exl3_layer_kc *layers, int count, int
  * (1..EXL3_MAX_BATCH): the results equal `count` calls of exl3_gemm_int8act.
  * One activation kernel for every layer's x (each layer's tile corrections
  * and block factors with its own code's centre and scale), per batch chunk one
- * int8 layer kernel per (K, code) class (in order of first appearance), one
- * output kernel.  Validation and errors as exl3_gemm_int8act_grouped, K and the
+ * int8 layer kernel per (K, code) class (in order of first appearance; in a
+ * chunk of one row, one for both codes of one K when their tiles give every
+ * SM at least 2048), one output kernel.  Validation and errors as exl3_gemm_int8act_grouped, K and the
  * code checked per layer; workspace >= exl3_multi_i8_workspace_bytes, same
  * zero-fill contract.
  */
