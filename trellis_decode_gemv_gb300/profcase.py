@@ -11,7 +11,8 @@ words, the input recipe's signs, scales and activations), `--calls` calls of
 exl3_gemm_small in turn.  `group`: the Llama-3-8B layer set of one (K, code)
 class (q, k, v, o, gate, up, down) as one exl3_gemm_grouped call (with
 `--int8`, one exl3_gemm_int8act_grouped call; with several codes, the set once
-per code in one exl3_gemm_multi call), `--calls` times.  Nothing is checked here: the parity tests do that.
+per code in one exl3_gemm_multi call, or exl3_gemm_int8act_multi with
+`--int8`), `--calls` times.  Nothing is checked here: the parity tests do that.
 """
 import argparse
 
@@ -68,10 +69,14 @@ def main(argv=None):
         if len(cbs) > 1:
             layers = [dict(_layer(m, n, a.K, a.M, 3000 + 10 * i + 100 * c, dev), K=a.K, cb=c)
                       for c in cbs for i, (m, n) in enumerate(LLAMA8B_CLASS)]
-            ws = B.alloc_group_workspace([(L["m"], L["n"]) for L in layers], a.M, dev)
+            shapes = [(L["m"], L["n"]) for L in layers]
+            if a.int8:
+                ws = torch.zeros(B.exl3_multi_i8_workspace_bytes(shapes, a.M), dtype=torch.uint8, device=dev)
+            else:
+                ws = B.alloc_group_workspace(shapes, a.M, dev)
 
             def call(ls, K, cb, workspace):
-                B.exl3_gemm_multi(ls, workspace=workspace)
+                (B.exl3_gemm_int8act_multi if a.int8 else B.exl3_gemm_multi)(ls, workspace=workspace)
         else:
             layers = [_layer(m, n, a.K, a.M, 2000 + 10 * i, dev) for i, (m, n) in enumerate(LLAMA8B_CLASS)]
             if a.int8:
