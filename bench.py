@@ -85,6 +85,12 @@ TRAFFIC_RATIO = {
     # (54.889 + 0.029) / 54.940 MB
     "int8": ((54.889 + 0.029) / 54.940, "the ncu capture of i8_kernel (32-tile sub-units) on one grouped "
                                         "int8-activation call over the 7 Llama-3-8B projections, K2 1MAD"),
+    # the one-K kernels (classes of one K in one launch) over the 7 projections
+    # at two codes of K2, 436 M weights: reads + writes against 109.88 MB
+    "kset": ((109.782 + 3.208) / 109.879, "the ncu capture of layer_kernel_kset<2> on one multi-code call over "
+                                          "the 7 Llama-3-8B projections at 3INST and 1MAD"),
+    "int8kset": ((109.791 + 3.569) / 109.879, "the ncu capture of i8_kernel_kset<2> on one multi-code call over "
+                                              "the 7 Llama-3-8B projections at 1MAD and mul1"),
 }
 
 
@@ -752,10 +758,22 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     dense = M > 32 and args.path != "tensor"
     passes = M > 32 and args.path == "tensor"
     fused = dense and (args.prefill == "fused" or (args.prefill == "auto" and M <= 256))
+    # batch 1 with every GEMV of a step in multi-code calls: do classes of one K
+    # share a launch (the one-K kernel)?
+    kset = False
+    if grouping == "step" and M == 1 and uses_shuffle(args.path, M):
+        for g in groups:
+            classes = {}
+            for i in g:
+                classes.setdefault((calls[i]["K"], calls[i]["cb"]), []).append((calls[i]["m"], calls[i]["n"]))
+            kset = kset or multi_layer_launches(1, classes, sms) < len(classes)
     if int8:
         kname = ("i8_kernel (window, generator, one dp4a per weight into int32 tile sums) + activation "
                  "rotation/quantization and output kernels")
-        tkey = "int8"
+        tkey = "int8kset" if kset else "int8"
+        if kset:
+            kname = ("i8_kernel_kset (one launch per K over its byte-sum codes: window, generator, one dp4a per "
+                     "weight into int32 tile sums) + activation rotation/quantization and output kernels")
     elif fused:
         kname = ("dense_kernel, fused (sixteen warps decode each stage's codes into the operand-A image in shared "
                  "memory; tcgen05 128xNx16 MMAs, N = 64/128/256 by batch) + operand-B kernel")
@@ -769,7 +787,10 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
         tkey = "tensor"
     elif shuffle:
         kname = "layer_kernel / seg_layer_kernel (trellis decode + HFMA2 + warp shuffles) + x-pair and output kernels"
-        tkey = "shuffle"
+        tkey = "kset" if kset else "shuffle"
+        if kset:
+            kname = ("layer_kernel_kset (one launch per K over its codes: trellis decode + HFMA2 + warp shuffles) + "
+                     "x-pair and output kernels")
     else:
         kname = ("mv_kernel (decode into TMEM, tcgen05 128xNx16 MMAs; input RHT by in-kernel x warps at M <= 2, "
                  "output RHT by the CTA completing each 128-row block)" + (" + operand-image kernel" if M > 2 else ""))
