@@ -52,6 +52,7 @@ from trellis_decode_gemv_gb300 import synth  # noqa: E402
 
 METRIC = "fused trellis GEMV weights/s & effective HBM GB/s, batch 1, % of roofline"
 L2_BYTES = 129 * 1024 * 1024
+MAX_GROUP = 64  # layers per grouped call (EXL3_MAX_GROUP in include/exl3.h)
 SM_COUNT_NOMINAL = 152
 SM_MAX_MHZ_NOMINAL = 2070.0
 INT_LANES_PER_SM_CLK = 128
@@ -255,7 +256,7 @@ def step_groups(gemvs, max_group: int):
 
 GROUPING_CALLS = {
     "step": "every GEMV of the step in multi-code calls of up to 64 layers (mixed K and code: one input "
-            "kernel, a layer kernel per (K, code) class, one output kernel)",
+            "kernel, a layer kernel per (K, code) class, at batch 1 one per K, one output kernel)",
     "class": "every GEMV of the step that shares K and the code in one grouped call",
     "decoder": "q/k/v and gate/up grouped per call (the projections a decoder applies to one step), "
                "the rest one call each",
@@ -470,6 +471,8 @@ def run_reference(args):
     wl = "llama8b" if args.workload == "all" else args.workload
     desc, cfg, gemvs, M = workload(wl, args.batch)
     whole = wl == "whole"
+    # the GPU arm's grouping for this workload (its line's `config`)
+    ref_grouping = resolve_grouping(args.grouping, M, whole)
     per_step = 1 if whole else min(6, len(gemvs))
     # the whole-vector oracle runs full layers: take the smallest GEMVs
     pool = [i for i, g in enumerate(gemvs) if g[1] * g[2] == min(h[1] * h[2] for h in gemvs)] if whole \
@@ -502,7 +505,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tt / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "batch": M},
+        "config": step_config(args, desc, gemvs, M, ref_grouping,
+                              groups_of([(g[0], g[1], g[2], g[3], g[4]) for g in gemvs], ref_grouping, MAX_GROUP),
+                              args.path),
         "cpu_baseline": {"value": value, "unit": "weights/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -575,6 +580,51 @@ def launches_of_group(B, path, M, shapes, sms, whole, int8, kcs=None):
     return kernels_per_group(path, M, shapes, sms)
 
 
+def resolve_grouping(grouping, M, whole):
+    """The grouping a workload's step runs with: grouped calls take at most 32
+    batch rows, and the whole-vector variant has no multi-code call."""
+    if M > 32:
+        return "none"
+    if grouping == "step" and whole:
+        return "class"
+    return grouping
+
+
+def groups_of(shapes_kc, grouping, max_group):
+    if grouping == "step":
+        return step_groups(shapes_kc, max_group)
+    if grouping == "class":
+        return class_groups(shapes_kc, max_group)
+    return decoder_groups(shapes_kc, grouped=grouping == "decoder")
+
+
+def step_config(args, desc, gemvs, M, grouping, groups, path, cuda_graph=True):
+    """The `config` of a workload's line: what the step computes and how it is
+    called (the same for the GPU arm and the reference arm)."""
+    whole, int8 = args_workload_kind(desc)
+    alg = [algorithmic(m, n, K, cb, M, path, int8) for _, m, n, K, cb in gemvs]
+    packed = sum(m * n * K // 8 for _, m, n, K, _ in gemvs)
+    l2_note = (f"inputs larger than L2: {packed / 1e6:.0f} MB of packed codes per step "
+               f"vs {L2_BYTES / 1e6:.0f} MB L2") if packed > L2_BYTES else "L2 NOT exceeded"
+    return {"workload": desc, "gemvs_per_step": len(gemvs), "batch": M,
+            "weights_per_step": sum(a[0] for a in alg), "packed_bytes_per_step": packed,
+            "algorithmic_bytes_per_step": sum(a[1] for a in alg), "l2": l2_note,
+            "cuda_graph": cuda_graph, "kernel_path": path, "prefill": args.prefill,
+            "grouping": grouping,
+            "calls": GROUPING_CALLS[grouping] + (
+                " (exl3_gemm, prefill)" if M > 32 and not whole else
+                " (exl3_gemm_whole_grouped / exl3_gemm_whole)" if whole else
+                " (exl3_gemm_int8act_multi / exl3_gemm_int8act)" if int8 and grouping == "step" else
+                " (exl3_gemm_int8act_grouped / exl3_gemm_int8act)" if int8 else
+                " (exl3_gemm_multi / exl3_gemm_small)" if grouping == "step" else
+                " (exl3_gemm_grouped / exl3_gemm_small)") + f"; {len(groups)} calls per step"}
+
+
+def args_workload_kind(desc):
+    """(whole-vector variant, int8 activations) of a workload, from its description."""
+    return "whole-vector rotations" in desc, "int8 activations" in desc
+
+
 def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cpu=False, grouping=None):
     """One workload: resident inputs, warm-up, graph capture, `steps` timed
     graph replays (CUDA events on the launch stream), per-call apportioning,
@@ -622,19 +672,9 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
         yo += M * m
     torch.cuda.synchronize(dev)
 
-    # grouped calls take at most 32 batch rows
-    grouping = grouping or args.grouping
-    if M > 32:
-        grouping = "none"
+    grouping = resolve_grouping(grouping or args.grouping, M, whole)
     shapes_kc = [(c["name"], c["m"], c["n"], c["K"], c["cb"]) for c in calls]
-    if grouping == "step" and whole:
-        grouping = "class"
-    if grouping == "step":
-        groups = step_groups(shapes_kc, B.MAX_GROUP)
-    elif grouping == "class":
-        groups = class_groups(shapes_kc, B.MAX_GROUP)
-    else:
-        groups = decoder_groups(shapes_kc, grouped=grouping == "decoder")
+    groups = groups_of(shapes_kc, grouping, MAX_GROUP)
     gws_of = (B.exl3_group_i8_workspace_bytes if int8 else B.exl3_gemm_whole_grouped_workspace_bytes if whole
               else B.exl3_group_workspace_bytes)
     gws = max([gws_of([(calls[i]["m"], calls[i]["n"]) for i in g], M)
@@ -667,8 +707,6 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
     weights_step = sum(a[0] for a in alg)
     bytes_step = sum(a[1] for a in alg)
     ops_step = sum(a[2] for a in alg)
-    l2_note = (f"inputs larger than L2: {packed / 1e6:.0f} MB of packed codes per step "
-               f"vs {L2_BYTES / 1e6:.0f} MB L2") if packed > L2_BYTES else "L2 NOT exceeded"
 
     # ---- warm-up + graph capture ----------------------------------------
     with torch.cuda.stream(stream):
@@ -855,16 +893,7 @@ def measure_workload(ctx, args, wl, batch, steps, warmup, want_e2e=True, want_cp
                                           else None) for g in groups)
     res = {
         "value": value, "unit": "weights/s", "steps": steps, "warmup": warmup, "ms_per_step": ms_step,
-        "config": {"workload": desc, "gemvs_per_step": len(calls), "batch": M,
-                   "weights_per_step": weights_step, "packed_bytes_per_step": packed,
-                   "algorithmic_bytes_per_step": bytes_step, "l2": l2_note,
-                   "cuda_graph": graph is not None, "kernel_path": args.path, "prefill": args.prefill,
-                   "grouping": grouping,
-                   "calls": GROUPING_CALLS[grouping] + (
-                       " (exl3_gemm_whole_grouped / exl3_gemm_whole)" if whole else
-                       " (exl3_gemm_int8act_multi / exl3_gemm_int8act)" if int8 and grouping == "step" else
-                       " (exl3_gemm_int8act_grouped / exl3_gemm_int8act)" if int8 else
-                       " (exl3_gemm_grouped / exl3_gemm_small)") + f"; {len(groups)} calls per step"},
+        "config": step_config(args, desc, gemvs, M, grouping, groups, args.path, cuda_graph=graph is not None),
         "effective_gbs": bytes_step * world / (ms_step / 1e3) / 1e9,
         "macs_per_s": value * M,
         "roofline_pct": roof_pct,

@@ -132,3 +132,19 @@ def test_decoder_groups_whole_vector_stack():
     for x in g:
         names = [gemvs[i][0].split(".")[1] for i in x]
         assert names in (["q", "k", "v"], ["o"])
+
+
+def test_reference_config_matches_the_gpu_line():
+    """The reference arm's `config` is the GPU arm's (same workload, shapes,
+    grouping and call count), built from host information only."""
+    from trellis_decode_gemv_gb300 import binding as B
+    assert bench.MAX_GROUP == B.MAX_GROUP
+    args = bench.argparse.Namespace(prefill="auto", grouping="step", path="auto")
+    desc, cfg, gemvs, M = bench.workload("llama8b", 1)
+    grouping = bench.resolve_grouping("step", M, False)
+    groups = bench.groups_of([tuple(g) for g in gemvs], grouping, bench.MAX_GROUP)
+    c = bench.step_config(args, desc, gemvs, M, grouping, groups, "auto")
+    assert c["gemvs_per_step"] == 42 and c["packed_bytes_per_step"] == 490733568
+    assert c["grouping"] == "step" and c["calls"].endswith("; 1 calls per step")
+    assert bench.resolve_grouping("step", 512, False) == "none"
+    assert bench.resolve_grouping("step", 1, True) == "class"
