@@ -23,8 +23,12 @@
 // consecutive tiles of one tile row; one CTA per SM; warp w of CTA b takes the
 // sub-units w * grid + b + i * (grid * warps), each warp's tile row found by
 // a multiply-high with a per-layer magic number and its layer by stepping
-// forward from the one of its previous sub-unit.  In a sub-unit, lane 8*jt + p handles tiles
-// J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each: 32 consecutive
+// forward from the one of its previous sub-unit.  In grouped calls the
+// sub-units of every layer of the call are numbered one after the other; at
+// batch 1 the layers of several codes of one K can share one launch
+// (layer_kernel_kset, one loop per code).  In a sub-unit, lane 8*jt + p
+// handles tiles J0 + jt, J0 + jt + 4, ... and the row pair 2p, 2p+1 of each:
+// 32 consecutive
 // trellis steps from a word-aligned window per tile (code words loaded two
 // tiles ahead of their decode), with the x pairs of the tile's 16 columns read
 // from L1/L2.  Per column one packed binary16 FMA (HFMA2):
